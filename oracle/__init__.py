@@ -1,0 +1,190 @@
+"""CPU oracle of the Flint NVFP4 W4A16 routed-expert MoE block.
+
+TEST INFRASTRUCTURE.  Only the tests, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The product path (the C-ABI library and its Python binding) never
+imports it, and this package imports nothing from the product path.
+
+The arithmetic lives in ``flint_oracle.c`` (plain C, one IEEE binary32
+operation per C operator, compiled with ``-O2 -ffp-contract=off``).  This file
+only compiles it with gcc and marshals numpy / torch CPU arrays through ctypes.
+Rules and citations are in the C file's header.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "flint_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libflint_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP over tokens).  Returns the .so path."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared",
+           "-std=c11", "-Wall", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i32 = ctypes.c_int
+            lib.oracle_e2m1_value.restype = ctypes.c_float
+            lib.oracle_e2m1_value.argtypes = [i32]
+            lib.oracle_e4m3_value.restype = ctypes.c_float
+            lib.oracle_e4m3_value.argtypes = [i32]
+            lib.oracle_bf16_round.restype = None
+            lib.oracle_bf16_round.argtypes = [P, P, ctypes.c_int64]
+            lib.oracle_nvfp4_dequant.restype = None
+            lib.oracle_nvfp4_dequant.argtypes = [P, P, ctypes.c_int64, i32, P]
+            lib.oracle_route.restype = i32
+            lib.oracle_route.argtypes = [P, P, i32, i32, i32, i32, P, P, P]
+            lib.oracle_topk.restype = i32
+            lib.oracle_topk.argtypes = [P, i32, i32, i32, P, P]
+            lib.oracle_forward.restype = i32
+            lib.oracle_forward.argtypes = [P] * 10 + [i32] * 6 + [P, i32] + [P] * 8 + [i32]
+            lib.oracle_max_threads.restype = i32
+            lib.oracle_max_threads.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _np(t, dtype):
+    """torch (CPU) tensor or numpy array -> contiguous numpy array of dtype
+    (bit reinterpretation for bf16 / fp8, never a value conversion)."""
+    try:
+        import torch
+        if isinstance(t, torch.Tensor):
+            t = t.detach().cpu().contiguous()
+            if t.dtype == torch.bfloat16:
+                t = t.view(torch.int16)
+            elif t.dtype == torch.float8_e4m3fn:
+                t = t.view(torch.uint8)
+            t = t.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(t)
+    if a.dtype != dtype:
+        if a.dtype.itemsize == np.dtype(dtype).itemsize and a.dtype.kind in "iu" and np.dtype(dtype).kind in "iu":
+            a = a.view(dtype)
+        else:
+            a = a.astype(dtype)
+    return a
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def e2m1_value(code: int) -> float:
+    return float(_load().oracle_e2m1_value(int(code)))
+
+
+def e4m3_value(byte: int) -> float:
+    return float(_load().oracle_e4m3_value(int(byte)))
+
+
+def bf16_round_bits(x) -> np.ndarray:
+    """fp32 array -> uint16 bf16 bit patterns, round to nearest even."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    out = np.empty(a.shape, dtype=np.uint16)
+    _load().oracle_bf16_round(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def bf16_bits_to_f32(bits) -> np.ndarray:
+    b = np.asarray(bits).astype(np.uint32) << 16
+    return b.view(np.float32)
+
+
+def nvfp4_dequant(codes, sf, K: int) -> np.ndarray:
+    """Dequantise packed NVFP4 rows ([rows, K/2] codes, [rows, K/16] scales)."""
+    c = _np(codes, np.uint8)
+    s = _np(sf, np.uint8)
+    rows = c.size // (K // 2)
+    out = np.empty((rows, K), dtype=np.float32)
+    _load().oracle_nvfp4_dequant(_ptr(c), _ptr(s), rows, K, _ptr(out))
+    return out.reshape(tuple(c.shape[:-1]) + (K,))
+
+
+def route(x, router_w, top_k: int):
+    """Returns (logits bf16 bits uint16 [M, E], ids int32 [M, k], tw fp32 [M, k])."""
+    xa = _np(x, np.uint16)
+    wa = _np(router_w, np.uint16)
+    M, H = xa.shape
+    E = wa.shape[0]
+    logits = np.empty((M, E), dtype=np.uint16)
+    ids = np.empty((M, top_k), dtype=np.int32)
+    tw = np.empty((M, top_k), dtype=np.float32)
+    rc = _load().oracle_route(_ptr(xa), _ptr(wa), M, H, E, top_k, _ptr(logits), _ptr(ids), _ptr(tw))
+    if rc != 0:
+        raise ValueError("oracle_route: invalid shape")
+    return logits, ids, tw
+
+
+def topk(logit_bits, top_k: int):
+    """Top-k on given bf16 logits (uint16 bit patterns [M, E])."""
+    lb = _np(logit_bits, np.uint16)
+    M, E = lb.shape
+    ids = np.empty((M, top_k), dtype=np.int32)
+    tw = np.empty((M, top_k), dtype=np.float32)
+    if _load().oracle_topk(_ptr(lb), M, E, top_k, _ptr(ids), _ptr(tw)) != 0:
+        raise ValueError("oracle_topk: invalid shape")
+    return ids, tw
+
+
+def forward(x, layer, top_k: int, tokens=None, intermediates: bool = False, nthreads: int = 0):
+    """The whole block for the selected tokens (all by default).
+
+    ``layer`` is a synth.MoELayer (CPU tensors) or anything with the same
+    attributes.  Returns a dict of numpy arrays: out (bf16 bits [n, H]), ids,
+    tw and, with ``intermediates``, logits, act, y, sact, ys."""
+    xa = _np(x, np.uint16)
+    M, H = xa.shape
+    E, I, SI = int(layer.E), int(layer.I), int(layer.SI)
+    k = int(top_k)
+    arrs = [
+        xa, _np(layer.router_w, np.uint16), _np(layer.w13, np.uint8), _np(layer.w13_sf, np.uint8),
+        _np(layer.w13_gs, np.float32), _np(layer.w2, np.uint8), _np(layer.w2_sf, np.uint8),
+        _np(layer.w2_gs, np.float32), _np(layer.shared_gu, np.uint16) if SI else None,
+        _np(layer.shared_down, np.uint16) if SI else None,
+    ]
+    tok = None if tokens is None else np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    n = M if tok is None else tok.size
+    res = {"out": np.empty((n, H), np.uint16), "ids": np.empty((n, k), np.int32),
+           "tw": np.empty((n, k), np.float32)}
+    if intermediates:
+        res.update(logits=np.empty((n, E), np.uint16), act=np.empty((n, k, I), np.uint16),
+                   y=np.empty((n, k, H), np.uint16), sact=np.empty((n, max(SI, 1)), np.uint16),
+                   ys=np.empty((n, H), np.uint16))
+    g = res.get
+    rc = _load().oracle_forward(
+        *[_ptr(a) for a in arrs], M, H, E, k, I, SI, _ptr(tok), n,
+        _ptr(res["out"]), _ptr(res["ids"]), _ptr(res["tw"]), _ptr(g("logits")), _ptr(g("act")),
+        _ptr(g("y")), _ptr(g("sact")), _ptr(g("ys")), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_forward: invalid shape or token list")
+    return res
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())

@@ -1,0 +1,330 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each test names what fixes the expected value: a library conversion, a closed
+form, brute force, an independent float64 re-derivation, or a special case
+that reduces to a library matmul.  Everything runs on the CPU.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp64_reference import (bf16_bits_to_f64, dequant, e2m1_decode, forward64, order_key,
+                            tensor_bits)
+from nvfp4_w4a16_mixture_gb300 import synth
+from tolerance import bits_to_f64, check_bf16
+
+
+# ----------------------------------------------------------------- formats
+def test_e4m3_decode_matches_torch():
+    """All 256 float8_e4m3fn patterns against torch's conversion (library)."""
+    lib = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn)
+    ref = lib.to(torch.float32).numpy()
+    got = np.array([oracle.e4m3_value(b) for b in range(256)], dtype=np.float32)
+    nan = np.isnan(ref)
+    assert nan.sum() == 2  # S.1111.111 only
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_e2m1_decode_via_e4m3_embedding():
+    """E2M1 codes through their exact E4M3 embedding, decoded by torch."""
+    ref = e2m1_decode(np.arange(16))
+    got = np.array([oracle.e2m1_value(c) for c in range(16)])
+    assert np.array_equal(got, ref)
+    assert np.array_equal(np.signbit(got), np.arange(16) >= 8)
+
+
+def test_e2m1_closed_form_facts():
+    """Format facts: 8 magnitudes, max 6, smallest positive 0.5 (subnormal),
+    sign-symmetric."""
+    v = np.array([oracle.e2m1_value(c) for c in range(16)])
+    assert v.max() == 6.0 and v.min() == -6.0
+    assert np.min(v[v > 0]) == 0.5
+    assert np.array_equal(v[8:], -v[:8])
+    assert len(set(np.abs(v).tolist())) == 8
+
+
+def test_dequant_products_exact_in_bf16():
+    """Brute force over all 16 x 254 finite (code, scale) pairs: the oracle's
+    dequantised weight equals the float64 product and survives a bf16
+    round trip (the pages: weights dequantised exactly)."""
+    codes = np.arange(16, dtype=np.uint8)
+    scales = np.array([b for b in range(256) if (b & 0x7F) != 0x7F], dtype=np.uint8)
+    # one row per scale, 16 codes packed (even K in the low nibble)
+    row_codes = np.tile(codes, (scales.size, 1))
+    packed = (row_codes[:, 0::2] | (row_codes[:, 1::2] << 4)).astype(np.uint8)
+    sf = scales[:, None].astype(np.uint8)
+    got = oracle.nvfp4_dequant(packed, sf, 16)
+    ref = np.outer(
+        torch.from_numpy(scales).view(torch.float8_e4m3fn).to(torch.float64).numpy(),
+        e2m1_decode(codes))
+    assert np.array_equal(got.astype(np.float64), ref)
+    rt = torch.from_numpy(got).to(torch.bfloat16).to(torch.float32).numpy()
+    assert np.array_equal(rt, got)
+
+
+def test_bf16_rounding_matches_torch():
+    """fp32 -> bf16 RNE against torch's conversion: 2^22 random patterns plus
+    every exponent with tie, above-tie, below-tie and saturating mantissas."""
+    rng = np.random.default_rng(0)
+    rand = rng.integers(0, 2 ** 32, size=1 << 22, dtype=np.uint64).astype(np.uint32)
+    exps = np.arange(256, dtype=np.uint32) << 23
+    mants = np.array([0, 1, 0x7FFF, 0x8000, 0x8001, 0x18000, 0x17FFF, 0x7FFFFF, 0x7F8000,
+                      0x7F7FFF, 0x10000], dtype=np.uint32)
+    special = (exps[:, None] | mants[None, :]).ravel()
+    pats = np.concatenate([rand, special, special | 0x80000000])
+    f = pats.view(np.float32)
+    got = oracle.bf16_round_bits(f)
+    ref = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(f)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.isnan(bits_to_f64(got[nan])).all()
+
+
+def test_nibble_and_scale_placement():
+    """Hand-built row: code c at K index c (c = 0..15) and a different scale
+    per 16-block lands at the documented positions (even K = low nibble)."""
+    K = 32
+    codes = np.array(list(range(16)) + list(range(15, -1, -1)), dtype=np.uint8)
+    packed = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)[None, :]
+    sf = np.array([[0x38, 0x40]], dtype=np.uint8)  # 1.0 and 2.0
+    got = oracle.nvfp4_dequant(packed, sf, K)[0]
+    e2 = e2m1_decode(np.arange(16))
+    assert np.array_equal(got[:16], e2)
+    assert np.array_equal(got[16:], 2.0 * e2[::-1])
+
+
+# --------------------------------------------------------------- quantiser
+def test_quantiser_round_trip_and_midpoints():
+    """Values on the E2M1 grid (times one power-of-two factor) quantise to
+    exactly their own codes with a saturated block scale; E2M1 midpoints round
+    to the even code."""
+    mid = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.0, -0.25, -5.0, 0.0, -0.0])
+    want = torch.tensor([0, 2, 2, 4, 4, 6, 6, 7, 8, 14, 0, 8], dtype=torch.uint8)
+    assert torch.equal(synth.e2m1_codes(mid), want)
+    g = torch.Generator().manual_seed(3)
+    grid = torch.tensor([0.0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    vals = grid[torch.randint(0, 8, (64, 128), generator=g)]
+    vals = vals * torch.where(torch.rand(64, 128, generator=g) < 0.5, -1.0, 1.0)
+    # make every 16-block's max magnitude 6 so the block scale is exactly 1 * gs
+    vals[:, ::16] = 6.0
+    w = vals * 0.125
+    packed, sf, gs = synth.quantize_nvfp4(w)
+    # every block max is the tensor max, so every block scale saturates at 448
+    assert (sf == 0x7E).all()
+    assert float(gs) == np.float32(0.75) / np.float32(6 * 448)
+    deq = oracle.nvfp4_dequant(packed.numpy(), sf.numpy(), 128)
+    assert np.array_equal(deq, (vals * 448.0).numpy())
+
+
+# ---------------------------------------------------------------- routing
+def _brute_force_rank(logit_bits: np.ndarray, k: int) -> list[int]:
+    """Full stable sort: numeric value descending, +0 above -0, then lower
+    expert index (the pages' tie rule), written with float comparisons."""
+    vals = bits_to_f64(logit_bits)
+    neg_zero = (logit_bits == 0x8000)
+    items = list(range(len(vals)))
+    items.sort(key=lambda e: (-vals[e], 1 if neg_zero[e] else 0, e))
+    return items[:k]
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (16, 16), (128, 8), (256, 8), (32, 1)])
+def test_topk_matches_brute_force_sort(E, k):
+    g = torch.Generator().manual_seed(E * 31 + k)
+    M, H = 24, 256
+    x = synth.make_x(M, H, g)
+    wr = (torch.randn(E, H, generator=g) * H ** -0.5).to(torch.bfloat16)
+    if E >= 16:  # duplicated rows -> identical logits -> lower index wins
+        wr[E - 1] = wr[3]
+        wr[E // 2] = wr[E // 2 + 1]
+    logits, ids, tw = oracle.route(x, wr, k)
+    for t in range(M):
+        assert ids[t].tolist() == _brute_force_rank(logits[t], k)
+
+
+def test_topk_signed_zero_and_ties_constructed():
+    """Constructed logits: ties go to the lower index and +0 ranks above -0
+    (stand-alone top-k on given logits)."""
+    vals = torch.tensor([0.5, -0.0, 0.0, 0.5, -1.0, 2.0, 0.0, -0.0], dtype=torch.bfloat16)
+    bits = vals.view(torch.int16).numpy().view(np.uint16)[None, :]
+    ids, _ = oracle.topk(bits, 8)
+    assert ids[0].tolist() == [5, 0, 3, 2, 6, 1, 7, 4]
+    assert ids[0].tolist() == _brute_force_rank(bits[0], 8)
+
+
+def test_router_sum_never_yields_negative_zero():
+    """The router GEMV sums from +0, and +0 + -0 = +0 in IEEE arithmetic: a
+    row of -0 products gives a +0 logit, which then ties by index."""
+    H, E = 16, 8
+    x = torch.zeros(1, H, dtype=torch.bfloat16)
+    x[0, 0] = 1.0
+    col = torch.tensor([0.5, -0.0, 0.0, 0.5, -1.0, 2.0, 0.0, -0.0], dtype=torch.bfloat16)
+    wr = torch.zeros(E, H, dtype=torch.bfloat16)
+    wr[:, 0] = col
+    logits, ids, _ = oracle.route(x, wr, E)
+    assert logits[0, 1] == 0 and logits[0, 7] == 0
+    assert ids[0].tolist() == [5, 0, 3, 1, 2, 6, 7, 4]
+
+
+def test_routing_weights_renormalise():
+    """tw is bf16-valued, positive, sums to 1 within k * 2^-9 (bf16 rounding
+    of each weight); top_k = 1 gives exactly 1."""
+    M, H, E, k = 64, 512, 64, 8
+    g = torch.Generator().manual_seed(5)
+    x = synth.make_x(M, H, g)
+    wr = (torch.randn(E, H, generator=g) * H ** -0.5).to(torch.bfloat16)
+    _, ids, tw = oracle.route(x, wr, k)
+    assert np.array_equal(tw.view(np.uint32) & 0xFFFF, np.zeros_like(tw.view(np.uint32)))
+    assert (tw > 0).all()
+    assert np.abs(tw.astype(np.float64).sum(1) - 1.0).max() <= k * 2.0 ** -9
+    _, _, tw1 = oracle.route(x, wr, 1)
+    assert (tw1 == 1.0).all()
+
+
+def test_router_logits_match_float64():
+    """Canonical-order fp32 logits agree with the exactly summed float64
+    logit rounded to bf16, except within fp32 noise of a rounding midpoint."""
+    M, H, E = 32, 2048, 128
+    g = torch.Generator().manual_seed(11)
+    x = synth.make_x(M, H, g)
+    wr = (torch.randn(E, H, generator=g) * H ** -0.5).to(torch.bfloat16)
+    logits, _, _ = oracle.route(x, wr, 8)
+    xf = bf16_bits_to_f64(tensor_bits(x))
+    wf = bf16_bits_to_f64(tensor_bits(wr))
+    exact = xf @ wf.T
+    got = bits_to_f64(logits)
+    lsb = np.exp2(np.floor(np.log2(np.abs(exact))) - 7)
+    assert (np.abs(got - exact) <= lsb).all()  # within one bf16 ulp always
+    rounded = torch.from_numpy(exact.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert (got == rounded).mean() > 0.999
+
+
+# ------------------------------------------------------- whole-block pins
+@pytest.fixture(scope="module")
+def tiny():
+    M, H, E, k, I, SI = synth.CONFIGS["tiny"]
+    x, layer = synth.make_problem(16, H, E, k, I, SI, seed=0)
+    return x, layer, k
+
+
+def test_oracle_matches_float64_tiny(tiny):
+    x, layer, k = tiny
+    r = oracle.forward(x, layer, k)
+    q = forward64(x, layer, k)
+    sel = ~q["ambiguous"]
+    assert np.array_equal(r["ids"][sel], q["ids"][sel])
+    check_bf16(r["out"], q["out"])
+
+
+@pytest.mark.slow
+def test_oracle_matches_float64_decode_layer():
+    M, H, E, k, I, SI = synth.CONFIGS["decode8"]
+    x, layer = synth.make_problem(M, H, E, k, I, SI, seed=0)
+    r = oracle.forward(x, layer, k)
+    q = forward64(x, layer, k)
+    sel = ~q["ambiguous"]
+    assert np.array_equal(r["ids"][sel], q["ids"][sel])
+    check_bf16(r["out"], q["out"])
+
+
+def test_combine_top1_reduces_to_sum(tiny):
+    """top_k = 1: tw = 1 exactly, so out = bf16(y_0 + ys) for every element
+    (torch's fp32 add and bf16 rounding on the oracle's own intermediates)."""
+    x, layer, _ = tiny
+    r = oracle.forward(x, layer, 1, intermediates=True)
+    assert (r["tw"] == 1.0).all()
+    y0 = torch.from_numpy(bits_to_f64(r["y"][:, 0, :]).astype(np.float32))
+    ys = torch.from_numpy(bits_to_f64(r["ys"]).astype(np.float32))
+    want = (y0 + ys).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(r["out"], want)
+
+
+def test_all_experts_equals_dense_mixture(tiny):
+    """k = E: the routed block equals the dense renormalised-sigmoid mixture of
+    every expert (float64 matmuls on torch-decoded weights), within the rule."""
+    x, layer, _ = tiny
+    E, H, I = layer.E, layer.H, layer.I
+    r = oracle.forward(x, layer, E, intermediates=True)
+    xf = bf16_bits_to_f64(tensor_bits(x))
+    wr = bf16_bits_to_f64(tensor_bits(layer.router_w))
+    lg = torch.from_numpy((xf @ wr.T).astype(np.float32)).to(torch.bfloat16).double().numpy()
+    s = 1 / (1 + np.exp(-lg))
+    tw = torch.from_numpy((s / s.sum(1, keepdims=True)).astype(np.float32)).to(torch.bfloat16).double().numpy()
+    R = np.zeros((x.shape[0], H))
+    for e in range(E):
+        d13 = dequant(layer.w13[e].numpy(), layer.w13_sf[e].numpy())
+        d2 = dequant(layer.w2[e].numpy(), layer.w2_sf[e].numpy())
+        gu = (xf @ d13.T) * float(layer.w13_gs[e])
+        g, u = gu[:, :I], gu[:, I:]
+        act = torch.from_numpy((g / (1 + np.exp(-g)) * u).astype(np.float32)).to(torch.bfloat16).double().numpy()
+        y = torch.from_numpy(((act @ d2.T) * float(layer.w2_gs[e])).astype(np.float32)).to(torch.bfloat16).double().numpy()
+        R += tw[:, e:e + 1] * y
+    Rb = torch.from_numpy(R.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    ys = bits_to_f64(r["ys"])
+    want = torch.from_numpy((Rb + ys).astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    check_bf16(r["out"], want)
+
+
+def test_unit_scales_reduce_to_matmul():
+    """All block scales 1.0 (e4m3 0x38) and global scales 1: the NVFP4 gate/up
+    projection is a plain matmul on the E2M1 grid (torch float64 matmul)."""
+    M, H, E, k, I, SI = 4, 256, 4, 2, 64, 64
+    x, layer = synth.make_problem(M, H, E, k, I, SI, seed=7)
+    layer.w13_sf.fill_(0x38)
+    layer.w2_sf.fill_(0x38)
+    layer.w13_gs.fill_(1.0)
+    layer.w2_gs.fill_(1.0)
+    r = oracle.forward(x, layer, k, intermediates=True)
+    xf = torch.from_numpy(bf16_bits_to_f64(tensor_bits(x)))
+    same = []
+    for t in range(M):
+        for j in range(k):
+            e = int(r["ids"][t, j])
+            lo = (layer.w13[e] & 15).long()
+            hi = (layer.w13[e] >> 4).long()
+            codes = torch.stack([lo, hi], -1).reshape(2 * I, H).numpy()
+            w = torch.from_numpy(e2m1_decode(codes))
+            gu = torch.matmul(w, xf[t])
+            g, u = gu[:I], gu[I:]
+            act = (g / (1 + torch.exp(-g)) * u).float().to(torch.bfloat16)
+            got = torch.from_numpy(r["act"][t, j].view(np.int16)).view(torch.bfloat16)
+            diff = (got.float() - act.float()).abs()
+            assert (diff <= act.float().abs() * 2 ** -7 + 1e-30).all()  # <= 1 bf16 ulp
+            same.append((got == act).float())
+    # act differs only where fp32 rounding of g, u or the sigmoid meets a bf16
+    # midpoint
+    assert torch.cat(same).mean() > 0.97
+
+
+def test_token_permutation_and_sampling(tiny):
+    """Tokens are independent: permuting rows permutes outputs bitwise, and a
+    sampled token list reproduces the matching rows."""
+    x, layer, k = tiny
+    full = oracle.forward(x, layer, k)
+    perm = torch.randperm(x.shape[0], generator=torch.Generator().manual_seed(1))
+    pr = oracle.forward(x[perm].contiguous(), layer, k)
+    assert np.array_equal(pr["out"], full["out"][perm.numpy()])
+    assert np.array_equal(pr["ids"], full["ids"][perm.numpy()])
+    sub = [5, 0, 9]
+    sr = oracle.forward(x, layer, k, tokens=sub)
+    assert np.array_equal(sr["out"], full["out"][sub])
+
+
+def test_golden_tiny_regression():
+    """The stored tiny-layer outputs (written by tests/golden/make_golden.py,
+    which calls only the oracle) still reproduce bit for bit."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "tiny_seed0.json")
+    with open(path) as f:
+        gold = json.load(f)
+    M, H, E, k, I, SI = gold["shape"]
+    x, layer = synth.make_problem(M, H, E, k, I, SI, seed=gold["seed"])
+    r = oracle.forward(x, layer, k)
+    assert r["ids"].tolist() == gold["ids"]
+    assert r["tw"].tolist() == gold["tw"]
+    assert r["out"].astype(int).tolist() == gold["out_bf16_bits"]

@@ -1,0 +1,412 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed-expert NVFP4 MoE block on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config decode1|decode2..decode64|prefill4096|skew16384|tiny]
+
+A step is one forward of the whole MoE block (router, top-k, grouping, routed
+gate/up + SiLU*up, shared gate/up, routed and shared down, weighted combine and
+shared add) over one batch of synthetic tokens.  The default workload is
+single-token decode (M=1, H=2048, E=128, top_k=8, I=768, shared I=768).
+
+Weights of `layers` independent synthetic layers stay resident in HBM and the
+steps rotate through them (step i runs layer i mod layers), so every step
+streams its experts from HBM rather than L2 (the rotation's working set is far
+larger than the 129 MB L2).  The timed region replays CUDA graphs of the steps.
+
+Multi-GPU: one process per GPU (torchrun); every rank runs its own replica on
+its own tokens (the block has no cross-token exchange), so scaling is weak and
+no collective touches the data path.  Rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle (the plain C implementation the parity
+tests use) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from nvfp4_w4a16_mixture_gb300 import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s & weight HBM GB/s (decode M<=64); TFLOP/s at M=4096"
+DECODE_MAX_TOKENS = 64
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=0, help="0 = 10000 (decode) / 40 (large batches)")
+    p.add_argument("--warmup", type=int, default=0, help="0 = 200 (decode) / 5 (large batches)")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--config", default="decode1", choices=sorted(synth.CONFIGS))
+    p.add_argument("--layers", type=int, default=0, help="weight sets rotated (0 = auto)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def workload_name(cfg: str) -> str:
+    M, H, E, k, I, SI = synth.CONFIGS[cfg]
+    extra = ", Zipf(1.2)-skewed router" if cfg.startswith("skew") else ""
+    return f"{cfg}: M={M} H={H} E={E} top_k={k} I={I} SI={SI} (NVFP4 experts, BF16 shared{extra})"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts + frac, float(parts[2]), float(parts[3]), parts[5:]))
+            except Exception:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        use = inside or sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            for name, v in zip(names, r[3][1:5]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted(reasons), "samples": len(use),
+                "samples_inside_timed_region": len(inside)}
+
+
+# --------------------------------------------------------------- workload
+def make_layers(cfg: str, n_layers: int, device: str, seed: int):
+    M, H, E, k, I, SI = synth.CONFIGS[cfg]
+    scale = synth.zipf_router_scale(E) if cfg.startswith("skew") else None
+    layers, xs = [], []
+    for li in range(n_layers):
+        gen = torch.Generator(device=device).manual_seed(seed * 1000 + li)
+        xs.append(synth.make_x(M, H, gen, device))
+        layers.append(synth.make_layer(H, E, I, SI, gen, device, router_row_scale=scale))
+    return xs, layers
+
+
+def launches_per_step(M: int) -> int:
+    return 3 if M <= DECODE_MAX_TOKENS else 6
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (hash match), else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    from nvfp4_w4a16_mixture_gb300 import build as b
+    h = hashlib.sha256()
+    for p in sorted(b.sources()):
+        h.update(open(p, "rb").read())
+    entry = rec.get(kernel)
+    if entry and entry.get("csrc_sha256") == h.hexdigest():
+        return entry.get("dram_bytes_per_step")
+    return None
+
+
+# -------------------------------------------------------------------- ours
+def run_ours(args, rank, world, local):
+    import nvfp4_w4a16_mixture_gb300 as fm
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    cfg = args.config
+    M, H, E, k, I, SI = synth.CONFIGS[cfg]
+    n_layers = args.layers or (16 if M <= DECODE_MAX_TOKENS else 2)
+    fm.load()
+    xs, layers = make_layers(cfg, n_layers, dev, seed=1 + rank)
+    ws = fm.alloc_workspace(M, H, E, k, I, SI, dev)
+    outs = [torch.empty_like(x) for x in xs]
+    ids = [torch.empty(M, k, dtype=torch.int32, device=dev) for _ in xs]
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, s):
+        li = i % n_layers
+        fm.forward_layer(xs[li], layers[li], k, workspace=ws, out=outs[li], ids_out=ids[li], stream=s)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, n_layers)):
+            step(i, stream)
+    stream.synchronize()
+    assert fm.flint_moe_status(ws, stream) == fm.FLINT_OK
+
+    # bytes each step reads: the experts its tokens route to + router + shared
+    uniq = [int(torch.unique(t).numel()) for t in ids]
+    wb = [synth.weight_bytes(H, E, I, SI, u) for u in uniq]
+    flops = synth.flops_of(M, H, E, k, I, SI)
+
+    # graphs: one of all layers, one of the remainder
+    K = args.steps
+    full, rem = divmod(K, n_layers)
+    g_full = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_full, stream=stream):
+        for i in range(n_layers):
+            step(i, stream)
+    g_rem = None
+    if rem:
+        g_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_rem, stream=stream):
+            for i in range(rem):
+                step(i, stream)
+    with torch.cuda.stream(stream):
+        g_full.replay()
+    stream.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(full):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
+    stream.synchronize()
+    t1 = time.time()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    clk = clocks.stop(t0, t1)
+    assert fm.flint_moe_status(ws, stream) == fm.FLINT_OK
+
+    # ---- end to end through the C ABI with host buffers (pinned), eager
+    x_host = [x.cpu().pin_memory() for x in xs]
+    out_host = [torch.empty(M, H, dtype=torch.bfloat16).pin_memory() for _ in xs]
+    K_e2e = min(K, 2000)
+    with torch.cuda.stream(stream):
+        for i in range(min(50, K_e2e)):
+            li = i % n_layers
+            xs[li].copy_(x_host[li], non_blocking=True)
+            step(i, stream)
+            out_host[li].copy_(outs[li], non_blocking=True)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(K_e2e):
+            li = i % n_layers
+            xs[li].copy_(x_host[li], non_blocking=True)
+            step(i, stream)
+            out_host[li].copy_(outs[li], non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / K_e2e
+
+    # ---- max over ranks
+    t_local = torch.tensor([ms_total, ms_e2e], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t_local, op=torch.distributed.ReduceOp.MAX)
+    ms_total, ms_e2e = float(t_local[0]), float(t_local[1])
+    ms_step = ms_total / K
+
+    tokens_per_s = M * K * world / (ms_total / 1e3)
+    e2e_tokens_per_s = M * world / (ms_e2e / 1e3)
+    peaks = load_peaks()
+    mean_bytes = sum(w["total"] for w in wb) / len(wb)
+    mean_expert_bytes = sum(w["experts"] for w in wb) / len(wb)
+    step_s = ms_step / 1e3
+    decode = M <= DECODE_MAX_TOKENS
+    if decode:
+        achieved = mean_bytes / step_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": traffic_record(cfg),
+                "kernel": "whole step (router+top-k, gate/up, down+combine; PDL-chained)",
+                "algorithmic_bytes_per_step": int(mean_bytes),
+                "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"}
+    else:
+        achieved = flops["total"] / step_s / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic_record(cfg),
+                "kernel": "whole step", "algorithmic_flops_per_step": flops["total"],
+                "peak_source": peaks["source"] + " (bf16_tflops burst)"}
+    res = {
+        "metric": METRIC, "value": round(tokens_per_s, 2), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; NVFP4-quantised N(0,0.02) experts, N(0,1) tokens)",
+        "config": {"workload": workload_name(cfg), "global_batch": M * world, "tokens_per_step": M,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "layers_rotated": n_layers,
+                   "l2": f"weights of {n_layers} layers rotate ({sum(l.expert_bytes() * E for l in layers) / 1e9:.1f} GB resident), step working set streams from HBM"},
+        "weight_gbs": round(mean_bytes / step_s / 1e9, 1),
+        "expert_weight_gbs": round(mean_expert_bytes / step_s / 1e9, 1),
+        "tflops": round(flops["total"] / step_s / 1e12, 3),
+        "roofline": roof,
+        "e2e": {"value": round(e2e_tokens_per_s, 2), "unit": "tokens/s",
+                "h2d_bytes_per_step": M * H * 2, "d2h_bytes_per_step": M * H * 2,
+                "ms_per_step": round(ms_e2e, 6), "steps": K_e2e},
+        "gpu_launches": K * launches_per_step(M),
+        "clocks": clk,
+    }
+    return res, xs, layers
+
+
+def cpu_baseline(cfg: str, n_tokens: int = 64, seed: int = 5):
+    """The oracle on a bounded sample: n_tokens tokens of the configuration's
+    layer shape (one layer), all host cores (OpenMP over tokens)."""
+    import oracle
+    M, H, E, k, I, SI = synth.CONFIGS[cfg]
+    scale = synth.zipf_router_scale(E) if cfg.startswith("skew") else None
+    gen = torch.Generator().manual_seed(seed)
+    x = synth.make_x(n_tokens, H, gen)
+    layer = synth.make_layer(H, E, I, SI, gen, router_row_scale=scale)
+    oracle.build()
+    oracle.forward(x[:1], layer, k)  # warm
+    t0 = time.perf_counter()
+    oracle.forward(x, layer, k)
+    dt = time.perf_counter() - t0
+    cores = oracle.max_threads()
+    return {"value": round(n_tokens / dt, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n_tokens} tokens of one {cfg} layer (M-independent per-token work), "
+                      f"{dt:.1f} s wall on {cores} threads"}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle, timed over K steps of the workload."""
+    import oracle
+    cfg = args.config
+    M, H, E, k, I, SI = synth.CONFIGS[cfg]
+    scale = synth.zipf_router_scale(E) if cfg.startswith("skew") else None
+    oracle.build()
+    gen = torch.Generator().manual_seed(11)
+    layer = synth.make_layer(H, E, I, SI, gen, router_row_scale=scale)
+    # bounded sample: a decode step is its M tokens; a large-batch step is
+    # sampled down to 32 of its tokens (the per-token work does not depend on
+    # M) and throughput counts the tokens computed.  The token total is capped
+    # so that the run stays within a few minutes.
+    K = args.steps
+    per_step = M if M <= DECODE_MAX_TOKENS else 32
+    per_step_eff = max(1, min(per_step, 12000 // max(K, 1)))
+    K_eff = K
+    W = min(args.warmup, 8)
+    x = synth.make_x(per_step_eff * (K_eff + W), H, gen)
+    if W:
+        oracle.forward(x[: per_step_eff * W], layer, k)
+    t0 = time.perf_counter()
+    oracle.forward(x[per_step_eff * W:], layer, k)
+    dt = time.perf_counter() - t0
+    tokens_per_s = per_step_eff * K_eff / dt
+    cores = oracle.max_threads()
+    ms_step = dt / K_eff * 1e3 * (M / per_step_eff)
+    value = round(tokens_per_s, 3)
+    sample = (f"{K_eff} steps x {per_step_eff} tokens of one {cfg} layer on {cores} threads "
+              f"(OpenMP over tokens), {dt:.1f} s")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": K_eff, "warmup": W, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload_name(cfg), "global_batch": M},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    M = synth.CONFIGS[args.config][0]
+    if args.steps <= 0:
+        args.steps = 10000 if M <= DECODE_MAX_TOKENS else 40
+    if args.warmup <= 0:
+        args.warmup = 200 if M <= DECODE_MAX_TOKENS else 5
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    res, xs, layers = run_ours(args, rank, world, local)
+    if world > 1:
+        torch.distributed.barrier()
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(args.config)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

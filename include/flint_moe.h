@@ -1,0 +1,129 @@
+/*
+ * flint_moe: routed-expert MoE block with NVFP4 (W4) experts and BF16 (A16)
+ * activations, for one NVIDIA GB300 (sm_103a).
+ *
+ * The block is the one the vLLM API page "vllm.models.flint.ops.moe"
+ * describes in its module docstring ("Numerics") and in flint_moe / route:
+ * BF16 router logits, fp32 sigmoid top-k renormalised and rounded to BF16,
+ * per selected expert an NVFP4 gate/up projection (E2M1 codes times E4M3
+ * block scales, fp32 accumulation, per-expert fp32 global scale on the
+ * accumulator), act = bf16(silu(g) * u), an NVFP4 down projection
+ * y_e = bf16(acc * gs_e), the routed sum bf16(sum_j tw_j * y_j) accumulated
+ * in fp32 in rank order, plus an ungated BF16 shared expert:
+ * out = bf16(routed + shared).
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers, row-major, contiguous and
+ *    16-byte aligned.  The caller owns every buffer; the library keeps no
+ *    per-call global state and allocates nothing.
+ *  - Work is enqueued on `stream` and returns before it completes.  Argument
+ *    errors are reported synchronously (negative return, nothing enqueued);
+ *    launch failures return FLINT_ERR_CUDA.
+ *  - `workspace` is caller-owned device memory of at least
+ *    flint_moe_workspace_bytes(shape) bytes, zero-filled ONCE after
+ *    allocation (e.g. cudaMemsetAsync).  Every launch leaves its counters at
+ *    zero again, so the same workspace serves any number of calls in stream
+ *    order (and CUDA-graph replays).  Calls that may overlap on the GPU (two
+ *    streams) need separate workspaces.
+ */
+#ifndef FLINT_MOE_H_
+#define FLINT_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* flint_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+enum {
+  FLINT_OK = 0,
+  FLINT_ERR_INVALID_ARG = -1, /* null/misaligned pointer, bad shape */
+  FLINT_ERR_UNSUPPORTED = -2, /* shape outside what the kernels support */
+  FLINT_ERR_WORKSPACE = -3,   /* workspace missing or too small */
+  FLINT_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
+  FLINT_ERR_TIMEOUT = -5,     /* a bounded device-side wait gave up */
+};
+
+/* Problem shape.
+ *   M      tokens (rows of x), M >= 1
+ *   H      hidden size; multiple of 128
+ *   E      routed experts, 1..256
+ *   top_k  experts per token, 1..min(E, 32)
+ *   I      routed-expert intermediate size; multiple of 128
+ *   SI     shared-expert intermediate size; 0 (no shared expert) or a
+ *          multiple of 128 */
+typedef struct {
+  int M, H, E, top_k, I, SI;
+} flint_moe_shape;
+
+/* Bytes of device workspace flint_moe_route / flint_moe_forward need for
+ * `shape`; 0 if the shape is invalid. */
+size_t flint_moe_workspace_bytes(const flint_moe_shape* shape);
+
+/* Routing only: "route" on the page above (BF16 router logits -> top-k ids
+ * int32 and renormalised fp32 weights), with the _topk_row rules: experts
+ * ranked by BF16 logit (bit order: -0 below +0), ties to the lower expert
+ * index; s = 1 / (1 + exp(-logit)) in fp32; tw = bf16(s / (sum_k s + 1e-20))
+ * stored as fp32; both outputs in rank order (column 0 = largest logit).
+ * The fp32 logit sum is taken in one fixed order (32 strided partial sums
+ * combined by a xor butterfly), so ids are reproducible bit for bit.
+ *
+ *   x          bf16 [M, H]
+ *   router_w   bf16 [E, H]
+ *   ids        int32 [M, top_k]   (output)
+ *   tw         fp32  [M, top_k]   (output)
+ */
+int flint_moe_route(const void* x, const void* router_w, const flint_moe_shape* shape,
+                    int32_t* ids, float* tw, void* workspace, size_t workspace_bytes,
+                    flint_stream_t stream);
+
+/* The whole MoE block: "flint_moe" on the page above (routing, NVFP4 experts,
+ * weighted combine) plus the ungated shared expert's output added in.
+ *
+ *   x            bf16 [M, H]
+ *   router_w     bf16 [E, H]
+ *   w13          uint8 [E, 2I, H/2]  e2m1 codes, gate rows [0, I) then up rows
+ *                                     [I, 2I); even K index in the low nibble
+ *   w13_sf       uint8 [E, 2I, H/16] e4m3 (float8_e4m3fn) block scales, one per
+ *                                     16 consecutive K of a row
+ *   w13_gs       fp32  [E]           global scale of gate and up (ModelOpt
+ *                                     weight_scale_2; gate and up must share it)
+ *   w2           uint8 [E, H, I/2], w2_sf uint8 [E, H, I/16], w2_gs fp32 [E]
+ *   shared_gu    bf16 [2*SI, H]      shared expert gate rows then up rows
+ *                                     (NULL when SI == 0)
+ *   shared_down  bf16 [H, SI]        (NULL when SI == 0)
+ *   out          bf16 [M, H]         (output)
+ *   ids_out, tw_out  optional int32 / fp32 [M, top_k] copies of the routing
+ *                    (NULL to skip)
+ *
+ * Numerics: BF16 activations, E2M1 x E4M3 weights dequantised exactly,
+ * fp32 accumulation with the global scale applied to the accumulator;
+ * act = bf16(silu(g) * u) with sigmoid = rcp.approx(1 + ex2.approx(-g log2 e));
+ * y_e = bf16(acc * gs2_e); shared expert gS, uS = bf16(dot),
+ * sact = bf16(silu(gS) * uS), ys = bf16(dot); out = bf16(bf16(sum_j tw_j y_j) + ys).
+ * Precondition: |x| < 2^120 (activations are multiplied by weights scaled by
+ * 2^-7 internally; far beyond any fp32-representable product range). */
+int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13,
+                      const uint8_t* w13_sf, const float* w13_gs, const uint8_t* w2,
+                      const uint8_t* w2_sf, const float* w2_gs, const void* shared_gu,
+                      const void* shared_down, const flint_moe_shape* shape, void* out,
+                      int32_t* ids_out, float* tw_out, void* workspace, size_t workspace_bytes,
+                      flint_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the device status word of
+ * `workspace`: FLINT_OK, or the error a kernel recorded (FLINT_ERR_TIMEOUT
+ * when a bounded device-side wait gave up).  FLINT_ERR_CUDA if the stream
+ * reports an error. */
+int flint_moe_status(void* workspace, flint_stream_t stream);
+
+/* Static description of an error code. */
+const char* flint_moe_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLINT_MOE_H_ */

@@ -1,0 +1,158 @@
+"""ctypes binding of libflint_moe (include/flint_moe.h), same names as the C ABI.
+
+Argument marshalling only: every step of the MoE block runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors (torch provides device memory
+and streams); their device pointers are passed straight through.  If the
+library cannot be built or loaded this module raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import build as _build
+
+FLINT_OK = 0
+FLINT_ERR_INVALID_ARG = -1
+FLINT_ERR_UNSUPPORTED = -2
+FLINT_ERR_WORKSPACE = -3
+FLINT_ERR_CUDA = -4
+FLINT_ERR_TIMEOUT = -5
+
+# Every C symbol the header declares (checked by tests/test_abi.py).
+EXPORTED = ("flint_moe_workspace_bytes", "flint_moe_route", "flint_moe_forward",
+            "flint_moe_status", "flint_moe_strerror")
+
+
+class FlintMoEError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {flint_moe_strerror(code)} (code {code})")
+        self.code = code
+
+
+class flint_moe_shape(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int), ("H", ctypes.c_int), ("E", ctypes.c_int),
+                ("top_k", ctypes.c_int), ("I", ctypes.c_int), ("SI", ctypes.c_int)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Build (if stale) and load libflint_moe.so; raises on failure."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            lib = ctypes.CDLL(path)
+            P, S = ctypes.c_void_p, ctypes.POINTER(flint_moe_shape)
+            lib.flint_moe_workspace_bytes.restype = ctypes.c_size_t
+            lib.flint_moe_workspace_bytes.argtypes = [S]
+            lib.flint_moe_route.restype = ctypes.c_int
+            lib.flint_moe_route.argtypes = [P, P, S, P, P, P, ctypes.c_size_t, P]
+            lib.flint_moe_forward.restype = ctypes.c_int
+            lib.flint_moe_forward.argtypes = [P] * 10 + [S, P, P, P, P, ctypes.c_size_t, P]
+            lib.flint_moe_status.restype = ctypes.c_int
+            lib.flint_moe_status.argtypes = [P, P]
+            lib.flint_moe_strerror.restype = ctypes.c_char_p
+            lib.flint_moe_strerror.argtypes = [ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream or None
+    return int(stream) or None
+
+
+def _shape(M, H, E, top_k, I, SI) -> flint_moe_shape:
+    return flint_moe_shape(int(M), int(H), int(E), int(top_k), int(I), int(SI))
+
+
+def flint_moe_strerror(code: int) -> str:
+    return load().flint_moe_strerror(int(code)).decode()
+
+
+def flint_moe_workspace_bytes(M: int, H: int, E: int, top_k: int, I: int, SI: int) -> int:
+    """Workspace bytes for the shape (0 if the shape is invalid)."""
+    s = _shape(M, H, E, top_k, I, SI)
+    return int(load().flint_moe_workspace_bytes(ctypes.byref(s)))
+
+
+def flint_moe_route(x, router_w, top_k: int, ids, tw, workspace, *, I: int = 128, SI: int = 0,
+                    stream=None) -> None:
+    """ids (int32 [M, k]) and tw (fp32 [M, k]) of x (bf16 [M, H]) under
+    router_w (bf16 [E, H]).  `workspace` is a uint8 CUDA tensor sized by
+    flint_moe_workspace_bytes for the same (M, H, E, top_k, I, SI)."""
+    M, H = x.shape
+    E = router_w.shape[0]
+    s = _shape(M, H, E, top_k, I, SI)
+    rc = load().flint_moe_route(_ptr(x), _ptr(router_w), ctypes.byref(s), _ptr(ids), _ptr(tw),
+                                _ptr(workspace), workspace.numel(), _stream(stream))
+    if rc != FLINT_OK:
+        raise FlintMoEError(rc, "flint_moe_route")
+
+
+def flint_moe_forward(x, router_w, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, shared_gu, shared_down,
+                      top_k: int, out, workspace, ids_out=None, tw_out=None, stream=None) -> None:
+    """out (bf16 [M, H]) = MoE block of x; see include/flint_moe.h for the
+    layouts.  shared_gu / shared_down may be None (no shared expert)."""
+    M, H = x.shape
+    E = router_w.shape[0]
+    I = w2.shape[2] * 2
+    SI = 0 if shared_down is None else shared_down.shape[1]
+    s = _shape(M, H, E, top_k, I, SI)
+    rc = load().flint_moe_forward(
+        _ptr(x), _ptr(router_w), _ptr(w13), _ptr(w13_sf), _ptr(w13_gs), _ptr(w2), _ptr(w2_sf),
+        _ptr(w2_gs), _ptr(shared_gu), _ptr(shared_down), ctypes.byref(s), _ptr(out), _ptr(ids_out),
+        _ptr(tw_out), _ptr(workspace), workspace.numel(), _stream(stream))
+    if rc != FLINT_OK:
+        raise FlintMoEError(rc, "flint_moe_forward")
+
+
+def flint_moe_status(workspace, stream=None) -> int:
+    """Synchronise `stream` and return (and clear) the workspace status word."""
+    return int(load().flint_moe_status(_ptr(workspace), _stream(stream)))
+
+
+# ---------------------------------------------------------------- helpers
+def alloc_workspace(M: int, H: int, E: int, top_k: int, I: int, SI: int,
+                    device="cuda") -> torch.Tensor:
+    """A zero-filled workspace (do this once, outside graph capture)."""
+    n = flint_moe_workspace_bytes(M, H, E, top_k, I, SI)
+    if n == 0:
+        raise FlintMoEError(FLINT_ERR_INVALID_ARG, "alloc_workspace")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def forward_layer(x, layer, top_k: int, workspace=None, out=None, ids_out=None, tw_out=None,
+                  stream=None):
+    """flint_moe_forward on a synth.MoELayer-like object (CUDA tensors)."""
+    M, H = x.shape
+    if workspace is None:
+        workspace = alloc_workspace(M, H, layer.E, top_k, layer.I, layer.SI, x.device)
+    if out is None:
+        out = torch.empty_like(x)
+    flint_moe_forward(x, layer.router_w, layer.w13, layer.w13_sf, layer.w13_gs, layer.w2,
+                      layer.w2_sf, layer.w2_gs, layer.shared_gu if layer.SI else None,
+                      layer.shared_down if layer.SI else None, top_k, out, workspace,
+                      ids_out=ids_out, tw_out=tw_out, stream=stream)
+    return out

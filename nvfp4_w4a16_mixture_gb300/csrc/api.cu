@@ -1,0 +1,181 @@
+// C-ABI entry points of libflint_moe (declared in include/flint_moe.h).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "flint_moe.h"
+#include "internal.h"
+
+namespace flint {
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static bool shape_valid(const flint_moe_shape* s) {
+  if (!s) return false;
+  if (s->M < 1 || s->H < 128 || s->H % 128 != 0) return false;
+  if (s->E < 1 || s->E > kMaxE) return false;
+  if (s->top_k < 1 || s->top_k > s->E || s->top_k > kMaxTopK) return false;
+  if (s->I < 128 || s->I % 128 != 0) return false;
+  if (s->SI < 0 || s->SI % 128 != 0) return false;
+  // element counts addressed with 32-bit indices in places
+  if ((int64_t)s->M * s->top_k > (int64_t)1 << 30) return false;
+  if ((int64_t)s->H * 2 * s->I > (int64_t)1 << 31) return false;
+  return true;
+}
+
+WsLayout ws_layout(const flint_moe_shape& s) {
+  WsLayout L{};
+  const size_t M = s.M, H = s.H, E = s.E, k = s.top_k, I = s.I, SI = s.SI;
+  const size_t np = M * k;
+  const size_t nchunks = (np + 1023) / 1024;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.status = take(16);
+  L.tok_cnt = take(4 * ((M + kRouteTokens - 1) / kRouteTokens));
+  L.glob_cnt = take(16);
+  L.hblk_cnt = take(4 * (H / 16));
+  L.logits = take(2 * M * E);
+  L.ids = take(4 * np);
+  L.tw = take(4 * np);
+  L.e_cnt = take(4 * E);
+  L.e_off = take(4 * (E + 1));
+  L.uniq = take(4 * (E + 1));
+  L.sorted_pairs = take(4 * np);
+  L.rowof = take(4 * np);
+  L.gcnt = take(4 * 2 * nchunks * E);
+  L.act = take(2 * np * I);
+  L.sact = take(2 * M * (SI > 0 ? SI : 1));
+  L.y = take(2 * np * H);
+  L.ys = take(2 * M * H);
+  L.total = off;
+  return L;
+}
+
+Ws ws_pointers(void* base, const WsLayout& L) {
+  char* b = static_cast<char*>(base);
+  Ws w;
+  w.status = reinterpret_cast<int*>(b + L.status);
+  w.tok_cnt = reinterpret_cast<int*>(b + L.tok_cnt);
+  w.glob_cnt = reinterpret_cast<int*>(b + L.glob_cnt);
+  w.hblk_cnt = reinterpret_cast<int*>(b + L.hblk_cnt);
+  w.logits = reinterpret_cast<uint16_t*>(b + L.logits);
+  w.ids = reinterpret_cast<int*>(b + L.ids);
+  w.tw = reinterpret_cast<float*>(b + L.tw);
+  w.e_cnt = reinterpret_cast<int*>(b + L.e_cnt);
+  w.e_off = reinterpret_cast<int*>(b + L.e_off);
+  w.uniq = reinterpret_cast<int*>(b + L.uniq);
+  w.sorted_pairs = reinterpret_cast<int*>(b + L.sorted_pairs);
+  w.rowof = reinterpret_cast<int*>(b + L.rowof);
+  w.gcnt = reinterpret_cast<int*>(b + L.gcnt);
+  w.act = reinterpret_cast<uint16_t*>(b + L.act);
+  w.sact = reinterpret_cast<uint16_t*>(b + L.sact);
+  w.y = reinterpret_cast<uint16_t*>(b + L.y);
+  w.ys = reinterpret_cast<uint16_t*>(b + L.ys);
+  return w;
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace flint
+
+using namespace flint;
+
+extern "C" {
+
+size_t flint_moe_workspace_bytes(const flint_moe_shape* shape) {
+  if (!shape_valid(shape)) return 0;
+  return ws_layout(*shape).total;
+}
+
+int flint_moe_route(const void* x, const void* router_w, const flint_moe_shape* shape, int32_t* ids,
+                    float* tw, void* workspace, size_t workspace_bytes, flint_stream_t stream) {
+  if (!shape_valid(shape)) return FLINT_ERR_INVALID_ARG;
+  if (!x || !router_w || !ids || !tw) return FLINT_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(router_w, 16) || !aligned(ids, 4) || !aligned(tw, 4))
+    return FLINT_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return FLINT_ERR_WORKSPACE;
+  const WsLayout L = ws_layout(*shape);
+  if (workspace_bytes < L.total) return FLINT_ERR_WORKSPACE;
+  MoEArgs a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.router_w = static_cast<const uint16_t*>(router_w);
+  a.ids_out = ids;
+  a.tw_out = tw;
+  a.M = shape->M; a.H = shape->H; a.E = shape->E; a.k = shape->top_k; a.I = shape->I; a.SI = shape->SI;
+  a.ws = ws_pointers(workspace, L);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_route(a, false, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
+  return FLINT_OK;
+}
+
+int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13, const uint8_t* w13_sf,
+                      const float* w13_gs, const uint8_t* w2, const uint8_t* w2_sf,
+                      const float* w2_gs, const void* shared_gu, const void* shared_down,
+                      const flint_moe_shape* shape, void* out, int32_t* ids_out, float* tw_out,
+                      void* workspace, size_t workspace_bytes, flint_stream_t stream) {
+  if (!shape_valid(shape)) return FLINT_ERR_INVALID_ARG;
+  if (!x || !router_w || !w13 || !w13_sf || !w13_gs || !w2 || !w2_sf || !w2_gs || !out)
+    return FLINT_ERR_INVALID_ARG;
+  if (shape->SI > 0 && (!shared_gu || !shared_down)) return FLINT_ERR_INVALID_ARG;
+  const void* p16[] = {x, router_w, w13, w13_sf, w2, w2_sf, out};
+  for (const void* p : p16)
+    if (!aligned(p, 16)) return FLINT_ERR_INVALID_ARG;
+  if (shape->SI > 0 && (!aligned(shared_gu, 16) || !aligned(shared_down, 16)))
+    return FLINT_ERR_INVALID_ARG;
+  if (!aligned(w13_gs, 4) || !aligned(w2_gs, 4)) return FLINT_ERR_INVALID_ARG;
+  if ((ids_out && !aligned(ids_out, 4)) || (tw_out && !aligned(tw_out, 4)))
+    return FLINT_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return FLINT_ERR_WORKSPACE;
+  const WsLayout L = ws_layout(*shape);
+  if (workspace_bytes < L.total) return FLINT_ERR_WORKSPACE;
+
+  MoEArgs a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.router_w = static_cast<const uint16_t*>(router_w);
+  a.w13 = w13; a.w13_sf = w13_sf; a.w13_gs = w13_gs;
+  a.w2 = w2; a.w2_sf = w2_sf; a.w2_gs = w2_gs;
+  a.shared_gu = static_cast<const uint16_t*>(shared_gu);
+  a.shared_down = static_cast<const uint16_t*>(shared_down);
+  a.out = static_cast<uint16_t*>(out);
+  a.ids_out = ids_out;
+  a.tw_out = tw_out;
+  a.M = shape->M; a.H = shape->H; a.E = shape->E; a.k = shape->top_k; a.I = shape->I; a.SI = shape->SI;
+  a.ws = ws_pointers(workspace, L);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  if (launch_route(a, true, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
+  if (launch_decode_gate_up(a, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
+  if (launch_decode_down(a, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
+  return FLINT_OK;
+}
+
+int flint_moe_status(void* workspace, flint_stream_t stream) {
+  if (!workspace) return FLINT_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FLINT_ERR_CUDA;
+  int status = 0;
+  if (cudaMemcpy(&status, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FLINT_ERR_CUDA;
+  if (status != 0) {
+    if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return FLINT_ERR_CUDA;
+    return status;
+  }
+  return FLINT_OK;
+}
+
+const char* flint_moe_strerror(int code) {
+  switch (code) {
+    case FLINT_OK: return "ok";
+    case FLINT_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, or bad shape)";
+    case FLINT_ERR_UNSUPPORTED: return "shape not supported by the kernels";
+    case FLINT_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case FLINT_ERR_CUDA: return "CUDA runtime or launch error";
+    case FLINT_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+    default: return "unknown error";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,134 @@
+// Device helpers shared by the flint_moe kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#define FLINT_DEV __device__ __forceinline__
+
+namespace flint {
+
+// ------------------------------------------------------------------ bf16 --
+FLINT_DEV float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// fp32 -> bf16 bits, round to nearest even (cvt.rn.bf16.f32).
+FLINT_DEV uint32_t f32_to_bf16_bits(float f) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+FLINT_DEV float round_bf16(float f) { return __bfloat162float(__float2bfloat16_rn(f)); }
+
+// ------------------------------------------------------------------ NVFP4 --
+// Two e2m1 codes -> one bf16x2 holding e2m1(code) * 2^-126 each, exactly.
+// Placing the code's exponent/mantissa bits (c = bits 2..0) at bf16 bits 8..6
+// makes the bf16 exponent field equal to the e2m1 exponent field, so the
+// bf16 value is 2^(E-127) * (1 + m/2) = e2m1 * 2^-126 for E > 0 and the bf16
+// subnormal m/2 * 2^-126 = e2m1 * 2^-126 for E = 0; the sign goes to bit 15.
+// `v` carries code A in bits 3..0 and code B in bits 19..16.
+FLINT_DEV uint32_t e2m1x2_to_bf16x2_scaled(uint32_t v) {
+  return ((v << 6) & 0x01C001C0u) | ((v << 12) & 0x80008000u);
+}
+
+// Pair `a` (0..3) of a word of 8 codes (nibble i = K offset i): codes a and
+// a + 4 as (lo, hi) of a bf16x2, each e2m1 * 2^-126.
+FLINT_DEV uint32_t e2m1_pair(uint32_t word, int a) {
+  return e2m1x2_to_bf16x2_scaled(word >> (4 * a));
+}
+
+// Two e4m3 block-scale bytes (lo = bits 7..0, hi = bits 15..8 of `b2`) ->
+// bf16x2 of scale * 2^119 each, exact: e4m3 -> f16 is exact (hardware cvt),
+// the fp32 product with 2^119 is exact (max 448 * 2^119 < 2^128) and the
+// result has at most 4 significant bits, so the bf16 rounding is exact.
+FLINT_DEV uint32_t e4m3x2_to_bf16x2_x2p119(uint32_t b2) {
+  uint32_t h2;
+  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h2) : "r"(b2));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  const float k = __int_as_float((119 + 127) << 23);  // 2^119
+  float lo = __low2float(h) * k;
+  float hi = __high2float(h) * k;
+  __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+FLINT_DEV uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a),
+                             *reinterpret_cast<__nv_bfloat162*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Broadcast the lo (sel 0) or hi (sel 1) bf16 of a bf16x2 to both halves.
+FLINT_DEV uint32_t bf16x2_bcast(uint32_t v, int hi) {
+  return hi ? __byte_perm(v, 0, 0x3232) : __byte_perm(v, 0, 0x1010);
+}
+
+// ------------------------------------------------------------ tensor core --
+// D = A * B + D, m16n8k16, bf16 inputs, fp32 accumulators (mma.sync).
+FLINT_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// --------------------------------------------------------------- memory --
+FLINT_DEV uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+FLINT_DEV uint32_t ldg_nc_u16(const void* p) {
+  unsigned short r;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  return r;
+}
+
+// L2-coherent loads for data written by other CTAs of the same or an
+// earlier, still-overlapping grid.
+FLINT_DEV uint4 ldg_cg_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+FLINT_DEV int ldg_cg_i32(const int* p) {
+  int r;
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+FLINT_DEV float ldg_cg_f32(const float* p) {
+  float r;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(r) : "l"(p));
+  return r;
+}
+FLINT_DEV uint32_t ldg_cg_u16(const void* p) {
+  unsigned short r;
+  asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  return r;
+}
+
+// ------------------------------------------------ programmatic launches --
+// Wait until the preceding grid in the stream has completed and its writes
+// are visible (no-op when launched without the PDL attribute).
+FLINT_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next grid in the stream to start launching.
+FLINT_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// --------------------------------------------------------------- math --
+// sigmoid as rcp.approx(1 + ex2.approx(-g * log2 e)); silu(g) = g * sigmoid(g).
+FLINT_DEV float silu_approx(float g) {
+  float e, r;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(e) : "f"(-g * 1.4426950408889634f));
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return g * r;
+}
+
+FLINT_DEV uint32_t ordered_bf16(uint32_t b) { return (b & 0x8000u) ? (b ^ 0xFFFFu) : (b | 0x8000u); }
+
+}  // namespace flint

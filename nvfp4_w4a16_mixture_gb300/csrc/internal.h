@@ -1,0 +1,90 @@
+// Internal interface between the C-ABI entry points and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "flint_moe.h"
+
+namespace flint {
+
+constexpr int kMaxE = 256;
+constexpr int kMaxTopK = 32;
+constexpr int kDecodeMaxTokens = 64;  // M above this uses the grouped path
+
+// Offsets (bytes from the workspace base) of every workspace region.  All
+// regions are 256-byte aligned.  Counters and the status word live in the
+// first region; every launch returns its counters to zero.
+struct WsLayout {
+  size_t status;       // int32[1]: first error recorded by a kernel
+  size_t tok_cnt;      // int32[ceil(M / kRouteTokens)]: router last-arriver counters
+  size_t glob_cnt;     // int32[4]: global last-arriver counters
+  size_t hblk_cnt;     // int32[H / 16]: down/combine last-arriver counters
+  size_t logits;       // bf16 [M, E]
+  size_t ids;          // int32 [M, k]
+  size_t tw;           // fp32 [M, k]
+  size_t e_cnt;        // int32 [E]: pairs routed to each expert
+  size_t e_off;        // int32 [E + 1]: exclusive prefix of e_cnt
+  size_t uniq;         // int32 [1 + E]: [0] = U (experts with >= 1 pair), then their ids
+  size_t sorted_pairs; // int32 [M * k]: pair ids t*k+j, stable-sorted by expert
+  size_t rowof;        // int32 [M * k]: sorted position of pair t*k+j
+  size_t gcnt;         // int32 [2, nchunks, E]: per-chunk counts and offsets (grouping)
+  size_t act;          // bf16 [M * k, I]   row = sorted position of the pair
+  size_t sact;         // bf16 [M, SI]
+  size_t y;            // bf16 [M * k, H]   row = sorted position of the pair
+  size_t ys;           // bf16 [M, H]
+  size_t total;
+};
+
+constexpr int kRouteTokens = 8;  // tokens per router CTA
+
+WsLayout ws_layout(const flint_moe_shape& s);
+
+struct Ws {  // device pointers into one workspace
+  int* status;
+  int* tok_cnt;
+  int* glob_cnt;
+  int* hblk_cnt;
+  uint16_t* logits;
+  int* ids;
+  float* tw;
+  int* e_cnt;
+  int* e_off;
+  int* uniq;
+  int* sorted_pairs;
+  int* rowof;
+  int* gcnt;
+  uint16_t* act;
+  uint16_t* sact;
+  uint16_t* y;
+  uint16_t* ys;
+};
+
+Ws ws_pointers(void* base, const WsLayout& L);
+
+struct MoEArgs {
+  const uint16_t* x;
+  const uint16_t* router_w;
+  const uint8_t* w13;
+  const uint8_t* w13_sf;
+  const float* w13_gs;
+  const uint8_t* w2;
+  const uint8_t* w2_sf;
+  const float* w2_gs;
+  const uint16_t* shared_gu;
+  const uint16_t* shared_down;
+  uint16_t* out;
+  int* ids_out;   // optional user copy
+  float* tw_out;  // optional user copy
+  int M, H, E, k, I, SI;
+  Ws ws;
+};
+
+// Launchers (return cudaSuccess or the launch error).  `pdl` launches the
+// kernel with programmatic stream serialisation.
+cudaError_t launch_route(const MoEArgs& a, bool build_meta, cudaStream_t st, bool pdl);
+cudaError_t launch_decode_gate_up(const MoEArgs& a, cudaStream_t st, bool pdl);
+cudaError_t launch_decode_down(const MoEArgs& a, cudaStream_t st, bool pdl);
+
+}  // namespace flint

@@ -1,0 +1,107 @@
+"""The C-ABI library builds, loads and exports every symbol include/*.h
+declares; argument validation answers synchronously (no GPU work)."""
+from __future__ import annotations
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import nvfp4_w4a16_mixture_gb300 as fm
+from nvfp4_w4a16_mixture_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions() -> set[str]:
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(flint_moe_\w+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_binding_names():
+    assert declared_functions() == set(fm.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = fm.load()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_workspace_bytes_valid_and_invalid_shapes():
+    ok = fm.flint_moe_workspace_bytes(1, 2048, 128, 8, 768, 768)
+    assert ok > 0 and ok % 256 == 0
+    big = fm.flint_moe_workspace_bytes(4096, 2048, 128, 8, 768, 768)
+    assert big > ok
+    for bad in [(0, 2048, 128, 8, 768, 768), (1, 2000, 128, 8, 768, 768),
+                (1, 2048, 257, 8, 768, 768), (1, 2048, 8, 9, 768, 768),
+                (1, 2048, 128, 0, 768, 768), (1, 2048, 128, 33, 768, 768),
+                (1, 2048, 128, 8, 700, 768), (1, 2048, 128, 8, 768, 100),
+                (1, 2048, 128, 8, 768, -128)]:
+        assert fm.flint_moe_workspace_bytes(*bad) == 0, bad
+    assert fm.flint_moe_workspace_bytes(3, 256, 8, 2, 128, 0) > 0  # no shared expert
+
+
+def test_strerror_covers_codes():
+    for code in (fm.FLINT_OK, fm.FLINT_ERR_INVALID_ARG, fm.FLINT_ERR_UNSUPPORTED,
+                 fm.FLINT_ERR_WORKSPACE, fm.FLINT_ERR_CUDA, fm.FLINT_ERR_TIMEOUT):
+        assert fm.flint_moe_strerror(code) not in ("", "unknown error")
+    assert fm.flint_moe_strerror(12345) == "unknown error"
+
+
+def _call_forward(ptrs, shape, ws_bytes):
+    lib = fm.load()
+    s = _lib.flint_moe_shape(*shape)
+    return lib.flint_moe_forward(*ptrs[:10], ctypes.byref(s), ptrs[10], None, None, ptrs[11],
+                                 ws_bytes, None)
+
+
+def test_validation_is_synchronous_and_touches_no_memory():
+    """Null, misaligned and undersized arguments are rejected before any CUDA
+    call (fake, never-dereferenced addresses)."""
+    shape = (2, 256, 8, 2, 128, 128)
+    need = fm.flint_moe_workspace_bytes(*shape)
+    good = [0x10000 * (i + 1) for i in range(12)]
+    assert _call_forward([None] + good[1:], shape, need) == fm.FLINT_ERR_INVALID_ARG
+    mis = list(good)
+    mis[2] += 8  # w13 not 16-byte aligned
+    assert _call_forward(mis, shape, need) == fm.FLINT_ERR_INVALID_ARG
+    assert _call_forward(good, shape, need - 1) == fm.FLINT_ERR_WORKSPACE
+    ws_mis = list(good)
+    ws_mis[11] += 16
+    assert _call_forward(ws_mis, shape, need) == fm.FLINT_ERR_WORKSPACE
+    assert _call_forward(good, (2, 256, 8, 3, 128, 100), need) == fm.FLINT_ERR_INVALID_ARG
+    noshared = list(good)
+    noshared[8] = None
+    assert _call_forward(noshared, shape, need) == fm.FLINT_ERR_INVALID_ARG
+    lib = fm.load()
+    s = _lib.flint_moe_shape(*shape)
+    assert lib.flint_moe_route(None, good[1], ctypes.byref(s), good[2], good[3], good[4], need,
+                               None) == fm.FLINT_ERR_INVALID_ARG
+
+
+def test_product_path_does_not_import_oracle():
+    """The package never imports the oracle (the oracle is test-only)."""
+    pkg = os.path.join(ROOT, "nvfp4_w4a16_mixture_gb300")
+    for path in glob.glob(os.path.join(pkg, "**", "*.py"), recursive=True):
+        src = open(path).read()
+        assert not re.search(r"^\s*(import|from)\s+oracle", src, re.M), path
+    for path in glob.glob(os.path.join(pkg, "csrc", "*")):
+        assert "oracle" not in open(path).read().lower(), path
+
+
+@pytest.mark.parametrize("shape", [(1, 2048, 128, 8, 768, 768), (64, 2048, 128, 8, 768, 768),
+                                   (4096, 2048, 128, 8, 768, 768)])
+def test_workspace_fits_expected_regions(shape):
+    M, H, E, k, I, SI = shape
+    need = fm.flint_moe_workspace_bytes(*shape)
+    floor = 2 * M * k * (I + H) + 2 * M * (SI + H)  # act, y, sact, ys
+    assert floor <= need <= floor + 4 * 1024 * 1024 + 16 * M * k + 2 * M * E

@@ -1,0 +1,191 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+ids must match bit for bit; tw and the BF16 outputs follow the tolerance rule
+in tests/tolerance.py.  Inputs are seeded and synthetic (synth.py recipe);
+full-size layers are drawn on the GPU with torch's seeded generator and copied
+to the CPU for the oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import nvfp4_w4a16_mixture_gb300 as fm
+from nvfp4_w4a16_mixture_gb300 import synth
+from tolerance import check_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(a, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def run_gpu(x, layer, k, ws=None):
+    M, H = x.shape
+    ids = torch.empty(M, k, dtype=torch.int32, device=x.device)
+    tw = torch.empty(M, k, dtype=torch.float32, device=x.device)
+    out = torch.empty_like(x)
+    if ws is None:
+        ws = fm.alloc_workspace(M, H, layer.E, k, layer.I, layer.SI)
+    fm.forward_layer(x, layer, k, workspace=ws, out=out, ids_out=ids, tw_out=tw)
+    assert fm.flint_moe_status(ws) == fm.FLINT_OK
+    return out, ids, tw
+
+
+def compare(x, layer, k, tokens=None, ws=None, gpu=None):
+    """GPU forward vs oracle (on `tokens`, all by default)."""
+    out, ids, tw = gpu if gpu is not None else run_gpu(x, layer, k, ws)
+    xc, lc = x.cpu(), layer.to("cpu")
+    ref = oracle.forward(xc, lc, k, tokens=tokens)
+    sel = slice(None) if tokens is None else np.asarray(tokens)
+    g_ids = ids.cpu().numpy()[sel]
+    assert np.array_equal(g_ids, ref["ids"]), "expert ids differ"
+    g_tw = tw.cpu().numpy()[sel]
+    assert np.array_equal(f32_to_bf16_bits(g_tw).astype(np.uint32) << 16,
+                          np.ascontiguousarray(g_tw).view(np.uint32)), "tw not bf16-valued"
+    check_bf16(f32_to_bf16_bits(g_tw), f32_to_bf16_bits(ref["tw"]), "tw")
+    return check_bf16(bits(out)[sel], ref["out"], "out")
+
+
+def problem(M, H, E, k, I, SI, seed=0, device="cuda", scale=None):
+    x, layer = synth.make_problem(M, H, E, k, I, SI, seed=seed, device=device, router_row_scale=scale)
+    return x.to("cuda"), layer.to("cuda")
+
+
+# ------------------------------------------------------------------- small
+@pytest.mark.parametrize("shape", [
+    synth.CONFIGS["tiny"],
+    (13, 384, 96, 6, 256, 128),   # ragged M, E not a power of two
+    (5, 256, 8, 1, 128, 128),     # top_k = 1
+    (3, 256, 8, 8, 128, 128),     # top_k = E
+    (7, 256, 16, 4, 128, 0),      # no shared expert
+    (9, 512, 256, 8, 256, 256),   # E = 256
+    (1, 128, 4, 2, 128, 128),     # smallest H and I
+    (64, 256, 32, 8, 128, 128),   # 64 tokens: largest decode batch
+    (65, 256, 32, 8, 128, 128),   # first grouped-path batch
+    (300, 384, 24, 5, 256, 128),  # grouped path, ragged everything
+])
+def test_parity_small_shapes(shape):
+    x, layer = problem(*shape, seed=sum(shape), device="cpu")
+    compare(x, layer, shape[3])
+
+
+def test_route_only_matches_oracle():
+    M, H, E, k = 37, 2048, 128, 8
+    x, layer = problem(M, H, E, k, 128, 0, seed=4, device="cpu")
+    ws = fm.alloc_workspace(M, H, E, k, 128, 0)
+    ids = torch.empty(M, k, dtype=torch.int32, device="cuda")
+    tw = torch.empty(M, k, dtype=torch.float32, device="cuda")
+    fm.flint_moe_route(x, layer.router_w, k, ids, tw, ws)
+    torch.cuda.synchronize()
+    _, r_ids, r_tw = oracle.route(x.cpu(), layer.router_w.cpu(), k)
+    assert np.array_equal(ids.cpu().numpy(), r_ids)
+    check_bf16(f32_to_bf16_bits(tw.cpu().numpy()), f32_to_bf16_bits(r_tw), "tw")
+
+
+def test_router_ties_go_to_lower_index():
+    """Duplicated router rows give identical logits; the lower expert wins."""
+    M, H, E, k = 16, 256, 16, 4
+    x, layer = problem(M, H, E, k, 128, 128, seed=9, device="cpu")
+    w = layer.router_w.clone()
+    w[1::2] = w[0::2]
+    layer.router_w = w.contiguous()
+    compare(x, layer, k)
+
+
+# ------------------------------------------------------ full-size layers
+@pytest.fixture(scope="module")
+def decode_layer():
+    M, H, E, k, I, SI = synth.CONFIGS["decode1"]
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    x1 = synth.make_x(1, H, gen, "cuda")
+    layer = synth.make_layer(H, E, I, SI, gen, "cuda")
+    return x1, layer, k
+
+
+def test_parity_decode_single_token(decode_layer):
+    x1, layer, k = decode_layer
+    compare(x1, layer, k)
+
+
+@pytest.mark.parametrize("M", [2, 4, 8, 16, 32, 64])
+def test_parity_decode_batch_sweep(decode_layer, M):
+    _, layer, k = decode_layer
+    gen = torch.Generator(device="cuda").manual_seed(100 + M)
+    x = synth.make_x(M, layer.H, gen, "cuda")
+    compare(x, layer, k)
+
+
+def test_parity_prefill_4096_sampled(decode_layer):
+    """M = 4096 at full layer size: every token's ids against the oracle's
+    routing, outputs on a seeded sample of tokens."""
+    _, layer, k = decode_layer
+    M = 4096
+    gen = torch.Generator(device="cuda").manual_seed(4096)
+    x = synth.make_x(M, layer.H, gen, "cuda")
+    out, ids, tw = run_gpu(x, layer, k)
+    _, r_ids, _ = oracle.route(x.cpu(), layer.router_w.cpu(), k)
+    assert np.array_equal(ids.cpu().numpy(), r_ids)
+    tokens = np.sort(np.random.default_rng(0).choice(M, 48, replace=False))
+    tokens = np.concatenate([[0], tokens, [M - 1]])
+    compare(x, layer, k, tokens=tokens, gpu=(out, ids, tw))
+
+
+def test_parity_skewed_16384_sampled():
+    M, H, E, k, I, SI = synth.CONFIGS["skew16384"]
+    scale = synth.zipf_router_scale(E)
+    gen = torch.Generator(device="cuda").manual_seed(16384)
+    x = synth.make_x(M, H, gen, "cuda")
+    layer = synth.make_layer(H, E, I, SI, gen, "cuda", router_row_scale=scale)
+    out, ids, tw = run_gpu(x, layer, k)
+    _, r_ids, _ = oracle.route(x.cpu(), layer.router_w.cpu(), k)
+    assert np.array_equal(ids.cpu().numpy(), r_ids)
+    tokens = np.sort(np.random.default_rng(1).choice(M, 32, replace=False))
+    compare(x, layer, k, tokens=tokens, gpu=(out, ids, tw))
+
+
+# ------------------------------------------------------------- properties
+def test_deterministic_and_token_permutation_invariant(decode_layer):
+    _, layer, k = decode_layer
+    M = 48
+    gen = torch.Generator(device="cuda").manual_seed(7)
+    x = synth.make_x(M, layer.H, gen, "cuda")
+    ws = fm.alloc_workspace(M, layer.H, layer.E, k, layer.I, layer.SI)
+    o1, i1, t1 = run_gpu(x, layer, k, ws)
+    o2, i2, t2 = run_gpu(x, layer, k, ws)  # same workspace: counters came back to zero
+    assert torch.equal(o1, o2) and torch.equal(i1, i2) and torch.equal(t1, t2)
+    perm = torch.randperm(M, generator=torch.Generator().manual_seed(3)).cuda()
+    o3, i3, _ = run_gpu(x[perm].contiguous(), layer, k, ws)
+    assert torch.equal(o3, o1[perm]) and torch.equal(i3, i1[perm])
+
+
+def test_workspace_reuse_across_shapes_in_stream_order(decode_layer):
+    """One workspace sized for the largest call serves smaller calls."""
+    _, layer, k = decode_layer
+    ws = fm.alloc_workspace(64, layer.H, layer.E, k, layer.I, layer.SI)
+    for M in (1, 64, 3, 17):
+        gen = torch.Generator(device="cuda").manual_seed(200 + M)
+        x = synth.make_x(M, layer.H, gen, "cuda")
+        compare(x, layer, k, ws=ws)
+
+
+def test_bad_arguments_raise_before_launch(decode_layer):
+    x1, layer, k = decode_layer
+    ws = fm.alloc_workspace(1, layer.H, layer.E, k, layer.I, layer.SI)
+    out = torch.empty_like(x1)
+    with pytest.raises(fm.FlintMoEError) as ei:
+        fm.flint_moe_forward(x1, layer.router_w, layer.w13, layer.w13_sf, layer.w13_gs, layer.w2,
+                             layer.w2_sf, layer.w2_gs, layer.shared_gu, layer.shared_down, 9999,
+                             out, ws)
+    assert ei.value.code == fm.FLINT_ERR_INVALID_ARG
+    small = ws[: ws.numel() // 2]
+    with pytest.raises(fm.FlintMoEError) as ei:
+        fm.forward_layer(x1, layer, k, workspace=small, out=out)
+    assert ei.value.code == fm.FLINT_ERR_WORKSPACE

@@ -13,10 +13,9 @@
  * vllm.models.flint.model (sigmoid top-k with renormalised weights, ungated
  * shared expert).
  *
- * Plain, slow and sequential: one token at a time, every sum in ascending
- * index order, every intermediate held in the type the pages name.  Compile
- * with -O2 -ffp-contract=off and without fast-math so that each C operator is
- * one IEEE-754 binary32 operation.
+ * Plain, slow and sequential: one token at a time, every intermediate held
+ * in the type the pages name.  Compile with -O2 -ffp-contract=off and without
+ * fast-math so that each C operator is one IEEE-754 operation.
  *
  * Readings taken where the pages are silent (each is listed in the design doc):
  *  R1  router-logit summation order (the pages use a Triton tree sum): 32
@@ -33,6 +32,15 @@
  *  R6  ranking uses the pages' total order on bf16 bit patterns (numeric
  *      order, except that -0 ranks below +0); equal bit patterns go to the
  *      lower expert index.
+ *  R7  "products are accumulated in fp32" fixes the accumulator's type, not
+ *      the order of the additions.  Every expert and shared-expert dot
+ *      product therefore takes the order-independent value: the exact sum of
+ *      the (exact) products, rounded once to the fp32 accumulator.  The sum
+ *      is formed in double; products of <= 13 significant bits summed over
+ *      <= 2^16 terms lose nothing unless the terms span more than ~2^24 in
+ *      magnitude, far below fp32 resolution.  The router logits keep the
+ *      fixed fp32 order of R1 (ids must be reproducible bit for bit), and the
+ *      weighted combine keeps the pages' sequential fp32 loop over j.
  */
 #include <math.h>
 #include <stdint.h>
@@ -209,11 +217,12 @@ static void forward_token(const uint16_t* xrow, const uint16_t* wr, const uint8_
     const uint8_t* s13 = w13_sf + e * (int64_t)(2 * I) * (H / 16);
     float gs13 = w13_gs[e];
     for (int r = 0; r < I; ++r) {
-      float accg = 0.0f, accu = 0.0f;
+      double sg = 0.0, su = 0.0; /* reading R7 */
       for (int h = 0; h < H; ++h) {
-        accg = accg + nvfp4_deq(c13, s13, r, H, h) * xf[h];      /* gate row r   */
-        accu = accu + nvfp4_deq(c13, s13, I + r, H, h) * xf[h];  /* up row I + r */
+        sg += (double)(nvfp4_deq(c13, s13, r, H, h) * xf[h]);      /* gate row r   */
+        su += (double)(nvfp4_deq(c13, s13, I + r, H, h) * xf[h]);  /* up row I + r */
       }
+      float accg = (float)sg, accu = (float)su;
       float g = accg * gs13, u = accu * gs13;  /* global scale on the accumulator */
       act[r] = round_bf16(silu_exact(g) * u);  /* act = bf16(silu(g) * u) */
       if (act_o)
@@ -223,9 +232,10 @@ static void forward_token(const uint16_t* xrow, const uint16_t* wr, const uint8_
     const uint8_t* s2 = w2_sf + e * (int64_t)H * (I / 16);
     float gs2 = w2_gs[e];
     for (int h = 0; h < H; ++h) {
-      float acc = 0.0f;
+      double sum = 0.0;
       for (int i = 0; i < I; ++i)
-        acc = acc + nvfp4_deq(c2, s2, h, I, i) * act[i];
+        sum += (double)(nvfp4_deq(c2, s2, h, I, i) * act[i]);
+      float acc = (float)sum;
       float y = round_bf16(acc * gs2);  /* y_e = bf16(acc * gs_e) */
       if (y_o)
         y_o[(int64_t)j * H + h] = f32_to_bf16(y);
@@ -236,12 +246,12 @@ static void forward_token(const uint16_t* xrow, const uint16_t* wr, const uint8_
   /* shared expert (reading R5) and the final add */
   float* sact = (float*)malloc(sizeof(float) * (size_t)(SI > 0 ? SI : 1));
   for (int r = 0; r < SI; ++r) {
-    float accg = 0.0f, accu = 0.0f;
+    double sg = 0.0, su = 0.0;
     for (int h = 0; h < H; ++h) {
-      accg = accg + bf16_to_f32(sgu[(int64_t)r * H + h]) * xf[h];
-      accu = accu + bf16_to_f32(sgu[(int64_t)(SI + r) * H + h]) * xf[h];
+      sg += (double)(bf16_to_f32(sgu[(int64_t)r * H + h]) * xf[h]);
+      su += (double)(bf16_to_f32(sgu[(int64_t)(SI + r) * H + h]) * xf[h]);
     }
-    float gS = round_bf16(accg), uS = round_bf16(accu);
+    float gS = round_bf16((float)sg), uS = round_bf16((float)su);
     sact[r] = round_bf16(silu_exact(gS) * uS);
     if (sact_o)
       sact_o[r] = f32_to_bf16(sact[r]);
@@ -249,10 +259,10 @@ static void forward_token(const uint16_t* xrow, const uint16_t* wr, const uint8_
   for (int h = 0; h < H; ++h) {
     float ys = 0.0f;
     if (SI > 0) {
-      float acc = 0.0f;
+      double sum = 0.0;
       for (int i = 0; i < SI; ++i)
-        acc = acc + sact[i] * bf16_to_f32(sdown[(int64_t)h * SI + i]);
-      ys = round_bf16(acc);
+        sum += (double)(sact[i] * bf16_to_f32(sdown[(int64_t)h * SI + i]));
+      ys = round_bf16((float)sum);
     }
     if (ys_o)
       ys_o[h] = f32_to_bf16(ys);

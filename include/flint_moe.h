@@ -20,11 +20,12 @@
  *    errors are reported synchronously (negative return, nothing enqueued);
  *    launch failures return FLINT_ERR_CUDA.
  *  - `workspace` is caller-owned device memory of at least
- *    flint_moe_workspace_bytes(shape) bytes, zero-filled ONCE after
- *    allocation (e.g. cudaMemsetAsync).  Every launch leaves its counters at
- *    zero again, so the same workspace serves any number of calls in stream
- *    order (and CUDA-graph replays).  Calls that may overlap on the GPU (two
- *    streams) need separate workspaces.
+ *    flint_moe_workspace_bytes(shape) bytes (256-byte aligned), zero-filled
+ *    ONCE after allocation (e.g. cudaMemsetAsync).  Every launch leaves its
+ *    counters at zero again, so the same workspace serves any number of calls
+ *    in stream order (and CUDA-graph replays) with the same H, E, I and SI
+ *    and any M up to the one it was sized for.  Calls that may overlap on the
+ *    GPU (two streams) need separate workspaces.
  */
 #ifndef FLINT_MOE_H_
 #define FLINT_MOE_H_
@@ -104,8 +105,10 @@ int flint_moe_route(const void* x, const void* router_w, const flint_moe_shape* 
  * act = bf16(silu(g) * u) with sigmoid = rcp.approx(1 + ex2.approx(-g log2 e));
  * y_e = bf16(acc * gs2_e); shared expert gS, uS = bf16(dot),
  * sact = bf16(silu(gS) * uS), ys = bf16(dot); out = bf16(bf16(sum_j tw_j y_j) + ys).
- * Precondition: |x| < 2^120 (activations are multiplied by weights scaled by
- * 2^-7 internally; far beyond any fp32-representable product range). */
+ * The kernels multiply activations by weights scaled by 2^-7 (exactly) and
+ * scale the fp32 accumulator back by 2^7, so single products below 2^-119 in
+ * magnitude are formed as fp32 subnormals; no sum of realistic size resolves
+ * them. */
 int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13,
                       const uint8_t* w13_sf, const float* w13_gs, const uint8_t* w2,
                       const uint8_t* w2_sf, const float* w2_gs, const void* shared_gu,

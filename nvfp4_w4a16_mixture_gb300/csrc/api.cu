@@ -34,9 +34,10 @@ WsLayout ws_layout(const flint_moe_shape& s) {
     return o;
   };
   L.status = take(16);
-  L.tok_cnt = take(4 * ((M + kRouteTokens - 1) / kRouteTokens));
   L.glob_cnt = take(16);
   L.hblk_cnt = take(4 * (H / 16));
+  L.mk_ctr = take(decode_mk_ctr_bytes(s));
+  L.tok_cnt = take(4 * ((M + kRouteTokens - 1) / kRouteTokens));
   L.logits = take(2 * M * E);
   L.ids = take(4 * np);
   L.tw = take(4 * np);
@@ -50,6 +51,7 @@ WsLayout ws_layout(const flint_moe_shape& s) {
   L.sact = take(2 * M * (SI > 0 ? SI : 1));
   L.y = take(2 * np * H);
   L.ys = take(2 * M * H);
+  L.mk_part = take(decode_mk_supported(s) ? decode_mk_part_bytes(s) : 16);
   L.total = off;
   return L;
 }
@@ -74,6 +76,8 @@ Ws ws_pointers(void* base, const WsLayout& L) {
   w.sact = reinterpret_cast<uint16_t*>(b + L.sact);
   w.y = reinterpret_cast<uint16_t*>(b + L.y);
   w.ys = reinterpret_cast<uint16_t*>(b + L.ys);
+  w.mk_ctr = reinterpret_cast<int*>(b + L.mk_ctr);
+  w.mk_part = reinterpret_cast<float*>(b + L.mk_part);
   return w;
 }
 
@@ -146,6 +150,10 @@ int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13, c
   a.ws = ws_pointers(workspace, L);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
+  if (decode_mk_supported(*shape)) {
+    if (launch_decode_mk(a, a.ws.mk_ctr, a.ws.mk_part, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
+    return FLINT_OK;
+  }
   if (launch_route(a, true, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
   if (launch_decode_gate_up(a, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
   if (launch_decode_down(a, st, true) != cudaSuccess) return FLINT_ERR_CUDA;

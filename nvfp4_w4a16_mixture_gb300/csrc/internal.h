@@ -13,14 +13,18 @@ constexpr int kMaxE = 256;
 constexpr int kMaxTopK = 32;
 constexpr int kDecodeMaxTokens = 64;  // M above this uses the grouped path
 
-// Offsets (bytes from the workspace base) of every workspace region.  All
-// regions are 256-byte aligned.  Counters and the status word live in the
-// first region; every launch returns its counters to zero.
+// Offsets (bytes from the workspace base) of every workspace region, all
+// 256-byte aligned.  The control block comes first: the status word and every
+// counter, at offsets that depend only on (H, E, SI), with the per-token-block
+// router counters last, so that a workspace sized for M serves any call with
+// the same (H, E, I, SI) and a smaller M.  Every launch returns its counters
+// to zero.  The data regions after it need no initial value.
 struct WsLayout {
-  size_t status;       // int32[1]: first error recorded by a kernel
-  size_t tok_cnt;      // int32[ceil(M / kRouteTokens)]: router last-arriver counters
+  size_t status;       // int32[4]: [0] first error recorded by a kernel
   size_t glob_cnt;     // int32[4]: global last-arriver counters
   size_t hblk_cnt;     // int32[H / 16]: down/combine last-arriver counters
+  size_t mk_ctr;       // decode megakernel counters
+  size_t tok_cnt;      // int32[ceil(M / kRouteTokens)]: router last-arriver counters
   size_t logits;       // bf16 [M, E]
   size_t ids;          // int32 [M, k]
   size_t tw;           // fp32 [M, k]
@@ -34,6 +38,7 @@ struct WsLayout {
   size_t sact;         // bf16 [M, SI]
   size_t y;            // bf16 [M * k, H]   row = sorted position of the pair
   size_t ys;           // bf16 [M, H]
+  size_t mk_part;      // decode megakernel fp32 partial sums
   size_t total;
 };
 
@@ -46,6 +51,7 @@ struct Ws {  // device pointers into one workspace
   int* tok_cnt;
   int* glob_cnt;
   int* hblk_cnt;
+  int* mk_ctr;
   uint16_t* logits;
   int* ids;
   float* tw;
@@ -59,6 +65,7 @@ struct Ws {  // device pointers into one workspace
   uint16_t* sact;
   uint16_t* y;
   uint16_t* ys;
+  float* mk_part;
 };
 
 Ws ws_pointers(void* base, const WsLayout& L);
@@ -86,5 +93,12 @@ struct MoEArgs {
 cudaError_t launch_route(const MoEArgs& a, bool build_meta, cudaStream_t st, bool pdl);
 cudaError_t launch_decode_gate_up(const MoEArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_decode_down(const MoEArgs& a, cudaStream_t st, bool pdl);
+
+// Decode megakernel (whole block in one persistent launch, M <= kDecodeMaxTokens).
+bool decode_mk_supported(const flint_moe_shape& s);
+size_t decode_mk_ctr_bytes(const flint_moe_shape& s);
+size_t decode_mk_part_bytes(const flint_moe_shape& s);
+cudaError_t launch_decode_mk(const MoEArgs& a, int* mk_ctr, float* mk_part, cudaStream_t st,
+                             bool pdl);
 
 }  // namespace flint

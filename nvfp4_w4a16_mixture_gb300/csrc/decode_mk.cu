@@ -5,31 +5,33 @@
 // (router GEMV, top-k by the token's last program), _gate_up_gemv_kernel
 // (per (token, expert) NVFP4 gate/up + SiLU * up) and _down_gemv_kernel
 // (down GEMV over the top-k experts, weighted combine, shared-expert add),
-// with the shared expert on an auxiliary stream.  Here the same steps run as
+// with the shared expert on an auxiliary stream.  Here the same steps are
 // work tiles of one kernel, chained by device-side counters, so the weight
-// stream never drains between steps:
+// stream never drains between steps.  Tile order (every tile depends only on
+// tiles of lower index):
 //
-//   phase 1 (static, no dependencies; weights staged before the PDL wait)
-//     ROUTER  one router row: logits of all tokens in a fixed fp32 order; the
-//             last router tile runs top-k + expert grouping, then raises the
-//             routing flag
+//   static (round robin over CTAs; weights staged before the PDL wait)
+//     ROUTER  router row e: logits of every token, fixed fp32 order
 //     SGU     shared expert gate/up: 8 intermediate rows (gate + up), a K part
-//   phase 2 (dynamic, atomic work counter, decoded after the routing flag)
-//     RGU     routed expert gate/up: expert u, 8 intermediate rows, all K
-//     SDN     shared expert down: 16 output rows, a K part  (after all SGU)
-//     RDN     routed expert down: expert u, 16 output rows  (after u's RGU)
-//   the last tile of each 16-row output block forms
-//     out = bf16(bf16(sum_j tw_j y_j) + ys) for every token.
+//             -> fp32 partial sums
+//     TOPK    top-k + sigmoid renormalisation + expert grouping -> routing flag
+//   dynamic (atomic work counter, decoded once the routing flag is up)
+//     RGU     routed expert u: 8 intermediate rows, all K -> act
+//     SFIN    64 shared intermediate rows: sact = bf16(silu(gS) * uS)
+//     SDN     shared expert down: 16 output rows, a K part -> fp32 partials
+//     RDN     routed expert u: 16 output rows -> y
+//     COMBINE 128 output rows: out = bf16(bf16(sum_j tw_j y_j) + ys)
 //
 // CTA: 8 consumer warps + 1 producer warp.  The producer copies each tile's
 // weight rows (NVFP4 codes + E4M3 scales, or BF16 rows) into a 3-stage
-// shared-memory ring with cp.async.bulk (mbarrier completion), running ahead
-// of the consumers; a tile's dependency wait happens after its weights have
-// landed.  Consumers split K across warps (128-wide slices), run mma.sync
-// m16n8k16 (bf16, fp32 accumulate) with the weight rows as A and up to 8
-// tokens per B tile, reduce in shared memory in warp order, and apply the
-// tile's epilogue.  Deadlock freedom: every wait targets tiles of lower index,
-// tiles are taken in index order and all counters are bounded waits.
+// shared-memory ring with cp.async.bulk and stages x once; a tile's
+// dependency wait happens after its weights have landed.  Consumer warps run
+// independently: inside a tile, warp w takes n-tile (w mod nn) and every
+// (8 / nn)-th 128-wide K slice, multiplies on the tensor cores (mma.sync
+// m16n8k16, bf16 operands, fp32 accumulate) and leaves its partial in shared
+// memory; the last warp to finish (shared counter) sums the partials in
+// fixed warp order and applies the epilogue.  Completion is signalled with
+// release adds; every wait is bounded (status FLINT_ERR_TIMEOUT on expiry).
 #include "common.cuh"
 #include "internal.h"
 
@@ -37,145 +39,181 @@ namespace flint {
 
 namespace {
 
-constexpr int kCW = 8;                       // consumer warps
-constexpr int kThreads = (kCW + 1) * 32;     // + producer warp
+constexpr int kCW = 8;                    // consumer warps
+constexpr int kThreads = (kCW + 1) * 32;  // + producer warp
 constexpr int kStages = 3;
 constexpr int kStageBytes = 32 * 1024;
-constexpr int kNTP = 4;                      // 8-token n-tiles per pass
+constexpr int kXsBytes = 64 * 1024;       // staged x (M * H * 2 <= this)
 constexpr int kSliceK = 128;
-constexpr int kBarConsumers = 1;             // named barrier id
-constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s bound on any wait
+constexpr int kSfinRows = 64;             // shared intermediate rows per SFIN tile
+constexpr int kCombineBlocks = 8;         // 16-row output blocks per COMBINE tile
+constexpr unsigned long long kWaitNs = 2000000000ull;
 
-enum : int { T_END = 0, T_ROUTER = 1, T_SGU = 2, T_RGU = 3, T_SDN = 4, T_RDN = 5 };
+enum : int { T_END = 0, T_ROUTER, T_SGU, T_TOPK, T_RGU, T_SFIN, T_SDN, T_RDN, T_COMBINE };
+
+// counters (int32, workspace control block)
+enum : int { C_WORK = 0, C_ROUTER = 1, C_ROUTED = 2, C_SGU = 3, C_SFIN = 4, C_EXIT = 5, C_N = 8 };
 
 struct Tile {
   int type;
-  int u, e;        // unique-expert slot and expert id (routed tiles)
-  int row0;        // first intermediate row (gate/up) or output row (down)
-  int part;        // K part (shared tiles)
-  int s0, ns;      // first K slice and slice count of this tile
+  int u, e;   // unique-expert slot, expert id (routed tiles)
+  int row0;   // first intermediate / output row
+  int part;   // K part (shared tiles)
+  int s0, ns; // first K slice and slice count
 };
 
 struct Smem {
   uint8_t stage[kStages][kStageBytes];
-  float red[kCW][kNTP][32][4];
+  uint8_t xs[kXsBytes];
+  float red[kStages][kCW][32][4];
   Tile info[kStages];
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  int flag;
-  int stop;
+  uint64_t xbar;
+  int arr[kStages];
+  int exit_arr;
   int cnt[kMaxE];
   int base[kMaxE];
 };
 
-FLINT_DEV unsigned long long now_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
+struct Geo {
+  int nsl_H, nsl_I, nsl_SI;  // K slices of 128
+  int P_sg, spp_sg;          // shared gate/up: K parts, slices per part
+  int P_sd, spp_sd;          // shared down: K parts, slices per part
+  int NSG, N1;               // shared gate/up tiles, static tiles
+  int NSF, NCB;              // SFIN and COMBINE tiles
+  int xs;                    // x staged in shared memory
+};
 
-// Bounded wait until *p >= target.  On timeout records FLINT_ERR_TIMEOUT in
-// the status word; returns immediately once any error is recorded.
+}  // namespace
+
+struct MkArgs {
+  MoEArgs a;
+  Geo G;
+  int* ctr;        // [C_N]
+  int* gu_done;    // [E]   RGU tiles done per routed-expert slot
+  int* down_cnt;   // [H/16] SDN parts + RDN tiles done per output block
+  float* part_sg;  // [SI/8][P_sg][16][64]
+  float* part_sd;  // [H/16][P_sd][16][64]
+};
+
+namespace {
+
+// Bounded wait (one lane) until *p >= target.
 FLINT_DEV bool wait_ge(const int* p, int target, int* status) {
-  const unsigned long long t0 = now_ns();
+  const unsigned long long t0 = globaltimer_ns();
   for (int i = 0;; ++i) {
     if (ld_acquire(p) >= target) return true;
-    if (i >= 32) {
+    if (i >= 16) {
       if (ld_acquire(status) != 0) return false;
-      if (now_ns() - t0 > kWaitNs) {
+      if (globaltimer_ns() - t0 > kWaitNs) {
         atomicCAS(status, 0, FLINT_ERR_TIMEOUT);
         return false;
       }
-      __nanosleep(64);
+      __nanosleep(32);
     }
   }
 }
 
+// Warp-uniform bounded wait (lane 0 polls).
+FLINT_DEV bool warp_wait_ge(const int* p, int target, int* status, int lane) {
+  int ok = 1;
+  if (lane == 0) ok = wait_ge(p, target, status);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
 FLINT_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = now_ns();
+  const unsigned long long t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (now_ns() - t0 > kWaitNs) {
+    if (globaltimer_ns() - t0 > kWaitNs) {
       atomicCAS(status, 0, FLINT_ERR_TIMEOUT);
       return false;
     }
   }
 }
 
-FLINT_DEV void cbar() { named_bar(kBarConsumers, kCW * 32); }
-
-// -------------------------------------------------------------- geometry
-struct Geo {
-  int nsl_H, nsl_I, nsl_SI;  // K slices of 128
-  int P_sg, spp_sg;          // shared gate/up: K parts, slices per part
-  int P_sd, spp_sd;          // shared down: K parts, slices per part
-  int NR, NSG, N1;           // router tiles, shared gate/up tiles, phase-1 total
-};
-
+// ------------------------------------------------------------ tile list
 FLINT_DEV Tile static_tile(const MoEArgs& a, const Geo& G, int idx) {
   Tile t{};
-  if (idx < G.NR) {
+  if (idx < a.E) {
     t.type = T_ROUTER;
     t.e = idx;
-    return t;
+  } else if (idx < a.E + G.NSG) {
+    const int d = idx - a.E;
+    t.type = T_SGU;
+    t.row0 = (d / G.P_sg) * 8;
+    t.part = d % G.P_sg;
+    t.s0 = t.part * G.spp_sg;
+    t.ns = min(G.spp_sg, G.nsl_H - t.s0);
+  } else {
+    t.type = T_TOPK;
   }
-  const int d = idx - G.NR;
-  t.type = T_SGU;
-  t.row0 = (d / G.P_sg) * 8;
-  t.part = d % G.P_sg;
-  t.s0 = t.part * G.spp_sg;
-  t.ns = min(G.spp_sg, G.nsl_H - t.s0);
   return t;
 }
 
 FLINT_DEV Tile dynamic_tile(const MoEArgs& a, const Geo& G, int d, int U) {
   Tile t{};
   const int nrg = U * (a.I / 8);
+  const int nsf = G.NSF;
   const int nsd = a.SI > 0 ? (a.H / 16) * G.P_sd : 0;
   const int nrd = U * (a.H / 16);
+  const int ncb = G.NCB;
   if (d < nrg) {
     t.type = T_RGU;
     t.u = d / (a.I / 8);
     t.row0 = (d % (a.I / 8)) * 8;
-    t.s0 = 0;
     t.ns = G.nsl_H;
-  } else if (d < nrg + nsd) {
-    const int dd = d - nrg;
+    return t;
+  }
+  d -= nrg;
+  if (d < nsf) {
+    t.type = T_SFIN;
+    t.row0 = d * kSfinRows;
+    return t;
+  }
+  d -= nsf;
+  if (d < nsd) {
     t.type = T_SDN;
-    t.row0 = (dd / G.P_sd) * 16;
-    t.part = dd % G.P_sd;
+    t.row0 = (d / G.P_sd) * 16;
+    t.part = d % G.P_sd;
     t.s0 = t.part * G.spp_sd;
     t.ns = min(G.spp_sd, G.nsl_SI - t.s0);
-  } else if (d < nrg + nsd + nrd) {
-    const int dd = d - nrg - nsd;
-    t.type = T_RDN;
-    t.u = dd / (a.H / 16);
-    t.row0 = (dd % (a.H / 16)) * 16;
-    t.s0 = 0;
-    t.ns = G.nsl_I;
-  } else {
-    t.type = T_END;
+    return t;
   }
+  d -= nsd;
+  if (d < nrd) {
+    t.type = T_RDN;
+    t.u = d / (a.H / 16);
+    t.row0 = (d % (a.H / 16)) * 16;
+    t.ns = G.nsl_I;
+    return t;
+  }
+  d -= nrd;
+  if (d < ncb) {
+    t.type = T_COMBINE;
+    t.row0 = d * kCombineBlocks * 16;
+    return t;
+  }
+  t.type = T_END;
   return t;
 }
 
-// Issue the bulk copies of a tile's weights into stage `buf`; returns bytes.
-FLINT_DEV uint32_t issue_tile(const MoEArgs& a, const Geo& G, const Tile& t, uint8_t* buf,
-                              uint64_t* bar) {
+// Bulk copies of a tile's weights into a stage; completion on `bar`.
+FLINT_DEV void issue_tile(const MoEArgs& a, const Geo& G, const Tile& t, uint8_t* buf,
+                          uint64_t* bar) {
   const int H = a.H, I = a.I, SI = a.SI;
-  uint32_t bytes = 0;
   switch (t.type) {
-    case T_ROUTER: {
-      bytes = H * 2;
-      mbar_arrive_expect_tx(bar, bytes);
-      bulk_g2s(buf, a.router_w + (size_t)t.e * H, bytes, bar);
+    case T_ROUTER:
+      mbar_arrive_expect_tx(bar, H * 2);
+      bulk_g2s(buf, a.router_w + (size_t)t.e * H, H * 2, bar);
       break;
-    }
     case T_SGU: {
-      const int pk = t.ns * kSliceK;  // K elements in this part
-      bytes = 16 * pk * 2;
-      mbar_arrive_expect_tx(bar, bytes);
+      const int pk = t.ns * kSliceK;
+      mbar_arrive_expect_tx(bar, 16 * pk * 2);
       if (G.P_sg == 1) {
         bulk_g2s(buf, a.shared_gu + (size_t)t.row0 * H, 8 * H * 2, bar);
         bulk_g2s(buf + 8 * H * 2, a.shared_gu + (size_t)(SI + t.row0) * H, 8 * H * 2, bar);
@@ -189,8 +227,7 @@ FLINT_DEV uint32_t issue_tile(const MoEArgs& a, const Geo& G, const Tile& t, uin
     }
     case T_RGU: {
       const size_t rg = (size_t)t.e * 2 * I + t.row0, ru = rg + I;
-      bytes = 16 * (H / 2) + 16 * (H / 16);
-      mbar_arrive_expect_tx(bar, bytes);
+      mbar_arrive_expect_tx(bar, 16 * (H / 2) + 16 * (H / 16));
       bulk_g2s(buf, a.w13 + rg * (H / 2), 8 * (H / 2), bar);
       bulk_g2s(buf + 8 * (H / 2), a.w13 + ru * (H / 2), 8 * (H / 2), bar);
       bulk_g2s(buf + 16 * (H / 2), a.w13_sf + rg * (H / 16), 8 * (H / 16), bar);
@@ -199,8 +236,7 @@ FLINT_DEV uint32_t issue_tile(const MoEArgs& a, const Geo& G, const Tile& t, uin
     }
     case T_SDN: {
       const int pk = t.ns * kSliceK;
-      bytes = 16 * pk * 2;
-      mbar_arrive_expect_tx(bar, bytes);
+      mbar_arrive_expect_tx(bar, 16 * pk * 2);
       if (G.P_sd == 1) {
         bulk_g2s(buf, a.shared_down + (size_t)t.row0 * SI, 16 * SI * 2, bar);
       } else {
@@ -212,21 +248,17 @@ FLINT_DEV uint32_t issue_tile(const MoEArgs& a, const Geo& G, const Tile& t, uin
     }
     case T_RDN: {
       const size_t r = (size_t)t.e * H + t.row0;
-      bytes = 16 * (I / 2) + 16 * (I / 16);
-      mbar_arrive_expect_tx(bar, bytes);
+      mbar_arrive_expect_tx(bar, 16 * (I / 2) + 16 * (I / 16));
       bulk_g2s(buf, a.w2 + r * (I / 2), 16 * (I / 2), bar);
       bulk_g2s(buf + 16 * (I / 2), a.w2_sf + r * (I / 16), 16 * (I / 16), bar);
       break;
     }
     default:
-      mbar_arrive(bar);
+      mbar_arrive(bar);  // tiles without weights
   }
-  return bytes;
 }
 
-// ---------------------------------------------------------------- compute
-// NVFP4 rows: cg / cg8 point at the codes of tile rows g and g + 8 (row
-// stride irrelevant here), sg / sg8 at their scales; slice s of the tile.
+// ------------------------------------------------------------ A operand
 FLINT_DEV void a_frags_fp4(const uint8_t* cg, const uint8_t* cg8, const uint8_t* sg,
                            const uint8_t* sg8, int s, int t, uint32_t (&af)[4][2][4]) {
   const uint4 c0 = *reinterpret_cast<const uint4*>(cg + s * (kSliceK / 2) + 16 * t);
@@ -251,7 +283,6 @@ FLINT_DEV void a_frags_fp4(const uint8_t* cg, const uint8_t* cg8, const uint8_t*
   }
 }
 
-// BF16 rows: rg / rg8 point at K element 0 of tile rows g and g + 8.
 FLINT_DEV void a_frags_bf16(const uint16_t* rg, const uint16_t* rg8, int s, int t,
                             uint32_t (&af)[4][2][4]) {
 #pragma unroll
@@ -269,50 +300,31 @@ FLINT_DEV void a_frags_bf16(const uint16_t* rg, const uint16_t* rg8, int s, int 
   }
 }
 
-// acc[nt] += A(slice) * B(rows brow[nt], K offset koff of the activation row)
-FLINT_DEV void mma_tiles(float (&acc)[kNTP][4], const uint32_t (&af)[4][2][4],
-                         const uint16_t* const (&brow)[kNTP], int koff, int t, int ntiles) {
+// 32 activations (16-bit) of one row at K offset koff + 32 t: smem or global.
+FLINT_DEV void load_b(uint4 (&xb)[4], const uint16_t* row, bool smem, int koff, int t) {
 #pragma unroll
-  for (int nt = 0; nt < kNTP; ++nt) {
-    if (nt >= ntiles) break;
-    uint4 xb[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      xb[q] = brow[nt] ? ldg_cg_v4(brow[nt] + koff + 32 * t + 8 * q) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      mma_bf16_16816(acc[nt], af[q][0][0], af[q][0][1], af[q][0][2], af[q][0][3],
-                     __byte_perm(xb[q].x, xb[q].z, 0x5410), __byte_perm(xb[q].x, xb[q].z, 0x7632));
-      mma_bf16_16816(acc[nt], af[q][1][0], af[q][1][1], af[q][1][2], af[q][1][3],
-                     __byte_perm(xb[q].y, xb[q].w, 0x5410), __byte_perm(xb[q].y, xb[q].w, 0x7632));
+  for (int q = 0; q < 4; ++q) {
+    if (!row) {
+      xb[q] = make_uint4(0, 0, 0, 0);
+    } else if (smem) {
+      xb[q] = *reinterpret_cast<const uint4*>(row + koff + 32 * t + 8 * q);
+    } else {
+      xb[q] = ldg_cg_v4(row + koff + 32 * t + 8 * q);
     }
   }
 }
 
-FLINT_DEV void zero_acc(float (&acc)[kNTP][4]) {
+FLINT_DEV void mma_slice(float (&acc)[4], const uint32_t (&af)[4][2][4], const uint4 (&xb)[4]) {
 #pragma unroll
-  for (int nt = 0; nt < kNTP; ++nt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+  for (int q = 0; q < 4; ++q) {
+    mma_bf16_16816(acc, af[q][0][0], af[q][0][1], af[q][0][2], af[q][0][3],
+                   __byte_perm(xb[q].x, xb[q].z, 0x5410), __byte_perm(xb[q].x, xb[q].z, 0x7632));
+    mma_bf16_16816(acc, af[q][1][0], af[q][1][1], af[q][1][2], af[q][1][3],
+                   __byte_perm(xb[q].y, xb[q].w, 0x5410), __byte_perm(xb[q].y, xb[q].w, 0x7632));
+  }
 }
 
-FLINT_DEV void store_red(Smem& S, const float (&acc)[kNTP][4], int cw, int lane) {
-#pragma unroll
-  for (int nt = 0; nt < kNTP; ++nt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) S.red[cw][nt][lane][i] = acc[nt][i];
-}
-
-FLINT_DEV float red_sum(const Smem& S, int nt, int lane, int i) {
-  float v = S.red[0][nt][lane][i];
-#pragma unroll
-  for (int w = 1; w < kCW; ++w) v += S.red[w][nt][lane][i];
-  return v;
-}
-
-// --------------------------------------------------------- routing step
-// Top-k of one token by one warp (keys: order-preserving bf16 bits << 8 |
-// (E - 1 - e)); writes ids / tw (workspace and optional user copies).
+// ----------------------------------------------------------- routing
 FLINT_DEV void topk_token(const MoEArgs& a, int t, int lane) {
   const int E = a.E, k = a.k;
   int key[kMaxE / 32];
@@ -338,7 +350,7 @@ FLINT_DEV void topk_token(const MoEArgs& a, int t, int lane) {
     const uint32_t o = (uint32_t)best >> 8;
     const uint32_t b16 = (o & 0x8000u) ? (o ^ 0x8000u) : (o ^ 0xFFFFu);
     const float s = __fdiv_rn(1.0f, 1.0f + expf(-bf16_bits_to_f32(b16)));
-    sum = sum + s;
+    sum = sum + s;  // rank order
     if (lane == j) { my_s = s; my_e = E - 1 - (best & 0xFF); }
   }
   if (lane < k) {
@@ -350,8 +362,8 @@ FLINT_DEV void topk_token(const MoEArgs& a, int t, int lane) {
   }
 }
 
-// Expert grouping of the M*k pairs by one warp: counts, offsets, the list of
-// routed experts, and the pairs stable-sorted by expert (rowof = inverse).
+// Expert grouping of the M*k pairs (one warp): counts, offsets, routed
+// experts, pairs stable-sorted by expert and the inverse map.
 FLINT_DEV void group_pairs(const MoEArgs& a, Smem& S, int lane) {
   const int E = a.E, np = a.M * a.k;
   for (int e = lane; e < E; e += 32) S.cnt[e] = 0;
@@ -395,38 +407,26 @@ FLINT_DEV void group_pairs(const MoEArgs& a, Smem& S, int lane) {
   }
 }
 
-// out for the 16 output rows of block hb, all tokens (consumer threads).
-FLINT_DEV void combine_block(const MoEArgs& a, int hb, int ctid) {
-  const int H = a.H, k = a.k, h0 = hb * 16;
-  for (int idx = ctid; idx < a.M * 16; idx += kCW * 32) {
-    const int tt = idx >> 4, h = h0 + (idx & 15);
-    float R = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      const int p = tt * k + j;
-      const float w = ldg_cg_f32(a.ws.tw + p);
-      const int row = ldg_cg_i32(a.ws.rowof + p);
-      R = R + w * bf16_bits_to_f32(ldg_cg_u16(a.ws.y + (size_t)row * H + h));  // rank order
+// Warp-level arrival at a tile: true for the last of the 8 warps.
+FLINT_DEV bool tile_arrive(Smem& S, int st, int lane) {
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) {
+    __threadfence();  // this warp's global and shared writes before the count
+    last = (atomicAdd(&S.arr[st], 1) == kCW - 1);
+    if (last) {
+      S.arr[st] = 0;
+      __threadfence();
     }
-    const float ys = a.SI > 0 ? bf16_bits_to_f32(ldg_cg_u16(a.ws.ys + (size_t)tt * H + h)) : 0.0f;
-    a.out[(size_t)tt * H + h] = (uint16_t)f32_to_bf16_bits(round_bf16(R) + ys);
   }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  __syncwarp();
+  return last != 0;
 }
 
 }  // namespace
 
-struct MkArgs {
-  MoEArgs a;
-  Geo G;
-  int* ctr;       // [0] work, [1] router tiles done, [2] routing flag, [3] shared gate/up
-                  // tiles done, [4] CTAs exited
-  int* sg_cnt;    // [SI/8]   K parts done per shared gate/up tile
-  int* sd_cnt;    // [H/16]   K parts done per shared down tile
-  int* gu_done;   // [E]      gate/up tiles done per routed-expert slot
-  int* down_cnt;  // [H/16]   down tiles done per output block
-  float* part_sg; // [SI/8][P_sg][16][64]
-  float* part_sd; // [H/16][P_sd][16][64]
-};
-
+// ======================================================================
 __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(MkArgs A) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
@@ -435,48 +435,62 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(MkArgs A) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   int* status = a.ws.status;
+  const int H = a.H, I = a.I, SI = a.SI, E = a.E, k = a.k, M = a.M;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], 1);
+      S.arr[s] = 0;
     }
+    mbar_init(&S.xbar, 1);
+    S.exit_arr = 0;
     fence_mbar_init();
-    S.stop = 0;
   }
   __syncthreads();
 
   // ======================================================= producer warp
   if (warp == kCW) {
     if (lane != 0) return;
-    int n = 0;  // tiles staged so far
+    int n = 0;
     bool ok = true;
-    auto put = [&](const Tile& tl) {
-      const int st = n % kStages;
+    auto slot = [&](int& st) {
+      st = n % kStages;
       if (n >= kStages && !mbar_wait(&S.empty[st], ((n / kStages) - 1) & 1, status)) ok = false;
-      S.info[st] = tl;
-      issue_tile(a, G, tl, S.stage[st], &S.full[st]);
-      ++n;
+      return ok;
     };
     int idx = blockIdx.x;
     // weights of the first static tiles do not depend on earlier grids
-    for (; idx < G.N1 && n < kStages; idx += gridDim.x) put(static_tile(a, G, idx));
+    for (; idx < G.N1 && n < kStages; idx += gridDim.x, ++n) {
+      const Tile tl = static_tile(a, G, idx);
+      S.info[n] = tl;
+      if (tl.type != T_TOPK) issue_tile(a, G, tl, S.stage[n], &S.full[n]);
+    }
     pdl_wait();
-    for (; idx < G.N1; idx += gridDim.x) put(static_tile(a, G, idx));
+    for (int i = 0; i < n; ++i)  // a TOPK tile reads the workspace: release it after the wait
+      if (S.info[i].type == T_TOPK) mbar_arrive(&S.full[i]);
+    if (G.xs) {
+      mbar_arrive_expect_tx(&S.xbar, M * H * 2);
+      bulk_g2s(S.xs, a.x, M * H * 2, &S.xbar);
+    }
+    for (; idx < G.N1; idx += gridDim.x) {
+      int st;
+      if (!slot(st)) break;
+      const Tile tl = static_tile(a, G, idx);
+      S.info[st] = tl;
+      issue_tile(a, G, tl, S.stage[st], &S.full[st]);
+      ++n;
+    }
     int U = -1;
     for (;;) {
-      const int st = n % kStages;
-      if (!ok || (n >= kStages && !mbar_wait(&S.empty[st], ((n / kStages) - 1) & 1, status))) {
-        // a bounded wait gave up (error recorded): tell the consumers to stop
+      int st;
+      if (!slot(st)) {
         S.info[st].type = T_END;
         mbar_arrive(&S.full[st]);
         break;
       }
-      const int d = atomicAdd(&A.ctr[0], 1);
-      if (U < 0) {
-        U = 0;
-        if (wait_ge(&A.ctr[2], 1, status)) U = ldg_cg_i32(a.ws.uniq);
-      }
+      const int d = atomicAdd(&A.ctr[C_WORK], 1);
+      if (U < 0) U = wait_ge(&A.ctr[C_ROUTED], 1, status) ? ldg_cg_i32(a.ws.uniq) : 0;
       Tile tl = dynamic_tile(a, G, d, U);
       if (tl.type == T_RGU || tl.type == T_RDN) tl.e = ldg_cg_i32(a.ws.uniq + 1 + tl.u);
       S.info[st] = tl;
@@ -488,31 +502,33 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(MkArgs A) {
   }
 
   // ==================================================== consumer warps
-  const int cw = warp, ctid = threadIdx.x;
+  const int cw = warp;
   pdl_wait();
   pdl_launch_dependents();
-  const int H = a.H, I = a.I, SI = a.SI, E = a.E, k = a.k, M = a.M;
+  bool xs_ok = true;
+  if (G.xs) xs_ok = __all_sync(0xffffffffu, mbar_wait(&S.xbar, 0, status));
 
-  for (int n = 0;; ++n) {
+  for (int n = 0; xs_ok; ++n) {
     const int st = n % kStages;
-    // every consumer thread waits; the stop decision is made uniform
-    if (!mbar_wait(&S.full[st], (n / kStages) & 1, status)) S.stop = 1;
-    cbar();
-    if (S.stop) break;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&S.full[st], (n / kStages) & 1, status));
+    if (!ok) break;
     const Tile tl = S.info[st];
     if (tl.type == T_END) break;
     const uint8_t* buf = S.stage[st];
 
+    // ---------------------------------------------------------- ROUTER
     if (tl.type == T_ROUTER) {
-      // logits[t, e] for every token; lane l owns h = 256 c + 8 l (c = 0..)
+      // logits[t, e]: lane l owns h = 256 c + 8 l, partial over (c, i)
+      // ascending with fmaf, then the xor butterfly 16, 8, 4, 2, 1
       const uint16_t* w = reinterpret_cast<const uint16_t*>(buf);
       for (int tok = cw; tok < M; tok += kCW) {
-        const uint16_t* xr = a.x + (size_t)tok * H;
+        const uint16_t* xr = G.xs ? reinterpret_cast<const uint16_t*>(S.xs) + (size_t)tok * H
+                                  : a.x + (size_t)tok * H;
         float acc = 0.0f;
         for (int c = 0; 256 * c < H; ++c) {
           const int h = 256 * c + 8 * lane;
           if (h < H) {
-            const uint4 xv = ldg_cg_v4(xr + h);
+            const uint4 xv = G.xs ? *reinterpret_cast<const uint4*>(xr + h) : ldg_cg_v4(xr + h);
             const uint4 wv = *reinterpret_cast<const uint4*>(w + h);
             const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
             const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
@@ -527,234 +543,262 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(MkArgs A) {
         for (int o = 16; o >= 1; o >>= 1) acc = acc + __shfl_xor_sync(0xffffffffu, acc, o);
         if (lane == 0) a.ws.logits[(size_t)tok * E + tl.e] = (uint16_t)f32_to_bf16_bits(acc);
       }
-      cbar();
-      if (ctid == 0) {
+      if (tile_arrive(S, st, lane) && lane == 0) {
+        red_release_add(&A.ctr[C_ROUTER], 1);
         mbar_arrive(&S.empty[st]);
-        __threadfence();
-        S.flag = (atomicAdd(&A.ctr[1], 1) == E - 1);
       }
-      cbar();
-      if (S.flag) {
-        __threadfence();
+      continue;
+    }
+
+    // ------------------------------------------------------------ TOPK
+    if (tl.type == T_TOPK) {
+      if (warp_wait_ge(&A.ctr[C_ROUTER], E, status, lane))
         for (int tok = cw; tok < M; tok += kCW) topk_token(a, tok, lane);
-        __threadfence();
-        cbar();
-        if (cw == 0) group_pairs(a, S, lane);
-        __threadfence();
-        cbar();
-        if (ctid == 0) st_release(&A.ctr[2], 1);
-      }
-      continue;
-    }
-
-    // ---- MMA tiles: geometry of A rows g / g + 8 in the stage
-    const bool fp4 = (tl.type == T_RGU || tl.type == T_RDN);
-    const uint8_t *cg = nullptr, *cg8 = nullptr, *sg = nullptr, *sg8 = nullptr;
-    const uint16_t *rg = nullptr, *rg8 = nullptr;
-    if (tl.type == T_RGU) {
-      cg = buf + g * (H / 2);
-      cg8 = buf + (8 + g) * (H / 2);
-      sg = buf + 16 * (H / 2) + g * (H / 16);
-      sg8 = buf + 16 * (H / 2) + (8 + g) * (H / 16);
-    } else if (tl.type == T_RDN) {
-      cg = buf + g * (I / 2);
-      cg8 = buf + (8 + g) * (I / 2);
-      sg = buf + 16 * (I / 2) + g * (I / 16);
-      sg8 = buf + 16 * (I / 2) + (8 + g) * (I / 16);
-    } else {
-      const int pk = tl.ns * kSliceK;
-      rg = reinterpret_cast<const uint16_t*>(buf) + g * pk;
-      rg8 = reinterpret_cast<const uint16_t*>(buf) + (8 + g) * pk;
-    }
-
-    // ---- dependencies (weights are already in the stage)
-    int ntok = M, off = 0, cnt = 0;
-    if (tl.type == T_RGU || tl.type == T_RDN) {
-      cnt = ldg_cg_i32(a.ws.e_cnt + tl.e);
-      off = ldg_cg_i32(a.ws.e_off + tl.e);
-      ntok = cnt;
-    }
-    if (tl.type == T_SDN || tl.type == T_RDN) {
-      if (ctid == 0) {
-        if (tl.type == T_SDN) wait_ge(&A.ctr[3], SI / 8, status);
-        else wait_ge(&A.gu_done[tl.u], I / 8, status);
-      }
-      cbar();
-    }
-
-    // ---- passes of up to 32 tokens
-    for (int n0 = 0; n0 < ntok; n0 += kNTP * 8) {
-      const int npass = min(ntok - n0, kNTP * 8);
-      const int ntiles = (npass + 7) / 8;
-      const uint16_t* brow[kNTP];
-#pragma unroll
-      for (int nt = 0; nt < kNTP; ++nt) {
-        const int nn = n0 + nt * 8 + g;
-        const uint16_t* p = nullptr;
-        if (nt * 8 + g < npass) {
-          if (tl.type == T_RGU) p = a.x + (size_t)(ldg_cg_i32(a.ws.sorted_pairs + off + nn) / k) * H;
-          else if (tl.type == T_SGU) p = a.x + (size_t)nn * H;
-          else if (tl.type == T_RDN) p = a.ws.act + (size_t)(off + nn) * I;
-          else p = a.ws.sact + (size_t)nn * SI;
-        }
-        brow[nt] = p;
-      }
-      float acc[kNTP][4];
-      zero_acc(acc);
-      for (int s = cw; s < tl.ns; s += kCW) {
-        uint32_t af[4][2][4];
-        if (fp4) a_frags_fp4(cg, cg8, sg, sg8, s, t, af);
-        else a_frags_bf16(rg, rg8, s, t, af);
-        mma_tiles(acc, af, brow, (tl.s0 + s) * kSliceK, t, ntiles);
-      }
-      store_red(S, acc, cw, lane);
-      cbar();
-      if (ctid == 0 && n0 + kNTP * 8 >= ntok) mbar_arrive(&S.empty[st]);  // stage fully read
-      if (cw < ntiles) {
-        const int nt = cw;
-        if (tl.type == T_RGU) {
-          const float gs = a.w13_gs[tl.e];
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int nn = nt * 8 + 2 * t + c;
-            if (nn < npass) {
-              const float gv = red_sum(S, nt, lane, c) * 128.0f * gs;
-              const float uv = red_sum(S, nt, lane, 2 + c) * 128.0f * gs;
-              a.ws.act[(size_t)(off + n0 + nn) * I + tl.row0 + g] =
-                  (uint16_t)f32_to_bf16_bits(silu_approx(gv) * uv);
-            }
-          }
-        } else if (tl.type == T_RDN) {
-          const float gs2 = a.w2_gs[tl.e];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int nn = nt * 8 + 2 * t + (i & 1);
-            if (nn < npass)
-              a.ws.y[(size_t)(off + n0 + nn) * H + tl.row0 + g + (i >> 1) * 8] =
-                  (uint16_t)f32_to_bf16_bits(red_sum(S, nt, lane, i) * 128.0f * gs2);
-          }
-        } else {
-          // shared tiles: fp32 partial of this K part, [row][token]
-          float* part = tl.type == T_SGU
-                            ? A.part_sg + ((size_t)(tl.row0 / 8) * G.P_sg + tl.part) * 16 * 64
-                            : A.part_sd + ((size_t)(tl.row0 / 16) * G.P_sd + tl.part) * 16 * 64;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int nn = nt * 8 + 2 * t + (i & 1);
-            if (nn < npass) part[(g + (i >> 1) * 8) * 64 + n0 + nn] = red_sum(S, nt, lane, i);
-          }
-        }
-      }
-      cbar();
-    }
-    if (ntok == 0 && ctid == 0) mbar_arrive(&S.empty[st]);
-
-    // ---- completion
-    if (tl.type == T_RGU) {
-      if (ctid == 0) {
-        __threadfence();
-        atomicAdd(&A.gu_done[tl.u], 1);
-      }
-      continue;
-    }
-    int hb = -1;  // output block that received a down tile
-    if (tl.type == T_SGU || tl.type == T_SDN) {
-      const bool sgu = tl.type == T_SGU;
-      int* pc = sgu ? &A.sg_cnt[tl.row0 / 8] : &A.sd_cnt[tl.row0 / 16];
-      const int P = sgu ? G.P_sg : G.P_sd;
-      if (ctid == 0) {
-        __threadfence();
-        S.flag = (atomicAdd(pc, 1) == P - 1);
-      }
-      cbar();
-      if (!S.flag) continue;
-      __threadfence();
-      if (ctid == 0) *pc = 0;
-      const float* part = sgu ? A.part_sg + (size_t)(tl.row0 / 8) * P * 16 * 64
-                              : A.part_sd + (size_t)(tl.row0 / 16) * P * 16 * 64;
-      if (sgu) {
-        for (int idx = ctid; idx < 8 * M; idx += kCW * 32) {
-          const int r = idx / M, tok = idx % M;
-          float gsum = 0.0f, usum = 0.0f;
-          for (int pp = 0; pp < P; ++pp) {
-            gsum += ldg_cg_f32(part + ((size_t)pp * 16 + r) * 64 + tok);
-            usum += ldg_cg_f32(part + ((size_t)pp * 16 + 8 + r) * 64 + tok);
-          }
-          const float gS = round_bf16(gsum), uS = round_bf16(usum);
-          a.ws.sact[(size_t)tok * SI + tl.row0 + r] = (uint16_t)f32_to_bf16_bits(silu_approx(gS) * uS);
-        }
-        cbar();
-        if (ctid == 0) {
+      if (tile_arrive(S, st, lane)) {
+        group_pairs(a, S, lane);
+        __syncwarp();
+        if (lane == 0) {
           __threadfence();
-          atomicAdd(&A.ctr[3], 1);
+          st_release(&A.ctr[C_ROUTED], 1);
+          mbar_arrive(&S.empty[st]);
         }
-        continue;
       }
-      for (int idx = ctid; idx < 16 * M; idx += kCW * 32) {
-        const int r = idx / M, tok = idx % M;
-        float sum = 0.0f;
-        for (int pp = 0; pp < P; ++pp) sum += ldg_cg_f32(part + ((size_t)pp * 16 + r) * 64 + tok);
-        a.ws.ys[(size_t)tok * H + tl.row0 + r] = (uint16_t)f32_to_bf16_bits(sum);
+      continue;
+    }
+
+    // ------------------------------------------------------------ SFIN
+    if (tl.type == T_SFIN) {
+      if (warp_wait_ge(&A.ctr[C_SGU], G.NSG, status, lane)) {
+        const int nr = min(kSfinRows, SI - tl.row0);
+        for (int idx = cw * 32 + lane; idx < nr * M; idx += kCW * 32) {
+          const int r = tl.row0 + idx / M, tok = idx % M;
+          const float* part = A.part_sg + (size_t)(r / 8) * G.P_sg * 16 * 64;
+          float gsum = 0.0f, usum = 0.0f;
+          for (int pp = 0; pp < G.P_sg; ++pp) {
+            gsum += ldg_cg_f32(part + ((size_t)pp * 16 + r % 8) * 64 + tok);
+            usum += ldg_cg_f32(part + ((size_t)pp * 16 + 8 + r % 8) * 64 + tok);
+          }
+          // stock BF16 SwiGLU: gS, uS rounded, silu(gS) = gS / (1 + exp(-gS))
+          const float gS = round_bf16(gsum), uS = round_bf16(usum);
+          const float v = __fdiv_rn(gS, 1.0f + expf(-gS)) * uS;
+          a.ws.sact[(size_t)tok * SI + r] = (uint16_t)f32_to_bf16_bits(v);
+        }
       }
-      cbar();
-      hb = tl.row0 / 16;
-    } else {  // T_RDN
-      hb = tl.row0 / 16;
+      if (tile_arrive(S, st, lane) && lane == 0) {
+        red_release_add(&A.ctr[C_SFIN], 1);
+        mbar_arrive(&S.empty[st]);
+      }
+      continue;
     }
-    // a down tile of output block hb is complete: last one combines
-    if (ctid == 0) {
-      __threadfence();
-      const int expect = ldg_cg_i32(a.ws.uniq) + (SI > 0 ? 1 : 0);
-      S.flag = (atomicAdd(&A.down_cnt[hb], 1) == expect - 1);
+
+    // --------------------------------------------------------- COMBINE
+    if (tl.type == T_COMBINE) {
+      const int U = ldg_cg_i32(a.ws.uniq);
+      const int expect = U + (SI > 0 ? G.P_sd : 0);
+      const int h_end = min(H, tl.row0 + kCombineBlocks * 16);
+      bool ok2 = true;
+      for (int hb = tl.row0 / 16; hb < h_end / 16 && ok2; ++hb)
+        ok2 = warp_wait_ge(&A.down_cnt[hb], expect, status, lane);
+      if (ok2) {
+        const int nh = h_end - tl.row0;
+        for (int idx = cw * 32 + lane; idx < nh * M; idx += kCW * 32) {
+          const int tok = idx / nh, h = tl.row0 + idx % nh;
+          float R = 0.0f;
+          for (int j = 0; j < k; ++j) {
+            const int p = tok * k + j;
+            const float w = ldg_cg_f32(a.ws.tw + p);
+            const int row = ldg_cg_i32(a.ws.rowof + p);
+            R = R + w * bf16_bits_to_f32(ldg_cg_u16(a.ws.y + (size_t)row * H + h));  // rank order
+          }
+          float ys = 0.0f;
+          if (SI > 0) {
+            const float* part = A.part_sd + (size_t)(h / 16) * G.P_sd * 16 * 64;
+            float sum = 0.0f;
+            for (int pp = 0; pp < G.P_sd; ++pp)
+              sum += ldg_cg_f32(part + ((size_t)pp * 16 + h % 16) * 64 + tok);
+            ys = round_bf16(sum);
+          }
+          a.out[(size_t)tok * H + h] = (uint16_t)f32_to_bf16_bits(round_bf16(R) + ys);
+        }
+      }
+      if (tile_arrive(S, st, lane) && lane == 0) mbar_arrive(&S.empty[st]);
+      continue;
     }
-    cbar();
-    if (S.flag) {
+
+    // ------------------------------------------------------ MMA tiles
+    const bool fp4 = (tl.type == T_RGU || tl.type == T_RDN);
+    int ntok = M, off = 0;
+    if (fp4) {
+      ntok = ldg_cg_i32(a.ws.e_cnt + tl.e);
+      off = ldg_cg_i32(a.ws.e_off + tl.e);
+    }
+    const int nn = max(1, min((ntok + 7) / 8, kCW));  // n-tiles (ntok <= 64)
+    const int nk = kCW / nn;                          // K groups
+    const int nw = cw % nn, kw = cw / nn;
+    const bool active = cw < nn * nk;
+
+    bool dep_ok = true;
+    if (tl.type == T_SDN) dep_ok = warp_wait_ge(&A.ctr[C_SFIN], G.NSF, status, lane);
+    if (tl.type == T_RDN) dep_ok = warp_wait_ge(&A.gu_done[tl.u], I / 8, status, lane);
+
+    if (active) {
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (dep_ok) {
+        // activation row of this lane's token column (n = nw * 8 + g)
+        const int n = nw * 8 + g;
+        const uint16_t* brow = nullptr;
+        bool bsm = false;
+        if (n < ntok) {
+          if (tl.type == T_RGU) {
+            const int tok = ldg_cg_i32(a.ws.sorted_pairs + off + n) / k;
+            brow = G.xs ? reinterpret_cast<const uint16_t*>(S.xs) + (size_t)tok * H : a.x + (size_t)tok * H;
+            bsm = G.xs;
+          } else if (tl.type == T_SGU) {
+            brow = G.xs ? reinterpret_cast<const uint16_t*>(S.xs) + (size_t)n * H : a.x + (size_t)n * H;
+            bsm = G.xs;
+          } else if (tl.type == T_RDN) {
+            brow = a.ws.act + (size_t)(off + n) * I;
+          } else {
+            brow = a.ws.sact + (size_t)n * SI;
+          }
+        }
+        const uint8_t *cg = nullptr, *cg8 = nullptr, *sg = nullptr, *sg8 = nullptr;
+        const uint16_t *rg = nullptr, *rg8 = nullptr;
+        if (tl.type == T_RGU) {
+          cg = buf + g * (H / 2);
+          cg8 = buf + (8 + g) * (H / 2);
+          sg = buf + 16 * (H / 2) + g * (H / 16);
+          sg8 = buf + 16 * (H / 2) + (8 + g) * (H / 16);
+        } else if (tl.type == T_RDN) {
+          cg = buf + g * (I / 2);
+          cg8 = buf + (8 + g) * (I / 2);
+          sg = buf + 16 * (I / 2) + g * (I / 16);
+          sg8 = buf + 16 * (I / 2) + (8 + g) * (I / 16);
+        } else {
+          const int pk = tl.ns * kSliceK;
+          rg = reinterpret_cast<const uint16_t*>(buf) + g * pk;
+          rg8 = reinterpret_cast<const uint16_t*>(buf) + (8 + g) * pk;
+        }
+        int s = kw;
+        uint4 xb[4];
+        if (s < tl.ns) load_b(xb, brow, bsm, (tl.s0 + s) * kSliceK, t);
+        for (; s < tl.ns; s += nk) {
+          uint32_t af[4][2][4];
+          if (fp4) a_frags_fp4(cg, cg8, sg, sg8, s, t, af);
+          else a_frags_bf16(rg, rg8, s, t, af);
+          uint4 xn[4];
+          if (s + nk < tl.ns) load_b(xn, brow, bsm, (tl.s0 + s + nk) * kSliceK, t);
+          mma_slice(acc, af, xb);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) xb[q] = xn[q];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) S.red[st][cw][lane][i] = acc[i];
+    }
+    if (!tile_arrive(S, st, lane)) continue;
+
+    // ---- last warp: fixed-order reduction over K groups + epilogue
+    for (int nt = 0; nt < nn; ++nt) {
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float sum = S.red[st][nt][lane][i];
+        for (int q = 1; q < nk; ++q) sum += S.red[st][q * nn + nt][lane][i];
+        v[i] = sum;
+      }
+      if (tl.type == T_RGU) {
+        const float gs = a.w13_gs[tl.e];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int nn_ = nt * 8 + 2 * t + c;
+          if (nn_ < ntok) {
+            const float gv = v[c] * 128.0f * gs, uv = v[2 + c] * 128.0f * gs;
+            a.ws.act[(size_t)(off + nn_) * I + tl.row0 + g] = (uint16_t)f32_to_bf16_bits(silu_approx(gv) * uv);
+          }
+        }
+      } else if (tl.type == T_RDN) {
+        const float gs2 = a.w2_gs[tl.e];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int nn_ = nt * 8 + 2 * t + (i & 1);
+          if (nn_ < ntok)
+            a.ws.y[(size_t)(off + nn_) * H + tl.row0 + g + (i >> 1) * 8] =
+                (uint16_t)f32_to_bf16_bits(v[i] * 128.0f * gs2);
+        }
+      } else {
+        float* part = tl.type == T_SGU
+                          ? A.part_sg + ((size_t)(tl.row0 / 8) * G.P_sg + tl.part) * 16 * 64
+                          : A.part_sd + ((size_t)(tl.row0 / 16) * G.P_sd + tl.part) * 16 * 64;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int nn_ = nt * 8 + 2 * t + (i & 1);
+          if (nn_ < ntok) part[(g + (i >> 1) * 8) * 64 + nn_] = v[i];
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
       __threadfence();
-      combine_block(a, hb, ctid);
+      if (tl.type == T_RGU) red_release_add(&A.gu_done[tl.u], 1);
+      else if (tl.type == T_SGU) red_release_add(&A.ctr[C_SGU], 1);
+      else red_release_add(&A.down_cnt[tl.row0 / 16], 1);
+      mbar_arrive(&S.empty[st]);
     }
   }
 
-  // ---- exit: the last CTA returns every counter to zero
-  cbar();
-  if (ctid == 0) {
+  // ---- exit: the last warp of the last CTA returns every counter to zero
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) {
     __threadfence();
-    S.flag = (atomicAdd(&A.ctr[4], 1) == (int)gridDim.x - 1);
+    last = (atomicAdd(&S.exit_arr, 1) == kCW - 1);
   }
-  cbar();
-  if (S.flag) {
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  if (lane == 0) {
     __threadfence();
-    for (int i = ctid; i < 4; i += kCW * 32) A.ctr[i] = 0;
-    for (int i = ctid; i < E; i += kCW * 32) A.gu_done[i] = 0;
-    for (int i = ctid; i < H / 16; i += kCW * 32) { A.down_cnt[i] = 0; A.sd_cnt[i] = 0; }
-    for (int i = ctid; i < SI / 8; i += kCW * 32) A.sg_cnt[i] = 0;
-    cbar();
-    if (ctid == 0) { __threadfence(); A.ctr[4] = 0; }
+    last = (atomicAdd(&A.ctr[C_EXIT], 1) == (int)gridDim.x - 1);
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __threadfence();
+  for (int i = lane; i < C_N; i += 32)
+    if (i != C_EXIT) A.ctr[i] = 0;
+  for (int i = lane; i < E; i += 32) A.gu_done[i] = 0;
+  for (int i = lane; i < H / 16; i += 32) A.down_cnt[i] = 0;
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    A.ctr[C_EXIT] = 0;
   }
 }
 
 // ---------------------------------------------------------------- launch
 static int g_num_sms = 0;
 
-static Geo make_geo(const MoEArgs& a) {
+static Geo make_geo(int M, int H, int I, int SI, int E) {
   Geo G{};
-  G.nsl_H = a.H / kSliceK;
-  G.nsl_I = a.I / kSliceK;
-  G.nsl_SI = a.SI / kSliceK;
-  const int max_sl_bf16 = kStageBytes / (16 * kSliceK * 2);  // slices of 16 BF16 rows per stage
-  G.P_sg = (G.nsl_H + max_sl_bf16 - 1) / max_sl_bf16;
+  G.nsl_H = H / kSliceK;
+  G.nsl_I = I / kSliceK;
+  G.nsl_SI = SI / kSliceK;
+  const int max_sl = kStageBytes / (16 * kSliceK * 2);  // slices of 16 BF16 rows per stage
+  G.P_sg = (G.nsl_H + max_sl - 1) / max_sl;
   G.spp_sg = (G.nsl_H + G.P_sg - 1) / G.P_sg;
   G.P_sg = (G.nsl_H + G.spp_sg - 1) / G.spp_sg;
-  if (a.SI > 0) {
-    G.P_sd = (G.nsl_SI + max_sl_bf16 - 1) / max_sl_bf16;
+  if (SI > 0) {
+    G.P_sd = (G.nsl_SI + max_sl - 1) / max_sl;
     G.spp_sd = (G.nsl_SI + G.P_sd - 1) / G.P_sd;
     G.P_sd = (G.nsl_SI + G.spp_sd - 1) / G.spp_sd;
   } else {
     G.P_sd = 1;
     G.spp_sd = 1;
   }
-  G.NR = a.E;
-  G.NSG = (a.SI / 8) * G.P_sg;
-  G.N1 = G.NR + G.NSG;
+  G.NSG = (SI / 8) * G.P_sg;
+  G.N1 = E + G.NSG + 1;
+  G.NSF = (SI + kSfinRows - 1) / kSfinRows;
+  G.NCB = (H / 16 + kCombineBlocks - 1) / kCombineBlocks;
+  G.xs = (size_t)M * H * 2 <= (size_t)kXsBytes ? 1 : 0;
   return G;
 }
 
@@ -764,13 +808,11 @@ bool decode_mk_supported(const flint_moe_shape& s) {
 }
 
 size_t decode_mk_ctr_bytes(const flint_moe_shape& s) {
-  return (size_t)(8 + s.SI / 8 + 2 * (s.H / 16) + s.E) * 4;
+  return (size_t)(C_N + s.E + s.H / 16) * 4;
 }
 
 size_t decode_mk_part_bytes(const flint_moe_shape& s) {
-  MoEArgs a{};
-  a.H = s.H; a.I = s.I; a.SI = s.SI; a.E = s.E;
-  const Geo G = make_geo(a);
+  const Geo G = make_geo(s.M, s.H, s.I, s.SI, s.E);
   return ((size_t)(s.SI / 8) * G.P_sg + (size_t)(s.H / 16) * G.P_sd) * 16 * 64 * 4;
 }
 
@@ -785,12 +827,10 @@ cudaError_t launch_decode_mk(const MoEArgs& a, int* mk_ctr, float* mk_part, cuda
   }
   MkArgs A{};
   A.a = a;
-  A.G = make_geo(a);
+  A.G = make_geo(a.M, a.H, a.I, a.SI, a.E);
   A.ctr = mk_ctr;
-  A.sg_cnt = A.ctr + 8;
-  A.sd_cnt = A.sg_cnt + a.SI / 8;
-  A.down_cnt = A.sd_cnt + a.H / 16;
-  A.gu_done = A.down_cnt + a.H / 16;
+  A.gu_done = A.ctr + C_N;
+  A.down_cnt = A.gu_done + a.E;
   A.part_sg = mk_part;
   A.part_sd = A.part_sg + (size_t)(a.SI / 8) * A.G.P_sg * 16 * 64;
 

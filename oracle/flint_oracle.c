@@ -28,7 +28,9 @@
  *  R4  silu(g) = g * sigmoid(g) with an accurately rounded sigmoid; the
  *      product with u is formed last (act = bf16(silu(g) * u)).
  *  R5  the shared expert is a stock BF16 SwiGLU MLP: gS, uS = bf16(fp32 dot),
- *      sact = bf16(silu(gS) * uS), ys = bf16(fp32 dot(sact, Wd)).
+ *      sact = bf16(silu(gS) * uS) with the stock form silu(v) = v / (1 +
+ *      exp(-v)) (accurately rounded exp, fp32 division), ys = bf16(fp32
+ *      dot(sact, Wd)).
  *  R6  ranking uses the pages' total order on bf16 bit patterns (numeric
  *      order, except that -0 ranks below +0); equal bit patterns go to the
  *      lower expert index.
@@ -187,6 +189,12 @@ static void route_token(const uint16_t* logit_bits, int E, int k, int32_t* ids, 
 
 static float silu_exact(float g) { return g * sigmoid_exact(g); }
 
+/* silu of the stock BF16 SwiGLU layer (reading R5): v / (1 + exp(-v)). */
+static float silu_div(float v) {
+  float e = (float)exp(-(double)v);
+  return v / (1.0f + e);
+}
+
 /* One token through the whole block.  Writes out_row[H]; optional
  * intermediates (NULL to skip): ids[k], tw[k], logits[E] (bf16 bits),
  * act[k, I], y[k, H], sact[SI], ys[H] (bf16 bits). */
@@ -252,7 +260,7 @@ static void forward_token(const uint16_t* xrow, const uint16_t* wr, const uint8_
       su += (double)(bf16_to_f32(sgu[(int64_t)(SI + r) * H + h]) * xf[h]);
     }
     float gS = round_bf16((float)sg), uS = round_bf16((float)su);
-    sact[r] = round_bf16(silu_exact(gS) * uS);
+    sact[r] = round_bf16(silu_div(gS) * uS);
     if (sact_o)
       sact_o[r] = f32_to_bf16(sact[r]);
   }

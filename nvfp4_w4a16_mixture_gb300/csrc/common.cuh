@@ -150,13 +150,23 @@ FLINT_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
 FLINT_DEV void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
-FLINT_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// Test for phase completion; if not complete the thread may be suspended
+// (woken by the completion) for up to `hint_ns` before returning false.
+FLINT_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns = 0) {
   uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
+  if (hint_ns) {
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+  } else {
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes).
@@ -191,4 +201,19 @@ FLINT_DEV unsigned long long globaltimer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+}  // namespace flint
+
+namespace flint {
+// Shared-memory add with acquire-release semantics at CTA scope; returns old.
+FLINT_DEV int atom_add_acqrel_cta_smem(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(smem_addr(p)), "r"(v)
+               : "memory");
+  return old;
+}
+// Order this thread's earlier generic-proxy global accesses (and what it has
+// observed) before its later async-proxy (bulk copy) accesses.
+FLINT_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 }  // namespace flint

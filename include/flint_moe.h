@@ -46,6 +46,7 @@ enum {
   FLINT_ERR_WORKSPACE = -3,   /* workspace missing or too small */
   FLINT_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
   FLINT_ERR_TIMEOUT = -5,     /* a bounded device-side wait gave up */
+  FLINT_ERR_SCRATCH = -6,     /* shape needs more than the fixed static scratch */
 };
 
 /* Problem shape.
@@ -115,6 +116,40 @@ int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13,
                       const void* shared_down, const flint_moe_shape* shape, void* out,
                       int32_t* ids_out, float* tw_out, void* workspace, size_t workspace_bytes,
                       flint_stream_t stream);
+
+/* Routing without caller memory: the same kernel, numerics and outputs as
+ * flint_moe_route, but its intermediates live in a fixed scratch array that
+ * the library itself holds in device memory (2 MiB per device, a file-scope
+ * __device__ array).  The pages describe no such entry point; it exists for
+ * callers that cannot hand over or allocate device memory at the point of the
+ * call (inside an allocator hook, a memory-pool callback, or code that must
+ * not touch the caching allocator), and it makes no cudaMalloc/cudaFree or
+ * other allocating call.
+ *
+ *   x, router_w, ids, tw, shape, stream: as for flint_moe_route (I and SI of
+ *   the shape are ignored).
+ *
+ * Size limit: the call needs flint_moe_route_noalloc_bytes(shape) bytes of
+ * scratch, 256-aligned regions for ceil(M/8) int32 counters, bf16 [M, E]
+ * logits and int32 + fp32 [M, top_k]; when that exceeds
+ * flint_moe_route_noalloc_capacity() the call returns FLINT_ERR_SCRATCH and
+ * enqueues nothing (at E = 128, top_k = 8 about 6500 tokens fit).
+ * The first call on each device looks up the scratch's device address with
+ * that device current (cudaGetSymbolAddress, which may load the module); make
+ * that first call outside any stream capture.  Every call clears the counters
+ * (cudaMemsetAsync on `stream`) before the kernel; nothing else needs an
+ * initial value.  All calls on one device share the one scratch: two calls
+ * that may run at the same time on the GPU (different streams or host threads
+ * without ordering between them) race and give wrong results; order them on
+ * one stream or with events. */
+int flint_moe_route_noalloc(const void* x, const void* router_w, const flint_moe_shape* shape,
+                            int32_t* ids, float* tw, flint_stream_t stream);
+
+/* Scratch bytes flint_moe_route_noalloc needs for `shape` (0 if invalid). */
+size_t flint_moe_route_noalloc_bytes(const flint_moe_shape* shape);
+
+/* Size of the fixed scratch (bytes per device). */
+size_t flint_moe_route_noalloc_capacity(void);
 
 /* Synchronises `stream`, then reads and clears the device status word of
  * `workspace`: FLINT_OK, or the error a kernel recorded (FLINT_ERR_TIMEOUT

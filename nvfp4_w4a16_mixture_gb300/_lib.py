@@ -20,10 +20,12 @@ FLINT_ERR_UNSUPPORTED = -2
 FLINT_ERR_WORKSPACE = -3
 FLINT_ERR_CUDA = -4
 FLINT_ERR_TIMEOUT = -5
+FLINT_ERR_SCRATCH = -6
 
 # Every C symbol the header declares (checked by tests/test_abi.py).
 EXPORTED = ("flint_moe_workspace_bytes", "flint_moe_route", "flint_moe_forward",
-            "flint_moe_status", "flint_moe_strerror")
+            "flint_moe_route_noalloc", "flint_moe_route_noalloc_bytes",
+            "flint_moe_route_noalloc_capacity", "flint_moe_status", "flint_moe_strerror")
 
 
 class FlintMoEError(RuntimeError):
@@ -59,6 +61,12 @@ def load() -> ctypes.CDLL:
             lib.flint_moe_route.argtypes = [P, P, S, P, P, P, ctypes.c_size_t, P]
             lib.flint_moe_forward.restype = ctypes.c_int
             lib.flint_moe_forward.argtypes = [P] * 10 + [S, P, P, P, P, ctypes.c_size_t, P]
+            lib.flint_moe_route_noalloc.restype = ctypes.c_int
+            lib.flint_moe_route_noalloc.argtypes = [P, P, S, P, P, P]
+            lib.flint_moe_route_noalloc_bytes.restype = ctypes.c_size_t
+            lib.flint_moe_route_noalloc_bytes.argtypes = [S]
+            lib.flint_moe_route_noalloc_capacity.restype = ctypes.c_size_t
+            lib.flint_moe_route_noalloc_capacity.argtypes = []
             lib.flint_moe_status.restype = ctypes.c_int
             lib.flint_moe_status.argtypes = [P, P]
             lib.flint_moe_strerror.restype = ctypes.c_char_p
@@ -126,6 +134,28 @@ def flint_moe_forward(x, router_w, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, shared
         _ptr(tw_out), _ptr(workspace), workspace.numel(), _stream(stream))
     if rc != FLINT_OK:
         raise FlintMoEError(rc, "flint_moe_forward")
+
+
+def flint_moe_route_noalloc(x, router_w, top_k: int, ids, tw, stream=None) -> None:
+    """flint_moe_route without a caller workspace: the library's fixed
+    static scratch holds the intermediates (see include/flint_moe.h for the
+    size limit and the rule that calls sharing a device must be ordered)."""
+    M, H = x.shape
+    E = router_w.shape[0]
+    s = _shape(M, H, E, top_k, 128, 0)
+    rc = load().flint_moe_route_noalloc(_ptr(x), _ptr(router_w), ctypes.byref(s), _ptr(ids),
+                                        _ptr(tw), _stream(stream))
+    if rc != FLINT_OK:
+        raise FlintMoEError(rc, "flint_moe_route_noalloc")
+
+
+def flint_moe_route_noalloc_bytes(M: int, H: int, E: int, top_k: int) -> int:
+    s = _shape(M, H, E, top_k, 128, 0)
+    return int(load().flint_moe_route_noalloc_bytes(ctypes.byref(s)))
+
+
+def flint_moe_route_noalloc_capacity() -> int:
+    return int(load().flint_moe_route_noalloc_capacity())
 
 
 def flint_moe_status(workspace, stream=None) -> int:

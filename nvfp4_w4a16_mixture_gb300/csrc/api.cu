@@ -182,6 +182,7 @@ const char* flint_moe_strerror(int code) {
     case FLINT_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case FLINT_ERR_CUDA: return "CUDA runtime or launch error";
     case FLINT_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+    case FLINT_ERR_SCRATCH: return "shape needs more than the library's fixed static scratch";
     default: return "unknown error";
   }
 }

@@ -52,7 +52,8 @@ def test_workspace_bytes_valid_and_invalid_shapes():
 
 def test_strerror_covers_codes():
     for code in (fm.FLINT_OK, fm.FLINT_ERR_INVALID_ARG, fm.FLINT_ERR_UNSUPPORTED,
-                 fm.FLINT_ERR_WORKSPACE, fm.FLINT_ERR_CUDA, fm.FLINT_ERR_TIMEOUT):
+                 fm.FLINT_ERR_WORKSPACE, fm.FLINT_ERR_CUDA, fm.FLINT_ERR_TIMEOUT,
+                 fm.FLINT_ERR_SCRATCH):
         assert fm.flint_moe_strerror(code) not in ("", "unknown error")
     assert fm.flint_moe_strerror(12345) == "unknown error"
 
@@ -86,6 +87,27 @@ def test_validation_is_synchronous_and_touches_no_memory():
     s = _lib.flint_moe_shape(*shape)
     assert lib.flint_moe_route(None, good[1], ctypes.byref(s), good[2], good[3], good[4], need,
                                None) == fm.FLINT_ERR_INVALID_ARG
+
+
+def test_route_noalloc_size_limit_is_checked_before_any_cuda_call():
+    """The static-scratch router rejects oversize and invalid shapes
+    synchronously (fake, never-dereferenced addresses; no GPU here)."""
+    cap = fm.flint_moe_route_noalloc_capacity()
+    assert cap == 2 << 20
+    need = fm.flint_moe_route_noalloc_bytes(6543, 2048, 128, 8)
+    assert 0 < need <= cap
+    assert fm.flint_moe_route_noalloc_bytes(6544, 2048, 128, 8) > cap
+    assert fm.flint_moe_route_noalloc_bytes(1, 2048, 128, 33) == 0
+    lib = fm.load()
+    fake = [0x10000 * (i + 1) for i in range(4)]
+    big = _lib.flint_moe_shape(6544, 2048, 128, 8, 128, 0)
+    assert lib.flint_moe_route_noalloc(fake[0], fake[1], ctypes.byref(big), fake[2], fake[3],
+                                       None) == fm.FLINT_ERR_SCRATCH
+    ok = _lib.flint_moe_shape(4, 2048, 128, 8, 128, 0)
+    assert lib.flint_moe_route_noalloc(None, fake[1], ctypes.byref(ok), fake[2], fake[3],
+                                       None) == fm.FLINT_ERR_INVALID_ARG
+    assert lib.flint_moe_route_noalloc(fake[0] + 8, fake[1], ctypes.byref(ok), fake[2], fake[3],
+                                       None) == fm.FLINT_ERR_INVALID_ARG
 
 
 def test_product_path_does_not_import_oracle():

@@ -150,6 +150,10 @@ int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13, c
   a.ws = ws_pointers(workspace, L);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
+  if (decode2_supported(*shape)) {
+    if (launch_decode2(a, st) != cudaSuccess) return FLINT_ERR_CUDA;
+    return FLINT_OK;
+  }
   if (decode_mk_supported(*shape)) {
     if (launch_decode_mk(a, a.ws.mk_ctr, a.ws.mk_part, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
     return FLINT_OK;

@@ -1,0 +1,713 @@
+// Decode-path expert kernels for few tokens (M <= 64): NVFP4 gate/up with
+// SiLU * up, and the down projection with the weighted combine and the
+// shared-expert add.
+//
+// Page "vllm.models.flint.ops.moe": _gate_up_gemv_kernel
+// (act[p] = silu(x[t] Wg[e]^T) * (x[t] Wu[e]^T), global scale on the fp32
+// accumulator), _down_gemv_kernel (y_j = bf16(act W2[e_j]^T * gs),
+// out = bf16(bf16(sum_j tw_j y_j) + shared)), and the module's Numerics rule.
+//
+// Both kernels stream weights through a ring of shared-memory stages filled
+// by 1-D bulk copies (cp.async.bulk, completion counted on an mbarrier) from
+// one producer warp; eight consumer warps run the products on the tensor
+// cores (mma.sync m16n8k16, weights as the 16-row A operand, up to 8 tokens
+// per B tile).  The producer runs ahead by the whole ring, so every SM keeps
+// several tens of KB of weight reads in flight.
+//
+// Chaining (programmatic dependent launch):
+//   router (plain launch: it starts after all earlier work has finished)
+//     -> gate/up: launched early; before its dependency wait it computes the
+//        whole shared-expert gate/up (x and the weights are inputs), then
+//        streams the routed experts' tiles named by the router's metadata.
+//     -> down: launched when every gate/up CTA is past its wait (so the
+//        routing metadata is final); its producer fills the ring with down
+//        weights before the dependency wait, the consumers wait for act.
+// Every wait is bounded: on expiry the kernel records FLINT_ERR_TIMEOUT in
+// the status word, later waits return at once, and the control flow of all
+// warps stays identical (no barrier is skipped), so the launch always ends.
+#include "common.cuh"
+#include "frag.cuh"
+#include "internal.h"
+
+namespace flint {
+namespace {
+
+constexpr int kCons = 8;                    // consumer warps
+constexpr int kThreads = (kCons + 1) * 32;  // + one producer warp
+constexpr int kNT = 8;                      // n-tiles of 8 tokens: 64 tokens
+constexpr int kPad = 16;                    // smem row padding (bank spread)
+constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms
+
+// ---- gate/up ring: a stage holds 32 NVFP4 rows (16 gate + 16 up) of up to
+// 2048 K with their scales, or 16 BF16 rows (8 gate + 8 up) of up to 1024 K.
+constexpr int kGuStages = 5;
+constexpr int kGuKst4 = 2048;
+constexpr int kGuKst16 = 1024;
+constexpr int kGuStageBytes = 32 * (kGuKst4 / 2 + kPad) + 32 * (kGuKst4 / 16);  // 37376
+static_assert(16 * (2 * kGuKst16 + kPad) <= kGuStageBytes, "bf16 stage fits");
+
+// ---- down ring: a stage holds up to 8 weight blocks of 16 output rows.
+constexpr int kDnStages = 3;
+constexpr int kDnStageBytes = 57344;
+constexpr int kDnMaxBlocks = 8;
+constexpr int kDnMaxItems = 64;
+
+struct GuInfo {
+  int kind;   // 0 shared (bf16), 1 routed (nvfp4), -1 end of work
+  int first;  // first / last stage of its tile
+  int last;
+  int k0;     // K offset of the stage within the rows
+  int kst;    // K covered by the stage
+  int pitch;  // smem bytes per weight row
+  int sf_off; // byte offset of the scale rows (routed)
+  int sf_pitch;
+  int r0;     // first intermediate row of the tile
+  int e;      // expert (routed)
+  int cnt;    // tokens
+  int off;    // sorted position of the expert's first pair (routed)
+  short tok[64];
+};
+
+struct DnBlock {
+  int kind;   // 0 shared (bf16), 1 routed (nvfp4)
+  int e;
+  int cnt;
+  int off;
+  int smem;   // byte offset of the block in the stage
+  int pitch;
+  short pair[64];  // routed: pair id t * k + j of each token
+};
+
+struct DnInfo {
+  int nblocks;  // 0 = end of work
+  int nitems;
+  unsigned char item_blk[kDnMaxItems];
+  unsigned char item_nt[kDnMaxItems];
+  DnBlock blk[kDnMaxBlocks];
+};
+
+struct Ctl {
+  uint64_t full[kGuStages];
+  uint64_t empty[kGuStages];
+  int abort;
+};
+
+// Bounded wait on an mbarrier phase.  Returns false (and records the
+// timeout) once the deadline passes or another warp has given up.
+FLINT_DEV bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+  if (*abort) return false;
+  unsigned long long t0 = 0;
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long now = globaltimer_ns();
+    if (t0 == 0) t0 = now;
+    if (now - t0 > kWaitNs || *abort) {
+      *abort = 1;
+      atomicCAS(status, 0, FLINT_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+FLINT_DEV bool warp_wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
+                               int lane) {
+  int ok = 0;
+  if (lane == 0) ok = wait_phase(bar, parity, abort, status);
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Producer side of slot `n % S`: wait until the consumers released its
+// previous use.
+FLINT_DEV void acquire_slot(Ctl& c, int n, int S, volatile int* abort, int* status) {
+  if (n >= S) wait_phase(&c.empty[n % S], ((n / S) - 1) & 1, abort, status);
+}
+
+// Before the CTA exits, wait (bounded) for the copies of the stages issued
+// last, so that no bulk copy lands after the CTA has left.  `n` is the end
+// marker's stage: it reused the slot of stage n - S, whose copies had landed
+// (acquiring the slot waited for its consumers), so stages n - S + 1 .. n - 1
+// remain.
+FLINT_DEV void drain_slots(Ctl& c, int n, int S, volatile int* abort, int* status) {
+  for (int i = (n - S + 1 > 0 ? n - S + 1 : 0); i < n; ++i) {
+    const uint32_t parity = (i / S) & 1;
+    unsigned long long t0 = globaltimer_ns();
+    while (!mbar_try_wait(&c.full[i % S], parity)) {
+      if (globaltimer_ns() - t0 > kWaitNs) {
+        *abort = 1;
+        atomicCAS(status, 0, FLINT_ERR_TIMEOUT);
+        break;
+      }
+    }
+  }
+}
+
+// 8 mma of one 128-K slice against one 8-token B tile whose lane-g row is
+// `brow` (K already offset to the slice; nullptr = zero column).  The slice
+// is accumulated from zero and then added to `acc` with an fp32 add, so the
+// tensor core's own accumulation only ever spans 128 products.
+FLINT_DEV void mma_b(float (&acc)[4], const uint32_t (&af)[4][2][4], const uint16_t* brow, int t,
+                     bool l2_only) {
+  float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  uint4 xb[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (!brow) xb[q] = make_uint4(0, 0, 0, 0);
+    else xb[q] = l2_only ? ldg_cg_v4(brow + 32 * t + 8 * q) : ldg_nc_v4(brow + 32 * t + 8 * q);
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t b00 = __byte_perm(xb[q].x, xb[q].z, 0x5410);
+    const uint32_t b01 = __byte_perm(xb[q].x, xb[q].z, 0x7632);
+    const uint32_t b10 = __byte_perm(xb[q].y, xb[q].w, 0x5410);
+    const uint32_t b11 = __byte_perm(xb[q].y, xb[q].w, 0x7632);
+    mma_bf16_16816(d, af[q][0][0], af[q][0][1], af[q][0][2], af[q][0][3], b00, b01);
+    mma_bf16_16816(d, af[q][1][0], af[q][1][1], af[q][1][2], af[q][1][3], b10, b11);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] += d[i];
+}
+
+// A fragments of slice s from smem rows `rg` (row g) and `rg8` (row g + 8).
+FLINT_DEV void frags_fp4(uint32_t (&af)[4][2][4], const uint8_t* rg, const uint8_t* rg8,
+                         const uint8_t* sg, const uint8_t* sg8, int s, int t) {
+  Fp4Slice d;
+  d.c0 = *reinterpret_cast<const uint4*>(rg + s * (kSliceK / 2) + 16 * t);
+  d.c1 = *reinterpret_cast<const uint4*>(rg8 + s * (kSliceK / 2) + 16 * t);
+  d.s0 = *reinterpret_cast<const uint16_t*>(sg + s * (kSliceK / 16) + 2 * t);
+  d.s1 = *reinterpret_cast<const uint16_t*>(sg8 + s * (kSliceK / 16) + 2 * t);
+  a_frags(d, af);
+}
+
+FLINT_DEV void frags_bf16(uint32_t (&af)[4][2][4], const uint8_t* rg, const uint8_t* rg8, int s,
+                          int t) {
+  Bf16Slice d;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    d.r0[q] = *reinterpret_cast<const uint4*>(rg + 2 * (s * kSliceK + 32 * t + 8 * q));
+    d.r1[q] = *reinterpret_cast<const uint4*>(rg8 + 2 * (s * kSliceK + 32 * t + 8 * q));
+  }
+  a_frags(d, af);
+}
+
+// =============================================================== gate/up ==
+// Tiles: shared expert, 8 intermediate rows each (tile rows 0..7 gate rows
+// r0.., rows 8..15 up rows SI + r0..), stages of up to 1024 K; then routed
+// (expert u, 16 intermediate rows), smem rows 0..15 gate, 16..31 up, stages
+// of up to 2048 K.  Shared tiles go round-robin over the CTAs; the routed
+// tiles (U * I / 16 of them, expert-major) in contiguous chunks, so that
+// consecutive tiles of a CTA share an expert and its token rows stay in L1.
+//
+// Consumer warp w: routed stages -> 16-row A tile a = w & 1 (gate/up rows
+// 8a..8a+7), K slices s = w >> 1 (mod 4); shared stages -> the one A tile,
+// K slices s = w (mod 8).  After a tile's last stage the partial sums are
+// reduced over the warps in smem, in a fixed order.
+struct GuSmem {
+  Ctl ctl;
+  GuInfo info[kGuStages];
+};
+
+constexpr size_t kGuRedBytes = size_t(kCons) * kNT * 32 * 4 * sizeof(float);
+constexpr size_t kGuSmemBytes = size_t(kGuStages) * kGuStageBytes + kGuRedBytes + sizeof(GuSmem);
+
+FLINT_DEV int gu_issue_shared(const MoEArgs& a, uint8_t* stage, GuInfo& inf, uint64_t* full,
+                              int tile, int k0, int lane) {
+  const int H = a.H, SI = a.SI;
+  const int kst = min(H - k0, kGuKst16);
+  const int pitch = 2 * kst + kPad;
+  const int r0 = tile * 8;
+  if (lane == 0) {
+    inf.kind = 0; inf.first = (k0 == 0); inf.last = (k0 + kst >= H);
+    inf.k0 = k0; inf.kst = kst; inf.pitch = pitch; inf.sf_off = 0; inf.sf_pitch = 0;
+    inf.r0 = r0; inf.e = -1; inf.cnt = a.M; inf.off = 0;
+    mbar_arrive_expect_tx(full, 16u * 2u * kst);
+  }
+  __syncwarp();
+  if (lane < 16) {
+    const int row = lane < 8 ? r0 + lane : SI + r0 + (lane - 8);
+    bulk_g2s(stage + lane * pitch, a.shared_gu + (size_t)row * H + k0, 2u * kst, full);
+  }
+  return kst;
+}
+
+FLINT_DEV void gu_issue_routed(const MoEArgs& a, uint8_t* stage, GuInfo& inf, uint64_t* full,
+                               int e, int r0, int k0, int lane) {
+  const int H = a.H, I = a.I;
+  const int kst = min(H - k0, kGuKst4);
+  const int pitch = kst / 2 + kPad;
+  const int sf_off = 32 * pitch;
+  const int sfp = kst / 16;
+  const size_t g0 = (size_t)e * 2 * I + r0;  // first gate row
+  const size_t u0 = g0 + I;                  // first up row
+  if (lane == 0) {
+    inf.kind = 1; inf.first = (k0 == 0); inf.last = (k0 + kst >= H);
+    inf.k0 = k0; inf.kst = kst; inf.pitch = pitch; inf.sf_off = sf_off; inf.sf_pitch = sfp;
+    inf.r0 = r0; inf.e = e;
+    mbar_arrive_expect_tx(full, 32u * (kst / 2) + 32u * sfp);
+  }
+  __syncwarp();
+  const size_t row = lane < 16 ? g0 + lane : u0 + (lane - 16);
+  bulk_g2s(stage + lane * pitch, a.w13 + row * (H / 2) + k0 / 2, kst / 2, full);
+  if (kst == H) {  // whole rows: the 16 scale rows of gate (up) are contiguous
+    if (lane == 0) bulk_g2s(stage + sf_off, a.w13_sf + g0 * (H / 16), 16u * sfp, full);
+    if (lane == 1) bulk_g2s(stage + sf_off + 16 * sfp, a.w13_sf + u0 * (H / 16), 16u * sfp, full);
+  } else {
+    bulk_g2s(stage + sf_off + lane * sfp, a.w13_sf + row * (H / 16) + k0 / 16, sfp, full);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* stages = smem;
+  float* red = reinterpret_cast<float*>(smem + size_t(kGuStages) * kGuStageBytes);
+  GuSmem& S = *reinterpret_cast<GuSmem*>(smem + size_t(kGuStages) * kGuStageBytes + kGuRedBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int H = a.H, I = a.I, SI = a.SI;
+  const int G = gridDim.x, c = blockIdx.x;
+  int* status = a.ws.status;
+  volatile int* abort = &S.ctl.abort;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kGuStages; ++i) {
+      mbar_init(&S.ctl.full[i], 1);
+      mbar_init(&S.ctl.empty[i], kCons);
+    }
+    S.ctl.abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kCons) {
+    // ------------------------------------------------------------ producer
+    int n = 0;
+    const int nS = SI / 8;
+    for (int tile = c; tile < nS; tile += G) {
+      for (int k0 = 0; k0 < H; k0 += kGuKst16) {
+        if (lane == 0) acquire_slot(S.ctl, n, kGuStages, abort, status);
+        __syncwarp();
+        const int sl = n % kGuStages;
+        gu_issue_shared(a, stages + (size_t)sl * kGuStageBytes, S.info[sl], &S.ctl.full[sl], tile,
+                        k0, lane);
+        ++n;
+      }
+    }
+    pdl_wait();  // router finished: routing metadata is final
+    pdl_launch_dependents();
+    const int U = ldg_cg_i32(a.ws.uniq);
+    const int tpe = I / 16;  // tiles per expert
+    const int T = U * tpe;
+    const int lo = (int)((long long)T * c / G), hi = (int)((long long)T * (c + 1) / G);
+    int cur_u = -1, e = 0, cnt = 0, off = 0;
+    short tok0 = 0, tok1 = 0;
+    for (int tile = lo; tile < hi; ++tile) {
+      const int u = tile / tpe, r0 = (tile % tpe) * 16;
+      if (u != cur_u) {  // tokens of the expert, read once per expert
+        e = ldg_cg_i32(a.ws.uniq + 1 + u);
+        cnt = ldg_cg_i32(a.ws.e_cnt + e);
+        off = ldg_cg_i32(a.ws.e_off + e);
+        tok0 = lane < cnt ? (short)(ldg_cg_i32(a.ws.sorted_pairs + off + lane) / a.k) : 0;
+        tok1 = lane + 32 < cnt ? (short)(ldg_cg_i32(a.ws.sorted_pairs + off + lane + 32) / a.k) : 0;
+        cur_u = u;
+      }
+      for (int k0 = 0; k0 < H; k0 += kGuKst4) {
+        if (lane == 0) acquire_slot(S.ctl, n, kGuStages, abort, status);
+        __syncwarp();
+        const int sl = n % kGuStages;
+        GuInfo& inf = S.info[sl];
+        inf.tok[lane] = tok0;
+        inf.tok[lane + 32] = tok1;
+        if (lane == 0) { inf.cnt = cnt; inf.off = off; }
+        __syncwarp();  // info complete before the arrive that publishes it
+        gu_issue_routed(a, stages + (size_t)sl * kGuStageBytes, inf, &S.ctl.full[sl], e, r0, k0,
+                        lane);
+        ++n;
+      }
+    }
+    // end marker: a stage with no copies
+    if (lane == 0) {
+      acquire_slot(S.ctl, n, kGuStages, abort, status);
+      const int sl = n % kGuStages;
+      S.info[sl].kind = -1;
+      mbar_arrive(&S.ctl.full[sl]);
+      drain_slots(S.ctl, n, kGuStages, abort, status);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  float acc[kNT][4];
+  bool triggered = false;
+  for (int n = 0;; ++n) {
+    const int sl = n % kGuStages;
+    warp_wait_phase(&S.ctl.full[sl], (n / kGuStages) & 1, abort, status, lane);
+    const GuInfo& inf = S.info[sl];
+    const int kind = inf.kind;
+    if (kind != 0 && !triggered) {  // past the producer's dependency wait
+      pdl_launch_dependents();
+      triggered = true;
+    }
+    if (kind < 0) break;
+    const int first = inf.first, last = inf.last, k0 = inf.k0, kst = inf.kst;
+    const int pitch = inf.pitch, cnt = inf.cnt;
+    const int ntiles = (cnt + 7) / 8;
+    const uint8_t* st = stages + (size_t)sl * kGuStageBytes;
+    if (first) {
+#pragma unroll
+      for (int i = 0; i < kNT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+    }
+    // B rows of this lane (token column g of every n-tile)
+    const uint16_t* brow[kNT];
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+      const int nn = nt * 8 + g;
+      brow[nt] = nullptr;
+      if (nn < cnt) brow[nt] = a.x + (size_t)(kind ? inf.tok[nn] : nn) * H + k0;
+    }
+    const int nsl = kst / kSliceK;
+    if (kind == 1) {
+      const int at = warp & 1, kp = warp >> 1;
+      const uint8_t* rg = st + (8 * at + g) * pitch;
+      const uint8_t* rg8 = st + (16 + 8 * at + g) * pitch;
+      const uint8_t* sg = st + inf.sf_off + (8 * at + g) * inf.sf_pitch;
+      const uint8_t* sg8 = st + inf.sf_off + (16 + 8 * at + g) * inf.sf_pitch;
+      for (int s = kp; s < nsl; s += 4) {
+        uint32_t af[4][2][4];
+        frags_fp4(af, rg, rg8, sg, sg8, s, t);
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+          if (nt < ntiles) mma_b(acc[nt], af, brow[nt] ? brow[nt] + s * kSliceK : nullptr, t, false);
+      }
+    } else {
+      const uint8_t* rg = st + g * pitch;
+      const uint8_t* rg8 = st + (8 + g) * pitch;
+      for (int s = warp; s < nsl; s += kCons) {
+        uint32_t af[4][2][4];
+        frags_bf16(af, rg, rg8, s, t);
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+          if (nt < ntiles) mma_b(acc[nt], af, brow[nt] ? brow[nt] + s * kSliceK : nullptr, t, false);
+      }
+    }
+    const int r0 = inf.r0, e = inf.e, off = inf.off;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.ctl.empty[sl]);  // stage consumed
+    if (!last) continue;
+
+    // ---- tile epilogue: reduce the warps' partials (fixed order), write
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+      if (nt < ntiles)
+        *reinterpret_cast<float4*>(red + ((size_t)(warp * kNT + nt) * 32 + lane) * 4) =
+            make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+    named_bar(1, kCons * 32);
+    if (kind == 1) {
+      const float gs = a.w13_gs[e] * 128.0f;  // 2^7 undoes the operand scaling
+      for (int it = warp; it < 2 * ntiles; it += kCons) {
+        const int at = it & 1, nt = it >> 1;
+        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int kp = 0; kp < 4; ++kp) {
+          const float4 p = *reinterpret_cast<const float4*>(
+              red + ((size_t)((at + 2 * kp) * kNT + nt) * 32 + lane) * 4);
+          v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
+        }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int nn = nt * 8 + 2 * t + cc;
+          if (nn < cnt) {
+            const float gv = v[cc] * gs, uv = v[2 + cc] * gs;
+            a.ws.act[(size_t)(off + nn) * I + r0 + 8 * at + g] =
+                (uint16_t)f32_to_bf16_bits(silu_approx(gv) * uv);
+          }
+        }
+      }
+    } else {
+      for (int nt = warp; nt < ntiles; nt += kCons) {
+        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int w = 0; w < kCons; ++w) {
+          const float4 p =
+              *reinterpret_cast<const float4*>(red + ((size_t)(w * kNT + nt) * 32 + lane) * 4);
+          v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
+        }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int nn = nt * 8 + 2 * t + cc;
+          if (nn < cnt) {
+            // stock BF16 SwiGLU: gS, uS rounded, silu(gS) = gS / (1 + exp(-gS))
+            const float gS = round_bf16(v[cc]), uS = round_bf16(v[2 + cc]);
+            const float sv = __fdiv_rn(gS, 1.0f + expf(-gS)) * uS;
+            a.ws.sact[(size_t)nn * SI + r0 + g] = (uint16_t)f32_to_bf16_bits(sv);
+          }
+        }
+      }
+    }
+    named_bar(1, kCons * 32);  // red free for the next tile
+  }
+  if (!triggered) pdl_launch_dependents();
+}
+
+// ================================================================== down ==
+// CTA hb owns output rows h0 = 16 hb .. h0 + 15 for every token.  Weight
+// blocks: the shared expert's 16 rows (BF16, SI <= 1024 K) and, per routed
+// expert u < U, its 16 rows of w2 (NVFP4, I <= 2048 K) with their scales,
+// packed in order into stages of up to 8 blocks.  Work items are (block,
+// 8-token n-tile); warp w takes items w, w + 8, ... of a stage and runs the
+// whole K of its item, so no cross-warp reduction is needed.  Results go to
+// smem: y (bf16, per pair t * k + j) and ys (bf16, per token); after the last
+// stage the CTA forms out = bf16(bf16(sum_j tw_j y_j) + ys) for its rows.
+struct DnSmem {
+  Ctl ctl;
+  DnInfo info[kDnStages];
+};
+
+// Byte offsets in the down kernel's dynamic smem: stages, y, ys, control.
+struct DnLayout {
+  size_t y, ys, ctl, total;
+};
+__host__ __device__ inline DnLayout dn_layout(int M, int k) {
+  DnLayout L;
+  L.y = size_t(kDnStages) * kDnStageBytes;
+  L.ys = L.y + (size_t(M) * k * 16 * 2 + 15) / 16 * 16;
+  L.ctl = L.ys + (size_t(M) * 16 * 2 + 15) / 16 * 16;
+  L.total = L.ctl + sizeof(DnSmem);
+  return L;
+}
+
+size_t dn_smem_bytes(const flint_moe_shape& s) { return dn_layout(s.M, s.top_k).total; }
+
+FLINT_DEV int dn_block_bytes(int kind, int I, int SI) {
+  return kind ? 16 * (I / 2 + kPad) + I : 16 * (2 * SI + kPad);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* stages = smem;
+  const DnLayout L = dn_layout(a.M, a.k);
+  uint16_t* ysm = reinterpret_cast<uint16_t*>(smem + L.y);
+  uint16_t* yss = reinterpret_cast<uint16_t*>(smem + L.ys);
+  DnSmem& S = *reinterpret_cast<DnSmem*>(smem + L.ctl);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int H = a.H, I = a.I, SI = a.SI, k = a.k, M = a.M;
+  const int h0 = blockIdx.x * 16;
+  int* status = a.ws.status;
+  volatile int* abort = &S.ctl.abort;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDnStages; ++i) {
+      mbar_init(&S.ctl.full[i], 1);
+      mbar_init(&S.ctl.empty[i], kCons);
+    }
+    S.ctl.abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kCons) {
+    // ------------------------------------------------------------ producer
+    // The gate/up grid released this grid only after its own dependency
+    // wait, which follows the router's completion: the metadata is final.
+    const int U = ldg_cg_i32(a.ws.uniq);
+    const int nunits = U + (SI > 0 ? 1 : 0);
+    int n = 0, unit = 0;
+    while (unit < nunits) {
+      if (lane == 0) acquire_slot(S.ctl, n, kDnStages, abort, status);
+      __syncwarp();
+      const int sl = n % kDnStages;
+      uint8_t* st = stages + (size_t)sl * kDnStageBytes;
+      DnInfo& inf = S.info[sl];
+      int used = 0, nb = 0, ni = 0;
+      uint32_t bytes = 0;
+      // plan the stage (all lanes compute the same plan)
+      int first_unit = unit;
+      while (unit < nunits && nb < kDnMaxBlocks) {
+        const bool shared = SI > 0 && unit == 0;
+        const int bb = dn_block_bytes(shared ? 0 : 1, I, SI);
+        if (used + bb > kDnStageBytes) break;
+        int e = -1, cnt = M, off = 0;
+        if (!shared) {
+          e = ldg_cg_i32(a.ws.uniq + 1 + (unit - (SI > 0 ? 1 : 0)));
+          cnt = ldg_cg_i32(a.ws.e_cnt + e);
+          off = ldg_cg_i32(a.ws.e_off + e);
+        }
+        const int nit = (cnt + 7) / 8;
+        if (ni + nit > kDnMaxItems) break;
+        DnBlock& b = inf.blk[nb];
+        if (lane == 0) {
+          b.kind = shared ? 0 : 1; b.e = e; b.cnt = cnt; b.off = off; b.smem = used;
+          b.pitch = shared ? 2 * SI + kPad : I / 2 + kPad;
+          for (int i = 0; i < nit; ++i) {
+            inf.item_blk[ni + i] = (unsigned char)nb;
+            inf.item_nt[ni + i] = (unsigned char)i;
+          }
+        }
+        if (!shared) {
+          if (lane < cnt) b.pair[lane] = (short)ldg_cg_i32(a.ws.sorted_pairs + off + lane);
+          if (lane + 32 < cnt) b.pair[lane + 32] = (short)ldg_cg_i32(a.ws.sorted_pairs + off + lane + 32);
+          bytes += 16u * (I / 2) + 16u * (I / 16);
+        } else {
+          bytes += 16u * 2u * SI;
+        }
+        used += bb;
+        ++nb;
+        ni += nit;
+        ++unit;
+      }
+      if (lane == 0) { inf.nblocks = nb; inf.nitems = ni; }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&S.ctl.full[sl], bytes);
+      __syncwarp();
+      // issue the copies of every block of the stage
+      for (int bi = 0; bi < nb; ++bi) {
+        const int u = first_unit + bi;
+        const bool shared = SI > 0 && u == 0;
+        const DnBlock& b = inf.blk[bi];
+        uint8_t* dst = st + b.smem;
+        if (shared) {
+          if (lane < 16)
+            bulk_g2s(dst + lane * b.pitch, a.shared_down + (size_t)(h0 + lane) * SI, 2u * SI,
+                     &S.ctl.full[sl]);
+        } else {
+          const size_t row0 = (size_t)b.e * H + h0;
+          if (lane < 16)
+            bulk_g2s(dst + lane * b.pitch, a.w2 + (row0 + lane) * (I / 2), I / 2, &S.ctl.full[sl]);
+          if (lane == 16)
+            bulk_g2s(dst + 16 * b.pitch, a.w2_sf + row0 * (I / 16), 16u * (I / 16), &S.ctl.full[sl]);
+        }
+      }
+      ++n;
+    }
+    if (lane == 0) {
+      acquire_slot(S.ctl, n, kDnStages, abort, status);
+      const int sl = n % kDnStages;
+      S.info[sl].nblocks = 0;
+      mbar_arrive(&S.ctl.full[sl]);
+      drain_slots(S.ctl, n, kDnStages, abort, status);
+    }
+    // the combine below needs every consumer's results
+    named_bar(2, kThreads);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  pdl_wait();  // gate/up finished: act and sact are complete
+  for (int n = 0;; ++n) {
+    const int sl = n % kDnStages;
+    warp_wait_phase(&S.ctl.full[sl], (n / kDnStages) & 1, abort, status, lane);
+    const DnInfo& inf = S.info[sl];
+    if (inf.nblocks == 0) break;
+    const uint8_t* st = stages + (size_t)sl * kDnStageBytes;
+    for (int it = warp; it < inf.nitems; it += kCons) {
+      const DnBlock& b = inf.blk[inf.item_blk[it]];
+      const int nt = inf.item_nt[it];
+      const int nn = nt * 8 + g;  // token column of this lane
+      const uint8_t* rg = st + b.smem + g * b.pitch;
+      const uint8_t* rg8 = st + b.smem + (8 + g) * b.pitch;
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (b.kind == 1) {
+        const uint16_t* brow = nn < b.cnt ? a.ws.act + (size_t)(b.off + nn) * I : nullptr;
+        const uint8_t* sg = st + b.smem + 16 * b.pitch + g * (I / 16);
+        const uint8_t* sg8 = sg + 8 * (I / 16);
+        for (int s = 0; s < I / kSliceK; ++s) {
+          uint32_t af[4][2][4];
+          frags_fp4(af, rg, rg8, sg, sg8, s, t);
+          mma_b(acc, af, brow ? brow + s * kSliceK : nullptr, t, true);
+        }
+        const float gs2 = a.w2_gs[b.e] * 128.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int tok = nt * 8 + 2 * t + (i & 1);
+          if (tok < b.cnt) {
+            const int p = b.pair[tok];
+            ysm[(size_t)p * 16 + g + (i >> 1) * 8] = (uint16_t)f32_to_bf16_bits(acc[i] * gs2);
+          }
+        }
+      } else {
+        const uint16_t* brow = nn < M ? a.ws.sact + (size_t)nn * SI : nullptr;
+        for (int s = 0; s < SI / kSliceK; ++s) {
+          uint32_t af[4][2][4];
+          frags_bf16(af, rg, rg8, s, t);
+          mma_b(acc, af, brow ? brow + s * kSliceK : nullptr, t, true);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int tok = nt * 8 + 2 * t + (i & 1);
+          if (tok < M) yss[(size_t)tok * 16 + g + (i >> 1) * 8] = (uint16_t)f32_to_bf16_bits(acc[i]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.ctl.empty[sl]);
+  }
+  named_bar(2, kThreads);
+
+  // ---- combine: out = bf16(bf16(sum_j tw_j y_j) + ys), j in rank order
+  for (int idx = threadIdx.x; idx < M * 16; idx += kCons * 32) {
+    const int tt = idx >> 4, h = idx & 15;
+    float R = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const float w = ldg_cg_f32(a.ws.tw + tt * k + j);
+      R = R + w * bf16_bits_to_f32(ysm[(size_t)(tt * k + j) * 16 + h]);
+    }
+    const float ys = SI > 0 ? bf16_bits_to_f32(yss[tt * 16 + h]) : 0.0f;
+    a.out[(size_t)tt * H + h0 + h] = (uint16_t)f32_to_bf16_bits(round_bf16(R) + ys);
+  }
+}
+
+// ------------------------------------------------------------------ launch
+struct DevCache {
+  int sms = 0;
+  bool attrs = false;
+};
+DevCache g_dev[64];
+
+cudaError_t launch_ex(const void* fn, dim3 grid, size_t smem, void** args, cudaStream_t st,
+                      bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace
+
+bool decode2_supported(const flint_moe_shape& s) {
+  return s.M <= kDecodeMaxTokens && s.M * s.top_k <= 1024 && s.I <= kGuKst4 &&
+         s.SI <= kGuKst16 && (s.H <= kGuKst4 || s.H % 256 == 0) &&
+         dn_smem_bytes(s) <= 232448 && 16 * (s.I / 2 + kPad) + s.I <= kDnStageBytes;
+}
+
+cudaError_t launch_decode2(const MoEArgs& a, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  DevCache& dc = g_dev[dev];
+  if (!dc.attrs) {
+    err = cudaDeviceGetAttribute(&dc.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute((const void*)gate_up2_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGuSmemBytes);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute((const void*)down2_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (err != cudaSuccess) return err;
+    dc.attrs = true;
+  }
+  const flint_moe_shape s{a.M, a.H, a.E, a.k, a.I, a.SI};
+  MoEArgs aa = a;
+  void* args[] = {&aa};
+  err = launch_route(a, true, st, false);
+  if (err != cudaSuccess) return err;
+  err = launch_ex((const void*)gate_up2_kernel, dim3(dc.sms), kGuSmemBytes, args, st, true);
+  if (err != cudaSuccess) return err;
+  return launch_ex((const void*)down2_kernel, dim3(a.H / 16), dn_smem_bytes(s), args, st, true);
+}
+
+}  // namespace flint

@@ -94,6 +94,12 @@ cudaError_t launch_route(const MoEArgs& a, bool build_meta, cudaStream_t st, boo
 cudaError_t launch_decode_gate_up(const MoEArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_decode_down(const MoEArgs& a, cudaStream_t st, bool pdl);
 
+// Decode path of few tokens: router, gate/up and down+combine kernels chained
+// with programmatic dependent launch (M <= kDecodeMaxTokens and the limits
+// decode2_supported checks).
+bool decode2_supported(const flint_moe_shape& s);
+cudaError_t launch_decode2(const MoEArgs& a, cudaStream_t st);
+
 // Decode megakernel (whole block in one persistent launch, M <= kDecodeMaxTokens).
 bool decode_mk_supported(const flint_moe_shape& s);
 size_t decode_mk_ctr_bytes(const flint_moe_shape& s);

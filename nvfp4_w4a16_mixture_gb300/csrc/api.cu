@@ -46,6 +46,7 @@ WsLayout ws_layout(const flint_moe_shape& s) {
   L.uniq = take(4 * (E + 1));
   L.sorted_pairs = take(4 * np);
   L.rowof = take(4 * np);
+  L.urec = take(4 * (size_t)kUrecInts * (np < E ? np : E));
   L.gcnt = take(4 * 2 * nchunks * E);
   L.act = take(2 * np * I);
   L.sact = take(2 * M * (SI > 0 ? SI : 1));
@@ -71,6 +72,7 @@ Ws ws_pointers(void* base, const WsLayout& L) {
   w.uniq = reinterpret_cast<int*>(b + L.uniq);
   w.sorted_pairs = reinterpret_cast<int*>(b + L.sorted_pairs);
   w.rowof = reinterpret_cast<int*>(b + L.rowof);
+  w.urec = reinterpret_cast<int*>(b + L.urec);
   w.gcnt = reinterpret_cast<int*>(b + L.gcnt);
   w.act = reinterpret_cast<uint16_t*>(b + L.act);
   w.sact = reinterpret_cast<uint16_t*>(b + L.sact);

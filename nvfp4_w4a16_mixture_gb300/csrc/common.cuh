@@ -26,8 +26,11 @@ FLINT_DEV float round_bf16(float f) { return __bfloat162float(__float2bfloat16_r
 // bf16 value is 2^(E-127) * (1 + m/2) = e2m1 * 2^-126 for E > 0 and the bf16
 // subnormal m/2 * 2^-126 = e2m1 * 2^-126 for E = 0; the sign goes to bit 15.
 // `v` carries code A in bits 3..0 and code B in bits 19..16.
+// Both moves are one multiply: a 4-bit field times 2^6 + 2^12 lands at bits
+// 6..9 and 12..15 without overlap (so without carries), and the mask keeps
+// bits 6..8 of the first copy and bit 15 (the sign) of the second.
 FLINT_DEV uint32_t e2m1x2_to_bf16x2_scaled(uint32_t v) {
-  return ((v << 6) & 0x01C001C0u) | ((v << 12) & 0x80008000u);
+  return ((v & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
 }
 
 // Pair `a` (0..3) of a word of 8 codes (nibble i = K offset i): codes a and
@@ -144,6 +147,12 @@ FLINT_DEV void mbar_init(uint64_t* bar, uint32_t count) {
 FLINT_DEV void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 FLINT_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// Adds `bytes` to the expected transaction count without arriving.
+FLINT_DEV void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)),
                "r"(bytes)
                : "memory");
 }

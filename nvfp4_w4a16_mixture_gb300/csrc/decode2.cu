@@ -9,18 +9,18 @@
 //
 // Both kernels stream weights through a ring of shared-memory stages filled
 // by 1-D bulk copies (cp.async.bulk, completion counted on an mbarrier) from
-// one producer warp; eight consumer warps run the products on the tensor
+// one producer warp; sixteen consumer warps run the products on the tensor
 // cores (mma.sync m16n8k16, weights as the 16-row A operand, up to 8 tokens
 // per B tile).  The producer runs ahead by the whole ring, so every SM keeps
-// several tens of KB of weight reads in flight.
+// well over 100 KB of weight reads in flight.
 //
 // Chaining (programmatic dependent launch):
 //   router (plain launch: it starts after all earlier work has finished)
 //     -> gate/up: launched early; before its dependency wait it computes the
 //        whole shared-expert gate/up (x and the weights are inputs), then
-//        streams the routed experts' tiles named by the router's metadata.
+//        streams the routed experts' tiles named by the router's records.
 //     -> down: launched when every gate/up CTA is past its wait (so the
-//        routing metadata is final); its producer fills the ring with down
+//        routing records are final); its producer fills the ring with down
 //        weights before the dependency wait, the consumers wait for act.
 // Every wait is bounded: on expiry the kernel records FLINT_ERR_TIMEOUT in
 // the status word, later waits return at once, and the control flow of all
@@ -32,19 +32,21 @@
 namespace flint {
 namespace {
 
-constexpr int kCons = 8;                    // consumer warps
+constexpr int kCons = 16;                   // consumer warps
 constexpr int kThreads = (kCons + 1) * 32;  // + one producer warp
-constexpr int kNT = 8;                      // n-tiles of 8 tokens: 64 tokens
 constexpr int kPad = 16;                    // smem row padding (bank spread)
+constexpr int kMaxSmem = 232448;            // opt-in shared memory per CTA
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms
+constexpr uint32_t kSuspendNs = 50000;  // suspend-time hint of one try_wait
 
 // ---- gate/up ring: a stage holds 32 NVFP4 rows (16 gate + 16 up) of up to
 // 2048 K with their scales, or 16 BF16 rows (8 gate + 8 up) of up to 1024 K.
-constexpr int kGuStages = 5;
+constexpr int kGuMaxStages = 5;
 constexpr int kGuKst4 = 2048;
 constexpr int kGuKst16 = 1024;
 constexpr int kGuStageBytes = 32 * (kGuKst4 / 2 + kPad) + 32 * (kGuKst4 / 16);  // 37376
 static_assert(16 * (2 * kGuKst16 + kPad) <= kGuStageBytes, "bf16 stage fits");
+constexpr int kKP = kCons / 2;  // K parts of a routed stage (x 2 A tiles)
 
 // ---- down ring: a stage holds up to 8 weight blocks of 16 output rows.
 constexpr int kDnStages = 3;
@@ -65,61 +67,89 @@ struct GuInfo {
   int e;      // expert (routed)
   int cnt;    // tokens
   int off;    // sorted position of the expert's first pair (routed)
-  short tok[64];
+  short tok[kDecodeMaxTokens];
 };
 
 struct DnBlock {
-  int kind;   // 0 shared (bf16), 1 routed (nvfp4)
+  int kind;      // 0 shared (bf16), 1 routed (nvfp4)
   int e;
+  int u;         // routed: index of the expert's routing record
   int cnt;
   int off;
-  int smem;   // byte offset of the block in the stage
+  int smem;      // byte offset of the weight rows in the stage
   int pitch;
-  short pair[64];  // routed: pair id t * k + j of each token
+  int act_smem;  // byte offset of the block's activation rows, -1 = read from global
 };
 
 struct DnInfo {
   int nblocks;  // 0 = end of work
   int nitems;
+  int abytes;   // bytes of activation rows staged with the block weights
   unsigned char item_blk[kDnMaxItems];
   unsigned char item_nt[kDnMaxItems];
   DnBlock blk[kDnMaxBlocks];
 };
 
 struct Ctl {
-  uint64_t full[kGuStages];
-  uint64_t empty[kGuStages];
+  uint64_t full[kGuMaxStages];
+  uint64_t empty[kGuMaxStages];
+  uint64_t bar[2];  // CTA barriers among warps (bounded, unlike bar.sync)
   int abort;
 };
 
+// Records a timeout: status[0] = FLINT_ERR_TIMEOUT, and for the first one
+// status[1] = wait site, status[2] = CTA, status[3] = stage.
+FLINT_DEV void record_timeout(int* status, int site, int n) {
+  if (atomicCAS(status, 0, FLINT_ERR_TIMEOUT) == 0) {
+    status[1] = site;
+    status[2] = (int)blockIdx.x;
+    status[3] = n;
+  }
+}
+
 // Bounded wait on an mbarrier phase.  Returns false (and records the
 // timeout) once the deadline passes or another warp has given up.
-FLINT_DEV bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+FLINT_DEV bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
+                          int site, int n) {
   if (*abort) return false;
   unsigned long long t0 = 0;
   for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
+    // suspends until the phase completes (or the hint runs out), so idle
+    // warps leave the issue slots to the working ones
+    if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
+    if (*abort) return false;
     const unsigned long long now = globaltimer_ns();
     if (t0 == 0) t0 = now;
-    if (now - t0 > kWaitNs || *abort) {
+    if (now - t0 > kWaitNs) {
       *abort = 1;
-      atomicCAS(status, 0, FLINT_ERR_TIMEOUT);
+      record_timeout(status, site, n);
       return false;
     }
   }
 }
 
 FLINT_DEV bool warp_wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
-                               int lane) {
+                               int lane, int site, int n) {
   int ok = 0;
-  if (lane == 0) ok = wait_phase(bar, parity, abort, status);
+  if (lane == 0) ok = wait_phase(bar, parity, abort, status, site, n);
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Barrier among the `count` warps that share mbarrier `bar` (lane 0 of each
+// arrives); `phase` is the warp's own count of passed barriers on it.
+FLINT_DEV void warp_barrier(uint64_t* bar, uint32_t& phase, volatile int* abort, int* status,
+                            int lane, int site) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  warp_wait_phase(bar, phase & 1, abort, status, lane, site, (int)phase);
+  ++phase;
 }
 
 // Producer side of slot `n % S`: wait until the consumers released its
 // previous use.
-FLINT_DEV void acquire_slot(Ctl& c, int n, int S, volatile int* abort, int* status) {
-  if (n >= S) wait_phase(&c.empty[n % S], ((n / S) - 1) & 1, abort, status);
+FLINT_DEV bool acquire_slot(Ctl& c, int n, int S, volatile int* abort, int* status, int site) {
+  if (n < S) return !*abort;
+  return wait_phase(&c.empty[n % S], ((n / S) - 1) & 1, abort, status, site, n);
 }
 
 // Before the CTA exits, wait (bounded) for the copies of the stages issued
@@ -131,29 +161,31 @@ FLINT_DEV void drain_slots(Ctl& c, int n, int S, volatile int* abort, int* statu
   for (int i = (n - S + 1 > 0 ? n - S + 1 : 0); i < n; ++i) {
     const uint32_t parity = (i / S) & 1;
     unsigned long long t0 = globaltimer_ns();
-    while (!mbar_try_wait(&c.full[i % S], parity)) {
+    while (!mbar_try_wait(&c.full[i % S], parity, kSuspendNs)) {
       if (globaltimer_ns() - t0 > kWaitNs) {
         *abort = 1;
-        atomicCAS(status, 0, FLINT_ERR_TIMEOUT);
+        record_timeout(status, 9, i);
         break;
       }
     }
   }
 }
 
-// 8 mma of one 128-K slice against one 8-token B tile whose lane-g row is
-// `brow` (K already offset to the slice; nullptr = zero column).  The slice
-// is accumulated from zero and then added to `acc` with an fp32 add, so the
-// tensor core's own accumulation only ever spans 128 products.
-FLINT_DEV void mma_b(float (&acc)[4], const uint32_t (&af)[4][2][4], const uint16_t* brow, int t,
-                     bool l2_only) {
-  float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  uint4 xb[4];
+// The lane's 32 B-operand K values of one slice (token row `brow`, already
+// offset to the slice; nullptr = zero column).
+FLINT_DEV void load_b(uint4 (&xb)[4], const uint16_t* brow, int t, bool l2_only) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     if (!brow) xb[q] = make_uint4(0, 0, 0, 0);
     else xb[q] = l2_only ? ldg_cg_v4(brow + 32 * t + 8 * q) : ldg_nc_v4(brow + 32 * t + 8 * q);
   }
+}
+
+// 8 mma of one 128-K slice against one 8-token B tile.  The slice is
+// accumulated from zero and then added to `acc` with an fp32 add, so the
+// tensor core's own accumulation only ever spans 128 products.
+FLINT_DEV void mma_b(float (&acc)[4], const uint32_t (&af)[4][2][4], const uint4 (&xb)[4]) {
+  float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const uint32_t b00 = __byte_perm(xb[q].x, xb[q].z, 0x5410);
@@ -198,19 +230,36 @@ FLINT_DEV void frags_bf16(uint32_t (&af)[4][2][4], const uint8_t* rg, const uint
 // consecutive tiles of a CTA share an expert and its token rows stay in L1.
 //
 // Consumer warp w: routed stages -> 16-row A tile a = w & 1 (gate/up rows
-// 8a..8a+7), K slices s = w >> 1 (mod 4); shared stages -> the one A tile,
-// K slices s = w (mod 8).  After a tile's last stage the partial sums are
-// reduced over the warps in smem, in a fixed order.
+// 8a..8a+7), K slices s = w >> 1 (mod 8); shared stages -> the one A tile,
+// K slices s = w (mod 8), warps 8..15 idle.  Token n-tiles are taken NTG at
+// a time in registers; each warp adds its partial sums for the tile into its
+// own smem rows (red), which the tile epilogue sums over the warps in a
+// fixed order.
 struct GuSmem {
   Ctl ctl;
-  GuInfo info[kGuStages];
+  GuInfo info[kGuMaxStages];
 };
 
-constexpr size_t kGuRedBytes = size_t(kCons) * kNT * 32 * 4 * sizeof(float);
-constexpr size_t kGuSmemBytes = size_t(kGuStages) * kGuStageBytes + kGuRedBytes + sizeof(GuSmem);
+struct GuLayout {
+  int stages;
+  size_t red, ctl, total;
+};
 
-FLINT_DEV int gu_issue_shared(const MoEArgs& a, uint8_t* stage, GuInfo& inf, uint64_t* full,
-                              int tile, int k0, int lane) {
+__host__ __device__ inline GuLayout gu_layout(int M) {
+  const int ntmax = (M + 7) / 8;
+  GuLayout L;
+  const size_t red_bytes = size_t(kCons) * ntmax * 32 * 16;
+  const size_t room = kMaxSmem - sizeof(GuSmem) - red_bytes;
+  L.stages = (int)(room / kGuStageBytes);
+  if (L.stages > kGuMaxStages) L.stages = kGuMaxStages;
+  L.red = size_t(L.stages) * kGuStageBytes;
+  L.ctl = L.red + red_bytes;
+  L.total = L.ctl + sizeof(GuSmem);
+  return L;
+}
+
+FLINT_DEV void gu_issue_shared(const MoEArgs& a, uint8_t* stage, GuInfo& inf, uint64_t* full,
+                               int tile, int k0, int lane) {
   const int H = a.H, SI = a.SI;
   const int kst = min(H - k0, kGuKst16);
   const int pitch = 2 * kst + kPad;
@@ -226,14 +275,14 @@ FLINT_DEV int gu_issue_shared(const MoEArgs& a, uint8_t* stage, GuInfo& inf, uin
     const int row = lane < 8 ? r0 + lane : SI + r0 + (lane - 8);
     bulk_g2s(stage + lane * pitch, a.shared_gu + (size_t)row * H + k0, 2u * kst, full);
   }
-  return kst;
 }
 
 FLINT_DEV void gu_issue_routed(const MoEArgs& a, uint8_t* stage, GuInfo& inf, uint64_t* full,
                                int e, int r0, int k0, int lane) {
   const int H = a.H, I = a.I;
   const int kst = min(H - k0, kGuKst4);
-  const int pitch = kst / 2 + kPad;
+  const bool whole = (kst == H);  // whole rows: 16 gate (up) rows are one block
+  const int pitch = whole ? kst / 2 : kst / 2 + kPad;
   const int sf_off = 32 * pitch;
   const int sfp = kst / 16;
   const size_t g0 = (size_t)e * 2 * I + r0;  // first gate row
@@ -245,34 +294,43 @@ FLINT_DEV void gu_issue_routed(const MoEArgs& a, uint8_t* stage, GuInfo& inf, ui
     mbar_arrive_expect_tx(full, 32u * (kst / 2) + 32u * sfp);
   }
   __syncwarp();
-  const size_t row = lane < 16 ? g0 + lane : u0 + (lane - 16);
-  bulk_g2s(stage + lane * pitch, a.w13 + row * (H / 2) + k0 / 2, kst / 2, full);
-  if (kst == H) {  // whole rows: the 16 scale rows of gate (up) are contiguous
-    if (lane == 0) bulk_g2s(stage + sf_off, a.w13_sf + g0 * (H / 16), 16u * sfp, full);
-    if (lane == 1) bulk_g2s(stage + sf_off + 16 * sfp, a.w13_sf + u0 * (H / 16), 16u * sfp, full);
-  } else {
+  if (whole) {  // four copies: gate codes, up codes, gate scales, up scales
+    if (lane == 0) bulk_g2s(stage, a.w13 + g0 * (H / 2), 16u * (H / 2), full);
+    if (lane == 1) bulk_g2s(stage + 16 * pitch, a.w13 + u0 * (H / 2), 16u * (H / 2), full);
+    if (lane == 2) bulk_g2s(stage + sf_off, a.w13_sf + g0 * (H / 16), 16u * sfp, full);
+    if (lane == 3) bulk_g2s(stage + sf_off + 16 * sfp, a.w13_sf + u0 * (H / 16), 16u * sfp, full);
+  } else {  // a K chunk of each row, rows padded against bank conflicts
+    const size_t row = lane < 16 ? g0 + lane : u0 + (lane - 16);
+    bulk_g2s(stage + lane * pitch, a.w13 + row * (H / 2) + k0 / 2, kst / 2, full);
     bulk_g2s(stage + sf_off + lane * sfp, a.w13_sf + row * (H / 16) + k0 / 16, sfp, full);
   }
 }
 
+// NTG: token n-tiles held in registers at a time (1 when M <= 8).
+template <int NTG>
 __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
+  const GuLayout L = gu_layout(a.M);
+  const int S = L.stages;
   uint8_t* stages = smem;
-  float* red = reinterpret_cast<float*>(smem + size_t(kGuStages) * kGuStageBytes);
-  GuSmem& S = *reinterpret_cast<GuSmem*>(smem + size_t(kGuStages) * kGuStageBytes + kGuRedBytes);
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  GuSmem& SM = *reinterpret_cast<GuSmem*>(smem + L.ctl);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int H = a.H, I = a.I, SI = a.SI;
+  const int H = a.H, I = a.I, SI = a.SI, M = a.M;
+  const int ntmax = (M + 7) / 8;
   const int G = gridDim.x, c = blockIdx.x;
   int* status = a.ws.status;
-  volatile int* abort = &S.ctl.abort;
+  volatile int* abort = &SM.ctl.abort;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kGuStages; ++i) {
-      mbar_init(&S.ctl.full[i], 1);
-      mbar_init(&S.ctl.empty[i], kCons);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&SM.ctl.full[i], 1);
+      mbar_init(&SM.ctl.empty[i], kCons);
     }
-    S.ctl.abort = 0;
+    mbar_init(&SM.ctl.bar[0], kCons);
+    mbar_init(&SM.ctl.bar[1], kCons);
+    SM.ctl.abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -283,15 +341,16 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
     const int nS = SI / 8;
     for (int tile = c; tile < nS; tile += G) {
       for (int k0 = 0; k0 < H; k0 += kGuKst16) {
-        if (lane == 0) acquire_slot(S.ctl, n, kGuStages, abort, status);
-        __syncwarp();
-        const int sl = n % kGuStages;
-        gu_issue_shared(a, stages + (size_t)sl * kGuStageBytes, S.info[sl], &S.ctl.full[sl], tile,
-                        k0, lane);
+        int ok = 1;
+        if (lane == 0) ok = acquire_slot(SM.ctl, n, S, abort, status, 1);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        const int sl = n % S;
+        gu_issue_shared(a, stages + (size_t)sl * kGuStageBytes, SM.info[sl], &SM.ctl.full[sl],
+                        tile, k0, lane);
         ++n;
       }
     }
-    pdl_wait();  // router finished: routing metadata is final
+    pdl_wait();  // router finished: routing records are final
     pdl_launch_dependents();
     const int U = ldg_cg_i32(a.ws.uniq);
     const int tpe = I / 16;  // tiles per expert
@@ -301,46 +360,54 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
     short tok0 = 0, tok1 = 0;
     for (int tile = lo; tile < hi; ++tile) {
       const int u = tile / tpe, r0 = (tile % tpe) * 16;
-      if (u != cur_u) {  // tokens of the expert, read once per expert
-        e = ldg_cg_i32(a.ws.uniq + 1 + u);
-        cnt = ldg_cg_i32(a.ws.e_cnt + e);
-        off = ldg_cg_i32(a.ws.e_off + e);
-        tok0 = lane < cnt ? (short)(ldg_cg_i32(a.ws.sorted_pairs + off + lane) / a.k) : 0;
-        tok1 = lane + 32 < cnt ? (short)(ldg_cg_i32(a.ws.sorted_pairs + off + lane + 32) / a.k) : 0;
+      if (u != cur_u) {  // the expert's record: one round trip, lanes in parallel
+        const int* rec = a.ws.urec + (size_t)u * kUrecInts;
+        const int hdr = lane < 3 ? ldg_cg_i32(rec + lane) : 0;
+        const int p0 = ldg_cg_i32(rec + 4 + lane);
+        const int p1 = ldg_cg_i32(rec + 36 + lane);
+        e = __shfl_sync(0xffffffffu, hdr, 0);
+        cnt = __shfl_sync(0xffffffffu, hdr, 1);
+        off = __shfl_sync(0xffffffffu, hdr, 2);
+        tok0 = lane < cnt ? (short)(p0 / a.k) : 0;
+        tok1 = lane + 32 < cnt ? (short)(p1 / a.k) : 0;
         cur_u = u;
       }
       for (int k0 = 0; k0 < H; k0 += kGuKst4) {
-        if (lane == 0) acquire_slot(S.ctl, n, kGuStages, abort, status);
-        __syncwarp();
-        const int sl = n % kGuStages;
-        GuInfo& inf = S.info[sl];
+        int ok = 1;
+        if (lane == 0) ok = acquire_slot(SM.ctl, n, S, abort, status, 2);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        const int sl = n % S;
+        GuInfo& inf = SM.info[sl];
         inf.tok[lane] = tok0;
         inf.tok[lane + 32] = tok1;
         if (lane == 0) { inf.cnt = cnt; inf.off = off; }
         __syncwarp();  // info complete before the arrive that publishes it
-        gu_issue_routed(a, stages + (size_t)sl * kGuStageBytes, inf, &S.ctl.full[sl], e, r0, k0,
+        gu_issue_routed(a, stages + (size_t)sl * kGuStageBytes, inf, &SM.ctl.full[sl], e, r0, k0,
                         lane);
         ++n;
       }
     }
-    // end marker: a stage with no copies
+    // end marker: a stage with no copies (consumers that gave up have
+    // left already; the bounded waits keep this from blocking)
     if (lane == 0) {
-      acquire_slot(S.ctl, n, kGuStages, abort, status);
-      const int sl = n % kGuStages;
-      S.info[sl].kind = -1;
-      mbar_arrive(&S.ctl.full[sl]);
-      drain_slots(S.ctl, n, kGuStages, abort, status);
+      if (acquire_slot(SM.ctl, n, S, abort, status, 3)) {
+        const int sl = n % S;
+        SM.info[sl].kind = -1;
+        mbar_arrive(&SM.ctl.full[sl]);
+      }
+      drain_slots(SM.ctl, n, S, abort, status);
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
-  float acc[kNT][4];
   bool triggered = false;
+  uint32_t bph0 = 0, bph1 = 0;
+  float4* myred = reinterpret_cast<float4*>(red) + (size_t)warp * ntmax * 32 + lane;
   for (int n = 0;; ++n) {
-    const int sl = n % kGuStages;
-    warp_wait_phase(&S.ctl.full[sl], (n / kGuStages) & 1, abort, status, lane);
-    const GuInfo& inf = S.info[sl];
+    const int sl = n % S;
+    if (!warp_wait_phase(&SM.ctl.full[sl], (n / S) & 1, abort, status, lane, 4, n)) break;
+    const GuInfo& inf = SM.info[sl];
     const int kind = inf.kind;
     if (kind != 0 && !triggered) {  // past the producer's dependency wait
       pdl_launch_dependents();
@@ -351,63 +418,74 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
     const int pitch = inf.pitch, cnt = inf.cnt;
     const int ntiles = (cnt + 7) / 8;
     const uint8_t* st = stages + (size_t)sl * kGuStageBytes;
-    if (first) {
-#pragma unroll
-      for (int i = 0; i < kNT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
-    }
-    // B rows of this lane (token column g of every n-tile)
-    const uint16_t* brow[kNT];
-#pragma unroll
-    for (int nt = 0; nt < kNT; ++nt) {
-      const int nn = nt * 8 + g;
-      brow[nt] = nullptr;
-      if (nn < cnt) brow[nt] = a.x + (size_t)(kind ? inf.tok[nn] : nn) * H + k0;
-    }
     const int nsl = kst / kSliceK;
+    // this warp's rows and K slices
+    int s0, sstep;
+    const uint8_t *rg, *rg8, *sg = nullptr, *sg8 = nullptr;
     if (kind == 1) {
-      const int at = warp & 1, kp = warp >> 1;
-      const uint8_t* rg = st + (8 * at + g) * pitch;
-      const uint8_t* rg8 = st + (16 + 8 * at + g) * pitch;
-      const uint8_t* sg = st + inf.sf_off + (8 * at + g) * inf.sf_pitch;
-      const uint8_t* sg8 = st + inf.sf_off + (16 + 8 * at + g) * inf.sf_pitch;
-      for (int s = kp; s < nsl; s += 4) {
-        uint32_t af[4][2][4];
-        frags_fp4(af, rg, rg8, sg, sg8, s, t);
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt)
-          if (nt < ntiles) mma_b(acc[nt], af, brow[nt] ? brow[nt] + s * kSliceK : nullptr, t, false);
-      }
+      const int at = warp & 1;
+      s0 = warp >> 1;
+      sstep = kKP;
+      rg = st + (8 * at + g) * pitch;
+      rg8 = st + (16 + 8 * at + g) * pitch;
+      sg = st + inf.sf_off + (8 * at + g) * inf.sf_pitch;
+      sg8 = st + inf.sf_off + (16 + 8 * at + g) * inf.sf_pitch;
     } else {
-      const uint8_t* rg = st + g * pitch;
-      const uint8_t* rg8 = st + (8 + g) * pitch;
-      for (int s = warp; s < nsl; s += kCons) {
-        uint32_t af[4][2][4];
-        frags_bf16(af, rg, rg8, s, t);
+      s0 = warp < 8 ? warp : nsl;
+      sstep = 8;
+      rg = st + g * pitch;
+      rg8 = st + (8 + g) * pitch;
+    }
+    for (int n0 = 0; n0 < ntiles; n0 += NTG) {
+      float acc[NTG][4];
+      const uint16_t* brow[NTG];
 #pragma unroll
-        for (int nt = 0; nt < kNT; ++nt)
-          if (nt < ntiles) mma_b(acc[nt], af, brow[nt] ? brow[nt] + s * kSliceK : nullptr, t, false);
+      for (int i = 0; i < NTG; ++i) {
+        acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+        const int nn = (n0 + i) * 8 + g;
+        brow[i] = nn < cnt ? a.x + (size_t)(kind ? inf.tok[nn] : nn) * H + k0 : nullptr;
+      }
+      for (int s = s0; s < nsl; s += sstep) {
+        // activations first: their load latency hides behind the dequant
+        uint4 xb[NTG][4];
+#pragma unroll
+        for (int i = 0; i < NTG; ++i)
+          load_b(xb[i], (n0 + i < ntiles && brow[i]) ? brow[i] + s * kSliceK : nullptr, t, false);
+        uint32_t af[4][2][4];
+        if (kind == 1) frags_fp4(af, rg, rg8, sg, sg8, s, t);
+        else frags_bf16(af, rg, rg8, s, t);
+#pragma unroll
+        for (int i = 0; i < NTG; ++i)
+          if (n0 + i < ntiles) mma_b(acc[i], af, xb[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < NTG; ++i) {
+        if (n0 + i < ntiles) {
+          float4* r = myred + (size_t)(n0 + i) * 32;
+          float4 v = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+          if (!first) {
+            const float4 o = *r;
+            v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+          }
+          *r = v;
+        }
       }
     }
     const int r0 = inf.r0, e = inf.e, off = inf.off;
     __syncwarp();
-    if (lane == 0) mbar_arrive(&S.ctl.empty[sl]);  // stage consumed
+    if (lane == 0) mbar_arrive(&SM.ctl.empty[sl]);  // stage consumed
     if (!last) continue;
 
-    // ---- tile epilogue: reduce the warps' partials (fixed order), write
-#pragma unroll
-    for (int nt = 0; nt < kNT; ++nt)
-      if (nt < ntiles)
-        *reinterpret_cast<float4*>(red + ((size_t)(warp * kNT + nt) * 32 + lane) * 4) =
-            make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-    named_bar(1, kCons * 32);
+    // ---- tile epilogue: sum the warps' partials (fixed order), write
+    warp_barrier(&SM.ctl.bar[0], bph0, abort, status, lane, 5);
+    const float4* red4 = reinterpret_cast<const float4*>(red);
     if (kind == 1) {
       const float gs = a.w13_gs[e] * 128.0f;  // 2^7 undoes the operand scaling
       for (int it = warp; it < 2 * ntiles; it += kCons) {
         const int at = it & 1, nt = it >> 1;
         float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int kp = 0; kp < 4; ++kp) {
-          const float4 p = *reinterpret_cast<const float4*>(
-              red + ((size_t)((at + 2 * kp) * kNT + nt) * 32 + lane) * 4);
+        for (int kp = 0; kp < kKP; ++kp) {
+          const float4 p = red4[((size_t)(at + 2 * kp) * ntmax + nt) * 32 + lane];
           v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
         }
 #pragma unroll
@@ -423,9 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
     } else {
       for (int nt = warp; nt < ntiles; nt += kCons) {
         float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int w = 0; w < kCons; ++w) {
-          const float4 p =
-              *reinterpret_cast<const float4*>(red + ((size_t)(w * kNT + nt) * 32 + lane) * 4);
+        for (int w = 0; w < 8; ++w) {
+          const float4 p = red4[((size_t)w * ntmax + nt) * 32 + lane];
           v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
         }
 #pragma unroll
@@ -440,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
         }
       }
     }
-    named_bar(1, kCons * 32);  // red free for the next tile
+    warp_barrier(&SM.ctl.bar[1], bph1, abort, status, lane, 6);  // red free again
   }
   if (!triggered) pdl_launch_dependents();
 }
@@ -450,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
 // blocks: the shared expert's 16 rows (BF16, SI <= 1024 K) and, per routed
 // expert u < U, its 16 rows of w2 (NVFP4, I <= 2048 K) with their scales,
 // packed in order into stages of up to 8 blocks.  Work items are (block,
-// 8-token n-tile); warp w takes items w, w + 8, ... of a stage and runs the
+// 8-token n-tile); warp w takes items w, w + 16, ... of a stage and runs the
 // whole K of its item, so no cross-warp reduction is needed.  Results go to
 // smem: y (bf16, per pair t * k + j) and ys (bf16, per token); after the last
 // stage the CTA forms out = bf16(bf16(sum_j tw_j y_j) + ys) for its rows.
@@ -472,10 +549,10 @@ __host__ __device__ inline DnLayout dn_layout(int M, int k) {
   return L;
 }
 
-size_t dn_smem_bytes(const flint_moe_shape& s) { return dn_layout(s.M, s.top_k).total; }
-
+// Weight rows of a block sit unpadded in smem (16 consecutive rows are one
+// contiguous block in global memory, so one copy brings them in).
 FLINT_DEV int dn_block_bytes(int kind, int I, int SI) {
-  return kind ? 16 * (I / 2 + kPad) + I : 16 * (2 * SI + kPad);
+  return kind ? 16 * (I / 2) + I : 16 * (2 * SI);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
@@ -484,20 +561,21 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
   const DnLayout L = dn_layout(a.M, a.k);
   uint16_t* ysm = reinterpret_cast<uint16_t*>(smem + L.y);
   uint16_t* yss = reinterpret_cast<uint16_t*>(smem + L.ys);
-  DnSmem& S = *reinterpret_cast<DnSmem*>(smem + L.ctl);
+  DnSmem& SM = *reinterpret_cast<DnSmem*>(smem + L.ctl);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int H = a.H, I = a.I, SI = a.SI, k = a.k, M = a.M;
   const int h0 = blockIdx.x * 16;
   int* status = a.ws.status;
-  volatile int* abort = &S.ctl.abort;
+  volatile int* abort = &SM.ctl.abort;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDnStages; ++i) {
-      mbar_init(&S.ctl.full[i], 1);
-      mbar_init(&S.ctl.empty[i], kCons);
+      mbar_init(&SM.ctl.full[i], 1);
+      mbar_init(&SM.ctl.empty[i], kCons);
     }
-    S.ctl.abort = 0;
+    mbar_init(&SM.ctl.bar[0], kCons + 1);
+    SM.ctl.abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -505,86 +583,131 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
   if (warp == kCons) {
     // ------------------------------------------------------------ producer
     // The gate/up grid released this grid only after its own dependency
-    // wait, which follows the router's completion: the metadata is final.
+    // wait, which follows the router's completion: the records are final.
     const int U = ldg_cg_i32(a.ws.uniq);
-    const int nunits = U + (SI > 0 ? 1 : 0);
-    int n = 0, unit = 0;
-    while (unit < nunits) {
-      if (lane == 0) acquire_slot(S.ctl, n, kDnStages, abort, status);
+    const int nsh = SI > 0 ? 1 : 0;
+    const int nunits = U + nsh;
+    int n = 0, unit = 0, pend = 0;  // stages [pend, n) still need their activations
+    bool waited = false;
+    // Activation rows of a stage: copied once the gate/up grid has finished,
+    // then the producer's arrival completes the stage.
+    auto finish = [&](int m) {
+      const int sl = m % kDnStages;
+      const DnInfo& inf = SM.info[sl];
+      uint8_t* st = stages + (size_t)sl * kDnStageBytes;
+      if (lane == 0) mbar_expect_tx(&SM.ctl.full[sl], (uint32_t)inf.abytes);
       __syncwarp();
+      for (int bi = lane; bi < inf.nblocks; bi += 32) {
+        const DnBlock& b = inf.blk[bi];
+        if (b.act_smem < 0) continue;
+        if (b.kind == 0)
+          bulk_g2s(st + b.act_smem, a.ws.sact, (uint32_t)M * SI * 2, &SM.ctl.full[sl]);
+        else
+          bulk_g2s(st + b.act_smem, a.ws.act + (size_t)b.off * I, (uint32_t)b.cnt * I * 2,
+                   &SM.ctl.full[sl]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&SM.ctl.full[sl]);
+    };
+    while (unit < nunits) {
+      int ok = 1;
+      if (lane == 0) ok = acquire_slot(SM.ctl, n, kDnStages, abort, status, 11);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       const int sl = n % kDnStages;
       uint8_t* st = stages + (size_t)sl * kDnStageBytes;
-      DnInfo& inf = S.info[sl];
+      DnInfo& inf = SM.info[sl];
+      // headers of the next (up to) 32 routed units, one per lane
+      const int ul = unit - nsh + lane;
+      int hdr_e = 0, hdr_c = 0, hdr_o = 0;
+      if (ul >= 0 && ul < U) {
+        const int* rec = a.ws.urec + (size_t)ul * kUrecInts;
+        hdr_e = ldg_cg_i32(rec);
+        hdr_c = ldg_cg_i32(rec + 1);
+        hdr_o = ldg_cg_i32(rec + 2);
+      }
       int used = 0, nb = 0, ni = 0;
-      uint32_t bytes = 0;
-      // plan the stage (all lanes compute the same plan)
-      int first_unit = unit;
-      while (unit < nunits && nb < kDnMaxBlocks) {
-        const bool shared = SI > 0 && unit == 0;
-        const int bb = dn_block_bytes(shared ? 0 : 1, I, SI);
-        if (used + bb > kDnStageBytes) break;
-        int e = -1, cnt = M, off = 0;
-        if (!shared) {
-          e = ldg_cg_i32(a.ws.uniq + 1 + (unit - (SI > 0 ? 1 : 0)));
-          cnt = ldg_cg_i32(a.ws.e_cnt + e);
-          off = ldg_cg_i32(a.ws.e_off + e);
-        }
+      uint32_t wbytes = 0, abytes = 0;
+      const int first_unit = unit;
+      while (unit < nunits && nb < kDnMaxBlocks) {  // same plan in every lane
+        const bool shared = nsh && unit == 0;
+        const int wb = dn_block_bytes(shared ? 0 : 1, I, SI);
+        const int src = unit - first_unit;  // lane holding this unit's header
+        const int e = __shfl_sync(0xffffffffu, hdr_e, src);
+        const int cnt = shared ? M : __shfl_sync(0xffffffffu, hdr_c, src);
+        const int off = __shfl_sync(0xffffffffu, hdr_o, src);
+        const int ab = cnt * (shared ? SI : I) * 2;
+        int act_at = -1;
+        if (used + wb + ab <= kDnStageBytes) act_at = used + wb;
+        else if (nb > 0 || used + wb > kDnStageBytes) break;
         const int nit = (cnt + 7) / 8;
         if (ni + nit > kDnMaxItems) break;
         DnBlock& b = inf.blk[nb];
         if (lane == 0) {
-          b.kind = shared ? 0 : 1; b.e = e; b.cnt = cnt; b.off = off; b.smem = used;
-          b.pitch = shared ? 2 * SI + kPad : I / 2 + kPad;
+          b.kind = shared ? 0 : 1; b.e = shared ? -1 : e; b.u = unit - nsh;
+          b.cnt = cnt; b.off = off; b.smem = used;
+          b.pitch = shared ? 2 * SI : I / 2;
+          b.act_smem = act_at;
           for (int i = 0; i < nit; ++i) {
             inf.item_blk[ni + i] = (unsigned char)nb;
             inf.item_nt[ni + i] = (unsigned char)i;
           }
         }
-        if (!shared) {
-          if (lane < cnt) b.pair[lane] = (short)ldg_cg_i32(a.ws.sorted_pairs + off + lane);
-          if (lane + 32 < cnt) b.pair[lane + 32] = (short)ldg_cg_i32(a.ws.sorted_pairs + off + lane + 32);
-          bytes += 16u * (I / 2) + 16u * (I / 16);
-        } else {
-          bytes += 16u * 2u * SI;
-        }
-        used += bb;
+        wbytes += shared ? 16u * 2u * SI : 16u * (I / 2) + 16u * (I / 16);
+        if (act_at >= 0) abytes += ab;
+        used += wb + (act_at >= 0 ? ab : 0);
         ++nb;
         ni += nit;
         ++unit;
       }
-      if (lane == 0) { inf.nblocks = nb; inf.nitems = ni; }
+      if (nb == 0) {  // cannot happen for supported shapes; never spin on it
+        if (lane == 0) { *abort = 1; record_timeout(status, 12, n); }
+        break;
+      }
+      if (lane == 0) {
+        inf.nblocks = nb; inf.nitems = ni; inf.abytes = (int)abytes;
+        mbar_expect_tx(&SM.ctl.full[sl], wbytes);
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&S.ctl.full[sl], bytes);
-      __syncwarp();
-      // issue the copies of every block of the stage
-      for (int bi = 0; bi < nb; ++bi) {
-        const int u = first_unit + bi;
-        const bool shared = SI > 0 && u == 0;
+      for (int bi = 0; bi < nb; ++bi) {  // weights: known before the dependency wait
         const DnBlock& b = inf.blk[bi];
         uint8_t* dst = st + b.smem;
-        if (shared) {
-          if (lane < 16)
-            bulk_g2s(dst + lane * b.pitch, a.shared_down + (size_t)(h0 + lane) * SI, 2u * SI,
-                     &S.ctl.full[sl]);
+        if ((bi & 15) != (lane >> 1)) continue;  // two lanes per block
+        if (b.kind == 0) {
+          if (!(lane & 1))
+            bulk_g2s(dst, a.shared_down + (size_t)h0 * SI, 16u * 2u * SI, &SM.ctl.full[sl]);
         } else {
           const size_t row0 = (size_t)b.e * H + h0;
-          if (lane < 16)
-            bulk_g2s(dst + lane * b.pitch, a.w2 + (row0 + lane) * (I / 2), I / 2, &S.ctl.full[sl]);
-          if (lane == 16)
-            bulk_g2s(dst + 16 * b.pitch, a.w2_sf + row0 * (I / 16), 16u * (I / 16), &S.ctl.full[sl]);
+          if (!(lane & 1)) bulk_g2s(dst, a.w2 + row0 * (I / 2), 16u * (I / 2), &SM.ctl.full[sl]);
+          else bulk_g2s(dst + 16 * b.pitch, a.w2_sf + row0 * (I / 16), 16u * (I / 16), &SM.ctl.full[sl]);
         }
       }
       ++n;
+      if (waited) {
+        finish(n - 1);
+        pend = n;
+      } else if (n - pend == kDnStages || unit >= nunits) {
+        pdl_wait();  // gate/up finished: act and sact are complete
+        fence_proxy_async_global();
+        waited = true;
+        for (; pend < n; ++pend) finish(pend);
+      }
+    }
+    if (!waited) {  // nothing was planned (or the ring gave up): keep the order
+      pdl_wait();
+      waited = true;
+      for (; pend < n; ++pend) finish(pend);
     }
     if (lane == 0) {
-      acquire_slot(S.ctl, n, kDnStages, abort, status);
-      const int sl = n % kDnStages;
-      S.info[sl].nblocks = 0;
-      mbar_arrive(&S.ctl.full[sl]);
-      drain_slots(S.ctl, n, kDnStages, abort, status);
+      if (acquire_slot(SM.ctl, n, kDnStages, abort, status, 13)) {
+        const int sl = n % kDnStages;
+        SM.info[sl].nblocks = 0;
+        mbar_arrive(&SM.ctl.full[sl]);
+      }
+      drain_slots(SM.ctl, n, kDnStages, abort, status);
     }
     // the combine below needs every consumer's results
-    named_bar(2, kThreads);
+    uint32_t ph = 0;
+    warp_barrier(&SM.ctl.bar[0], ph, abort, status, lane, 14);
     return;
   }
 
@@ -592,8 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
   pdl_wait();  // gate/up finished: act and sact are complete
   for (int n = 0;; ++n) {
     const int sl = n % kDnStages;
-    warp_wait_phase(&S.ctl.full[sl], (n / kDnStages) & 1, abort, status, lane);
-    const DnInfo& inf = S.info[sl];
+    if (!warp_wait_phase(&SM.ctl.full[sl], (n / kDnStages) & 1, abort, status, lane, 15, n)) break;
+    const DnInfo& inf = SM.info[sl];
     if (inf.nblocks == 0) break;
     const uint8_t* st = stages + (size_t)sl * kDnStageBytes;
     for (int it = warp; it < inf.nitems; it += kCons) {
@@ -603,31 +726,50 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
       const uint8_t* rg = st + b.smem + g * b.pitch;
       const uint8_t* rg8 = st + b.smem + (8 + g) * b.pitch;
       float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if (b.kind == 1) {
-        const uint16_t* brow = nn < b.cnt ? a.ws.act + (size_t)(b.off + nn) * I : nullptr;
-        const uint8_t* sg = st + b.smem + 16 * b.pitch + g * (I / 16);
-        const uint8_t* sg8 = sg + 8 * (I / 16);
-        for (int s = 0; s < I / kSliceK; ++s) {
-          uint32_t af[4][2][4];
-          frags_fp4(af, rg, rg8, sg, sg8, s, t);
-          mma_b(acc, af, brow ? brow + s * kSliceK : nullptr, t, true);
+      const bool routed = b.kind == 1;
+      const int K = routed ? I : SI;
+      const int ncnt = routed ? b.cnt : M;
+      // this lane's pair ids (routed), read early: used only at the end
+      int pr[2] = {0, 0};
+      if (routed) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int tok = nt * 8 + 2 * t + c;
+          if (tok < ncnt) pr[c] = ldg_cg_i32(a.ws.urec + (size_t)b.u * kUrecInts + 4 + tok);
         }
+      }
+      const uint16_t* brow = nullptr;  // global B row (activations not staged)
+      const uint8_t* bsm = nullptr;    // staged B row
+      if (nn < ncnt) {
+        if (b.act_smem >= 0) bsm = st + b.act_smem + (size_t)nn * K * 2;
+        else brow = routed ? a.ws.act + (size_t)(b.off + nn) * I : a.ws.sact + (size_t)nn * SI;
+      }
+      const uint8_t* sg = st + b.smem + 16 * b.pitch + g * (I / 16);
+      const uint8_t* sg8 = sg + 8 * (I / 16);
+      const int nsl = K / kSliceK;
+      for (int s = 0; s < nsl; ++s) {
+        uint4 xb[4];
+        if (bsm) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            xb[q] = *reinterpret_cast<const uint4*>(bsm + 2 * (s * kSliceK + 32 * t + 8 * q));
+        } else {
+          load_b(xb, brow ? brow + s * kSliceK : nullptr, t, true);
+        }
+        uint32_t af[4][2][4];
+        if (routed) frags_fp4(af, rg, rg8, sg, sg8, s, t);
+        else frags_bf16(af, rg, rg8, s, t);
+        mma_b(acc, af, xb);
+      }
+      if (routed) {
         const float gs2 = a.w2_gs[b.e] * 128.0f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int tok = nt * 8 + 2 * t + (i & 1);
-          if (tok < b.cnt) {
-            const int p = b.pair[tok];
-            ysm[(size_t)p * 16 + g + (i >> 1) * 8] = (uint16_t)f32_to_bf16_bits(acc[i] * gs2);
-          }
+          if (tok < ncnt)
+            ysm[(size_t)pr[i & 1] * 16 + g + (i >> 1) * 8] = (uint16_t)f32_to_bf16_bits(acc[i] * gs2);
         }
       } else {
-        const uint16_t* brow = nn < M ? a.ws.sact + (size_t)nn * SI : nullptr;
-        for (int s = 0; s < SI / kSliceK; ++s) {
-          uint32_t af[4][2][4];
-          frags_bf16(af, rg, rg8, s, t);
-          mma_b(acc, af, brow ? brow + s * kSliceK : nullptr, t, true);
-        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int tok = nt * 8 + 2 * t + (i & 1);
@@ -636,9 +778,11 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&S.ctl.empty[sl]);
+    if (lane == 0) mbar_arrive(&SM.ctl.empty[sl]);
   }
-  named_bar(2, kThreads);
+  uint32_t ph = 0;
+  warp_barrier(&SM.ctl.bar[0], ph, abort, status, lane, 16);
+  if (*abort) return;
 
   // ---- combine: out = bf16(bf16(sum_j tw_j y_j) + ys), j in rank order
   for (int idx = threadIdx.x; idx < M * 16; idx += kCons * 32) {
@@ -680,7 +824,8 @@ cudaError_t launch_ex(const void* fn, dim3 grid, size_t smem, void** args, cudaS
 bool decode2_supported(const flint_moe_shape& s) {
   return s.M <= kDecodeMaxTokens && s.M * s.top_k <= 1024 && s.I <= kGuKst4 &&
          s.SI <= kGuKst16 && (s.H <= kGuKst4 || s.H % 256 == 0) &&
-         dn_smem_bytes(s) <= 232448 && 16 * (s.I / 2 + kPad) + s.I <= kDnStageBytes;
+         dn_layout(s.M, s.top_k).total <= (size_t)kMaxSmem &&
+         gu_layout(s.M).stages >= 2 && 16 * (s.I / 2 + kPad) + s.I <= kDnStageBytes;
 }
 
 cudaError_t launch_decode2(const MoEArgs& a, cudaStream_t st) {
@@ -692,22 +837,26 @@ cudaError_t launch_decode2(const MoEArgs& a, cudaStream_t st) {
   if (!dc.attrs) {
     err = cudaDeviceGetAttribute(&dc.sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute((const void*)gate_up2_kernel,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGuSmemBytes);
+    err = cudaFuncSetAttribute((const void*)gate_up2_kernel<1>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute((const void*)gate_up2_kernel<2>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute((const void*)down2_kernel,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (err != cudaSuccess) return err;
     dc.attrs = true;
   }
-  const flint_moe_shape s{a.M, a.H, a.E, a.k, a.I, a.SI};
   MoEArgs aa = a;
   void* args[] = {&aa};
-  err = launch_route(a, true, st, false);
+  err = route_cluster_supported(a) ? launch_route_cluster(a, st) : launch_route(a, true, st, false);
   if (err != cudaSuccess) return err;
-  err = launch_ex((const void*)gate_up2_kernel, dim3(dc.sms), kGuSmemBytes, args, st, true);
+  const void* gu = a.M <= 8 ? (const void*)gate_up2_kernel<1> : (const void*)gate_up2_kernel<2>;
+  err = launch_ex(gu, dim3(dc.sms), gu_layout(a.M).total, args, st, true);
   if (err != cudaSuccess) return err;
-  return launch_ex((const void*)down2_kernel, dim3(a.H / 16), dn_smem_bytes(s), args, st, true);
+  return launch_ex((const void*)down2_kernel, dim3(a.H / 16), dn_layout(a.M, a.k).total, args, st,
+                   true);
 }
 
 }  // namespace flint

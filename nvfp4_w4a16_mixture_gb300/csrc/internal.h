@@ -33,6 +33,7 @@ struct WsLayout {
   size_t uniq;         // int32 [1 + E]: [0] = U (experts with >= 1 pair), then their ids
   size_t sorted_pairs; // int32 [M * k]: pair ids t*k+j, stable-sorted by expert
   size_t rowof;        // int32 [M * k]: sorted position of pair t*k+j
+  size_t urec;         // int32 [min(E, M * k), kUrecInts]: per routed expert (M <= 64)
   size_t gcnt;         // int32 [2, nchunks, E]: per-chunk counts and offsets (grouping)
   size_t act;          // bf16 [M * k, I]   row = sorted position of the pair
   size_t sact;         // bf16 [M, SI]
@@ -43,6 +44,10 @@ struct WsLayout {
 };
 
 constexpr int kRouteTokens = 8;  // tokens per router CTA
+// Record of the u-th routed expert (M <= kDecodeMaxTokens): [0] expert id,
+// [1] pairs routed to it, [2] sorted position of its first pair, [3] unused,
+// [4 ..] its pair ids t * k + j in sorted order.
+constexpr int kUrecInts = 4 + kDecodeMaxTokens;
 
 WsLayout ws_layout(const flint_moe_shape& s);
 
@@ -60,6 +65,7 @@ struct Ws {  // device pointers into one workspace
   int* uniq;
   int* sorted_pairs;
   int* rowof;
+  int* urec;
   int* gcnt;
   uint16_t* act;
   uint16_t* sact;
@@ -91,6 +97,9 @@ struct MoEArgs {
 // Launchers (return cudaSuccess or the launch error).  `pdl` launches the
 // kernel with programmatic stream serialisation.
 cudaError_t launch_route(const MoEArgs& a, bool build_meta, cudaStream_t st, bool pdl);
+// One-cluster router with the small-M grouping (plain launch); for M <= 16.
+bool route_cluster_supported(const MoEArgs& a);
+cudaError_t launch_route_cluster(const MoEArgs& a, cudaStream_t st);
 cudaError_t launch_decode_gate_up(const MoEArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_decode_down(const MoEArgs& a, cudaStream_t st, bool pdl);
 

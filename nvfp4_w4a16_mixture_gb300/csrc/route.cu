@@ -7,6 +7,8 @@
 // (token, slot) pairs by expert) is the token permutation the grouped path of
 // flint_moe consumes ("perm" of _combine_kernel); the decode path uses the
 // same grouping to stream each routed expert's weights once per call.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -58,7 +60,13 @@ __device__ void build_groups_small(const MoEArgs& a, const int* ids, int* rowof)
   for (int e = tid; e < E; e += nthr) {
     a.ws.e_cnt[e] = s_cnt[e];
     a.ws.e_off[e] = s_off[e];
-    if (s_cnt[e] > 0) a.ws.uniq[1 + s_uoff[e]] = e;
+    int* rec = a.ws.urec + (size_t)s_uoff[e] * kUrecInts;
+    if (s_cnt[e] > 0) {
+      a.ws.uniq[1 + s_uoff[e]] = e;
+      rec[0] = e;
+      rec[1] = s_cnt[e];
+      rec[2] = s_off[e];
+    }
     int c = s_off[e];
     for (int t = 0; t < M; ++t) {
       int j = s_pos[t][e];
@@ -66,11 +74,97 @@ __device__ void build_groups_small(const MoEArgs& a, const int* ids, int* rowof)
         int p = t * k + j;
         a.ws.sorted_pairs[c] = p;
         rowof[p] = c;
+        rec[4 + c - s_off[e]] = p;
         ++c;
       }
     }
   }
   if (tid == 0) { a.ws.e_off[E] = s_off[E]; a.ws.uniq[0] = s_uoff[E]; }
+}
+
+// ----------------------------------------------------------------------------
+// The fp32 router dot product of one token row with one router row in the
+// canonical order (see route_kernel); `wreg` holds the row's 16-byte chunks
+// when H <= 2048, else they are read from `wrow`.  Every lane returns the
+// butterfly result (lane 0's value is the one that is rounded to BF16).
+FLINT_DEV float router_dot(const uint16_t* xrow, const uint4 (&wreg)[8], const uint16_t* wrow,
+                           int H, int lane) {
+  const int nchunk = (H + 255) / 256;
+  float acc = 0.0f;
+  auto chunk = [&](const uint4& xv, const uint4& wv) {
+    const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
+    const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      acc = fmaf(__uint_as_float(xs[q] << 16), __uint_as_float(ws[q] << 16), acc);
+      acc = fmaf(__uint_as_float(xs[q] & 0xFFFF0000u), __uint_as_float(ws[q] & 0xFFFF0000u), acc);
+    }
+  };
+  if (H <= 2048) {
+    // every chunk's load is issued before the first product, so the loads
+    // overlap instead of costing one round trip each
+    uint4 xreg[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int h = 256 * c + 8 * lane;
+      xreg[c] = (c < nchunk && h < H) ? ldg_cg_v4(xrow + h) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      if (c < nchunk && 256 * c + 8 * lane < H) chunk(xreg[c], wreg[c]);
+  } else {
+    for (int c = 0; c < nchunk; ++c) {
+      const int h = 256 * c + 8 * lane;
+      if (h < H) chunk(ldg_cg_v4(xrow + h), ldg_nc_v4(wrow + h));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) acc = acc + __shfl_xor_sync(0xffffffffu, acc, o);
+  return acc;
+}
+
+FLINT_DEV void router_row_regs(uint4 (&wreg)[8], const uint16_t* wrow, int H, int lane, bool active) {
+  const int nchunk = (H + 255) / 256;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    int h = 256 * c + 8 * lane;
+    wreg[c] = (active && c < nchunk && h < H && H <= 2048) ? ldg_nc_v4(wrow + h) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// Top-k of one token by one warp from its E BF16 logit bit patterns
+// (get(e)): key = (order-preserving bf16 bits << 8) | (E - 1 - e), so the
+// maximum key is the largest logit and, among equal bit patterns, the lowest
+// expert index.  s = 1 / (1 + exp(-logit)) in fp32, summed in rank order;
+// lane j < k ends with the j-th expert and tw = bf16(s_j / (sum + 1e-20)).
+template <class Get>
+FLINT_DEV void topk_warp(Get get, int E, int k, int lane, int& out_e, float& out_w) {
+  int key[kMaxE / 32];
+#pragma unroll
+  for (int q = 0; q < kMaxE / 32; ++q) {
+    int ee = q * 32 + lane;
+    key[q] = -1;
+    if (ee < E) key[q] = (int)((ordered_bf16(get(ee)) << 8) | (uint32_t)(E - 1 - ee));
+  }
+  float sum = 0.0f, my_s = 0.0f;
+  int my_e = 0;
+  for (int j = 0; j < k; ++j) {
+    int lm = key[0];
+#pragma unroll
+    for (int q = 1; q < kMaxE / 32; ++q) lm = max(lm, key[q]);
+    const int best = __reduce_max_sync(0xffffffffu, lm);
+#pragma unroll
+    for (int q = 0; q < kMaxE / 32; ++q)
+      if (key[q] == best) key[q] = -1;
+    const uint32_t o = (uint32_t)best >> 8;
+    const uint32_t b16 = (o & 0x8000u) ? (o ^ 0x8000u) : (o ^ 0xFFFFu);
+    const float logit = bf16_bits_to_f32(b16);
+    const float s = __fdiv_rn(1.0f, 1.0f + expf(-logit));
+    sum = sum + s;  // rank order
+    if (lane == j) { my_s = s; my_e = E - 1 - (best & 0xFF); }
+  }
+  out_e = my_e;
+  out_w = round_bf16(__fdiv_rn(my_s, sum + 1e-20f));
 }
 
 // ----------------------------------------------------------------------------
@@ -95,47 +189,17 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(MoEArgs a, int 
   const int H = a.H, E = a.E, k = a.k;
   const int t0 = tb * kRouteTokens;
   const int nt = min(kRouteTokens, a.M - t0);
-  const int nchunk = (H + 255) / 256;
   const bool active = e < E;
   const uint16_t* wrow = a.router_w + (size_t)(active ? e : 0) * H;
 
   // router weights do not depend on earlier grids: fetch before the wait
   uint4 wreg[8];
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    int h = 256 * c + 8 * lane;
-    wreg[c] = (active && c < nchunk && h < H && H <= 2048) ? ldg_nc_v4(wrow + h) : make_uint4(0, 0, 0, 0);
-  }
+  router_row_regs(wreg, wrow, H, lane, active);
   pdl_wait();
 
   if (active) {
     for (int tt = 0; tt < nt; ++tt) {
-      const uint16_t* xrow = a.x + (size_t)(t0 + tt) * H;
-      float acc = 0.0f;
-      for (int c = 0; c < nchunk; ++c) {
-        int h = 256 * c + 8 * lane;
-        if (h < H) {
-          uint4 xv = ldg_cg_v4(xrow + h);
-          uint4 wv;
-          if (H <= 2048) {
-            wv = wreg[0];
-#pragma unroll
-            for (int cc = 1; cc < 8; ++cc)
-              if (cc == c) wv = wreg[cc];
-          } else {
-            wv = ldg_nc_v4(wrow + h);
-          }
-          const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-          const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            acc = fmaf(__uint_as_float(xs[q] << 16), __uint_as_float(ws[q] << 16), acc);
-            acc = fmaf(__uint_as_float(xs[q] & 0xFFFF0000u), __uint_as_float(ws[q] & 0xFFFF0000u), acc);
-          }
-        }
-      }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) acc = acc + __shfl_xor_sync(0xffffffffu, acc, o);
+      const float acc = router_dot(a.x + (size_t)(t0 + tt) * H, wreg, wrow, H, lane);
       if (lane == 0) a.ws.logits[(size_t)(t0 + tt) * E + e] = (uint16_t)f32_to_bf16_bits(acc);
     }
   }
@@ -155,37 +219,11 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(MoEArgs a, int 
 
   for (int tt = warp; tt < nt; tt += kRouteWarps) {
     const int t = t0 + tt;
-    // key = (order-preserving bf16 bits << 8) | (E - 1 - e): max key = largest
-    // logit, lowest expert index among equal bit patterns
-    int key[kMaxE / 32];
-#pragma unroll
-    for (int q = 0; q < kMaxE / 32; ++q) {
-      int ee = q * 32 + lane;
-      key[q] = -1;
-      if (ee < E) {
-        uint32_t b = ldg_cg_u16(a.ws.logits + (size_t)t * E + ee);
-        key[q] = (int)((ordered_bf16(b) << 8) | (uint32_t)(E - 1 - ee));
-      }
-    }
-    float sum = 0.0f, my_s = 0.0f;
-    int my_e = 0;
-    for (int j = 0; j < k; ++j) {
-      int lm = key[0];
-#pragma unroll
-      for (int q = 1; q < kMaxE / 32; ++q) lm = max(lm, key[q]);
-      const int best = __reduce_max_sync(0xffffffffu, lm);
-#pragma unroll
-      for (int q = 0; q < kMaxE / 32; ++q)
-        if (key[q] == best) key[q] = -1;
-      const uint32_t o = (uint32_t)best >> 8;
-      const uint32_t b16 = (o & 0x8000u) ? (o ^ 0x8000u) : (o ^ 0xFFFFu);
-      const float logit = bf16_bits_to_f32(b16);
-      const float s = __fdiv_rn(1.0f, 1.0f + expf(-logit));
-      sum = sum + s;  // rank order
-      if (lane == j) { my_s = s; my_e = E - 1 - (best & 0xFF); }
-    }
+    int my_e;
+    float w;
+    topk_warp([&](int ee) { return ldg_cg_u16(a.ws.logits + (size_t)t * E + ee); }, E, k, lane,
+              my_e, w);
     if (lane < k) {
-      const float w = round_bf16(__fdiv_rn(my_s, sum + 1e-20f));
       a.ws.ids[t * k + lane] = my_e;
       a.ws.tw[t * k + lane] = w;
       if (a.ids_out) a.ids_out[t * k + lane] = my_e;
@@ -329,6 +367,121 @@ static cudaError_t launch(const void* fn, dim3 grid, dim3 block, void** args, cu
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// ----------------------------------------------------------------------------
+// Router for few tokens (M <= kRcMaxTokens) as one cluster of kRcCtas CTAs:
+// warp w of CTA r computes the logits of experts r * kRcWarps + w (+ multiples
+// of kRcCtas * kRcWarps) for every token, with router_dot (the canonical
+// order, so ids match route_kernel bit for bit), and stores them into the
+// leader CTA's shared memory.  After the cluster barrier the leader runs the
+// top-k (warp per token) and the expert grouping from shared memory: per
+// expert a bit mask of its tokens, counts and offsets by a scan, a pair's
+// sorted position = its expert's offset + the number of earlier tokens in the
+// mask.  No global atomics and no re-reads of global results on the way.
+constexpr int kRcCtas = 8;
+constexpr int kRcWarps = 16;
+constexpr int kRcMaxTokens = 16;
+
+struct RcSmem {
+  uint16_t logit[kRcMaxTokens][kMaxE];
+  int ids[kRcMaxTokens][kMaxTopK];
+  unsigned long long mask[kMaxE];
+  int off[kMaxE + 1];
+  int uidx[kMaxE + 1];
+};
+
+__global__ void __cluster_dims__(kRcCtas, 1, 1) __launch_bounds__(kRcWarps * 32)
+    route_cluster_kernel(MoEArgs a) {
+  __shared__ RcSmem S;
+  pdl_launch_dependents();
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int H = a.H, E = a.E, k = a.k, M = a.M;
+  RcSmem* lead = cl.map_shared_rank(&S, 0);
+
+  for (int e = rank * kRcWarps + warp; e < E; e += kRcCtas * kRcWarps) {
+    const uint16_t* wrow = a.router_w + (size_t)e * H;
+    uint4 wreg[8];
+    router_row_regs(wreg, wrow, H, lane, true);
+    for (int t = 0; t < M; ++t) {
+      const float acc = router_dot(a.x + (size_t)t * H, wreg, wrow, H, lane);
+      if (lane == 0) lead->logit[t][e] = (uint16_t)f32_to_bf16_bits(acc);
+    }
+  }
+  cl.sync();  // every logit is in the leader's shared memory
+  if (rank != 0) return;
+
+  for (int e = tid; e < E; e += kRcWarps * 32) S.mask[e] = 0ull;
+  for (int t = warp; t < M; t += kRcWarps) {
+    int my_e;
+    float w;
+    topk_warp([&](int ee) { return (uint32_t)S.logit[t][ee]; }, E, k, lane, my_e, w);
+    if (lane < k) {
+      S.ids[t][lane] = my_e;
+      a.ws.ids[t * k + lane] = my_e;
+      a.ws.tw[t * k + lane] = w;
+      if (a.ids_out) a.ids_out[t * k + lane] = my_e;
+      if (a.tw_out) a.tw_out[t * k + lane] = w;
+    }
+  }
+  __syncthreads();
+  const int np = M * k;
+  for (int p = tid; p < np; p += kRcWarps * 32)
+    atomicOr(&S.mask[S.ids[p / k][p % k]], 1ull << (p / k));
+  __syncthreads();
+  if (warp == 0) {  // exclusive scans of counts and of "routed" flags
+    int run = 0, urun = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int c = e < E ? __popcll(S.mask[e]) : 0;
+      const int u = c > 0 ? 1 : 0;
+      int ic = c, iu = u;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int vc = __shfl_up_sync(0xffffffffu, ic, o);
+        const int vu = __shfl_up_sync(0xffffffffu, iu, o);
+        if (lane >= o) { ic += vc; iu += vu; }
+      }
+      if (e < E) { S.off[e] = run + ic - c; S.uidx[e] = urun + iu - u; }
+      run += __shfl_sync(0xffffffffu, ic, 31);
+      urun += __shfl_sync(0xffffffffu, iu, 31);
+    }
+    if (lane == 0) { S.off[E] = run; S.uidx[E] = urun; }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kRcWarps * 32) {
+    const int c = __popcll(S.mask[e]);
+    a.ws.e_cnt[e] = c;
+    a.ws.e_off[e] = S.off[e];
+    if (c > 0) {
+      a.ws.uniq[1 + S.uidx[e]] = e;
+      int* rec = a.ws.urec + (size_t)S.uidx[e] * kUrecInts;
+      rec[0] = e;
+      rec[1] = c;
+      rec[2] = S.off[e];
+    }
+  }
+  if (tid == 0) { a.ws.e_off[E] = S.off[E]; a.ws.uniq[0] = S.uidx[E]; }
+  for (int p = tid; p < np; p += kRcWarps * 32) {
+    const int t = p / k, e = S.ids[t][p % k];
+    const int r = __popcll(S.mask[e] & ((1ull << t) - 1ull));
+    const int pos = S.off[e] + r;
+    a.ws.sorted_pairs[pos] = p;
+    a.ws.rowof[p] = pos;
+    a.ws.urec[(size_t)S.uidx[e] * kUrecInts + 4 + r] = p;
+  }
+}
+
+bool route_cluster_supported(const MoEArgs& a) { return a.M <= kRcMaxTokens; }
+
+cudaError_t launch_route_cluster(const MoEArgs& a, cudaStream_t st) {
+  MoEArgs aa = a;
+  void* args[] = {&aa};
+  return launch((const void*)route_cluster_kernel, dim3(kRcCtas), dim3(kRcWarps * 32), args, st,
+                false);
 }
 
 cudaError_t launch_route(const MoEArgs& a, bool build_meta, cudaStream_t st, bool pdl) {

@@ -53,6 +53,10 @@ WsLayout ws_layout(const flint_moe_shape& s) {
   L.y = take(2 * np * H);
   L.ys = take(2 * M * H);
   L.mk_part = take(decode_mk_supported(s) ? decode_mk_part_bytes(s) : 16);
+  const bool grouped = M > (size_t)kDecodeMaxTokens;
+  L.x_perm = take(grouped ? 2 * np * H : 16);
+  L.st_table = take(grouped ? 16 * grouped_st_entries(s) : 16);
+  L.st_count = take(16);
   L.total = off;
   return L;
 }
@@ -80,6 +84,9 @@ Ws ws_pointers(void* base, const WsLayout& L) {
   w.ys = reinterpret_cast<uint16_t*>(b + L.ys);
   w.mk_ctr = reinterpret_cast<int*>(b + L.mk_ctr);
   w.mk_part = reinterpret_cast<float*>(b + L.mk_part);
+  w.x_perm = reinterpret_cast<uint16_t*>(b + L.x_perm);
+  w.st_table = reinterpret_cast<int*>(b + L.st_table);
+  w.st_count = reinterpret_cast<int*>(b + L.st_count);
   return w;
 }
 
@@ -152,6 +159,10 @@ int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13, c
   a.ws = ws_pointers(workspace, L);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
+  if (shape->M > kDecodeMaxTokens && grouped_supported(*shape)) {
+    if (launch_grouped(a, st) != cudaSuccess) return FLINT_ERR_CUDA;
+    return FLINT_OK;
+  }
   if (decode2_supported(*shape)) {
     if (launch_decode2(a, st) != cudaSuccess) return FLINT_ERR_CUDA;
     return FLINT_OK;

@@ -1,0 +1,597 @@
+// Grouped path for many tokens (M > 64): token permutation by expert,
+// grouped NVFP4 GEMMs on the tensor cores (tcgen05, TMEM accumulators), the
+// shared expert's BF16 GEMMs in the same launches, and the weighted combine.
+//
+// Page "vllm.models.flint.ops.moe": flint_moe for large M (per-expert
+// grouped GEMMs over the permuted tokens, then _combine_kernel), with the
+// module's Numerics rule: weights dequantised exactly (e2m1 x e4m3 block
+// scale), fp32 accumulation, the per-expert global scale on the
+// accumulator, act = bf16(silu(g) * u), y = bf16(acc * gs2),
+// out = bf16(bf16(sum_j tw_j y_j) + shared).
+//
+// Launches (chained with programmatic dependent launch):
+//   router + grouping (route.cu)  ->  plan  ->  gather  ->  GEMM1  ->  GEMM2  ->  combine
+// plan:    per expert, tiles of up to 256 of its sorted rows (token tiles).
+// gather:  x_perm[pos] = x[token of sorted pair pos] (so GEMM1 reads its A
+//          operand as plain 2-D TMA tiles).
+// GEMM1:   routed units (token tile, 32 intermediate rows): D = X W13^T over
+//          64 weight rows (32 gate + 32 up), epilogue SwiGLU -> act;
+//          shared units (256 tokens, 32 rows): BF16 weights, -> sact.
+// GEMM2:   routed units (token tile, 64 output rows): D = act W2^T, epilogue
+//          y = bf16(acc * gs2); shared units: sact Wsd^T -> ys.
+// combine: out[t] = bf16(bf16(sum_j tw_j y[row of (t, j)]) + ys[t]).
+//
+// GEMM kernel (persistent, one CTA per SM, 320 threads):
+//   warp 8: TMA producer (A tiles; the NVFP4 code tile or the BF16 B tile),
+//   warp 9: MMA issuer (one thread) and TMEM owner (512 columns: per
+//           128-token half four 128 x 64 fp32 accumulators, K block kb going
+//           to accumulator kb % 4, added in fp32 by the epilogue -- so the
+//           tensor core's own accumulation spans a quarter of the reduction;
+//           the shared expert's gate/up units take one 128-token half and
+//           eight accumulators, because its bf16(gS), bf16(uS) roundings feed
+//           every output of the token),
+//   warps 0..7: dequantise (threads 4r .. 4r + 3 own B row r: 16 codes each
+//           of a K block -> bf16 e2m1 * scale * 2^-7, exact, written in the
+//           128-byte swizzled K-major layout), then the epilogue (warps 0..3
+//           read half 0, warps 4..7 half 1; TMEM lane = token row).
+// Ring: 5 stages of {A 2 x 16 KB, B 8 KB, codes 2 KB}.  Every wait is
+// bounded (FLINT_ERR_TIMEOUT in the status word on expiry).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace flint {
+namespace {
+
+constexpr int kGWarps = 10;
+constexpr int kGThreads = kGWarps * 32;
+constexpr int kStages = 5;
+constexpr int kTile = 128 * 128;            // 128 rows x 64 bf16
+constexpr int kBRows = 64;                  // B rows (N) per unit
+constexpr int kParts = 4;                   // accumulators per 128-token half
+constexpr int kOffA = 0;                    // two A tiles
+constexpr int kOffB = 2 * kTile;            // kBRows B rows
+constexpr int kOffC = kOffB + kBRows * 128; // kBRows rows x 32 code bytes
+constexpr int kStageBytes = kOffC + kBRows * 32;  // 43008
+static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+constexpr int kTokTile = 256;
+constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;
+constexpr uint32_t kSuspendNs = 50000;
+constexpr int kStWords = 4;  // token-tile table entry: e, row0, row_end, unused
+
+struct GCtl {
+  uint64_t full_a[kStages];  // TMA bytes landed (count 1 + tx)
+  uint64_t full_b[kStages];  // dequantised B written (count 8 warps)
+  uint64_t empty[kStages];   // MMAs done with the stage (tcgen05.commit)
+  uint64_t acc_full;         // all MMAs of a unit done
+  uint64_t acc_empty;        // epilogue finished reading TMEM (count 8 warps)
+  uint32_t tmem;
+  int abort;
+};
+constexpr size_t kGSmem = (size_t)kStages * kStageBytes + sizeof(GCtl) + 1024;
+
+FLINT_DEV bool gwait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+  if (*abort) return false;
+  unsigned long long t0 = 0;
+  for (;;) {
+    if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
+    if (*abort) return false;
+    const unsigned long long now = globaltimer_ns();
+    if (t0 == 0) t0 = now;
+    if (now - t0 > kWaitNs) {
+      *abort = 1;
+      atomicCAS(status, 0, FLINT_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+FLINT_DEV bool gwait_warp(uint64_t* bar, uint32_t parity, volatile int* abort, int* status, int lane) {
+  int ok = 0;
+  if (lane == 0) ok = gwait(bar, parity, abort, status);
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+struct TMaps {
+  CUtensorMap a_routed;  // x_perm [np, H] (GEMM1) / act [np, I] (GEMM2), box {64, 128}
+  CUtensorMap a_shared;  // x [M, H] / sact [M, SI], box {64, 128}
+  CUtensorMap b_shared;  // shared_gu [2 SI, H] box {64, 32} / shared_down [H, SI] box {64, 64}
+  CUtensorMap codes;     // w13 [E 2I, H/2] bytes box {32, 32} / w2 [E H, I/2] box {32, 64}
+};
+
+// One unit of work, the same in every role.
+struct Unit {
+  int shared;   // 0 routed, 1 shared expert
+  int e;        // routed expert
+  int row0;     // first row of the token tile (sorted position / token)
+  int row_end;  // one past its last valid row
+  int nt;       // N tile
+  int K;        // reduction length
+  int halves;   // 128-row halves with valid rows (1 or 2)
+  int parts;    // accumulators per half (K block kb -> kb % parts)
+};
+
+template <int STAGE>
+FLINT_DEV Unit unit_of(const MoEArgs& a, int u, int R, int NT, int NTs) {
+  Unit x;
+  if (u < R) {
+    const int st = u / NT;
+    const int* ent = a.ws.st_table + (size_t)st * kStWords;
+    x.shared = 0;
+    x.e = ldg_cg_i32(ent);
+    x.row0 = ldg_cg_i32(ent + 1);
+    x.row_end = ldg_cg_i32(ent + 2);
+    x.nt = u % NT;
+    x.K = STAGE == 1 ? a.H : a.I;
+  } else {
+    const int v = u - R;
+    const int tile = STAGE == 1 ? 128 : kTokTile;  // shared gate/up: one half
+    x.shared = 1;
+    x.e = -1;
+    x.row0 = (v / NTs) * tile;
+    x.row_end = min(a.M, x.row0 + tile);
+    x.nt = v % NTs;
+    x.K = STAGE == 1 ? a.H : a.SI;
+  }
+  x.halves = (x.row_end - x.row0 > 128) ? 2 : 1;
+  x.parts = (x.shared && STAGE == 1) ? 2 * kParts : kParts;
+  return x;
+}
+
+// Dequantise quarter j of one K block of B row r (16 codes, their scale
+// byte) into the swizzled bf16 tile: values e2m1 * scale * 2^-7, exactly.
+FLINT_DEV void dequant_quarter(uint8_t* btile, int r, int j, const uint8_t* codes, uint32_t sc1) {
+  const uint32_t sc = bf16x2_bcast(e4m3x2_to_bf16x2_x2p119(sc1 & 0xFFu), 0);
+  const uint2 c0 = *reinterpret_cast<const uint2*>(codes);
+  const uint32_t w[2] = {c0.x, c0.y};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {  // word i: K 16 j + 8 i .. + 7
+    const int q = 2 * j + i;
+    const uint32_t p0 = bf16x2_mul(e2m1_pair(w[i], 0), sc);  // K 8q + 0, 8q + 4
+    const uint32_t p1 = bf16x2_mul(e2m1_pair(w[i], 1), sc);  // 1, 5
+    const uint32_t p2 = bf16x2_mul(e2m1_pair(w[i], 2), sc);  // 2, 6
+    const uint32_t p3 = bf16x2_mul(e2m1_pair(w[i], 3), sc);  // 3, 7
+    uint4 v;
+    v.x = __byte_perm(p0, p1, 0x5410);  // K 0, 1
+    v.y = __byte_perm(p2, p3, 0x5410);  // 2, 3
+    v.z = __byte_perm(p0, p1, 0x7632);  // 4, 5
+    v.w = __byte_perm(p2, p3, 0x7632);  // 6, 7
+    *reinterpret_cast<uint4*>(btile + tc::sw128_offset(r, 8 * q)) = v;
+  }
+}
+
+template <int STAGE>
+__global__ void __launch_bounds__(kGThreads, 1)
+    grouped_gemm_kernel(const MoEArgs a, const __grid_constant__ TMaps tm, int NT, int NTs,
+                        int n_shared_tiles) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  GCtl& C = *reinterpret_cast<GCtl*>(smem + (size_t)kStages * kStageBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* status = a.ws.status;
+  volatile int* abort = &C.abort;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&C.full_a[i], 1);
+      mbar_init(&C.full_b[i], 8);
+      mbar_init(&C.empty[i], 1);
+    }
+    mbar_init(&C.acc_full, 1);
+    mbar_init(&C.acc_empty, 8);
+    C.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) tc::tmem_alloc(&C.tmem, 512);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = C.tmem;
+
+  pdl_wait();  // routing, plan and the previous GEMM are complete
+  pdl_launch_dependents();
+  const int ST = ldg_cg_i32(a.ws.st_count);
+  const int R = ST * NT;
+  const int total = R + n_shared_tiles * NTs;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    int it = 0;
+    for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x) {
+      const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
+      const int nkb = x.K / 64;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int s = it % kStages;
+        int ok = 1;
+        if (it >= kStages) ok = gwait_warp(&C.empty[s], ((it / kStages) - 1) & 1, abort, status, lane);
+        if (!ok) break;
+        if (lane == 0) {
+          uint8_t* st = smem + (size_t)s * kStageBytes;
+          const CUtensorMap* ta = x.shared ? &tm.a_shared : &tm.a_routed;
+          uint32_t bytes = (uint32_t)x.halves * kTile;
+          if (x.shared) bytes += (uint32_t)kBRows * 128u;
+          else bytes += (uint32_t)kBRows * 32u;
+          mbar_arrive_expect_tx(&C.full_a[s], bytes);
+          tc::tma_load_2d(st + kOffA, ta, kb * 64, x.row0, &C.full_a[s]);
+          if (x.halves == 2) tc::tma_load_2d(st + kOffA + kTile, ta, kb * 64, x.row0 + 128, &C.full_a[s]);
+          if (x.shared) {
+            if (STAGE == 1) {  // 32 gate rows, then 32 up rows
+              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, 32 * x.nt, &C.full_a[s]);
+              tc::tma_load_2d(st + kOffB + 32 * 128, &tm.b_shared, kb * 64, a.SI + 32 * x.nt, &C.full_a[s]);
+            } else {
+              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, 64 * x.nt, &C.full_a[s]);
+            }
+          } else {
+            if (STAGE == 1) {
+              const int g0 = x.e * 2 * a.I + 32 * x.nt;
+              tc::tma_load_2d(st + kOffC, &tm.codes, kb * 32, g0, &C.full_a[s]);
+              tc::tma_load_2d(st + kOffC + 32 * 32, &tm.codes, kb * 32, g0 + a.I, &C.full_a[s]);
+            } else {
+              tc::tma_load_2d(st + kOffC, &tm.codes, kb * 32, x.e * a.H + 64 * x.nt, &C.full_a[s]);
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp == 9) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16(128, kBRows);
+      int it = 0, nu = 0;
+      for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x, ++nu) {
+        const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
+        const int nkb = x.K / 64;
+        if (nu > 0 && !gwait(&C.acc_empty, (nu - 1) & 1, abort, status)) break;
+        tc::fence_after_sync();
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t par = (it / kStages) & 1;
+          if (!gwait(&C.full_a[s], par, abort, status) || !gwait(&C.full_b[s], par, abort, status)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          uint8_t* st = smem + (size_t)s * kStageBytes;
+          const uint64_t db = tc::desc_sw128(st + kOffB);
+          const int p = kb % x.parts;  // K block kb accumulates into partial kb % parts
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            for (int h = 0; h < x.halves; ++h) {
+              const uint64_t da = tc::desc_sw128(st + kOffA + h * kTile);
+              tc::mma_bf16(tmem + 256 * h + kBRows * p, da + 2 * kk, db + 2 * kk, idesc,
+                           (kb >= x.parts) || (kk > 0));
+            }
+          }
+          tc::commit(&C.empty[s]);
+        }
+        if (!ok) break;
+        tc::commit(&C.acc_full);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------- dequant (B) and epilogue
+    const int r = threadIdx.x >> 2, jq = threadIdx.x & 3;  // B row, quarter of its K block
+    const int q = warp & 3, half = warp >> 2;
+    int it = 0, nu = 0;
+    for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x, ++nu) {
+      const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
+      const int nkb = x.K / 64;
+      // scale bytes of this row, 4 per K block, read ahead of use
+      const uint8_t* sfrow = nullptr;  // this thread's scale byte of each K block
+      if (!x.shared) {
+        if (STAGE == 1) {
+          const size_t row = (size_t)x.e * 2 * a.I + (r < 32 ? 32 * x.nt + r : a.I + 32 * x.nt + (r - 32));
+          sfrow = a.w13_sf + row * (a.H / 16) + jq;
+        } else {
+          sfrow = a.w2_sf + ((size_t)x.e * a.H + 64 * x.nt + r) * (a.I / 16) + jq;
+        }
+      }
+      uint32_t sc_next = sfrow ? (uint32_t)*sfrow : 0u;
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int s = it % kStages;
+        const uint32_t sc = sc_next;
+        if (sfrow && kb + 1 < nkb) sc_next = (uint32_t)sfrow[4 * (kb + 1)];
+        // the stage's previous MMAs are done (B area free), its codes landed
+        if (it >= kStages && !gwait_warp(&C.empty[s], ((it / kStages) - 1) & 1, abort, status, lane)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + (size_t)s * kStageBytes;
+        if (!x.shared) {
+          if (!gwait_warp(&C.full_a[s], (it / kStages) & 1, abort, status, lane)) {
+            ok = false;
+            break;
+          }
+          dequant_quarter(st + kOffB, r, jq, st + kOffC + r * 32 + 8 * jq, sc);
+          tc::fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&C.full_b[s]);
+      }
+      if (!ok) break;
+
+      // ---- epilogue: accumulator `half`, TMEM lanes 32 q .. 32 q + 31
+      if (!gwait_warp(&C.acc_full, nu & 1, abort, status, lane)) break;
+      tc::fence_after_sync();
+      const int row = x.row0 + 128 * half + 32 * q + lane;
+      const bool valid = half < x.halves && row < x.row_end;
+      const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + 256 * half;
+      if (half < x.halves) {
+        if (STAGE == 1) {
+          const int I = x.shared ? a.SI : a.I;
+          uint16_t* dst = (x.shared ? a.ws.sact : a.ws.act) + (size_t)row * I + 32 * x.nt;
+          const float gs = x.shared ? 1.0f : a.w13_gs[x.e] * 128.0f;
+          const int nparts = min(x.parts, x.K / 64);
+          {
+            const int c0 = 0;
+            uint32_t gv[32], uv[32], t2[32];
+            tc::tmem_ld32(tb, gv);       // gate rows, partial 0
+            tc::tmem_ld32(tb + 32, uv);  // up rows, partial 0
+            for (int p = 1; p < nparts; ++p) {
+              tc::tmem_ld32(tb + kBRows * p, t2);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) gv[i] = __float_as_uint(__uint_as_float(gv[i]) + __uint_as_float(t2[i]));
+              tc::tmem_ld32(tb + kBRows * p + 32, t2);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) uv[i] = __float_as_uint(__uint_as_float(uv[i]) + __uint_as_float(t2[i]));
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float v[2];
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const float gg = __uint_as_float(gv[i + j]), uu = __uint_as_float(uv[i + j]);
+                if (x.shared) {
+                  // stock BF16 SwiGLU: gS, uS rounded, silu(gS) = gS / (1 + exp(-gS))
+                  const float gS = round_bf16(gg), uS = round_bf16(uu);
+                  v[j] = __fdiv_rn(gS, 1.0f + expf(-gS)) * uS;
+                } else {
+                  v[j] = silu_approx(gg * gs) * (uu * gs);
+                }
+              }
+              pk[i / 2] = f32_to_bf16_bits(v[0]) | (f32_to_bf16_bits(v[1]) << 16);
+            }
+            if (valid) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                reinterpret_cast<uint4*>(dst + c0)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+        } else {
+          uint16_t* dst = (x.shared ? a.ws.ys : a.ws.y) + (size_t)row * a.H + kBRows * x.nt;
+          const float gs = x.shared ? 1.0f : a.w2_gs[x.e] * 128.0f;
+          const int nparts = min(x.parts, x.K / 64);
+          for (int c0 = 0; c0 < kBRows; c0 += 32) {
+            uint32_t v[32], t2[32];
+            tc::tmem_ld32(tb + c0, v);
+            for (int p = 1; p < nparts; ++p) {
+              tc::tmem_ld32(tb + kBRows * p + c0, t2);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(t2[i]));
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2)
+              pk[i / 2] = f32_to_bf16_bits(__uint_as_float(v[i]) * gs) |
+                          (f32_to_bf16_bits(__uint_as_float(v[i + 1]) * gs) << 16);
+            if (valid) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                reinterpret_cast<uint4*>(dst + c0)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&C.acc_empty);
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 9) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------- small kernels
+// Token tiles: per expert, ceil(cnt / 256) entries {e, row0, row_end}.
+__global__ void __launch_bounds__(256) plan_kernel(MoEArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ int s_n[kMaxE], s_start[kMaxE + 1];
+  const int E = a.E, tid = threadIdx.x;
+  for (int e = tid; e < E; e += blockDim.x) s_n[e] = (ldg_cg_i32(a.ws.e_cnt + e) + kTokTile - 1) / kTokTile;
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int e = 0; e < E; ++e) { s_start[e] = run; run += s_n[e]; }
+    s_start[E] = run;
+    a.ws.st_count[0] = run;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int off = ldg_cg_i32(a.ws.e_off + e), cnt = ldg_cg_i32(a.ws.e_cnt + e);
+    for (int i = 0; i < s_n[e]; ++i) {
+      int* ent = a.ws.st_table + (size_t)(s_start[e] + i) * kStWords;
+      ent[0] = e;
+      ent[1] = off + kTokTile * i;
+      ent[2] = off + cnt;
+      ent[3] = 0;
+    }
+  }
+}
+
+// x_perm[pos] = x[sorted_pairs[pos] / k], one warp per row.
+__global__ void __launch_bounds__(256) gather_kernel(MoEArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pos = blockIdx.x * 8 + warp;
+  if (pos >= a.M * a.k) return;
+  const int t = ldg_cg_i32(a.ws.sorted_pairs + pos) / a.k;
+  const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H);
+  uint4* dst = reinterpret_cast<uint4*>(a.ws.x_perm + (size_t)pos * a.H);
+  for (int i = lane; i < a.H / 8; i += 32) dst[i] = ldg_cg_v4(src + i);
+}
+
+// out[t, h..h+7] = bf16(bf16(sum_j tw_j y[row(t, j), h]) + ys[t, h]), j in rank order.
+__global__ void __launch_bounds__(256) combine_kernel(MoEArgs a) {
+  pdl_wait();
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int hv = a.H / 8;
+  if (idx >= (size_t)a.M * hv) return;
+  const int t = (int)(idx / hv), h = (int)(idx % hv) * 8;
+  float R[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int j = 0; j < a.k; ++j) {
+    const int p = t * a.k + j;
+    const float w = ldg_cg_f32(a.ws.tw + p);
+    const int row = ldg_cg_i32(a.ws.rowof + p);
+    const uint4 yv = ldg_cg_v4(a.ws.y + (size_t)row * a.H + h);
+    const uint32_t ys_[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      R[2 * i] = R[2 * i] + w * bf16_bits_to_f32(ys_[i] & 0xFFFFu);
+      R[2 * i + 1] = R[2 * i + 1] + w * bf16_bits_to_f32(ys_[i] >> 16);
+    }
+  }
+  uint32_t o[4];
+  uint4 sv = make_uint4(0, 0, 0, 0);
+  if (a.SI > 0) sv = ldg_cg_v4(a.ws.ys + (size_t)t * a.H + h);
+  const uint32_t s_[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = round_bf16(R[2 * i]) + bf16_bits_to_f32(s_[i] & 0xFFFFu);
+    const float hi = round_bf16(R[2 * i + 1]) + bf16_bits_to_f32(s_[i] >> 16);
+    o[i] = f32_to_bf16_bits(lo) | (f32_to_bf16_bits(hi) << 16);
+  }
+  *reinterpret_cast<uint4*>(a.out + (size_t)t * a.H + h) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool get_encoder() {
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      !fn)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// 2-D map over a row-major [rows, cols] matrix; bf16 tiles use the 128-byte
+// swizzle, byte (code) tiles none.
+bool make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t rows, uint64_t cols,
+              uint32_t box_cols, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * (bf16 ? 2 : 1)};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  bf16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, void** args,
+                       cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+struct GDev {
+  int sms = 0;
+  bool attrs = false;
+};
+GDev g_gdev[64];
+
+}  // namespace
+
+bool grouped_supported(const flint_moe_shape& s) {
+  // 32-row intermediate tiles of GEMM1, 64-row output tiles of GEMM2,
+  // 64-wide K blocks
+  return s.I % 128 == 0 && s.H % 128 == 0 && s.SI % 128 == 0;
+}
+
+size_t grouped_st_entries(const flint_moe_shape& s) {
+  return (size_t)s.M * s.top_k / kTokTile + s.E + 1;
+}
+
+cudaError_t launch_grouped(const MoEArgs& a, cudaStream_t st) {
+  if (!get_encoder()) return cudaErrorNotSupported;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  GDev& gd = g_gdev[dev];
+  if (!gd.attrs) {
+    err = cudaDeviceGetAttribute(&gd.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute((const void*)grouped_gemm_kernel<1>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute((const void*)grouped_gemm_kernel<2>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
+    if (err != cudaSuccess) return err;
+    gd.attrs = true;
+  }
+  const uint64_t np = (uint64_t)a.M * a.k;
+  const int H = a.H, I = a.I, SI = a.SI, E = a.E;
+  TMaps t1{}, t2{};
+  bool ok = make_map(&t1.a_routed, a.ws.x_perm, true, np, H, 64, 128) &&
+            make_map(&t1.a_shared, a.x, true, a.M, H, 64, 128) &&
+            make_map(&t1.codes, a.w13, false, (uint64_t)E * 2 * I, H / 2, 32, 32) &&
+            make_map(&t2.a_routed, a.ws.act, true, np, I, 64, 128) &&
+            make_map(&t2.codes, a.w2, false, (uint64_t)E * H, I / 2, 32, 64);
+  if (ok && SI > 0)
+    ok = make_map(&t1.b_shared, a.shared_gu, true, 2 * (uint64_t)SI, H, 64, 32) &&
+         make_map(&t2.a_shared, a.ws.sact, true, a.M, SI, 64, 128) &&
+         make_map(&t2.b_shared, a.shared_down, true, H, SI, 64, 64);
+  if (!ok) return cudaErrorInvalidValue;
+
+  err = launch_route(a, true, st, false);
+  if (err != cudaSuccess) return err;
+  MoEArgs aa = a;
+  void* args0[] = {&aa};
+  err = launch_pdl((const void*)plan_kernel, dim3(1), dim3(256), 0, args0, st);
+  if (err != cudaSuccess) return err;
+  err = launch_pdl((const void*)gather_kernel, dim3((unsigned)((np + 7) / 8)), dim3(256), 0, args0, st);
+  if (err != cudaSuccess) return err;
+  const int nsh1 = SI > 0 ? (a.M + 127) / 128 : 0;             // shared gate/up: 128 tokens
+  const int nsh2 = SI > 0 ? (a.M + kTokTile - 1) / kTokTile : 0;
+  int NT1 = I / 32, NTs1 = SI > 0 ? SI / 32 : 1, NT2 = H / kBRows, NTs2 = H / kBRows;
+  void* args1[] = {&aa, &t1, &NT1, &NTs1, (void*)&nsh1};
+  err = launch_pdl((const void*)grouped_gemm_kernel<1>, dim3(gd.sms), dim3(kGThreads), kGSmem, args1, st);
+  if (err != cudaSuccess) return err;
+  void* args2[] = {&aa, &t2, &NT2, &NTs2, (void*)&nsh2};
+  err = launch_pdl((const void*)grouped_gemm_kernel<2>, dim3(gd.sms), dim3(kGThreads), kGSmem, args2, st);
+  if (err != cudaSuccess) return err;
+  const size_t nthr = (size_t)a.M * (H / 8);
+  return launch_pdl((const void*)combine_kernel, dim3((unsigned)((nthr + 255) / 256)), dim3(256), 0,
+                    args0, st);
+}
+
+}  // namespace flint

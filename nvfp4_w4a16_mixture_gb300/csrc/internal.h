@@ -40,6 +40,9 @@ struct WsLayout {
   size_t y;            // bf16 [M * k, H]   row = sorted position of the pair
   size_t ys;           // bf16 [M, H]
   size_t mk_part;      // decode megakernel fp32 partial sums
+  size_t x_perm;       // bf16 [M * k, H]: token rows in sorted pair order (grouped path)
+  size_t st_table;     // int32 [entries, 4]: per-expert token tiles (grouped path)
+  size_t st_count;     // int32: number of token tiles
   size_t total;
 };
 
@@ -66,6 +69,9 @@ struct Ws {  // device pointers into one workspace
   int* sorted_pairs;
   int* rowof;
   int* urec;
+  uint16_t* x_perm;
+  int* st_table;
+  int* st_count;
   int* gcnt;
   uint16_t* act;
   uint16_t* sact;
@@ -102,6 +108,12 @@ bool route_cluster_supported(const MoEArgs& a);
 cudaError_t launch_route_cluster(const MoEArgs& a, cudaStream_t st);
 cudaError_t launch_decode_gate_up(const MoEArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_decode_down(const MoEArgs& a, cudaStream_t st, bool pdl);
+
+// Grouped path of many tokens (tcgen05 GEMMs): router + grouping, plan,
+// gather, GEMM1 (+ shared), GEMM2 (+ shared), combine.
+bool grouped_supported(const flint_moe_shape& s);
+size_t grouped_st_entries(const flint_moe_shape& s);
+cudaError_t launch_grouped(const MoEArgs& a, cudaStream_t st);
 
 // Decode path of few tokens: router, gate/up and down+combine kernels chained
 // with programmatic dependent launch (M <= kDecodeMaxTokens and the limits

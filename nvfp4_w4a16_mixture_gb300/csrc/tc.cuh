@@ -1,0 +1,110 @@
+// Blackwell tensor-core helpers (sm_103a): tcgen05 MMA with TMEM
+// accumulators, shared-memory matrix descriptors, 2-D TMA tiles.
+//
+// Operand layout used throughout: K-major tiles of R rows x 64 bf16 (128 B
+// per row), 128-byte swizzle -- the layout a 2-D TMA with
+// CU_TENSOR_MAP_SWIZZLE_128B and a {64, R} box writes: row r at r * 128 B,
+// its 16-byte chunk c stored at chunk position c ^ (r % 8); tiles start on a
+// 1024-byte boundary.
+#pragma once
+
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace flint {
+namespace tc {
+
+// ------------------------------------------------------------------- TMEM --
+// Allocate `ncols` (power of two >= 32) TMEM columns for this CTA; the base
+// address lands in *slot (shared memory).  Executed by one whole warp.
+FLINT_DEV void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_addr(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+FLINT_DEV void tmem_dealloc(uint32_t base, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(ncols)
+               : "memory");
+}
+
+FLINT_DEV void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+FLINT_DEV void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Generic-proxy shared-memory writes made visible to the async proxy (the
+// tensor core reads operands through it).
+FLINT_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// --------------------------------------------------------- descriptors --
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle.  Fields:
+// start address >> 4 (bits 0..13), leading byte offset >> 4 (16..29; unused
+// for swizzled K-major, 1), stride byte offset >> 4 (32..45; 1024 B between
+// 8-row groups), fixed 0b001 (46..48), base offset 0 (49..51), swizzle mode
+// 2 = 128 B (61..63).  Moving 16 elements (32 B) along K inside the 128-byte
+// row adds 2 to the start address field.
+FLINT_DEV uint64_t desc_sw128(const void* smem_tile) {
+  const uint64_t addr = (uint64_t)(smem_addr(smem_tile) & 0x3FFFFu) >> 4;
+  return addr | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: D fp32, A and B bf16, both K-major,
+// shape M x N (M = 64 or 128; N a multiple of 16 up to 256).
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one K = 16 step.  Issued by one thread.
+FLINT_DEV void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                        bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every MMA this thread issued before has completed.
+FLINT_DEV void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_addr(bar))
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (lane i of the
+// warp gets TMEM lane base + i); the warp may only touch lanes
+// 32 * (warp % 4) .. + 31.
+FLINT_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------------------- TMA --
+// 2-D tiled load of box {c0.., c1..} (c0 = innermost) into shared memory,
+// completion counted on `bar`.  c0 * element size must be a multiple of 16.
+FLINT_DEV void tma_load_2d(void* dst, const void* tmap, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Byte offset of element (r, k) (bf16, k < 64) inside a K-major 128-byte
+// swizzled tile.
+FLINT_DEV uint32_t sw128_offset(int r, int k) {
+  const uint32_t chunk = (uint32_t)(k >> 3) ^ (uint32_t)(r & 7);
+  return (uint32_t)r * 128u + chunk * 16u + (uint32_t)(k & 7) * 2u;
+}
+
+}  // namespace tc
+}  // namespace flint

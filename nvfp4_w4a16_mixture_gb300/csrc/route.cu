@@ -87,8 +87,12 @@ __device__ void build_groups_small(const MoEArgs& a, const int* ids, int* rowof)
 // canonical order (see route_kernel); `wreg` holds the row's 16-byte chunks
 // when H <= 2048, else they are read from `wrow`.  Every lane returns the
 // butterfly result (lane 0's value is the one that is rounded to BF16).
+template <bool XSMEM = false>
 FLINT_DEV float router_dot(const uint16_t* xrow, const uint4 (&wreg)[8], const uint16_t* wrow,
                            int H, int lane) {
+  auto xload = [&](int h) {
+    return XSMEM ? *reinterpret_cast<const uint4*>(xrow + h) : ldg_cg_v4(xrow + h);
+  };
   const int nchunk = (H + 255) / 256;
   float acc = 0.0f;
   auto chunk = [&](const uint4& xv, const uint4& wv) {
@@ -107,7 +111,7 @@ FLINT_DEV float router_dot(const uint16_t* xrow, const uint4 (&wreg)[8], const u
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const int h = 256 * c + 8 * lane;
-      xreg[c] = (c < nchunk && h < H) ? ldg_cg_v4(xrow + h) : make_uint4(0, 0, 0, 0);
+      xreg[c] = (c < nchunk && h < H) ? xload(h) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int c = 0; c < 8; ++c)
@@ -115,7 +119,7 @@ FLINT_DEV float router_dot(const uint16_t* xrow, const uint4 (&wreg)[8], const u
   } else {
     for (int c = 0; c < nchunk; ++c) {
       const int h = 256 * c + 8 * lane;
-      if (h < H) chunk(ldg_cg_v4(xrow + h), ldg_nc_v4(wrow + h));
+      if (h < H) chunk(xload(h), ldg_nc_v4(wrow + h));
     }
   }
 #pragma unroll
@@ -475,6 +479,59 @@ __global__ void __cluster_dims__(kRcCtas, 1, 1) __launch_bounds__(kRcWarps * 32)
   }
 }
 
+// ----------------------------------------------------------------------------
+// Router for many tokens: CTA b handles tokens 16 b .. 16 b + 15 with their
+// rows staged in shared memory; warp w computes the logits of experts w,
+// w + 16, ... for all 16 tokens (router row in registers, router_dot: the
+// canonical order, so ids match the other routers bit for bit), then warp w
+// runs the top-k of token 16 b + w from shared memory.  No cross-CTA step.
+constexpr int kRtTokens = 16;
+constexpr int kRtWarps = 16;
+
+__global__ void __launch_bounds__(kRtWarps * 32) route_tile_kernel(MoEArgs a) {
+  extern __shared__ __align__(16) uint8_t rt_smem[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(rt_smem);                  // [16][H]
+  uint16_t* lg = xs + (size_t)kRtTokens * a.H;                          // [16][E]
+  pdl_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = a.H, E = a.E, k = a.k;
+  const int t0 = blockIdx.x * kRtTokens;
+  const int nt = min(kRtTokens, a.M - t0);
+  pdl_wait();
+  {  // stage the token rows (16-byte vectors)
+    const int nv = nt * H / 8;
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t0 * H);
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) reinterpret_cast<uint4*>(xs)[i] = ldg_cg_v4(src + i);
+  }
+  __syncthreads();
+  for (int e = warp; e < E; e += kRtWarps) {
+    const uint16_t* wrow = a.router_w + (size_t)e * H;
+    uint4 wreg[8];
+    router_row_regs(wreg, wrow, H, lane, true);
+    for (int t = 0; t < nt; ++t) {
+      const float acc = router_dot<true>(xs + (size_t)t * H, wreg, wrow, H, lane);
+      if (lane == 0) lg[t * E + e] = (uint16_t)f32_to_bf16_bits(acc);
+    }
+  }
+  __syncthreads();
+  if (warp < nt) {
+    const int t = t0 + warp;
+    int my_e;
+    float w;
+    topk_warp([&](int ee) { return (uint32_t)lg[warp * E + ee]; }, E, k, lane, my_e, w);
+    if (lane < k) {
+      a.ws.ids[t * k + lane] = my_e;
+      a.ws.tw[t * k + lane] = w;
+      if (a.ids_out) a.ids_out[t * k + lane] = my_e;
+      if (a.tw_out) a.tw_out[t * k + lane] = w;
+    }
+  }
+}
+
+size_t route_tile_smem(const MoEArgs& a) {
+  return (size_t)kRtTokens * a.H * 2 + (size_t)kRtTokens * a.E * 2;
+}
+
 bool route_cluster_supported(const MoEArgs& a) { return a.M <= kRcMaxTokens; }
 
 cudaError_t launch_route_cluster(const MoEArgs& a, cudaStream_t st) {
@@ -490,8 +547,33 @@ cudaError_t launch_route(const MoEArgs& a, bool build_meta, cudaStream_t st, boo
   int meta_in_router = (build_meta && small) ? 1 : 0;
   MoEArgs aa = a;
   void* args[] = {&aa, &meta_in_router, &rowof};
-  dim3 grid((a.E + kRouteWarps - 1) / kRouteWarps, (a.M + kRouteTokens - 1) / kRouteTokens);
-  cudaError_t err = launch((const void*)route_kernel, grid, dim3(kRouteWarps * 32), args, st, pdl);
+  cudaError_t err;
+  if (!small && route_tile_smem(a) <= 200 * 1024) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+      err = cudaFuncSetAttribute((const void*)route_tile_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      if (err != cudaSuccess) return err;
+      attr_set[dev] = true;
+    }
+    void* targs[] = {&aa};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.M + kRtTokens - 1) / kRtTokens);
+    cfg.blockDim = dim3(kRtWarps * 32);
+    cfg.dynamicSmemBytes = route_tile_smem(a);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    err = cudaLaunchKernelExC(&cfg, (const void*)route_tile_kernel, targs);
+  } else {
+    dim3 grid((a.E + kRouteWarps - 1) / kRouteWarps, (a.M + kRouteTokens - 1) / kRouteTokens);
+    err = launch((const void*)route_kernel, grid, dim3(kRouteWarps * 32), args, st, pdl);
+  }
   if (err != cudaSuccess || !build_meta || small) return err;
 
   const int np = a.M * a.k;

@@ -36,7 +36,6 @@ WsLayout ws_layout(const flint_moe_shape& s) {
   L.status = take(16);
   L.glob_cnt = take(16);
   L.hblk_cnt = take(4 * (H / 16));
-  L.mk_ctr = take(decode_mk_ctr_bytes(s));
   L.tok_cnt = take(4 * ((M + kRouteTokens - 1) / kRouteTokens));
   L.logits = take(2 * M * E);
   L.ids = take(4 * np);
@@ -52,7 +51,6 @@ WsLayout ws_layout(const flint_moe_shape& s) {
   L.sact = take(2 * M * (SI > 0 ? SI : 1));
   L.y = take(2 * np * H);
   L.ys = take(2 * M * H);
-  L.mk_part = take(decode_mk_supported(s) ? decode_mk_part_bytes(s) : 16);
   const bool grouped = M > (size_t)kDecodeMaxTokens;
   L.x_perm = take(grouped ? 2 * np * H : 16);
   L.st_table = take(grouped ? 16 * grouped_st_entries(s) : 16);
@@ -82,8 +80,6 @@ Ws ws_pointers(void* base, const WsLayout& L) {
   w.sact = reinterpret_cast<uint16_t*>(b + L.sact);
   w.y = reinterpret_cast<uint16_t*>(b + L.y);
   w.ys = reinterpret_cast<uint16_t*>(b + L.ys);
-  w.mk_ctr = reinterpret_cast<int*>(b + L.mk_ctr);
-  w.mk_part = reinterpret_cast<float*>(b + L.mk_part);
   w.x_perm = reinterpret_cast<uint16_t*>(b + L.x_perm);
   w.st_table = reinterpret_cast<int*>(b + L.st_table);
   w.st_count = reinterpret_cast<int*>(b + L.st_count);
@@ -165,10 +161,6 @@ int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13, c
   }
   if (decode2_supported(*shape)) {
     if (launch_decode2(a, st) != cudaSuccess) return FLINT_ERR_CUDA;
-    return FLINT_OK;
-  }
-  if (decode_mk_supported(*shape)) {
-    if (launch_decode_mk(a, a.ws.mk_ctr, a.ws.mk_part, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
     return FLINT_OK;
   }
   if (launch_route(a, true, st, true) != cudaSuccess) return FLINT_ERR_CUDA;

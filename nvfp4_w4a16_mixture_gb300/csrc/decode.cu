@@ -1,5 +1,7 @@
-// Decode-path expert kernels (few tokens): NVFP4 gate/up + SiLU*up, and the
-// down projection with the weighted combine and the shared-expert add.
+// Fallback decode kernels (few tokens, M <= 64) for shapes outside the
+// main decode kernels' limits (decode2.cu: shared intermediate <= 1024,
+// expert intermediate <= 2048, M * top_k <= 1024): NVFP4 gate/up + SiLU*up,
+// and the down projection with the weighted combine and the shared-expert add.
 //
 // Page "vllm.models.flint.ops.moe": _gate_up_gemv_kernel
 // (act[p] = silu(x[t] Wg[e]^T) * (x[t] Wu[e]^T), global scale on the fp32

@@ -23,7 +23,6 @@ struct WsLayout {
   size_t status;       // int32[4]: [0] first error recorded by a kernel
   size_t glob_cnt;     // int32[4]: global last-arriver counters
   size_t hblk_cnt;     // int32[H / 16]: down/combine last-arriver counters
-  size_t mk_ctr;       // decode megakernel counters
   size_t tok_cnt;      // int32[ceil(M / kRouteTokens)]: router last-arriver counters
   size_t logits;       // bf16 [M, E]
   size_t ids;          // int32 [M, k]
@@ -39,7 +38,6 @@ struct WsLayout {
   size_t sact;         // bf16 [M, SI]
   size_t y;            // bf16 [M * k, H]   row = sorted position of the pair
   size_t ys;           // bf16 [M, H]
-  size_t mk_part;      // decode megakernel fp32 partial sums
   size_t x_perm;       // bf16 [M * k, H]: token rows in sorted pair order (grouped path)
   size_t st_table;     // int32 [entries, 4]: per-expert token tiles (grouped path)
   size_t st_count;     // int32: number of token tiles
@@ -59,7 +57,6 @@ struct Ws {  // device pointers into one workspace
   int* tok_cnt;
   int* glob_cnt;
   int* hblk_cnt;
-  int* mk_ctr;
   uint16_t* logits;
   int* ids;
   float* tw;
@@ -77,7 +74,6 @@ struct Ws {  // device pointers into one workspace
   uint16_t* sact;
   uint16_t* y;
   uint16_t* ys;
-  float* mk_part;
 };
 
 Ws ws_pointers(void* base, const WsLayout& L);
@@ -121,11 +117,6 @@ cudaError_t launch_grouped(const MoEArgs& a, cudaStream_t st);
 bool decode2_supported(const flint_moe_shape& s);
 cudaError_t launch_decode2(const MoEArgs& a, cudaStream_t st);
 
-// Decode megakernel (whole block in one persistent launch, M <= kDecodeMaxTokens).
-bool decode_mk_supported(const flint_moe_shape& s);
-size_t decode_mk_ctr_bytes(const flint_moe_shape& s);
-size_t decode_mk_part_bytes(const flint_moe_shape& s);
-cudaError_t launch_decode_mk(const MoEArgs& a, int* mk_ctr, float* mk_part, cudaStream_t st,
-                             bool pdl);
+
 
 }  // namespace flint

@@ -75,6 +75,8 @@ def problem(M, H, E, k, I, SI, seed=0, device="cuda", scale=None):
     (64, 256, 32, 8, 128, 128),   # 64 tokens: largest decode batch
     (65, 256, 32, 8, 128, 128),   # first grouped-path batch
     (300, 384, 24, 5, 256, 128),  # grouped path, ragged everything
+    (3, 256, 16, 4, 128, 1152),   # shared intermediate > 1024: fallback decode kernels
+    (2, 256, 8, 2, 2176, 128),    # expert intermediate > 2048: fallback decode kernels
 ])
 def test_parity_small_shapes(shape):
     x, layer = problem(*shape, seed=sum(shape), device="cpu")

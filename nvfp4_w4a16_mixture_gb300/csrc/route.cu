@@ -127,6 +127,41 @@ FLINT_DEV float router_dot(const uint16_t* xrow, const uint4 (&wreg)[8], const u
   return acc;
 }
 
+// router_dot for NT tokens at once from shared memory (H <= 2048): the same
+// per-token sequence of fmaf and the same butterfly, with the NT independent
+// chains interleaved so that they overlap in the pipeline.
+template <int NT>
+FLINT_DEV void router_dot_tile(float (&res)[NT], const uint16_t* xs0, int H, const uint4 (&wreg)[8],
+                               int lane) {
+  const int nchunk = (H + 255) / 256;
+  float acc[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) acc[j] = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int h = 256 * c + 8 * lane;
+    if (c < nchunk && h < H) {
+      const uint32_t ws[4] = {wreg[c].x, wreg[c].y, wreg[c].z, wreg[c].w};
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(xs0 + (size_t)j * H + h);
+        const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[j] = fmaf(__uint_as_float(xq[q] << 16), __uint_as_float(ws[q] << 16), acc[j]);
+          acc[j] = fmaf(__uint_as_float(xq[q] & 0xFFFF0000u), __uint_as_float(ws[q] & 0xFFFF0000u), acc[j]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) acc[j] = acc[j] + __shfl_xor_sync(0xffffffffu, acc[j], o);
+    res[j] = acc[j];
+  }
+}
+
 FLINT_DEV void router_row_regs(uint4 (&wreg)[8], const uint16_t* wrow, int H, int lane, bool active) {
   const int nchunk = (H + 255) / 256;
 #pragma unroll
@@ -508,9 +543,24 @@ __global__ void __launch_bounds__(kRtWarps * 32) route_tile_kernel(MoEArgs a) {
     const uint16_t* wrow = a.router_w + (size_t)e * H;
     uint4 wreg[8];
     router_row_regs(wreg, wrow, H, lane, true);
-    for (int t = 0; t < nt; ++t) {
-      const float acc = router_dot<true>(xs + (size_t)t * H, wreg, wrow, H, lane);
-      if (lane == 0) lg[t * E + e] = (uint16_t)f32_to_bf16_bits(acc);
+    if (H <= 2048) {
+      int t = 0;
+      for (; t + 4 <= nt; t += 4) {  // four tokens' chains interleaved
+        float r4[4];
+        router_dot_tile<4>(r4, xs + (size_t)t * H, H, wreg, lane);
+        if (lane == 0)
+          for (int j = 0; j < 4; ++j) lg[(t + j) * E + e] = (uint16_t)f32_to_bf16_bits(r4[j]);
+      }
+      for (; t < nt; ++t) {
+        float r1[1];
+        router_dot_tile<1>(r1, xs + (size_t)t * H, H, wreg, lane);
+        if (lane == 0) lg[t * E + e] = (uint16_t)f32_to_bf16_bits(r1[0]);
+      }
+    } else {
+      for (int t = 0; t < nt; ++t) {
+        const float acc = router_dot<true>(xs + (size_t)t * H, wreg, wrow, H, lane);
+        if (lane == 0) lg[t * E + e] = (uint16_t)f32_to_bf16_bits(acc);
+      }
     }
   }
   __syncthreads();

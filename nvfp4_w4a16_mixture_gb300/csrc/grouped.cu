@@ -14,27 +14,27 @@
 // plan:    per expert, tiles of up to 256 of its sorted rows (token tiles).
 // gather:  x_perm[pos] = x[token of sorted pair pos] (so GEMM1 reads its A
 //          operand as plain 2-D TMA tiles).
-// GEMM1:   routed units (token tile, 32 intermediate rows): D = X W13^T over
-//          64 weight rows (32 gate + 32 up), epilogue SwiGLU -> act;
-//          shared units (256 tokens, 32 rows): BF16 weights, -> sact.
-// GEMM2:   routed units (token tile, 64 output rows): D = act W2^T, epilogue
-//          y = bf16(acc * gs2); shared units: sact Wsd^T -> ys.
+// GEMM1:   routed units (token tile, 64 intermediate rows): D = X W13^T over
+//          128 weight rows (64 gate + 64 up), epilogue SwiGLU -> act;
+//          shared units (128 tokens, 32 rows): BF16 weights, -> sact.
+// GEMM2:   routed units (token tile, 128 output rows): D = act W2^T, epilogue
+//          y = bf16(acc * gs2); shared units likewise: sact Wsd^T -> ys.
 // combine: out[t] = bf16(bf16(sum_j tw_j y[row of (t, j)]) + ys[t]).
 //
 // GEMM kernel (persistent, one CTA per SM, 320 threads):
 //   warp 8: TMA producer (A tiles; the NVFP4 code tile or the BF16 B tile),
 //   warp 9: MMA issuer (one thread) and TMEM owner (512 columns: per
-//           128-token half four 128 x 64 fp32 accumulators, K block kb going
-//           to accumulator kb % 4, added in fp32 by the epilogue -- so the
-//           tensor core's own accumulation spans a quarter of the reduction;
-//           the shared expert's gate/up units take one 128-token half and
-//           eight accumulators, because its bf16(gS), bf16(uS) roundings feed
-//           every output of the token),
-//   warps 0..7: dequantise (threads 4r .. 4r + 3 own B row r: 16 codes each
+//           128-token half two 128 x 128 fp32 accumulators, K block kb going
+//           to accumulator kb % 2, added in fp32 by the epilogue -- so the
+//           tensor core's own accumulation spans half the reduction; the
+//           shared expert's gate/up units take one 128-token half, 64 weight
+//           rows and eight accumulators, because its bf16(gS), bf16(uS)
+//           roundings feed every output of the token),
+//   warps 0..7: dequantise (threads 2r, 2r + 1 own B row r: 32 codes each
 //           of a K block -> bf16 e2m1 * scale * 2^-7, exact, written in the
 //           128-byte swizzled K-major layout), then the epilogue (warps 0..3
 //           read half 0, warps 4..7 half 1; TMEM lane = token row).
-// Ring: 5 stages of {A 2 x 16 KB, B 8 KB, codes 2 KB}.  Every wait is
+// Ring: 4 stages of {A 2 x 16 KB, B 16 KB, codes 4 KB}.  Every wait is
 // bounded (FLINT_ERR_TIMEOUT in the status word on expiry).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -48,14 +48,13 @@ namespace {
 
 constexpr int kGWarps = 10;
 constexpr int kGThreads = kGWarps * 32;
-constexpr int kStages = 5;
+constexpr int kStages = 4;
 constexpr int kTile = 128 * 128;            // 128 rows x 64 bf16
-constexpr int kBRows = 64;                  // B rows (N) per unit
-constexpr int kParts = 4;                   // accumulators per 128-token half
+constexpr int kBRows = 128;                 // B rows (N) of a routed unit
 constexpr int kOffA = 0;                    // two A tiles
-constexpr int kOffB = 2 * kTile;            // kBRows B rows
+constexpr int kOffB = 2 * kTile;            // up to kBRows B rows
 constexpr int kOffC = kOffB + kBRows * 128; // kBRows rows x 32 code bytes
-constexpr int kStageBytes = kOffC + kBRows * 32;  // 43008
+constexpr int kStageBytes = kOffC + kBRows * 32;  // 53248
 static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
 constexpr int kTokTile = 256;
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;
@@ -97,8 +96,8 @@ FLINT_DEV bool gwait_warp(uint64_t* bar, uint32_t parity, volatile int* abort, i
 struct TMaps {
   CUtensorMap a_routed;  // x_perm [np, H] (GEMM1) / act [np, I] (GEMM2), box {64, 128}
   CUtensorMap a_shared;  // x [M, H] / sact [M, SI], box {64, 128}
-  CUtensorMap b_shared;  // shared_gu [2 SI, H] box {64, 32} / shared_down [H, SI] box {64, 64}
-  CUtensorMap codes;     // w13 [E 2I, H/2] bytes box {32, 32} / w2 [E H, I/2] box {32, 64}
+  CUtensorMap b_shared;  // shared_gu [2 SI, H] box {64, 32} / shared_down [H, SI] box {64, 128}
+  CUtensorMap codes;     // w13 [E 2I, H/2] bytes box {32, 64} / w2 [E H, I/2] box {32, 128}
 };
 
 // One unit of work, the same in every role.
@@ -111,6 +110,7 @@ struct Unit {
   int K;        // reduction length
   int halves;   // 128-row halves with valid rows (1 or 2)
   int parts;    // accumulators per half (K block kb -> kb % parts)
+  int n;        // B rows (MMA N)
 };
 
 template <int STAGE>
@@ -136,19 +136,22 @@ FLINT_DEV Unit unit_of(const MoEArgs& a, int u, int R, int NT, int NTs) {
     x.K = STAGE == 1 ? a.H : a.SI;
   }
   x.halves = (x.row_end - x.row0 > 128) ? 2 : 1;
-  x.parts = (x.shared && STAGE == 1) ? 2 * kParts : kParts;
+  const bool sgu = x.shared && STAGE == 1;
+  x.parts = sgu ? 8 : 2;
+  x.n = sgu ? 64 : kBRows;
   return x;
 }
 
-// Dequantise quarter j of one K block of B row r (16 codes, their scale
-// byte) into the swizzled bf16 tile: values e2m1 * scale * 2^-7, exactly.
-FLINT_DEV void dequant_quarter(uint8_t* btile, int r, int j, const uint8_t* codes, uint32_t sc1) {
-  const uint32_t sc = bf16x2_bcast(e4m3x2_to_bf16x2_x2p119(sc1 & 0xFFu), 0);
-  const uint2 c0 = *reinterpret_cast<const uint2*>(codes);
-  const uint32_t w[2] = {c0.x, c0.y};
+// Dequantise half j of one K block of B row r (32 codes, their 2 scale
+// bytes) into the swizzled bf16 tile: values e2m1 * scale * 2^-7, exactly.
+FLINT_DEV void dequant_half(uint8_t* btile, int r, int j, const uint8_t* codes, uint32_t sc2) {
+  const uint32_t s01 = e4m3x2_to_bf16x2_x2p119(sc2 & 0xFFFFu);
+  const uint4 c0 = *reinterpret_cast<const uint4*>(codes);
+  const uint32_t w[4] = {c0.x, c0.y, c0.z, c0.w};
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {  // word i: K 16 j + 8 i .. + 7
-    const int q = 2 * j + i;
+  for (int i = 0; i < 4; ++i) {  // word i: K 32 j + 8 i .. + 7, scale block i / 2
+    const int q = 4 * j + i;
+    const uint32_t sc = bf16x2_bcast(s01, i >> 1);
     const uint32_t p0 = bf16x2_mul(e2m1_pair(w[i], 0), sc);  // K 8q + 0, 8q + 4
     const uint32_t p1 = bf16x2_mul(e2m1_pair(w[i], 1), sc);  // 1, 5
     const uint32_t p2 = bf16x2_mul(e2m1_pair(w[i], 2), sc);  // 2, 6
@@ -211,8 +214,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
           uint8_t* st = smem + (size_t)s * kStageBytes;
           const CUtensorMap* ta = x.shared ? &tm.a_shared : &tm.a_routed;
           uint32_t bytes = (uint32_t)x.halves * kTile;
-          if (x.shared) bytes += (uint32_t)kBRows * 128u;
-          else bytes += (uint32_t)kBRows * 32u;
+          if (x.shared) bytes += (uint32_t)x.n * 128u;
+          else bytes += (uint32_t)x.n * 32u;
           mbar_arrive_expect_tx(&C.full_a[s], bytes);
           tc::tma_load_2d(st + kOffA, ta, kb * 64, x.row0, &C.full_a[s]);
           if (x.halves == 2) tc::tma_load_2d(st + kOffA + kTile, ta, kb * 64, x.row0 + 128, &C.full_a[s]);
@@ -221,15 +224,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
               tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, 32 * x.nt, &C.full_a[s]);
               tc::tma_load_2d(st + kOffB + 32 * 128, &tm.b_shared, kb * 64, a.SI + 32 * x.nt, &C.full_a[s]);
             } else {
-              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, 64 * x.nt, &C.full_a[s]);
+              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, 128 * x.nt, &C.full_a[s]);
             }
           } else {
-            if (STAGE == 1) {
-              const int g0 = x.e * 2 * a.I + 32 * x.nt;
+            if (STAGE == 1) {  // 64 gate rows, then 64 up rows
+              const int g0 = x.e * 2 * a.I + 64 * x.nt;
               tc::tma_load_2d(st + kOffC, &tm.codes, kb * 32, g0, &C.full_a[s]);
-              tc::tma_load_2d(st + kOffC + 32 * 32, &tm.codes, kb * 32, g0 + a.I, &C.full_a[s]);
+              tc::tma_load_2d(st + kOffC + 64 * 32, &tm.codes, kb * 32, g0 + a.I, &C.full_a[s]);
             } else {
-              tc::tma_load_2d(st + kOffC, &tm.codes, kb * 32, x.e * a.H + 64 * x.nt, &C.full_a[s]);
+              tc::tma_load_2d(st + kOffC, &tm.codes, kb * 32, x.e * a.H + 128 * x.nt, &C.full_a[s]);
             }
           }
         }
@@ -239,11 +242,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
   } else if (warp == 9) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = tc::idesc_bf16(128, kBRows);
       int it = 0, nu = 0;
       for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x, ++nu) {
         const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
         const int nkb = x.K / 64;
+        const uint32_t idesc = tc::idesc_bf16(128, x.n);
         if (nu > 0 && !gwait(&C.acc_empty, (nu - 1) & 1, abort, status)) break;
         tc::fence_after_sync();
         bool ok = true;
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           for (int kk = 0; kk < 4; ++kk) {
             for (int h = 0; h < x.halves; ++h) {
               const uint64_t da = tc::desc_sw128(st + kOffA + h * kTile);
-              tc::mma_bf16(tmem + 256 * h + kBRows * p, da + 2 * kk, db + 2 * kk, idesc,
+              tc::mma_bf16(tmem + 256 * h + x.n * p, da + 2 * kk, db + 2 * kk, idesc,
                            (kb >= x.parts) || (kk > 0));
             }
           }
@@ -275,28 +278,28 @@ __global__ void __launch_bounds__(kGThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------- dequant (B) and epilogue
-    const int r = threadIdx.x >> 2, jq = threadIdx.x & 3;  // B row, quarter of its K block
+    const int r = threadIdx.x >> 1, jh = threadIdx.x & 1;  // B row, half of its K block
     const int q = warp & 3, half = warp >> 2;
     int it = 0, nu = 0;
     for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x, ++nu) {
       const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
       const int nkb = x.K / 64;
       // scale bytes of this row, 4 per K block, read ahead of use
-      const uint8_t* sfrow = nullptr;  // this thread's scale byte of each K block
+      const uint8_t* sfrow = nullptr;  // this thread's 2 scale bytes of each K block
       if (!x.shared) {
         if (STAGE == 1) {
-          const size_t row = (size_t)x.e * 2 * a.I + (r < 32 ? 32 * x.nt + r : a.I + 32 * x.nt + (r - 32));
-          sfrow = a.w13_sf + row * (a.H / 16) + jq;
-        } else {
-          sfrow = a.w2_sf + ((size_t)x.e * a.H + 64 * x.nt + r) * (a.I / 16) + jq;
+          const size_t row = (size_t)x.e * 2 * a.I + (r < 64 ? 64 * x.nt + r : a.I + 64 * x.nt + (r - 64));
+          sfrow = a.w13_sf + row * (a.H / 16) + 2 * jh;
+        } else if (128 * x.nt + r < a.H) {  // rows past H (last tile) are not read
+          sfrow = a.w2_sf + ((size_t)x.e * a.H + 128 * x.nt + r) * (a.I / 16) + 2 * jh;
         }
       }
-      uint32_t sc_next = sfrow ? (uint32_t)*sfrow : 0u;
+      uint32_t sc_next = sfrow ? (uint32_t)*reinterpret_cast<const uint16_t*>(sfrow) : 0u;
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const int s = it % kStages;
         const uint32_t sc = sc_next;
-        if (sfrow && kb + 1 < nkb) sc_next = (uint32_t)sfrow[4 * (kb + 1)];
+        if (sfrow && kb + 1 < nkb) sc_next = (uint32_t)*reinterpret_cast<const uint16_t*>(sfrow + 4 * (kb + 1));
         // the stage's previous MMAs are done (B area free), its codes landed
         if (it >= kStages && !gwait_warp(&C.empty[s], ((it / kStages) - 1) & 1, abort, status, lane)) {
           ok = false;
@@ -308,7 +311,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             ok = false;
             break;
           }
-          dequant_quarter(st + kOffB, r, jq, st + kOffC + r * 32 + 8 * jq, sc);
+          dequant_half(st + kOffB, r, jh, st + kOffC + r * 32 + 16 * jh, sc);
           tc::fence_proxy_async_smem();
         }
         __syncwarp();
@@ -325,19 +328,19 @@ __global__ void __launch_bounds__(kGThreads, 1)
       if (half < x.halves) {
         if (STAGE == 1) {
           const int I = x.shared ? a.SI : a.I;
-          uint16_t* dst = (x.shared ? a.ws.sact : a.ws.act) + (size_t)row * I + 32 * x.nt;
+          const int hw = x.n / 2;  // intermediate rows of the unit: gate cols [0, hw), up [hw, n)
+          uint16_t* dst = (x.shared ? a.ws.sact : a.ws.act) + (size_t)row * I + hw * x.nt;
           const float gs = x.shared ? 1.0f : a.w13_gs[x.e] * 128.0f;
           const int nparts = min(x.parts, x.K / 64);
-          {
-            const int c0 = 0;
+          for (int c0 = 0; c0 < hw; c0 += 32) {
             uint32_t gv[32], uv[32], t2[32];
-            tc::tmem_ld32(tb, gv);       // gate rows, partial 0
-            tc::tmem_ld32(tb + 32, uv);  // up rows, partial 0
+            tc::tmem_ld32(tb + c0, gv);       // gate rows, partial 0
+            tc::tmem_ld32(tb + hw + c0, uv);  // up rows, partial 0
             for (int p = 1; p < nparts; ++p) {
-              tc::tmem_ld32(tb + kBRows * p, t2);
+              tc::tmem_ld32(tb + x.n * p + c0, t2);
 #pragma unroll
               for (int i = 0; i < 32; ++i) gv[i] = __float_as_uint(__uint_as_float(gv[i]) + __uint_as_float(t2[i]));
-              tc::tmem_ld32(tb + kBRows * p + 32, t2);
+              tc::tmem_ld32(tb + x.n * p + hw + c0, t2);
 #pragma unroll
               for (int i = 0; i < 32; ++i) uv[i] = __float_as_uint(__uint_as_float(uv[i]) + __uint_as_float(t2[i]));
             }
@@ -365,14 +368,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
             }
           }
         } else {
-          uint16_t* dst = (x.shared ? a.ws.ys : a.ws.y) + (size_t)row * a.H + kBRows * x.nt;
+          uint16_t* dst = (x.shared ? a.ws.ys : a.ws.y) + (size_t)row * a.H + x.n * x.nt;
           const float gs = x.shared ? 1.0f : a.w2_gs[x.e] * 128.0f;
           const int nparts = min(x.parts, x.K / 64);
-          for (int c0 = 0; c0 < kBRows; c0 += 32) {
+          const int ncols = min(x.n, a.H - x.n * x.nt);  // the last tile of H may be partial
+          for (int c0 = 0; c0 < x.n; c0 += 32) {
             uint32_t v[32], t2[32];
             tc::tmem_ld32(tb + c0, v);
             for (int p = 1; p < nparts; ++p) {
-              tc::tmem_ld32(tb + kBRows * p + c0, t2);
+              tc::tmem_ld32(tb + x.n * p + c0, t2);
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(t2[i]));
             }
@@ -381,7 +385,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             for (int i = 0; i < 32; i += 2)
               pk[i / 2] = f32_to_bf16_bits(__uint_as_float(v[i]) * gs) |
                           (f32_to_bf16_bits(__uint_as_float(v[i + 1]) * gs) << 16);
-            if (valid) {
+            if (valid && c0 < ncols) {
 #pragma unroll
               for (int i = 0; i < 4; ++i)
                 reinterpret_cast<uint4*>(dst + c0)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
@@ -563,13 +567,13 @@ cudaError_t launch_grouped(const MoEArgs& a, cudaStream_t st) {
   TMaps t1{}, t2{};
   bool ok = make_map(&t1.a_routed, a.ws.x_perm, true, np, H, 64, 128) &&
             make_map(&t1.a_shared, a.x, true, a.M, H, 64, 128) &&
-            make_map(&t1.codes, a.w13, false, (uint64_t)E * 2 * I, H / 2, 32, 32) &&
+            make_map(&t1.codes, a.w13, false, (uint64_t)E * 2 * I, H / 2, 32, 64) &&
             make_map(&t2.a_routed, a.ws.act, true, np, I, 64, 128) &&
-            make_map(&t2.codes, a.w2, false, (uint64_t)E * H, I / 2, 32, 64);
+            make_map(&t2.codes, a.w2, false, (uint64_t)E * H, I / 2, 32, 128);
   if (ok && SI > 0)
     ok = make_map(&t1.b_shared, a.shared_gu, true, 2 * (uint64_t)SI, H, 64, 32) &&
          make_map(&t2.a_shared, a.ws.sact, true, a.M, SI, 64, 128) &&
-         make_map(&t2.b_shared, a.shared_down, true, H, SI, 64, 64);
+         make_map(&t2.b_shared, a.shared_down, true, H, SI, 64, 128);
   if (!ok) return cudaErrorInvalidValue;
 
   err = launch_route(a, true, st, false);
@@ -582,7 +586,7 @@ cudaError_t launch_grouped(const MoEArgs& a, cudaStream_t st) {
   if (err != cudaSuccess) return err;
   const int nsh1 = SI > 0 ? (a.M + 127) / 128 : 0;             // shared gate/up: 128 tokens
   const int nsh2 = SI > 0 ? (a.M + kTokTile - 1) / kTokTile : 0;
-  int NT1 = I / 32, NTs1 = SI > 0 ? SI / 32 : 1, NT2 = H / kBRows, NTs2 = H / kBRows;
+  int NT1 = I / 64, NTs1 = SI > 0 ? SI / 32 : 1, NT2 = H / kBRows, NTs2 = H / kBRows;
   void* args1[] = {&aa, &t1, &NT1, &NTs1, (void*)&nsh1};
   err = launch_pdl((const void*)grouped_gemm_kernel<1>, dim3(gd.sms), dim3(kGThreads), kGSmem, args1, st);
   if (err != cudaSuccess) return err;

@@ -294,12 +294,20 @@ __global__ void __launch_bounds__(kGThreads, 1)
           sfrow = a.w2_sf + ((size_t)x.e * a.H + 128 * x.nt + r) * (a.I / 16) + 2 * jh;
         }
       }
-      uint32_t sc_next = sfrow ? (uint32_t)*reinterpret_cast<const uint16_t*>(sfrow) : 0u;
+      // scale bytes of the next four K blocks in flight (a global load takes
+      // longer than one K block's dequantisation)
+      auto sc_load = [&](int kb) {
+        return (sfrow && kb < nkb) ? (uint32_t)*reinterpret_cast<const uint16_t*>(sfrow + 4 * kb) : 0u;
+      };
+      uint32_t sc0 = sc_load(0), sc1 = sc_load(1), sc2 = sc_load(2), sc3 = sc_load(3);
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const int s = it % kStages;
-        const uint32_t sc = sc_next;
-        if (sfrow && kb + 1 < nkb) sc_next = (uint32_t)*reinterpret_cast<const uint16_t*>(sfrow + 4 * (kb + 1));
+        const uint32_t sc = sc0;
+        sc0 = sc1;
+        sc1 = sc2;
+        sc2 = sc3;
+        sc3 = sc_load(kb + 4);
         // the stage's previous MMAs are done (B area free), its codes landed
         if (it >= kStages && !gwait_warp(&C.empty[s], ((it / kStages) - 1) & 1, abort, status, lane)) {
           ok = false;
@@ -333,16 +341,23 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const float gs = x.shared ? 1.0f : a.w13_gs[x.e] * 128.0f;
           const int nparts = min(x.parts, x.K / 64);
           for (int c0 = 0; c0 < hw; c0 += 32) {
-            uint32_t gv[32], uv[32], t2[32];
-            tc::tmem_ld32(tb + c0, gv);       // gate rows, partial 0
-            tc::tmem_ld32(tb + hw + c0, uv);  // up rows, partial 0
-            for (int p = 1; p < nparts; ++p) {
-              tc::tmem_ld32(tb + x.n * p + c0, t2);
+            uint32_t gv[32], uv[32], t2[32], t3[32];
+            tc::tmem_ld32_async(tb + c0, gv);       // gate rows, partial 0
+            tc::tmem_ld32_async(tb + hw + c0, uv);  // up rows, partial 0
+            tc::tmem_wait_ld();
+            tc::tmem_regs_ready(gv);
+            tc::tmem_regs_ready(uv);
+            for (int p = 1; p < nparts; ++p) {  // each partial's gate and up together
+              tc::tmem_ld32_async(tb + x.n * p + c0, t2);
+              tc::tmem_ld32_async(tb + x.n * p + hw + c0, t3);
+              tc::tmem_wait_ld();
+              tc::tmem_regs_ready(t2);
+              tc::tmem_regs_ready(t3);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) gv[i] = __float_as_uint(__uint_as_float(gv[i]) + __uint_as_float(t2[i]));
-              tc::tmem_ld32(tb + x.n * p + hw + c0, t2);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) uv[i] = __float_as_uint(__uint_as_float(uv[i]) + __uint_as_float(t2[i]));
+              for (int i = 0; i < 32; ++i) {
+                gv[i] = __float_as_uint(__uint_as_float(gv[i]) + __uint_as_float(t2[i]));
+                uv[i] = __float_as_uint(__uint_as_float(uv[i]) + __uint_as_float(t3[i]));
+              }
             }
             uint32_t pk[16];
 #pragma unroll
@@ -374,9 +389,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const int ncols = min(x.n, a.H - x.n * x.nt);  // the last tile of H may be partial
           for (int c0 = 0; c0 < x.n; c0 += 32) {
             uint32_t v[32], t2[32];
-            tc::tmem_ld32(tb + c0, v);
+            tc::tmem_ld32_async(tb + c0, v);
+            if (nparts > 1) tc::tmem_ld32_async(tb + x.n + c0, t2);
+            tc::tmem_wait_ld();
+            tc::tmem_regs_ready(v);
+            tc::tmem_regs_ready(t2);
             for (int p = 1; p < nparts; ++p) {
-              tc::tmem_ld32(tb + x.n * p + c0, t2);
+              if (p > 1) tc::tmem_ld32(tb + x.n * p + c0, t2);
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(t2[i]));
             }

@@ -62,8 +62,9 @@ constexpr uint32_t kSuspendNs = 50000;
 constexpr int kStWords = 4;  // token-tile table entry: e, row0, row_end, unused
 
 struct GCtl {
-  uint64_t full_a[kStages];  // TMA bytes landed (count 1 + tx)
-  uint64_t full_b[kStages];  // dequantised B written (count 8 warps)
+  uint64_t full[kStages];    // stage ready for the MMA: A (and BF16 B) bytes landed
+                             // and the 8 dequantising warps done (count 1 + 8, + tx)
+  uint64_t codes[kStages];   // NVFP4 code tile landed (count 1 + tx)
   uint64_t empty[kStages];   // MMAs done with the stage (tcgen05.commit)
   uint64_t acc_full;         // all MMAs of a unit done
   uint64_t acc_empty;        // epilogue finished reading TMEM (count 8 warps)
@@ -73,11 +74,11 @@ struct GCtl {
 constexpr size_t kGSmem = (size_t)kStages * kStageBytes + sizeof(GCtl) + 1024;
 
 FLINT_DEV bool gwait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
-  if (*abort) return false;
+  if (mbar_try_wait(bar, parity, kSuspendNs)) return true;  // the common case: no other work
   unsigned long long t0 = 0;
   for (;;) {
-    if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
     if (*abort) return false;
+    if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
     const unsigned long long now = globaltimer_ns();
     if (t0 == 0) t0 = now;
     if (now - t0 > kWaitNs) {
@@ -178,8 +179,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&C.full_a[i], 1);
-      mbar_init(&C.full_b[i], 8);
+      mbar_init(&C.full[i], 1 + 8);
+      mbar_init(&C.codes[i], 1);
       mbar_init(&C.empty[i], 1);
     }
     mbar_init(&C.acc_full, 1);
@@ -215,24 +216,27 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const CUtensorMap* ta = x.shared ? &tm.a_shared : &tm.a_routed;
           uint32_t bytes = (uint32_t)x.halves * kTile;
           if (x.shared) bytes += (uint32_t)x.n * 128u;
-          else bytes += (uint32_t)x.n * 32u;
-          mbar_arrive_expect_tx(&C.full_a[s], bytes);
-          tc::tma_load_2d(st + kOffA, ta, kb * 64, x.row0, &C.full_a[s]);
-          if (x.halves == 2) tc::tma_load_2d(st + kOffA + kTile, ta, kb * 64, x.row0 + 128, &C.full_a[s]);
+          mbar_arrive_expect_tx(&C.full[s], bytes);
           if (x.shared) {
-            if (STAGE == 1) {  // 32 gate rows, then 32 up rows
-              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, 32 * x.nt, &C.full_a[s]);
-              tc::tma_load_2d(st + kOffB + 32 * 128, &tm.b_shared, kb * 64, a.SI + 32 * x.nt, &C.full_a[s]);
-            } else {
-              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, 128 * x.nt, &C.full_a[s]);
-            }
+            mbar_arrive(&C.codes[s]);  // no codes; keeps the barrier's phase in step
           } else {
+            mbar_arrive_expect_tx(&C.codes[s], (uint32_t)x.n * 32u);
             if (STAGE == 1) {  // 64 gate rows, then 64 up rows
               const int g0 = x.e * 2 * a.I + 64 * x.nt;
-              tc::tma_load_2d(st + kOffC, &tm.codes, kb * 32, g0, &C.full_a[s]);
-              tc::tma_load_2d(st + kOffC + 64 * 32, &tm.codes, kb * 32, g0 + a.I, &C.full_a[s]);
+              tc::tma_load_2d(st + kOffC, &tm.codes, kb * 32, g0, &C.codes[s]);
+              tc::tma_load_2d(st + kOffC + 64 * 32, &tm.codes, kb * 32, g0 + a.I, &C.codes[s]);
             } else {
-              tc::tma_load_2d(st + kOffC, &tm.codes, kb * 32, x.e * a.H + 128 * x.nt, &C.full_a[s]);
+              tc::tma_load_2d(st + kOffC, &tm.codes, kb * 32, x.e * a.H + 128 * x.nt, &C.codes[s]);
+            }
+          }
+          tc::tma_load_2d(st + kOffA, ta, kb * 64, x.row0, &C.full[s]);
+          if (x.halves == 2) tc::tma_load_2d(st + kOffA + kTile, ta, kb * 64, x.row0 + 128, &C.full[s]);
+          if (x.shared) {
+            if (STAGE == 1) {  // 32 gate rows, then 32 up rows
+              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, 32 * x.nt, &C.full[s]);
+              tc::tma_load_2d(st + kOffB + 32 * 128, &tm.b_shared, kb * 64, a.SI + 32 * x.nt, &C.full[s]);
+            } else {
+              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, 128 * x.nt, &C.full[s]);
             }
           }
         }
@@ -242,6 +246,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
   } else if (warp == 9) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
+      // descriptors of stage 0's tiles; a stage's are these plus its byte
+      // offset / 16 (shared addresses stay below 2^18, inside the 14-bit field)
+      const uint64_t dA0 = tc::desc_sw128(smem + kOffA), dA1 = tc::desc_sw128(smem + kOffA + kTile);
+      const uint64_t dB = tc::desc_sw128(smem + kOffB);
       int it = 0, nu = 0;
       for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x, ++nu) {
         const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
@@ -252,22 +260,25 @@ __global__ void __launch_bounds__(kGThreads, 1)
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kStages;
-          const uint32_t par = (it / kStages) & 1;
-          if (!gwait(&C.full_a[s], par, abort, status) || !gwait(&C.full_b[s], par, abort, status)) {
+          if (!gwait(&C.full[s], (it / kStages) & 1, abort, status)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          uint8_t* st = smem + (size_t)s * kStageBytes;
-          const uint64_t db = tc::desc_sw128(st + kOffB);
+          const uint64_t so = (uint64_t)(s * (kStageBytes >> 4));
+          const uint64_t da0 = dA0 + so, da1 = dA1 + so, db = dB + so;
           const int p = kb % x.parts;  // K block kb accumulates into partial kb % parts
+          const uint32_t d0 = tmem + (uint32_t)(x.n * p), d1 = d0 + 256;
+          const bool acc = kb >= x.parts;
+          if (x.halves == 2) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            for (int h = 0; h < x.halves; ++h) {
-              const uint64_t da = tc::desc_sw128(st + kOffA + h * kTile);
-              tc::mma_bf16(tmem + 256 * h + x.n * p, da + 2 * kk, db + 2 * kk, idesc,
-                           (kb >= x.parts) || (kk > 0));
+            for (int kk = 0; kk < 4; ++kk) {
+              tc::mma_bf16(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc || kk > 0);
+              tc::mma_bf16(d1, da1 + 2 * kk, db + 2 * kk, idesc, acc || kk > 0);
             }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc || kk > 0);
           }
           tc::commit(&C.empty[s]);
         }
@@ -315,7 +326,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         uint8_t* st = smem + (size_t)s * kStageBytes;
         if (!x.shared) {
-          if (!gwait_warp(&C.full_a[s], (it / kStages) & 1, abort, status, lane)) {
+          if (!gwait_warp(&C.codes[s], (it / kStages) & 1, abort, status, lane)) {
             ok = false;
             break;
           }
@@ -323,7 +334,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
           tc::fence_proxy_async_smem();
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&C.full_b[s]);
+        if (lane == 0) mbar_arrive(&C.full[s]);
       }
       if (!ok) break;
 

@@ -21,21 +21,28 @@
 //          y = bf16(acc * gs2); shared units likewise: sact Wsd^T -> ys.
 // combine: out[t] = bf16(bf16(sum_j tw_j y[row of (t, j)]) + ys[t]).
 //
-// GEMM kernel (persistent, one CTA per SM, 320 threads):
-//   warp 8: TMA producer (A tiles; the NVFP4 code tile or the BF16 B tile),
-//   warp 9: MMA issuer (one thread) and TMEM owner (512 columns: per
+// GEMM kernel (persistent, one CTA per SM, 608 threads):
+//   warp 16: TMA producer of the stages (A tiles; the shared expert's BF16 B
+//           tile),
+//   warp 18: TMA producer of the NVFP4 code tiles (a ring of their own, up
+//           to 6 K blocks ahead),
+//   warp 17: MMA issuer (one thread) and TMEM owner (512 columns: per
 //           128-token half two 128 x 128 fp32 accumulators, K block kb going
 //           to accumulator kb % 2, added in fp32 by the epilogue -- so the
 //           tensor core's own accumulation spans half the reduction; the
 //           shared expert's gate/up units take one 128-token half, 64 weight
 //           rows and eight accumulators, because its bf16(gS), bf16(uS)
 //           roundings feed every output of the token),
-//   warps 0..7: dequantise (threads 2r, 2r + 1 own B row r: 32 codes each
-//           of a K block -> bf16 e2m1 * scale * 2^-7, exact, written in the
-//           128-byte swizzled K-major layout), then the epilogue (warps 0..3
-//           read half 0, warps 4..7 half 1; TMEM lane = token row).
-// Ring: 4 stages of {A 2 x 16 KB, B 16 KB, codes 4 KB}.  Every wait is
-// bounded (FLINT_ERR_TIMEOUT in the status word on expiry).
+//   warps 0..15: two groups of 8 taking alternate K blocks; in a group,
+//           threads 2r, 2r + 1 own B row r: 32 codes each of a K block ->
+//           bf16 e2m1 * scale * 2^-7, exact, computed in registers as soon
+//           as the codes are in, written in the 128-byte swizzled K-major
+//           layout once the stage is free.  Then all 16 run the epilogue
+//           (TMEM lane quarter warp % 4, half (warp / 4) % 2, column half
+//           warp / 8; TMEM lane = token row).
+// Rings: 4 stages of {A 2 x 16 KB, B 16 KB}; 6 code tiles of 4 KB; the
+// dequantising threads' block scales (asynchronous copies, 6 K blocks ahead).
+// Every wait is bounded (FLINT_ERR_TIMEOUT in the status word on expiry).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -46,16 +53,21 @@
 namespace flint {
 namespace {
 
-constexpr int kGWarps = 10;
+constexpr int kGWarps = 19;  // 0..15 dequant + epilogue, 16 stage producer, 17 MMA, 18 code producer
+constexpr int kWarpProd = 16, kWarpMma = 17, kWarpCodes = 18;
 constexpr int kGThreads = kGWarps * 32;
 constexpr int kStages = 4;
 constexpr int kTile = 128 * 128;            // 128 rows x 64 bf16
 constexpr int kBRows = 128;                 // B rows (N) of a routed unit
 constexpr int kOffA = 0;                    // two A tiles
 constexpr int kOffB = 2 * kTile;            // up to kBRows B rows
-constexpr int kOffC = kOffB + kBRows * 128; // kBRows rows x 32 code bytes
-constexpr int kStageBytes = kOffC + kBRows * 32;  // 53248
+constexpr int kStageBytes = kOffB + kBRows * 128;  // 49152
 static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+// NVFP4 code tiles (kBRows rows x 32 bytes per K block) have a ring of their
+// own, deeper than the stages, so they land well before they are dequantised.
+constexpr int kCStages = 6;
+constexpr int kCodeBytes = kBRows * 32;
+constexpr int kOffCodes = kStages * kStageBytes;
 constexpr int kTokTile = 256;
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;
 constexpr uint32_t kSuspendNs = 50000;
@@ -64,14 +76,22 @@ constexpr int kStWords = 4;  // token-tile table entry: e, row0, row_end, unused
 struct GCtl {
   uint64_t full[kStages];    // stage ready for the MMA: A (and BF16 B) bytes landed
                              // and the 8 dequantising warps done (count 1 + 8, + tx)
-  uint64_t codes[kStages];   // NVFP4 code tile landed (count 1 + tx)
   uint64_t empty[kStages];   // MMAs done with the stage (tcgen05.commit)
+  uint64_t cfull[kCStages];  // code tile landed (count 1 + tx)
+  uint64_t cempty[kCStages]; // code tile read by the 8 dequantising warps
   uint64_t acc_full;         // all MMAs of a unit done
   uint64_t acc_empty;        // epilogue finished reading TMEM (count 8 warps)
   uint32_t tmem;
   int abort;
 };
-constexpr size_t kGSmem = (size_t)kStages * kStageBytes + sizeof(GCtl) + 1024;
+// Block-scale ring of the dequantising threads: slot j of thread t at word
+// j * 256 + t, filled by asynchronous 4-byte copies kScaleAhead K blocks
+// ahead of use (slot kb % kScaleSlots, never the one being read).
+constexpr int kScaleSlots = 4;
+constexpr int kScaleAhead = 3;
+constexpr int kOffScale = kOffCodes + kCStages * kCodeBytes;
+constexpr int kScaleBytes = kScaleSlots * 512 * 4;
+constexpr size_t kGSmem = (size_t)kOffScale + kScaleBytes + sizeof(GCtl) + 1024;
 
 FLINT_DEV bool gwait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
   if (mbar_try_wait(bar, parity, kSuspendNs)) return true;  // the common case: no other work
@@ -143,26 +163,22 @@ FLINT_DEV Unit unit_of(const MoEArgs& a, int u, int R, int NT, int NTs) {
   return x;
 }
 
-// Dequantise half j of one K block of B row r (32 codes, their 2 scale
-// bytes) into the swizzled bf16 tile: values e2m1 * scale * 2^-7, exactly.
-FLINT_DEV void dequant_half(uint8_t* btile, int r, int j, const uint8_t* codes, uint32_t sc2) {
+// Dequantise half j of one K block of a B row (32 codes, their 2 scale
+// bytes) to bf16 e2m1 * scale * 2^-7, exactly: v[i] holds K 32 j + 8 i .. + 7.
+FLINT_DEV void dequant_half(uint4 (&v)[4], const uint4 c0, uint32_t sc2) {
   const uint32_t s01 = e4m3x2_to_bf16x2_x2p119(sc2 & 0xFFFFu);
-  const uint4 c0 = *reinterpret_cast<const uint4*>(codes);
   const uint32_t w[4] = {c0.x, c0.y, c0.z, c0.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {  // word i: K 32 j + 8 i .. + 7, scale block i / 2
-    const int q = 4 * j + i;
     const uint32_t sc = bf16x2_bcast(s01, i >> 1);
-    const uint32_t p0 = bf16x2_mul(e2m1_pair(w[i], 0), sc);  // K 8q + 0, 8q + 4
+    const uint32_t p0 = bf16x2_mul(e2m1_pair(w[i], 0), sc);  // K 8 i + 0, 8 i + 4
     const uint32_t p1 = bf16x2_mul(e2m1_pair(w[i], 1), sc);  // 1, 5
     const uint32_t p2 = bf16x2_mul(e2m1_pair(w[i], 2), sc);  // 2, 6
     const uint32_t p3 = bf16x2_mul(e2m1_pair(w[i], 3), sc);  // 3, 7
-    uint4 v;
-    v.x = __byte_perm(p0, p1, 0x5410);  // K 0, 1
-    v.y = __byte_perm(p2, p3, 0x5410);  // 2, 3
-    v.z = __byte_perm(p0, p1, 0x7632);  // 4, 5
-    v.w = __byte_perm(p2, p3, 0x7632);  // 6, 7
-    *reinterpret_cast<uint4*>(btile + tc::sw128_offset(r, 8 * q)) = v;
+    v[i].x = __byte_perm(p0, p1, 0x5410);  // K 0, 1
+    v[i].y = __byte_perm(p2, p3, 0x5410);  // 2, 3
+    v[i].z = __byte_perm(p0, p1, 0x7632);  // 4, 5
+    v[i].w = __byte_perm(p2, p3, 0x7632);  // 6, 7
   }
 }
 
@@ -172,7 +188,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                         int n_shared_tiles) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  GCtl& C = *reinterpret_cast<GCtl*>(smem + (size_t)kStages * kStageBytes);
+  GCtl& C = *reinterpret_cast<GCtl*>(smem + (size_t)kOffScale + kScaleBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int* status = a.ws.status;
   volatile int* abort = &C.abort;
@@ -180,15 +196,18 @@ __global__ void __launch_bounds__(kGThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&C.full[i], 1 + 8);
-      mbar_init(&C.codes[i], 1);
       mbar_init(&C.empty[i], 1);
     }
+    for (int i = 0; i < kCStages; ++i) {
+      mbar_init(&C.cfull[i], 1);
+      mbar_init(&C.cempty[i], 8);
+    }
     mbar_init(&C.acc_full, 1);
-    mbar_init(&C.acc_empty, 8);
+    mbar_init(&C.acc_empty, 16);
     C.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 9) tc::tmem_alloc(&C.tmem, 512);
+  if (warp == kWarpMma) tc::tmem_alloc(&C.tmem, 512);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -200,7 +219,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
   const int R = ST * NT;
   const int total = R + n_shared_tiles * NTs;
 
-  if (warp == 8) {
+  if (warp == kWarpProd) {
     // ------------------------------------------------------------ producer
     int it = 0;
     for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x) {
@@ -217,18 +236,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
           uint32_t bytes = (uint32_t)x.halves * kTile;
           if (x.shared) bytes += (uint32_t)x.n * 128u;
           mbar_arrive_expect_tx(&C.full[s], bytes);
-          if (x.shared) {
-            mbar_arrive(&C.codes[s]);  // no codes; keeps the barrier's phase in step
-          } else {
-            mbar_arrive_expect_tx(&C.codes[s], (uint32_t)x.n * 32u);
-            if (STAGE == 1) {  // 64 gate rows, then 64 up rows
-              const int g0 = x.e * 2 * a.I + 64 * x.nt;
-              tc::tma_load_2d(st + kOffC, &tm.codes, kb * 32, g0, &C.codes[s]);
-              tc::tma_load_2d(st + kOffC + 64 * 32, &tm.codes, kb * 32, g0 + a.I, &C.codes[s]);
-            } else {
-              tc::tma_load_2d(st + kOffC, &tm.codes, kb * 32, x.e * a.H + 128 * x.nt, &C.codes[s]);
-            }
-          }
           tc::tma_load_2d(st + kOffA, ta, kb * 64, x.row0, &C.full[s]);
           if (x.halves == 2) tc::tma_load_2d(st + kOffA + kTile, ta, kb * 64, x.row0 + 128, &C.full[s]);
           if (x.shared) {
@@ -243,7 +250,38 @@ __global__ void __launch_bounds__(kGThreads, 1)
         __syncwarp();
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kWarpCodes) {
+    // ----------------------------------------------------- code-tile producer
+    // Runs up to kCStages K blocks ahead of dequantisation; K blocks of the
+    // shared expert (no codes) only advance the ring.
+    int it = 0;
+    for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x) {
+      const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
+      const int nkb = x.K / 64;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int c = it % kCStages;
+        int ok = 1;
+        if (it >= kCStages) ok = gwait_warp(&C.cempty[c], ((it / kCStages) - 1) & 1, abort, status, lane);
+        if (!ok) break;
+        if (lane == 0) {
+          if (x.shared) {
+            mbar_arrive(&C.cfull[c]);
+          } else {
+            uint8_t* dst = smem + kOffCodes + c * kCodeBytes;
+            mbar_arrive_expect_tx(&C.cfull[c], (uint32_t)x.n * 32u);
+            if (STAGE == 1) {  // 64 gate rows, then 64 up rows
+              const int g0 = x.e * 2 * a.I + 64 * x.nt;
+              tc::tma_load_2d(dst, &tm.codes, kb * 32, g0, &C.cfull[c]);
+              tc::tma_load_2d(dst + 64 * 32, &tm.codes, kb * 32, g0 + a.I, &C.cfull[c]);
+            } else {
+              tc::tma_load_2d(dst, &tm.codes, kb * 32, x.e * a.H + 128 * x.nt, &C.cfull[c]);
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp == kWarpMma) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
       // descriptors of stage 0's tiles; a stage's are these plus its byte
@@ -289,90 +327,110 @@ __global__ void __launch_bounds__(kGThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------- dequant (B) and epilogue
-    const int r = threadIdx.x >> 1, jh = threadIdx.x & 1;  // B row, half of its K block
-    const int q = warp & 3, half = warp >> 2;
+    // Two groups of 8 warps take alternate K blocks (global K block index
+    // it: group it % 2), so each warp has two K blocks' time for one.
+    const int grp = warp >> 3;
+    const int tg = threadIdx.x & 255;
+    const int r = tg >> 1, jh = tg & 1;  // B row, half of its K block
+    // epilogue: TMEM lane quarter, 128-token half, column group
+    const int q = warp & 3, half = (warp >> 2) & 1, cg = warp >> 3;
     int it = 0, nu = 0;
     for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x, ++nu) {
       const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
       const int nkb = x.K / 64;
-      // scale bytes of this row, 4 per K block, read ahead of use
-      const uint8_t* sfrow = nullptr;  // this thread's 2 scale bytes of each K block
+      const uint8_t* sfrow = nullptr;  // block scales of B row r (4 bytes per K block)
       if (!x.shared) {
         if (STAGE == 1) {
           const size_t row = (size_t)x.e * 2 * a.I + (r < 64 ? 64 * x.nt + r : a.I + 64 * x.nt + (r - 64));
-          sfrow = a.w13_sf + row * (a.H / 16) + 2 * jh;
+          sfrow = a.w13_sf + row * (a.H / 16);
         } else if (128 * x.nt + r < a.H) {  // rows past H (last tile) are not read
-          sfrow = a.w2_sf + ((size_t)x.e * a.H + 128 * x.nt + r) * (a.I / 16) + 2 * jh;
+          sfrow = a.w2_sf + ((size_t)x.e * a.H + 128 * x.nt + r) * (a.I / 16);
         }
       }
-      // scale bytes of the next four K blocks in flight (a global load takes
-      // longer than one K block's dequantisation)
-      auto sc_load = [&](int kb) {
-        return (sfrow && kb < nkb) ? (uint32_t)*reinterpret_cast<const uint16_t*>(sfrow + 4 * kb) : 0u;
+      const int kb0 = (grp - it) & 1;  // this group's first K block of the unit
+      const int nmine = (nkb - kb0 + 1) / 2;
+      // the row's 4 scale bytes of this group's j-th K block come through the
+      // scale ring; one copy group per K block, empty past the row's end
+      uint32_t* ring = reinterpret_cast<uint32_t*>(smem + kOffScale) + threadIdx.x;
+      auto sc_fetch = [&](int j) {
+        const int kb = kb0 + 2 * j;
+        if (sfrow && kb < nkb) cp_async4(ring + (j % kScaleSlots) * 512, sfrow + 4 * kb);
+        cp_async_commit();
       };
-      uint32_t sc0 = sc_load(0), sc1 = sc_load(1), sc2 = sc_load(2), sc3 = sc_load(3);
+      cp_async_wait_all();  // nothing of the previous unit in flight
+#pragma unroll
+      for (int d = 0; d < kScaleAhead; ++d) sc_fetch(d);
       bool ok = true;
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int s = it % kStages;
-        const uint32_t sc = sc0;
-        sc0 = sc1;
-        sc1 = sc2;
-        sc2 = sc3;
-        sc3 = sc_load(kb + 4);
-        // the stage's previous MMAs are done (B area free), its codes landed
-        if (it >= kStages && !gwait_warp(&C.empty[s], ((it / kStages) - 1) & 1, abort, status, lane)) {
+      for (int j = 0; j < nmine; ++j) {
+        const int itk = it + kb0 + 2 * j;
+        const int s = itk % kStages, c = itk % kCStages;
+        cp_async_wait_group<kScaleAhead - 1>();  // this K block's group has landed
+        const uint32_t sc = sfrow ? (ring[(j % kScaleSlots) * 512] >> (16 * jh)) & 0xFFFFu : 0u;
+        sc_fetch(j + kScaleAhead);
+        // codes of the K block (landed well ahead): into registers, slot released
+        if (!gwait_warp(&C.cfull[c], (itk / kCStages) & 1, abort, status, lane)) {
           ok = false;
           break;
         }
-        uint8_t* st = smem + (size_t)s * kStageBytes;
+        uint4 codes = make_uint4(0, 0, 0, 0);
+        if (!x.shared) codes = *reinterpret_cast<const uint4*>(smem + kOffCodes + c * kCodeBytes + r * 32 + 16 * jh);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&C.cempty[c]);
+        uint4 bv[4];
+        if (!x.shared) dequant_half(bv, codes, sc);
+        // the stage's previous MMAs are done: its B area is free
+        if (itk >= kStages && !gwait_warp(&C.empty[s], ((itk / kStages) - 1) & 1, abort, status, lane)) {
+          ok = false;
+          break;
+        }
         if (!x.shared) {
-          if (!gwait_warp(&C.codes[s], (it / kStages) & 1, abort, status, lane)) {
-            ok = false;
-            break;
-          }
-          dequant_half(st + kOffB, r, jh, st + kOffC + r * 32 + 16 * jh, sc);
+          uint8_t* bt = smem + (size_t)s * kStageBytes + kOffB;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(bt + tc::sw128_offset(r, 32 * jh + 8 * i)) = bv[i];
           tc::fence_proxy_async_smem();
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&C.full[s]);
       }
       if (!ok) break;
+      it += nkb;
 
-      // ---- epilogue: accumulator `half`, TMEM lanes 32 q .. 32 q + 31
+      // ---- epilogue: accumulator `half`, TMEM lanes 32 q .. 32 q + 31,
+      // column group cg (half of the unit's output columns), 16 at a time
       if (!gwait_warp(&C.acc_full, nu & 1, abort, status, lane)) break;
       tc::fence_after_sync();
       const int row = x.row0 + 128 * half + 32 * q + lane;
       const bool valid = half < x.halves && row < x.row_end;
       const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + 256 * half;
       if (half < x.halves) {
+        const int nparts = min(x.parts, x.K / 64);
         if (STAGE == 1) {
           const int I = x.shared ? a.SI : a.I;
           const int hw = x.n / 2;  // intermediate rows of the unit: gate cols [0, hw), up [hw, n)
           uint16_t* dst = (x.shared ? a.ws.sact : a.ws.act) + (size_t)row * I + hw * x.nt;
           const float gs = x.shared ? 1.0f : a.w13_gs[x.e] * 128.0f;
-          const int nparts = min(x.parts, x.K / 64);
-          for (int c0 = 0; c0 < hw; c0 += 32) {
-            uint32_t gv[32], uv[32], t2[32], t3[32];
-            tc::tmem_ld32_async(tb + c0, gv);       // gate rows, partial 0
-            tc::tmem_ld32_async(tb + hw + c0, uv);  // up rows, partial 0
+          for (int c0 = cg * (hw / 2); c0 < (cg + 1) * (hw / 2); c0 += 16) {
+            uint32_t gv[16], uv[16], t2[16], t3[16];
+            tc::tmem_ld16_async(tb + c0, gv);       // gate rows, partial 0
+            tc::tmem_ld16_async(tb + hw + c0, uv);  // up rows, partial 0
             tc::tmem_wait_ld();
-            tc::tmem_regs_ready(gv);
-            tc::tmem_regs_ready(uv);
+            tc::tmem_regs_ready16(gv);
+            tc::tmem_regs_ready16(uv);
             for (int p = 1; p < nparts; ++p) {  // each partial's gate and up together
-              tc::tmem_ld32_async(tb + x.n * p + c0, t2);
-              tc::tmem_ld32_async(tb + x.n * p + hw + c0, t3);
+              tc::tmem_ld16_async(tb + x.n * p + c0, t2);
+              tc::tmem_ld16_async(tb + x.n * p + hw + c0, t3);
               tc::tmem_wait_ld();
-              tc::tmem_regs_ready(t2);
-              tc::tmem_regs_ready(t3);
+              tc::tmem_regs_ready16(t2);
+              tc::tmem_regs_ready16(t3);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
+              for (int i = 0; i < 16; ++i) {
                 gv[i] = __float_as_uint(__uint_as_float(gv[i]) + __uint_as_float(t2[i]));
                 uv[i] = __float_as_uint(__uint_as_float(uv[i]) + __uint_as_float(t3[i]));
               }
             }
-            uint32_t pk[16];
+            uint32_t pk[8];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
+            for (int i = 0; i < 16; i += 2) {
               float v[2];
 #pragma unroll
               for (int j = 0; j < 2; ++j) {
@@ -388,37 +446,38 @@ __global__ void __launch_bounds__(kGThreads, 1)
               pk[i / 2] = f32_to_bf16_bits(v[0]) | (f32_to_bf16_bits(v[1]) << 16);
             }
             if (valid) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                reinterpret_cast<uint4*>(dst + c0)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              reinterpret_cast<uint4*>(dst + c0)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              reinterpret_cast<uint4*>(dst + c0)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
           }
         } else {
           uint16_t* dst = (x.shared ? a.ws.ys : a.ws.y) + (size_t)row * a.H + x.n * x.nt;
           const float gs = x.shared ? 1.0f : a.w2_gs[x.e] * 128.0f;
-          const int nparts = min(x.parts, x.K / 64);
           const int ncols = min(x.n, a.H - x.n * x.nt);  // the last tile of H may be partial
-          for (int c0 = 0; c0 < x.n; c0 += 32) {
-            uint32_t v[32], t2[32];
-            tc::tmem_ld32_async(tb + c0, v);
-            if (nparts > 1) tc::tmem_ld32_async(tb + x.n + c0, t2);
+          for (int c0 = cg * (x.n / 2); c0 < (cg + 1) * (x.n / 2); c0 += 16) {
+            uint32_t v[16], t2[16];
+            tc::tmem_ld16_async(tb + c0, v);
+            if (nparts > 1) tc::tmem_ld16_async(tb + x.n + c0, t2);
             tc::tmem_wait_ld();
-            tc::tmem_regs_ready(v);
-            tc::tmem_regs_ready(t2);
+            tc::tmem_regs_ready16(v);
+            tc::tmem_regs_ready16(t2);
             for (int p = 1; p < nparts; ++p) {
-              if (p > 1) tc::tmem_ld32(tb + x.n * p + c0, t2);
+              if (p > 1) {
+                tc::tmem_ld16_async(tb + x.n * p + c0, t2);
+                tc::tmem_wait_ld();
+                tc::tmem_regs_ready16(t2);
+              }
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(t2[i]));
+              for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(t2[i]));
             }
-            uint32_t pk[16];
+            uint32_t pk[8];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2)
+            for (int i = 0; i < 16; i += 2)
               pk[i / 2] = f32_to_bf16_bits(__uint_as_float(v[i]) * gs) |
                           (f32_to_bf16_bits(__uint_as_float(v[i + 1]) * gs) << 16);
             if (valid && c0 < ncols) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                reinterpret_cast<uint4*>(dst + c0)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              reinterpret_cast<uint4*>(dst + c0)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              reinterpret_cast<uint4*>(dst + c0)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
           }
         }
@@ -427,11 +486,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&C.acc_empty);
     }
+    cp_async_wait_all();  // no copy may land after the block has exited
   }
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
   }

@@ -161,6 +161,16 @@ FLINT_DEV void mbar_arrive(uint64_t* bar) {
 }
 // Test for phase completion; if not complete the thread may be suspended
 // (woken by the completion) for up to `hint_ns` before returning false.
+// Non-blocking probe of the phase with the given parity.
+FLINT_DEV bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 FLINT_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns = 0) {
   uint32_t ok;
   if (hint_ns) {

@@ -94,7 +94,7 @@ constexpr int kScaleBytes = kScaleSlots * 512 * 4;
 constexpr size_t kGSmem = (size_t)kOffScale + kScaleBytes + sizeof(GCtl) + 1024;
 
 FLINT_DEV bool gwait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
-  if (mbar_try_wait(bar, parity, kSuspendNs)) return true;  // the common case: no other work
+  if (mbar_test_wait(bar, parity)) return true;  // the common case: already complete
   unsigned long long t0 = 0;
   for (;;) {
     if (*abort) return false;
@@ -288,25 +288,29 @@ __global__ void __launch_bounds__(kGThreads, 1)
       // offset / 16 (shared addresses stay below 2^18, inside the 14-bit field)
       const uint64_t dA0 = tc::desc_sw128(smem + kOffA), dA1 = tc::desc_sw128(smem + kOffA + kTile);
       const uint64_t dB = tc::desc_sw128(smem + kOffB);
-      int it = 0, nu = 0;
+      // stage index, its phase bit and its descriptor offset run as counters
+      // (the issuing thread shares its scheduler with dequantising warps, so
+      // every instruction here costs)
+      int s = 0, nu = 0;
+      uint32_t ph = 0;
+      uint64_t so = 0;
       for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x, ++nu) {
         const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
         const int nkb = x.K / 64;
         const uint32_t idesc = tc::idesc_bf16(128, x.n);
+        const uint32_t dwrap = (uint32_t)(x.n * x.parts);
         if (nu > 0 && !gwait(&C.acc_empty, (nu - 1) & 1, abort, status)) break;
         tc::fence_after_sync();
         bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = it % kStages;
-          if (!gwait(&C.full[s], (it / kStages) & 1, abort, status)) {
+        uint32_t dcol = 0;  // accumulator of K block kb: columns x.n * (kb % parts)
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!gwait(&C.full[s], ph, abort, status)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const uint64_t so = (uint64_t)(s * (kStageBytes >> 4));
           const uint64_t da0 = dA0 + so, da1 = dA1 + so, db = dB + so;
-          const int p = kb % x.parts;  // K block kb accumulates into partial kb % parts
-          const uint32_t d0 = tmem + (uint32_t)(x.n * p), d1 = d0 + 256;
+          const uint32_t d0 = tmem + dcol, d1 = d0 + 256;
           const bool acc = kb >= x.parts;
           if (x.halves == 2) {
 #pragma unroll
@@ -319,6 +323,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
             for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc || kk > 0);
           }
           tc::commit(&C.empty[s]);
+          dcol += (uint32_t)x.n;
+          if (dcol == dwrap) dcol = 0;
+          so += (uint64_t)(kStageBytes >> 4);
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+            so = 0;
+          }
         }
         if (!ok) break;
         tc::commit(&C.acc_full);

@@ -52,6 +52,8 @@ def parse():
     p.add_argument("--config", default="decode1", choices=sorted(synth.CONFIGS))
     p.add_argument("--layers", type=int, default=0, help="weight sets rotated (0 = auto)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile", action="store_true",
+                   help="run --warmup then --steps plain (eager) forwards and exit, for ncu launch lists")
     return p.parse_args()
 
 
@@ -194,6 +196,32 @@ def traffic_record(kernel: str):
     if entry and entry.get("csrc_sha256") == h.hexdigest():
         return entry.get("dram_bytes_per_step")
     return None
+
+
+# ----------------------------------------------------------------- profile
+def run_profile(args, local):
+    """Eager forwards only (no graphs, no timing): `warmup` steps, then `steps`
+    steps, each a fixed sequence of launches_per_step(M) kernels, so an ncu
+    launch list can skip the first and capture the rest."""
+    import nvfp4_w4a16_mixture_gb300 as fm
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    M, H, E, k, I, SI = synth.CONFIGS[args.config]
+    n_layers = args.layers or (16 if M <= DECODE_MAX_TOKENS else 2)
+    fm.load()
+    xs, layers = make_layers(args.config, n_layers, dev, seed=1)
+    ws = fm.alloc_workspace(M, H, E, k, I, SI, dev)
+    outs = [torch.empty_like(x) for x in xs]
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            li = i % n_layers
+            fm.forward_layer(xs[li], layers[li], k, workspace=ws, out=outs[li], stream=stream)
+    stream.synchronize()
+    assert fm.flint_moe_status(ws, stream) == fm.FLINT_OK
+    print(f"profile: {args.config}, {args.warmup} + {args.steps} steps of "
+          f"{launches_per_step(M)} launches, {n_layers} layers rotated", file=sys.stderr)
 
 
 # -------------------------------------------------------------------- ours
@@ -412,6 +440,9 @@ def main():
     if args.warmup <= 0:
         args.warmup = 200 if M <= DECODE_MAX_TOKENS else 5
     rank, world, local = dist_env()
+    if args.profile:
+        run_profile(args, local)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)

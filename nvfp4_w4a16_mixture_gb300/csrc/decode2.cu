@@ -15,7 +15,8 @@
 // well over 100 KB of weight reads in flight.
 //
 // Chaining (programmatic dependent launch):
-//   router (plain launch: it starts after all earlier work has finished)
+//   router (loads its weight rows, then waits for every earlier kernel, and
+//   only then releases the gate/up grid -- so x is final when gate/up starts)
 //     -> gate/up: launched early; before its dependency wait it computes the
 //        whole shared-expert gate/up (x and the weights are inputs), then
 //        streams the routed experts' tiles named by the router's records.
@@ -531,9 +532,17 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
 // whole K of its item, so no cross-warp reduction is needed.  Results go to
 // smem: y (bf16, per pair t * k + j) and ys (bf16, per token); after the last
 // stage the CTA forms out = bf16(bf16(sum_j tw_j y_j) + ys) for its rows.
+// A stage with at most kDnSplitItems items gives each item two warps, one
+// per half of its K slices; the second half's fp32 partials go through
+// shared memory (a float4 per lane) and a per-item flag holding the stage
+// number + 1.
+constexpr int kDnSplitItems = kCons / 2;
+
 struct DnSmem {
   Ctl ctl;
   DnInfo info[kDnStages];
+  int flag[kDnStages][kDnSplitItems];
+  float4 part[kDnStages][kDnSplitItems][32];
 };
 
 // Byte offsets in the down kernel's dynamic smem: stages, y, ys, control.
@@ -557,6 +566,9 @@ FLINT_DEV int dn_block_bytes(int kind, int I, int SI) {
 
 __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
+  // the next kernel may start now: a router launched after this one loads
+  // only its weights before its own dependency wait
+  pdl_launch_dependents();
   uint8_t* stages = smem;
   const DnLayout L = dn_layout(a.M, a.k);
   uint16_t* ysm = reinterpret_cast<uint16_t*>(smem + L.y);
@@ -573,6 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
     for (int i = 0; i < kDnStages; ++i) {
       mbar_init(&SM.ctl.full[i], 1);
       mbar_init(&SM.ctl.empty[i], kCons);
+      for (int j = 0; j < kDnSplitItems; ++j) SM.flag[i][j] = 0;
     }
     mbar_init(&SM.ctl.bar[0], kCons + 1);
     SM.ctl.abort = 0;
@@ -719,7 +732,9 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
     const DnInfo& inf = SM.info[sl];
     if (inf.nblocks == 0) break;
     const uint8_t* st = stages + (size_t)sl * kDnStageBytes;
-    for (int it = warp; it < inf.nitems; it += kCons) {
+    const bool split = inf.nitems <= kDnSplitItems;
+    const int kh = split ? (warp & 1) : 0;  // K half of this warp (split stages)
+    for (int it = split ? (warp >> 1) : warp; it < inf.nitems; it += split ? kDnSplitItems : kCons) {
       const DnBlock& b = inf.blk[inf.item_blk[it]];
       const int nt = inf.item_nt[it];
       const int nn = nt * 8 + g;  // token column of this lane
@@ -747,7 +762,9 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
       const uint8_t* sg = st + b.smem + 16 * b.pitch + g * (I / 16);
       const uint8_t* sg8 = sg + 8 * (I / 16);
       const int nsl = K / kSliceK;
-      for (int s = 0; s < nsl; ++s) {
+      const int s_lo = split && kh ? (nsl + 1) / 2 : 0;
+      const int s_hi = split && !kh ? (nsl + 1) / 2 : nsl;
+      for (int s = s_lo; s < s_hi; ++s) {
         uint4 xb[4];
         if (bsm) {
 #pragma unroll
@@ -760,6 +777,32 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
         if (routed) frags_fp4(af, rg, rg8, sg, sg8, s, t);
         else frags_bf16(af, rg, rg8, s, t);
         mma_b(acc, af, xb);
+      }
+      if (split) {
+        float4* pp = &SM.part[sl][it][lane];
+        volatile int* fl = &SM.flag[sl][it];
+        if (kh) {  // second half: hand the partials over, the first half writes y
+          *pp = make_float4(acc[0], acc[1], acc[2], acc[3]);
+          __threadfence_block();
+          __syncwarp();
+          if (lane == 0) *fl = n + 1;
+          continue;
+        }
+        int ok = 1;
+        if (lane == 0) {
+          const unsigned long long t0 = globaltimer_ns();
+          while (*fl != n + 1) {
+            if (*abort || globaltimer_ns() - t0 > kWaitNs) {
+              if (!*abort) { *abort = 1; record_timeout(status, 17, n); }
+              ok = 0;
+              break;
+            }
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        __threadfence_block();
+        const float4 o = *pp;
+        acc[0] += o.x; acc[1] += o.y; acc[2] += o.z; acc[3] += o.w;
       }
       if (routed) {
         const float gs2 = a.w2_gs[b.e] * 128.0f;

@@ -99,7 +99,9 @@ struct MoEArgs {
 // Launchers (return cudaSuccess or the launch error).  `pdl` launches the
 // kernel with programmatic stream serialisation.
 cudaError_t launch_route(const MoEArgs& a, bool build_meta, cudaStream_t st, bool pdl);
-// One-cluster router with the small-M grouping (plain launch); for M <= 16.
+// One-cluster router with the small-M grouping; for M <= 16.  Launched with
+// programmatic dependent launch: it prefetches router rows, waits for the
+// previous kernel, then releases its dependents.
 bool route_cluster_supported(const MoEArgs& a);
 cudaError_t launch_route_cluster(const MoEArgs& a, cudaStream_t st);
 cudaError_t launch_decode_gate_up(const MoEArgs& a, cudaStream_t st, bool pdl);

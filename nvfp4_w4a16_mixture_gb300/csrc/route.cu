@@ -185,9 +185,8 @@ FLINT_DEV void topk_warp(Get get, int E, int k, int lane, int& out_e, float& out
     key[q] = -1;
     if (ee < E) key[q] = (int)((ordered_bf16(get(ee)) << 8) | (uint32_t)(E - 1 - ee));
   }
-  float sum = 0.0f, my_s = 0.0f;
-  int my_e = 0;
-  for (int j = 0; j < k; ++j) {
+  int my_e = 0, my_key = 0;
+  for (int j = 0; j < k; ++j) {  // selection only; lane j keeps rank j
     int lm = key[0];
 #pragma unroll
     for (int q = 1; q < kMaxE / 32; ++q) lm = max(lm, key[q]);
@@ -195,13 +194,18 @@ FLINT_DEV void topk_warp(Get get, int E, int k, int lane, int& out_e, float& out
 #pragma unroll
     for (int q = 0; q < kMaxE / 32; ++q)
       if (key[q] == best) key[q] = -1;
-    const uint32_t o = (uint32_t)best >> 8;
+    if (lane == j) { my_key = best; my_e = E - 1 - (best & 0xFF); }
+  }
+  // the k sigmoids side by side, then their sum in rank order
+  float my_s = 0.0f;
+  if (lane < k) {
+    const uint32_t o = (uint32_t)my_key >> 8;
     const uint32_t b16 = (o & 0x8000u) ? (o ^ 0x8000u) : (o ^ 0xFFFFu);
     const float logit = bf16_bits_to_f32(b16);
-    const float s = __fdiv_rn(1.0f, 1.0f + expf(-logit));
-    sum = sum + s;  // rank order
-    if (lane == j) { my_s = s; my_e = E - 1 - (best & 0xFF); }
+    my_s = __fdiv_rn(1.0f, 1.0f + expf(-logit));
   }
+  float sum = 0.0f;
+  for (int j = 0; j < k; ++j) sum = sum + __shfl_sync(0xffffffffu, my_s, j);
   out_e = my_e;
   out_w = round_bf16(__fdiv_rn(my_s, sum + 1e-20f));
 }
@@ -433,7 +437,6 @@ struct RcSmem {
 __global__ void __cluster_dims__(kRcCtas, 1, 1) __launch_bounds__(kRcWarps * 32)
     route_cluster_kernel(MoEArgs a) {
   __shared__ RcSmem S;
-  pdl_launch_dependents();
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   const int rank = (int)cl.block_rank();
@@ -441,10 +444,19 @@ __global__ void __cluster_dims__(kRcCtas, 1, 1) __launch_bounds__(kRcWarps * 32)
   const int H = a.H, E = a.E, k = a.k, M = a.M;
   RcSmem* lead = cl.map_shared_rank(&S, 0);
 
-  for (int e = rank * kRcWarps + warp; e < E; e += kRcCtas * kRcWarps) {
+  // The first router row of this warp is a weight, independent of earlier
+  // kernels: its load overlaps the previous kernel's tail.  Then wait for
+  // that kernel (x may be its output), and only then let the gate/up kernel
+  // start, because it reads x before its own dependency wait.
+  const int e0 = rank * kRcWarps + warp;
+  uint4 wreg[8];
+  router_row_regs(wreg, a.router_w + (size_t)min(e0, E - 1) * H, H, lane, e0 < E);
+  pdl_wait();
+  pdl_launch_dependents();
+
+  for (int e = e0; e < E; e += kRcCtas * kRcWarps) {
     const uint16_t* wrow = a.router_w + (size_t)e * H;
-    uint4 wreg[8];
-    router_row_regs(wreg, wrow, H, lane, true);
+    if (e != e0) router_row_regs(wreg, wrow, H, lane, true);
     for (int t = 0; t < M; ++t) {
       const float acc = router_dot(a.x + (size_t)t * H, wreg, wrow, H, lane);
       if (lane == 0) lead->logit[t][e] = (uint16_t)f32_to_bf16_bits(acc);
@@ -588,7 +600,7 @@ cudaError_t launch_route_cluster(const MoEArgs& a, cudaStream_t st) {
   MoEArgs aa = a;
   void* args[] = {&aa};
   return launch((const void*)route_cluster_kernel, dim3(kRcCtas), dim3(kRcWarps * 32), args, st,
-                false);
+                true);
 }
 
 cudaError_t launch_route(const MoEArgs& a, bool build_meta, cudaStream_t st, bool pdl) {

@@ -53,52 +53,90 @@
 namespace flint {
 namespace {
 
-constexpr int kGWarps = 19;  // 0..15 dequant + epilogue, 16 stage producer, 17 MMA, 18 code producer
-constexpr int kWarpProd = 16, kWarpMma = 17, kWarpCodes = 18;
+// Roles by warp.  A warp runs on scheduler warp % 4; the single MMA-issuing
+// thread shares its scheduler only with light warps (the two producers and the
+// two epilogue warps that must sit there for TMEM lane quarter 1), so its
+// instructions are not queued behind dequantisation math.
+//   scheduler 0: dequant 0, 3, 6; epilogue q0 (12, 16)
+//   scheduler 1: epilogue q1 (1, 5); MMA 9; stage producer 13; code producer 17
+//   scheduler 2: dequant 1, 4, 7; epilogue q2 (14, 18)
+//   scheduler 3: dequant 2, 5; epilogue q3 (11, 15); warp 19 idle
+constexpr int kGWarps = 20;
+constexpr int kWarpMma = 9, kWarpProd = 13, kWarpCodes = 17;
 constexpr int kGThreads = kGWarps * 32;
-constexpr int kStages = 4;
-constexpr int kTile = 128 * 128;            // 128 rows x 64 bf16
-constexpr int kBRows = 128;                 // B rows (N) of a routed unit
-constexpr int kOffA = 0;                    // two A tiles
-constexpr int kOffB = 2 * kTile;            // up to kBRows B rows
-constexpr int kStageBytes = kOffB + kBRows * 128;  // 49152
+// dequantising warp index (0..7: group = index / 4) or -1
+FLINT_DEV int dq_index(int warp) {
+  switch (warp) {
+    case 0: return 0;
+    case 2: return 1;
+    case 3: return 2;
+    case 4: return 3;
+    case 6: return 4;
+    case 7: return 5;
+    case 8: return 6;
+    case 10: return 7;
+    default: return -1;
+  }
+}
+// epilogue column group (0, 1) of an epilogue warp, or -1; its TMEM lane
+// quarter is warp % 4
+FLINT_DEV int epi_group(int warp) {
+  switch (warp) {
+    case 1: case 11: case 12: case 14: return 0;
+    case 5: case 15: case 16: case 18: return 1;
+    default: return -1;
+  }
+}
+constexpr int kStages = 6;
+constexpr int kATile = 128 * 128;                  // 128 token rows x 64 bf16
+constexpr int kBRows = 64;                         // B rows per CTA: N = 128 per pair
+constexpr int kOffA = 0;
+constexpr int kOffB = kATile;
+constexpr int kStageBytes = kATile + kBRows * 128;  // 24576
 static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
 // NVFP4 code tiles (kBRows rows x 32 bytes per K block) have a ring of their
 // own, deeper than the stages, so they land well before they are dequantised.
-constexpr int kCStages = 6;
+constexpr int kCStages = 8;
 constexpr int kCodeBytes = kBRows * 32;
 constexpr int kOffCodes = kStages * kStageBytes;
-constexpr int kTokTile = 256;
+// Block-scale ring of the 256 dequantising threads: slot j of thread t at
+// word j * 256 + t, filled by asynchronous 4-byte copies kScaleAhead of the
+// thread's K blocks ahead of use (slot j % kScaleSlots, never the one read).
+constexpr int kScaleSlots = 4;
+constexpr int kScaleAhead = 3;
+constexpr int kDqThreads = 256;
+constexpr int kOffScale = kOffCodes + kCStages * kCodeBytes;
+constexpr int kScaleBytes = kScaleSlots * kDqThreads * 4;
+constexpr int kTokTile = 256;   // token rows of a pair unit: 128 per CTA
+constexpr int kTmemBuf = 256;   // TMEM columns of one accumulator buffer (two buffers)
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;
 constexpr uint32_t kSuspendNs = 50000;
 constexpr int kStWords = 4;  // token-tile table entry: e, row0, row_end, unused
 
 struct GCtl {
-  uint64_t full[kStages];    // stage ready for the MMA: A (and BF16 B) bytes landed
-                             // and the 8 dequantising warps done (count 1 + 8, + tx)
-  uint64_t empty[kStages];   // MMAs done with the stage (tcgen05.commit)
-  uint64_t cfull[kCStages];  // code tile landed (count 1 + tx)
-  uint64_t cempty[kCStages]; // code tile read by the 8 dequantising warps
-  uint64_t acc_full;         // all MMAs of a unit done
-  uint64_t acc_empty;        // epilogue finished reading TMEM (count 8 warps)
+  uint64_t full[kStages];      // this CTA's stage is in: A (and BF16 B) bytes, and the
+                               // dequantising group's 4 warps (count 1 + 4, + tx)
+  uint64_t pfull[kStages];     // leader: the peer's stage is in (one remote arrive)
+  uint64_t empty[kStages];     // the pair's MMAs are done with the stage (commit, both CTAs)
+  uint64_t cfull[kCStages];    // code tile landed (count 1 + tx)
+  uint64_t cempty[kCStages];   // code tile read by its 4 dequantising warps
+  uint64_t acc_full[2];        // all MMAs of a unit done (commit, both CTAs)
+  uint64_t acc_empty[2];       // leader: the pair's 16 epilogue warps read the buffer
   uint32_t tmem;
   int abort;
 };
-// Block-scale ring of the dequantising threads: slot j of thread t at word
-// j * 256 + t, filled by asynchronous 4-byte copies kScaleAhead K blocks
-// ahead of use (slot kb % kScaleSlots, never the one being read).
-constexpr int kScaleSlots = 4;
-constexpr int kScaleAhead = 3;
-constexpr int kOffScale = kOffCodes + kCStages * kCodeBytes;
-constexpr int kScaleBytes = kScaleSlots * 512 * 4;
 constexpr size_t kGSmem = (size_t)kOffScale + kScaleBytes + sizeof(GCtl) + 1024;
 
+// Bounded waits (FLINT_ERR_TIMEOUT in the status word on expiry).  CL: the
+// barrier also receives the peer CTA's arrivals.
+template <bool CL = false>
 FLINT_DEV bool gwait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
-  if (mbar_test_wait(bar, parity)) return true;  // the common case: already complete
+  if (CL ? tc::mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
   unsigned long long t0 = 0;
   for (;;) {
     if (*abort) return false;
-    if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
+    if (CL ? tc::mbar_try_wait_cluster(bar, parity, kSuspendNs) : mbar_try_wait(bar, parity, kSuspendNs))
+      return true;
     const unsigned long long now = globaltimer_ns();
     if (t0 == 0) t0 = now;
     if (now - t0 > kWaitNs) {
@@ -117,11 +155,12 @@ FLINT_DEV bool gwait_warp(uint64_t* bar, uint32_t parity, volatile int* abort, i
 struct TMaps {
   CUtensorMap a_routed;  // x_perm [np, H] (GEMM1) / act [np, I] (GEMM2), box {64, 128}
   CUtensorMap a_shared;  // x [M, H] / sact [M, SI], box {64, 128}
-  CUtensorMap b_shared;  // shared_gu [2 SI, H] box {64, 32} / shared_down [H, SI] box {64, 128}
-  CUtensorMap codes;     // w13 [E 2I, H/2] bytes box {32, 64} / w2 [E H, I/2] box {32, 128}
+  CUtensorMap b_shared;  // shared_gu [2 SI, H] box {64, 32} / shared_down [H, SI] box {64, 64}
+  CUtensorMap codes;     // w13 [E 2I, H/2] bytes / w2 [E H, I/2], box {32, 64}
 };
 
-// One unit of work, the same in every role.
+// One pair unit, the same in every role of both CTAs: 256 token rows (CTA c
+// takes rows row0 + 128 c ..) by n weight rows (CTA c holds n / 2 of them).
 struct Unit {
   int shared;   // 0 routed, 1 shared expert
   int e;        // routed expert
@@ -129,9 +168,9 @@ struct Unit {
   int row_end;  // one past its last valid row
   int nt;       // N tile
   int K;        // reduction length
-  int halves;   // 128-row halves with valid rows (1 or 2)
-  int parts;    // accumulators per half (K block kb -> kb % parts)
-  int n;        // B rows (MMA N)
+  int parts;    // accumulators (K block kb -> kb % parts)
+  int n;        // B rows of the pair (MMA N)
+  int w;        // TMEM buffers taken (n * parts = w * kTmemBuf; two start at column 0)
 };
 
 template <int STAGE>
@@ -148,18 +187,19 @@ FLINT_DEV Unit unit_of(const MoEArgs& a, int u, int R, int NT, int NTs) {
     x.K = STAGE == 1 ? a.H : a.I;
   } else {
     const int v = u - R;
-    const int tile = STAGE == 1 ? 128 : kTokTile;  // shared gate/up: one half
     x.shared = 1;
     x.e = -1;
-    x.row0 = (v / NTs) * tile;
-    x.row_end = min(a.M, x.row0 + tile);
+    x.row0 = (v / NTs) * kTokTile;
+    x.row_end = min(a.M, x.row0 + kTokTile);
     x.nt = v % NTs;
     x.K = STAGE == 1 ? a.H : a.SI;
   }
-  x.halves = (x.row_end - x.row0 > 128) ? 2 : 1;
+  // the shared expert's gate/up keeps eight accumulators (both buffers),
+  // because its bf16(gS), bf16(uS) roundings feed every output of the token
   const bool sgu = x.shared && STAGE == 1;
   x.parts = sgu ? 8 : 2;
-  x.n = sgu ? 64 : kBRows;
+  x.n = sgu ? 64 : 128;
+  x.w = sgu ? 2 : 1;
   return x;
 }
 
@@ -183,33 +223,39 @@ FLINT_DEV void dequant_half(uint4 (&v)[4], const uint4 c0, uint32_t sc2) {
 }
 
 template <int STAGE>
-__global__ void __launch_bounds__(kGThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     grouped_gemm_kernel(const MoEArgs a, const __grid_constant__ TMaps tm, int NT, int NTs,
                         int n_shared_tiles) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   GCtl& C = *reinterpret_cast<GCtl*>(smem + (size_t)kOffScale + kScaleBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = tc::cluster_rank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   int* status = a.ws.status;
   volatile int* abort = &C.abort;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&C.full[i], 1 + 8);
+      mbar_init(&C.full[i], 1 + 4);
+      mbar_init(&C.pfull[i], 1);
       mbar_init(&C.empty[i], 1);
     }
     for (int i = 0; i < kCStages; ++i) {
       mbar_init(&C.cfull[i], 1);
-      mbar_init(&C.cempty[i], 8);
+      mbar_init(&C.cempty[i], 4);
     }
-    mbar_init(&C.acc_full, 1);
-    mbar_init(&C.acc_empty, 16);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&C.acc_full[b], 1);
+      mbar_init(&C.acc_empty[b], 16);
+    }
     C.abort = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) tc::tmem_alloc(&C.tmem, 512);
+  if (warp == kWarpMma) tc::tmem_alloc_pair(&C.tmem, 2 * kTmemBuf);
   tc::fence_before_sync();
-  __syncthreads();
+  tc::cluster_sync();  // both CTAs: barriers initialised, TMEM allocated
   tc::fence_after_sync();
   const uint32_t tmem = C.tmem;
 
@@ -220,9 +266,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
   const int total = R + n_shared_tiles * NTs;
 
   if (warp == kWarpProd) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------- stage producer
     int it = 0;
-    for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x) {
+    for (int u = pair; u < total && !*abort; u += npairs) {
       const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
       const int nkb = x.K / 64;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
@@ -233,18 +279,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (lane == 0) {
           uint8_t* st = smem + (size_t)s * kStageBytes;
           const CUtensorMap* ta = x.shared ? &tm.a_shared : &tm.a_routed;
-          uint32_t bytes = (uint32_t)x.halves * kTile;
-          if (x.shared) bytes += (uint32_t)x.n * 128u;
+          uint32_t bytes = kATile;
+          if (x.shared) bytes += (uint32_t)(x.n / 2) * 128u;
           mbar_arrive_expect_tx(&C.full[s], bytes);
-          tc::tma_load_2d(st + kOffA, ta, kb * 64, x.row0, &C.full[s]);
-          if (x.halves == 2) tc::tma_load_2d(st + kOffA + kTile, ta, kb * 64, x.row0 + 128, &C.full[s]);
+          tc::tma_load_2d(st + kOffA, ta, kb * 64, x.row0 + 128 * (int)rank, &C.full[s]);
           if (x.shared) {
-            if (STAGE == 1) {  // 32 gate rows, then 32 up rows
-              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, 32 * x.nt, &C.full[s]);
-              tc::tma_load_2d(st + kOffB + 32 * 128, &tm.b_shared, kb * 64, a.SI + 32 * x.nt, &C.full[s]);
-            } else {
-              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, 128 * x.nt, &C.full[s]);
-            }
+            if (STAGE == 1)  // leader 32 gate rows, peer the 32 matching up rows
+              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, (leader ? 0 : a.SI) + 32 * x.nt, &C.full[s]);
+            else
+              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, 128 * x.nt + 64 * (int)rank, &C.full[s]);
           }
         }
         __syncwarp();
@@ -255,7 +298,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     // Runs up to kCStages K blocks ahead of dequantisation; K blocks of the
     // shared expert (no codes) only advance the ring.
     int it = 0;
-    for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x) {
+    for (int u = pair; u < total && !*abort; u += npairs) {
       const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
       const int nkb = x.K / 64;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
@@ -267,62 +310,54 @@ __global__ void __launch_bounds__(kGThreads, 1)
           if (x.shared) {
             mbar_arrive(&C.cfull[c]);
           } else {
-            uint8_t* dst = smem + kOffCodes + c * kCodeBytes;
-            mbar_arrive_expect_tx(&C.cfull[c], (uint32_t)x.n * 32u);
-            if (STAGE == 1) {  // 64 gate rows, then 64 up rows
-              const int g0 = x.e * 2 * a.I + 64 * x.nt;
-              tc::tma_load_2d(dst, &tm.codes, kb * 32, g0, &C.cfull[c]);
-              tc::tma_load_2d(dst + 64 * 32, &tm.codes, kb * 32, g0 + a.I, &C.cfull[c]);
-            } else {
-              tc::tma_load_2d(dst, &tm.codes, kb * 32, x.e * a.H + 128 * x.nt, &C.cfull[c]);
-            }
+            // GEMM1: leader the expert's 64 gate rows of tile nt, peer its up rows
+            const int row = STAGE == 1 ? x.e * 2 * a.I + (leader ? 0 : a.I) + 64 * x.nt
+                                       : x.e * a.H + 128 * x.nt + 64 * (int)rank;
+            mbar_arrive_expect_tx(&C.cfull[c], (uint32_t)kCodeBytes);
+            tc::tma_load_2d(smem + kOffCodes + c * kCodeBytes, &tm.codes, kb * 32, row, &C.cfull[c]);
           }
         }
         __syncwarp();
       }
     }
   } else if (warp == kWarpMma) {
-    // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------- MMA issuer (leader)
       // descriptors of stage 0's tiles; a stage's are these plus its byte
       // offset / 16 (shared addresses stay below 2^18, inside the 14-bit field)
-      const uint64_t dA0 = tc::desc_sw128(smem + kOffA), dA1 = tc::desc_sw128(smem + kOffA + kTile);
-      const uint64_t dB = tc::desc_sw128(smem + kOffB);
-      // stage index, its phase bit and its descriptor offset run as counters
-      // (the issuing thread shares its scheduler with dequantising warps, so
-      // every instruction here costs)
-      int s = 0, nu = 0;
+      const uint64_t dA = tc::desc_sw128(smem + kOffA), dB = tc::desc_sw128(smem + kOffB);
+      // buffer uses are counted over both buffers: use sl goes to buffer
+      // sl % 2 and is that buffer's (sl / 2)-th
+      int s = 0, slot = 0;
       uint32_t ph = 0;
       uint64_t so = 0;
-      for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x, ++nu) {
+      for (int u = pair; u < total && !*abort; u += npairs) {
         const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
         const int nkb = x.K / 64;
-        const uint32_t idesc = tc::idesc_bf16(128, x.n);
+        const uint32_t idesc = tc::idesc_bf16(256, x.n);
         const uint32_t dwrap = (uint32_t)(x.n * x.parts);
-        if (nu > 0 && !gwait(&C.acc_empty, (nu - 1) & 1, abort, status)) break;
-        tc::fence_after_sync();
         bool ok = true;
-        uint32_t dcol = 0;  // accumulator of K block kb: columns x.n * (kb % parts)
+        // the buffers' previous units have been read out by both CTAs
+        for (int i = 0; i < x.w && ok; ++i) {
+          const int sl = slot + i;
+          if (sl >= 2) ok = gwait<true>(&C.acc_empty[sl & 1], ((sl >> 1) - 1) & 1, abort, status);
+        }
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t dbuf = tmem + (x.w == 2 ? 0u : (uint32_t)(kTmemBuf * (slot & 1)));
+        uint32_t dcol = 0;  // accumulator of K block kb: columns n * (kb % parts)
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!gwait(&C.full[s], ph, abort, status)) {
+          if (!gwait(&C.full[s], ph, abort, status) || !gwait<true>(&C.pfull[s], ph, abort, status)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const uint64_t da0 = dA0 + so, da1 = dA1 + so, db = dB + so;
-          const uint32_t d0 = tmem + dcol, d1 = d0 + 256;
+          const uint64_t da = dA + so, db = dB + so;
+          const uint32_t d = dbuf + dcol;
           const bool acc = kb >= x.parts;
-          if (x.halves == 2) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              tc::mma_bf16(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc || kk > 0);
-              tc::mma_bf16(d1, da1 + 2 * kk, db + 2 * kk, idesc, acc || kk > 0);
-            }
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(d0, da0 + 2 * kk, db + 2 * kk, idesc, acc || kk > 0);
-          }
-          tc::commit(&C.empty[s]);
+          for (int kk = 0; kk < 4; ++kk) tc::mma_bf16_pair(d, da + 2 * kk, db + 2 * kk, idesc, acc || kk > 0);
+          tc::commit_pair(&C.empty[s]);
           dcol += (uint32_t)x.n;
           if (dcol == dwrap) dcol = 0;
           so += (uint64_t)(kStageBytes >> 4);
@@ -333,40 +368,63 @@ __global__ void __launch_bounds__(kGThreads, 1)
           }
         }
         if (!ok) break;
-        tc::commit(&C.acc_full);
+        for (int i = 0; i < x.w; ++i) tc::commit_pair(&C.acc_full[(slot + i) & 1]);
+        slot += x.w;
+      }
+    } else if (lane == 0) {
+      // --------------------------------------------------- relay (peer CTA)
+      // tells the leader when this CTA's part of each stage is in
+      int s = 0;
+      uint32_t ph = 0;
+      for (int u = pair; u < total && !*abort; u += npairs) {
+        const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
+        const int nkb = x.K / 64;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!gwait(&C.full[s], ph, abort, status)) {
+            ok = false;
+            break;
+          }
+          // the stage's A (TMA) and B (dequantised, made visible to the async
+          // proxy) are writes to this CTA's shared memory
+          tc::mbar_arrive_remote_smem(tc::mapa(&C.pfull[s], 0));
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
       }
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------- dequant (B) and epilogue
-    // Two groups of 8 warps take alternate K blocks (global K block index
+  } else if (dq_index(warp) >= 0) {
+    // ------------------------------------------------------- dequantisation
+    // Two groups of 4 warps take alternate K blocks (global K block index
     // it: group it % 2), so each warp has two K blocks' time for one.
-    const int grp = warp >> 3;
-    const int tg = threadIdx.x & 255;
-    const int r = tg >> 1, jh = tg & 1;  // B row, half of its K block
-    // epilogue: TMEM lane quarter, 128-token half, column group
-    const int q = warp & 3, half = (warp >> 2) & 1, cg = warp >> 3;
-    int it = 0, nu = 0;
-    for (int u = blockIdx.x; u < total && !*abort; u += gridDim.x, ++nu) {
+    const int dq = dq_index(warp);
+    const int grp = dq >> 2;
+    const int dqt = dq * 32 + lane;      // 0..255
+    const int tg = dqt & 127;
+    const int r = tg >> 1, jh = tg & 1;  // B row of this CTA, half of its K block
+    int it = 0;
+    for (int u = pair; u < total && !*abort; u += npairs) {
       const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
       const int nkb = x.K / 64;
-      const uint8_t* sfrow = nullptr;  // block scales of B row r (4 bytes per K block)
+      const uint8_t* sfrow = nullptr;  // block scales of the row (4 bytes per K block)
       if (!x.shared) {
         if (STAGE == 1) {
-          const size_t row = (size_t)x.e * 2 * a.I + (r < 64 ? 64 * x.nt + r : a.I + 64 * x.nt + (r - 64));
+          const size_t row = (size_t)x.e * 2 * a.I + (leader ? 0 : a.I) + 64 * x.nt + r;
           sfrow = a.w13_sf + row * (a.H / 16);
-        } else if (128 * x.nt + r < a.H) {  // rows past H (last tile) are not read
-          sfrow = a.w2_sf + ((size_t)x.e * a.H + 128 * x.nt + r) * (a.I / 16);
+        } else {
+          sfrow = a.w2_sf + ((size_t)x.e * a.H + 128 * x.nt + 64 * rank + r) * (a.I / 16);
         }
       }
       const int kb0 = (grp - it) & 1;  // this group's first K block of the unit
       const int nmine = (nkb - kb0 + 1) / 2;
-      // the row's 4 scale bytes of this group's j-th K block come through the
-      // scale ring; one copy group per K block, empty past the row's end
-      uint32_t* ring = reinterpret_cast<uint32_t*>(smem + kOffScale) + threadIdx.x;
+      uint32_t* ring = reinterpret_cast<uint32_t*>(smem + kOffScale) + dqt;
       auto sc_fetch = [&](int j) {
         const int kb = kb0 + 2 * j;
-        if (sfrow && kb < nkb) cp_async4(ring + (j % kScaleSlots) * 512, sfrow + 4 * kb);
+        if (sfrow && kb < nkb) cp_async4(ring + (j % kScaleSlots) * kDqThreads, sfrow + 4 * kb);
         cp_async_commit();
       };
       cp_async_wait_all();  // nothing of the previous unit in flight
@@ -377,7 +435,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int itk = it + kb0 + 2 * j;
         const int s = itk % kStages, c = itk % kCStages;
         cp_async_wait_group<kScaleAhead - 1>();  // this K block's group has landed
-        const uint32_t sc = sfrow ? (ring[(j % kScaleSlots) * 512] >> (16 * jh)) & 0xFFFFu : 0u;
+        const uint32_t sc = sfrow ? (ring[(j % kScaleSlots) * kDqThreads] >> (16 * jh)) & 0xFFFFu : 0u;
         sc_fetch(j + kScaleAhead);
         // codes of the K block (landed well ahead): into registers, slot released
         if (!gwait_warp(&C.cfull[c], (itk / kCStages) & 1, abort, status, lane)) {
@@ -406,106 +464,123 @@ __global__ void __launch_bounds__(kGThreads, 1)
       }
       if (!ok) break;
       it += nkb;
-
-      // ---- epilogue: accumulator `half`, TMEM lanes 32 q .. 32 q + 31,
-      // column group cg (half of the unit's output columns), 16 at a time
-      if (!gwait_warp(&C.acc_full, nu & 1, abort, status, lane)) break;
+    }
+    cp_async_wait_all();  // no copy may land after the block has exited
+  } else if (epi_group(warp) >= 0) {
+    // ------------------------------------------------------------ epilogue
+    // TMEM lane quarter warp % 4 (lane = token row of this CTA), column half
+    // epi_group(warp) of the unit's outputs, 16 columns at a time; the
+    // accumulator buffers alternate, so this overlaps the next unit's MMAs.
+    const int q = warp & 3, cg = epi_group(warp);
+    int slot = 0;
+    for (int u = pair; u < total && !*abort; u += npairs) {
+      const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
+      bool ok = true;
+      for (int i = 0; i < x.w && ok; ++i) {
+        const int sl = slot + i;
+        ok = gwait_warp(&C.acc_full[sl & 1], (sl >> 1) & 1, abort, status, lane);
+      }
+      if (!ok) break;
       tc::fence_after_sync();
-      const int row = x.row0 + 128 * half + 32 * q + lane;
-      const bool valid = half < x.halves && row < x.row_end;
-      const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + 256 * half;
-      if (half < x.halves) {
-        const int nparts = min(x.parts, x.K / 64);
-        if (STAGE == 1) {
-          const int I = x.shared ? a.SI : a.I;
-          const int hw = x.n / 2;  // intermediate rows of the unit: gate cols [0, hw), up [hw, n)
-          uint16_t* dst = (x.shared ? a.ws.sact : a.ws.act) + (size_t)row * I + hw * x.nt;
-          const float gs = x.shared ? 1.0f : a.w13_gs[x.e] * 128.0f;
-          for (int c0 = cg * (hw / 2); c0 < (cg + 1) * (hw / 2); c0 += 16) {
-            uint32_t gv[16], uv[16], t2[16], t3[16];
-            tc::tmem_ld16_async(tb + c0, gv);       // gate rows, partial 0
-            tc::tmem_ld16_async(tb + hw + c0, uv);  // up rows, partial 0
+      const int row = x.row0 + 128 * (int)rank + 32 * q + lane;
+      const bool valid = row < x.row_end;
+      const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + (x.w == 2 ? 0u : (uint32_t)(kTmemBuf * (slot & 1)));
+      const int nparts = min(x.parts, x.K / 64);
+      if (STAGE == 1) {
+        const int I = x.shared ? a.SI : a.I;
+        const int hw = x.n / 2;  // intermediate columns of the unit: gate [0, hw), up [hw, n)
+        uint16_t* dst = (x.shared ? a.ws.sact : a.ws.act) + (size_t)row * I + hw * x.nt;
+        const float gs = x.shared ? 1.0f : a.w13_gs[x.e] * 128.0f;
+        const int cw = hw / 2 < 16 ? 16 : hw / 2;  // columns of this column group
+        for (int c0 = cg * cw; c0 < min(hw, (cg + 1) * cw); c0 += 16) {
+          uint32_t gv[16], uv[16], t2[16], t3[16];
+          tc::tmem_ld16_async(tb + c0, gv);       // gate, partial 0
+          tc::tmem_ld16_async(tb + hw + c0, uv);  // up, partial 0
+          tc::tmem_wait_ld();
+          tc::tmem_regs_ready16(gv);
+          tc::tmem_regs_ready16(uv);
+          for (int p = 1; p < nparts; ++p) {  // each partial's gate and up together
+            tc::tmem_ld16_async(tb + x.n * p + c0, t2);
+            tc::tmem_ld16_async(tb + x.n * p + hw + c0, t3);
             tc::tmem_wait_ld();
-            tc::tmem_regs_ready16(gv);
-            tc::tmem_regs_ready16(uv);
-            for (int p = 1; p < nparts; ++p) {  // each partial's gate and up together
-              tc::tmem_ld16_async(tb + x.n * p + c0, t2);
-              tc::tmem_ld16_async(tb + x.n * p + hw + c0, t3);
-              tc::tmem_wait_ld();
-              tc::tmem_regs_ready16(t2);
-              tc::tmem_regs_ready16(t3);
+            tc::tmem_regs_ready16(t2);
+            tc::tmem_regs_ready16(t3);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                gv[i] = __float_as_uint(__uint_as_float(gv[i]) + __uint_as_float(t2[i]));
-                uv[i] = __float_as_uint(__uint_as_float(uv[i]) + __uint_as_float(t3[i]));
-              }
-            }
-            uint32_t pk[8];
-#pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-              float v[2];
-#pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                const float gg = __uint_as_float(gv[i + j]), uu = __uint_as_float(uv[i + j]);
-                if (x.shared) {
-                  // stock BF16 SwiGLU: gS, uS rounded, silu(gS) = gS / (1 + exp(-gS))
-                  const float gS = round_bf16(gg), uS = round_bf16(uu);
-                  v[j] = __fdiv_rn(gS, 1.0f + expf(-gS)) * uS;
-                } else {
-                  v[j] = silu_approx(gg * gs) * (uu * gs);
-                }
-              }
-              pk[i / 2] = f32_to_bf16_bits(v[0]) | (f32_to_bf16_bits(v[1]) << 16);
-            }
-            if (valid) {
-              reinterpret_cast<uint4*>(dst + c0)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              reinterpret_cast<uint4*>(dst + c0)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            for (int i = 0; i < 16; ++i) {
+              gv[i] = __float_as_uint(__uint_as_float(gv[i]) + __uint_as_float(t2[i]));
+              uv[i] = __float_as_uint(__uint_as_float(uv[i]) + __uint_as_float(t3[i]));
             }
           }
-        } else {
-          uint16_t* dst = (x.shared ? a.ws.ys : a.ws.y) + (size_t)row * a.H + x.n * x.nt;
-          const float gs = x.shared ? 1.0f : a.w2_gs[x.e] * 128.0f;
-          const int ncols = min(x.n, a.H - x.n * x.nt);  // the last tile of H may be partial
-          for (int c0 = cg * (x.n / 2); c0 < (cg + 1) * (x.n / 2); c0 += 16) {
-            uint32_t v[16], t2[16];
-            tc::tmem_ld16_async(tb + c0, v);
-            if (nparts > 1) tc::tmem_ld16_async(tb + x.n + c0, t2);
-            tc::tmem_wait_ld();
-            tc::tmem_regs_ready16(v);
-            tc::tmem_regs_ready16(t2);
-            for (int p = 1; p < nparts; ++p) {
-              if (p > 1) {
-                tc::tmem_ld16_async(tb + x.n * p + c0, t2);
-                tc::tmem_wait_ld();
-                tc::tmem_regs_ready16(t2);
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            float v[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const float gg = __uint_as_float(gv[i + j]), uu = __uint_as_float(uv[i + j]);
+              if (x.shared) {
+                // stock BF16 SwiGLU: gS, uS rounded, silu(gS) = gS / (1 + exp(-gS))
+                const float gS = round_bf16(gg), uS = round_bf16(uu);
+                v[j] = __fdiv_rn(gS, 1.0f + expf(-gS)) * uS;
+              } else {
+                v[j] = silu_approx(gg * gs) * (uu * gs);
               }
-#pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(t2[i]));
             }
-            uint32_t pk[8];
-#pragma unroll
-            for (int i = 0; i < 16; i += 2)
-              pk[i / 2] = f32_to_bf16_bits(__uint_as_float(v[i]) * gs) |
-                          (f32_to_bf16_bits(__uint_as_float(v[i + 1]) * gs) << 16);
-            if (valid && c0 < ncols) {
-              reinterpret_cast<uint4*>(dst + c0)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              reinterpret_cast<uint4*>(dst + c0)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            pk[i / 2] = f32_to_bf16_bits(v[0]) | (f32_to_bf16_bits(v[1]) << 16);
+          }
+          if (valid) {
+            reinterpret_cast<uint4*>(dst + c0)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            reinterpret_cast<uint4*>(dst + c0)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      } else {
+        uint16_t* dst = (x.shared ? a.ws.ys : a.ws.y) + (size_t)row * a.H + x.n * x.nt;
+        const float gs = x.shared ? 1.0f : a.w2_gs[x.e] * 128.0f;
+        for (int c0 = cg * (x.n / 2); c0 < (cg + 1) * (x.n / 2); c0 += 16) {
+          uint32_t v[16], t2[16];
+          tc::tmem_ld16_async(tb + c0, v);
+          if (nparts > 1) tc::tmem_ld16_async(tb + x.n + c0, t2);
+          tc::tmem_wait_ld();
+          tc::tmem_regs_ready16(v);
+          tc::tmem_regs_ready16(t2);
+          for (int p = 1; p < nparts; ++p) {
+            if (p > 1) {
+              tc::tmem_ld16_async(tb + x.n * p + c0, t2);
+              tc::tmem_wait_ld();
+              tc::tmem_regs_ready16(t2);
             }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(t2[i]));
+          }
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 16; i += 2)
+            pk[i / 2] = f32_to_bf16_bits(__uint_as_float(v[i]) * gs) |
+                        (f32_to_bf16_bits(__uint_as_float(v[i + 1]) * gs) << 16);
+          if (valid) {
+            reinterpret_cast<uint4*>(dst + c0)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            reinterpret_cast<uint4*>(dst + c0)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
         }
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&C.acc_empty);
+      if (lane == 0) {
+        for (int i = 0; i < x.w; ++i) {
+          const int b = (slot + i) & 1;
+          if (leader) mbar_arrive(&C.acc_empty[b]);
+          else tc::mbar_arrive_remote(tc::mapa(&C.acc_empty[b], 0));
+        }
+      }
+      slot += x.w;
     }
-    cp_async_wait_all();  // no copy may land after the block has exited
   }
 
   tc::fence_before_sync();
-  __syncthreads();
+  tc::cluster_sync();  // no CTA leaves while its peer may still reach its memory
   if (warp == kWarpMma) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, 512);
+    tc::tmem_dealloc_pair(tmem, 2 * kTmemBuf);
   }
 }
 
@@ -630,6 +705,7 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, void*
 
 struct GDev {
   int sms = 0;
+  int pairs = 0;  // CTA pairs of the GEMM grid (all co-resident)
   bool attrs = false;
 };
 GDev g_gdev[64];
@@ -662,6 +738,16 @@ cudaError_t launch_grouped(const MoEArgs& a, cudaStream_t st) {
     err = cudaFuncSetAttribute((const void*)grouped_gemm_kernel<2>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
     if (err != cudaSuccess) return err;
+    // persistent pairs: as many clusters of two as can be resident at once
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gd.sms & ~1);
+    cfg.blockDim = dim3(kGThreads);
+    cfg.dynamicSmemBytes = kGSmem;
+    int nclusters = 0;
+    err = cudaOccupancyMaxActiveClusters(&nclusters, (const void*)grouped_gemm_kernel<1>, &cfg);
+    if (err != cudaSuccess) return err;
+    if (nclusters < 1) return cudaErrorNotSupported;
+    gd.pairs = nclusters < gd.sms / 2 ? nclusters : gd.sms / 2;
     gd.attrs = true;
   }
   const uint64_t np = (uint64_t)a.M * a.k;
@@ -671,11 +757,11 @@ cudaError_t launch_grouped(const MoEArgs& a, cudaStream_t st) {
             make_map(&t1.a_shared, a.x, true, a.M, H, 64, 128) &&
             make_map(&t1.codes, a.w13, false, (uint64_t)E * 2 * I, H / 2, 32, 64) &&
             make_map(&t2.a_routed, a.ws.act, true, np, I, 64, 128) &&
-            make_map(&t2.codes, a.w2, false, (uint64_t)E * H, I / 2, 32, 128);
+            make_map(&t2.codes, a.w2, false, (uint64_t)E * H, I / 2, 32, 64);
   if (ok && SI > 0)
     ok = make_map(&t1.b_shared, a.shared_gu, true, 2 * (uint64_t)SI, H, 64, 32) &&
          make_map(&t2.a_shared, a.ws.sact, true, a.M, SI, 64, 128) &&
-         make_map(&t2.b_shared, a.shared_down, true, H, SI, 64, 128);
+         make_map(&t2.b_shared, a.shared_down, true, H, SI, 64, 64);
   if (!ok) return cudaErrorInvalidValue;
 
   err = launch_route(a, true, st, false);
@@ -686,14 +772,16 @@ cudaError_t launch_grouped(const MoEArgs& a, cudaStream_t st) {
   if (err != cudaSuccess) return err;
   err = launch_pdl((const void*)gather_kernel, dim3((unsigned)((np + 7) / 8)), dim3(256), 0, args0, st);
   if (err != cudaSuccess) return err;
-  const int nsh1 = SI > 0 ? (a.M + 127) / 128 : 0;             // shared gate/up: 128 tokens
-  const int nsh2 = SI > 0 ? (a.M + kTokTile - 1) / kTokTile : 0;
-  int NT1 = I / 64, NTs1 = SI > 0 ? SI / 32 : 1, NT2 = H / kBRows, NTs2 = H / kBRows;
-  void* args1[] = {&aa, &t1, &NT1, &NTs1, (void*)&nsh1};
-  err = launch_pdl((const void*)grouped_gemm_kernel<1>, dim3(gd.sms), dim3(kGThreads), kGSmem, args1, st);
+  // pair units: 256 token rows by 128 weight rows (GEMM1: 64 gate + 64 up
+  // intermediate rows; the shared expert's gate/up 32 + 32), GEMM2 128 output rows
+  const int nsh = SI > 0 ? (a.M + kTokTile - 1) / kTokTile : 0;
+  int NT1 = I / 64, NTs1 = SI > 0 ? SI / 32 : 1, NT2 = H / 128, NTs2 = H / 128;
+  const dim3 grid(2 * gd.pairs);
+  void* args1[] = {&aa, &t1, &NT1, &NTs1, (void*)&nsh};
+  err = launch_pdl((const void*)grouped_gemm_kernel<1>, grid, dim3(kGThreads), kGSmem, args1, st);
   if (err != cudaSuccess) return err;
-  void* args2[] = {&aa, &t2, &NT2, &NTs2, (void*)&nsh2};
-  err = launch_pdl((const void*)grouped_gemm_kernel<2>, dim3(gd.sms), dim3(kGThreads), kGSmem, args2, st);
+  void* args2[] = {&aa, &t2, &NT2, &NTs2, (void*)&nsh};
+  err = launch_pdl((const void*)grouped_gemm_kernel<2>, grid, dim3(kGThreads), kGSmem, args2, st);
   if (err != cudaSuccess) return err;
   const size_t nthr = (size_t)a.M * (H / 8);
   return launch_pdl((const void*)combine_kernel, dim3((unsigned)((nthr + 255) / 256)), dim3(256), 0,

@@ -89,19 +89,20 @@ FLINT_DEV int epi_group(int warp) {
 }
 constexpr int kStages = 6;
 constexpr int kATile = 128 * 128;                  // 128 token rows x 64 bf16
-constexpr int kBRows = 64;                         // B rows per CTA: N = 128 per pair
+constexpr int kBRows = 128;                        // B rows per CTA: N = 256 per pair
 constexpr int kOffA = 0;
 constexpr int kOffB = kATile;
-constexpr int kStageBytes = kATile + kBRows * 128;  // 24576
+constexpr int kStageBytes = kATile + kBRows * 128;  // 32768
 static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
 // NVFP4 code tiles (kBRows rows x 32 bytes per K block) have a ring of their
 // own, deeper than the stages, so they land well before they are dequantised.
-constexpr int kCStages = 8;
+constexpr int kCStages = 6;
 constexpr int kCodeBytes = kBRows * 32;
 constexpr int kOffCodes = kStages * kStageBytes;
-// Block-scale ring of the 256 dequantising threads: slot j of thread t at
-// word j * 256 + t, filled by asynchronous 4-byte copies kScaleAhead of the
-// thread's K blocks ahead of use (slot j % kScaleSlots, never the one read).
+// Block-scale ring of the 256 dequantising threads (thread = B row of its
+// group): slot j of thread t at word j * 256 + t, filled by asynchronous
+// 4-byte copies kScaleAhead of the thread's K blocks ahead of use (slot
+// j % kScaleSlots, never the one read).
 constexpr int kScaleSlots = 4;
 constexpr int kScaleAhead = 3;
 constexpr int kDqThreads = 256;
@@ -155,8 +156,8 @@ FLINT_DEV bool gwait_warp(uint64_t* bar, uint32_t parity, volatile int* abort, i
 struct TMaps {
   CUtensorMap a_routed;  // x_perm [np, H] (GEMM1) / act [np, I] (GEMM2), box {64, 128}
   CUtensorMap a_shared;  // x [M, H] / sact [M, SI], box {64, 128}
-  CUtensorMap b_shared;  // shared_gu [2 SI, H] box {64, 32} / shared_down [H, SI] box {64, 64}
-  CUtensorMap codes;     // w13 [E 2I, H/2] bytes / w2 [E H, I/2], box {32, 64}
+  CUtensorMap b_shared;  // shared_gu [2 SI, H] box {64, 32} / shared_down [H, SI] box {64, 128}
+  CUtensorMap codes;     // w13 [E 2I, H/2] bytes / w2 [E H, I/2], box {32, 128}
 };
 
 // One pair unit, the same in every role of both CTAs: 256 token rows (CTA c
@@ -169,7 +170,7 @@ struct Unit {
   int nt;       // N tile
   int K;        // reduction length
   int parts;    // accumulators (K block kb -> kb % parts)
-  int n;        // B rows of the pair (MMA N)
+  int n;        // B rows of the pair (MMA N): n / 2 from each CTA
   int w;        // TMEM buffers taken (n * parts = w * kTmemBuf; two start at column 0)
 };
 
@@ -194,12 +195,15 @@ FLINT_DEV Unit unit_of(const MoEArgs& a, int u, int R, int NT, int NTs) {
     x.nt = v % NTs;
     x.K = STAGE == 1 ? a.H : a.SI;
   }
-  // the shared expert's gate/up keeps eight accumulators (both buffers),
-  // because its bf16(gS), bf16(uS) roundings feed every output of the token
+  // Routed units: N = 256 (GEMM1: 128 gate + 128 up rows of tile nt; GEMM2:
+  // output rows 256 nt ..), one accumulator, one TMEM buffer.  The shared
+  // expert keeps more accumulators (both buffers): its gate/up eight at
+  // N = 64 (its bf16(gS), bf16(uS) roundings feed every output of the token),
+  // its down two (its rounded ys is added to every output).
   const bool sgu = x.shared && STAGE == 1;
-  x.parts = sgu ? 8 : 2;
-  x.n = sgu ? 64 : 128;
-  x.w = sgu ? 2 : 1;
+  x.parts = sgu ? 8 : (x.shared ? 2 : 1);
+  x.n = sgu ? 64 : 256;
+  x.w = x.shared ? 2 : 1;
   return x;
 }
 
@@ -286,8 +290,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
           if (x.shared) {
             if (STAGE == 1)  // leader 32 gate rows, peer the 32 matching up rows
               tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, (leader ? 0 : a.SI) + 32 * x.nt, &C.full[s]);
-            else
-              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, 128 * x.nt + 64 * (int)rank, &C.full[s]);
+            else  // rows past H (last tile) read as zeros
+              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, 256 * x.nt + 128 * (int)rank, &C.full[s]);
           }
         }
         __syncwarp();
@@ -310,9 +314,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
           if (x.shared) {
             mbar_arrive(&C.cfull[c]);
           } else {
-            // GEMM1: leader the expert's 64 gate rows of tile nt, peer its up rows
-            const int row = STAGE == 1 ? x.e * 2 * a.I + (leader ? 0 : a.I) + 64 * x.nt
-                                       : x.e * a.H + 128 * x.nt + 64 * (int)rank;
+            // GEMM1: leader the expert's 128 gate rows of tile nt, peer its up
+            // rows; GEMM2: 128 output rows each (past H: the next expert's
+            // rows, or zeros past the tensor; never stored)
+            const int row = STAGE == 1 ? x.e * 2 * a.I + (leader ? 0 : a.I) + 128 * x.nt
+                                       : x.e * a.H + 256 * x.nt + 128 * (int)rank;
             mbar_arrive_expect_tx(&C.cfull[c], (uint32_t)kCodeBytes);
             tc::tma_load_2d(smem + kOffCodes + c * kCodeBytes, &tm.codes, kb * 32, row, &C.cfull[c]);
           }
@@ -404,8 +410,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     const int dq = dq_index(warp);
     const int grp = dq >> 2;
     const int dqt = dq * 32 + lane;      // 0..255
-    const int tg = dqt & 127;
-    const int r = tg >> 1, jh = tg & 1;  // B row of this CTA, half of its K block
+    const int r = dqt & 127;             // B row of this CTA
     int it = 0;
     for (int u = pair; u < total && !*abort; u += npairs) {
       const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
@@ -413,10 +418,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
       const uint8_t* sfrow = nullptr;  // block scales of the row (4 bytes per K block)
       if (!x.shared) {
         if (STAGE == 1) {
-          const size_t row = (size_t)x.e * 2 * a.I + (leader ? 0 : a.I) + 64 * x.nt + r;
+          const size_t row = (size_t)x.e * 2 * a.I + (leader ? 0 : a.I) + 128 * x.nt + r;
           sfrow = a.w13_sf + row * (a.H / 16);
-        } else {
-          sfrow = a.w2_sf + ((size_t)x.e * a.H + 128 * x.nt + 64 * rank + r) * (a.I / 16);
+        } else if (256 * x.nt + 128 * (int)rank + r < a.H) {  // rows past H are not read
+          sfrow = a.w2_sf + ((size_t)x.e * a.H + 256 * x.nt + 128 * rank + r) * (a.I / 16);
         }
       }
       const int kb0 = (grp - it) & 1;  // this group's first K block of the unit
@@ -435,19 +440,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
         const int itk = it + kb0 + 2 * j;
         const int s = itk % kStages, c = itk % kCStages;
         cp_async_wait_group<kScaleAhead - 1>();  // this K block's group has landed
-        const uint32_t sc = sfrow ? (ring[(j % kScaleSlots) * kDqThreads] >> (16 * jh)) & 0xFFFFu : 0u;
+        const uint32_t sc = sfrow ? ring[(j % kScaleSlots) * kDqThreads] : 0u;  // 4 block scales
         sc_fetch(j + kScaleAhead);
         // codes of the K block (landed well ahead): into registers, slot released
         if (!gwait_warp(&C.cfull[c], (itk / kCStages) & 1, abort, status, lane)) {
           ok = false;
           break;
         }
-        uint4 codes = make_uint4(0, 0, 0, 0);
-        if (!x.shared) codes = *reinterpret_cast<const uint4*>(smem + kOffCodes + c * kCodeBytes + r * 32 + 16 * jh);
+        uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
+        if (!x.shared) {
+          const uint4* cr = reinterpret_cast<const uint4*>(smem + kOffCodes + c * kCodeBytes + r * 32);
+          c0 = cr[0];
+          c1 = cr[1];
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&C.cempty[c]);
-        uint4 bv[4];
-        if (!x.shared) dequant_half(bv, codes, sc);
+        uint4 bv0[4], bv1[4];  // K 0..31, 32..63
+        if (!x.shared) {
+          dequant_half(bv0, c0, sc & 0xFFFFu);
+          dequant_half(bv1, c1, sc >> 16);
+        }
         // the stage's previous MMAs are done: its B area is free
         if (itk >= kStages && !gwait_warp(&C.empty[s], ((itk / kStages) - 1) & 1, abort, status, lane)) {
           ok = false;
@@ -456,7 +468,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
         if (!x.shared) {
           uint8_t* bt = smem + (size_t)s * kStageBytes + kOffB;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(bt + tc::sw128_offset(r, 32 * jh + 8 * i)) = bv[i];
+          for (int i = 0; i < 4; ++i) {
+            *reinterpret_cast<uint4*>(bt + tc::sw128_offset(r, 8 * i)) = bv0[i];
+            *reinterpret_cast<uint4*>(bt + tc::sw128_offset(r, 32 + 8 * i)) = bv1[i];
+          }
           tc::fence_proxy_async_smem();
         }
         __syncwarp();
@@ -536,7 +551,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
       } else {
         uint16_t* dst = (x.shared ? a.ws.ys : a.ws.y) + (size_t)row * a.H + x.n * x.nt;
         const float gs = x.shared ? 1.0f : a.w2_gs[x.e] * 128.0f;
-        for (int c0 = cg * (x.n / 2); c0 < (cg + 1) * (x.n / 2); c0 += 16) {
+        const int ncols = min(x.n, a.H - x.n * x.nt);  // the last tile of H may be partial
+        for (int c0 = cg * (x.n / 2); c0 < min(ncols, (cg + 1) * (x.n / 2)); c0 += 16) {
           uint32_t v[16], t2[16];
           tc::tmem_ld16_async(tb + c0, v);
           if (nparts > 1) tc::tmem_ld16_async(tb + x.n + c0, t2);
@@ -755,13 +771,13 @@ cudaError_t launch_grouped(const MoEArgs& a, cudaStream_t st) {
   TMaps t1{}, t2{};
   bool ok = make_map(&t1.a_routed, a.ws.x_perm, true, np, H, 64, 128) &&
             make_map(&t1.a_shared, a.x, true, a.M, H, 64, 128) &&
-            make_map(&t1.codes, a.w13, false, (uint64_t)E * 2 * I, H / 2, 32, 64) &&
+            make_map(&t1.codes, a.w13, false, (uint64_t)E * 2 * I, H / 2, 32, 128) &&
             make_map(&t2.a_routed, a.ws.act, true, np, I, 64, 128) &&
-            make_map(&t2.codes, a.w2, false, (uint64_t)E * H, I / 2, 32, 64);
+            make_map(&t2.codes, a.w2, false, (uint64_t)E * H, I / 2, 32, 128);
   if (ok && SI > 0)
     ok = make_map(&t1.b_shared, a.shared_gu, true, 2 * (uint64_t)SI, H, 64, 32) &&
          make_map(&t2.a_shared, a.ws.sact, true, a.M, SI, 64, 128) &&
-         make_map(&t2.b_shared, a.shared_down, true, H, SI, 64, 64);
+         make_map(&t2.b_shared, a.shared_down, true, H, SI, 64, 128);
   if (!ok) return cudaErrorInvalidValue;
 
   err = launch_route(a, true, st, false);
@@ -772,10 +788,11 @@ cudaError_t launch_grouped(const MoEArgs& a, cudaStream_t st) {
   if (err != cudaSuccess) return err;
   err = launch_pdl((const void*)gather_kernel, dim3((unsigned)((np + 7) / 8)), dim3(256), 0, args0, st);
   if (err != cudaSuccess) return err;
-  // pair units: 256 token rows by 128 weight rows (GEMM1: 64 gate + 64 up
-  // intermediate rows; the shared expert's gate/up 32 + 32), GEMM2 128 output rows
+  // pair units: 256 token rows by 256 weight rows (GEMM1: 128 gate + 128 up
+  // intermediate rows; the shared expert's gate/up 32 + 32), GEMM2 256
+  // output rows (the last tile of H may be half)
   const int nsh = SI > 0 ? (a.M + kTokTile - 1) / kTokTile : 0;
-  int NT1 = I / 64, NTs1 = SI > 0 ? SI / 32 : 1, NT2 = H / 128, NTs2 = H / 128;
+  int NT1 = I / 128, NTs1 = SI > 0 ? SI / 32 : 1, NT2 = (H + 255) / 256, NTs2 = NT2;
   const dim3 grid(2 * gd.pairs);
   void* args1[] = {&aa, &t1, &NT1, &NTs1, (void*)&nsh};
   err = launch_pdl((const void*)grouped_gemm_kernel<1>, grid, dim3(kGThreads), kGSmem, args1, st);

@@ -127,39 +127,71 @@ FLINT_DEV float router_dot(const uint16_t* xrow, const uint4 (&wreg)[8], const u
   return acc;
 }
 
-// router_dot for NT tokens at once from shared memory (H <= 2048): the same
-// per-token sequence of fmaf and the same butterfly, with the NT independent
-// chains interleaved so that they overlap in the pipeline.
-template <int NT>
-FLINT_DEV void router_dot_tile(float (&res)[NT], const uint16_t* xs0, int H, const uint4 (&wreg)[8],
-                               int lane) {
+// router_dot for a block of 4 experts x 4 tokens (H <= 2048): every
+// (expert, token) chain is the same per-lane sequence of fmaf (chunk c
+// ascending, element k ascending) and the same butterfly; the 16 chains run
+// side by side so that each x vector loaded from shared memory feeds four
+// experts and each router vector four tokens.  x is in fp32 in shared memory,
+// laid out [chunk c][half][lane][4] per token (2048 floats per token; lane
+// l's elements 256 c + 8 l + 4 half + 0..3).  Experts e >= E read row E - 1
+// and are not stored by the caller.
+FLINT_DEV void router_block_4x4(float (&res)[4][4], const float* xf0, const uint16_t* router_w,
+                                int e0, int E, int H, int lane) {
   const int nchunk = (H + 255) / 256;
-  float acc[NT];
+  float acc[4][4];
 #pragma unroll
-  for (int j = 0; j < NT; ++j) acc[j] = 0.0f;
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const int h = 256 * c + 8 * lane;
-    if (c < nchunk && h < H) {
-      const uint32_t ws[4] = {wreg[c].x, wreg[c].y, wreg[c].z, wreg[c].w};
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+  const uint16_t* wr[4];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        const uint4 xv = *reinterpret_cast<const uint4*>(xs0 + (size_t)j * H + h);
-        const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w};
+  for (int i = 0; i < 4; ++i) wr[i] = router_w + (size_t)min(e0 + i, E - 1) * H + 8 * lane;
+  // the router vectors of the next chunk are in flight while this one runs
+  const bool has0 = 8 * lane < H;
+  uint4 wn[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          acc[j] = fmaf(__uint_as_float(xq[q] << 16), __uint_as_float(ws[q] << 16), acc[j]);
-          acc[j] = fmaf(__uint_as_float(xq[q] & 0xFFFF0000u), __uint_as_float(ws[q] & 0xFFFF0000u), acc[j]);
-        }
+  for (int i = 0; i < 4; ++i) wn[i] = has0 ? ldg_nc_v4(wr[i]) : make_uint4(0, 0, 0, 0);
+  for (int c = 0; c < nchunk; ++c) {
+    const bool has = 256 * c + 8 * lane < H;
+    uint4 wq[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) wq[i] = wn[i];
+    const bool hasn = c + 1 < nchunk && 256 * (c + 1) + 8 * lane < H;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) wn[i] = hasn ? ldg_nc_v4(wr[i] + 256 * (c + 1)) : make_uint4(0, 0, 0, 0);
+    if (!has) continue;
+    float wf[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 q = wq[i];
+      const uint32_t ws[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        wf[i][2 * h] = __uint_as_float(ws[h] << 16);
+        wf[i][2 * h + 1] = __uint_as_float(ws[h] & 0xFFFF0000u);
       }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float* xp = xf0 + (size_t)j * 2048 + c * 256 + lane * 4;
+      const float4 lo = *reinterpret_cast<const float4*>(xp);
+      const float4 hi = *reinterpret_cast<const float4*>(xp + 128);
+      const float xv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i][j] = fmaf(xv[k], wf[i][k], acc[i][j]);
     }
   }
 #pragma unroll
-  for (int j = 0; j < NT; ++j) {
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) acc[j] = acc[j] + __shfl_xor_sync(0xffffffffu, acc[j], o);
-    res[j] = acc[j];
-  }
+    for (int j = 0; j < 4; ++j) {
+      float v = acc[i][j];
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, o);
+      res[i][j] = v;
+    }
 }
 
 FLINT_DEV void router_row_regs(uint4 (&wreg)[8], const uint16_t* wrow, int H, int lane, bool active) {
@@ -537,38 +569,57 @@ constexpr int kRtWarps = 16;
 
 __global__ void __launch_bounds__(kRtWarps * 32) route_tile_kernel(MoEArgs a) {
   extern __shared__ __align__(16) uint8_t rt_smem[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(rt_smem);                  // [16][H]
-  uint16_t* lg = xs + (size_t)kRtTokens * a.H;                          // [16][E]
+  const int H = a.H, E = a.E, k = a.k;
+  const bool f32 = H <= 2048;
+  float* xf = reinterpret_cast<float*>(rt_smem);      // H <= 2048: [16][2048] fp32, lane order
+  uint16_t* xs = reinterpret_cast<uint16_t*>(rt_smem);  // H > 2048: [16][H] bf16
+  uint16_t* lg = reinterpret_cast<uint16_t*>(rt_smem + (f32 ? (size_t)kRtTokens * 2048 * 4
+                                                             : (size_t)kRtTokens * H * 2));  // [16][E]
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int H = a.H, E = a.E, k = a.k;
   const int t0 = blockIdx.x * kRtTokens;
   const int nt = min(kRtTokens, a.M - t0);
   pdl_wait();
-  {  // stage the token rows (16-byte vectors)
-    const int nv = nt * H / 8;
+  {  // stage the token rows (16-byte vectors of 8 elements)
+    const int nvr = H / 8, nv = nt * nvr;
     const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t0 * H);
-    for (int i = threadIdx.x; i < nv; i += blockDim.x) reinterpret_cast<uint4*>(xs)[i] = ldg_cg_v4(src + i);
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+      const uint4 q = ldg_cg_v4(src + i);
+      if (f32) {  // vector v = h / 8 of token t goes to chunk v / 32, lane v % 32
+        const int t = i / nvr, v = i % nvr;
+        float* d = xf + (size_t)t * 2048 + (v >> 5) * 256 + (v & 31) * 4;
+        *reinterpret_cast<float4*>(d) = make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u),
+                                                    __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u));
+        *reinterpret_cast<float4*>(d + 128) = make_float4(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xFFFF0000u),
+                                                          __uint_as_float(q.w << 16), __uint_as_float(q.w & 0xFFFF0000u));
+      } else {
+        reinterpret_cast<uint4*>(xs)[i] = q;
+      }
+    }
   }
   __syncthreads();
-  for (int e = warp; e < E; e += kRtWarps) {
+  if (f32) {
+    // blocks of 4 experts x 4 tokens; chains of tokens past nt run on stale
+    // shared memory and are not stored
+    const int neb = (E + 3) / 4, ntb = (nt + 3) / 4;
+    for (int b = warp; b < neb * ntb; b += kRtWarps) {
+      const int e0 = 4 * (b / ntb), tb = 4 * (b % ntb);
+      float r[4][4];
+      router_block_4x4(r, xf + (size_t)tb * 2048, a.router_w, e0, E, H, lane);
+      if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (e0 + i < E && tb + j < nt) lg[(tb + j) * E + e0 + i] = (uint16_t)f32_to_bf16_bits(r[i][j]);
+      }
+    }
+  }
+  for (int e = warp; e < E && !f32; e += kRtWarps) {
     const uint16_t* wrow = a.router_w + (size_t)e * H;
     uint4 wreg[8];
     router_row_regs(wreg, wrow, H, lane, true);
-    if (H <= 2048) {
-      int t = 0;
-      for (; t + 4 <= nt; t += 4) {  // four tokens' chains interleaved
-        float r4[4];
-        router_dot_tile<4>(r4, xs + (size_t)t * H, H, wreg, lane);
-        if (lane == 0)
-          for (int j = 0; j < 4; ++j) lg[(t + j) * E + e] = (uint16_t)f32_to_bf16_bits(r4[j]);
-      }
-      for (; t < nt; ++t) {
-        float r1[1];
-        router_dot_tile<1>(r1, xs + (size_t)t * H, H, wreg, lane);
-        if (lane == 0) lg[t * E + e] = (uint16_t)f32_to_bf16_bits(r1[0]);
-      }
-    } else {
+    {
       for (int t = 0; t < nt; ++t) {
         const float acc = router_dot<true>(xs + (size_t)t * H, wreg, wrow, H, lane);
         if (lane == 0) lg[t * E + e] = (uint16_t)f32_to_bf16_bits(acc);
@@ -591,7 +642,8 @@ __global__ void __launch_bounds__(kRtWarps * 32) route_tile_kernel(MoEArgs a) {
 }
 
 size_t route_tile_smem(const MoEArgs& a) {
-  return (size_t)kRtTokens * a.H * 2 + (size_t)kRtTokens * a.E * 2;
+  return (a.H <= 2048 ? (size_t)kRtTokens * 2048 * 4 : (size_t)kRtTokens * a.H * 2) +
+         (size_t)kRtTokens * a.E * 2;
 }
 
 bool route_cluster_supported(const MoEArgs& a) { return a.M <= kRcMaxTokens; }

@@ -221,6 +221,10 @@ FLINT_DEV void cp_async4(void* smem_dst, const void* gsrc) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(smem_dst)), "l"(gsrc)
                : "memory");
 }
+FLINT_DEV void cp_async8(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(smem_dst)), "l"(gsrc)
+               : "memory");
+}
 FLINT_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's most recent copy groups are pending.
 template <int N>

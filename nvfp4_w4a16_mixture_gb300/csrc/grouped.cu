@@ -87,27 +87,28 @@ FLINT_DEV int epi_group(int warp) {
     default: return -1;
   }
 }
-constexpr int kStages = 6;
-constexpr int kATile = 128 * 128;                  // 128 token rows x 64 bf16
+constexpr int kKB = 128;                          // K per stage
+constexpr int kStages = 3;
+constexpr int kATile = 128 * 128;                  // one 128-row x 64-column bf16 tile
 constexpr int kBRows = 128;                        // B rows per CTA: N = 256 per pair
-constexpr int kOffA = 0;
-constexpr int kOffB = kATile;
-constexpr int kStageBytes = kATile + kBRows * 128;  // 32768
+constexpr int kOffA = 0;                           // A: tiles of K 0..63, 64..127
+constexpr int kOffB = 2 * kATile;                  // B: likewise
+constexpr int kStageBytes = 4 * kATile;            // 65536
 static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
-// NVFP4 code tiles (kBRows rows x 32 bytes per K block) have a ring of their
-// own, deeper than the stages, so they land well before they are dequantised.
-constexpr int kCStages = 6;
-constexpr int kCodeBytes = kBRows * 32;
+// NVFP4 code tiles (kBRows rows x 64 bytes per K block) have a ring of their
+// own, so they land well before they are dequantised.
+constexpr int kCStages = 3;
+constexpr int kCodeBytes = kBRows * (kKB / 2);
 constexpr int kOffCodes = kStages * kStageBytes;
 // Block-scale ring of the 256 dequantising threads (thread = B row of its
-// group): slot j of thread t at word j * 256 + t, filled by asynchronous
-// 4-byte copies kScaleAhead of the thread's K blocks ahead of use (slot
-// j % kScaleSlots, never the one read).
+// group): slot j of thread t at bytes 8 (j * 256 + t), filled by
+// asynchronous 8-byte copies kScaleAhead of the thread's K blocks ahead of
+// use (slot j % kScaleSlots, never the one read).
 constexpr int kScaleSlots = 4;
 constexpr int kScaleAhead = 3;
 constexpr int kDqThreads = 256;
 constexpr int kOffScale = kOffCodes + kCStages * kCodeBytes;
-constexpr int kScaleBytes = kScaleSlots * kDqThreads * 4;
+constexpr int kScaleBytes = kScaleSlots * kDqThreads * 8;
 constexpr int kTokTile = 256;   // token rows of a pair unit: 128 per CTA
 constexpr int kTmemBuf = 256;   // TMEM columns of one accumulator buffer (two buffers)
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;
@@ -116,8 +117,8 @@ constexpr int kStWords = 4;  // token-tile table entry: e, row0, row_end, unused
 
 struct GCtl {
   uint64_t full[kStages];      // this CTA's stage is in: A (and BF16 B) bytes, and the
-                               // dequantising group's 4 warps (count 1 + 4, + tx)
-  uint64_t pfull[kStages];     // leader: the peer's stage is in (one remote arrive)
+                               // dequantising group's 4 warps (count 1 + 4, + tx); the
+                               // leader's also counts the peer's relay (+ 1)
   uint64_t empty[kStages];     // the pair's MMAs are done with the stage (commit, both CTAs)
   uint64_t cfull[kCStages];    // code tile landed (count 1 + tx)
   uint64_t cempty[kCStages];   // code tile read by its 4 dequantising warps
@@ -157,7 +158,7 @@ struct TMaps {
   CUtensorMap a_routed;  // x_perm [np, H] (GEMM1) / act [np, I] (GEMM2), box {64, 128}
   CUtensorMap a_shared;  // x [M, H] / sact [M, SI], box {64, 128}
   CUtensorMap b_shared;  // shared_gu [2 SI, H] box {64, 32} / shared_down [H, SI] box {64, 128}
-  CUtensorMap codes;     // w13 [E 2I, H/2] bytes / w2 [E H, I/2], box {32, 128}
+  CUtensorMap codes;     // w13 [E 2I, H/2] bytes / w2 [E H, I/2], box {64, 128}
 };
 
 // One pair unit, the same in every role of both CTAs: 256 token rows (CTA c
@@ -242,8 +243,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&C.full[i], 1 + 4);
-      mbar_init(&C.pfull[i], 1);
+      mbar_init(&C.full[i], 1 + 4 + (leader ? 1 : 0));
       mbar_init(&C.empty[i], 1);
     }
     for (int i = 0; i < kCStages; ++i) {
@@ -274,7 +274,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     int it = 0;
     for (int u = pair; u < total && !*abort; u += npairs) {
       const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
-      const int nkb = x.K / 64;
+      const int nkb = x.K / kKB;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const int s = it % kStages;
         int ok = 1;
@@ -283,15 +283,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
         if (lane == 0) {
           uint8_t* st = smem + (size_t)s * kStageBytes;
           const CUtensorMap* ta = x.shared ? &tm.a_shared : &tm.a_routed;
-          uint32_t bytes = kATile;
-          if (x.shared) bytes += (uint32_t)(x.n / 2) * 128u;
+          uint32_t bytes = 2 * kATile;
+          if (x.shared) bytes += 2u * (uint32_t)(x.n / 2) * 128u;
           mbar_arrive_expect_tx(&C.full[s], bytes);
-          tc::tma_load_2d(st + kOffA, ta, kb * 64, x.row0 + 128 * (int)rank, &C.full[s]);
-          if (x.shared) {
-            if (STAGE == 1)  // leader 32 gate rows, peer the 32 matching up rows
-              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, (leader ? 0 : a.SI) + 32 * x.nt, &C.full[s]);
-            else  // rows past H (last tile) read as zeros
-              tc::tma_load_2d(st + kOffB, &tm.b_shared, kb * 64, 256 * x.nt + 128 * (int)rank, &C.full[s]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {  // the two 64-wide halves of the K block
+            const int k0 = kb * kKB + 64 * h;
+            tc::tma_load_2d(st + kOffA + h * kATile, ta, k0, x.row0 + 128 * (int)rank, &C.full[s]);
+            if (x.shared) {
+              if (STAGE == 1)  // leader 32 gate rows, peer the 32 matching up rows
+                tc::tma_load_2d(st + kOffB + h * kATile, &tm.b_shared, k0, (leader ? 0 : a.SI) + 32 * x.nt, &C.full[s]);
+              else  // rows past H (last tile) read as zeros
+                tc::tma_load_2d(st + kOffB + h * kATile, &tm.b_shared, k0, 256 * x.nt + 128 * (int)rank, &C.full[s]);
+            }
           }
         }
         __syncwarp();
@@ -304,7 +308,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     int it = 0;
     for (int u = pair; u < total && !*abort; u += npairs) {
       const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
-      const int nkb = x.K / 64;
+      const int nkb = x.K / kKB;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const int c = it % kCStages;
         int ok = 1;
@@ -320,7 +324,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
             const int row = STAGE == 1 ? x.e * 2 * a.I + (leader ? 0 : a.I) + 128 * x.nt
                                        : x.e * a.H + 256 * x.nt + 128 * (int)rank;
             mbar_arrive_expect_tx(&C.cfull[c], (uint32_t)kCodeBytes);
-            tc::tma_load_2d(smem + kOffCodes + c * kCodeBytes, &tm.codes, kb * 32, row, &C.cfull[c]);
+            tc::tma_load_2d(smem + kOffCodes + c * kCodeBytes, &tm.codes, kb * (kKB / 2), row, &C.cfull[c]);
           }
         }
         __syncwarp();
@@ -339,7 +343,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
       uint64_t so = 0;
       for (int u = pair; u < total && !*abort; u += npairs) {
         const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
-        const int nkb = x.K / 64;
+        const int nkb = x.K / kKB;
         const uint32_t idesc = tc::idesc_bf16(256, x.n);
         const uint32_t dwrap = (uint32_t)(x.n * x.parts);
         bool ok = true;
@@ -353,7 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
         const uint32_t dbuf = tmem + (x.w == 2 ? 0u : (uint32_t)(kTmemBuf * (slot & 1)));
         uint32_t dcol = 0;  // accumulator of K block kb: columns n * (kb % parts)
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!gwait(&C.full[s], ph, abort, status) || !gwait<true>(&C.pfull[s], ph, abort, status)) {
+          if (!gwait<true>(&C.full[s], ph, abort, status)) {  // both CTAs' parts
             ok = false;
             break;
           }
@@ -362,7 +366,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
           const uint32_t d = dbuf + dcol;
           const bool acc = kb >= x.parts;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) tc::mma_bf16_pair(d, da + 2 * kk, db + 2 * kk, idesc, acc || kk > 0);
+          for (int kk = 0; kk < 8; ++kk) {  // K 16 kk: tile kk / 4, 32-byte step kk % 4
+            const uint64_t o = (uint64_t)((kk >> 2) * (kATile >> 4) + 2 * (kk & 3));
+            tc::mma_bf16_pair(d, da + o, db + o, idesc, acc || kk > 0);
+          }
           tc::commit_pair(&C.empty[s]);
           dcol += (uint32_t)x.n;
           if (dcol == dwrap) dcol = 0;
@@ -384,7 +391,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
       uint32_t ph = 0;
       for (int u = pair; u < total && !*abort; u += npairs) {
         const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
-        const int nkb = x.K / 64;
+        const int nkb = x.K / kKB;
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!gwait(&C.full[s], ph, abort, status)) {
@@ -393,7 +400,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
           }
           // the stage's A (TMA) and B (dequantised, made visible to the async
           // proxy) are writes to this CTA's shared memory
-          tc::mbar_arrive_remote_smem(tc::mapa(&C.pfull[s], 0));
+          tc::mbar_arrive_remote_smem(tc::mapa(&C.full[s], 0));
           if (++s == kStages) {
             s = 0;
             ph ^= 1u;
@@ -414,8 +421,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     int it = 0;
     for (int u = pair; u < total && !*abort; u += npairs) {
       const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
-      const int nkb = x.K / 64;
-      const uint8_t* sfrow = nullptr;  // block scales of the row (4 bytes per K block)
+      const int nkb = x.K / kKB;
+      const uint8_t* sfrow = nullptr;  // block scales of the row (8 bytes per K block)
       if (!x.shared) {
         if (STAGE == 1) {
           const size_t row = (size_t)x.e * 2 * a.I + (leader ? 0 : a.I) + 128 * x.nt + r;
@@ -426,10 +433,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
       }
       const int kb0 = (grp - it) & 1;  // this group's first K block of the unit
       const int nmine = (nkb - kb0 + 1) / 2;
-      uint32_t* ring = reinterpret_cast<uint32_t*>(smem + kOffScale) + dqt;
+      uint2* ring = reinterpret_cast<uint2*>(smem + kOffScale) + dqt;
       auto sc_fetch = [&](int j) {
         const int kb = kb0 + 2 * j;
-        if (sfrow && kb < nkb) cp_async4(ring + (j % kScaleSlots) * kDqThreads, sfrow + 4 * kb);
+        if (sfrow && kb < nkb) cp_async8(ring + (j % kScaleSlots) * kDqThreads, sfrow + 8 * kb);
         cp_async_commit();
       };
       cp_async_wait_all();  // nothing of the previous unit in flight
@@ -440,25 +447,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
         const int itk = it + kb0 + 2 * j;
         const int s = itk % kStages, c = itk % kCStages;
         cp_async_wait_group<kScaleAhead - 1>();  // this K block's group has landed
-        const uint32_t sc = sfrow ? ring[(j % kScaleSlots) * kDqThreads] : 0u;  // 4 block scales
+        const uint2 sc = sfrow ? ring[(j % kScaleSlots) * kDqThreads] : make_uint2(0, 0);  // 8 block scales
         sc_fetch(j + kScaleAhead);
         // codes of the K block (landed well ahead): into registers, slot released
         if (!gwait_warp(&C.cfull[c], (itk / kCStages) & 1, abort, status, lane)) {
           ok = false;
           break;
         }
-        uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
+        uint4 cq[4];  // codes of K 0..31, 32..63, 64..95, 96..127
         if (!x.shared) {
-          const uint4* cr = reinterpret_cast<const uint4*>(smem + kOffCodes + c * kCodeBytes + r * 32);
-          c0 = cr[0];
-          c1 = cr[1];
+          const uint4* cr = reinterpret_cast<const uint4*>(smem + kOffCodes + c * kCodeBytes + r * 64);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) cq[i] = cr[i];
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&C.cempty[c]);
-        uint4 bv0[4], bv1[4];  // K 0..31, 32..63
+        uint4 bv0[4], bv1[4];  // K 0..31, 32..63 (dequantised before the stage is free)
         if (!x.shared) {
-          dequant_half(bv0, c0, sc & 0xFFFFu);
-          dequant_half(bv1, c1, sc >> 16);
+          dequant_half(bv0, cq[0], sc.x & 0xFFFFu);
+          dequant_half(bv1, cq[1], sc.x >> 16);
         }
         // the stage's previous MMAs are done: its B area is free
         if (itk >= kStages && !gwait_warp(&C.empty[s], ((itk / kStages) - 1) & 1, abort, status, lane)) {
@@ -471,6 +478,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
           for (int i = 0; i < 4; ++i) {
             *reinterpret_cast<uint4*>(bt + tc::sw128_offset(r, 8 * i)) = bv0[i];
             *reinterpret_cast<uint4*>(bt + tc::sw128_offset(r, 32 + 8 * i)) = bv1[i];
+          }
+          dequant_half(bv0, cq[2], sc.y & 0xFFFFu);  // second tile: K 64..127
+          dequant_half(bv1, cq[3], sc.y >> 16);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            *reinterpret_cast<uint4*>(bt + kATile + tc::sw128_offset(r, 8 * i)) = bv0[i];
+            *reinterpret_cast<uint4*>(bt + kATile + tc::sw128_offset(r, 32 + 8 * i)) = bv1[i];
           }
           tc::fence_proxy_async_smem();
         }
@@ -500,7 +514,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
       const int row = x.row0 + 128 * (int)rank + 32 * q + lane;
       const bool valid = row < x.row_end;
       const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + (x.w == 2 ? 0u : (uint32_t)(kTmemBuf * (slot & 1)));
-      const int nparts = min(x.parts, x.K / 64);
+      const int nparts = min(x.parts, x.K / kKB);
       if (STAGE == 1) {
         const int I = x.shared ? a.SI : a.I;
         const int hw = x.n / 2;  // intermediate columns of the unit: gate [0, hw), up [hw, n)
@@ -729,8 +743,8 @@ GDev g_gdev[64];
 }  // namespace
 
 bool grouped_supported(const flint_moe_shape& s) {
-  // 32-row intermediate tiles of GEMM1, 64-row output tiles of GEMM2,
-  // 64-wide K blocks
+  // 128-wide K blocks over H, I and SI; 128-row intermediate tiles of GEMM1
+  // (32 for the shared expert); GEMM2's last 256-row output tile may be half
   return s.I % 128 == 0 && s.H % 128 == 0 && s.SI % 128 == 0;
 }
 
@@ -771,9 +785,9 @@ cudaError_t launch_grouped(const MoEArgs& a, cudaStream_t st) {
   TMaps t1{}, t2{};
   bool ok = make_map(&t1.a_routed, a.ws.x_perm, true, np, H, 64, 128) &&
             make_map(&t1.a_shared, a.x, true, a.M, H, 64, 128) &&
-            make_map(&t1.codes, a.w13, false, (uint64_t)E * 2 * I, H / 2, 32, 128) &&
+            make_map(&t1.codes, a.w13, false, (uint64_t)E * 2 * I, H / 2, kKB / 2, 128) &&
             make_map(&t2.a_routed, a.ws.act, true, np, I, 64, 128) &&
-            make_map(&t2.codes, a.w2, false, (uint64_t)E * H, I / 2, 32, 128);
+            make_map(&t2.codes, a.w2, false, (uint64_t)E * H, I / 2, kKB / 2, 128);
   if (ok && SI > 0)
     ok = make_map(&t1.b_shared, a.shared_gu, true, 2 * (uint64_t)SI, H, 64, 32) &&
          make_map(&t2.a_shared, a.ws.sact, true, a.M, SI, 64, 128) &&

@@ -418,37 +418,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     const int grp = dq >> 2;
     const int dqt = dq * 32 + lane;      // 0..255
     const int r = dqt & 127;             // B row of this CTA
-    int it = 0;
+    // block scales of the row (8 bytes per K block), or null (shared expert,
+    // rows past H)
+    auto scale_row = [&](const Unit& x) -> const uint8_t* {
+      if (x.shared) return nullptr;
+      if (STAGE == 1)
+        return a.w13_sf + ((size_t)x.e * 2 * a.I + (leader ? 0 : a.I) + 128 * x.nt + r) * (a.H / 16);
+      if (256 * x.nt + 128 * (int)rank + r >= a.H) return nullptr;
+      return a.w2_sf + ((size_t)x.e * a.H + 256 * x.nt + 128 * rank + r) * (a.I / 16);
+    };
+    // The scale copies run kScaleAhead of this group's K blocks ahead of their
+    // use as one stream over the units (no wait at a unit's start); the
+    // fetch cursor: unit fu (its first global K block fit), K block fkb.
+    uint2* ring = reinterpret_cast<uint2*>(smem + kOffScale) + dqt;
+    int fu = pair, fit = 0, fkb = grp, fnkb = 0, jf = 0;
+    const uint8_t* frow = nullptr;
+    if (fu < total) {
+      const Unit fx = unit_of<STAGE>(a, fu, R, NT, NTs);
+      fnkb = fx.K / kKB;
+      frow = scale_row(fx);
+    }
+    auto fetch_next = [&]() {
+      while (fu < total && fkb >= fnkb) {  // on to this group's first K block of the next unit
+        fit += fnkb;
+        fu += npairs;
+        if (fu < total) {
+          const Unit fx = unit_of<STAGE>(a, fu, R, NT, NTs);
+          fnkb = fx.K / kKB;
+          frow = scale_row(fx);
+          fkb = (grp - fit) & 1;
+        }
+      }
+      if (fu < total && frow) cp_async8(ring + (jf % kScaleSlots) * kDqThreads, frow + 8 * fkb);
+      cp_async_commit();
+      ++jf;
+      fkb += 2;
+    };
+#pragma unroll 1
+    for (int d = 0; d < kScaleAhead; ++d) fetch_next();
+    int it = 0, jc = 0;
     for (int u = pair; u < total && !*abort; u += npairs) {
       const Unit x = unit_of<STAGE>(a, u, R, NT, NTs);
       const int nkb = x.K / kKB;
-      const uint8_t* sfrow = nullptr;  // block scales of the row (8 bytes per K block)
-      if (!x.shared) {
-        if (STAGE == 1) {
-          const size_t row = (size_t)x.e * 2 * a.I + (leader ? 0 : a.I) + 128 * x.nt + r;
-          sfrow = a.w13_sf + row * (a.H / 16);
-        } else if (256 * x.nt + 128 * (int)rank + r < a.H) {  // rows past H are not read
-          sfrow = a.w2_sf + ((size_t)x.e * a.H + 256 * x.nt + 128 * rank + r) * (a.I / 16);
-        }
-      }
+      const bool has_sf = scale_row(x) != nullptr;
       const int kb0 = (grp - it) & 1;  // this group's first K block of the unit
       const int nmine = (nkb - kb0 + 1) / 2;
-      uint2* ring = reinterpret_cast<uint2*>(smem + kOffScale) + dqt;
-      auto sc_fetch = [&](int j) {
-        const int kb = kb0 + 2 * j;
-        if (sfrow && kb < nkb) cp_async8(ring + (j % kScaleSlots) * kDqThreads, sfrow + 8 * kb);
-        cp_async_commit();
-      };
-      cp_async_wait_all();  // nothing of the previous unit in flight
-#pragma unroll
-      for (int d = 0; d < kScaleAhead; ++d) sc_fetch(d);
       bool ok = true;
-      for (int j = 0; j < nmine; ++j) {
+      for (int j = 0; j < nmine; ++j, ++jc) {
         const int itk = it + kb0 + 2 * j;
         const int s = itk % kStages, c = itk % kCStages;
-        cp_async_wait_group<kScaleAhead - 1>();  // this K block's group has landed
-        const uint2 sc = sfrow ? ring[(j % kScaleSlots) * kDqThreads] : make_uint2(0, 0);  // 8 block scales
-        sc_fetch(j + kScaleAhead);
+        cp_async_wait_group<kScaleAhead - 1>();  // this K block's copy has landed
+        const uint2 sc = has_sf ? ring[(jc % kScaleSlots) * kDqThreads] : make_uint2(0, 0);  // 8 block scales
+        fetch_next();
         // codes of the K block (landed well ahead): into registers, slot released
         if (!gwait_warp(&C.cfull[c], (itk / kCStages) & 1, abort, status, lane)) {
           ok = false;

@@ -55,6 +55,8 @@ WsLayout ws_layout(const flint_moe_shape& s) {
   L.x_perm = take(grouped ? 2 * np * H : 16);
   L.st_table = take(grouped ? 16 * grouped_st_entries(s) : 16);
   L.st_count = take(16);
+  L.x16 = take(M <= (size_t)kX16MaxTokens ? 2 * M * H : 16);
+  L.x16_exp = take(4 * M);
   L.total = off;
   return L;
 }
@@ -77,6 +79,8 @@ Ws ws_pointers(void* base, const WsLayout& L) {
   w.urec = reinterpret_cast<int*>(b + L.urec);
   w.gcnt = reinterpret_cast<int*>(b + L.gcnt);
   w.act = reinterpret_cast<uint16_t*>(b + L.act);
+  w.x16 = reinterpret_cast<uint16_t*>(b + L.x16);
+  w.x16_exp = reinterpret_cast<int*>(b + L.x16_exp);
   w.sact = reinterpret_cast<uint16_t*>(b + L.sact);
   w.y = reinterpret_cast<uint16_t*>(b + L.y);
   w.ys = reinterpret_cast<uint16_t*>(b + L.ys);

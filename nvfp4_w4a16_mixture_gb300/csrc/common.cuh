@@ -65,12 +65,52 @@ FLINT_DEV uint32_t bf16x2_bcast(uint32_t v, int hi) {
   return hi ? __byte_perm(v, 0, 0x3232) : __byte_perm(v, 0, 0x1010);
 }
 
+// ------------------------------------------------------------ NVFP4 (f16) --
+// The four code bytes of a word -> four f16x2 (byte b: low nibble = K 2b in
+// the low half, high nibble = K 2b + 1 in the high half), by the hardware
+// e2m1 -> f16 conversion (every e2m1 value is exact in f16).
+FLINT_DEV void e2m1x8_to_f16x2(uint32_t word, uint32_t (&p)[4]) {
+  asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3; }"
+      : "=r"(p[0]), "=r"(p[1]), "=r"(p[2]), "=r"(p[3])
+      : "r"(word));
+}
+// Two e4m3 block-scale bytes -> f16x2 (exact: e4m3 values are f16 values).
+FLINT_DEV uint32_t e4m3x2_to_f16x2(uint32_t b2) {
+  uint32_t h2;
+  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h2) : "r"(b2));
+  return h2;
+}
+FLINT_DEV uint32_t f16x2_bcast(uint32_t v, int hi) {
+  return hi ? __byte_perm(v, 0, 0x3232) : __byte_perm(v, 0, 0x1010);
+}
+// f16x2 product; exact for e2m1 x e4m3 (at most 6 significant bits, within
+// f16's normal range).
+FLINT_DEV uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// 2^e as fp32 for -126 <= e <= 127, by its bit pattern.
+FLINT_DEV float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+
 // ------------------------------------------------------------ tensor core --
 // D = A * B + D, m16n8k16, bf16 inputs, fp32 accumulators (mma.sync).
 FLINT_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                               uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Same with f16 operands.
+FLINT_DEV void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                             uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));

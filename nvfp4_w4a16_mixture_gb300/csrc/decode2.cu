@@ -68,6 +68,7 @@ struct GuInfo {
   int e;      // expert (routed)
   int cnt;    // tokens
   int off;    // sorted position of the expert's first pair (routed)
+  int x16;    // 1: the router's f16 copy of x is exact (routed, M <= kX16MaxTokens)
   short tok[kDecodeMaxTokens];
 };
 
@@ -222,6 +223,48 @@ FLINT_DEV void frags_bf16(uint32_t (&af)[4][2][4], const uint8_t* rg, const uint
   a_frags(d, af);
 }
 
+// A fragments of slice s on the f16 path (the few-token gate/up when the f16
+// copy of x is exact): byte b of a row's 16 code bytes of this thread ->
+// (K 2b, 2b + 1) by the hardware e2m1 -> f16 conversion, times the f16 block
+// scale; each mma gets the same K set as on the bf16 path (bytes 0, 2 of a
+// word, then 1, 3), so it sums the same products.
+FLINT_DEV void frags_fp4_f16(uint32_t (&af)[4][2][4], const uint8_t* rg, const uint8_t* rg8,
+                             const uint8_t* sg, const uint8_t* sg8, int s, int t) {
+  const uint4 c0 = *reinterpret_cast<const uint4*>(rg + s * (kSliceK / 2) + 16 * t);
+  const uint4 c1 = *reinterpret_cast<const uint4*>(rg8 + s * (kSliceK / 2) + 16 * t);
+  const uint32_t s0 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sg + s * (kSliceK / 16) + 2 * t));
+  const uint32_t s1 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sg8 + s * (kSliceK / 16) + 2 * t));
+  const uint32_t wg[4] = {c0.x, c0.y, c0.z, c0.w};
+  const uint32_t wg8[4] = {c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t sq = f16x2_bcast(s0, q >= 2), sq8 = f16x2_bcast(s1, q >= 2);
+    uint32_t p[4], p8[4];
+    e2m1x8_to_f16x2(wg[q], p);
+    e2m1x8_to_f16x2(wg8[q], p8);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {  // mma r: K {2r, 2r + 1} and {2r + 4, 2r + 5} of the word
+      af[q][r][0] = f16x2_mul(p[r], sq);
+      af[q][r][1] = f16x2_mul(p8[r], sq8);
+      af[q][r][2] = f16x2_mul(p[r + 2], sq);
+      af[q][r][3] = f16x2_mul(p8[r + 2], sq8);
+    }
+  }
+}
+
+// 8 mma of one 128-K slice on the f16 path: B is the f16 copy of x in natural
+// order (word 0 of a 16-byte chunk holds K 0, 1, word 2 K 4, 5, ...).
+FLINT_DEV void mma_b16(float (&acc)[4], const uint32_t (&af)[4][2][4], const uint4 (&xb)[4]) {
+  float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    mma_f16_16816(d, af[q][0][0], af[q][0][1], af[q][0][2], af[q][0][3], xb[q].x, xb[q].z);
+    mma_f16_16816(d, af[q][1][0], af[q][1][1], af[q][1][2], af[q][1][3], xb[q].y, xb[q].w);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] += d[i];
+}
+
 // =============================================================== gate/up ==
 // Tiles: shared expert, 8 intermediate rows each (tile rows 0..7 gate rows
 // r0.., rows 8..15 up rows SI + r0..), stages of up to 1024 K; then routed
@@ -250,11 +293,11 @@ __host__ __device__ inline GuLayout gu_layout(int M) {
   const int ntmax = (M + 7) / 8;
   GuLayout L;
   const size_t red_bytes = size_t(kCons) * ntmax * 32 * 16;
-  const size_t room = kMaxSmem - sizeof(GuSmem) - red_bytes;
+  const size_t room = kMaxSmem - sizeof(GuSmem) - 2 * red_bytes;
   L.stages = (int)(room / kGuStageBytes);
   if (L.stages > kGuMaxStages) L.stages = kGuMaxStages;
   L.red = size_t(L.stages) * kGuStageBytes;
-  L.ctl = L.red + red_bytes;
+  L.ctl = L.red + 2 * red_bytes;
   L.total = L.ctl + sizeof(GuSmem);
   return L;
 }
@@ -330,7 +373,6 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
       mbar_init(&SM.ctl.empty[i], kCons);
     }
     mbar_init(&SM.ctl.bar[0], kCons);
-    mbar_init(&SM.ctl.bar[1], kCons);
     SM.ctl.abort = 0;
     fence_mbar_init();
   }
@@ -354,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
     pdl_wait();  // router finished: routing records are final
     pdl_launch_dependents();
     const int U = ldg_cg_i32(a.ws.uniq);
+    const int x16 = (M <= kX16MaxTokens && ldg_cg_i32(a.ws.glob_cnt + 1) == 0) ? 1 : 0;
     const int tpe = I / 16;  // tiles per expert
     const int T = U * tpe;
     const int lo = (int)((long long)T * c / G), hi = (int)((long long)T * (c + 1) / G);
@@ -381,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
         GuInfo& inf = SM.info[sl];
         inf.tok[lane] = tok0;
         inf.tok[lane + 32] = tok1;
-        if (lane == 0) { inf.cnt = cnt; inf.off = off; }
+        if (lane == 0) { inf.cnt = cnt; inf.off = off; inf.x16 = x16; }
         __syncwarp();  // info complete before the arrive that publishes it
         gu_issue_routed(a, stages + (size_t)sl * kGuStageBytes, inf, &SM.ctl.full[sl], e, r0, k0,
                         lane);
@@ -402,9 +445,12 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
   }
 
   // -------------------------------------------------------------- consumers
-  bool triggered = false;
-  uint32_t bph0 = 0, bph1 = 0;
-  float4* myred = reinterpret_cast<float4*>(red) + (size_t)warp * ntmax * 32 + lane;
+  bool triggered = false, waited = false;
+  uint32_t bph0 = 0;
+  // two partial-sum buffers, alternating per tile: a tile's epilogue reads one
+  // while the warps that have no epilogue work already fill the other
+  const size_t red_floats = (size_t)kCons * ntmax * 32 * 4;
+  int ep = 0;  // tiles finished by this CTA
   for (int n = 0;; ++n) {
     const int sl = n % S;
     if (!warp_wait_phase(&SM.ctl.full[sl], (n / S) & 1, abort, status, lane, 4, n)) break;
@@ -414,7 +460,13 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
       pdl_launch_dependents();
       triggered = true;
     }
+    if (kind == 1 && !waited) {  // the router's outputs (the f16 copy of x) are visible
+      pdl_wait();
+      waited = true;
+    }
     if (kind < 0) break;
+    float4* myred = reinterpret_cast<float4*>(red + (ep & 1) * red_floats) +
+                    (size_t)warp * ntmax * 32 + lane;
     const int first = inf.first, last = inf.last, k0 = inf.k0, kst = inf.kst;
     const int pitch = inf.pitch, cnt = inf.cnt;
     const int ntiles = (cnt + 7) / 8;
@@ -437,6 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
       rg = st + g * pitch;
       rg8 = st + (8 + g) * pitch;
     }
+    const bool f16p = kind == 1 && inf.x16;
+    // the scale exponent of this lane's token, needed only in the epilogue
+    const int cexp = f16p && lane < cnt ? ldg_cg_i32(a.ws.x16_exp + inf.tok[lane]) : 0;
     for (int n0 = 0; n0 < ntiles; n0 += NTG) {
       float acc[NTG][4];
       const uint16_t* brow[NTG];
@@ -444,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
       for (int i = 0; i < NTG; ++i) {
         acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
         const int nn = (n0 + i) * 8 + g;
-        brow[i] = nn < cnt ? a.x + (size_t)(kind ? inf.tok[nn] : nn) * H + k0 : nullptr;
+        brow[i] = nn < cnt ? (f16p ? a.ws.x16 : a.x) + (size_t)(kind ? inf.tok[nn] : nn) * H + k0 : nullptr;
       }
       for (int s = s0; s < nsl; s += sstep) {
         // activations first: their load latency hides behind the dequant
@@ -453,11 +508,18 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
         for (int i = 0; i < NTG; ++i)
           load_b(xb[i], (n0 + i < ntiles && brow[i]) ? brow[i] + s * kSliceK : nullptr, t, false);
         uint32_t af[4][2][4];
-        if (kind == 1) frags_fp4(af, rg, rg8, sg, sg8, s, t);
-        else frags_bf16(af, rg, rg8, s, t);
+        if (f16p) {
+          frags_fp4_f16(af, rg, rg8, sg, sg8, s, t);
 #pragma unroll
-        for (int i = 0; i < NTG; ++i)
-          if (n0 + i < ntiles) mma_b(acc[i], af, xb[i]);
+          for (int i = 0; i < NTG; ++i)
+            if (n0 + i < ntiles) mma_b16(acc[i], af, xb[i]);
+        } else {
+          if (kind == 1) frags_fp4(af, rg, rg8, sg, sg8, s, t);
+          else frags_bf16(af, rg, rg8, s, t);
+#pragma unroll
+          for (int i = 0; i < NTG; ++i)
+            if (n0 + i < ntiles) mma_b(acc[i], af, xb[i]);
+        }
       }
 #pragma unroll
       for (int i = 0; i < NTG; ++i) {
@@ -477,11 +539,17 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
     if (lane == 0) mbar_arrive(&SM.ctl.empty[sl]);  // stage consumed
     if (!last) continue;
 
-    // ---- tile epilogue: sum the warps' partials (fixed order), write
+    // ---- tile epilogue: sum the warps' partials (fixed order), write.  A
+    // buffer is written again two tiles later, by warps past the next tile's
+    // barrier, which every warp reaches only after its part of this epilogue.
     warp_barrier(&SM.ctl.bar[0], bph0, abort, status, lane, 5);
-    const float4* red4 = reinterpret_cast<const float4*>(red);
+    const float4* red4 = reinterpret_cast<const float4*>(red + (ep & 1) * red_floats);
+    ++ep;
     if (kind == 1) {
-      const float gs = a.w13_gs[e] * 128.0f;  // 2^7 undoes the operand scaling
+      // bf16 path: 2^7 undoes the operand scaling; f16 path: 2^-x16_exp[token]
+      // undoes the activations' scaling
+      const float gs = a.w13_gs[e] * 128.0f;
+      const float gs16 = a.w13_gs[e];
       for (int it = warp; it < 2 * ntiles; it += kCons) {
         const int at = it & 1, nt = it >> 1;
         float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -492,8 +560,10 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int nn = nt * 8 + 2 * t + cc;
+          const int ex = __shfl_sync(0xffffffffu, cexp, nn & 31);  // all lanes take part
           if (nn < cnt) {
-            const float gv = v[cc] * gs, uv = v[2 + cc] * gs;
+            const float f = f16p ? gs16 * pow2f(-ex) : gs;
+            const float gv = v[cc] * f, uv = v[2 + cc] * f;
             a.ws.act[(size_t)(off + nn) * I + r0 + 8 * at + g] =
                 (uint16_t)f32_to_bf16_bits(silu_approx(gv) * uv);
           }
@@ -518,7 +588,6 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
         }
       }
     }
-    warp_barrier(&SM.ctl.bar[1], bph1, abort, status, lane, 6);  // red free again
   }
   if (!triggered) pdl_launch_dependents();
 }
@@ -547,13 +616,14 @@ struct DnSmem {
 
 // Byte offsets in the down kernel's dynamic smem: stages, y, ys, control.
 struct DnLayout {
-  size_t y, ys, ctl, total;
+  size_t y, ys, tw, ctl, total;
 };
 __host__ __device__ inline DnLayout dn_layout(int M, int k) {
   DnLayout L;
   L.y = size_t(kDnStages) * kDnStageBytes;
   L.ys = L.y + (size_t(M) * k * 16 * 2 + 15) / 16 * 16;
-  L.ctl = L.ys + (size_t(M) * 16 * 2 + 15) / 16 * 16;
+  L.tw = L.ys + (size_t(M) * 16 * 2 + 15) / 16 * 16;
+  L.ctl = L.tw + (size_t(M) * k * 4 + 15) / 16 * 16;
   L.total = L.ctl + sizeof(DnSmem);
   return L;
 }
@@ -573,6 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
   const DnLayout L = dn_layout(a.M, a.k);
   uint16_t* ysm = reinterpret_cast<uint16_t*>(smem + L.y);
   uint16_t* yss = reinterpret_cast<uint16_t*>(smem + L.ys);
+  float* tws = reinterpret_cast<float*>(smem + L.tw);
   DnSmem& SM = *reinterpret_cast<DnSmem*>(smem + L.ctl);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -718,6 +789,9 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
       }
       drain_slots(SM.ctl, n, kDnStages, abort, status);
     }
+    // the combine's weights (final since the router finished), staged while
+    // the consumers work
+    for (int i = lane; i < M * k; i += 32) tws[i] = ldg_cg_f32(a.ws.tw + i);
     // the combine below needs every consumer's results
     uint32_t ph = 0;
     warp_barrier(&SM.ctl.bar[0], ph, abort, status, lane, 14);
@@ -726,6 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
 
   // -------------------------------------------------------------- consumers
   pdl_wait();  // gate/up finished: act and sact are complete
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.ws.glob_cnt[1] = 0;  // f16-copy report consumed
   for (int n = 0;; ++n) {
     const int sl = n % kDnStages;
     if (!warp_wait_phase(&SM.ctl.full[sl], (n / kDnStages) & 1, abort, status, lane, 15, n)) break;
@@ -759,6 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
         if (b.act_smem >= 0) bsm = st + b.act_smem + (size_t)nn * K * 2;
         else brow = routed ? a.ws.act + (size_t)(b.off + nn) * I : a.ws.sact + (size_t)nn * SI;
       }
+      const float gs2 = routed ? ldg_cg_f32(a.w2_gs + b.e) * 128.0f : 0.0f;
       const uint8_t* sg = st + b.smem + 16 * b.pitch + g * (I / 16);
       const uint8_t* sg8 = sg + 8 * (I / 16);
       const int nsl = K / kSliceK;
@@ -805,7 +881,6 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
         acc[0] += o.x; acc[1] += o.y; acc[2] += o.z; acc[3] += o.w;
       }
       if (routed) {
-        const float gs2 = a.w2_gs[b.e] * 128.0f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int tok = nt * 8 + 2 * t + (i & 1);
@@ -832,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
     const int tt = idx >> 4, h = idx & 15;
     float R = 0.0f;
     for (int j = 0; j < k; ++j) {
-      const float w = ldg_cg_f32(a.ws.tw + tt * k + j);
+      const float w = tws[tt * k + j];
       R = R + w * bf16_bits_to_f32(ysm[(size_t)(tt * k + j) * 16 + h]);
     }
     const float ys = SI > 0 ? bf16_bits_to_f32(yss[tt * 16 + h]) : 0.0f;

@@ -41,8 +41,17 @@ struct WsLayout {
   size_t x_perm;       // bf16 [M * k, H]: token rows in sorted pair order (grouped path)
   size_t st_table;     // int32 [entries, 4]: per-expert token tiles (grouped path)
   size_t st_count;     // int32: number of token tiles
+  size_t x16;          // f16 [M, H]: x[t] * 2^x16_exp[t], exactly (M <= kX16MaxTokens)
+  size_t x16_exp;      // int32 [M]
   size_t total;
 };
+
+// Few-token decode: the cluster router also writes each token's row as f16
+// scaled by a power of two (the largest magnitude lands in [2^14, 2^15)) and
+// counts, in glob_cnt[1], its CTAs that met a value the f16 copy does not hold
+// exactly; the gate/up kernel uses the f16 copy only when that count is 0,
+// and the down kernel returns the count to 0.
+constexpr int kX16MaxTokens = 16;
 
 constexpr int kRouteTokens = 8;  // tokens per router CTA
 // Record of the u-th routed expert (M <= kDecodeMaxTokens): [0] expert id,
@@ -74,6 +83,8 @@ struct Ws {  // device pointers into one workspace
   uint16_t* sact;
   uint16_t* y;
   uint16_t* ys;
+  uint16_t* x16;
+  int* x16_exp;
 };
 
 Ws ws_pointers(void* base, const WsLayout& L);

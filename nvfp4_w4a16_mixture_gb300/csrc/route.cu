@@ -8,6 +8,7 @@
 // flint_moe consumes ("perm" of _combine_kernel); the decode path uses the
 // same grouping to stream each routed expert's weights once per call.
 #include <cooperative_groups.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -494,6 +495,52 @@ __global__ void __cluster_dims__(kRcCtas, 1, 1) __launch_bounds__(kRcWarps * 32)
       if (lane == 0) lead->logit[t][e] = (uint16_t)f32_to_bf16_bits(acc);
     }
   }
+  // f16 copy of x for the gate/up kernel: per token the power of two that
+  // puts the largest magnitude in [2^14, 2^15); this CTA converts columns
+  // rank * H / kRcCtas .. of every token and reports whether every value
+  // survived the round trip (then the copy is exact)
+  static_assert(kRcMaxTokens <= kX16MaxTokens, "the f16 copy covers the cluster router's tokens");
+  {
+    __shared__ int s_exp[kRcMaxTokens];
+    __shared__ int s_bad;
+    if (tid == 0) s_bad = 0;
+    for (int t = warp; t < M; t += kRcWarps) {
+      uint32_t mx = 0;  // largest bf16 magnitude bit pattern (orders like the values)
+      for (int h = 8 * lane; h < H; h += 256) {
+        const uint4 v = ldg_cg_v4(a.x + (size_t)t * H + h);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+      }
+      mx = __reduce_max_sync(0xffffffffu, mx);
+      if (lane == 0) {
+        int e = 0;
+        if (mx >= 0x7F80u) e = 1000;  // inf or nan: no f16 copy
+        else if (mx != 0) e = min(126, max(-110, 14 - ((int)(mx >> 7) - 127)));
+        s_exp[t] = e;
+      }
+    }
+    __syncthreads();
+    const int hn = H / kRcCtas, h0 = rank * hn;
+    bool bad = false;
+    for (int i = tid; i < M * (hn / 2); i += kRcWarps * 32) {
+      const int t = i / (hn / 2), h = h0 + 2 * (i % (hn / 2));
+      const int e = s_exp[t];
+      if (e == 1000) { bad = true; continue; }
+      const uint32_t xv = *reinterpret_cast<const uint32_t*>(a.x + (size_t)t * H + h);
+      const float sc = pow2f(e);
+      const float f0 = __uint_as_float(xv << 16) * sc, f1 = __uint_as_float(xv & 0xFFFF0000u) * sc;
+      const __half2 hv = __floats2half2_rn(f0, f1);
+      const float2 back = __half22float2(hv);
+      if (back.x != f0 || back.y != f1) bad = true;
+      *reinterpret_cast<__half2*>(a.ws.x16 + (size_t)t * H + h) = hv;
+    }
+    if (bad) s_bad = 1;
+    __syncthreads();
+    if (tid == 0 && s_bad) atomicAdd(&a.ws.glob_cnt[1], 1);
+    if (rank == 0 && tid < M) a.ws.x16_exp[tid] = s_exp[tid];
+  }
+
   cl.sync();  // every logit is in the leader's shared memory
   if (rank != 0) return;
 

@@ -35,6 +35,9 @@ namespace {
 
 constexpr int kCons = 16;                   // consumer warps
 constexpr int kThreads = (kCons + 1) * 32;  // + one producer warp
+constexpr int kEpi = kCons + 1;               // gate/up: the tile-epilogue warp
+constexpr int kGuThreads = (kCons + 2) * 32;  // gate/up: + producer + epilogue warp
+constexpr int kXsMaxBytes = 67584;            // gate/up: staged activations, at most
 constexpr int kPad = 16;                    // smem row padding (bank spread)
 constexpr int kMaxSmem = 232448;            // opt-in shared memory per CTA
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms
@@ -183,6 +186,13 @@ FLINT_DEV void load_b(uint4 (&xb)[4], const uint16_t* brow, int t, bool l2_only)
   }
 }
 
+// The same from activation rows staged in shared memory.
+FLINT_DEV void load_b_smem(uint4 (&xb)[4], const uint16_t* brow, int t) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    xb[q] = brow ? *reinterpret_cast<const uint4*>(brow + 32 * t + 8 * q) : make_uint4(0, 0, 0, 0);
+}
+
 // 8 mma of one 128-K slice against one 8-token B tile.  The slice is
 // accumulated from zero and then added to `acc` with an fp32 add, so the
 // tensor core's own accumulation only ever spans 128 products.
@@ -279,25 +289,46 @@ FLINT_DEV void mma_b16(float (&acc)[4], const uint32_t (&af)[4][2][4], const uin
 // a time in registers; each warp adds its partial sums for the tile into its
 // own smem rows (red), which the tile epilogue sums over the warps in a
 // fixed order.
+// What the epilogue warp needs of a finished tile (the stage's info may be
+// overwritten by then).
+struct EpiRec {
+  int kind;  // 0 shared, 1 routed, -1 no more tiles
+  int r0, e, off, cnt, f16p;
+  int exp[32];  // f16 path: scale exponent of pair nn's token (nn < cnt <= 16)
+};
+
 struct GuSmem {
-  Ctl ctl;
+  Ctl ctl;              // bar[b]: the consumers' partials of a tile of parity b are written
+  uint64_t redfree[2];  // the epilogue warp has read partial-sum buffer b
+  uint64_t xfull;       // the staged activation rows have landed
+  EpiRec er[2];
   GuInfo info[kGuMaxStages];
 };
 
 struct GuLayout {
   int stages;
-  size_t red, ctl, total;
+  size_t red, xs, xpitch, ctl, total;  // xpitch = 0: activations not staged
 };
 
-__host__ __device__ inline GuLayout gu_layout(int M) {
+// Activation rows of the routed tiles are staged in shared memory once per
+// CTA when they fit (few tokens): M rows, padded by 16 bytes against bank
+// conflicts between tokens.
+__host__ __device__ inline GuLayout gu_layout(int M, int H) {
   const int ntmax = (M + 7) / 8;
   GuLayout L;
   const size_t red_bytes = size_t(kCons) * ntmax * 32 * 16;
-  const size_t room = kMaxSmem - sizeof(GuSmem) - 2 * red_bytes;
+  L.xpitch = 0;
+  size_t xs_bytes = 0;
+  if (M <= kX16MaxTokens && size_t(M) * (2 * H + 16) <= kXsMaxBytes) {
+    L.xpitch = 2 * size_t(H) + 16;
+    xs_bytes = size_t(M) * L.xpitch;
+  }
+  const size_t room = kMaxSmem - sizeof(GuSmem) - 2 * red_bytes - xs_bytes;
   L.stages = (int)(room / kGuStageBytes);
   if (L.stages > kGuMaxStages) L.stages = kGuMaxStages;
   L.red = size_t(L.stages) * kGuStageBytes;
-  L.ctl = L.red + 2 * red_bytes;
+  L.xs = L.red + 2 * red_bytes;
+  L.ctl = L.xs + xs_bytes;
   L.total = L.ctl + sizeof(GuSmem);
   return L;
 }
@@ -352,12 +383,14 @@ FLINT_DEV void gu_issue_routed(const MoEArgs& a, uint8_t* stage, GuInfo& inf, ui
 
 // NTG: token n-tiles held in registers at a time (1 when M <= 8).
 template <int NTG>
-__global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
+__global__ void __launch_bounds__(kGuThreads, 1) gate_up2_kernel(MoEArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const GuLayout L = gu_layout(a.M);
+  const GuLayout L = gu_layout(a.M, a.H);
   const int S = L.stages;
   uint8_t* stages = smem;
   float* red = reinterpret_cast<float*>(smem + L.red);
+  uint8_t* xs = smem + L.xs;
+  const int xpitch = (int)L.xpitch;
   GuSmem& SM = *reinterpret_cast<GuSmem*>(smem + L.ctl);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -373,10 +406,82 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
       mbar_init(&SM.ctl.empty[i], kCons);
     }
     mbar_init(&SM.ctl.bar[0], kCons);
+    mbar_init(&SM.ctl.bar[1], kCons);
+    mbar_init(&SM.redfree[0], 1);
+    mbar_init(&SM.redfree[1], 1);
+    mbar_init(&SM.xfull, 1);
     SM.ctl.abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
+  // two partial-sum buffers, alternating per tile: the epilogue warp reads
+  // one while the consumers fill the other
+  const size_t red_floats = (size_t)kCons * ntmax * 32 * 4;
+
+  if (warp == kEpi) {
+    // ---------------------------------------------------------- epilogue
+    // Tile j: sum the consumers' partials in a fixed order, apply the
+    // scales and the activation, write act (routed) or sact (shared).
+    bool triggered = false;
+    for (int j = 0;; ++j) {
+      const int b = j & 1;
+      if (!warp_wait_phase(&SM.ctl.bar[b], (j >> 1) & 1, abort, status, lane, 5, j)) break;
+      const EpiRec& er = SM.er[b];
+      const int kind = er.kind;
+      if (kind < 0) break;
+      if (kind == 1 && !triggered) {  // routed tiles follow the router's completion
+        pdl_launch_dependents();
+        triggered = true;
+      }
+      const float4* red4 = reinterpret_cast<const float4*>(red + b * red_floats);
+      const int cnt = er.cnt, ntiles = (cnt + 7) / 8, r0 = er.r0, off = er.off;
+      if (kind == 1) {
+        // bf16 path: 2^7 undoes the operand scaling; f16 path: 2^-exp of the
+        // token undoes the activations' scaling
+        const float gs = er.f16p ? a.w13_gs[er.e] : a.w13_gs[er.e] * 128.0f;
+        for (int it = 0; it < 2 * ntiles; ++it) {
+          const int at = it & 1, nt = it >> 1;
+          float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          for (int kp = 0; kp < kKP; ++kp) {
+            const float4 p = red4[((size_t)(at + 2 * kp) * ntmax + nt) * 32 + lane];
+            v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
+          }
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int nn = nt * 8 + 2 * t + cc;
+            if (nn < cnt) {
+              const float f = er.f16p ? gs * pow2f(-er.exp[nn]) : gs;
+              const float gv = v[cc] * f, uv = v[2 + cc] * f;
+              a.ws.act[(size_t)(off + nn) * I + r0 + 8 * at + g] =
+                  (uint16_t)f32_to_bf16_bits(silu_approx(gv) * uv);
+            }
+          }
+        }
+      } else {
+        for (int nt = 0; nt < ntiles; ++nt) {
+          float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          for (int w = 0; w < 8; ++w) {
+            const float4 p = red4[((size_t)w * ntmax + nt) * 32 + lane];
+            v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
+          }
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int nn = nt * 8 + 2 * t + cc;
+            if (nn < cnt) {
+              // stock BF16 SwiGLU: gS, uS rounded, silu(gS) = gS / (1 + exp(-gS))
+              const float gS = round_bf16(v[cc]), uS = round_bf16(v[2 + cc]);
+              const float sv = __fdiv_rn(gS, 1.0f + expf(-gS)) * uS;
+              a.ws.sact[(size_t)nn * SI + r0 + g] = (uint16_t)f32_to_bf16_bits(sv);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&SM.redfree[b]);  // buffer b (and er[b]) free again
+    }
+    if (!triggered) pdl_launch_dependents();
+    return;
+  }
 
   if (warp == kCons) {
     // ------------------------------------------------------------ producer
@@ -400,6 +505,15 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
     const int tpe = I / 16;  // tiles per expert
     const int T = U * tpe;
     const int lo = (int)((long long)T * c / G), hi = (int)((long long)T * (c + 1) / G);
+    const bool staged = xpitch && lo < hi;
+    if (staged) {  // the routed tiles' activation rows, once: the f16 copy or x
+      fence_proxy_async_global();  // the router's f16 copy, read by bulk copies
+      const uint16_t* src = x16 ? a.ws.x16 : a.x;
+      if (lane == 0) mbar_arrive_expect_tx(&SM.xfull, (uint32_t)M * 2u * H);
+      __syncwarp();
+      for (int tk = lane; tk < M; tk += 32)
+        bulk_g2s(xs + (size_t)tk * xpitch, src + (size_t)tk * H, 2u * H, &SM.xfull);
+    }
     int cur_u = -1, e = 0, cnt = 0, off = 0;
     short tok0 = 0, tok1 = 0;
     for (int tile = lo; tile < hi; ++tile) {
@@ -440,17 +554,23 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
         mbar_arrive(&SM.ctl.full[sl]);
       }
       drain_slots(SM.ctl, n, S, abort, status);
+      if (staged) {  // no copy outlives the CTA
+        const unsigned long long t0 = globaltimer_ns();
+        while (!mbar_try_wait(&SM.xfull, 0, kSuspendNs)) {
+          if (globaltimer_ns() - t0 > kWaitNs) {
+            *abort = 1;
+            record_timeout(status, 7, n);
+            break;
+          }
+        }
+      }
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
-  bool triggered = false, waited = false;
-  uint32_t bph0 = 0;
-  // two partial-sum buffers, alternating per tile: a tile's epilogue reads one
-  // while the warps that have no epilogue work already fill the other
-  const size_t red_floats = (size_t)kCons * ntmax * 32 * 4;
-  int ep = 0;  // tiles finished by this CTA
+  bool triggered = false, waited = false, xready = false;
+  int ep = 0;  // tiles handed to the epilogue warp
   for (int n = 0;; ++n) {
     const int sl = n % S;
     if (!warp_wait_phase(&SM.ctl.full[sl], (n / S) & 1, abort, status, lane, 4, n)) break;
@@ -464,9 +584,23 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
       pdl_wait();
       waited = true;
     }
-    if (kind < 0) break;
-    float4* myred = reinterpret_cast<float4*>(red + (ep & 1) * red_floats) +
-                    (size_t)warp * ntmax * 32 + lane;
+    const int b = ep & 1;
+    // buffer b (partials and the epilogue record) was last used by tile ep - 2
+    if ((kind < 0 || inf.first) && ep >= 2 &&
+        !warp_wait_phase(&SM.redfree[b], ((ep >> 1) - 1) & 1, abort, status, lane, 10, ep))
+      break;
+    if (kind < 0) {  // no more tiles: tell the epilogue warp
+      if (warp == 0 && lane == 0) SM.er[b].kind = -1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&SM.ctl.bar[b]);
+      break;
+    }
+    const bool xsm = kind == 1 && xpitch;  // activations from the staged rows
+    if (xsm && !xready) {
+      if (!warp_wait_phase(&SM.xfull, 0, abort, status, lane, 6, n)) break;
+      xready = true;
+    }
+    float4* myred = reinterpret_cast<float4*>(red + b * red_floats) + (size_t)warp * ntmax * 32 + lane;
     const int first = inf.first, last = inf.last, k0 = inf.k0, kst = inf.kst;
     const int pitch = inf.pitch, cnt = inf.cnt;
     const int ntiles = (cnt + 7) / 8;
@@ -490,8 +624,9 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
       rg8 = st + (8 + g) * pitch;
     }
     const bool f16p = kind == 1 && inf.x16;
-    // the scale exponent of this lane's token, needed only in the epilogue
-    const int cexp = f16p && lane < cnt ? ldg_cg_i32(a.ws.x16_exp + inf.tok[lane]) : 0;
+    // the scale exponent of this lane's pair (f16 path), for the epilogue record
+    const int cexp =
+        f16p && last && warp == 0 && lane < cnt ? ldg_cg_i32(a.ws.x16_exp + inf.tok[lane]) : 0;
     for (int n0 = 0; n0 < ntiles; n0 += NTG) {
       float acc[NTG][4];
       const uint16_t* brow[NTG];
@@ -499,14 +634,19 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
       for (int i = 0; i < NTG; ++i) {
         acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
         const int nn = (n0 + i) * 8 + g;
-        brow[i] = nn < cnt ? (f16p ? a.ws.x16 : a.x) + (size_t)(kind ? inf.tok[nn] : nn) * H + k0 : nullptr;
+        if (nn >= cnt) brow[i] = nullptr;
+        else if (xsm) brow[i] = reinterpret_cast<const uint16_t*>(xs + (size_t)inf.tok[nn] * xpitch) + k0;
+        else brow[i] = (f16p ? a.ws.x16 : a.x) + (size_t)(kind ? inf.tok[nn] : nn) * H + k0;
       }
       for (int s = s0; s < nsl; s += sstep) {
         // activations first: their load latency hides behind the dequant
         uint4 xb[NTG][4];
 #pragma unroll
-        for (int i = 0; i < NTG; ++i)
-          load_b(xb[i], (n0 + i < ntiles && brow[i]) ? brow[i] + s * kSliceK : nullptr, t, false);
+        for (int i = 0; i < NTG; ++i) {
+          const uint16_t* bp = (n0 + i < ntiles && brow[i]) ? brow[i] + s * kSliceK : nullptr;
+          if (xsm) load_b_smem(xb[i], bp, t);
+          else load_b(xb[i], bp, t, false);
+        }
         uint32_t af[4][2][4];
         if (f16p) {
           frags_fp4_f16(af, rg, rg8, sg, sg8, s, t);
@@ -534,60 +674,19 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
         }
       }
     }
-    const int r0 = inf.r0, e = inf.e, off = inf.off;
+    if (last && warp == 0) {  // the tile's record, before the stage slot is released
+      EpiRec& er = SM.er[b];
+      if (lane == 0) {
+        er.kind = kind; er.r0 = inf.r0; er.e = inf.e; er.off = inf.off; er.cnt = cnt;
+        er.f16p = f16p ? 1 : 0;
+      }
+      er.exp[lane] = cexp;
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&SM.ctl.empty[sl]);  // stage consumed
     if (!last) continue;
-
-    // ---- tile epilogue: sum the warps' partials (fixed order), write.  A
-    // buffer is written again two tiles later, by warps past the next tile's
-    // barrier, which every warp reaches only after its part of this epilogue.
-    warp_barrier(&SM.ctl.bar[0], bph0, abort, status, lane, 5);
-    const float4* red4 = reinterpret_cast<const float4*>(red + (ep & 1) * red_floats);
+    if (lane == 0) mbar_arrive(&SM.ctl.bar[b]);  // partials (and record) of tile ep written
     ++ep;
-    if (kind == 1) {
-      // bf16 path: 2^7 undoes the operand scaling; f16 path: 2^-x16_exp[token]
-      // undoes the activations' scaling
-      const float gs = a.w13_gs[e] * 128.0f;
-      const float gs16 = a.w13_gs[e];
-      for (int it = warp; it < 2 * ntiles; it += kCons) {
-        const int at = it & 1, nt = it >> 1;
-        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int kp = 0; kp < kKP; ++kp) {
-          const float4 p = red4[((size_t)(at + 2 * kp) * ntmax + nt) * 32 + lane];
-          v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
-        }
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int nn = nt * 8 + 2 * t + cc;
-          const int ex = __shfl_sync(0xffffffffu, cexp, nn & 31);  // all lanes take part
-          if (nn < cnt) {
-            const float f = f16p ? gs16 * pow2f(-ex) : gs;
-            const float gv = v[cc] * f, uv = v[2 + cc] * f;
-            a.ws.act[(size_t)(off + nn) * I + r0 + 8 * at + g] =
-                (uint16_t)f32_to_bf16_bits(silu_approx(gv) * uv);
-          }
-        }
-      }
-    } else {
-      for (int nt = warp; nt < ntiles; nt += kCons) {
-        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int w = 0; w < 8; ++w) {
-          const float4 p = red4[((size_t)w * ntmax + nt) * 32 + lane];
-          v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
-        }
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int nn = nt * 8 + 2 * t + cc;
-          if (nn < cnt) {
-            // stock BF16 SwiGLU: gS, uS rounded, silu(gS) = gS / (1 + exp(-gS))
-            const float gS = round_bf16(v[cc]), uS = round_bf16(v[2 + cc]);
-            const float sv = __fdiv_rn(gS, 1.0f + expf(-gS)) * uS;
-            a.ws.sact[(size_t)nn * SI + r0 + g] = (uint16_t)f32_to_bf16_bits(sv);
-          }
-        }
-      }
-    }
   }
   if (!triggered) pdl_launch_dependents();
 }
@@ -601,17 +700,17 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up2_kernel(MoEArgs a) {
 // whole K of its item, so no cross-warp reduction is needed.  Results go to
 // smem: y (bf16, per pair t * k + j) and ys (bf16, per token); after the last
 // stage the CTA forms out = bf16(bf16(sum_j tw_j y_j) + ys) for its rows.
-// A stage with at most kDnSplitItems items gives each item two warps, one
-// per half of its K slices; the second half's fp32 partials go through
-// shared memory (a float4 per lane) and a per-item flag holding the stage
-// number + 1.
-constexpr int kDnSplitItems = kCons / 2;
+// A stage with at most 8 items gives each item P = 2 warps, one per half of
+// its K slices; parts 1 .. P - 1 hand their fp32 partials to
+// part 0 through shared memory (a float4 per lane) and a per-part flag
+// holding the stage number + 1; part 0 adds them in part order.
+constexpr int kDnPartSlots = kCons / 2;  // items * (P - 1) when P = 2
 
 struct DnSmem {
   Ctl ctl;
   DnInfo info[kDnStages];
-  int flag[kDnStages][kDnSplitItems];
-  float4 part[kDnStages][kDnSplitItems][32];
+  int flag[kDnStages][kDnPartSlots];
+  float4 part[kDnStages][kDnPartSlots][32];
 };
 
 // Byte offsets in the down kernel's dynamic smem: stages, y, ys, control.
@@ -656,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
     for (int i = 0; i < kDnStages; ++i) {
       mbar_init(&SM.ctl.full[i], 1);
       mbar_init(&SM.ctl.empty[i], kCons);
-      for (int j = 0; j < kDnSplitItems; ++j) SM.flag[i][j] = 0;
+      for (int j = 0; j < kDnPartSlots; ++j) SM.flag[i][j] = 0;
     }
     mbar_init(&SM.ctl.bar[0], kCons + 1);
     SM.ctl.abort = 0;
@@ -668,6 +767,21 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
     // ------------------------------------------------------------ producer
     // The gate/up grid released this grid only after its own dependency
     // wait, which follows the router's completion: the records are final.
+    // headers of routed units [win, win + 32), one per lane; the first window
+    // is read with U (records past U are allocated but unused)
+    const int urows = min(a.E, M * k);  // records the workspace holds
+    int win = 0, hdr_e = 0, hdr_c = 0, hdr_o = 0;
+    auto load_window = [&](int w0) {
+      const int ul = w0 + lane;
+      if (ul < urows) {
+        const int* rec = a.ws.urec + (size_t)ul * kUrecInts;
+        hdr_e = ldg_cg_i32(rec);
+        hdr_c = ldg_cg_i32(rec + 1);
+        hdr_o = ldg_cg_i32(rec + 2);
+      }
+      win = w0;
+    };
+    load_window(0);
     const int U = ldg_cg_i32(a.ws.uniq);
     const int nsh = SI > 0 ? 1 : 0;
     const int nunits = U + nsh;
@@ -700,22 +814,14 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
       const int sl = n % kDnStages;
       uint8_t* st = stages + (size_t)sl * kDnStageBytes;
       DnInfo& inf = SM.info[sl];
-      // headers of the next (up to) 32 routed units, one per lane
-      const int ul = unit - nsh + lane;
-      int hdr_e = 0, hdr_c = 0, hdr_o = 0;
-      if (ul >= 0 && ul < U) {
-        const int* rec = a.ws.urec + (size_t)ul * kUrecInts;
-        hdr_e = ldg_cg_i32(rec);
-        hdr_c = ldg_cg_i32(rec + 1);
-        hdr_o = ldg_cg_i32(rec + 2);
-      }
+      // a stage holds at most kDnMaxBlocks units: move the window if needed
+      if (unit - nsh + kDnMaxBlocks > win + 32) load_window(max(unit - nsh, 0));
       int used = 0, nb = 0, ni = 0;
       uint32_t wbytes = 0, abytes = 0;
-      const int first_unit = unit;
       while (unit < nunits && nb < kDnMaxBlocks) {  // same plan in every lane
         const bool shared = nsh && unit == 0;
         const int wb = dn_block_bytes(shared ? 0 : 1, I, SI);
-        const int src = unit - first_unit;  // lane holding this unit's header
+        const int src = (unit - nsh - win) & 31;  // lane holding this unit's header
         const int e = __shfl_sync(0xffffffffu, hdr_e, src);
         const int cnt = shared ? M : __shfl_sync(0xffffffffu, hdr_c, src);
         const int off = __shfl_sync(0xffffffffu, hdr_o, src);
@@ -807,9 +913,9 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
     const DnInfo& inf = SM.info[sl];
     if (inf.nblocks == 0) break;
     const uint8_t* st = stages + (size_t)sl * kDnStageBytes;
-    const bool split = inf.nitems <= kDnSplitItems;
-    const int kh = split ? (warp & 1) : 0;  // K half of this warp (split stages)
-    for (int it = split ? (warp >> 1) : warp; it < inf.nitems; it += split ? kDnSplitItems : kCons) {
+    const int P = inf.nitems <= kCons / 2 ? 2 : 1;  // K parts per item
+    const int kp = warp % P;                                     // this warp's part
+    for (int it = warp / P; it < inf.nitems; it += kCons / P) {
       const DnBlock& b = inf.blk[inf.item_blk[it]];
       const int nt = inf.item_nt[it];
       const int nn = nt * 8 + g;  // token column of this lane
@@ -838,8 +944,7 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
       const uint8_t* sg = st + b.smem + 16 * b.pitch + g * (I / 16);
       const uint8_t* sg8 = sg + 8 * (I / 16);
       const int nsl = K / kSliceK;
-      const int s_lo = split && kh ? (nsl + 1) / 2 : 0;
-      const int s_hi = split && !kh ? (nsl + 1) / 2 : nsl;
+      const int s_lo = nsl * kp / P, s_hi = nsl * (kp + 1) / P;
       for (int s = s_lo; s < s_hi; ++s) {
         uint4 xb[4];
         if (bsm) {
@@ -854,31 +959,35 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
         else frags_bf16(af, rg, rg8, s, t);
         mma_b(acc, af, xb);
       }
-      if (split) {
-        float4* pp = &SM.part[sl][it][lane];
-        volatile int* fl = &SM.flag[sl][it];
-        if (kh) {  // second half: hand the partials over, the first half writes y
-          *pp = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      if (P > 1) {
+        const int slot0 = it * (P - 1);  // slots of parts 1 .. P - 1
+        if (kp) {  // hand the partials over; part 0 writes y
+          SM.part[sl][slot0 + kp - 1][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
           __threadfence_block();
           __syncwarp();
-          if (lane == 0) *fl = n + 1;
+          if (lane == 0) reinterpret_cast<volatile int*>(SM.flag[sl])[slot0 + kp - 1] = n + 1;
           continue;
         }
         int ok = 1;
         if (lane == 0) {
           const unsigned long long t0 = globaltimer_ns();
-          while (*fl != n + 1) {
-            if (*abort || globaltimer_ns() - t0 > kWaitNs) {
-              if (!*abort) { *abort = 1; record_timeout(status, 17, n); }
-              ok = 0;
-              break;
+          for (int q = 1; q < P && ok; ++q) {
+            volatile int* fl = &SM.flag[sl][slot0 + q - 1];
+            while (*fl != n + 1) {
+              if (*abort || globaltimer_ns() - t0 > kWaitNs) {
+                if (!*abort) { *abort = 1; record_timeout(status, 17, n); }
+                ok = 0;
+                break;
+              }
             }
           }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         __threadfence_block();
-        const float4 o = *pp;
-        acc[0] += o.x; acc[1] += o.y; acc[2] += o.z; acc[3] += o.w;
+        for (int q = 1; q < P; ++q) {
+          const float4 o = SM.part[sl][slot0 + q - 1][lane];
+          acc[0] += o.x; acc[1] += o.y; acc[2] += o.z; acc[3] += o.w;
+        }
       }
       if (routed) {
 #pragma unroll
@@ -922,11 +1031,11 @@ struct DevCache {
 };
 DevCache g_dev[64];
 
-cudaError_t launch_ex(const void* fn, dim3 grid, size_t smem, void** args, cudaStream_t st,
-                      bool pdl) {
+cudaError_t launch_ex(const void* fn, dim3 grid, int threads, size_t smem, void** args,
+                      cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -943,7 +1052,7 @@ bool decode2_supported(const flint_moe_shape& s) {
   return s.M <= kDecodeMaxTokens && s.M * s.top_k <= 1024 && s.I <= kGuKst4 &&
          s.SI <= kGuKst16 && (s.H <= kGuKst4 || s.H % 256 == 0) &&
          dn_layout(s.M, s.top_k).total <= (size_t)kMaxSmem &&
-         gu_layout(s.M).stages >= 2 && 16 * (s.I / 2 + kPad) + s.I <= kDnStageBytes;
+         gu_layout(s.M, s.H).stages >= 2 && 16 * (s.I / 2 + kPad) + s.I <= kDnStageBytes;
 }
 
 cudaError_t launch_decode2(const MoEArgs& a, cudaStream_t st) {
@@ -971,10 +1080,10 @@ cudaError_t launch_decode2(const MoEArgs& a, cudaStream_t st) {
   err = route_cluster_supported(a) ? launch_route_cluster(a, st) : launch_route(a, true, st, false);
   if (err != cudaSuccess) return err;
   const void* gu = a.M <= 8 ? (const void*)gate_up2_kernel<1> : (const void*)gate_up2_kernel<2>;
-  err = launch_ex(gu, dim3(dc.sms), gu_layout(a.M).total, args, st, true);
+  err = launch_ex(gu, dim3(dc.sms), kGuThreads, gu_layout(a.M, a.H).total, args, st, true);
   if (err != cudaSuccess) return err;
-  return launch_ex((const void*)down2_kernel, dim3(a.H / 16), dn_layout(a.M, a.k).total, args, st,
-                   true);
+  return launch_ex((const void*)down2_kernel, dim3(a.H / 16), kThreads, dn_layout(a.M, a.k).total,
+                   args, st, true);
 }
 
 }  // namespace flint

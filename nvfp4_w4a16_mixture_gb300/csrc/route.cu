@@ -129,69 +129,89 @@ FLINT_DEV float router_dot(const uint16_t* xrow, const uint4 (&wreg)[8], const u
 }
 
 // router_dot for a block of 4 experts x 4 tokens (H <= 2048): every
-// (expert, token) chain is the same per-lane sequence of fmaf (chunk c
+// (expert, token) chain is the same per-lane sequence of fp32 fmas (chunk c
 // ascending, element k ascending) and the same butterfly; the 16 chains run
 // side by side so that each x vector loaded from shared memory feeds four
-// experts and each router vector four tokens.  x is in fp32 in shared memory,
-// laid out [chunk c][half][lane][4] per token (2048 floats per token; lane
-// l's elements 256 c + 8 l + 4 half + 0..3).  Experts e >= E read row E - 1
-// and are not stored by the caller.
-FLINT_DEV void router_block_4x4(float (&res)[4][4], const float* xf0, const uint16_t* router_w,
+// experts and each router vector four tokens.  Two tokens' chains share one
+// packed fma.rn.f32x2 (two independent IEEE fmas), so the chains round
+// exactly as scalar fmaf does.  x is in fp32 in shared memory, token pairs
+// interleaved: pair p, chunk c, quad q (elements 2q, 2q + 1 of the lane's
+// 8), lane l holds float4 {x[2p][h], x[2p + 1][h], x[2p][h + 1],
+// x[2p + 1][h + 1]} with h = 256 c + 8 l + 2 q (kRtPairFloats floats per
+// pair).  Experts e >= E read row E - 1 and are not stored by the caller.
+constexpr int kRtPairFloats = 2 * 2048;
+
+FLINT_DEV uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+FLINT_DEV void f32x2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+FLINT_DEV void fma_f32x2(uint64_t& acc, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+// One 256-wide chunk of the block: w holds the lane's 8 router elements of
+// the 4 experts, xc points at pair 0's chunk.
+FLINT_DEV void router_chunk_4x4(uint64_t (&acc)[4][2], const uint4 (&w)[4], const float* xc,
+                                int lane) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    ulonglong2 xv[2];  // per pair: {x(2q) of both tokens, x(2q + 1) of both tokens}
+#pragma unroll
+    for (int p = 0; p < 2; ++p)
+      xv[p] = *reinterpret_cast<const ulonglong2*>(xc + (size_t)p * kRtPairFloats + (q * 32 + lane) * 4);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t word = q == 0 ? w[i].x : q == 1 ? w[i].y : q == 2 ? w[i].z : w[i].w;
+      const float w0 = __uint_as_float(word << 16), w1 = __uint_as_float(word & 0xFFFF0000u);
+      const uint64_t w0p = f32x2_pack(w0, w0), w1p = f32x2_pack(w1, w1);
+#pragma unroll
+      for (int p = 0; p < 2; ++p) fma_f32x2(acc[i][p], xv[p].x, w0p);
+#pragma unroll
+      for (int p = 0; p < 2; ++p) fma_f32x2(acc[i][p], xv[p].y, w1p);
+    }
+  }
+}
+
+FLINT_DEV void router_block_4x4(float (&res)[4][4], const float* xp0, const uint16_t* router_w,
                                 int e0, int E, int H, int lane) {
   const int nchunk = (H + 255) / 256;
-  float acc[4][4];
+  uint64_t acc[4][2];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+  for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0ull;  // +0.0f in both halves
   const uint16_t* wr[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) wr[i] = router_w + (size_t)min(e0 + i, E - 1) * H + 8 * lane;
-  // the router vectors of the next chunk are in flight while this one runs
-  const bool has0 = 8 * lane < H;
-  uint4 wn[4];
+  auto load = [&](uint4 (&w)[4], int c) {
+    const bool has = c < nchunk && 256 * c + 8 * lane < H;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) wn[i] = has0 ? ldg_nc_v4(wr[i]) : make_uint4(0, 0, 0, 0);
-  for (int c = 0; c < nchunk; ++c) {
-    const bool has = 256 * c + 8 * lane < H;
-    uint4 wq[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) wq[i] = wn[i];
-    const bool hasn = c + 1 < nchunk && 256 * (c + 1) + 8 * lane < H;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) wn[i] = hasn ? ldg_nc_v4(wr[i] + 256 * (c + 1)) : make_uint4(0, 0, 0, 0);
-    if (!has) continue;
-    float wf[4][8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 q = wq[i];
-      const uint32_t ws[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        wf[i][2 * h] = __uint_as_float(ws[h] << 16);
-        wf[i][2 * h + 1] = __uint_as_float(ws[h] & 0xFFFF0000u);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float* xp = xf0 + (size_t)j * 2048 + c * 256 + lane * 4;
-      const float4 lo = *reinterpret_cast<const float4*>(xp);
-      const float4 hi = *reinterpret_cast<const float4*>(xp + 128);
-      const float xv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i][j] = fmaf(xv[k], wf[i][k], acc[i][j]);
-    }
+    for (int i = 0; i < 4; ++i) w[i] = has ? ldg_nc_v4(wr[i] + 256 * c) : make_uint4(0, 0, 0, 0);
+  };
+  // two register sets of router vectors, the next chunk's in flight
+  uint4 wa[4], wb[4];
+  load(wa, 0);
+  for (int c = 0; c < nchunk; c += 2) {
+    load(wb, c + 1);
+    if (256 * c + 8 * lane < H) router_chunk_4x4(acc, wa, xp0 + (size_t)c * 512, lane);
+    load(wa, c + 2);
+    if (c + 1 < nchunk && 256 * (c + 1) + 8 * lane < H)
+      router_chunk_4x4(acc, wb, xp0 + (size_t)(c + 1) * 512, lane);
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float v = acc[i][j];
+    for (int p = 0; p < 2; ++p) {
+      float v[2];
+      f32x2_unpack(acc[i][p], v[0], v[1]);
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, o);
-      res[i][j] = v;
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) v[h] = v[h] + __shfl_xor_sync(0xffffffffu, v[h], o);
+        res[i][2 * p + h] = v[h];
+      }
     }
 }
 
@@ -618,7 +638,7 @@ __global__ void __launch_bounds__(kRtWarps * 32) route_tile_kernel(MoEArgs a) {
   extern __shared__ __align__(16) uint8_t rt_smem[];
   const int H = a.H, E = a.E, k = a.k;
   const bool f32 = H <= 2048;
-  float* xf = reinterpret_cast<float*>(rt_smem);      // H <= 2048: [16][2048] fp32, lane order
+  float* xf = reinterpret_cast<float*>(rt_smem);      // H <= 2048: [8 pairs][4096] fp32, pair order
   uint16_t* xs = reinterpret_cast<uint16_t*>(rt_smem);  // H > 2048: [16][H] bf16
   uint16_t* lg = reinterpret_cast<uint16_t*>(rt_smem + (f32 ? (size_t)kRtTokens * 2048 * 4
                                                              : (size_t)kRtTokens * H * 2));  // [16][E]
@@ -628,20 +648,28 @@ __global__ void __launch_bounds__(kRtWarps * 32) route_tile_kernel(MoEArgs a) {
   const int nt = min(kRtTokens, a.M - t0);
   pdl_wait();
   {  // stage the token rows (16-byte vectors of 8 elements)
-    const int nvr = H / 8, nv = nt * nvr;
+    const int nvr = H / 8;
     const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t0 * H);
-    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
-      const uint4 q = ldg_cg_v4(src + i);
-      if (f32) {  // vector v = h / 8 of token t goes to chunk v / 32, lane v % 32
-        const int t = i / nvr, v = i % nvr;
-        float* d = xf + (size_t)t * 2048 + (v >> 5) * 256 + (v & 31) * 4;
-        *reinterpret_cast<float4*>(d) = make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u),
-                                                    __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u));
-        *reinterpret_cast<float4*>(d + 128) = make_float4(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xFFFF0000u),
-                                                          __uint_as_float(q.w << 16), __uint_as_float(q.w & 0xFFFF0000u));
-      } else {
-        reinterpret_cast<uint4*>(xs)[i] = q;
+    if (f32) {
+      // vector v = h / 8 of tokens 2p and 2p + 1 -> pair p, chunk v / 32,
+      // lane v % 32: four float4, one per quad of elements (tokens past nt
+      // read as zero)
+      const int np = (nt + 1) / 2, nv = np * nvr;
+      for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        const int p = i / nvr, v = i % nvr;
+        const uint4 q0 = ldg_cg_v4(src + (size_t)(2 * p) * nvr + v);
+        const uint4 q1 = 2 * p + 1 < nt ? ldg_cg_v4(src + (size_t)(2 * p + 1) * nvr + v)
+                                        : make_uint4(0, 0, 0, 0);
+        const uint32_t a0[4] = {q0.x, q0.y, q0.z, q0.w}, a1[4] = {q1.x, q1.y, q1.z, q1.w};
+        float* d = xf + (size_t)p * kRtPairFloats + (v >> 5) * 512 + (v & 31) * 4;
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd)
+          *reinterpret_cast<float4*>(d + qd * 128) =
+              make_float4(__uint_as_float(a0[qd] << 16), __uint_as_float(a1[qd] << 16),
+                          __uint_as_float(a0[qd] & 0xFFFF0000u), __uint_as_float(a1[qd] & 0xFFFF0000u));
       }
+    } else {
+      for (int i = threadIdx.x; i < nt * nvr; i += blockDim.x) reinterpret_cast<uint4*>(xs)[i] = ldg_cg_v4(src + i);
     }
   }
   __syncthreads();
@@ -652,7 +680,7 @@ __global__ void __launch_bounds__(kRtWarps * 32) route_tile_kernel(MoEArgs a) {
     for (int b = warp; b < neb * ntb; b += kRtWarps) {
       const int e0 = 4 * (b / ntb), tb = 4 * (b % ntb);
       float r[4][4];
-      router_block_4x4(r, xf + (size_t)tb * 2048, a.router_w, e0, E, H, lane);
+      router_block_4x4(r, xf + (size_t)(tb / 2) * kRtPairFloats, a.router_w, e0, E, H, lane);
       if (lane == 0) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)

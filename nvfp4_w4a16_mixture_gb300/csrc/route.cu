@@ -128,11 +128,11 @@ FLINT_DEV float router_dot(const uint16_t* xrow, const uint4 (&wreg)[8], const u
   return acc;
 }
 
-// router_dot for a block of 4 experts x 4 tokens (H <= 2048): every
+// router_dot for a block of 4 experts x 2 NP tokens (H <= 2048): every
 // (expert, token) chain is the same per-lane sequence of fp32 fmas (chunk c
 // ascending, element k ascending) and the same butterfly; the 16 chains run
 // side by side so that each x vector loaded from shared memory feeds four
-// experts and each router vector four tokens.  Two tokens' chains share one
+// experts and each router vector 2 NP tokens.  Two tokens' chains share one
 // packed fma.rn.f32x2 (two independent IEEE fmas), so the chains round
 // exactly as scalar fmaf does.  x is in fp32 in shared memory, token pairs
 // interleaved: pair p, chunk c, quad q (elements 2q, 2q + 1 of the lane's
@@ -155,13 +155,13 @@ FLINT_DEV void fma_f32x2(uint64_t& acc, uint64_t a, uint64_t b) {
 
 // One 256-wide chunk of the block: w holds the lane's 8 router elements of
 // the 4 experts, xc points at pair 0's chunk.
-FLINT_DEV void router_chunk_4x4(uint64_t (&acc)[4][2], const uint4 (&w)[4], const float* xc,
-                                int lane) {
+template <int NP>
+FLINT_DEV void router_chunk(uint64_t (&acc)[4][NP], const uint4 (&w)[4], const float* xc, int lane) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    ulonglong2 xv[2];  // per pair: {x(2q) of both tokens, x(2q + 1) of both tokens}
+    ulonglong2 xv[NP];  // per pair: {x(2q) of both tokens, x(2q + 1) of both tokens}
 #pragma unroll
-    for (int p = 0; p < 2; ++p)
+    for (int p = 0; p < NP; ++p)
       xv[p] = *reinterpret_cast<const ulonglong2*>(xc + (size_t)p * kRtPairFloats + (q * 32 + lane) * 4);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -169,19 +169,22 @@ FLINT_DEV void router_chunk_4x4(uint64_t (&acc)[4][2], const uint4 (&w)[4], cons
       const float w0 = __uint_as_float(word << 16), w1 = __uint_as_float(word & 0xFFFF0000u);
       const uint64_t w0p = f32x2_pack(w0, w0), w1p = f32x2_pack(w1, w1);
 #pragma unroll
-      for (int p = 0; p < 2; ++p) fma_f32x2(acc[i][p], xv[p].x, w0p);
+      for (int p = 0; p < NP; ++p) fma_f32x2(acc[i][p], xv[p].x, w0p);
 #pragma unroll
-      for (int p = 0; p < 2; ++p) fma_f32x2(acc[i][p], xv[p].y, w1p);
+      for (int p = 0; p < NP; ++p) fma_f32x2(acc[i][p], xv[p].y, w1p);
     }
   }
 }
 
-FLINT_DEV void router_block_4x4(float (&res)[4][4], const float* xp0, const uint16_t* router_w,
-                                int e0, int E, int H, int lane) {
+template <int NP>
+FLINT_DEV void router_block(float (&res)[4][2 * NP], const float* xp0, const uint16_t* router_w,
+                            int e0, int E, int H, int lane) {
   const int nchunk = (H + 255) / 256;
-  uint64_t acc[4][2];
+  uint64_t acc[4][NP];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0ull;  // +0.0f in both halves
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int p = 0; p < NP; ++p) acc[i][p] = 0ull;  // +0.0f in both halves
   const uint16_t* wr[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) wr[i] = router_w + (size_t)min(e0 + i, E - 1) * H + 8 * lane;
@@ -195,15 +198,15 @@ FLINT_DEV void router_block_4x4(float (&res)[4][4], const float* xp0, const uint
   load(wa, 0);
   for (int c = 0; c < nchunk; c += 2) {
     load(wb, c + 1);
-    if (256 * c + 8 * lane < H) router_chunk_4x4(acc, wa, xp0 + (size_t)c * 512, lane);
+    if (256 * c + 8 * lane < H) router_chunk<NP>(acc, wa, xp0 + (size_t)c * 512, lane);
     load(wa, c + 2);
     if (c + 1 < nchunk && 256 * (c + 1) + 8 * lane < H)
-      router_chunk_4x4(acc, wb, xp0 + (size_t)(c + 1) * 512, lane);
+      router_chunk<NP>(acc, wb, xp0 + (size_t)(c + 1) * 512, lane);
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int p = 0; p < 2; ++p) {
+    for (int p = 0; p < NP; ++p) {
       float v[2];
       f32x2_unpack(acc[i][p], v[0], v[1]);
 #pragma unroll
@@ -674,18 +677,18 @@ __global__ void __launch_bounds__(kRtWarps * 32) route_tile_kernel(MoEArgs a) {
   }
   __syncthreads();
   if (f32) {
-    // blocks of 4 experts x 4 tokens; chains of tokens past nt run on stale
+    // blocks of 4 experts x 8 tokens; chains of tokens past nt run on stale
     // shared memory and are not stored
-    const int neb = (E + 3) / 4, ntb = (nt + 3) / 4;
+    const int neb = (E + 3) / 4, ntb = (nt + 7) / 8;
     for (int b = warp; b < neb * ntb; b += kRtWarps) {
-      const int e0 = 4 * (b / ntb), tb = 4 * (b % ntb);
-      float r[4][4];
-      router_block_4x4(r, xf + (size_t)(tb / 2) * kRtPairFloats, a.router_w, e0, E, H, lane);
+      const int e0 = 4 * (b / ntb), tb = 8 * (b % ntb);
+      float r[4][8];
+      router_block<4>(r, xf + (size_t)(tb / 2) * kRtPairFloats, a.router_w, e0, E, H, lane);
       if (lane == 0) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
+          for (int j = 0; j < 8; ++j)
             if (e0 + i < E && tb + j < nt) lg[(tb + j) * E + e0 + i] = (uint16_t)f32_to_bf16_bits(r[i][j]);
       }
     }

@@ -11,7 +11,7 @@
 // by 1-D bulk copies (cp.async.bulk, completion counted on an mbarrier) from
 // one producer warp; sixteen consumer warps run the products on the tensor
 // cores (mma.sync m16n8k16, weights as the 16-row A operand, up to 8 tokens
-// per B tile).  The producer runs ahead by the whole ring, so every SM keeps
+// per B tile); in the gate/up kernel a further warp runs the tile epilogues.  The producer runs ahead by the whole ring, so every SM keeps
 // well over 100 KB of weight reads in flight.
 //
 // Chaining (programmatic dependent launch):
@@ -281,14 +281,16 @@ FLINT_DEV void mma_b16(float (&acc)[4], const uint32_t (&af)[4][2][4], const uin
 // (expert u, 16 intermediate rows), smem rows 0..15 gate, 16..31 up, stages
 // of up to 2048 K.  Shared tiles go round-robin over the CTAs; the routed
 // tiles (U * I / 16 of them, expert-major) in contiguous chunks, so that
-// consecutive tiles of a CTA share an expert and its token rows stay in L1.
+// consecutive tiles of a CTA share an expert.  For few tokens the routed
+// tiles' activation rows are copied into shared memory once per CTA.
 //
 // Consumer warp w: routed stages -> 16-row A tile a = w & 1 (gate/up rows
 // 8a..8a+7), K slices s = w >> 1 (mod 8); shared stages -> the one A tile,
 // K slices s = w (mod 8), warps 8..15 idle.  Token n-tiles are taken NTG at
 // a time in registers; each warp adds its partial sums for the tile into its
-// own smem rows (red), which the tile epilogue sums over the warps in a
-// fixed order.
+// own smem rows of one of two alternating buffers (red) and goes on; the
+// epilogue warp sums them over the warps in a fixed order, writes act (or
+// sact) and releases the buffer.
 // What the epilogue warp needs of a finished tile (the stage's info may be
 // overwritten by then).
 struct EpiRec {

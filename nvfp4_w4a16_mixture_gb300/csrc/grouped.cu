@@ -14,34 +14,36 @@
 // plan:    per expert, tiles of up to 256 of its sorted rows (token tiles).
 // gather:  x_perm[pos] = x[token of sorted pair pos] (so GEMM1 reads its A
 //          operand as plain 2-D TMA tiles).
-// GEMM1:   routed units (token tile, 64 intermediate rows): D = X W13^T over
-//          128 weight rows (64 gate + 64 up), epilogue SwiGLU -> act;
-//          shared units (128 tokens, 32 rows): BF16 weights, -> sact.
-// GEMM2:   routed units (token tile, 128 output rows): D = act W2^T, epilogue
+// GEMM1:   routed units (token tile, 128 intermediate rows): D = X W13^T over
+//          256 weight rows (128 gate + the 128 matching up rows), epilogue
+//          SwiGLU -> act; shared units (256 tokens, 32 rows): BF16 weights,
+//          -> sact.
+// GEMM2:   routed units (token tile, 256 output rows): D = act W2^T, epilogue
 //          y = bf16(acc * gs2); shared units likewise: sact Wsd^T -> ys.
 // combine: out[t] = bf16(bf16(sum_j tw_j y[row of (t, j)]) + ys[t]).
 //
-// GEMM kernel (persistent, one CTA per SM, 608 threads):
-//   warp 16: TMA producer of the stages (A tiles; the shared expert's BF16 B
-//           tile),
-//   warp 18: TMA producer of the NVFP4 code tiles (a ring of their own, up
-//           to 6 K blocks ahead),
-//   warp 17: MMA issuer (one thread) and TMEM owner (512 columns: per
-//           128-token half two 128 x 128 fp32 accumulators, K block kb going
-//           to accumulator kb % 2, added in fp32 by the epilogue -- so the
-//           tensor core's own accumulation spans half the reduction; the
-//           shared expert's gate/up units take one 128-token half, 64 weight
-//           rows and eight accumulators, because its bf16(gS), bf16(uS)
-//           roundings feed every output of the token),
-//   warps 0..15: two groups of 8 taking alternate K blocks; in a group,
-//           threads 2r, 2r + 1 own B row r: 32 codes each of a K block ->
-//           bf16 e2m1 * scale * 2^-7, exact, computed in registers as soon
-//           as the codes are in, written in the 128-byte swizzled K-major
-//           layout once the stage is free.  Then all 16 run the epilogue
-//           (TMEM lane quarter warp % 4, half (warp / 4) % 2, column half
-//           warp / 8; TMEM lane = token row).
-// Rings: 4 stages of {A 2 x 16 KB, B 16 KB}; 6 code tiles of 4 KB; the
-// dequantising threads' block scales (asynchronous copies, 6 K blocks ahead).
+// GEMM kernel: persistent clusters of two CTAs on two SMs (one pair per two
+// SMs), 640 threads per CTA.  Every unit is a pair unit: 256 token rows
+// (CTA c owns rows 128 c ..) by n weight rows (CTA c dequantises n / 2 of
+// them); one thread of the leader CTA issues tcgen05.mma.cta_group::2
+// (M = 256), which reads A and B halves from both CTAs' shared memory and
+// writes each CTA's 128 token rows into its own TMEM.
+//   warp 13: TMA producer of the stages (A tiles; the shared expert's BF16
+//           B tiles),
+//   warp 17: TMA producer of the NVFP4 code tiles (a ring of their own),
+//   warp 9:  leader: MMA issuer and TMEM owner (two 256-column accumulator
+//           buffers, so one unit's epilogue overlaps the next unit's MMAs);
+//           peer: relays "this CTA's half of stage s is in" to the leader's
+//           barrier,
+//   8 dequantising warps: two groups of 4 taking alternate K blocks; one
+//           thread per B row: 128 codes of a K block -> bf16 e2m1 * scale *
+//           2^-7, exact, the first half before the stage is free and the
+//           second after, stored into the 128-byte swizzled K-major layout,
+//   8 epilogue warps: TMEM -> registers (tcgen05.ld), scales, SwiGLU, BF16
+//           stores (lane quarter warp % 4, two column groups).
+// Rings: 3 stages of {A 2 x 16 KB, B 2 x 16 KB} (K blocks of 128); 3 code
+// tiles of 8 KB; the dequantising threads' block scales (asynchronous 8-byte
+// copies three K blocks ahead, across unit boundaries).
 // Every wait is bounded (FLINT_ERR_TIMEOUT in the status word on expiry).
 #include <cuda.h>
 #include <cudaTypedefs.h>

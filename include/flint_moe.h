@@ -50,7 +50,9 @@ enum {
 };
 
 /* Problem shape.
- *   M      tokens (rows of x), M >= 1
+ *   M      tokens (rows of x), M >= 0.  M = 0 (an empty batch) is checked
+ *          as a shape and returns FLINT_OK without any launch or memory
+ *          access; the M-sized buffers and the workspace may then be NULL.
  *   H      hidden size; multiple of 128
  *   E      routed experts, 1..256
  *   top_k  experts per token, 1..min(E, 32)

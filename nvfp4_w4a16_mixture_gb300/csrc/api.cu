@@ -11,7 +11,7 @@ static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 static bool shape_valid(const flint_moe_shape* s) {
   if (!s) return false;
-  if (s->M < 1 || s->H < 128 || s->H % 128 != 0) return false;
+  if (s->M < 0 || s->H < 128 || s->H % 128 != 0) return false;
   if (s->E < 1 || s->E > kMaxE) return false;
   if (s->top_k < 1 || s->top_k > s->E || s->top_k > kMaxTopK) return false;
   if (s->I < 128 || s->I % 128 != 0) return false;
@@ -106,6 +106,7 @@ size_t flint_moe_workspace_bytes(const flint_moe_shape* shape) {
 int flint_moe_route(const void* x, const void* router_w, const flint_moe_shape* shape, int32_t* ids,
                     float* tw, void* workspace, size_t workspace_bytes, flint_stream_t stream) {
   if (!shape_valid(shape)) return FLINT_ERR_INVALID_ARG;
+  if (shape->M == 0) return FLINT_OK;  // an empty batch: nothing to launch
   if (!x || !router_w || !ids || !tw) return FLINT_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(router_w, 16) || !aligned(ids, 4) || !aligned(tw, 4))
     return FLINT_ERR_INVALID_ARG;
@@ -130,6 +131,7 @@ int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13, c
                       const flint_moe_shape* shape, void* out, int32_t* ids_out, float* tw_out,
                       void* workspace, size_t workspace_bytes, flint_stream_t stream) {
   if (!shape_valid(shape)) return FLINT_ERR_INVALID_ARG;
+  if (shape->M == 0) return FLINT_OK;  // an empty batch: nothing to launch
   if (!x || !router_w || !w13 || !w13_sf || !w13_gs || !w2 || !w2_sf || !w2_gs || !out)
     return FLINT_ERR_INVALID_ARG;
   if (shape->SI > 0 && (!shared_gu || !shared_down)) return FLINT_ERR_INVALID_ARG;

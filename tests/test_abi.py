@@ -41,7 +41,8 @@ def test_workspace_bytes_valid_and_invalid_shapes():
     assert ok > 0 and ok % 256 == 0
     big = fm.flint_moe_workspace_bytes(4096, 2048, 128, 8, 768, 768)
     assert big > ok
-    for bad in [(0, 2048, 128, 8, 768, 768), (1, 2000, 128, 8, 768, 768),
+    assert fm.flint_moe_workspace_bytes(0, 2048, 128, 8, 768, 768) > 0  # empty batch
+    for bad in [(-1, 2048, 128, 8, 768, 768), (1, 2000, 128, 8, 768, 768),
                 (1, 2048, 257, 8, 768, 768), (1, 2048, 8, 9, 768, 768),
                 (1, 2048, 128, 0, 768, 768), (1, 2048, 128, 33, 768, 768),
                 (1, 2048, 128, 8, 700, 768), (1, 2048, 128, 8, 768, 100),
@@ -63,6 +64,21 @@ def _call_forward(ptrs, shape, ws_bytes):
     s = _lib.flint_moe_shape(*shape)
     return lib.flint_moe_forward(*ptrs[:10], ctypes.byref(s), ptrs[10], None, None, ptrs[11],
                                  ws_bytes, None)
+
+
+def test_empty_batch_is_a_no_op():
+    """M = 0: the shape is checked and every entry point returns FLINT_OK
+    before any CUDA call, even with NULL buffers and no workspace (so this
+    runs without a GPU); a bad shape with M = 0 is still rejected."""
+    lib = fm.load()
+    s = _lib.flint_moe_shape(0, 2048, 128, 8, 768, 768)
+    assert lib.flint_moe_forward(*([None] * 10), ctypes.byref(s), None, None, None, None, 0,
+                                 None) == fm.FLINT_OK
+    assert lib.flint_moe_route(None, None, ctypes.byref(s), None, None, None, 0, None) == fm.FLINT_OK
+    assert lib.flint_moe_route_noalloc(None, None, ctypes.byref(s), None, None, None) == fm.FLINT_OK
+    bad = _lib.flint_moe_shape(0, 2000, 128, 8, 768, 768)
+    assert lib.flint_moe_forward(*([None] * 10), ctypes.byref(bad), None, None, None, None, 0,
+                                 None) == fm.FLINT_ERR_INVALID_ARG
 
 
 def test_validation_is_synchronous_and_touches_no_memory():

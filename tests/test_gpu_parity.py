@@ -208,3 +208,19 @@ def test_bad_arguments_raise_before_launch(decode_layer):
     with pytest.raises(fm.FlintMoEError) as ei:
         fm.forward_layer(x1, layer, k, workspace=small, out=out)
     assert ei.value.code == fm.FLINT_ERR_WORKSPACE
+
+
+def test_empty_batch_between_real_calls(decode_layer):
+    """M = 0 through the binding (zero-row CUDA tensors) returns without
+    launching, and leaves the stream and workspace fit for the next call."""
+    _, layer, k = decode_layer
+    ws = fm.alloc_workspace(16, layer.H, layer.E, k, layer.I, layer.SI)
+    x0 = torch.empty(0, layer.H, dtype=torch.bfloat16, device="cuda")
+    out0 = fm.forward_layer(x0, layer, k, workspace=ws)
+    assert out0.shape == (0, layer.H)
+    ids0 = torch.empty(0, k, dtype=torch.int32, device="cuda")
+    tw0 = torch.empty(0, k, dtype=torch.float32, device="cuda")
+    fm.flint_moe_route(x0, layer.router_w, k, ids0, tw0, ws, I=layer.I, SI=layer.SI)
+    assert fm.flint_moe_status(ws) == fm.FLINT_OK
+    gen = torch.Generator(device="cuda").manual_seed(300)
+    compare(synth.make_x(16, layer.H, gen, "cuda"), layer, k, ws=ws)

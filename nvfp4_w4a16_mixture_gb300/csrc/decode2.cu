@@ -502,11 +502,21 @@ __global__ void __launch_bounds__(kGuThreads, 1) gate_up2_kernel(MoEArgs a) {
     }
     pdl_wait();  // router finished: routing records are final
     pdl_launch_dependents();
-    const int U = ldg_cg_i32(a.ws.uniq);
-    const int x16 = (M <= kX16MaxTokens && ldg_cg_i32(a.ws.glob_cnt + 1) == 0) ? 1 : 0;
+    // one token routes to k distinct experts, so U needs no read then, and
+    // the first record's loads go out with the f16-copy report
+    const int U = M == 1 ? a.k : ldg_cg_i32(a.ws.uniq);
     const int tpe = I / 16;  // tiles per expert
     const int T = U * tpe;
     const int lo = (int)((long long)T * c / G), hi = (int)((long long)T * (c + 1) / G);
+    int r_hdr = 0, r_p0 = 0, r_p1 = 0;  // the record of expert slot lo / tpe, in flight
+    auto load_record = [&](int u) {
+      const int* rec = a.ws.urec + (size_t)u * kUrecInts;
+      r_hdr = lane < 3 ? ldg_cg_i32(rec + lane) : 0;
+      r_p0 = ldg_cg_i32(rec + 4 + lane);
+      r_p1 = ldg_cg_i32(rec + 36 + lane);
+    };
+    if (lo < hi) load_record(lo / tpe);
+    const int x16 = (M <= kX16MaxTokens && ldg_cg_i32(a.ws.glob_cnt + 1) == 0) ? 1 : 0;
     const bool staged = xpitch && lo < hi;
     if (staged) {  // the routed tiles' activation rows, once: the f16 copy or x
       fence_proxy_async_global();  // the router's f16 copy, read by bulk copies
@@ -521,15 +531,12 @@ __global__ void __launch_bounds__(kGuThreads, 1) gate_up2_kernel(MoEArgs a) {
     for (int tile = lo; tile < hi; ++tile) {
       const int u = tile / tpe, r0 = (tile % tpe) * 16;
       if (u != cur_u) {  // the expert's record: one round trip, lanes in parallel
-        const int* rec = a.ws.urec + (size_t)u * kUrecInts;
-        const int hdr = lane < 3 ? ldg_cg_i32(rec + lane) : 0;
-        const int p0 = ldg_cg_i32(rec + 4 + lane);
-        const int p1 = ldg_cg_i32(rec + 36 + lane);
-        e = __shfl_sync(0xffffffffu, hdr, 0);
-        cnt = __shfl_sync(0xffffffffu, hdr, 1);
-        off = __shfl_sync(0xffffffffu, hdr, 2);
-        tok0 = lane < cnt ? (short)(p0 / a.k) : 0;
-        tok1 = lane + 32 < cnt ? (short)(p1 / a.k) : 0;
+        if (tile != lo) load_record(u);
+        e = __shfl_sync(0xffffffffu, r_hdr, 0);
+        cnt = __shfl_sync(0xffffffffu, r_hdr, 1);
+        off = __shfl_sync(0xffffffffu, r_hdr, 2);
+        tok0 = lane < cnt ? (short)(r_p0 / a.k) : 0;
+        tok1 = lane + 32 < cnt ? (short)(r_p1 / a.k) : 0;
         cur_u = u;
       }
       for (int k0 = 0; k0 < H; k0 += kGuKst4) {

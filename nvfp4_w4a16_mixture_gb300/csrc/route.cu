@@ -586,23 +586,37 @@ __global__ void __cluster_dims__(kRcCtas, 1, 1) __launch_bounds__(kRcWarps * 32)
     atomicOr(&S.mask[S.ids[p / k][p % k]], 1ull << (p / k));
   __syncthreads();
   if (warp == 0) {  // exclusive scans of counts and of "routed" flags
-    int run = 0, urun = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      const int c = e < E ? __popcll(S.mask[e]) : 0;
-      const int u = c > 0 ? 1 : 0;
-      int ic = c, iu = u;
+    // lane l takes experts per * l .. per * l + per - 1: its own sums, then
+    // one warp scan of the lanes' totals
+    constexpr int kPer = kMaxE / 32;
+    const int per = (E + 31) / 32;
+    int c[kPer], sc = 0, su = 0;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int vc = __shfl_up_sync(0xffffffffu, ic, o);
-        const int vu = __shfl_up_sync(0xffffffffu, iu, o);
-        if (lane >= o) { ic += vc; iu += vu; }
-      }
-      if (e < E) { S.off[e] = run + ic - c; S.uidx[e] = urun + iu - u; }
-      run += __shfl_sync(0xffffffffu, ic, 31);
-      urun += __shfl_sync(0xffffffffu, iu, 31);
+    for (int q = 0; q < kPer; ++q) {
+      const int e = per * lane + q;
+      c[q] = q < per && e < E ? __popcll(S.mask[e]) : 0;
+      sc += c[q];
+      su += c[q] > 0 ? 1 : 0;
     }
-    if (lane == 0) { S.off[E] = run; S.uidx[E] = urun; }
+    int ic = sc, iu = su;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int vc = __shfl_up_sync(0xffffffffu, ic, o);
+      const int vu = __shfl_up_sync(0xffffffffu, iu, o);
+      if (lane >= o) { ic += vc; iu += vu; }
+    }
+    int run = ic - sc, urun = iu - su;  // exclusive starts of this lane's experts
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int e = per * lane + q;
+      if (q < per && e < E) {
+        S.off[e] = run;
+        S.uidx[e] = urun;
+      }
+      run += c[q];
+      urun += c[q] > 0 ? 1 : 0;
+    }
+    if (lane == 31) { S.off[E] = ic; S.uidx[E] = iu; }
   }
   __syncthreads();
   for (int e = tid; e < E; e += kRcWarps * 32) {

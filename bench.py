@@ -371,9 +371,10 @@ def run_ours(args, rank, world, local):
     return res, xs, layers
 
 
-def cpu_baseline(cfg: str, n_tokens: int = 64, seed: int = 5):
+def cpu_baseline(cfg: str, n_tokens: int = 384, seed: int = 5):
     """The oracle on a bounded sample: n_tokens tokens of the configuration's
-    layer shape (one layer), all host cores (OpenMP over tokens)."""
+    layer shape (one layer), all host cores (OpenMP over tokens); 384 tokens
+    are about 25 s of CPU work on 16 cores."""
     import oracle
     M, H, E, k, I, SI = synth.CONFIGS[cfg]
     scale = synth.zipf_router_scale(E) if cfg.startswith("skew") else None

@@ -54,6 +54,10 @@ constexpr int kKP = kCons / 2;  // K parts of a routed stage (x 2 A tiles)
 
 // ---- down ring: a stage holds up to 8 weight blocks of 16 output rows.
 constexpr int kDnStages = 3;
+// down stages whose weights are requested before the dependency wait; the
+// activation copies of stage 0 then go out right after it, ahead of the
+// later stages' weights
+constexpr int kDnPrefetch = 1;
 constexpr int kDnStageBytes = 57344;
 constexpr int kDnMaxBlocks = 8;
 constexpr int kDnMaxItems = 64;
@@ -884,7 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
       if (waited) {
         finish(n - 1);
         pend = n;
-      } else if (n - pend == kDnStages || unit >= nunits) {
+      } else if (n - pend == kDnPrefetch || unit >= nunits) {
         pdl_wait();  // gate/up finished: act and sact are complete
         fence_proxy_async_global();
         waited = true;

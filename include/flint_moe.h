@@ -162,6 +162,19 @@ int flint_moe_status(void* workspace, flint_stream_t stream);
 /* Static description of an error code. */
 const char* flint_moe_strerror(int code);
 
+/* Test hook for the failure path (process-wide, default off).  With
+ * site = FLINT_FAULT_DOWN_HANDOVER the next launches of the decode down
+ * kernel leave out one signal: the warp holding the second half of an item's
+ * K never raises its hand-over flag, so the warp waiting for it gives up
+ * after its bounded wait (200 ms), records FLINT_ERR_TIMEOUT with the wait
+ * site, CTA and stage in status words 1..3 of the workspace, and every warp
+ * of the launch exits; the outputs of such a call are undefined, the context
+ * stays usable and the next call without the hook is exact again.  Nothing
+ * faults, traps or hangs.  site = 0 turns the hook off.  Returns FLINT_OK, or
+ * FLINT_ERR_INVALID_ARG for an unknown site. */
+enum { FLINT_FAULT_NONE = 0, FLINT_FAULT_DOWN_HANDOVER = 17 };
+int flint_moe_debug_fault(int site);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,11 +21,14 @@ FLINT_ERR_WORKSPACE = -3
 FLINT_ERR_CUDA = -4
 FLINT_ERR_TIMEOUT = -5
 FLINT_ERR_SCRATCH = -6
+FLINT_FAULT_NONE = 0
+FLINT_FAULT_DOWN_HANDOVER = 17
 
 # Every C symbol the header declares (checked by tests/test_abi.py).
 EXPORTED = ("flint_moe_workspace_bytes", "flint_moe_route", "flint_moe_forward",
             "flint_moe_route_noalloc", "flint_moe_route_noalloc_bytes",
-            "flint_moe_route_noalloc_capacity", "flint_moe_status", "flint_moe_strerror")
+            "flint_moe_route_noalloc_capacity", "flint_moe_status", "flint_moe_strerror",
+            "flint_moe_debug_fault")
 
 
 class FlintMoEError(RuntimeError):
@@ -71,6 +74,8 @@ def load() -> ctypes.CDLL:
             lib.flint_moe_status.argtypes = [P, P]
             lib.flint_moe_strerror.restype = ctypes.c_char_p
             lib.flint_moe_strerror.argtypes = [ctypes.c_int]
+            lib.flint_moe_debug_fault.restype = ctypes.c_int
+            lib.flint_moe_debug_fault.argtypes = [ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -161,6 +166,14 @@ def flint_moe_route_noalloc_capacity() -> int:
 def flint_moe_status(workspace, stream=None) -> int:
     """Synchronise `stream` and return (and clear) the workspace status word."""
     return int(load().flint_moe_status(_ptr(workspace), _stream(stream)))
+
+
+def flint_moe_debug_fault(site: int) -> None:
+    """Failure-path test hook (see include/flint_moe.h): leave one device
+    signal out so that a bounded wait gives up; FLINT_FAULT_NONE turns it off."""
+    rc = load().flint_moe_debug_fault(int(site))
+    if rc != FLINT_OK:
+        raise FlintMoEError(rc, "flint_moe_debug_fault")
 
 
 # ---------------------------------------------------------------- helpers

@@ -9,6 +9,9 @@ namespace flint {
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+static int g_fault_site = 0;  // test hook, see flint_moe_debug_fault
+int debug_fault_site() { return g_fault_site; }
+
 static bool shape_valid(const flint_moe_shape* s) {
   if (!s) return false;
   if (s->M < 0 || s->H < 128 || s->H % 128 != 0) return false;
@@ -119,6 +122,7 @@ int flint_moe_route(const void* x, const void* router_w, const flint_moe_shape* 
   a.ids_out = ids;
   a.tw_out = tw;
   a.M = shape->M; a.H = shape->H; a.E = shape->E; a.k = shape->top_k; a.I = shape->I; a.SI = shape->SI;
+  a.fault = debug_fault_site();
   a.ws = ws_pointers(workspace, L);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (launch_route(a, false, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
@@ -158,6 +162,7 @@ int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13, c
   a.ids_out = ids_out;
   a.tw_out = tw_out;
   a.M = shape->M; a.H = shape->H; a.E = shape->E; a.k = shape->top_k; a.I = shape->I; a.SI = shape->SI;
+  a.fault = debug_fault_site();
   a.ws = ws_pointers(workspace, L);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
@@ -186,6 +191,12 @@ int flint_moe_status(void* workspace, flint_stream_t stream) {
     if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return FLINT_ERR_CUDA;
     return status;
   }
+  return FLINT_OK;
+}
+
+int flint_moe_debug_fault(int site) {
+  if (site != FLINT_FAULT_NONE && site != FLINT_FAULT_DOWN_HANDOVER) return FLINT_ERR_INVALID_ARG;
+  g_fault_site = site;
   return FLINT_OK;
 }
 

@@ -104,8 +104,12 @@ struct MoEArgs {
   int* ids_out;   // optional user copy
   float* tw_out;  // optional user copy
   int M, H, E, k, I, SI;
+  int fault;  // test hook: a FLINT_FAULT_* site whose signal is left out (0: none)
   Ws ws;
 };
+
+// The failure-path test hook's current site (flint_moe_debug_fault).
+int debug_fault_site();
 
 // Launchers (return cudaSuccess or the launch error).  `pdl` launches the
 // kernel with programmatic stream serialisation.

@@ -66,6 +66,15 @@ def _call_forward(ptrs, shape, ws_bytes):
                                  ws_bytes, None)
 
 
+def test_fault_hook_accepts_only_known_sites():
+    """The failure-path test hook is a host-side switch (no CUDA call)."""
+    lib = fm.load()
+    assert lib.flint_moe_debug_fault(fm.FLINT_FAULT_DOWN_HANDOVER) == fm.FLINT_OK
+    assert lib.flint_moe_debug_fault(fm.FLINT_FAULT_NONE) == fm.FLINT_OK
+    for bad in (1, -1, 9999):
+        assert lib.flint_moe_debug_fault(bad) == fm.FLINT_ERR_INVALID_ARG
+
+
 def test_empty_batch_is_a_no_op():
     """M = 0: the shape is checked and every entry point returns FLINT_OK
     before any CUDA call, even with NULL buffers and no workspace (so this

@@ -224,3 +224,27 @@ def test_empty_batch_between_real_calls(decode_layer):
     assert fm.flint_moe_status(ws) == fm.FLINT_OK
     gen = torch.Generator(device="cuda").manual_seed(300)
     compare(synth.make_x(16, layer.H, gen, "cuda"), layer, k, ws=ws)
+
+
+def test_bounded_wait_reports_timeout_and_context_recovers(decode_layer):
+    """Failure path without a GPU fault: the test hook leaves out the down
+    kernel's K-half hand-over signal, the waiting warp gives up after its
+    bounded wait, the launch ends and the status word reports
+    FLINT_ERR_TIMEOUT with the wait site; the next call without the hook is
+    exact again on the same workspace and stream."""
+    x1, layer, k = decode_layer
+    ws = fm.alloc_workspace(16, layer.H, layer.E, k, layer.I, layer.SI)
+    fm.flint_moe_debug_fault(fm.FLINT_FAULT_DOWN_HANDOVER)
+    try:
+        fm.forward_layer(x1, layer, k, workspace=ws)
+        torch.cuda.synchronize()
+        words = ws[:16].view(torch.int32).cpu().tolist()
+    finally:
+        fm.flint_moe_debug_fault(fm.FLINT_FAULT_NONE)
+    assert words[0] == fm.FLINT_ERR_TIMEOUT
+    assert words[1] == fm.FLINT_FAULT_DOWN_HANDOVER  # the wait site that gave up
+    assert fm.flint_moe_status(ws) == fm.FLINT_ERR_TIMEOUT  # read and cleared
+    assert fm.flint_moe_status(ws) == fm.FLINT_OK
+    gen = torch.Generator(device="cuda").manual_seed(301)
+    compare(synth.make_x(16, layer.H, gen, "cuda"), layer, k, ws=ws)
+    assert fm.flint_moe_status(ws) == fm.FLINT_OK

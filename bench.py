@@ -30,6 +30,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -111,7 +112,10 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # raw samples (the JSON line carries their summary); FLINT_BENCH_CLOCKS_DIR
+        # keeps them somewhere else than the temporary directory
+        out_dir = os.environ.get("FLINT_BENCH_CLOCKS_DIR", tempfile.gettempdir())
+        self.path = os.path.join(out_dir, f"flint_clocks_rank{index}.csv")
 
     def start(self):
         try:

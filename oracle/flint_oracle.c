@@ -17,7 +17,7 @@
  * in the type the pages name.  Compile with -O2 -ffp-contract=off and without
  * fast-math so that each C operator is one IEEE-754 operation.
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *  R1  router-logit summation order (the pages use a Triton tree sum): 32
  *      fp32 partial sums, partial l holding the products of the elements h
  *      with (h / 8) mod 32 == l in ascending h, then combined by the xor

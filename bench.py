@@ -138,30 +138,43 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10:
-                continue
-            try:
-                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
-                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
-                rows.append((ts + frac, float(parts[2]), float(parts[3]), parts[5:]))
-            except Exception:
-                continue
-        if not rows:
-            return None
-        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
-        use = inside or sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
-        reasons = set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in use:
-            for name, v in zip(names, r[3][1:5]):
-                if v.strip().lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
-                "reasons": sorted(reasons), "samples": len(use),
-                "samples_inside_timed_region": len(inside)}
+        with open(self.path) as f:
+            return summarize_clocks(parse_clock_lines(f), t0, t1)
+
+
+def parse_clock_lines(lines):
+    """Rows (unix time, SM MHz, max SM MHz, [reason fields]) of nvidia-smi's
+    csv,noheader,nounits output for ClockSampler.FIELDS; other lines skipped."""
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+            rows.append((ts + frac, float(parts[2]), float(parts[3]), parts[5:]))
+        except Exception:
+            continue
+    return rows
+
+
+def summarize_clocks(rows, t0: float, t1: float):
+    """The JSON line's clocks object: median SM clock and the throttle reasons
+    seen in [t0, t1] (the nearest three samples if none fell inside)."""
+    if not rows:
+        return None
+    inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+    use = inside or sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
+    reasons = set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for r in use:
+        for name, v in zip(names, r[3][1:5]):
+            if v.strip().lower() == "active":
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+            "reasons": sorted(reasons), "samples": len(use),
+            "samples_inside_timed_region": len(inside)}
 
 
 # --------------------------------------------------------------- workload

@@ -248,3 +248,21 @@ def test_bounded_wait_reports_timeout_and_context_recovers(decode_layer):
     gen = torch.Generator(device="cuda").manual_seed(301)
     compare(synth.make_x(16, layer.H, gen, "cuda"), layer, k, ws=ws)
     assert fm.flint_moe_status(ws) == fm.FLINT_OK
+
+
+def test_decode_f16_copy_guard_with_an_unrepresentable_value(decode_layer):
+    """A token holding 2^-40 next to values near 4: scaled by its power of two
+    into f16 that value underflows, so the router reports the copy inexact and
+    the batch's routed gate/up takes the bf16 path; the outputs still match
+    the oracle, and the next batch on the same workspace (copy exact again)
+    does too."""
+    _, layer, k = decode_layer
+    ws = fm.alloc_workspace(16, layer.H, layer.E, k, layer.I, layer.SI)
+    gen = torch.Generator(device="cuda").manual_seed(302)
+    x = synth.make_x(16, layer.H, gen, "cuda")
+    x[3, 5] = 2.0 ** -40
+    assert float(x[3, 5]) == 2.0 ** -40  # held exactly in bf16
+    compare(x, layer, k, ws=ws)
+    assert fm.flint_moe_status(ws) == fm.FLINT_OK
+    compare(synth.make_x(16, layer.H, gen, "cuda"), layer, k, ws=ws)
+    assert fm.flint_moe_status(ws) == fm.FLINT_OK

@@ -471,7 +471,7 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     if rank == 0:
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and world == 1:  # the host baseline is an N = 1 figure
             res["cpu_baseline"] = cpu_baseline(args.config)
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -130,7 +130,7 @@ FLINT_DEV float router_dot(const uint16_t* xrow, const uint4 (&wreg)[8], const u
 
 // router_dot for a block of 4 experts x 2 NP tokens (H <= 2048): every
 // (expert, token) chain is the same per-lane sequence of fp32 fmas (chunk c
-// ascending, element k ascending) and the same butterfly; the 16 chains run
+// ascending, element k ascending) and the same butterfly; the 8 NP chains run
 // side by side so that each x vector loaded from shared memory feeds four
 // experts and each router vector 2 NP tokens.  Two tokens' chains share one
 // packed fma.rn.f32x2 (two independent IEEE fmas), so the chains round
@@ -644,10 +644,11 @@ __global__ void __cluster_dims__(kRcCtas, 1, 1) __launch_bounds__(kRcWarps * 32)
 
 // ----------------------------------------------------------------------------
 // Router for many tokens: CTA b handles tokens 16 b .. 16 b + 15 with their
-// rows staged in shared memory; warp w computes the logits of experts w,
-// w + 16, ... for all 16 tokens (router row in registers, router_dot: the
-// canonical order, so ids match the other routers bit for bit), then warp w
-// runs the top-k of token 16 b + w from shared memory.  No cross-CTA step.
+// rows staged in shared memory; the warps take blocks of 4 experts x 8 tokens
+// (router_block, H <= 2048) or one expert's row for all 16 tokens
+// (router_dot, longer rows), the canonical per-chain order either way, so ids
+// match the other routers bit for bit; then warp w runs the top-k of token
+// 16 b + w from shared memory.  No cross-CTA step.
 constexpr int kRtTokens = 16;
 constexpr int kRtWarps = 16;
 

@@ -136,9 +136,12 @@ int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13,
  * logits and int32 + fp32 [M, top_k]; when that exceeds
  * flint_moe_route_noalloc_capacity() the call returns FLINT_ERR_SCRATCH and
  * enqueues nothing (at E = 128, top_k = 8 about 6500 tokens fit).
- * The first call on each device looks up the scratch's device address with
- * that device current (cudaGetSymbolAddress, which may load the module); make
- * that first call outside any stream capture.  Every call clears the counters
+ * The first call in each CUDA context looks up the scratch's device address
+ * in that context (cudaGetSymbolAddress, which may load the module) and
+ * caches it under the context's process-unique id, so a context created
+ * later (another device, a driver-API context, or the primary context
+ * re-created after cudaDeviceReset) gets its own lookup; make the first call
+ * in a context outside any stream capture.  Every call clears the counters
  * (cudaMemsetAsync on `stream`) before the kernel; nothing else needs an
  * initial value.  All calls on one device share the one scratch: two calls
  * that may run at the same time on the GPU (different streams or host threads
@@ -156,7 +159,10 @@ size_t flint_moe_route_noalloc_capacity(void);
 /* Synchronises `stream`, then reads and clears the device status word of
  * `workspace`: FLINT_OK, or the error a kernel recorded (FLINT_ERR_TIMEOUT
  * when a bounded device-side wait gave up).  FLINT_ERR_CUDA if the stream
- * reports an error. */
+ * reports an error.  This call blocks the calling host thread: it waits for
+ * `stream` and then reads (and, when non-zero, clears) the word with
+ * synchronous copies on the legacy default stream, so it does not belong
+ * inside stream capture or a latency-critical loop. */
 int flint_moe_status(void* workspace, flint_stream_t stream);
 
 /* Static description of an error code. */

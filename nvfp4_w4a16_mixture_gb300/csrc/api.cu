@@ -1,4 +1,6 @@
 // C-ABI entry points of libflint_moe (declared in include/flint_moe.h).
+#include <atomic>
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -9,8 +11,8 @@ namespace flint {
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-static int g_fault_site = 0;  // test hook, see flint_moe_debug_fault
-int debug_fault_site() { return g_fault_site; }
+static std::atomic<int> g_fault_site{0};  // test hook, see flint_moe_debug_fault
+int debug_fault_site() { return g_fault_site.load(std::memory_order_relaxed); }
 
 static bool shape_valid(const flint_moe_shape* s) {
   if (!s) return false;
@@ -196,7 +198,7 @@ int flint_moe_status(void* workspace, flint_stream_t stream) {
 
 int flint_moe_debug_fault(int site) {
   if (site != FLINT_FAULT_NONE && site != FLINT_FAULT_DOWN_HANDOVER) return FLINT_ERR_INVALID_ARG;
-  g_fault_site = site;
+  g_fault_site.store(site, std::memory_order_relaxed);
   return FLINT_OK;
 }
 

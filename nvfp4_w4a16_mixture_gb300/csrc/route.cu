@@ -7,6 +7,8 @@
 // (token, slot) pairs by expert) is the token permutation the grouped path of
 // flint_moe consumes ("perm" of _combine_kernel); the decode path uses the
 // same grouping to stream each routed expert's weights once per call.
+#include <atomic>
+
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
 
@@ -756,14 +758,14 @@ cudaError_t launch_route(const MoEArgs& a, bool build_meta, cudaStream_t st, boo
   void* args[] = {&aa, &meta_in_router, &rowof};
   cudaError_t err;
   if (!small && route_tile_smem(a) <= 200 * 1024) {
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
       err = cudaFuncSetAttribute((const void*)route_tile_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
       if (err != cudaSuccess) return err;
-      attr_set[dev] = true;
+      attr_set[dev].store(true, std::memory_order_release);
     }
     void* targs[] = {&aa};
     cudaLaunchConfig_t cfg = {};

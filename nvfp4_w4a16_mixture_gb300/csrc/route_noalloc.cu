@@ -1,7 +1,7 @@
 // flint_moe_route_noalloc: routing with the library's own fixed scratch
 // (declared in include/flint_moe.h).  Same kernel and numerics as
 // flint_moe_route; only where the intermediates live differs.
-#include <atomic>
+#include <mutex>
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -13,12 +13,27 @@ namespace flint {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;  // 2 MiB per device
-constexpr int kMaxDevices = 64;
 
 // The scratch itself: zero at module load, like all static device memory.
 __device__ __align__(256) unsigned char g_route_scratch[kNoAllocScratchBytes];
 
-std::atomic<void*> g_scratch_addr[kMaxDevices];
+// Device addresses of the scratch, one per CUDA context that has called the
+// entry point, keyed by the context's process-unique id (cuCtxGetId): a
+// context created later (another device, a driver-API context, or the primary
+// context re-created after cudaDeviceReset) never matches an older entry.
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+constexpr int kMaxContexts = 64;
+std::mutex g_scratch_mu;
+ScratchEntry g_scratch[kMaxContexts];
+int g_scratch_n = 0;
+
+using CtxGetCurrentFn = int (*)(void**);
+using CtxGetIdFn = int (*)(void*, unsigned long long*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
@@ -50,16 +65,60 @@ bool shape_ok(const flint_moe_shape* s) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Device address of this device's copy of the scratch, looked up once per
-// device (with that device current) and cached.
+// Id of the calling thread's current CUDA context (0 when it has none yet).
+// The driver entry points are looked up through the runtime (no link against
+// the driver library).
+int current_context_id(unsigned long long* id) {
+  if (!g_ctx_get_current || !g_ctx_get_id) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) !=
+            cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || !f1)
+      return FLINT_ERR_CUDA;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) !=
+            cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess || !f2)
+      return FLINT_ERR_CUDA;
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f2);
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+  }
+  void* ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != 0) return FLINT_ERR_CUDA;
+  *id = 0;
+  if (ctx && g_ctx_get_id(ctx, id) != 0) return FLINT_ERR_CUDA;
+  return FLINT_OK;
+}
+
+// Device address of the scratch in the current context.  The first call in
+// a context looks it up with cudaGetSymbolAddress (which may load the module
+// into that context, so it belongs outside stream capture); later calls in
+// the same context reuse the cached address.
 int scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FLINT_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return FLINT_ERR_UNSUPPORTED;
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (!p) {
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return FLINT_ERR_CUDA;
-    g_scratch_addr[dev].store(p, std::memory_order_release);
+  unsigned long long id = 0;
+  int rc = current_context_id(&id);
+  if (rc != FLINT_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (id != 0)
+    for (int i = 0; i < g_scratch_n; ++i)
+      if (g_scratch[i].ctx_id == id) {
+        *out = g_scratch[i].addr;
+        return FLINT_OK;
+      }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return FLINT_ERR_CUDA;
+  if (id == 0) {  // the lookup above made the runtime's context current
+    rc = current_context_id(&id);
+    if (rc != FLINT_OK) return rc;
+  }
+  if (id != 0) {
+    if (g_scratch_n < kMaxContexts) {
+      g_scratch[g_scratch_n++] = {id, p};
+    } else {  // more contexts than slots: recycle the oldest entry
+      for (int i = 1; i < kMaxContexts; ++i) g_scratch[i - 1] = g_scratch[i];
+      g_scratch[kMaxContexts - 1] = {id, p};
+    }
   }
   *out = p;
   return FLINT_OK;

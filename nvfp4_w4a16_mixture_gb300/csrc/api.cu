@@ -40,6 +40,7 @@ WsLayout ws_layout(const flint_moe_shape& s) {
   };
   L.status = take(16);
   L.glob_cnt = take(16);
+  L.fd_cnt = take(16);
   L.hblk_cnt = take(4 * (H / 16));
   L.tok_cnt = take(4 * ((M + kRouteTokens - 1) / kRouteTokens));
   L.logits = take(2 * M * E);
@@ -70,6 +71,7 @@ Ws ws_pointers(void* base, const WsLayout& L) {
   char* b = static_cast<char*>(base);
   Ws w;
   w.status = reinterpret_cast<int*>(b + L.status);
+  w.fd_cnt = reinterpret_cast<int*>(b + L.fd_cnt);
   w.tok_cnt = reinterpret_cast<int*>(b + L.tok_cnt);
   w.glob_cnt = reinterpret_cast<int*>(b + L.glob_cnt);
   w.hblk_cnt = reinterpret_cast<int*>(b + L.hblk_cnt);
@@ -96,6 +98,23 @@ Ws ws_pointers(void* base, const WsLayout& L) {
 }
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Streaming multiprocessors of the current device (cached per device).
+static cudaError_t device_sms(int* sms) {
+  static std::atomic<int> cache[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v <= 0) {
+    err = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    cache[dev].store(v, std::memory_order_relaxed);
+  }
+  *sms = v;
+  return cudaSuccess;
+}
 
 }  // namespace flint
 
@@ -170,6 +189,12 @@ int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13, c
 
   if (shape->M > kDecodeMaxTokens && grouped_supported(*shape)) {
     if (launch_grouped(a, st) != cudaSuccess) return FLINT_ERR_CUDA;
+    return FLINT_OK;
+  }
+  int sms = 0;
+  if (device_sms(&sms) != cudaSuccess) return FLINT_ERR_CUDA;
+  if (fused_supported(*shape, sms)) {
+    if (launch_fused(a, st, sms) != cudaSuccess) return FLINT_ERR_CUDA;
     return FLINT_OK;
   }
   if (decode2_supported(*shape)) {

@@ -22,6 +22,7 @@ constexpr int kDecodeMaxTokens = 64;  // M above this uses the grouped path
 struct WsLayout {
   size_t status;       // int32[4]: [0] first error recorded by a kernel
   size_t glob_cnt;     // int32[4]: global last-arriver counters
+  size_t fd_cnt;       // int32[4]: single-launch decode grid barriers [0], [1], CTAs done [2]
   size_t hblk_cnt;     // int32[H / 16]: down/combine last-arriver counters
   size_t tok_cnt;      // int32[ceil(M / kRouteTokens)]: router last-arriver counters
   size_t logits;       // bf16 [M, E]
@@ -63,6 +64,7 @@ WsLayout ws_layout(const flint_moe_shape& s);
 
 struct Ws {  // device pointers into one workspace
   int* status;
+  int* fd_cnt;
   int* tok_cnt;
   int* glob_cnt;
   int* hblk_cnt;
@@ -133,6 +135,13 @@ cudaError_t launch_grouped(const MoEArgs& a, cudaStream_t st);
 // decode2_supported checks).
 bool decode2_supported(const flint_moe_shape& s);
 cudaError_t launch_decode2(const MoEArgs& a, cudaStream_t st);
+
+// Single-launch decode path (decode_fused.cu): router, top-k, grouping,
+// gate/up, down and combine in one cooperative launch of `sms` CTAs, for
+// M <= kFusedMaxTokens and the limits fused_supported checks.
+constexpr int kFusedMaxTokens = 8;
+bool fused_supported(const flint_moe_shape& s, int sms);
+cudaError_t launch_fused(const MoEArgs& a, cudaStream_t st, int sms);
 
 
 

@@ -293,4 +293,7 @@ FLINT_DEV int atom_add_acqrel_cta_smem(int* p, int v) {
 // Order this thread's earlier generic-proxy global accesses (and what it has
 // observed) before its later async-proxy (bulk copy) accesses.
 FLINT_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+// Generic-proxy shared-memory accesses ordered with the async proxy's (bulk
+// copies and the tensor core read and write shared memory through it).
+FLINT_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 }  // namespace flint

@@ -89,7 +89,7 @@ enum {
   kSiteTopk = 7, kSiteSplit = 8, kSiteRdone = 9, kSiteRows = 10, kSiteAct = 11, kSiteDrain = 12,
 };
 
-enum { kKindShared = 0, kKindRouted = 1, kKindDown = 2, kKindShDown = 3, kKindEnd = -1 };
+enum { kKindShared = 0, kKindRouted = 1, kKindDown = 2 };
 
 // A record is the unit of work of one consumer warp: a shared gate/up tile
 // (sh_stages ring stages), a routed gate/up item, the shared down, or a
@@ -102,9 +102,8 @@ struct Stage {
   int kind;
   int k0, kst;      // kind 0: K offset and extent
   int tile;         // kind 0: shared tile j (intermediate rows 8j .. 8j + 7)
-  int u, r0;        // kind 1: expert slot and first intermediate row
-  int nblk;         // kind 2: routed experts (blocks) in the stage
-  int blk_u[2];
+  int u, r0;        // kind 1: expert slot and first intermediate row; kind 2: u
+  int act_in;       // kind 2: the stage's copies include the activation rows
 };
 
 struct Route {
@@ -120,7 +119,7 @@ struct Route {
 
 struct Ctl {
   uint64_t full[kMaxStages], empty[kMaxStages];
-  uint64_t rfull, sdfull;
+  uint64_t xfull, rfull, sdfull;
   uint64_t rdone, split_done, topk_done, logits_ready, routed_ready, act_ready;
   uint64_t abar[kCons];  // per consumer warp: its bulk copies of activation rows
   int abort;
@@ -128,14 +127,17 @@ struct Ctl {
   int all_done;  // records finished (+1 once the routing is known)
   int ca_target, all_target;
   int left;      // the CTA has counted itself out of the grid
+  int parts;     // warps sharing one routed gate/up item (its K split)
+  int pcnt[kMaxStages];  // parts of the slot's item finished
   Stage info[kMaxStages];
   float xp2[kMaxM][kMaxSlices];  // 2^q of token t, slice s
+  float xp2zero[kMaxSlices];     // a column that holds no token
   Route rt;
 };
 
 struct Layout {
   int stages;
-  size_t xh, xl, xpitch, rrow, sdown, ysm, yss, ctl, total;
+  size_t xr, xh, xl, xpitch, rrow, sdown, ysm, yss, ctl, total;
 };
 
 __host__ __device__ inline size_t al16(size_t v) { return (v + 15) / 16 * 16; }
@@ -148,11 +150,13 @@ __host__ __device__ inline Layout fused_layout(int M, int H, int SI) {
   const size_t sdown = al16((size_t)16 * (SI > 0 ? SI : 0) * 2);
   const size_t ysm = (size_t)kMaxPairs * 16 * 2;
   const size_t yss = al16((size_t)kMaxM * 16 * 2);
-  const size_t fixed = 2 * xsplit + rrow + sdown + ysm + yss + al16(sizeof(Ctl));
+  const size_t xraw = al16((size_t)M * H * 2);
+  const size_t fixed = xraw + 2 * xsplit + rrow + sdown + ysm + yss + al16(sizeof(Ctl));
   const size_t room = fixed < (size_t)kMaxSmem ? kMaxSmem - fixed : 0;
   L.stages = (int)(room / kStageBytes);
   if (L.stages > kMaxStages) L.stages = kMaxStages;
-  L.xh = (size_t)L.stages * kStageBytes;
+  L.xr = (size_t)L.stages * kStageBytes;
+  L.xh = L.xr + xraw;
   L.xl = L.xh + xsplit;
   L.rrow = L.xl + xsplit;
   L.sdown = L.rrow + rrow;
@@ -164,7 +168,7 @@ __host__ __device__ inline Layout fused_layout(int M, int H, int SI) {
 }
 
 // --------------------------------------------------------------- waits --
-FLINT_DEV void record_timeout(int* status, int site, int n) {
+__device__ __noinline__ void record_timeout(int* status, int site, int n) {
   if (atomicCAS(status, 0, FLINT_ERR_TIMEOUT) == 0) {
     status[1] = site;
     status[2] = (int)blockIdx.x;
@@ -172,7 +176,7 @@ FLINT_DEV void record_timeout(int* status, int site, int n) {
   }
 }
 
-FLINT_DEV bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
+__device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
                           int site, int n) {
   if (*abort) return false;
   unsigned long long t0 = 0;
@@ -189,15 +193,50 @@ FLINT_DEV bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort, i
   }
 }
 
-FLINT_DEV bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status, int lane,
+__device__ __noinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status, int lane,
                          int site, int n) {
   int ok = 0;
   if (lane == 0) ok = wait_phase(bar, parity, abort, status, site, n);
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Bounded wait for a phase that must complete whatever happened elsewhere
+// (it counts bulk copies in flight, which may not outlive the CTA): on
+// expiry it records the timeout and returns.
+__device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status, int n) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity, kSuspendNs))
+    if (globaltimer_ns() - t0 > kWaitNs) {
+      *abort = 1;
+      record_timeout(status, kSiteDrain, n);
+      return;
+    }
+}
+
+// Bounded poll until a ring slot carries stage number nn.  The stamp comes
+// at least a copy's latency before the data, so the poll backs off to 512 ns:
+// a waiting warp then costs the compute warps of its SM almost no issue slots.
+__device__ __noinline__ bool wait_stamp(const int* seq, int nn, volatile int* abort, int* status) {
+  const volatile int* sq = seq;
+  unsigned long long t0 = 0;
+  unsigned sleep_ns = 32;
+  while (*sq != nn) {
+    if (*abort) return false;
+    const unsigned long long now = globaltimer_ns();
+    if (t0 == 0) t0 = now;
+    if (now - t0 > kWaitNs) {
+      *abort = 1;
+      record_timeout(status, kSiteFull, nn);
+      return false;
+    }
+    __nanosleep(sleep_ns);
+    sleep_ns = min(2 * sleep_ns, 512u);
+  }
+  return true;
+}
+
 // Spin (bounded) until the grid counter reaches `target` (acquire, GPU scope).
-FLINT_DEV bool wait_counter(const int* p, int target, volatile int* abort, int* status, int site) {
+__device__ __noinline__ bool wait_counter(const int* p, int target, volatile int* abort, int* status, int site) {
   unsigned long long t0 = 0;
   for (;;) {
     if (ld_acquire(p) >= target) return true;
@@ -232,7 +271,7 @@ FLINT_DEV int bf16_margin(float v) {
 
 // exp(v) correctly rounded to fp32 but for a double-ulp window at the fp32
 // rounding boundaries: double-precision exp, rounded once.
-FLINT_DEV float exp_f32_rn(float v) { return (float)exp((double)v); }
+__device__ __noinline__ float exp_f32_rn(float v) { return (float)exp((double)v); }
 
 // act = bf16(silu(g) * u), silu(g) = g * (1 / (1 + exp(-g))), every step one
 // fp32 rounding.  expf is within 2 ulps of the rounded exp; that moves the
@@ -373,75 +412,116 @@ FLINT_DEV void a_frags_f16(uint32_t (&af)[4][2][4], const uint4& c0, const uint4
   }
 }
 
-// Span (in binades) of the non-zero e4m3 block scales of one row over the
-// slice: the two bytes of this thread, then the row's four threads.
-FLINT_DEV int scale_span(uint32_t two) {
-  int lo = 99, hi = -1;
+FLINT_DEV void load_col_smem(uint4 (&xb)[4], const uint8_t* p) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    xb[q] = p ? *reinterpret_cast<const uint4*>(p + 16 * q) : make_uint4(0, 0, 0, 0);
+}
+FLINT_DEV void load_col_global(uint4 (&xb)[4], const uint16_t* p) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) xb[q] = p ? ldg_cg_v4(p + 8 * q) : make_uint4(0, 0, 0, 0);
+}
+
+// Min / max exponent field of the non-zero e4m3 block scales among the two
+// bytes of `two` (subnormal scales share field 1's grid).
+FLINT_DEV void scale_fields(uint32_t two, int& lo, int& hi) {
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const uint32_t b = (two >> (8 * i)) & 0x7Fu;
     if (b) {
-      const int f = max((int)(b >> 3), 1);  // subnormal scales share field 1's grid
+      const int f = max((int)(b >> 3), 1);
       lo = min(lo, f);
       hi = max(hi, f);
     }
   }
-  lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, 1));
-  lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, 2));
-  hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, 1));
-  hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, 2));
-  return hi >= lo ? hi - lo : 0;
 }
 
-// Routed gate/up, one 128-K slice of the 16-row tile (rows g, g + 8: codes
-// rg / rg8, scales sg / sg8) against activation columns on the f16 path.
-// bh: this lane's column of X_hi (integers) or, with `combined`, X_hi for
-// columns 0..3 and x_lo for columns 4..7; bl: x_lo (not combined).  p2: 2^q
-// of the lane's two columns.  hi products go exactly into (S, C), lo ones
-// into C.
-FLINT_DEV void slice_gateup(float (&S)[4], float (&C)[4], const uint8_t* rg, const uint8_t* rg8,
-                            const uint8_t* sg, const uint8_t* sg8, int s, int t, const uint4 (&bh)[4],
-                            const uint4 (&bl)[4], bool combined, const float (&p2)[2]) {
-  const uint4 c0 = *reinterpret_cast<const uint4*>(rg + s * (kSliceK / 2) + 16 * t);
-  const uint4 c1 = *reinterpret_cast<const uint4*>(rg8 + s * (kSliceK / 2) + 16 * t);
-  const uint32_t s0b = *reinterpret_cast<const uint16_t*>(sg + s * (kSliceK / 16) + 2 * t);
-  const uint32_t s1b = *reinterpret_cast<const uint16_t*>(sg8 + s * (kSliceK / 16) + 2 * t);
-  uint32_t af[4][2][4];
-  a_frags_f16(af, c0, c1, s0b, s1b);
-  const bool wide = __any_sync(0xffffffffu, max(scale_span(s0b), scale_span(s1b)) > 4);
-  float dl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  if (!wide) {
-    // the slice's hi products: integers (<= 32 * 180) on the grid of the
-    // smallest scale, at most 128 * 5760 * 2^4 < 2^24 in total: exact chain
-    float dh[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+// Routed gate/up of one item part: a 16-row NVFP4 tile (rows g, g + 8 of
+// lane (g, t): gate row g and up row g) over the 128-K slices s_lo .. s_hi - 1,
+// against the activation columns on the f16 path.  bcol: this lane's column
+// of X_hi (integers), or, with `combined`, X_hi for columns 0..3 and x_lo for
+// columns 4..7; lcol: x_lo (not combined); p2[s][c]: 2^q of the lane's two
+// columns in slice s.  hi products go exactly into (S, C), lo ones into C.
+//
+// Exactness of the hi sums: X_hi is an integer of at most 5 bits and a
+// weight an integer of at most 8 bits on its block's grid, so a slice's 128
+// hi products are integers on the grid of its smallest block scale and sum
+// to less than 2^24 when the block scales span at most 2^4 binades (checked
+// over both rows and the part's slices): the slice's mma's then run in two
+// exact chains (words 0-1 and 2-3) whose fp32 sum is exact too, and the
+// slice total is added with one TwoSum.  With a wider span every mma (16
+// products, exact for spans up to 2^7) is added alone.
+FLINT_DEV void item_gateup(float (&S)[4], float (&C)[4], const uint8_t* st, int H, int g, int t,
+                           const uint8_t* bcol, const uint8_t* lcol, bool combined,
+                           const float* p2c0, const float* p2c1, int s_lo, int s_hi) {
+  const uint8_t* rg = st + g * (H / 2);
+  const uint8_t* rg8 = st + (g + 8) * (H / 2);
+  const uint8_t* sg = st + 16 * (H / 2) + g * (H / 16);
+  const uint8_t* sg8 = st + 16 * (H / 2) + (g + 8) * (H / 16);
+  // block-scale span of rows g and g + 8 over the part's slices
+  int lo0 = 99, hi0 = -1, lo1 = 99, hi1 = -1;
+  for (int s = s_lo; s < s_hi; ++s) {
+    scale_fields(*reinterpret_cast<const uint16_t*>(sg + s * 8 + 2 * t), lo0, hi0);
+    scale_fields(*reinterpret_cast<const uint16_t*>(sg8 + s * 8 + 2 * t), lo1, hi1);
+  }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      mmah(dh, af[q][0], bh[q].x, bh[q].z);
-      mmah(dh, af[q][1], bh[q].y, bh[q].w);
-      if (!combined) {
+  for (int o = 1; o <= 2; o <<= 1) {
+    lo0 = min(lo0, __shfl_xor_sync(0xffffffffu, lo0, o));
+    hi0 = max(hi0, __shfl_xor_sync(0xffffffffu, hi0, o));
+    lo1 = min(lo1, __shfl_xor_sync(0xffffffffu, lo1, o));
+    hi1 = max(hi1, __shfl_xor_sync(0xffffffffu, hi1, o));
+  }
+  const bool wide = __any_sync(0xffffffffu, hi0 - lo0 > 4 || hi1 - lo1 > 4);
+
+  for (int s = s_lo; s < s_hi; ++s) {
+    const uint4 c0 = *reinterpret_cast<const uint4*>(rg + s * (kSliceK / 2) + 16 * t);
+    const uint4 c1 = *reinterpret_cast<const uint4*>(rg8 + s * (kSliceK / 2) + 16 * t);
+    const uint32_t s0b = *reinterpret_cast<const uint16_t*>(sg + s * (kSliceK / 16) + 2 * t);
+    const uint32_t s1b = *reinterpret_cast<const uint16_t*>(sg8 + s * (kSliceK / 16) + 2 * t);
+    uint4 bh[4];
+    load_col_smem(bh, bcol ? bcol + 2 * (s * kSliceK + 32 * t) : nullptr);
+    const float pa = p2c0[s], pb = p2c1[s];
+    uint32_t af[4][2][4];
+    a_frags_f16(af, c0, c1, s0b, s1b);
+    if (!wide) {
+      float da[4] = {0.0f, 0.0f, 0.0f, 0.0f}, db[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        mmah(da, af[q][0], bh[q].x, bh[q].z);
+        mmah(db, af[q + 2][0], bh[q + 2].x, bh[q + 2].z);
+        mmah(da, af[q][1], bh[q].y, bh[q].w);
+        mmah(db, af[q + 2][1], bh[q + 2].y, bh[q + 2].w);
+      }
+      // (the x_lo columns of a combined item round in the mma already; their
+      // sum is about 2^-5 of the hi one, so one more rounding costs nothing)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) two_sum(S[i], C[i], __fadd_rn(da[i], db[i]) * ((i & 1) ? pb : pa));
+    } else {
+      // (rare: block scales spread over more than 2^4; kept compact)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          mmah(d, af[q][r], r ? bh[q].y : bh[q].x, r ? bh[q].w : bh[q].z);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) two_sum(S[i], C[i], d[i] * ((i & 1) ? pb : pa));
+        }
+      }
+    }
+    if (!combined) {
+      uint4 bl[4];
+      load_col_smem(bl, lcol ? lcol + 2 * (s * kSliceK + 32 * t) : nullptr);
+      float dl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
         mmah(dl, af[q][0], bl[q].x, bl[q].z);
         mmah(dl, af[q][1], bl[q].y, bl[q].w);
       }
-    }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) two_sum(S[i], C[i], dh[i] * p2[i & 1]);
-  } else {
-    // block scales spread wider: every mma alone (16 products) is exact
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        mmah(d, af[q][r], r ? bh[q].y : bh[q].x, r ? bh[q].w : bh[q].z);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) two_sum(S[i], C[i], d[i] * p2[i & 1]);
-        if (!combined) mmah(dl, af[q][r], r ? bl[q].y : bl[q].x, r ? bl[q].w : bl[q].z);
-      }
+      for (int i = 0; i < 4; ++i) C[i] = __fadd_rn(C[i], dl[i] * ((i & 1) ? pb : pa));
     }
   }
-  if (!combined)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) C[i] = __fadd_rn(C[i], dl[i] * p2[i & 1]);
 }
 
 // One 128-K slice of a 16-row BF16 tile (rows g, g + 8 in natural order at
@@ -501,16 +581,19 @@ FLINT_DEV void slice_down_fp4(float (&S)[4], float (&C)[4], const uint8_t* rg, c
   d.s1 = *reinterpret_cast<const uint16_t*>(sg8 + s * (kSliceK / 16) + 2 * t);
   uint32_t af[4][2][4];
   a_frags(d, af);
-  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 4; ++q) {  // words 0-1 and 2-3 in two chains
     uint32_t b[2][2];
     b_regs(xb[q], b);
-    mma16(acc, af[q][0], b[0][0], b[0][1]);
-    mma16(acc, af[q][1], b[1][0], b[1][1]);
+    mma16(acc[q >> 1], af[q][0], b[0][0], b[0][1]);
+    mma16(acc[q >> 1], af[q][1], b[1][0], b[1][1]);
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) two_sum(S[i], C[i], acc[i]);
+  for (int i = 0; i < 4; ++i) {
+    two_sum(S[i], C[i], acc[0][i]);
+    two_sum(S[i], C[i], acc[1][i]);
+  }
 }
 
 // The same for a BF16 down block in natural row order (shared expert).
@@ -529,16 +612,6 @@ FLINT_DEV void slice_down_bf16(float (&S)[4], float (&C)[4], const uint16_t* ra,
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) two_sum(S[i], C[i], acc[i]);
-}
-
-FLINT_DEV void load_col_smem(uint4 (&xb)[4], const uint8_t* p) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    xb[q] = p ? *reinterpret_cast<const uint4*>(p + 16 * q) : make_uint4(0, 0, 0, 0);
-}
-FLINT_DEV void load_col_global(uint4 (&xb)[4], const uint16_t* p) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) xb[q] = p ? ldg_cg_v4(p + 8 * q) : make_uint4(0, 0, 0, 0);
 }
 
 // ---------------------------------------------------------- top-k warp --
@@ -578,7 +651,7 @@ FLINT_DEV void topk_token(Get get, int E, int k, int lane, int& out_e, float& ou
       const float e = pass == 0 ? expf(-logit) : exp_f32_rn(-logit);
       s = __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
     }
-    float sum = 0.0f;
+    float sum = 0.0f;  // in rank order
     for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, s, j));
     const float q = __fdiv_rn(s, __fadd_rn(sum, 1e-20f));
     w = round_bf16(q);
@@ -595,31 +668,29 @@ struct Items {
   int lo, hi;
 };
 
-// The routed gate/up items (T = U * I / 8) are split over the CTAs in
-// proportion to their remaining byte budget: CTAs that also own output rows
-// (c < n_dn) carry U routed down blocks and take fewer items.
-FLINT_DEV Items item_range(int c, int G, int U, int H, int I) {
-  const long long T = (long long)U * (I / 8);
-  const long long A = 16LL * (H / 2 + H / 16);  // bytes per item
-  const long long D = (long long)U * 16 * (I / 2 + I / 16);
-  const int n_dn = min(H / 16, G);
-  const long long tot = T * A + (long long)n_dn * D;
-  const long long cap_dn = max(0LL, tot - (long long)G * D);  // x G
-  const long long cap_other = tot;                            // x G
-  auto prefix = [&](int cc) {
-    const int d = min(cc, n_dn);
-    return (long long)d * cap_dn + (long long)(cc - d) * cap_other;
-  };
-  const long long PG = prefix(G);
+// The routed gate/up items (T = U * I / 8) are split evenly over the CTAs:
+// the down work comes after the grid barrier that ends the gate/up phase, so
+// each phase is balanced on its own.
+FLINT_DEV Items item_range(int c, int G, int U, int I) {
+  const int T = U * (I / 8);  // T * G < 2^31 (U <= 256, I <= 2048, G <= 1024)
   Items r;
-  if (PG <= 0) {
-    r.lo = (int)(T * c / G);
-    r.hi = (int)(T * (c + 1) / G);
-  } else {
-    r.lo = (int)(T * prefix(c) / PG);
-    r.hi = (int)(T * prefix(c + 1) / PG);
-  }
+  r.lo = T * c / G;
+  r.hi = T * (c + 1) / G;
   return r;
+}
+
+// Parts per item for a CTA with ni items: the number (1 .. 4, at most the
+// slice count, within the stage's spare room) that minimises the slices the
+// busiest warp sums when the ni * Q part records go round-robin over the
+// consumer warps; fewer parts on ties.
+FLINT_DEV int item_parts(int ni, int nsl, int room, bool wide_cols) {
+  int best = 1, best_cost = 0x7fffffff;
+  for (int q = 1; q <= 4 && q <= nsl; ++q) {
+    if (q > 1 && q * (wide_cols ? 1024 : 512) > room) break;
+    const int cost = (ni * q + kCons - 1) / kCons * ((nsl + q - 1) / q);
+    if (cost < best_cost) { best_cost = cost; best = q; }
+  }
+  return best;
 }
 
 // ======================================================================
@@ -630,16 +701,13 @@ struct RecPlan {
   int n_sh, n_items, n_shd, n_dn, total;
 };
 
-// Routed down blocks of stage d: experts [ub, ub + nb), packed greedily so
-// that their weight blocks and activation rows fit a stage (at most two).
-FLINT_DEV int down_block_bytes(int I, int cnt) { return 16 * (I / 2) + I + cnt * (2 * I + 16); }
-
 __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int M = a.M, H = a.H, E = a.E, k = a.k, I = a.I, SI = a.SI;
   const Layout L = fused_layout(M, H, SI);
   const int S = L.stages;
   uint8_t* ring = smem;
+  const uint16_t* xr = reinterpret_cast<const uint16_t*>(smem + L.xr);  // bf16 x [token][H]
   uint8_t* xh = smem + L.xh;  // f16 X_hi [token][H]
   uint8_t* xl = smem + L.xl;  // f16 x_lo [token][H]
   const int xpitch = (int)L.xpitch;
@@ -668,12 +736,15 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
   for (int e = c; e < E; e += G) ++my_rrows;
 
   for (int i = threadIdx.x; i < kMaxE; i += kThreads) RT.emask[i] = 0u;
+  for (int i = threadIdx.x; i < kMaxSlices; i += kThreads) SM.xp2zero[i] = 0.0f;
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&SM.full[i], 1);
       mbar_init(&SM.empty[i], 1);
       SM.info[i].seq = -1;
+      SM.pcnt[i] = 0;
     }
+    mbar_init(&SM.xfull, 1);
     mbar_init(&SM.rfull, 1);
     mbar_init(&SM.sdfull, 1);
     mbar_init(&SM.rdone, kCons);
@@ -702,17 +773,23 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
   if (warp == kProd) {
     // ================================================================ producer
     bool dead = false;
+    pdl_wait();  // x belongs to the stream's earlier work
     if (lane == 0) {
-      // phase A: weights that depend on no routing
+      // phase A: the token rows, then weights that depend on no routing
+      mbar_arrive_expect_tx(&SM.xfull, (uint32_t)M * 2u * H);
+      bulk_g2s(smem + L.xr, a.x, (uint32_t)M * 2u * H, &SM.xfull);
       mbar_arrive_expect_tx(&SM.rfull, (uint32_t)my_rrows * 2u * H);
       int i = 0;
       for (int e = c; e < E; e += G, ++i)
         bulk_g2s(smem + L.rrow + (size_t)i * 2 * H, a.router_w + (size_t)e * H, 2u * H, &SM.rfull);
-      const uint32_t sb = (has_dn && SI > 0) ? 16u * (uint32_t)SI * 2u : 0u;
+      // the shared expert's weights go out once the router rows have landed,
+      // so that the routing, on the critical path, does not queue behind them
+      if (!wait_phase(&SM.rfull, 0, abort, status, kSiteRows, 0)) dead = true;
+      const uint32_t sb = (!dead && has_dn && SI > 0) ? 16u * (uint32_t)SI * 2u : 0u;
       mbar_arrive_expect_tx(&SM.sdfull, sb);
       if (sb) bulk_g2s(smem + L.sdown, a.shared_down + (size_t)h0 * SI, sb, &SM.sdfull);
     }
-    __syncwarp();
+    dead = __shfl_sync(0xffffffffu, dead, 0);
     int n = 0;
     // shared gate/up tiles: a stage is 8 gate + 8 up rows over up to 512 K
     for (int j = c; j < nSh && !dead; j += G) {
@@ -740,7 +817,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
     // barrier 1: this CTA's logits are written (consumers), then every CTA's
     if (lane == 0) {
       if (wait_phase(&SM.rdone, 0, abort, status, kSiteRdone, 0)) {
-        __threadfence();
         red_release_add(cnt + 0, 1);
         if (wait_counter(cnt + 0, G, abort, status, kSiteBar1)) mbar_arrive(&SM.logits_ready);
       } else {
@@ -777,49 +853,40 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
                    &SM.full[sl]);
         ++n;
       }
-      // phase D stages: the shared down (its weight rows are resident; the
-      // owning warp copies sact into the slot), then the routed down blocks
-      // of the output tile (weights here, activation rows by the owning warp)
+      // phase D stages: the routed down blocks of the output tile (the shared
+      // down needs none: its weight rows are resident since phase A)
       if (has_dn && !dead) {
-        if (SI > 0) {
-          int ok = 1;
-          if (lane == 0) ok = acquire_slot(n);
-          if (!__shfl_sync(0xffffffffu, ok, 0)) dead = true;
-          if (!dead) {
-            if (lane == 0) {
-              SM.info[n % S].kind = kKindShDown;
-              SM.info[n % S].seq = n;
-              mbar_arrive(&SM.full[n % S]);
-            }
-            ++n;
-          }
-        }
+        // one routed expert per stage; once the activation rows are
+        // complete (barrier 2 passed) their copies join the stage's weights
         const int wb = 16 * (I / 2) + I;  // weight bytes of a block
-        for (int ub = 0; ub < U && !dead;) {
-          int nb = 1;
-          if (ub + 1 < U && down_block_bytes(I, RT.cnt[ub]) + down_block_bytes(I, RT.cnt[ub + 1]) <= kStageBytes)
-            nb = 2;
+        for (int ub = 0; ub < U && !dead; ++ub) {
           int ok = 1;
           if (lane == 0) ok = acquire_slot(n);
           if (!__shfl_sync(0xffffffffu, ok, 0)) { dead = true; break; }
           const int sl = n % S;
           Stage& inf = SM.info[sl];
           uint8_t* st = ring + (size_t)sl * kStageBytes;
+          int act_in = 0;
+          if (lane == 0) act_in = mbar_test_wait(&SM.act_ready, 0) ? 1 : 0;
+          act_in = __shfl_sync(0xffffffffu, act_in, 0);
+          const int cn = RT.cnt[ub];
           if (lane == 0) {
-            inf.kind = kKindDown; inf.nblk = nb; inf.blk_u[0] = ub; inf.blk_u[1] = ub + 1;
+            inf.kind = kKindDown; inf.u = ub; inf.act_in = act_in;
             inf.seq = n;
-            mbar_arrive_expect_tx(&SM.full[sl], (uint32_t)(nb * wb));
+            mbar_arrive_expect_tx(&SM.full[sl], (uint32_t)(wb + (act_in ? cn * 2 * I : 0)));
           }
           __syncwarp();
-          for (int b = 0; b < nb; ++b) {
-            const size_t row0 = (size_t)RT.e[ub + b] * H + h0;
-            if (lane == 2 * b)
-              bulk_g2s(st + b * wb, a.w2 + row0 * (I / 2), 16u * (I / 2), &SM.full[sl]);
-            if (lane == 2 * b + 1)
-              bulk_g2s(st + b * wb + 16 * (I / 2), a.w2_sf + row0 * (I / 16), 16u * (I / 16),
+          const size_t row0 = (size_t)RT.e[ub] * H + h0;
+          if (lane == 0) bulk_g2s(st, a.w2 + row0 * (I / 2), 16u * (I / 2), &SM.full[sl]);
+          if (lane == 1) bulk_g2s(st + 16 * (I / 2), a.w2_sf + row0 * (I / 16), 16u * (I / 16), &SM.full[sl]);
+          if (act_in) {
+            // the rows were written by other CTAs before barrier 2 (generic
+            // proxy); the proxy fence orders them before these copies
+            fence_proxy_async_global();
+            for (int r = lane; r < cn; r += 32)
+              bulk_g2s(st + wb + (size_t)r * (2 * I + 16), a.ws.act + (size_t)(RT.off[ub] + r) * I, 2u * I,
                        &SM.full[sl]);
           }
-          ub += nb;
           ++n;
         }
       }
@@ -827,17 +894,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
     if (lane == 0) {
       // no bulk copy may outlive the CTA: wait (bounded) for the stages that
       // may still be in flight and for the phase-A copies
-      for (int i = (n - S > 0 ? n - S : 0); i < n; ++i) {
-        const unsigned long long t0 = globaltimer_ns();
-        while (!mbar_try_wait(&SM.full[i % S], (i / S) & 1, kSuspendNs))
-          if (globaltimer_ns() - t0 > kWaitNs) { *abort = 1; record_timeout(status, kSiteDrain, i); break; }
-      }
-      uint64_t* once[2] = {&SM.rfull, &SM.sdfull};
-      for (int i = 0; i < 2; ++i) {
-        const unsigned long long t0 = globaltimer_ns();
-        while (!mbar_try_wait(once[i], 0, kSuspendNs))
-          if (globaltimer_ns() - t0 > kWaitNs) { *abort = 1; record_timeout(status, kSiteDrain, -1 - i); break; }
-      }
+      for (int i = (n - S > 0 ? n - S : 0); i < n; ++i)
+        drain_wait(&SM.full[i % S], (i / S) & 1, abort, status, i);
+      drain_wait(&SM.xfull, 0, abort, status, -1);
+      drain_wait(&SM.rfull, 0, abort, status, -2);
+      drain_wait(&SM.sdfull, 0, abort, status, -3);
     }
     return;
   }
@@ -849,17 +910,22 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
   // ---- phase A.1: router logits of this CTA's experts, task = (row, token);
   // lane l sums the products of h = 256 c + 8 l + i ascending in (c, i) with
   // fmaf (exact products), then the xor butterfly 16 .. 1
-  pdl_wait();  // x and the workspace belong to the stream's earlier work
-  if (my_rrows * M > warp) ok = warp_wait(&SM.rfull, 0, abort, status, lane, kSiteRows, 0);
+  pdl_wait();  // the workspace belongs to the stream's earlier work
+  ok = warp_wait(&SM.xfull, 0, abort, status, lane, kSiteRows, 0);
+  if (ok && my_rrows * M > warp) ok = warp_wait(&SM.rfull, 0, abort, status, lane, kSiteRows, 0);
   for (int task = warp; ok && task < my_rrows * M; task += kCons) {
     const int i = task / M, tt = task % M, e = c + i * G;
     const uint16_t* wr = rrow + (size_t)i * H;
-    const uint16_t* xr = a.x + (size_t)tt * H;
+    const uint16_t* xt = xr + (size_t)tt * H;
     float acc = 0.0f;
-    for (int h = 8 * lane; h < H; h += 256) {
-      const uint4 xv = ldg_nc_v4(xr + h);
+#pragma unroll
+    for (int cch = 0; cch < 8; ++cch) {
+      const int h = 256 * cch + 8 * lane;
+      if (h >= H) break;
+      const uint4 xv = *reinterpret_cast<const uint4*>(xt + h);
       const uint4 wv = *reinterpret_cast<const uint4*>(wr + h);
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         acc = fmaf(__uint_as_float(xw[q] << 16), __uint_as_float(ww[q] << 16), acc);
@@ -870,16 +936,17 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
     for (int o = 16; o >= 1; o >>= 1) acc = acc + __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) a.ws.logits[(size_t)tt * E + e] = (uint16_t)f32_to_bf16_bits(acc);
   }
-  __threadfence();
   __syncwarp();
-  if (lane == 0) mbar_arrive(&SM.rdone);  // the producer releases barrier 1
+  // the arrive (release, CTA scope) orders the logit stores before the
+  // producer's GPU-scope release of barrier 1
+  if (lane == 0) mbar_arrive(&SM.rdone);
 
   // ---- phase A.2: the routed gate/up operands, task = (token, slice):
   // q = (largest exponent of the slice) - 4, X_hi = round(x 2^-q) (|X_hi| <=
   // 32), x_lo = x 2^-q - X_hi, both f16 in natural K order
-  for (int task = warp; task < M * nsl_h; task += kCons) {
+  for (int task = warp; ok && task < M * nsl_h; task += kCons) {
     const int tt = task / nsl_h, s = task % nsl_h;
-    const uint2 raw = *reinterpret_cast<const uint2*>(a.x + (size_t)tt * H + s * kSliceK + 4 * lane);
+    const uint2 raw = *reinterpret_cast<const uint2*>(xr + (size_t)tt * H + s * kSliceK + 4 * lane);
     const uint32_t w2[2] = {raw.x, raw.y};
     int ef = 0;
 #pragma unroll
@@ -931,39 +998,51 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
   if (warp == 0 && ok) ok = warp_wait(&SM.topk_done, 0, abort, status, lane, kSiteTopk, 0);
   if (warp == 0 && ok) {
     // experts in ascending order get consecutive slots u and sorted pair
-    // positions; the pairs of one expert in ascending token order
-    int run_u = 0, run_off = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      const unsigned mask = e < E ? RT.emask[e] : 0u;
-      const int ce = __popc(mask), ue = ce > 0 ? 1 : 0;
-      int ic = ce, iu = ue;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int vc = __shfl_up_sync(0xffffffffu, ic, o);
-        const int vu = __shfl_up_sync(0xffffffffu, iu, o);
-        if (lane >= o) { ic += vc; iu += vu; }
-      }
-      const int off = run_off + ic - ce, u = run_u + iu - ue;
-      if (ce > 0) {
-        RT.e[u] = e;
-        RT.cnt[u] = ce;
-        RT.off[u] = off;
-        int i = 0;
-        for (unsigned m = mask; m; m &= m - 1, ++i) {
-          const int tt = __ffs(m) - 1;
-          RT.tok[u][i] = (unsigned char)tt;
-          RT.pos[tt][RT.jslot[tt][e]] = off + i;
-        }
-      }
-      run_off += __shfl_sync(0xffffffffu, ic, 31);
-      run_u += __shfl_sync(0xffffffffu, iu, 31);
+    // positions; the pairs of one expert in ascending token order.  Lane l
+    // takes experts l * per .. l * per + per - 1; one packed scan gives every
+    // lane its first pair position (high half) and slot (low half).
+    const int per = (E + 31) / 32;
+    int tot = 0;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      const int ce = e < E ? __popc(RT.emask[e]) : 0;
+      tot += (ce << 16) | (ce > 0 ? 1 : 0);
     }
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int off = (incl - tot) >> 16, u = (incl - tot) & 0xFFFF;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      const unsigned mask = e < E ? RT.emask[e] : 0u;
+      if (mask) {
+        const int base = off;
+        RT.e[u] = e;
+        RT.cnt[u] = __popc(mask);
+        RT.off[u] = base;
+        for (unsigned m = mask; m; m &= m - 1, ++off) {
+          const int tt = __ffs(m) - 1;
+          RT.tok[u][off - base] = (unsigned char)tt;
+          RT.pos[tt][RT.jslot[tt][e]] = off;
+        }
+        ++u;
+      }
+    }
+    const int run_u = __shfl_sync(0xffffffffu, incl & 0xFFFF, 31);
     if (lane == 0) {
       RT.U = run_u;
-      const Items r = item_range(c, G, run_u, H, I);
+      const Items r = item_range(c, G, run_u, I);
       RT.item_lo = r.lo;
       RT.item_hi = r.hi;
+      // few items per CTA: split each one's K over up to 4 warps; a part's
+      // (sum, compensation) pairs take 512 bytes of the stage's spare room
+      // (1 KB when the item has more than 4 tokens)
+      bool wide_cols = false;
+      for (int it = r.lo; it < r.hi; ++it) wide_cols |= RT.cnt[it / (I / 8)] > 4;
+      SM.parts = item_parts(r.hi - r.lo, nsl_h, kStageBytes - 16 * (H / 2 + H / 16), wide_cols);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&SM.routed_ready);
@@ -978,7 +1057,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
     __syncwarp();
     int last_ca = 0, last_all = 0;
     if (lane == 0) {
-      __threadfence();
+      // the acq_rel shared-memory atomics order this warp's act / sact / y
+      // writes (made visible to lane 0 by the __syncwarp above) before the
+      // last finisher's GPU-scope release of barrier 2; no GPU-scope fence is
+      // needed here (one would wait for the SM's bulk copies in flight)
       volatile int* tg = &SM.ca_target;
       if (ca) {
         const int old = atom_add_acqrel_cta_smem(&SM.ca_done, 1);
@@ -1005,6 +1087,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
       for (int cc = 0; cc < 2; ++cc) {
         const int row = 2 * rp + cc;
         float R = 0.0f;
+#pragma unroll 1
         for (int j = 0; j < k; ++j)
           R = __fadd_rn(R, __fmul_rn(RT.tw[tt][j], bf16_bits_to_f32(ysm[RT.pos[tt][j] * 16 + row])));
         const float ysv = SI > 0 ? bf16_bits_to_f32(yss[tt * 16 + row]) : 0.0f;
@@ -1031,22 +1114,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
   // stage number: from then on the barrier's open phase is this stage's.
   auto wait_full = [&](int nn) -> bool {
     int ok2 = 1;
-    if (lane == 0) {
-      const volatile int* sq = &SM.info[nn % S].seq;
-      unsigned long long t0 = 0;
-      while (*sq != nn) {
-        if (*abort) { ok2 = 0; break; }
-        const unsigned long long now = globaltimer_ns();
-        if (t0 == 0) t0 = now;
-        if (now - t0 > kWaitNs) {
-          *abort = 1;
-          record_timeout(status, kSiteFull, nn);
-          ok2 = 0;
-          break;
-        }
-        __nanosleep(20);
-      }
-    }
+    if (lane == 0) ok2 = wait_stamp(&SM.info[nn % S].seq, nn, abort, status);
     if (!__shfl_sync(0xffffffffu, ok2, 0)) return false;
     return warp_wait(&SM.full[nn % S], (nn / S) & 1, abort, status, lane, kSiteFull, nn);
   };
@@ -1059,10 +1127,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
   // barrier, and wait for them.  The rows were written by other CTAs before
   // barrier 2 (generic proxy); the proxy fence orders them before the copies.
   auto copy_rows = [&](uint8_t* dst, const uint16_t* src, int rows, int len) -> bool {
-    if (lane == 0) {
-      fence_proxy_async_global();
-      mbar_arrive_expect_tx(&SM.abar[warp], (uint32_t)rows * 2u * len);
-    }
+    fence_proxy_async_global();
+    if (lane == 0) mbar_arrive_expect_tx(&SM.abar[warp], (uint32_t)rows * 2u * len);
     __syncwarp();
     for (int r = lane; r < rows; r += 32)
       bulk_g2s(dst + (size_t)r * (2 * len + 16), src + (size_t)r * len, 2u * len, &SM.abar[warp]);
@@ -1072,22 +1138,22 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
   };
 
   const int sh_stage_total = my_sh_tiles * sh_stages;
-  int n_items = 0, n_shd = 0, n_dn = 0, total = my_sh_tiles;
+  int n_items = 0, n_shd = 0, n_dn = 0, total = sh_stage_total, Q = 1;
   bool routed = false, act_ok = false;
+  bool closing = false;  // this warp finished the CTA's last record
   for (int r = kCons - 1 - warp; ok; r += kCons) {
-    if (r >= my_sh_tiles && !routed) {
+    if (r >= sh_stage_total && !routed) {
       // the routing (and the operand split) are needed from here on
       ok = warp_wait(&SM.routed_ready, 0, abort, status, lane, kSiteRouted, 0) &&
            warp_wait(&SM.split_done, 0, abort, status, lane, kSiteSplit, 0);
       if (!ok) break;
       routed = true;
       n_items = RT.item_hi - RT.item_lo;
+      Q = SM.parts;
       n_shd = (has_dn && SI > 0) ? 1 : 0;
       n_dn = 0;
-      if (has_dn)
-        for (int ub = 0; ub < RT.U; ++n_dn)
-          ub += (ub + 1 < RT.U && down_block_bytes(I, RT.cnt[ub]) + down_block_bytes(I, RT.cnt[ub + 1]) <= kStageBytes) ? 2 : 1;
-      total = my_sh_tiles + n_items + n_shd + n_dn;
+      if (has_dn) n_dn = RT.U;  // one routed expert per down stage
+      total = sh_stage_total + n_items * Q + n_shd + n_dn;
       if (warp == 0 && lane == 0) {
         SM.ca_target = my_sh_tiles + n_items + 1;
         SM.all_target = total + 1;
@@ -1095,30 +1161,68 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
       if (warp == 0) {  // the routing is known: count it once on both counters
         const int2 fl = finish(true);
         if (fl.x && lane == 0) open_down();
-        if (fl.y) { final_rows(); leave(); }
+        if (fl.y) { closing = true; break; }
       }
     }
     if (routed && r >= total) break;
-    if (r < my_sh_tiles) {
-      // ---- shared gate/up tile: its sh_stages stages, 4 slices each
+    if (r < sh_stage_total) {
+      // ---- shared gate/up stage: 8 gate + 8 up rows over up to 512 K.  The
+      // sh_stages stages of a tile are records of their own; their pairs
+      // meet in the stages' spare bytes and the last one to finish adds them
+      // up in K order, releases the tile's stages and writes sact
+      const int n = r, part = r % sh_stages, n0 = r - part;
+      if (!wait_full(n)) { ok = false; break; }
+      const Stage& inf = SM.info[n % S];
+      uint8_t* st = ring + (size_t)(n % S) * kStageBytes;
+      const int tile = inf.tile;
       float S_[4] = {0.0f, 0.0f, 0.0f, 0.0f}, C_[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      int tile = 0;
-      for (int si = 0; ok && si < sh_stages; ++si) {
-        const int n = r * sh_stages + si;
-        if (!wait_full(n)) { ok = false; break; }
-        const Stage& inf = SM.info[n % S];
-        const uint8_t* st = ring + (size_t)(n % S) * kStageBytes;
-        tile = inf.tile;
-        for (int s = 0; s < inf.kst / kSliceK; ++s) {
-          uint4 xb[4];
-          load_col_global(xb, g < M ? a.x + (size_t)g * H + inf.k0 + s * kSliceK + 32 * t : nullptr);
-          const uint16_t* ra = reinterpret_cast<const uint16_t*>(st + g * kShPitch) + s * kSliceK + 32 * t;
-          const uint16_t* rb = reinterpret_cast<const uint16_t*>(st + (g + 8) * kShPitch) + s * kSliceK + 32 * t;
-          slice_bf16_exact(S_, C_, ra, rb, xb);
+      for (int s = 0; s < inf.kst / kSliceK; ++s) {
+        uint4 xb[4];
+        load_col_smem(xb, g < M ? reinterpret_cast<const uint8_t*>(xr + (size_t)g * H + inf.k0 + s * kSliceK + 32 * t)
+                                : nullptr);
+        const uint16_t* ra = reinterpret_cast<const uint16_t*>(st + g * kShPitch) + s * kSliceK + 32 * t;
+        const uint16_t* rb = reinterpret_cast<const uint16_t*>(st + (g + 8) * kShPitch) + s * kSliceK + 32 * t;
+        slice_bf16_exact(S_, C_, ra, rb, xb);
+      }
+      if (sh_stages > 1) {
+        float* area = reinterpret_cast<float*>(st + 16 * kShPitch);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          area[i * 32 + lane] = S_[i];
+          area[(4 + i) * 32 + lane] = C_[i];
         }
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          last = atom_add_acqrel_cta_smem(&SM.pcnt[n0 % S], 1) == sh_stages - 1;
+          if (last) SM.pcnt[n0 % S] = 0;
+        }
+        if (!__shfl_sync(0xffffffffu, last, 0)) {
+          const int2 fl = finish(false);
+          if (fl.y) { closing = true; break; }
+          continue;
+        }
+        __syncwarp();  // lane 0's acquire covers every lane's reads below
+        for (int pp = 0; pp < sh_stages; ++pp) {
+          const float* ar =
+              reinterpret_cast<const float*>(ring + (size_t)((n0 + pp) % S) * kStageBytes + 16 * kShPitch);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (pp == 0) {
+              S_[i] = ar[i * 32 + lane];
+              C_[i] = ar[(4 + i) * 32 + lane];
+            } else {
+              two_sum(S_[i], C_[i], ar[i * 32 + lane]);
+              C_[i] = __fadd_rn(C_[i], ar[(4 + i) * 32 + lane]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0)
+          for (int pp = 0; pp < sh_stages; ++pp) mbar_arrive(&SM.empty[(n0 + pp) % S]);
+      } else {
         release(n);
       }
-      if (!ok) break;
       const int row = 8 * tile + g;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -1131,17 +1235,54 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
       }
       const int2 fl = finish(true);
       if (fl.x && lane == 0) open_down();
-      if (fl.y) { final_rows(); leave(); }
+      if (fl.y) { closing = true; break; }
       continue;
     }
-    const int n = sh_stage_total + (r - my_sh_tiles);
+    // item records: Q parts of one stage each; the shared down (no stage);
+    // then one record per routed down stage
+    const int rr = r - sh_stage_total;
+    if (n_shd && rr == n_items * Q) {
+      // ---- shared down: rows h0 .. h0 + 15 (resident) against sact, copied
+      // into the split activations' room (every item of the CTA is done)
+      if (!act_ok) {
+        if (!warp_wait(&SM.act_ready, 0, abort, status, lane, FLINT_FAULT_DOWN_HANDOVER, r)) {
+          ok = false;
+          break;
+        }
+        act_ok = true;
+      }
+      // (the room was last read through the generic proxy: fence it before
+      // the bulk copies write it)
+      fence_proxy_async_smem();
+      if (!warp_wait(&SM.sdfull, 0, abort, status, lane, kSiteRows, r) ||
+          !copy_rows(xh, a.ws.sact, M, SI)) { ok = false; break; }
+      float S_[4] = {0.0f, 0.0f, 0.0f, 0.0f}, C_[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int s = 0; s < SI / kSliceK; ++s) {
+        uint4 xb[4];
+        load_col_smem(xb, g < M ? xh + (size_t)g * (2 * SI + 16) + 2 * (s * kSliceK + 32 * t) : nullptr);
+        slice_down_bf16(S_, C_, sdown + (size_t)g * SI + s * kSliceK + 32 * t,
+                        sdown + (size_t)(g + 8) * SI + s * kSliceK + 32 * t, xb);
+      }
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int tt = 2 * t + cc;
+        if (tt < M) {
+          yss[tt * 16 + g] = (uint16_t)f32_to_bf16_bits(__fadd_rn(S_[cc], C_[cc]));
+          yss[tt * 16 + g + 8] = (uint16_t)f32_to_bf16_bits(__fadd_rn(S_[2 + cc], C_[2 + cc]));
+        }
+      }
+      const int2 fl = finish(false);
+      if (fl.y) { closing = true; break; }
+      continue;
+    }
+    const int n = sh_stage_total + (rr < n_items * Q ? rr / Q : rr - n_items * (Q - 1) - n_shd);
     if (!wait_full(n)) { ok = false; break; }
     const Stage& inf = SM.info[n % S];
     uint8_t* st = ring + (size_t)(n % S) * kStageBytes;
     const int kind = inf.kind;
     if (kind == kKindRouted) {
-      // ---- routed gate/up item: 16 rows (8 gate, 8 up) over all of K
-      const int u = inf.u, r0 = inf.r0, cn = RT.cnt[u];
+      // ---- routed gate/up item part: 16 rows (8 gate, 8 up) over 1 / Q of K
+      const int u = inf.u, r0 = inf.r0, cn = RT.cnt[u], part = rr % Q;
       const bool combined = cn <= 4;
       // B column g: X_hi of token g, or (combined) X_hi of token g for g < 4
       // and x_lo of token g - 4 for g >= 4
@@ -1156,17 +1297,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
         ctok[cc] = c2 < cn ? RT.tok[u][c2] : -1;
       }
       float S_[4] = {0.0f, 0.0f, 0.0f, 0.0f}, C_[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      const uint8_t* sc = st + 16 * (H / 2);
-      for (int s = 0; s < nsl_h; ++s) {
-        uint4 bh[4], bl[4];
-        load_col_smem(bh, bcol ? bcol + 2 * (s * kSliceK + 32 * t) : nullptr);
-        if (!combined) load_col_smem(bl, lcol ? lcol + 2 * (s * kSliceK + 32 * t) : nullptr);
-        const float p2[2] = {ctok[0] >= 0 ? SM.xp2[ctok[0]][s] : 0.0f,
-                             ctok[1] >= 0 ? SM.xp2[ctok[1]][s] : 0.0f};
-        slice_gateup(S_, C_, st + g * (H / 2), st + (g + 8) * (H / 2), sc + g * (H / 16),
-                     sc + (g + 8) * (H / 16), s, t, bh, bl, combined, p2);
-      }
-      release(n);
+      const float* p2a = ctok[0] >= 0 ? SM.xp2[ctok[0]] : SM.xp2zero;
+      const float* p2b = ctok[1] >= 0 ? SM.xp2[ctok[1]] : SM.xp2zero;
+      item_gateup(S_, C_, st, H, g, t, bcol, lcol, combined, p2a, p2b, part * nsl_h / Q,
+                  (part + 1) * nsl_h / Q);
       if (combined) {
         // lanes t = 2, 3 hold the x_lo columns of lanes t - 2's tokens
 #pragma unroll
@@ -1175,6 +1309,49 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
           C_[i] = __fadd_rn(C_[i], lo);
         }
       }
+      if (Q > 1) {
+        // every part leaves its pairs in the stage's spare bytes; the last
+        // one to finish adds them up in part order (the same result whichever
+        // part comes last) and finishes the item
+        float* area = reinterpret_cast<float*>(st + 16 * (H / 2 + H / 16));
+        const int per = combined ? 16 : 32;
+        const bool keep = !combined || t < 2;
+        const int li = combined ? 2 * g + t : lane;
+        if (keep) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            area[(part * 8 + i) * per + li] = S_[i];
+            area[(part * 8 + 4 + i) * per + li] = C_[i];
+          }
+        }
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          last = atom_add_acqrel_cta_smem(&SM.pcnt[n % S], 1) == Q - 1;
+          if (last) SM.pcnt[n % S] = 0;
+        }
+        if (!__shfl_sync(0xffffffffu, last, 0)) {
+          const int2 fl = finish(false);
+          if (fl.y) { closing = true; break; }
+          continue;
+        }
+        __syncwarp();  // lane 0's acquire covers every lane's reads below
+        if (keep) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            S_[i] = area[i * per + li];
+            C_[i] = area[(4 + i) * per + li];
+          }
+          for (int pp = 1; pp < Q; ++pp) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              two_sum(S_[i], C_[i], area[(pp * 8 + i) * per + li]);
+              C_[i] = __fadd_rn(C_[i], area[(pp * 8 + 4 + i) * per + li]);
+            }
+          }
+        }
+      }
+      release(n);
       const float gsc = a.w13_gs[RT.e[u]];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -1187,72 +1364,51 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a
       }
       const int2 fl = finish(true);
       if (fl.x && lane == 0) open_down();
-      if (fl.y) { final_rows(); leave(); }
+      if (fl.y) { closing = true; break; }
       continue;
     }
     // down records: every CTA's act and sact are in the workspace
-    if (!act_ok) {
+    if (!act_ok && !(kind == kKindDown && inf.act_in)) {
       if (!warp_wait(&SM.act_ready, 0, abort, status, lane, FLINT_FAULT_DOWN_HANDOVER, n)) {
         ok = false;
         break;
       }
       act_ok = true;
     }
-    if (kind == kKindShDown) {
-      // ---- shared down: rows h0 .. h0 + 15 (resident) against sact (copied here)
-      if (!warp_wait(&SM.sdfull, 0, abort, status, lane, kSiteRows, n) ||
-          !copy_rows(st, a.ws.sact, M, SI)) { ok = false; break; }
+    {
+      // ---- routed down stage: rows h0 .. h0 + 15 of one expert
+      const int u = inf.u, cn = RT.cnt[u], wb = 16 * (I / 2) + I;
+      uint8_t* arow = st + wb;
+      if (!inf.act_in && !copy_rows(arow, a.ws.act + (size_t)RT.off[u] * I, cn, I)) { ok = false; break; }
+      const uint8_t* sc = st + 16 * (I / 2);
       float S_[4] = {0.0f, 0.0f, 0.0f, 0.0f}, C_[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      for (int s = 0; s < SI / kSliceK; ++s) {
+      for (int s = 0; s < I / kSliceK; ++s) {
         uint4 xb[4];
-        load_col_smem(xb, g < M ? st + (size_t)g * (2 * SI + 16) + 2 * (s * kSliceK + 32 * t) : nullptr);
-        slice_down_bf16(S_, C_, sdown + (size_t)g * SI + s * kSliceK + 32 * t,
-                        sdown + (size_t)(g + 8) * SI + s * kSliceK + 32 * t, xb);
+        load_col_smem(xb, g < cn ? arow + (size_t)g * (2 * I + 16) + 2 * (s * kSliceK + 32 * t) : nullptr);
+        slice_down_fp4(S_, C_, st + g * (I / 2), st + (g + 8) * (I / 2), sc + g * (I / 16),
+                       sc + (g + 8) * (I / 16), s, t, xb);
       }
-      release(n);
+      const float gs2 = a.w2_gs[RT.e[u]];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        const int tt = 2 * t + cc;
-        if (tt < M) {
-          yss[tt * 16 + g] = (uint16_t)f32_to_bf16_bits(__fadd_rn(S_[cc], C_[cc]));
-          yss[tt * 16 + g + 8] = (uint16_t)f32_to_bf16_bits(__fadd_rn(S_[2 + cc], C_[2 + cc]));
+        const int nn = 2 * t + cc;
+        if (nn < cn) {
+          const int p = RT.off[u] + nn;
+          ysm[p * 16 + g] = (uint16_t)f32_to_bf16_bits(__fmul_rn(__fadd_rn(S_[cc], C_[cc]) * 128.0f, gs2));
+          ysm[p * 16 + g + 8] =
+              (uint16_t)f32_to_bf16_bits(__fmul_rn(__fadd_rn(S_[2 + cc], C_[2 + cc]) * 128.0f, gs2));
         }
       }
-    } else {
-      // ---- routed down stage: rows h0 .. h0 + 15 of one or two experts
-      const int nb = inf.nblk, wb = 16 * (I / 2) + I;
-      int aoff = nb * wb;
-      for (int blk = 0; ok && blk < nb; ++blk) {
-        const int u = inf.blk_u[blk], cn = RT.cnt[u];
-        uint8_t* arow = st + aoff;
-        if (!copy_rows(arow, a.ws.act + (size_t)RT.off[u] * I, cn, I)) { ok = false; break; }
-        aoff += cn * (2 * I + 16);
-        const uint8_t* base = st + blk * wb;
-        const uint8_t* sc = base + 16 * (I / 2);
-        float S_[4] = {0.0f, 0.0f, 0.0f, 0.0f}, C_[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int s = 0; s < I / kSliceK; ++s) {
-          uint4 xb[4];
-          load_col_smem(xb, g < cn ? arow + (size_t)g * (2 * I + 16) + 2 * (s * kSliceK + 32 * t) : nullptr);
-          slice_down_fp4(S_, C_, base + g * (I / 2), base + (g + 8) * (I / 2), sc + g * (I / 16),
-                         sc + (g + 8) * (I / 16), s, t, xb);
-        }
-        const float gs2 = a.w2_gs[RT.e[u]];
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int nn = 2 * t + cc;
-          if (nn < cn) {
-            const int p = RT.off[u] + nn;
-            ysm[p * 16 + g] = (uint16_t)f32_to_bf16_bits(__fmul_rn(__fadd_rn(S_[cc], C_[cc]) * 128.0f, gs2));
-            ysm[p * 16 + g + 8] =
-                (uint16_t)f32_to_bf16_bits(__fmul_rn(__fadd_rn(S_[2 + cc], C_[2 + cc]) * 128.0f, gs2));
-          }
-        }
-      }
-      if (!ok) break;
       release(n);
     }
     const int2 fl = finish(false);
-    if (fl.y) { final_rows(); leave(); }
+    if (fl.y) { closing = true; break; }
+  }
+  // the output rows are written once, after the loop, by the warp that
+  // finished the CTA's last record
+  if (closing) {
+    final_rows();
+    leave();
   }
   if (!ok) {
     // a wait gave up: count this warp out once so that the CTA still leaves
@@ -1271,12 +1427,13 @@ bool fused_supported(const flint_moe_shape& s, int sms) {
   if (s.H > 2048 || s.H % 128 != 0 || s.H / 16 > sms) return false;
   if (s.I > 2048 || s.I % 128 != 0 || s.SI > 1024 || s.SI % 128 != 0) return false;
   if (s.E > kMaxRouterRows * sms) return false;
-  // a routed down block with all M of its activation rows, and the shared
-  // down's activation rows, fit one stage
+  // a routed down block with all M of its activation rows fits one stage
   if (16 * (s.I / 2) + s.I + s.M * (2 * s.I + 16) > kStageBytes) return false;
-  if (s.M * (2 * s.SI + 16) > kStageBytes) return false;
+  // the shared down's activation rows fit the split activations' room
+  if (2 * s.SI + 16 > 2 * (2 * s.H + 16)) return false;
   const Layout L = fused_layout(s.M, s.H, s.SI);
-  return L.stages >= 3 && L.total <= (size_t)kMaxSmem;
+  // the (up to 4) stages of a shared gate/up tile are resident together
+  return L.stages >= 4 && L.total <= (size_t)kMaxSmem;
 }
 
 cudaError_t launch_fused(const MoEArgs& a, cudaStream_t st, int sms) {

@@ -509,7 +509,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
             *reinterpret_cast<uint4*>(bt + kATile + tc::sw128_offset(r, 8 * i)) = bv0[i];
             *reinterpret_cast<uint4*>(bt + kATile + tc::sw128_offset(r, 32 + 8 * i)) = bv1[i];
           }
-          tc::fence_proxy_async_smem();
+          fence_proxy_async_smem();
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&C.full[s]);

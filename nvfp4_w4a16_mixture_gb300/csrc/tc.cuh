@@ -33,9 +33,6 @@ FLINT_DEV void tmem_dealloc(uint32_t base, uint32_t ncols) {
 FLINT_DEV void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 FLINT_DEV void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Generic-proxy shared-memory writes made visible to the async proxy (the
-// tensor core reads operands through it).
-FLINT_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // --------------------------------------------------------- descriptors --
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle.  Fields:

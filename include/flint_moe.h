@@ -53,18 +53,23 @@ enum {
  *   M      tokens (rows of x), M >= 0.  M = 0 (an empty batch) is checked
  *          as a shape and returns FLINT_OK without any launch or memory
  *          access; the M-sized buffers and the workspace may then be NULL.
- *   H      hidden size; multiple of 128
+ *   H      hidden size; multiple of 64
  *   E      routed experts, 1..256
  *   top_k  experts per token, 1..min(E, 32)
- *   I      routed-expert intermediate size; multiple of 128
+ *   I      routed-expert intermediate size; multiple of 64
  *   SI     shared-expert intermediate size; 0 (no shared expert) or a
- *          multiple of 128 */
+ *          multiple of 64
+ * A shape outside these limits is invalid (FLINT_ERR_INVALID_ARG).  The
+ * kernels run K in 128-wide slices: a valid shape whose H, I or SI is an odd
+ * multiple of 64 is not supported yet, and every entry point returns
+ * FLINT_ERR_UNSUPPORTED for it without enqueuing anything (the size queries
+ * return 0). */
 typedef struct {
   int M, H, E, top_k, I, SI;
 } flint_moe_shape;
 
 /* Bytes of device workspace flint_moe_route / flint_moe_forward need for
- * `shape`; 0 if the shape is invalid. */
+ * `shape`; 0 if the shape is invalid or not supported. */
 size_t flint_moe_workspace_bytes(const flint_moe_shape* shape);
 
 /* Routing only: "route" on the page above (BF16 router logits -> top-k ids
@@ -105,13 +110,22 @@ int flint_moe_route(const void* x, const void* router_w, const flint_moe_shape* 
  *
  * Numerics: BF16 activations, E2M1 x E4M3 weights dequantised exactly,
  * fp32 accumulation with the global scale applied to the accumulator;
- * act = bf16(silu(g) * u) with sigmoid = rcp.approx(1 + ex2.approx(-g log2 e));
- * y_e = bf16(acc * gs2_e); shared expert gS, uS = bf16(dot),
- * sact = bf16(silu(gS) * uS), ys = bf16(dot); out = bf16(bf16(sum_j tw_j y_j) + ys).
- * The kernels multiply activations by weights scaled by 2^-7 (exactly) and
- * scale the fp32 accumulator back by 2^7, so single products below 2^-119 in
- * magnitude are formed as fp32 subnormals; no sum of realistic size resolves
- * them. */
+ * act = bf16(silu(g) * u); y_e = bf16(acc * gs2_e); shared expert
+ * gS, uS = bf16(dot), sact = bf16(silu(gS) * uS), ys = bf16(dot);
+ * out = bf16(bf16(sum_j tw_j y_j) + ys), the routed sum in rank order.
+ * How close the sums come to the exact ones depends on the path (see
+ * flint_moe_plan):
+ *  - FLINT_PATH_SINGLE_LAUNCH forms every gate/up sum (routed and shared) as
+ *    the exact sum of the exact products rounded once to fp32, the down sums
+ *    from exact 128-K partial sums added with TwoSum, and every sigmoid with
+ *    the correctly rounded exp wherever the BF16 rounding depends on it;
+ *  - the other paths accumulate in the tensor cores' fp32 order with
+ *    sigmoid = rcp.approx(1 + ex2.approx(-g log2 e)), which now and then
+ *    moves a BF16 rounding of an intermediate by one ulp.
+ * The kernels of the decode paths multiply activations by weights scaled by
+ * 2^-7 (exactly) and scale the fp32 accumulator back by 2^7, so single
+ * products below 2^-119 in magnitude are formed as fp32 subnormals; no sum
+ * of realistic size resolves them. */
 int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13,
                       const uint8_t* w13_sf, const float* w13_gs, const uint8_t* w2,
                       const uint8_t* w2_sf, const float* w2_gs, const void* shared_gu,
@@ -150,7 +164,8 @@ int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13,
 int flint_moe_route_noalloc(const void* x, const void* router_w, const flint_moe_shape* shape,
                             int32_t* ids, float* tw, flint_stream_t stream);
 
-/* Scratch bytes flint_moe_route_noalloc needs for `shape` (0 if invalid). */
+/* Scratch bytes flint_moe_route_noalloc needs for `shape` (0 if invalid or
+ * not supported). */
 size_t flint_moe_route_noalloc_bytes(const flint_moe_shape* shape);
 
 /* Size of the fixed scratch (bytes per device). */
@@ -165,19 +180,44 @@ size_t flint_moe_route_noalloc_capacity(void);
  * inside stream capture or a latency-critical loop. */
 int flint_moe_status(void* workspace, flint_stream_t stream);
 
+/* Which kernels flint_moe_forward runs for `shape` on the calling thread's
+ * current device (a host-side query; nothing is enqueued):
+ *   FLINT_PATH_NONE            M = 0: nothing
+ *   FLINT_PATH_SINGLE_LAUNCH   one cooperative kernel: router, top-k, expert
+ *                              grouping, gate/up, down and combine (few tokens;
+ *                              every gate/up sum exact before its rounding)
+ *   FLINT_PATH_DECODE          router, gate/up and down kernels chained with
+ *                              programmatic dependent launch (M <= 64)
+ *   FLINT_PATH_DECODE_FALLBACK the same three steps for shapes outside the
+ *                              limits of the two paths above
+ *   FLINT_PATH_GROUPED         many tokens: router with expert histogram,
+ *                              per-expert tcgen05 GEMMs, combine
+ * or a negative FLINT_ERR_* code (invalid / unsupported shape, CUDA error). */
+enum {
+  FLINT_PATH_NONE = 0,
+  FLINT_PATH_SINGLE_LAUNCH = 1,
+  FLINT_PATH_DECODE = 2,
+  FLINT_PATH_DECODE_FALLBACK = 3,
+  FLINT_PATH_GROUPED = 4,
+};
+int flint_moe_plan(const flint_moe_shape* shape);
+
 /* Static description of an error code. */
 const char* flint_moe_strerror(int code);
 
 /* Test hook for the failure path (process-wide, default off).  With
- * site = FLINT_FAULT_DOWN_HANDOVER the next launches of the decode down
- * kernel leave out one signal: the warp holding the second half of an item's
- * K never raises its hand-over flag, so the warp waiting for it gives up
- * after its bounded wait (200 ms), records FLINT_ERR_TIMEOUT with the wait
- * site, CTA and stage in status words 1..3 of the workspace, and every warp
- * of the launch exits; the outputs of such a call are undefined, the context
- * stays usable and the next call without the hook is exact again.  Nothing
- * faults, traps or hangs.  site = 0 turns the hook off.  Returns FLINT_OK, or
- * FLINT_ERR_INVALID_ARG for an unknown site. */
+ * site = FLINT_FAULT_DOWN_HANDOVER the next forward launches leave out one
+ * hand-over signal into the down projection: in the three-kernel decode
+ * path the warp holding the second half of an item's K never raises its
+ * flag; in the single-launch path the CTA that sees the grid barrier before
+ * the down phase complete never passes that on to its down records.  The
+ * waiting warps give up after their bounded wait (200 ms), record
+ * FLINT_ERR_TIMEOUT with the wait site (17), CTA and stage in status words
+ * 1..3 of the workspace, and every warp of the launch exits; the outputs of
+ * such a call are undefined, the context stays usable and the next call
+ * without the hook is exact again.  Nothing faults, traps or hangs.
+ * site = 0 turns the hook off.  Returns FLINT_OK, or FLINT_ERR_INVALID_ARG
+ * for an unknown site. */
 enum { FLINT_FAULT_NONE = 0, FLINT_FAULT_DOWN_HANDOVER = 17 };
 int flint_moe_debug_fault(int site);
 

@@ -23,12 +23,17 @@ FLINT_ERR_TIMEOUT = -5
 FLINT_ERR_SCRATCH = -6
 FLINT_FAULT_NONE = 0
 FLINT_FAULT_DOWN_HANDOVER = 17
+FLINT_PATH_NONE = 0
+FLINT_PATH_SINGLE_LAUNCH = 1
+FLINT_PATH_DECODE = 2
+FLINT_PATH_DECODE_FALLBACK = 3
+FLINT_PATH_GROUPED = 4
 
 # Every C symbol the header declares (checked by tests/test_abi.py).
 EXPORTED = ("flint_moe_workspace_bytes", "flint_moe_route", "flint_moe_forward",
             "flint_moe_route_noalloc", "flint_moe_route_noalloc_bytes",
             "flint_moe_route_noalloc_capacity", "flint_moe_status", "flint_moe_strerror",
-            "flint_moe_debug_fault")
+            "flint_moe_debug_fault", "flint_moe_plan")
 
 
 class FlintMoEError(RuntimeError):
@@ -76,6 +81,8 @@ def load() -> ctypes.CDLL:
             lib.flint_moe_strerror.argtypes = [ctypes.c_int]
             lib.flint_moe_debug_fault.restype = ctypes.c_int
             lib.flint_moe_debug_fault.argtypes = [ctypes.c_int]
+            lib.flint_moe_plan.restype = ctypes.c_int
+            lib.flint_moe_plan.argtypes = [S]
             _lib = lib
     return _lib
 
@@ -105,7 +112,7 @@ def flint_moe_strerror(code: int) -> str:
 
 
 def flint_moe_workspace_bytes(M: int, H: int, E: int, top_k: int, I: int, SI: int) -> int:
-    """Workspace bytes for the shape (0 if the shape is invalid)."""
+    """Workspace bytes for the shape (0 if the shape is invalid or unsupported)."""
     s = _shape(M, H, E, top_k, I, SI)
     return int(load().flint_moe_workspace_bytes(ctypes.byref(s)))
 
@@ -163,6 +170,16 @@ def flint_moe_route_noalloc_capacity() -> int:
     return int(load().flint_moe_route_noalloc_capacity())
 
 
+def flint_moe_plan(M: int, H: int, E: int, top_k: int, I: int, SI: int) -> int:
+    """The FLINT_PATH_* flint_moe_forward takes for the shape on the current
+    device; raises FlintMoEError for an invalid or unsupported shape."""
+    s = _shape(M, H, E, top_k, I, SI)
+    rc = int(load().flint_moe_plan(ctypes.byref(s)))
+    if rc < 0:
+        raise FlintMoEError(rc, "flint_moe_plan")
+    return rc
+
+
 def flint_moe_status(workspace, stream=None) -> int:
     """Synchronise `stream` and return (and clear) the workspace status word."""
     return int(load().flint_moe_status(_ptr(workspace), _stream(stream)))
@@ -182,7 +199,10 @@ def alloc_workspace(M: int, H: int, E: int, top_k: int, I: int, SI: int,
     """A zero-filled workspace (do this once, outside graph capture)."""
     n = flint_moe_workspace_bytes(M, H, E, top_k, I, SI)
     if n == 0:
-        raise FlintMoEError(FLINT_ERR_INVALID_ARG, "alloc_workspace")
+        code = FLINT_ERR_INVALID_ARG
+        if all(v % 64 == 0 for v in (H, I, SI)) and not all(v % 128 == 0 for v in (H, I, SI)):
+            code = FLINT_ERR_UNSUPPORTED
+        raise FlintMoEError(code, "alloc_workspace")
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 

@@ -14,17 +14,32 @@ static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 static std::atomic<int> g_fault_site{0};  // test hook, see flint_moe_debug_fault
 int debug_fault_site() { return g_fault_site.load(std::memory_order_relaxed); }
 
+// A well-formed shape: H, I and SI multiples of 64 (the unit of the block's
+// interface), counts in range.
 static bool shape_valid(const flint_moe_shape* s) {
   if (!s) return false;
-  if (s->M < 0 || s->H < 128 || s->H % 128 != 0) return false;
+  if (s->M < 0 || s->H < 64 || s->H % 64 != 0) return false;
   if (s->E < 1 || s->E > kMaxE) return false;
   if (s->top_k < 1 || s->top_k > s->E || s->top_k > kMaxTopK) return false;
-  if (s->I < 128 || s->I % 128 != 0) return false;
-  if (s->SI < 0 || s->SI % 128 != 0) return false;
+  if (s->I < 64 || s->I % 64 != 0) return false;
+  if (s->SI < 0 || s->SI % 64 != 0) return false;
   // element counts addressed with 32-bit indices in places
   if ((int64_t)s->M * s->top_k > (int64_t)1 << 30) return false;
   if ((int64_t)s->H * 2 * s->I > (int64_t)1 << 31) return false;
   return true;
+}
+
+// Shapes the kernels run: every K extent a whole number of 128-wide slices.
+static bool shape_supported(const flint_moe_shape* s) {
+  return s->H % 128 == 0 && s->I % 128 == 0 && s->SI % 128 == 0;
+}
+
+// The path flint_moe_forward takes for a valid, supported shape with M > 0.
+static int plan(const flint_moe_shape& s, int sms) {
+  if (s.M > kDecodeMaxTokens && grouped_supported(s)) return FLINT_PATH_GROUPED;
+  if (fused_supported(s, sms)) return FLINT_PATH_SINGLE_LAUNCH;
+  if (decode2_supported(s)) return FLINT_PATH_DECODE;
+  return FLINT_PATH_DECODE_FALLBACK;
 }
 
 WsLayout ws_layout(const flint_moe_shape& s) {
@@ -123,13 +138,14 @@ using namespace flint;
 extern "C" {
 
 size_t flint_moe_workspace_bytes(const flint_moe_shape* shape) {
-  if (!shape_valid(shape)) return 0;
+  if (!shape_valid(shape) || !shape_supported(shape)) return 0;
   return ws_layout(*shape).total;
 }
 
 int flint_moe_route(const void* x, const void* router_w, const flint_moe_shape* shape, int32_t* ids,
                     float* tw, void* workspace, size_t workspace_bytes, flint_stream_t stream) {
   if (!shape_valid(shape)) return FLINT_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return FLINT_ERR_UNSUPPORTED;
   if (shape->M == 0) return FLINT_OK;  // an empty batch: nothing to launch
   if (!x || !router_w || !ids || !tw) return FLINT_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(router_w, 16) || !aligned(ids, 4) || !aligned(tw, 4))
@@ -156,6 +172,7 @@ int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13, c
                       const flint_moe_shape* shape, void* out, int32_t* ids_out, float* tw_out,
                       void* workspace, size_t workspace_bytes, flint_stream_t stream) {
   if (!shape_valid(shape)) return FLINT_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return FLINT_ERR_UNSUPPORTED;
   if (shape->M == 0) return FLINT_OK;  // an empty batch: nothing to launch
   if (!x || !router_w || !w13 || !w13_sf || !w13_gs || !w2 || !w2_sf || !w2_gs || !out)
     return FLINT_ERR_INVALID_ARG;
@@ -187,24 +204,33 @@ int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13, c
   a.ws = ws_pointers(workspace, L);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-  if (shape->M > kDecodeMaxTokens && grouped_supported(*shape)) {
-    if (launch_grouped(a, st) != cudaSuccess) return FLINT_ERR_CUDA;
-    return FLINT_OK;
-  }
   int sms = 0;
   if (device_sms(&sms) != cudaSuccess) return FLINT_ERR_CUDA;
-  if (fused_supported(*shape, sms)) {
-    if (launch_fused(a, st, sms) != cudaSuccess) return FLINT_ERR_CUDA;
-    return FLINT_OK;
+  switch (plan(*shape, sms)) {
+    case FLINT_PATH_GROUPED:
+      if (launch_grouped(a, st) != cudaSuccess) return FLINT_ERR_CUDA;
+      return FLINT_OK;
+    case FLINT_PATH_SINGLE_LAUNCH:
+      if (launch_fused(a, st, sms) != cudaSuccess) return FLINT_ERR_CUDA;
+      return FLINT_OK;
+    case FLINT_PATH_DECODE:
+      if (launch_decode2(a, st) != cudaSuccess) return FLINT_ERR_CUDA;
+      return FLINT_OK;
+    default:
+      if (launch_route(a, true, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
+      if (launch_decode_gate_up(a, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
+      if (launch_decode_down(a, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
+      return FLINT_OK;
   }
-  if (decode2_supported(*shape)) {
-    if (launch_decode2(a, st) != cudaSuccess) return FLINT_ERR_CUDA;
-    return FLINT_OK;
-  }
-  if (launch_route(a, true, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
-  if (launch_decode_gate_up(a, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
-  if (launch_decode_down(a, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
-  return FLINT_OK;
+}
+
+int flint_moe_plan(const flint_moe_shape* shape) {
+  if (!shape_valid(shape)) return FLINT_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return FLINT_ERR_UNSUPPORTED;
+  if (shape->M == 0) return FLINT_PATH_NONE;
+  int sms = 0;
+  if (device_sms(&sms) != cudaSuccess) return FLINT_ERR_CUDA;
+  return plan(*shape, sms);
 }
 
 int flint_moe_status(void* workspace, flint_stream_t stream) {

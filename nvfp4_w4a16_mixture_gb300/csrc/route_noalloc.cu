@@ -55,9 +55,11 @@ NoAllocLayout noalloc_layout(const flint_moe_shape& s) {
   return L;
 }
 
+// Well-formed (H a multiple of 64, as for flint_moe_route); the kernel runs
+// H in whole 128-wide slices.
 bool shape_ok(const flint_moe_shape* s) {
   if (!s) return false;
-  if (s->M < 0 || s->H < 128 || s->H % 128 != 0) return false;
+  if (s->M < 0 || s->H < 64 || s->H % 64 != 0) return false;
   if (s->E < 1 || s->E > kMaxE) return false;
   if (s->top_k < 1 || s->top_k > s->E || s->top_k > kMaxTopK) return false;
   return true;
@@ -132,7 +134,7 @@ using namespace flint;
 extern "C" {
 
 size_t flint_moe_route_noalloc_bytes(const flint_moe_shape* shape) {
-  if (!shape_ok(shape)) return 0;
+  if (!shape_ok(shape) || shape->H % 128 != 0) return 0;
   return noalloc_layout(*shape).total;
 }
 
@@ -141,6 +143,7 @@ size_t flint_moe_route_noalloc_capacity(void) { return kNoAllocScratchBytes; }
 int flint_moe_route_noalloc(const void* x, const void* router_w, const flint_moe_shape* shape,
                             int32_t* ids, float* tw, flint_stream_t stream) {
   if (!shape_ok(shape)) return FLINT_ERR_INVALID_ARG;
+  if (shape->H % 128 != 0) return FLINT_ERR_UNSUPPORTED;
   if (shape->M == 0) return FLINT_OK;  // an empty batch: nothing to launch
   if (!x || !router_w || !ids || !tw) return FLINT_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(router_w, 16) || !aligned(ids, 4) || !aligned(tw, 4))

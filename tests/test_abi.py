@@ -154,3 +154,39 @@ def test_workspace_fits_expected_regions(shape):
     if M > 64:
         floor += 2 * M * k * H  # token rows in sorted pair order (grouped path)
     assert floor <= need <= floor + 4 * 1024 * 1024 + 16 * M * k + 2 * M * E + 272 * E
+
+
+def test_multiples_of_64_are_valid_but_unsupported():
+    """H, I and SI are valid in multiples of 64; the kernels run 128-wide K
+    slices, so an odd multiple of 64 is refused as unsupported (not as a bad
+    argument), synchronously and before any CUDA call."""
+    lib = fm.load()
+    fake = [0x10000 * (i + 1) for i in range(12)]
+    for shape in [(3, 192, 8, 2, 128, 128), (3, 256, 8, 2, 192, 128), (3, 256, 8, 2, 128, 64),
+                  (3, 64, 8, 2, 64, 64)]:
+        assert fm.flint_moe_workspace_bytes(*shape) == 0, shape
+        assert _call_forward(fake, shape, 1 << 30) == fm.FLINT_ERR_UNSUPPORTED, shape
+        s = _lib.flint_moe_shape(*shape)
+        assert lib.flint_moe_route(fake[0], fake[1], ctypes.byref(s), fake[2], fake[3], fake[4],
+                                   1 << 30, None) == fm.FLINT_ERR_UNSUPPORTED, shape
+        assert lib.flint_moe_plan(ctypes.byref(s)) == fm.FLINT_ERR_UNSUPPORTED, shape
+        with pytest.raises(fm.FlintMoEError) as ei:
+            fm.flint_moe_plan(*shape)
+        assert ei.value.code == fm.FLINT_ERR_UNSUPPORTED
+        with pytest.raises(fm.FlintMoEError) as ei:
+            fm.alloc_workspace(*shape, device="cpu")
+        assert ei.value.code == fm.FLINT_ERR_UNSUPPORTED
+    s = _lib.flint_moe_shape(3, 192, 8, 2, 128, 0)
+    assert lib.flint_moe_route_noalloc(fake[0], fake[1], ctypes.byref(s), fake[2], fake[3],
+                                       None) == fm.FLINT_ERR_UNSUPPORTED
+    assert fm.flint_moe_route_noalloc_bytes(3, 192, 8, 2) == 0
+    # not a multiple of 64: a malformed shape
+    assert _call_forward(fake, (3, 160, 8, 2, 128, 128), 1 << 30) == fm.FLINT_ERR_INVALID_ARG
+
+
+def test_plan_is_a_host_query():
+    """flint_moe_plan answers an empty batch and a bad shape without a GPU."""
+    assert fm.flint_moe_plan(0, 2048, 128, 8, 768, 768) == fm.FLINT_PATH_NONE
+    with pytest.raises(fm.FlintMoEError) as ei:
+        fm.flint_moe_plan(1, 2048, 128, 0, 768, 768)
+    assert ei.value.code == fm.FLINT_ERR_INVALID_ARG

@@ -328,3 +328,40 @@ def test_golden_tiny_regression():
     assert r["ids"].tolist() == gold["ids"]
     assert r["tw"].tolist() == gold["tw"]
     assert r["out"].astype(int).tolist() == gold["out_bf16_bits"]
+
+
+def test_shared_silu_is_the_division_form():
+    """The shared expert's SiLU is v / (1 + exp(-v)), not v * sigmoid(v):
+    the two fp32 forms differ in the last bit for some v, and for
+    (gS, uS) = (0.78515625, 0.87109375) that bit decides the BF16 rounding of
+    silu(gS) * uS.  x is one-hot in column 0 and the shared rows carry gS and
+    uS in column 0, so gS and uS are exact; the expected bits come from
+    numpy's fp32 arithmetic with exp taken in float64 and rounded once."""
+    M, H, E, k, I, SI = 1, 128, 4, 1, 128, 128
+    x, layer = synth.make_problem(M, H, E, k, I, SI, seed=3)
+    x.zero_()
+    x[0, 0] = 1.0
+    rng = np.random.default_rng(11)
+    g = rng.uniform(-4, 4, SI).astype(np.float32)
+    u = rng.uniform(-2, 2, SI).astype(np.float32)
+    g[0], u[0] = 0.78515625, 0.87109375      # the forms round apart here
+    g[1], u[1] = 0.78515625, 0.0272216796875  # and here
+    gb = torch.from_numpy(g).to(torch.bfloat16)
+    ub = torch.from_numpy(u).to(torch.bfloat16)
+    gu = torch.zeros(2 * SI, H, dtype=torch.bfloat16)
+    gu[:SI, 0], gu[SI:, 0] = gb, ub
+    layer.shared_gu = gu
+    r = oracle.forward(x, layer, k, intermediates=True)
+    gv, uv = gb.float().numpy(), ub.float().numpy()
+    e = np.exp(-gv.astype(np.float64)).astype(np.float32)
+    den = (np.float32(1) + e).astype(np.float32)
+    div = (gv / den).astype(np.float32)
+    mul = (gv * (np.float32(1) / den).astype(np.float32)).astype(np.float32)
+
+    def bf16_bits(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+    want_div = bf16_bits((div * uv).astype(np.float32))
+    want_mul = bf16_bits((mul * uv).astype(np.float32))
+    assert (want_div[:2] != want_mul[:2]).all()  # the constructed rows separate the forms
+    assert np.array_equal(r["sact"][0], want_div)

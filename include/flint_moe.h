@@ -119,9 +119,13 @@ int flint_moe_route(const void* x, const void* router_w, const flint_moe_shape* 
  *    the exact sum of the exact products rounded once to fp32, the down sums
  *    from exact 128-K partial sums added with TwoSum, and every sigmoid with
  *    the correctly rounded exp wherever the BF16 rounding depends on it;
- *  - the other paths accumulate in the tensor cores' fp32 order with
- *    sigmoid = rcp.approx(1 + ex2.approx(-g log2 e)), which now and then
- *    moves a BF16 rounding of an intermediate by one ulp.
+ *  - FLINT_PATH_DECODE forms the shared expert's gate/up sums exactly (its
+ *    activation reaches every output of a token) and evaluates act and sact
+ *    with the correctly rounded exp; the routed sums follow the tensor
+ *    cores' fp32 order in 128-K chains;
+ *  - the fallback and grouped paths accumulate in the tensor cores' fp32
+ *    order with sigmoid = rcp.approx(1 + ex2.approx(-g log2 e)).
+ * Where a sum is not exact, its BF16 rounding now and then moves by one ulp.
  * The kernels of the decode paths multiply activations by weights scaled by
  * 2^-7 (exactly) and scale the fp32 accumulator back by 2^7, so single
  * products below 2^-119 in magnitude are formed as fp32 subnormals; no sum
@@ -201,6 +205,16 @@ enum {
   FLINT_PATH_GROUPED = 4,
 };
 int flint_moe_plan(const flint_moe_shape* shape);
+
+/* Path preference (process-wide, default FLINT_PATH_NONE).  By default a
+ * batch of at most 64 tokens runs FLINT_PATH_DECODE, which measures faster.
+ * With FLINT_PATH_SINGLE_LAUNCH, flint_moe_forward runs the single-launch
+ * kernel wherever it supports the shape (M <= 8, M * top_k <= 64,
+ * H <= 2048, I <= 2048, SI <= 1024 and E <= twice the SM count): its gate/up
+ * sums are the exact sums rounded once to fp32.  Returns FLINT_OK, or
+ * FLINT_ERR_INVALID_ARG for another value.  Set it between calls, not while
+ * another host thread enqueues work. */
+int flint_moe_prefer_path(int path);
 
 /* Static description of an error code. */
 const char* flint_moe_strerror(int code);

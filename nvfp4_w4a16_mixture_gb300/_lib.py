@@ -33,7 +33,7 @@ FLINT_PATH_GROUPED = 4
 EXPORTED = ("flint_moe_workspace_bytes", "flint_moe_route", "flint_moe_forward",
             "flint_moe_route_noalloc", "flint_moe_route_noalloc_bytes",
             "flint_moe_route_noalloc_capacity", "flint_moe_status", "flint_moe_strerror",
-            "flint_moe_debug_fault", "flint_moe_plan")
+            "flint_moe_debug_fault", "flint_moe_plan", "flint_moe_prefer_path")
 
 
 class FlintMoEError(RuntimeError):
@@ -83,6 +83,8 @@ def load() -> ctypes.CDLL:
             lib.flint_moe_debug_fault.argtypes = [ctypes.c_int]
             lib.flint_moe_plan.restype = ctypes.c_int
             lib.flint_moe_plan.argtypes = [S]
+            lib.flint_moe_prefer_path.restype = ctypes.c_int
+            lib.flint_moe_prefer_path.argtypes = [ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -178,6 +180,13 @@ def flint_moe_plan(M: int, H: int, E: int, top_k: int, I: int, SI: int) -> int:
     if rc < 0:
         raise FlintMoEError(rc, "flint_moe_plan")
     return rc
+
+
+def flint_moe_prefer_path(path: int) -> None:
+    """Process-wide path preference (FLINT_PATH_NONE or FLINT_PATH_SINGLE_LAUNCH)."""
+    rc = load().flint_moe_prefer_path(int(path))
+    if rc != FLINT_OK:
+        raise FlintMoEError(rc, "flint_moe_prefer_path")
 
 
 def flint_moe_status(workspace, stream=None) -> int:

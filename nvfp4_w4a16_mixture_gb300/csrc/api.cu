@@ -12,6 +12,7 @@ namespace flint {
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 static std::atomic<int> g_fault_site{0};  // test hook, see flint_moe_debug_fault
+static std::atomic<int> g_prefer{0};      // flint_moe_prefer_path
 int debug_fault_site() { return g_fault_site.load(std::memory_order_relaxed); }
 
 // A well-formed shape: H, I and SI multiples of 64 (the unit of the block's
@@ -35,10 +36,15 @@ static bool shape_supported(const flint_moe_shape* s) {
 }
 
 // The path flint_moe_forward takes for a valid, supported shape with M > 0.
+// The three-kernel decode path is the default for few tokens (it measures
+// faster than the single launch at every M it serves); the single launch
+// runs where the caller prefers it and it supports the shape.
 static int plan(const flint_moe_shape& s, int sms) {
   if (s.M > kDecodeMaxTokens && grouped_supported(s)) return FLINT_PATH_GROUPED;
-  if (fused_supported(s, sms)) return FLINT_PATH_SINGLE_LAUNCH;
+  if (g_prefer.load(std::memory_order_relaxed) == FLINT_PATH_SINGLE_LAUNCH && fused_supported(s, sms))
+    return FLINT_PATH_SINGLE_LAUNCH;
   if (decode2_supported(s)) return FLINT_PATH_DECODE;
+  if (fused_supported(s, sms)) return FLINT_PATH_SINGLE_LAUNCH;
   return FLINT_PATH_DECODE_FALLBACK;
 }
 
@@ -244,6 +250,12 @@ int flint_moe_status(void* workspace, flint_stream_t stream) {
     if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return FLINT_ERR_CUDA;
     return status;
   }
+  return FLINT_OK;
+}
+
+int flint_moe_prefer_path(int path) {
+  if (path != FLINT_PATH_NONE && path != FLINT_PATH_SINGLE_LAUNCH) return FLINT_ERR_INVALID_ARG;
+  g_prefer.store(path, std::memory_order_relaxed);
   return FLINT_OK;
 }
 

@@ -27,6 +27,7 @@
 // the status word, later waits return at once, and the control flow of all
 // warps stays identical (no barrier is skipped), so the launch always ends.
 #include "common.cuh"
+#include "exact.cuh"
 #include "frag.cuh"
 #include "internal.h"
 
@@ -458,26 +459,33 @@ __global__ void __launch_bounds__(kGuThreads, 1) gate_up2_kernel(MoEArgs a) {
             if (nn < cnt) {
               const float f = er.f16p ? gs * pow2f(-er.exp[nn]) : gs;
               const float gv = v[cc] * f, uv = v[2 + cc] * f;
-              a.ws.act[(size_t)(off + nn) * I + r0 + 8 * at + g] =
-                  (uint16_t)f32_to_bf16_bits(silu_approx(gv) * uv);
+              a.ws.act[(size_t)(off + nn) * I + r0 + 8 * at + g] = (uint16_t)act_bits(gv, uv);
             }
           }
         }
       } else {
+        // shared tile: warp w < 8 left the (sum, compensation) pair of its K
+        // slices in its own slots and in warp w + 8's; they are added in warp
+        // order with TwoSum
         for (int nt = 0; nt < ntiles; ++nt) {
-          float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          float S[4] = {0.0f, 0.0f, 0.0f, 0.0f}, C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
           for (int w = 0; w < 8; ++w) {
             const float4 p = red4[((size_t)w * ntmax + nt) * 32 + lane];
-            v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
+            const float4 q = red4[((size_t)(w + 8) * ntmax + nt) * 32 + lane];
+            two_sum(S[0], C[0], p.x); two_sum(S[1], C[1], p.y);
+            two_sum(S[2], C[2], p.z); two_sum(S[3], C[3], p.w);
+            C[0] = __fadd_rn(C[0], q.x); C[1] = __fadd_rn(C[1], q.y);
+            C[2] = __fadd_rn(C[2], q.z); C[3] = __fadd_rn(C[3], q.w);
           }
+          const float v[4] = {__fadd_rn(S[0], C[0]), __fadd_rn(S[1], C[1]), __fadd_rn(S[2], C[2]),
+                              __fadd_rn(S[3], C[3])};
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             const int nn = nt * 8 + 2 * t + cc;
             if (nn < cnt) {
               // stock BF16 SwiGLU: gS, uS rounded, silu(gS) = gS / (1 + exp(-gS))
               const float gS = round_bf16(v[cc]), uS = round_bf16(v[2 + cc]);
-              const float sv = __fdiv_rn(gS, 1.0f + expf(-gS)) * uS;
-              a.ws.sact[(size_t)nn * SI + r0 + g] = (uint16_t)f32_to_bf16_bits(sv);
+              a.ws.sact[(size_t)nn * SI + r0 + g] = (uint16_t)sact_bits(gS, uS);
             }
           }
         }
@@ -635,6 +643,50 @@ __global__ void __launch_bounds__(kGuThreads, 1) gate_up2_kernel(MoEArgs a) {
       sstep = 8;
       rg = st + g * pitch;
       rg8 = st + (8 + g) * pitch;
+    }
+    if (kind == 0) {
+      // ---- shared tile: warp w < 8 sums its K slices s = w (mod 8) of
+      // every token tile exactly (the shared activation of a token feeds all
+      // of its outputs) into a (sum, compensation) pair, carried from stage
+      // to stage in the partial buffer: the sum in its own slot, the
+      // compensation in idle warp w + 8's
+      if (warp < 8) {
+        for (int nt = 0; nt < ntiles; ++nt) {
+          float S_[4] = {0.0f, 0.0f, 0.0f, 0.0f}, C_[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          float4* rs = reinterpret_cast<float4*>(red + b * red_floats) + ((size_t)warp * ntmax + nt) * 32 + lane;
+          float4* rc =
+              reinterpret_cast<float4*>(red + b * red_floats) + ((size_t)(warp + 8) * ntmax + nt) * 32 + lane;
+          if (!first) {
+            const float4 o = *rs, q = *rc;
+            S_[0] = o.x; S_[1] = o.y; S_[2] = o.z; S_[3] = o.w;
+            C_[0] = q.x; C_[1] = q.y; C_[2] = q.z; C_[3] = q.w;
+          }
+          const int nn = nt * 8 + g;
+          const uint16_t* brow = nn < cnt ? a.x + (size_t)nn * H + k0 : nullptr;
+          for (int s = warp; s < nsl; s += 8) {
+            uint4 xb[4];
+            load_b(xb, brow ? brow + s * kSliceK : nullptr, t, false);
+            slice_bf16_exact(S_, C_, reinterpret_cast<const uint16_t*>(rg) + s * kSliceK + 32 * t,
+                             reinterpret_cast<const uint16_t*>(rg8) + s * kSliceK + 32 * t, xb);
+          }
+          *rs = make_float4(S_[0], S_[1], S_[2], S_[3]);
+          *rc = make_float4(C_[0], C_[1], C_[2], C_[3]);
+        }
+      }
+      if (last && warp == 0) {  // the tile's record, before the stage slot is released
+        EpiRec& er = SM.er[b];
+        if (lane == 0) {
+          er.kind = kind; er.r0 = inf.r0; er.e = inf.e; er.off = inf.off; er.cnt = cnt;
+          er.f16p = 0;
+        }
+        er.exp[lane] = 0;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&SM.ctl.empty[sl]);  // stage consumed
+      if (!last) continue;
+      if (lane == 0) mbar_arrive(&SM.ctl.bar[b]);  // partials (and record) of tile ep written
+      ++ep;
+      continue;
     }
     const bool f16p = kind == 1 && inf.x16;
     // the scale exponent of this lane's pair (f16 path), for the epilogue record

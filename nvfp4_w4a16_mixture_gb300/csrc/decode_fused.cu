@@ -61,6 +61,7 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "exact.cuh"
 #include "frag.cuh"
 #include "internal.h"
 
@@ -81,7 +82,6 @@ constexpr int kMaxRouterRows = 2;          // router rows per CTA (E <= 2 * grid
 constexpr int kMaxSmem = 232448;
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms
 constexpr uint32_t kSuspendNs = 50000;
-constexpr int kMargin = 64;  // fp32 ulps kept clear of a BF16 rounding boundary
 
 // wait sites recorded with a timeout (status word 1)
 enum {
@@ -252,140 +252,6 @@ __device__ __noinline__ bool wait_counter(const int* p, int target, volatile int
   }
 }
 
-// ------------------------------------------------------------ numerics --
-// s += v with the rounding error of the addition kept in c (TwoSum: s + e
-// equals the exact sum of the old s and v).
-FLINT_DEV void two_sum(float& s, float& c, float v) {
-  const float t = __fadd_rn(s, v);
-  const float z = __fsub_rn(t, s);
-  const float e = __fadd_rn(__fsub_rn(s, __fsub_rn(t, z)), __fsub_rn(v, z));
-  c = __fadd_rn(c, e);
-  s = t;
-}
-
-// fp32 ulps between v and the nearest BF16 rounding boundary (the midpoint
-// between two BF16 neighbours, where round-to-nearest-even decides).
-FLINT_DEV int bf16_margin(float v) {
-  return abs((int)(__float_as_uint(v) & 0xFFFFu) - 0x8000);
-}
-
-// exp(v) correctly rounded to fp32 but for a double-ulp window at the fp32
-// rounding boundaries: double-precision exp, rounded once.
-__device__ __noinline__ float exp_f32_rn(float v) { return (float)exp((double)v); }
-
-// act = bf16(silu(g) * u), silu(g) = g * (1 / (1 + exp(-g))), every step one
-// fp32 rounding.  expf is within 2 ulps of the rounded exp; that moves the
-// product by at most about 16 ulps, so a result more than kMargin ulps from a
-// BF16 boundary rounds as the correctly rounded exp would make it round.
-FLINT_DEV uint32_t act_bits(float g, float u) {
-  float e = expf(-g);
-  float v = __fmul_rn(__fmul_rn(g, __fdiv_rn(1.0f, __fadd_rn(1.0f, e))), u);
-  if (bf16_margin(v) <= kMargin) {
-    e = exp_f32_rn(-g);
-    v = __fmul_rn(__fmul_rn(g, __fdiv_rn(1.0f, __fadd_rn(1.0f, e))), u);
-  }
-  return f32_to_bf16_bits(v);
-}
-
-// shared expert: sact = bf16((gS / (1 + exp(-gS))) * uS) with gS, uS BF16
-// values (the stock SiLU form), same certification.
-FLINT_DEV uint32_t sact_bits(float gS, float uS) {
-  float e = expf(-gS);
-  float v = __fmul_rn(__fdiv_rn(gS, __fadd_rn(1.0f, e)), uS);
-  if (bf16_margin(v) <= kMargin) {
-    e = exp_f32_rn(-gS);
-    v = __fmul_rn(__fdiv_rn(gS, __fadd_rn(1.0f, e)), uS);
-  }
-  return f32_to_bf16_bits(v);
-}
-
-// bf16x2 arithmetic, round to nearest even
-FLINT_DEV uint32_t bf2_add(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-FLINT_DEV uint32_t bf2_sub(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-// Largest biased exponent field among the 32 bf16 values of v (two per word).
-FLINT_DEV int max_exp_field(const uint4 (&v)[4]) {
-  int m = 0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) m = max(m, (int)max((w[i] >> 23) & 0xFFu, (w[i] >> 7) & 0xFFu));
-  }
-  return m;
-}
-
-// Split 32 bf16 values as v = hi + lo, exactly: hi is v rounded to the grid
-// 2^(ef - 132) (ef = the largest biased exponent field among the values that
-// share the grid), so |hi| / grid <= 64, and lo = v - hi holds the rest (at
-// most 8 significant bits, a BF16 value).  The rounding adds and subtracts
-// C = 1.5 * 2^(ef - 125): v + C stays in one binade whose BF16 spacing is the
-// grid.
-FLINT_DEV void split_hi_lo(const uint4 (&v)[4], int ef, uint4 (&hi)[4], uint4 (&lo)[4]) {
-  ef = min(max(ef, 1), 252);
-  const uint32_t cb = ((uint32_t)(ef + 2) << 7) | 0x40u;
-  const uint32_t c2 = cb | (cb << 16);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    hi[q].x = bf2_sub(bf2_add(v[q].x, c2), c2);
-    hi[q].y = bf2_sub(bf2_add(v[q].y, c2), c2);
-    hi[q].z = bf2_sub(bf2_add(v[q].z, c2), c2);
-    hi[q].w = bf2_sub(bf2_add(v[q].w, c2), c2);
-    lo[q].x = bf2_sub(v[q].x, hi[q].x);
-    lo[q].y = bf2_sub(v[q].y, hi[q].y);
-    lo[q].z = bf2_sub(v[q].z, hi[q].z);
-    lo[q].w = bf2_sub(v[q].w, hi[q].w);
-  }
-}
-
-// The activation column of lane (g, t) for one 128-K slice (32 K values at K
-// offset 32 t), split hi / lo on the grid of the column's largest value over
-// the whole slice (the four lanes of column g agree).
-FLINT_DEV void split_column(const uint4 (&xb)[4], uint4 (&xh)[4], uint4 (&xl)[4]) {
-  int ef = max_exp_field(xb);
-  ef = max(ef, __shfl_xor_sync(0xffffffffu, ef, 1));
-  ef = max(ef, __shfl_xor_sync(0xffffffffu, ef, 2));
-  split_hi_lo(xb, ef, xh, xl);
-}
-
-// B operand registers of word q on the BF16 path (the K permutation of the
-// A fragments in frag.cuh: pairs (0, 4), (1, 5) for the first mma, (2, 6),
-// (3, 7) for the second).
-FLINT_DEV void b_regs(const uint4& x, uint32_t (&b)[2][2]) {
-  b[0][0] = __byte_perm(x.x, x.z, 0x5410);
-  b[0][1] = __byte_perm(x.x, x.z, 0x7632);
-  b[1][0] = __byte_perm(x.y, x.w, 0x5410);
-  b[1][1] = __byte_perm(x.y, x.w, 0x7632);
-}
-
-// A fragments of word q from natural-order bf16 rows (row g: a, row g + 8:
-// b), as a_frags(Bf16Slice) builds them.
-FLINT_DEV void a_regs_bf16(const uint4& a, const uint4& b, uint32_t (&af)[2][4]) {
-  af[0][0] = __byte_perm(a.x, a.z, 0x5410);
-  af[0][2] = __byte_perm(a.x, a.z, 0x7632);
-  af[1][0] = __byte_perm(a.y, a.w, 0x5410);
-  af[1][2] = __byte_perm(a.y, a.w, 0x7632);
-  af[0][1] = __byte_perm(b.x, b.z, 0x5410);
-  af[0][3] = __byte_perm(b.x, b.z, 0x7632);
-  af[1][1] = __byte_perm(b.y, b.w, 0x5410);
-  af[1][3] = __byte_perm(b.y, b.w, 0x7632);
-}
-
-FLINT_DEV void mma16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  mma_bf16_16816(d, a[0], a[1], a[2], a[3], b0, b1);
-}
-FLINT_DEV void mmah(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  mma_f16_16816(d, a[0], a[1], a[2], a[3], b0, b1);
-}
-
 // A fragments of one slice on the f16 path: byte b of a row's 16 code bytes
 // of this thread -> (K 2b, 2b + 1) by the hardware e2m1 -> f16 conversion,
 // times the f16 block scale (exact: at most 6 significant bits, inside f16's
@@ -521,52 +387,6 @@ FLINT_DEV void item_gateup(float (&S)[4], float (&C)[4], const uint8_t* st, int 
 #pragma unroll
       for (int i = 0; i < 4; ++i) C[i] = __fadd_rn(C[i], dl[i] * ((i & 1) ? pb : pa));
     }
-  }
-}
-
-// One 128-K slice of a 16-row BF16 tile (rows g, g + 8 in natural order at
-// ra / rb, this lane's 32 K at offset 32 t of the slice) against xb: the
-// weights are split per row over the slice, w_hi * x_hi accumulates exactly
-// in one chained mma (products of two <= 6-bit integers, 128 of them), the
-// rest goes to C.
-FLINT_DEV void slice_bf16_exact(float (&S)[4], float (&C)[4], const uint16_t* ra, const uint16_t* rb,
-                                const uint4 (&xb)[4]) {
-  uint4 xh[4], xl[4];
-  split_column(xb, xh, xl);
-  uint4 wa[4], wb[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    wa[q] = *reinterpret_cast<const uint4*>(ra + 8 * q);
-    wb[q] = *reinterpret_cast<const uint4*>(rb + 8 * q);
-  }
-  int ea = max_exp_field(wa), eb = max_exp_field(wb);
-  ea = max(ea, __shfl_xor_sync(0xffffffffu, ea, 1));
-  ea = max(ea, __shfl_xor_sync(0xffffffffu, ea, 2));
-  eb = max(eb, __shfl_xor_sync(0xffffffffu, eb, 1));
-  eb = max(eb, __shfl_xor_sync(0xffffffffu, eb, 2));
-  uint4 wah[4], wal[4], wbh[4], wbl[4];
-  split_hi_lo(wa, ea, wah, wal);
-  split_hi_lo(wb, eb, wbh, wbl);
-  float hh[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ap[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t bh[2][2], bl[2][2], ah[2][4], alo[2][4], aw[2][4];
-    b_regs(xh[q], bh);
-    b_regs(xl[q], bl);
-    a_regs_bf16(wah[q], wbh[q], ah);
-    a_regs_bf16(wal[q], wbl[q], alo);
-    a_regs_bf16(wa[q], wb[q], aw);
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mma16(hh, ah[r], bh[r][0], bh[r][1]);
-      mma16(ap, alo[r], bh[r][0], bh[r][1]);
-      mma16(ap, aw[r], bl[r][0], bl[r][1]);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    two_sum(S[i], C[i], hh[i]);
-    C[i] = __fadd_rn(C[i], ap[i]);
   }
 }
 

@@ -14,6 +14,14 @@ steps rotate through them (step i runs layer i mod layers), so every step
 streams its experts from HBM rather than L2 (the rotation's working set is far
 larger than the 129 MB L2).  The timed region replays CUDA graphs of the steps.
 
+The default command reports the whole metric in one JSON line: the headline
+(single-token decode, tokens/s with its HBM roofline and the end-to-end figure)
+and, under "records", the decode batch sweep (M = 2 .. 64, HBM roofline), the
+M = 4096 prefill and the Zipf-skewed M = 16384 workload (tensor roofline, total
+and routed-only TFLOP/s, per-expert load histogram), each timed the same way
+with its own SM-clock record.  cpu_baseline times the oracle on all host cores
+and on one thread, with the CPU model.
+
 Multi-GPU: one process per GPU (torchrun); every rank runs its own replica on
 its own tokens (the block has no cross-token exchange), so scaling is weak and
 no collective touches the data path.  Rank 0 prints one JSON line.
@@ -53,6 +61,9 @@ def parse():
     p.add_argument("--config", default="decode1", choices=sorted(synth.CONFIGS))
     p.add_argument("--layers", type=int, default=0, help="weight sets rotated (0 = auto)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-sweep", dest="sweep", action="store_false",
+                   help="time the headline configuration only (the default also times the decode "
+                        "sweep, prefill4096 and skew16384 as records of the same line)")
     p.add_argument("--profile", action="store_true",
                    help="run --warmup then --steps plain (eager) forwards and exit, for ncu launch lists")
     return p.parse_args()
@@ -189,10 +200,15 @@ def make_layers(cfg: str, n_layers: int, device: str, seed: int):
     return xs, layers
 
 
-def launches_per_step(M: int) -> int:
-    """Kernels of one forward: decode (M <= 64) router, gate/up, down+combine;
-    grouped path router, group count/scan/scatter, plan, gather, GEMM1,
-    GEMM2, combine."""
+LAUNCHES_PER_PATH = {1: 1, 2: 3, 3: 3, 4: 9}  # FLINT_PATH_* -> kernels per forward
+
+
+def launches_per_step(M: int, path: int = 0) -> int:
+    """Kernels of one forward: the single launch (1); decode router, gate/up,
+    down+combine (3); grouped path router, group count/scan/scatter, plan,
+    gather, GEMM1, GEMM2, combine (9).  Without a path: the default for M."""
+    if path:
+        return LAUNCHES_PER_PATH[path]
     return 3 if M <= DECODE_MAX_TOKENS else 9
 
 
@@ -242,53 +258,60 @@ def run_profile(args, local):
 
 
 # -------------------------------------------------------------------- ours
-def run_ours(args, rank, world, local):
-    import nvfp4_w4a16_mixture_gb300 as fm
+SWEEP = ("decode2", "decode4", "decode8", "decode16", "decode32", "decode64", "prefill4096",
+         "skew16384")
 
-    torch.cuda.set_device(local)
-    dev = f"cuda:{local}"
-    cfg = args.config
-    M, H, E, k, I, SI = synth.CONFIGS[cfg]
-    n_layers = args.layers or (16 if M <= DECODE_MAX_TOKENS else 2)
-    fm.load()
-    xs, layers = make_layers(cfg, n_layers, dev, seed=1 + rank)
-    ws = fm.alloc_workspace(M, H, E, k, I, SI, dev)
-    outs = [torch.empty_like(x) for x in xs]
-    ids = [torch.empty(M, k, dtype=torch.int32, device=dev) for _ in xs]
-    stream = torch.cuda.Stream(device=dev)
 
-    def step(i, s):
-        li = i % n_layers
-        fm.forward_layer(xs[li], layers[li], k, workspace=ws, out=outs[li], ids_out=ids[li], stream=s)
+class Workload:
+    """Resident weights and inputs of one configuration (several layers
+    rotated) and the graphs of its steps."""
 
+    def __init__(self, cfg, dev, rank, n_layers, layers=None):
+        import nvfp4_w4a16_mixture_gb300 as fm
+        self.fm = fm
+        self.cfg = cfg
+        self.M, self.H, self.E, self.k, self.I, self.SI = synth.CONFIGS[cfg]
+        self.n_layers = n_layers
+        if layers is None:
+            _, layers = make_layers(cfg, n_layers, dev, seed=1 + rank)
+        self.layers = layers
+        self.xs = [synth.make_x(self.M, self.H, torch.Generator(device=dev).manual_seed(9000 + 97 * rank + li), dev)
+                   for li in range(n_layers)]
+        self.ws = fm.alloc_workspace(self.M, self.H, self.E, self.k, self.I, self.SI, dev)
+        self.outs = [torch.empty_like(x) for x in self.xs]
+        self.ids = [torch.empty(self.M, self.k, dtype=torch.int32, device=dev) for _ in self.xs]
+        self.stream = torch.cuda.Stream(device=dev)
+        self.path = fm.flint_moe_plan(self.M, self.H, self.E, self.k, self.I, self.SI)
+
+    def step(self, i, s):
+        li = i % self.n_layers
+        self.fm.forward_layer(self.xs[li], self.layers[li], self.k, workspace=self.ws, out=self.outs[li],
+                              ids_out=self.ids[li], stream=s)
+
+
+def time_workload(w: Workload, steps: int, warmup: int, world: int, local: int):
+    """Device time of `steps` steps replayed from CUDA graphs (max over
+    ranks), with the SM clocks sampled during the timed region."""
+    fm, stream = w.fm, w.stream
     with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, n_layers)):
-            step(i, stream)
+        for i in range(max(warmup, w.n_layers)):
+            w.step(i, stream)
     stream.synchronize()
-    assert fm.flint_moe_status(ws, stream) == fm.FLINT_OK
-
-    # bytes each step reads: the experts its tokens route to + router + shared
-    uniq = [int(torch.unique(t).numel()) for t in ids]
-    wb = [synth.weight_bytes(H, E, I, SI, u) for u in uniq]
-    flops = synth.flops_of(M, H, E, k, I, SI)
-
-    # graphs: one of all layers, one of the remainder
-    K = args.steps
-    full, rem = divmod(K, n_layers)
+    assert fm.flint_moe_status(w.ws, stream) == fm.FLINT_OK
+    full, rem = divmod(steps, w.n_layers)
     g_full = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_full, stream=stream):
-        for i in range(n_layers):
-            step(i, stream)
+        for i in range(w.n_layers):
+            w.step(i, stream)
     g_rem = None
     if rem:
         g_rem = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_rem, stream=stream):
             for i in range(rem):
-                step(i, stream)
+                w.step(i, stream)
     with torch.cuda.stream(stream):
         g_full.replay()
     stream.synchronize()
-
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -311,87 +334,176 @@ def run_ours(args, rank, world, local):
         torch.distributed.barrier()
     ms_total = ev0.elapsed_time(ev1)
     clk = clocks.stop(t0, t1)
-    assert fm.flint_moe_status(ws, stream) == fm.FLINT_OK
+    assert fm.flint_moe_status(w.ws, stream) == fm.FLINT_OK
+    del g_full, g_rem
+    (ms_total,) = max_over_ranks([ms_total], device=f"cuda:{local}")
+    return ms_total, clk
 
-    # ---- end to end through the C ABI with host buffers (pinned), eager
-    x_host = [x.cpu().pin_memory() for x in xs]
-    out_host = [torch.empty(M, H, dtype=torch.bfloat16).pin_memory() for _ in xs]
-    K_e2e = min(K, 2000)
+
+def expert_load(w: Workload) -> dict:
+    """Pairs per expert over the resident batches (one step per layer)."""
+    cnt = torch.zeros(w.E, dtype=torch.int64)
+    for t in w.ids:
+        cnt += torch.bincount(t.reshape(-1).cpu().long(), minlength=w.E)
+    n = int(cnt.sum())
+    top = torch.sort(cnt, descending=True).values
+    return {"pairs": n, "steps": len(w.ids), "per_expert": cnt.tolist(),
+            "max_over_mean": round(float(top[0]) * w.E / max(n, 1), 3),
+            "top8_share": round(float(top[:8].sum()) / max(n, 1), 4),
+            "experts_unused": int((cnt == 0).sum())}
+
+
+def record_of(w: Workload, ms_total: float, steps: int, world: int, clk, peaks) -> dict:
+    """One configuration's timing with its roofline."""
+    M, H, E, k, I, SI = w.M, w.H, w.E, w.k, w.I, w.SI
+    ms_step = ms_total / steps
+    step_s = ms_step / 1e3
+    uniq = [int(torch.unique(t).numel()) for t in w.ids]
+    wb = [synth.weight_bytes(H, E, I, SI, u) for u in uniq]
+    mean_bytes = sum(x["total"] for x in wb) / len(wb)
+    mean_expert_bytes = sum(x["experts"] for x in wb) / len(wb)
+    flops = synth.flops_of(M, H, E, k, I, SI)
+    rec = {"workload": workload_name(w.cfg), "tokens_per_step": M, "steps": steps,
+           "ms_per_step": round(ms_step, 6),
+           "tokens_per_s": round(job_tokens_per_s(M, steps, world, ms_total), 2),
+           "path": {1: "single launch", 2: "decode (3 kernels)", 3: "decode fallback (3 kernels)",
+                    4: "grouped (9 kernels)"}.get(w.path, str(w.path)),
+           "gpu_launches_per_step": launches_per_step(M, w.path),
+           "weight_gbs": round(mean_bytes / step_s / 1e9, 1),
+           "expert_weight_gbs": round(mean_expert_bytes / step_s / 1e9, 1),
+           "tflops": round(flops["total"] / step_s / 1e12, 3),
+           "clocks": clk, "traffic": traffic_record(w.cfg)}
+    if M <= DECODE_MAX_TOKENS:
+        achieved = mean_bytes / step_s / 1e9
+        rec["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                           "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                           "traffic": rec["traffic"], "algorithmic_bytes_per_step": int(mean_bytes),
+                           "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"}
+    else:
+        peak = peaks["bf16_tflops"]
+        total = flops["total"] / step_s / 1e12
+        routed = flops["routed"] / step_s / 1e12
+        rec["roofline"] = {"bound": "tensor", "achieved": round(total, 1), "peak": peak, "unit": "TFLOP/s",
+                           "frac": round(total / peak, 4), "routed_only_tflops": round(routed, 1),
+                           "routed_only_frac": round(routed / peak, 4), "traffic": rec["traffic"],
+                           "algorithmic_flops_per_step": flops["total"],
+                           "routed_flops_per_step": flops["routed"],
+                           "peak_source": peaks["source"] + " (bf16_tflops burst)"}
+    return rec
+
+
+def e2e_of(w: Workload, steps: int, local: int, world: int) -> dict:
+    """End to end through the C ABI from pinned host buffers: every step
+    copies its tokens in and its outputs back inside the timed region."""
+    stream = w.stream
+    x_host = [x.cpu().pin_memory() for x in w.xs]
+    out_host = [torch.empty(w.M, w.H, dtype=torch.bfloat16).pin_memory() for _ in w.xs]
+
+    def run(n):
+        for i in range(n):
+            li = i % w.n_layers
+            w.xs[li].copy_(x_host[li], non_blocking=True)
+            w.step(i, stream)
+            out_host[li].copy_(w.outs[li], non_blocking=True)
+
     with torch.cuda.stream(stream):
-        for i in range(min(50, K_e2e)):
-            li = i % n_layers
-            xs[li].copy_(x_host[li], non_blocking=True)
-            step(i, stream)
-            out_host[li].copy_(outs[li], non_blocking=True)
+        run(min(50, steps))
     stream.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for i in range(K_e2e):
-            li = i % n_layers
-            xs[li].copy_(x_host[li], non_blocking=True)
-            step(i, stream)
-            out_host[li].copy_(outs[li], non_blocking=True)
+        run(steps)
         e1.record(stream)
     stream.synchronize()
-    ms_e2e = e0.elapsed_time(e1) / K_e2e
+    (ms,) = max_over_ranks([e0.elapsed_time(e1) / steps], device=f"cuda:{local}")
+    return {"value": round(w.M * world / (ms / 1e3), 2), "unit": "tokens/s",
+            "h2d_bytes_per_step": w.M * w.H * 2, "d2h_bytes_per_step": w.M * w.H * 2,
+            "ms_per_step": round(ms, 6), "steps": steps}
 
-    # ---- max over ranks
-    ms_total, ms_e2e = max_over_ranks([ms_total, ms_e2e], device=dev)
-    ms_step = ms_total / K
 
-    tokens_per_s = job_tokens_per_s(M, K, world, ms_total)
-    e2e_tokens_per_s = M * world / (ms_e2e / 1e3)
+def run_ours(args, rank, world, local):
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
     peaks = load_peaks()
-    mean_bytes = sum(w["total"] for w in wb) / len(wb)
-    mean_expert_bytes = sum(w["experts"] for w in wb) / len(wb)
-    step_s = ms_step / 1e3
-    decode = M <= DECODE_MAX_TOKENS
-    if decode:
-        achieved = mean_bytes / step_s / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": traffic_record(cfg),
-                "kernel": "whole step: router+top-k -> gate/up (+shared) -> down+combine "
-                          "(3 launches chained by programmatic dependent launch; the gate/up "
-                          "and down kernels overlap the router, so the step is timed whole)",
-                "algorithmic_bytes_per_step": int(mean_bytes),
-                "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"}
-    else:
-        achieved = flops["total"] / step_s / 1e12
-        peak = peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic_record(cfg),
-                "kernel": "whole step: router, grouping, gather, grouped tcgen05 GEMM1 "
-                          "(+shared), GEMM2 (+shared), combine (9 launches)",
-                "algorithmic_flops_per_step": flops["total"],
-                "peak_source": peaks["source"] + " (bf16_tflops burst)"}
+    cfg = args.config
+    M = synth.CONFIGS[cfg][0]
+    n_layers = args.layers or (16 if M <= DECODE_MAX_TOKENS else 2)
+    w = Workload(cfg, dev, rank, n_layers)
+    K = args.steps
+    ms_total, clk = time_workload(w, K, args.warmup, world, local)
+    head = record_of(w, ms_total, K, world, clk, peaks)
+    e2e = e2e_of(w, min(K, 2000), local, world)
+    rl = head["roofline"]
+    rl["kernel"] = ("whole step: " + head["path"] + " (the kernels of a step overlap through "
+                    "programmatic dependent launch, so the step is timed whole)")
     res = {
-        "metric": METRIC, "value": round(tokens_per_s, 2), "unit": "tokens/s", "n_gpus": world,
-        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
+        "metric": METRIC, "value": head["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; NVFP4-quantised N(0,0.02) experts, N(0,1) tokens)",
-        "config": {"workload": workload_name(cfg), "global_batch": M * world, "tokens_per_step": M,
+        "config": {"workload": head["workload"], "global_batch": M * world, "tokens_per_step": M,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "layers_rotated": n_layers,
-                   "l2": f"weights of {n_layers} layers rotate ({sum(l.expert_bytes() * E for l in layers) / 1e9:.1f} GB resident), step working set streams from HBM"},
-        "weight_gbs": round(mean_bytes / step_s / 1e9, 1),
-        "expert_weight_gbs": round(mean_expert_bytes / step_s / 1e9, 1),
-        "tflops": round(flops["total"] / step_s / 1e12, 3),
-        "roofline": roof,
-        "e2e": {"value": round(e2e_tokens_per_s, 2), "unit": "tokens/s",
-                "h2d_bytes_per_step": M * H * 2, "d2h_bytes_per_step": M * H * 2,
-                "ms_per_step": round(ms_e2e, 6), "steps": K_e2e},
-        "gpu_launches": K * launches_per_step(M),
+                   "l2": f"weights of {n_layers} layers rotate "
+                         f"({sum(l.expert_bytes() * w.E for l in w.layers) / 1e9:.1f} GB resident), "
+                         "each step's working set streams from HBM"},
+        "weight_gbs": head["weight_gbs"], "expert_weight_gbs": head["expert_weight_gbs"],
+        "tflops": head["tflops"], "path": head["path"],
+        "roofline": rl, "e2e": e2e,
+        "gpu_launches": K * head["gpu_launches_per_step"],
         "clocks": clk,
     }
-    return res, xs, layers
+    if args.sweep:
+        # the rest of the metric: the decode batch sweep and the large-batch
+        # workloads, each timed the same way (decode shapes share the
+        # headline's resident layers)
+        recs = {}
+        for c in SWEEP:
+            Mc = synth.CONFIGS[c][0]
+            if Mc <= DECODE_MAX_TOKENS:
+                wc = Workload(c, dev, rank, n_layers, layers=w.layers)
+                steps_c, warm_c = 2000, 50
+            else:
+                wc = Workload(c, dev, rank, 2)
+                steps_c, warm_c = (20, 3) if Mc <= 4096 else (10, 3)
+            ms_c, clk_c = time_workload(wc, steps_c, warm_c, world, local)
+            r = record_of(wc, ms_c, steps_c, world, clk_c, peaks)
+            if c.startswith("skew") or c.startswith("prefill"):
+                r["expert_load"] = expert_load(wc)
+            r["gpu_launches"] = steps_c * r["gpu_launches_per_step"]
+            recs[c] = r
+            del wc
+            torch.cuda.empty_cache()
+        res["records"] = recs
+    return res
 
 
-def cpu_baseline(cfg: str, n_tokens: int = 384, seed: int = 5):
-    """The oracle on a bounded sample: n_tokens tokens of the configuration's
-    layer shape (one layer), all host cores (OpenMP over tokens); 384 tokens
-    are about 25 s of CPU work on 16 cores."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the
+    architecture)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                v = line.split(":", 1)[1].strip()
+                if v and not v.isdigit():
+                    return v
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+def cpu_baseline(cfg: str, n_tokens: int = 384, n_tokens_1t: int = 32, seed: int = 5):
+    """The oracle on a bounded sample of the configuration's layer shape (one
+    layer; its per-token work does not depend on M): n_tokens tokens on all
+    host cores (OpenMP over tokens), and n_tokens_1t tokens on one thread."""
     import oracle
     M, H, E, k, I, SI = synth.CONFIGS[cfg]
     scale = synth.zipf_router_scale(E) if cfg.startswith("skew") else None
@@ -400,13 +512,18 @@ def cpu_baseline(cfg: str, n_tokens: int = 384, seed: int = 5):
     layer = synth.make_layer(H, E, I, SI, gen, router_row_scale=scale)
     oracle.build()
     oracle.forward(x[:1], layer, k)  # warm
-    t0 = time.perf_counter()
-    oracle.forward(x, layer, k)
-    dt = time.perf_counter() - t0
     cores = oracle.max_threads()
+    t0 = time.perf_counter()
+    oracle.forward(x, layer, k, nthreads=cores)
+    dt = time.perf_counter() - t0
+    t1 = time.perf_counter()
+    oracle.forward(x[:n_tokens_1t], layer, k, nthreads=1)
+    dt1 = time.perf_counter() - t1
     return {"value": round(n_tokens / dt, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n_tokens} tokens of one {cfg} layer (M-independent per-token work), "
-                      f"{dt:.1f} s wall on {cores} threads"}
+            "cpu_model": cpu_model(),
+            "sample": f"{n_tokens} tokens of one {cfg} layer, {dt:.1f} s wall on {cores} threads",
+            "one_thread": {"value": round(n_tokens_1t / dt1, 3), "unit": "tokens/s", "cores": 1,
+                           "sample": f"{n_tokens_1t} tokens of the same layer, {dt1:.1f} s on 1 thread"}}
 
 
 def run_reference(args):
@@ -467,7 +584,9 @@ def main():
         return
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
-    res, xs, layers = run_ours(args, rank, world, local)
+    if args.config != "decode1":
+        args.sweep = False  # the records belong to the headline line
+    res = run_ours(args, rank, world, local)
     if world > 1:
         torch.distributed.barrier()
     if rank == 0:

@@ -137,6 +137,32 @@ int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13,
                       int32_t* ids_out, float* tw_out, void* workspace, size_t workspace_bytes,
                       flint_stream_t stream);
 
+/* The decode MoE block with its add-RMSNorm prologue: "flint_moe_ll" on the
+ * page above.  residual' = attn_out + residual and x = rms_norm(residual')
+ * are formed as norm.fused_add_rms_norm (_add_rms_norm on that page): from
+ * the unrounded fp32 sum s = a + r, residual' = bf16(s),
+ * v = sum_h(s^2) / H + eps (the sum of squares as the exact sum rounded once
+ * to fp32), inv = 1 / sqrt(v) rounded once to fp32, xn = bf16((s * inv) * w);
+ * then the MoE block of flint_moe_forward runs on xn.
+ *
+ *   attn_out, residual  bf16 [M, H]   (inputs, not modified)
+ *   ln_weight           bf16 [H]      norm weight
+ *   eps                 0 <= eps <= 1
+ *   residual_out        bf16 [M, H]   (output) residual'
+ *   xn_out              bf16 [M, H]   (optional output) the normalised rows;
+ *                                      NULL keeps them in the workspace
+ *   the other arguments as for flint_moe_forward; out is the MoE output.
+ * One more kernel (one warp per token) runs ahead of the block's kernels,
+ * chained to them with programmatic dependent launch.  The workspace is the
+ * one flint_moe_workspace_bytes(shape) sizes. */
+int flint_moe_forward_add_norm(const void* attn_out, const void* residual, const void* ln_weight,
+                               float eps, const void* router_w, const uint8_t* w13,
+                               const uint8_t* w13_sf, const float* w13_gs, const uint8_t* w2,
+                               const uint8_t* w2_sf, const float* w2_gs, const void* shared_gu,
+                               const void* shared_down, const flint_moe_shape* shape, void* out,
+                               void* residual_out, void* xn_out, int32_t* ids_out, float* tw_out,
+                               void* workspace, size_t workspace_bytes, flint_stream_t stream);
+
 /* Routing without caller memory: the same kernel, numerics and outputs as
  * flint_moe_route, but its intermediates live in a fixed scratch array that
  * the library itself holds in device memory (2 MiB per device, a file-scope

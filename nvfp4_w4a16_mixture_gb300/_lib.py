@@ -33,7 +33,8 @@ FLINT_PATH_GROUPED = 4
 EXPORTED = ("flint_moe_workspace_bytes", "flint_moe_route", "flint_moe_forward",
             "flint_moe_route_noalloc", "flint_moe_route_noalloc_bytes",
             "flint_moe_route_noalloc_capacity", "flint_moe_status", "flint_moe_strerror",
-            "flint_moe_debug_fault", "flint_moe_plan", "flint_moe_prefer_path")
+            "flint_moe_debug_fault", "flint_moe_plan", "flint_moe_prefer_path",
+            "flint_moe_forward_add_norm")
 
 
 class FlintMoEError(RuntimeError):
@@ -69,6 +70,9 @@ def load() -> ctypes.CDLL:
             lib.flint_moe_route.argtypes = [P, P, S, P, P, P, ctypes.c_size_t, P]
             lib.flint_moe_forward.restype = ctypes.c_int
             lib.flint_moe_forward.argtypes = [P] * 10 + [S, P, P, P, P, ctypes.c_size_t, P]
+            lib.flint_moe_forward_add_norm.restype = ctypes.c_int
+            lib.flint_moe_forward_add_norm.argtypes = ([P, P, P, ctypes.c_float] + [P] * 9 +
+                                                       [S, P, P, P, P, P, P, ctypes.c_size_t, P])
             lib.flint_moe_route_noalloc.restype = ctypes.c_int
             lib.flint_moe_route_noalloc.argtypes = [P, P, S, P, P, P]
             lib.flint_moe_route_noalloc_bytes.restype = ctypes.c_size_t
@@ -150,6 +154,25 @@ def flint_moe_forward(x, router_w, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, shared
         raise FlintMoEError(rc, "flint_moe_forward")
 
 
+def flint_moe_forward_add_norm(attn_out, residual, ln_weight, eps: float, router_w, w13, w13_sf,
+                               w13_gs, w2, w2_sf, w2_gs, shared_gu, shared_down, top_k: int, out,
+                               residual_out, workspace, xn_out=None, ids_out=None, tw_out=None,
+                               *, I: int, SI: int, stream=None) -> None:
+    """The MoE block with its add-RMSNorm prologue (flint_moe_ll): writes out
+    and residual_out (and xn_out when given)."""
+    M, H = attn_out.shape
+    E = router_w.shape[0]
+    s = _shape(M, H, E, top_k, I, SI)
+    rc = load().flint_moe_forward_add_norm(
+        _ptr(attn_out), _ptr(residual), _ptr(ln_weight), float(eps), _ptr(router_w), _ptr(w13),
+        _ptr(w13_sf), _ptr(w13_gs), _ptr(w2), _ptr(w2_sf), _ptr(w2_gs), _ptr(shared_gu),
+        _ptr(shared_down), ctypes.byref(s), _ptr(out), _ptr(residual_out), _ptr(xn_out),
+        _ptr(ids_out), _ptr(tw_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    if rc != FLINT_OK:
+        raise FlintMoEError(rc, "flint_moe_forward_add_norm")
+
+
 def flint_moe_route_noalloc(x, router_w, top_k: int, ids, tw, stream=None) -> None:
     """flint_moe_route without a caller workspace: the library's fixed
     static scratch holds the intermediates (see include/flint_moe.h for the
@@ -213,6 +236,27 @@ def alloc_workspace(M: int, H: int, E: int, top_k: int, I: int, SI: int,
             code = FLINT_ERR_UNSUPPORTED
         raise FlintMoEError(code, "alloc_workspace")
     return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def forward_add_norm_layer(attn_out, residual, ln_weight, eps: float, layer, top_k: int, workspace=None,
+                           out=None, residual_out=None, xn_out=None, ids_out=None, tw_out=None,
+                           stream=None):
+    """flint_moe_forward_add_norm on a synth.MoELayer-like object; returns
+    (out, residual_out)."""
+    M, H = attn_out.shape
+    if workspace is None:
+        workspace = alloc_workspace(M, H, layer.E, top_k, layer.I, layer.SI, attn_out.device)
+    if out is None:
+        out = torch.empty_like(attn_out)
+    if residual_out is None:
+        residual_out = torch.empty_like(residual)
+    flint_moe_forward_add_norm(attn_out, residual, ln_weight, eps, layer.router_w, layer.w13,
+                               layer.w13_sf, layer.w13_gs, layer.w2, layer.w2_sf, layer.w2_gs,
+                               layer.shared_gu if layer.SI else None,
+                               layer.shared_down if layer.SI else None, top_k, out, residual_out,
+                               workspace, xn_out=xn_out, ids_out=ids_out, tw_out=tw_out, I=layer.I,
+                               SI=layer.SI, stream=stream)
+    return out, residual_out
 
 
 def forward_layer(x, layer, top_k: int, workspace=None, out=None, ids_out=None, tw_out=None,

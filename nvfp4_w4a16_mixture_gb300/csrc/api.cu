@@ -84,6 +84,7 @@ WsLayout ws_layout(const flint_moe_shape& s) {
   L.st_count = take(16);
   L.x16 = take(M <= (size_t)kX16MaxTokens ? 2 * M * H : 16);
   L.x16_exp = take(4 * M);
+  L.xn = take(2 * M * H);
   L.total = off;
   return L;
 }
@@ -109,6 +110,7 @@ Ws ws_pointers(void* base, const WsLayout& L) {
   w.act = reinterpret_cast<uint16_t*>(b + L.act);
   w.x16 = reinterpret_cast<uint16_t*>(b + L.x16);
   w.x16_exp = reinterpret_cast<int*>(b + L.x16_exp);
+  w.xn = reinterpret_cast<uint16_t*>(b + L.xn);
   w.sact = reinterpret_cast<uint16_t*>(b + L.sact);
   w.y = reinterpret_cast<uint16_t*>(b + L.y);
   w.ys = reinterpret_cast<uint16_t*>(b + L.ys);
@@ -172,14 +174,12 @@ int flint_moe_route(const void* x, const void* router_w, const flint_moe_shape* 
   return FLINT_OK;
 }
 
-int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13, const uint8_t* w13_sf,
-                      const float* w13_gs, const uint8_t* w2, const uint8_t* w2_sf,
-                      const float* w2_gs, const void* shared_gu, const void* shared_down,
-                      const flint_moe_shape* shape, void* out, int32_t* ids_out, float* tw_out,
-                      void* workspace, size_t workspace_bytes, flint_stream_t stream) {
-  if (!shape_valid(shape)) return FLINT_ERR_INVALID_ARG;
-  if (!shape_supported(shape)) return FLINT_ERR_UNSUPPORTED;
-  if (shape->M == 0) return FLINT_OK;  // an empty batch: nothing to launch
+// Argument checks of the forward entry points (x: the rows the MoE block reads).
+static int check_forward(const void* x, const void* router_w, const uint8_t* w13, const uint8_t* w13_sf,
+                         const float* w13_gs, const uint8_t* w2, const uint8_t* w2_sf, const float* w2_gs,
+                         const void* shared_gu, const void* shared_down, const flint_moe_shape* shape,
+                         void* out, int32_t* ids_out, float* tw_out, void* workspace,
+                         size_t workspace_bytes) {
   if (!x || !router_w || !w13 || !w13_sf || !w13_gs || !w2 || !w2_sf || !w2_gs || !out)
     return FLINT_ERR_INVALID_ARG;
   if (shape->SI > 0 && (!shared_gu || !shared_down)) return FLINT_ERR_INVALID_ARG;
@@ -192,24 +192,12 @@ int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13, c
   if ((ids_out && !aligned(ids_out, 4)) || (tw_out && !aligned(tw_out, 4)))
     return FLINT_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, 256)) return FLINT_ERR_WORKSPACE;
-  const WsLayout L = ws_layout(*shape);
-  if (workspace_bytes < L.total) return FLINT_ERR_WORKSPACE;
+  if (workspace_bytes < ws_layout(*shape).total) return FLINT_ERR_WORKSPACE;
+  return FLINT_OK;
+}
 
-  MoEArgs a{};
-  a.x = static_cast<const uint16_t*>(x);
-  a.router_w = static_cast<const uint16_t*>(router_w);
-  a.w13 = w13; a.w13_sf = w13_sf; a.w13_gs = w13_gs;
-  a.w2 = w2; a.w2_sf = w2_sf; a.w2_gs = w2_gs;
-  a.shared_gu = static_cast<const uint16_t*>(shared_gu);
-  a.shared_down = static_cast<const uint16_t*>(shared_down);
-  a.out = static_cast<uint16_t*>(out);
-  a.ids_out = ids_out;
-  a.tw_out = tw_out;
-  a.M = shape->M; a.H = shape->H; a.E = shape->E; a.k = shape->top_k; a.I = shape->I; a.SI = shape->SI;
-  a.fault = debug_fault_site();
-  a.ws = ws_pointers(workspace, L);
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-
+// Enqueue the MoE block on rows a.x (arguments checked).
+static int enqueue_forward(MoEArgs& a, const flint_moe_shape* shape, cudaStream_t st) {
   int sms = 0;
   if (device_sms(&sms) != cudaSuccess) return FLINT_ERR_CUDA;
   switch (plan(*shape, sms)) {
@@ -228,6 +216,74 @@ int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13, c
       if (launch_decode_down(a, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
       return FLINT_OK;
   }
+}
+
+static MoEArgs make_args(const void* x, const void* router_w, const uint8_t* w13, const uint8_t* w13_sf,
+                         const float* w13_gs, const uint8_t* w2, const uint8_t* w2_sf, const float* w2_gs,
+                         const void* shared_gu, const void* shared_down, const flint_moe_shape* shape,
+                         void* out, int32_t* ids_out, float* tw_out, void* workspace) {
+  MoEArgs a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.router_w = static_cast<const uint16_t*>(router_w);
+  a.w13 = w13; a.w13_sf = w13_sf; a.w13_gs = w13_gs;
+  a.w2 = w2; a.w2_sf = w2_sf; a.w2_gs = w2_gs;
+  a.shared_gu = static_cast<const uint16_t*>(shared_gu);
+  a.shared_down = static_cast<const uint16_t*>(shared_down);
+  a.out = static_cast<uint16_t*>(out);
+  a.ids_out = ids_out;
+  a.tw_out = tw_out;
+  a.M = shape->M; a.H = shape->H; a.E = shape->E; a.k = shape->top_k; a.I = shape->I; a.SI = shape->SI;
+  a.fault = debug_fault_site();
+  a.ws = ws_pointers(workspace, ws_layout(*shape));
+  return a;
+}
+
+int flint_moe_forward(const void* x, const void* router_w, const uint8_t* w13, const uint8_t* w13_sf,
+                      const float* w13_gs, const uint8_t* w2, const uint8_t* w2_sf,
+                      const float* w2_gs, const void* shared_gu, const void* shared_down,
+                      const flint_moe_shape* shape, void* out, int32_t* ids_out, float* tw_out,
+                      void* workspace, size_t workspace_bytes, flint_stream_t stream) {
+  if (!shape_valid(shape)) return FLINT_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return FLINT_ERR_UNSUPPORTED;
+  if (shape->M == 0) return FLINT_OK;  // an empty batch: nothing to launch
+  const int rc = check_forward(x, router_w, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, shared_gu, shared_down,
+                               shape, out, ids_out, tw_out, workspace, workspace_bytes);
+  if (rc != FLINT_OK) return rc;
+  MoEArgs a = make_args(x, router_w, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, shared_gu, shared_down, shape,
+                        out, ids_out, tw_out, workspace);
+  return enqueue_forward(a, shape, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int flint_moe_forward_add_norm(const void* attn_out, const void* residual, const void* ln_weight, float eps,
+                               const void* router_w, const uint8_t* w13, const uint8_t* w13_sf,
+                               const float* w13_gs, const uint8_t* w2, const uint8_t* w2_sf,
+                               const float* w2_gs, const void* shared_gu, const void* shared_down,
+                               const flint_moe_shape* shape, void* out, void* residual_out, void* xn_out,
+                               int32_t* ids_out, float* tw_out, void* workspace, size_t workspace_bytes,
+                               flint_stream_t stream) {
+  if (!shape_valid(shape)) return FLINT_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return FLINT_ERR_UNSUPPORTED;
+  if (shape->M == 0) return FLINT_OK;
+  if (!attn_out || !residual || !ln_weight || !residual_out) return FLINT_ERR_INVALID_ARG;
+  if (!aligned(attn_out, 16) || !aligned(residual, 16) || !aligned(ln_weight, 16) ||
+      !aligned(residual_out, 16) || (xn_out && !aligned(xn_out, 16)))
+    return FLINT_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f) || eps > 1.0f) return FLINT_ERR_INVALID_ARG;  // also rejects NaN
+  // the MoE block reads the normalised rows: the caller's xn_out, else the
+  // workspace's region (checked once the workspace is known to be valid)
+  const int rc = check_forward(attn_out, router_w, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, shared_gu,
+                               shared_down, shape, out, ids_out, tw_out, workspace, workspace_bytes);
+  if (rc != FLINT_OK) return rc;
+  MoEArgs a = make_args(nullptr, router_w, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, shared_gu, shared_down,
+                        shape, out, ids_out, tw_out, workspace);
+  uint16_t* xn = xn_out ? static_cast<uint16_t*>(xn_out) : a.ws.xn;
+  a.x = xn;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_add_rms_norm(static_cast<const uint16_t*>(attn_out), static_cast<const uint16_t*>(residual),
+                          static_cast<const uint16_t*>(ln_weight), eps, shape->M, shape->H,
+                          static_cast<uint16_t*>(residual_out), xn, st) != cudaSuccess)
+    return FLINT_ERR_CUDA;
+  return enqueue_forward(a, shape, st);
 }
 
 int flint_moe_plan(const flint_moe_shape* shape) {

@@ -44,6 +44,7 @@ struct WsLayout {
   size_t st_count;     // int32: number of token tiles
   size_t x16;          // f16 [M, H]: x[t] * 2^x16_exp[t], exactly (M <= kX16MaxTokens)
   size_t x16_exp;      // int32 [M]
+  size_t xn;           // bf16 [M, H]: normalised rows (add-RMSNorm entry point)
   size_t total;
 };
 
@@ -87,6 +88,7 @@ struct Ws {  // device pointers into one workspace
   uint16_t* ys;
   uint16_t* x16;
   int* x16_exp;
+  uint16_t* xn;
 };
 
 Ws ws_pointers(void* base, const WsLayout& L);
@@ -142,6 +144,11 @@ cudaError_t launch_decode2(const MoEArgs& a, cudaStream_t st);
 constexpr int kFusedMaxTokens = 8;
 bool fused_supported(const flint_moe_shape& s, int sms);
 cudaError_t launch_fused(const MoEArgs& a, cudaStream_t st, int sms);
+
+// norm.fused_add_rms_norm of rows a + r (add_norm.cu): residual' and xn, both
+// bf16 [M, H]; one warp per token, launched with programmatic dependent launch.
+cudaError_t launch_add_rms_norm(const uint16_t* a, const uint16_t* r, const uint16_t* w, float eps,
+                                int M, int H, uint16_t* res_out, uint16_t* xn, cudaStream_t st);
 
 
 

@@ -62,6 +62,8 @@ def _load():
             lib.oracle_topk.argtypes = [P, i32, i32, i32, P, P]
             lib.oracle_forward.restype = i32
             lib.oracle_forward.argtypes = [P] * 10 + [i32] * 6 + [P, i32] + [P] * 8 + [i32]
+            lib.oracle_add_rms_norm.restype = i32
+            lib.oracle_add_rms_norm.argtypes = [P, P, P, i32, i32, ctypes.c_float, P, P]
             lib.oracle_max_threads.restype = i32
             lib.oracle_max_threads.argtypes = []
             _lib = lib
@@ -184,6 +186,20 @@ def forward(x, layer, top_k: int, tokens=None, intermediates: bool = False, nthr
     if rc != 0:
         raise ValueError("oracle_forward: invalid shape or token list")
     return res
+
+
+def add_rms_norm(a, r, w, eps: float):
+    """norm.fused_add_rms_norm (reading R8) of bf16 rows a + r with bf16
+    weight w [H]: returns (residual' bits, xn bits), both [M, H] uint16."""
+    aa, ra, wa = _np(a, np.uint16), _np(r, np.uint16), _np(w, np.uint16)
+    M, H = aa.shape
+    assert ra.shape == (M, H) and wa.shape == (H,)
+    res = np.empty((M, H), np.uint16)
+    xn = np.empty((M, H), np.uint16)
+    rc = _load().oracle_add_rms_norm(_ptr(aa), _ptr(ra), _ptr(wa), M, H, float(eps), _ptr(res), _ptr(xn))
+    if rc != 0:
+        raise ValueError("oracle_add_rms_norm: invalid shape")
+    return res, xn
 
 
 def max_threads() -> int:

@@ -34,6 +34,13 @@
  *  R6  ranking uses the pages' total order on bf16 bit patterns (numeric
  *      order, except that -0 ranks below +0); equal bit patterns go to the
  *      lower expert index.
+ *  R8  add-RMSNorm (_add_rms_norm on the same page, used by flint_moe_ll):
+ *      s = a + r in fp32, residual' = bf16(s); the sum of squares, whose
+ *      order the page's tree sum leaves open, is the exact sum of the fp32
+ *      squares rounded once to fp32 (as R7); v = sum / H + eps in fp32;
+ *      the page names the reciprocal square root (_rsqrt) without defining
+ *      it: inv = 1 / sqrt(v) correctly rounded to fp32;
+ *      xn = bf16((s * inv) * w), each product one fp32 rounding.
  *  R7  "products are accumulated in fp32" fixes the accumulator's type, not
  *      the order of the additions.  Every expert and shared-expert dot
  *      product therefore takes the order-independent value: the exact sum of
@@ -372,6 +379,35 @@ ORACLE_API int oracle_forward(const uint16_t* x, const uint16_t* wr, const uint8
                   act ? act + (int64_t)i * k * I : NULL, y ? y + (int64_t)i * k * H : NULL,
                   sact ? sact + (int64_t)i * SI : NULL, ys ? ys + (int64_t)i * H : NULL);
   }
+  return 0;
+}
+
+/* norm.fused_add_rms_norm of rows a + r (reading R8): residual' and the
+ * normalised rows xn, both bf16 [M, H]; w is the bf16 norm weight [H]. */
+ORACLE_API int oracle_add_rms_norm(const uint16_t* a, const uint16_t* r, const uint16_t* w, int M,
+                                   int H, float eps, uint16_t* res_out, uint16_t* xn_out) {
+  if (M < 0 || H < 1)
+    return -1;
+  float* s = (float*)malloc(sizeof(float) * (size_t)H);
+  if (!s)
+    return -1;
+  for (int t = 0; t < M; ++t) {
+    const uint16_t* at = a + (int64_t)t * H;
+    const uint16_t* rt = r + (int64_t)t * H;
+    double sq = 0.0; /* squares of fp32 values are exact in double */
+    for (int h = 0; h < H; ++h) {
+      s[h] = bf16_to_f32(at[h]) + bf16_to_f32(rt[h]);
+      res_out[(int64_t)t * H + h] = f32_to_bf16(s[h]);
+      sq += (double)s[h] * (double)s[h];
+    }
+    const float v = (float)sq / (float)H + eps;
+    const float inv = (float)(1.0 / sqrt((double)v));
+    for (int h = 0; h < H; ++h) {
+      const float p = s[h] * inv;
+      xn_out[(int64_t)t * H + h] = f32_to_bf16(p * bf16_to_f32(w[h]));
+    }
+  }
+  free(s);
   return 0;
 }
 

@@ -150,7 +150,7 @@ def test_product_path_does_not_import_oracle():
 def test_workspace_fits_expected_regions(shape):
     M, H, E, k, I, SI = shape
     need = fm.flint_moe_workspace_bytes(*shape)
-    floor = 2 * M * k * (I + H) + 2 * M * (SI + H)  # act, y, sact, ys
+    floor = 2 * M * k * (I + H) + 2 * M * (SI + H) + 2 * M * H  # act, y, sact, ys, xn
     if M > 64:
         floor += 2 * M * k * H  # token rows in sorted pair order (grouped path)
     assert floor <= need <= floor + 4 * 1024 * 1024 + 16 * M * k + 2 * M * E + 272 * E
@@ -190,3 +190,30 @@ def test_plan_is_a_host_query():
     with pytest.raises(fm.FlintMoEError) as ei:
         fm.flint_moe_plan(1, 2048, 128, 0, 768, 768)
     assert ei.value.code == fm.FLINT_ERR_INVALID_ARG
+
+
+def test_forward_add_norm_validation_is_synchronous():
+    """The add-RMSNorm entry point checks its extra arguments before any CUDA
+    call (fake, never-dereferenced addresses)."""
+    lib = fm.load()
+    shape = (2, 256, 8, 2, 128, 128)
+    need = fm.flint_moe_workspace_bytes(*shape)
+    f = [0x10000 * (i + 1) for i in range(20)]
+    s = _lib.flint_moe_shape(*shape)
+
+    def call(attn=f[0], resid=f[1], lnw=f[2], eps=1e-6, res_out=f[14], xn_out=None, ws=f[17], shp=s):
+        return lib.flint_moe_forward_add_norm(attn, resid, lnw, eps, *f[3:12], ctypes.byref(shp), f[13],
+                                              res_out, xn_out, None, None, ws, need, None)
+
+    assert call(res_out=None) == fm.FLINT_ERR_INVALID_ARG
+    assert call(resid=None) == fm.FLINT_ERR_INVALID_ARG
+    assert call(lnw=f[2] + 8) == fm.FLINT_ERR_INVALID_ARG
+    assert call(eps=float("nan")) == fm.FLINT_ERR_INVALID_ARG
+    assert call(eps=-1.0) == fm.FLINT_ERR_INVALID_ARG
+    assert call(xn_out=f[15] + 4) == fm.FLINT_ERR_INVALID_ARG
+    assert call(ws=None) == fm.FLINT_ERR_WORKSPACE
+    odd = _lib.flint_moe_shape(2, 192, 8, 2, 128, 128)
+    assert call(shp=odd) == fm.FLINT_ERR_UNSUPPORTED
+    empty = _lib.flint_moe_shape(0, 256, 8, 2, 128, 128)
+    assert lib.flint_moe_forward_add_norm(*([None] * 3), 1e-6, *([None] * 9), ctypes.byref(empty),
+                                          *([None] * 6), 0, None) == fm.FLINT_OK

@@ -405,3 +405,37 @@ def test_decode_f16_copy_guard_with_an_unrepresentable_value(decode_layer):
     assert fm.flint_moe_status(ws) == fm.FLINT_OK
     compare(synth.make_x(16, layer.H, gen, "cuda"), layer, k, ws=ws)
     assert fm.flint_moe_status(ws) == fm.FLINT_OK
+
+
+# ------------------------------------------------------- add-RMSNorm entry
+@pytest.mark.parametrize("M", [1, 16, 64, 300])
+def test_forward_add_norm(decode_layer, M):
+    """flint_moe_forward_add_norm: residual' and the normalised rows bit for
+    bit against the oracle's add_rms_norm, the MoE output of those rows within
+    the rule (M = 300 runs the grouped path on a smaller layer)."""
+    if M <= 64:
+        _, layer, k = decode_layer
+    else:
+        x0, layer = synth.make_problem(M, 384, 24, 4, 256, 128, seed=31, device="cuda")
+        k = 4
+    H = layer.H
+    g = torch.Generator(device="cuda").manual_seed(600 + M)
+    attn = synth.make_x(M, H, g, "cuda")
+    resid = (synth.make_x(M, H, g, "cuda").float() * 3).to(torch.bfloat16)
+    lnw = (1 + 0.1 * torch.randn(H, generator=g, device="cuda")).to(torch.bfloat16)
+    eps = 1e-6
+    ws = fm.alloc_workspace(M, H, layer.E, k, layer.I, layer.SI)
+    xn = torch.empty_like(attn)
+    ids = torch.empty(M, k, dtype=torch.int32, device="cuda")
+    tw = torch.empty(M, k, dtype=torch.float32, device="cuda")
+    out, res_out = fm.forward_add_norm_layer(attn, resid, lnw, eps, layer, k, workspace=ws, xn_out=xn,
+                                             ids_out=ids, tw_out=tw)
+    assert fm.flint_moe_status(ws) == fm.FLINT_OK
+    r_res, r_xn = oracle.add_rms_norm(attn.cpu(), resid.cpu(), lnw.cpu(), eps)
+    assert np.array_equal(bits(res_out), r_res)
+    assert np.array_equal(bits(xn), r_xn)
+    xn_t = torch.from_numpy(r_xn.view(np.int16)).view(torch.bfloat16)
+    compare(xn_t.cuda(), layer, k, gpu=(out, ids, tw))
+    # the normalised rows may also stay in the workspace
+    out2, res2 = fm.forward_add_norm_layer(attn, resid, lnw, eps, layer, k, workspace=ws)
+    assert torch.equal(out2, out) and torch.equal(res2, res_out)

@@ -365,3 +365,69 @@ def test_shared_silu_is_the_division_form():
     want_mul = bf16_bits((mul * uv).astype(np.float32))
     assert (want_div[:2] != want_mul[:2]).all()  # the constructed rows separate the forms
     assert np.array_equal(r["sact"][0], want_div)
+
+
+# ------------------------------------------------------------ add-RMSNorm
+def _bf16(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.bfloat16).contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _norm_inputs(M, H, seed):
+    g = torch.Generator().manual_seed(seed)
+    a = torch.randn(M, H, generator=g).to(torch.bfloat16)
+    r = (torch.randn(M, H, generator=g) * 2).to(torch.bfloat16)
+    w = (1 + 0.1 * torch.randn(H, generator=g)).to(torch.bfloat16)
+    return a, r, w
+
+
+def test_add_rms_norm_residual_is_the_bf16_sum():
+    """residual' = bf16(a + r) with the sum in fp32: torch's fp32 add and
+    bf16 cast (library)."""
+    a, r, w = _norm_inputs(7, 384, 1)
+    res, _ = oracle.add_rms_norm(a, r, w, 1e-6)
+    assert np.array_equal(res, _bf16(a.float() + r.float()))
+
+
+def test_add_rms_norm_matches_float64():
+    """xn against an independent float64 derivation (one rounding, to bf16,
+    at the end), within the parity rule."""
+    a, r, w = _norm_inputs(16, 2048, 2)
+    _, xn = oracle.add_rms_norm(a, r, w, 1e-6)
+    s = a.double() + r.double()
+    inv = 1.0 / torch.sqrt((s * s).mean(dim=1, keepdim=True) + 1e-6)
+    want = _bf16(s * inv * w.double())
+    st = check_bf16(xn, want)
+    assert st["n_exact"] > 0.95 * st["n"]
+
+
+def test_add_rms_norm_closed_forms():
+    """Constant rows c (r = 0, w = 1, eps = 0) normalise to sign(c) exactly;
+    w = 2 doubles every output and scaling a, r by 2 changes nothing (both
+    exact in binary floating point)."""
+    H = 256
+    c = torch.tensor([1.5, -3.0, 0.25, -0.75]).repeat_interleave(H).reshape(4, H)
+    a = c.to(torch.bfloat16)
+    z = torch.zeros_like(a)
+    one = torch.ones(H, dtype=torch.bfloat16)
+    _, xn = oracle.add_rms_norm(a, z, one, 0.0)
+    assert np.array_equal(bits_to_f64(xn), np.sign(c.numpy()).astype(np.float64))
+    a2, r2, w2 = _norm_inputs(5, 512, 3)
+    _, x1 = oracle.add_rms_norm(a2, r2, w2, 0.0)
+    _, x2 = oracle.add_rms_norm((a2.float() * 2).to(torch.bfloat16), (r2.float() * 2).to(torch.bfloat16), w2, 0.0)
+    assert np.array_equal(x1, x2)
+    _, x3 = oracle.add_rms_norm(a2, r2, (w2.float() * 2).to(torch.bfloat16), 0.0)
+    assert np.array_equal(bits_to_f64(x3), 2 * bits_to_f64(x1))
+
+
+def test_add_rms_norm_eps_enters_before_the_root():
+    """Zero rows: s = 0 everywhere, v = eps, inv = 1 / sqrt(eps) and xn = 0;
+    a row of all-equal 2^-10 with eps = 3 * 2^-20 gives v = 2^-18, so
+    inv = 2^9 and xn = 2^-1 exactly (eps added after the mean)."""
+    H = 128
+    z = torch.zeros(1, H, dtype=torch.bfloat16)
+    one = torch.ones(H, dtype=torch.bfloat16)
+    _, xn = oracle.add_rms_norm(z, z, one, 1e-5)
+    assert (bits_to_f64(xn) == 0).all()
+    a = torch.full((1, H), 2.0 ** -10).to(torch.bfloat16)
+    _, xn = oracle.add_rms_norm(a, z, one, 3 * 2.0 ** -20)
+    assert (bits_to_f64(xn) == 0.5).all()

@@ -152,38 +152,71 @@ FLINT_DEV void mmah(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t
   mma_f16_16816(d, a[0], a[1], a[2], a[3], b0, b1);
 }
 
+// Largest biased exponent field among the 8 bf16 values of one word.
+FLINT_DEV int max_exp_word(const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  int m = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m = max(m, (int)max((w[i] >> 23) & 0xFFu, (w[i] >> 7) & 0xFFu));
+  return m;
+}
+
+// split_hi_lo of one word with the rounding constant c2 of the grid.
+FLINT_DEV void split_word(const uint4& v, uint32_t c2, uint4& hi, uint4& lo) {
+  hi.x = bf2_sub(bf2_add(v.x, c2), c2);
+  hi.y = bf2_sub(bf2_add(v.y, c2), c2);
+  hi.z = bf2_sub(bf2_add(v.z, c2), c2);
+  hi.w = bf2_sub(bf2_add(v.w, c2), c2);
+  lo.x = bf2_sub(v.x, hi.x);
+  lo.y = bf2_sub(v.y, hi.y);
+  lo.z = bf2_sub(v.z, hi.z);
+  lo.w = bf2_sub(v.w, hi.w);
+}
+
+// The rounding constant C = 1.5 * 2^(ef - 125) of split_hi_lo, twice.
+FLINT_DEV uint32_t split_const(int ef) {
+  ef = min(max(ef, 1), 252);
+  const uint32_t cb = ((uint32_t)(ef + 2) << 7) | 0x40u;
+  return cb | (cb << 16);
+}
+
 // One 128-K slice of a 16-row BF16 tile (rows g, g + 8 in natural order at
 // ra / rb, this lane's 32 K at offset 32 t of the slice) against xb: the
 // weights are split per row over the slice, w_hi * x_hi accumulates exactly
 // in one chained mma (products of two <= 6-bit integers, 128 of them), the
-// rest goes to C.
+// rest goes to C.  The grids come first (one pass over the words); the
+// words are then split one at a time, so few registers stay live.
 FLINT_DEV void slice_bf16_exact(float (&S)[4], float (&C)[4], const uint16_t* ra, const uint16_t* rb,
                                 const uint4 (&xb)[4]) {
-  uint4 xh[4], xl[4];
-  split_column(xb, xh, xl);
-  uint4 wa[4], wb[4];
+  int ex = 0, ea = 0, eb = 0;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    wa[q] = *reinterpret_cast<const uint4*>(ra + 8 * q);
-    wb[q] = *reinterpret_cast<const uint4*>(rb + 8 * q);
+    ex = max(ex, max_exp_word(xb[q]));
+    ea = max(ea, max_exp_word(*reinterpret_cast<const uint4*>(ra + 8 * q)));
+    eb = max(eb, max_exp_word(*reinterpret_cast<const uint4*>(rb + 8 * q)));
   }
-  int ea = max_exp_field(wa), eb = max_exp_field(wb);
-  ea = max(ea, __shfl_xor_sync(0xffffffffu, ea, 1));
-  ea = max(ea, __shfl_xor_sync(0xffffffffu, ea, 2));
-  eb = max(eb, __shfl_xor_sync(0xffffffffu, eb, 1));
-  eb = max(eb, __shfl_xor_sync(0xffffffffu, eb, 2));
-  uint4 wah[4], wal[4], wbh[4], wbl[4];
-  split_hi_lo(wa, ea, wah, wal);
-  split_hi_lo(wb, eb, wbh, wbl);
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    ex = max(ex, __shfl_xor_sync(0xffffffffu, ex, o));
+    ea = max(ea, __shfl_xor_sync(0xffffffffu, ea, o));
+    eb = max(eb, __shfl_xor_sync(0xffffffffu, eb, o));
+  }
+  const uint32_t cx = split_const(ex), ca = split_const(ea), cb = split_const(eb);
   float hh[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ap[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
+    const uint4 wa = *reinterpret_cast<const uint4*>(ra + 8 * q);
+    const uint4 wb = *reinterpret_cast<const uint4*>(rb + 8 * q);
+    uint4 xh, xl, wah, wal, wbh, wbl;
+    split_word(xb[q], cx, xh, xl);
+    split_word(wa, ca, wah, wal);
+    split_word(wb, cb, wbh, wbl);
     uint32_t bh[2][2], bl[2][2], ah[2][4], alo[2][4], aw[2][4];
-    b_regs(xh[q], bh);
-    b_regs(xl[q], bl);
-    a_regs_bf16(wah[q], wbh[q], ah);
-    a_regs_bf16(wal[q], wbl[q], alo);
-    a_regs_bf16(wa[q], wb[q], aw);
+    b_regs(xh, bh);
+    b_regs(xl, bl);
+    a_regs_bf16(wah, wbh, ah);
+    a_regs_bf16(wal, wbl, alo);
+    a_regs_bf16(wa, wb, aw);
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       mma16(hh, ah[r], bh[r][0], bh[r][1]);

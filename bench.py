@@ -421,6 +421,72 @@ def e2e_of(w: Workload, steps: int, local: int, world: int) -> dict:
             "ms_per_step": round(ms, 6), "steps": steps}
 
 
+def kernel_spans(w: Workload, steps: int = 40) -> dict:
+    """Per-kernel spans of `steps` eager steps (each timed alone: the buffer
+    is zeroed, the step runs, its spans are read): mean ns per kernel from its
+    first CTA's start to its last warp's exit, the step's span, and each
+    kernel's share of the sum of spans."""
+    fm = w.fm
+    buf = torch.zeros(fm._lib.SPAN_KERNELS * fm._lib.SPAN_CTAS * 2, dtype=torch.int64, device=w.ws.device)
+    acc, step_ns = {}, []
+    fm.flint_moe_record_spans(buf)
+    try:
+        for i in range(steps):
+            buf.zero_()
+            with torch.cuda.stream(w.stream):
+                w.step(i, w.stream)
+            w.stream.synchronize()
+            sp = fm.spans_of(buf)
+            if not sp:
+                continue
+            t0 = min(v[0] for v in sp.values())
+            step_ns.append(max(v[1] for v in sp.values()) - t0)
+            for name, (a, b) in sp.items():
+                acc.setdefault(name, []).append((b - a, a - t0))
+    finally:
+        fm.flint_moe_record_spans(None)
+    tot = sum(sum(d for d, _ in v) / len(v) for v in acc.values()) or 1
+    out = {name: {"us": round(sum(d for d, _ in v) / len(v) / 1e3, 3),
+                  "start_us": round(sum(o for _, o in v) / len(v) / 1e3, 3),
+                  "share": round(sum(d for d, _ in v) / len(v) / tot, 4)} for name, v in acc.items()}
+    return {"steps": len(step_ns), "step_span_us": round(sum(step_ns) / max(len(step_ns), 1) / 1e3, 3),
+            "kernels": out,
+            "how": "globaltimer at each CTA's start and each warp's exit (flint_moe_record_spans), "
+                   "eager steps each timed alone"}
+
+
+def dominant_roofline(w: Workload, spans: dict, peaks) -> dict | None:
+    """The dominant kernel against its own roofline, from its measured span:
+    the decode gate/up kernel's weight bytes (routed w13 + scales of the
+    step's experts, shared gate/up) over its span; the grouped GEMM1's flops
+    over its span."""
+    ks = spans.get("kernels", {})
+    if not ks:
+        return None
+    name = max(ks, key=lambda n: ks[n]["us"])
+    M, H, E, k, I, SI = w.M, w.H, w.E, w.k, w.I, w.SI
+    us = ks[name]["us"]
+    if name in ("gate_up", "single_launch", "down") and M <= DECODE_MAX_TOKENS:
+        uniq = sum(int(torch.unique(t).numel()) for t in w.ids) / len(w.ids)
+        if name == "gate_up":
+            b = uniq * (2 * I * H // 2 + 2 * I * H // 16) + 2 * SI * H * 2
+        elif name == "down":
+            b = uniq * (H * I // 2 + H * I // 16) + SI * H * 2
+        else:
+            b = synth.weight_bytes(H, E, I, SI, int(round(uniq)))["total"]
+        ach = b / (us * 1e-6) / 1e9
+        return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "span_us": us,
+                "algorithmic_bytes": int(b)}
+    if name in ("gemm1", "gemm2"):
+        f = 2 * M * k * (2 * I * H if name == "gemm1" else H * I) + 2 * M * (2 * SI * H if name == "gemm1" else SI * H)
+        ach = f / (us * 1e-6) / 1e12
+        return {"kernel": name, "bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "span_us": us,
+                "algorithmic_flops": int(f)}
+    return {"kernel": name, "span_us": us}
+
+
 def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
@@ -433,7 +499,9 @@ def run_ours(args, rank, world, local):
     ms_total, clk = time_workload(w, K, args.warmup, world, local)
     head = record_of(w, ms_total, K, world, clk, peaks)
     e2e = e2e_of(w, min(K, 2000), local, world)
+    spans = kernel_spans(w)
     rl = head["roofline"]
+    rl["dominant_kernel"] = dominant_roofline(w, spans, peaks)
     rl["kernel"] = ("whole step: " + head["path"] + " (the kernels of a step overlap through "
                     "programmatic dependent launch, so the step is timed whole)")
     res = {
@@ -452,6 +520,7 @@ def run_ours(args, rank, world, local):
         "roofline": rl, "e2e": e2e,
         "gpu_launches": K * head["gpu_launches_per_step"],
         "clocks": clk,
+        "kernel_spans": spans,
     }
     if args.sweep:
         # the rest of the metric: the decode batch sweep and the large-batch
@@ -470,6 +539,8 @@ def run_ours(args, rank, world, local):
             r = record_of(wc, ms_c, steps_c, world, clk_c, peaks)
             if c.startswith("skew") or c.startswith("prefill"):
                 r["expert_load"] = expert_load(wc)
+            r["kernel_spans"] = kernel_spans(wc, steps=10 if Mc > DECODE_MAX_TOKENS else 40)
+            r["roofline"]["dominant_kernel"] = dominant_roofline(wc, r["kernel_spans"], peaks)
             r["gpu_launches"] = steps_c * r["gpu_launches_per_step"]
             recs[c] = r
             del wc

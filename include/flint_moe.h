@@ -242,6 +242,24 @@ int flint_moe_plan(const flint_moe_shape* shape);
  * another host thread enqueues work. */
 int flint_moe_prefer_path(int path);
 
+/* Kernel spans for profiling (process-wide, default off).  With a device
+ * buffer of FLINT_SPAN_KERNELS * FLINT_SPAN_CTAS * 2 uint64 words that the
+ * caller zero-fills, every later launch records, for each of its kernels
+ * (index FLINT_SPAN_*) and CTA c (slot c mod FLINT_SPAN_CTAS), the
+ * %globaltimer value (ns) at the CTA's start, stored as its bitwise
+ * complement (word 2 * slot), and at its last warp's exit (word 2 * slot + 1).
+ * A kernel's span is then [min start, max exit] over its slots.  The cost
+ * is one atomic per CTA and one per warp; NULL turns it off.  Set it between
+ * calls; the buffer must outlive the launches that write it. */
+enum {
+  FLINT_SPAN_ROUTE = 0, FLINT_SPAN_GATE_UP = 1, FLINT_SPAN_DOWN = 2, FLINT_SPAN_SINGLE_LAUNCH = 3,
+  FLINT_SPAN_GROUP_COUNT = 4, FLINT_SPAN_GROUP_SCAN = 5, FLINT_SPAN_GROUP_SCATTER = 6,
+  FLINT_SPAN_PLAN = 7, FLINT_SPAN_GATHER = 8, FLINT_SPAN_GEMM1 = 9, FLINT_SPAN_GEMM2 = 10,
+  FLINT_SPAN_COMBINE = 11, FLINT_SPAN_ADD_NORM = 12,
+  FLINT_SPAN_KERNELS = 16, FLINT_SPAN_CTAS = 1024
+};
+int flint_moe_record_spans(unsigned long long* spans);
+
 /* Static description of an error code. */
 const char* flint_moe_strerror(int code);
 

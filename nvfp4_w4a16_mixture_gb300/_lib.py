@@ -34,7 +34,7 @@ EXPORTED = ("flint_moe_workspace_bytes", "flint_moe_route", "flint_moe_forward",
             "flint_moe_route_noalloc", "flint_moe_route_noalloc_bytes",
             "flint_moe_route_noalloc_capacity", "flint_moe_status", "flint_moe_strerror",
             "flint_moe_debug_fault", "flint_moe_plan", "flint_moe_prefer_path",
-            "flint_moe_forward_add_norm")
+            "flint_moe_forward_add_norm", "flint_moe_record_spans")
 
 
 class FlintMoEError(RuntimeError):
@@ -89,6 +89,8 @@ def load() -> ctypes.CDLL:
             lib.flint_moe_plan.argtypes = [S]
             lib.flint_moe_prefer_path.restype = ctypes.c_int
             lib.flint_moe_prefer_path.argtypes = [ctypes.c_int]
+            lib.flint_moe_record_spans.restype = ctypes.c_int
+            lib.flint_moe_record_spans.argtypes = [P]
             _lib = lib
     return _lib
 
@@ -210,6 +212,33 @@ def flint_moe_prefer_path(path: int) -> None:
     rc = load().flint_moe_prefer_path(int(path))
     if rc != FLINT_OK:
         raise FlintMoEError(rc, "flint_moe_prefer_path")
+
+
+SPAN_NAMES = ("route", "gate_up", "down", "single_launch", "group_count", "group_scan",
+              "group_scatter", "plan", "gather", "gemm1", "gemm2", "combine", "add_norm")
+SPAN_KERNELS = 16
+SPAN_CTAS = 1024
+
+
+def flint_moe_record_spans(buf) -> None:
+    """Record kernel spans into `buf` (a zeroed int64 CUDA tensor of
+    SPAN_KERNELS * SPAN_CTAS * 2 words), or stop recording (None)."""
+    if buf is not None:
+        assert buf.numel() * buf.element_size() >= SPAN_KERNELS * SPAN_CTAS * 16
+    load().flint_moe_record_spans(_ptr(buf))
+
+
+def spans_of(buf) -> dict:
+    """{kernel name: (start ns, end ns)} of the kernels that recorded into buf."""
+    a = buf.view(torch.int64).cpu().reshape(SPAN_KERNELS, SPAN_CTAS, 2)
+    res = {}
+    for i, name in enumerate(SPAN_NAMES):
+        st, en = a[i, :, 0], a[i, :, 1]
+        used = st != 0
+        if bool(used.any()):
+            start = int((~st[used]).min())
+            res[name] = (start, int(en[used].max()))
+    return res
 
 
 def flint_moe_status(workspace, stream=None) -> int:

@@ -13,6 +13,7 @@ static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 static std::atomic<int> g_fault_site{0};  // test hook, see flint_moe_debug_fault
 static std::atomic<int> g_prefer{0};      // flint_moe_prefer_path
+static std::atomic<unsigned long long*> g_spans{nullptr};  // flint_moe_record_spans
 int debug_fault_site() { return g_fault_site.load(std::memory_order_relaxed); }
 
 // A well-formed shape: H, I and SI multiples of 64 (the unit of the block's
@@ -168,6 +169,7 @@ int flint_moe_route(const void* x, const void* router_w, const flint_moe_shape* 
   a.tw_out = tw;
   a.M = shape->M; a.H = shape->H; a.E = shape->E; a.k = shape->top_k; a.I = shape->I; a.SI = shape->SI;
   a.fault = debug_fault_site();
+  a.spans = g_spans.load(std::memory_order_relaxed);
   a.ws = ws_pointers(workspace, L);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (launch_route(a, false, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
@@ -234,6 +236,7 @@ static MoEArgs make_args(const void* x, const void* router_w, const uint8_t* w13
   a.tw_out = tw_out;
   a.M = shape->M; a.H = shape->H; a.E = shape->E; a.k = shape->top_k; a.I = shape->I; a.SI = shape->SI;
   a.fault = debug_fault_site();
+  a.spans = g_spans.load(std::memory_order_relaxed);
   a.ws = ws_pointers(workspace, ws_layout(*shape));
   return a;
 }
@@ -281,7 +284,7 @@ int flint_moe_forward_add_norm(const void* attn_out, const void* residual, const
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (launch_add_rms_norm(static_cast<const uint16_t*>(attn_out), static_cast<const uint16_t*>(residual),
                           static_cast<const uint16_t*>(ln_weight), eps, shape->M, shape->H,
-                          static_cast<uint16_t*>(residual_out), xn, st) != cudaSuccess)
+                          static_cast<uint16_t*>(residual_out), xn, a.spans, st) != cudaSuccess)
     return FLINT_ERR_CUDA;
   return enqueue_forward(a, shape, st);
 }
@@ -312,6 +315,11 @@ int flint_moe_status(void* workspace, flint_stream_t stream) {
 int flint_moe_prefer_path(int path) {
   if (path != FLINT_PATH_NONE && path != FLINT_PATH_SINGLE_LAUNCH) return FLINT_ERR_INVALID_ARG;
   g_prefer.store(path, std::memory_order_relaxed);
+  return FLINT_OK;
+}
+
+int flint_moe_record_spans(unsigned long long* spans) {
+  g_spans.store(spans, std::memory_order_relaxed);
   return FLINT_OK;
 }
 

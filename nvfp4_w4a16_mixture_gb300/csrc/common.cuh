@@ -293,6 +293,31 @@ FLINT_DEV int atom_add_acqrel_cta_smem(int* p, int v) {
 // Order this thread's earlier generic-proxy global accesses (and what it has
 // observed) before its later async-proxy (bulk copy) accesses.
 FLINT_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// ------------------------------------------------------------------ spans --
+// Kernel spans (flint_moe_record_spans): per kernel id and CTA (mod
+// kSpanCtas) the CTA's start, stored as its bitwise complement so that
+// atomicMax keeps the earliest, and the exit of its last warp.  The guard's
+// destructor runs on every return path; with a null buffer it does nothing.
+constexpr int kSpanCtas = 1024;
+enum {
+  kSpanRoute = 0, kSpanGateUp = 1, kSpanDown = 2, kSpanSingle = 3, kSpanGroupCount = 4,
+  kSpanGroupScan = 5, kSpanGroupScatter = 6, kSpanPlan = 7, kSpanGather = 8, kSpanGemm1 = 9,
+  kSpanGemm2 = 10, kSpanCombine = 11, kSpanAddNorm = 12
+};
+struct SpanGuard {
+  unsigned long long* slot;
+  __device__ __forceinline__ SpanGuard(unsigned long long* spans, int id) : slot(nullptr) {
+    if (spans) {
+      const unsigned cta = (blockIdx.x + gridDim.x * blockIdx.y) % kSpanCtas;
+      slot = spans + ((size_t)id * kSpanCtas + cta) * 2;
+      if (threadIdx.x == 0) atomicMax(slot, ~globaltimer_ns());
+    }
+  }
+  __device__ __forceinline__ ~SpanGuard() {
+    if (slot && (threadIdx.x & 31) == 0) atomicMax(slot + 1, globaltimer_ns());
+  }
+};
 // Generic-proxy shared-memory accesses ordered with the async proxy's (bulk
 // copies and the tensor core read and write shared memory through it).
 FLINT_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }

@@ -522,6 +522,7 @@ struct RecPlan {
 };
 
 __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a) {
+  SpanGuard span_guard(a.spans, kSpanSingle);
   extern __shared__ __align__(128) uint8_t smem[];
   const int M = a.M, H = a.H, E = a.E, k = a.k, I = a.I, SI = a.SI;
   const Layout L = fused_layout(M, H, SI);

@@ -283,6 +283,7 @@ FLINT_DEV void topk_warp(Get get, int E, int k, int lane, int& out_e, float& out
 // expert grouping (M <= kDecodeMaxTokens).
 __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(MoEArgs a, int build_meta,
                                                                  int* rowof) {
+  SpanGuard span_guard(a.spans, kSpanRoute);
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * kRouteWarps + warp;
@@ -356,6 +357,7 @@ constexpr int kGroupChunk = 1024;
 constexpr int kGroupThreads = 256;
 
 __global__ void __launch_bounds__(kGroupThreads) group_count_kernel(MoEArgs a, int* ccnt) {
+  SpanGuard span_guard(a.spans, kSpanGroupCount);
   pdl_launch_dependents();
   pdl_wait();
   __shared__ int s_cnt[kMaxE];
@@ -374,6 +376,7 @@ __global__ void __launch_bounds__(kGroupThreads) group_count_kernel(MoEArgs a, i
 // One CTA: thread e walks the chunks of expert e.
 __global__ void __launch_bounds__(kMaxE) group_scan_kernel(MoEArgs a, const int* ccnt, int* coff,
                                                            int nchunks) {
+  SpanGuard span_guard(a.spans, kSpanGroupScan);
   pdl_launch_dependents();
   pdl_wait();
   __shared__ int s_tot[kMaxE];
@@ -416,6 +419,7 @@ __global__ void __launch_bounds__(kMaxE) group_scan_kernel(MoEArgs a, const int*
 // __match_any_sync inside a warp plus per-warp counts across warps.
 __global__ void __launch_bounds__(kGroupThreads) group_scatter_kernel(MoEArgs a, const int* coff,
                                                                       int* rowof) {
+  SpanGuard span_guard(a.spans, kSpanGroupScatter);
   pdl_launch_dependents();
   pdl_wait();
   constexpr int kW = kGroupThreads / 32;
@@ -494,6 +498,7 @@ struct RcSmem {
 
 __global__ void __cluster_dims__(kRcCtas, 1, 1) __launch_bounds__(kRcWarps * 32)
     route_cluster_kernel(MoEArgs a) {
+  SpanGuard span_guard(a.spans, kSpanRoute);
   __shared__ RcSmem S;
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
@@ -655,6 +660,7 @@ constexpr int kRtTokens = 16;
 constexpr int kRtWarps = 16;
 
 __global__ void __launch_bounds__(kRtWarps * 32) route_tile_kernel(MoEArgs a) {
+  SpanGuard span_guard(a.spans, kSpanRoute);
   extern __shared__ __align__(16) uint8_t rt_smem[];
   const int H = a.H, E = a.E, k = a.k;
   const bool f32 = H <= 2048;

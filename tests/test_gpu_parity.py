@@ -439,3 +439,28 @@ def test_forward_add_norm(decode_layer, M):
     # the normalised rows may also stay in the workspace
     out2, res2 = fm.forward_add_norm_layer(attn, resid, lnw, eps, layer, k, workspace=ws)
     assert torch.equal(out2, out) and torch.equal(res2, res_out)
+
+
+def test_kernel_spans_are_recorded(decode_layer):
+    """flint_moe_record_spans: a decode step records its three kernels, each
+    span positive and in launch order of their starts; with recording off the
+    buffer stays untouched."""
+    x1, layer, k = decode_layer
+    ws = fm.alloc_workspace(1, layer.H, layer.E, k, layer.I, layer.SI)
+    buf = torch.zeros(16 * 1024 * 2, dtype=torch.int64, device="cuda")
+    fm.flint_moe_record_spans(buf)
+    try:
+        fm.forward_layer(x1, layer, k, workspace=ws)
+        torch.cuda.synchronize()
+    finally:
+        fm.flint_moe_record_spans(None)
+    sp = fm.spans_of(buf)
+    assert set(sp) == {"route", "gate_up", "down"}, sp
+    for a, b in sp.values():
+        assert 0 < b - a < 10 ** 7
+    assert sp["route"][0] <= sp["gate_up"][0] <= sp["down"][0]
+    buf.zero_()
+    fm.forward_layer(x1, layer, k, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(buf.abs().sum()) == 0
+    assert fm.flint_moe_status(ws) == fm.FLINT_OK

@@ -22,9 +22,8 @@ constexpr int kNormWarps = 8;
 
 __global__ void __launch_bounds__(kNormWarps * 32) add_rms_norm_kernel(
     const uint16_t* __restrict__ a, const uint16_t* __restrict__ r, const uint16_t* __restrict__ w,
-    float eps, int M, int H, uint16_t* __restrict__ res_out, uint16_t* __restrict__ xn,
-    unsigned long long* spans) {
-  SpanGuard span_guard(spans, kSpanAddNorm);
+    float eps, int M, int H, uint16_t* __restrict__ res_out, uint16_t* __restrict__ xn) {
+  SpanGuard<kSpanAddNorm> span_guard;
   pdl_wait();  // the inputs belong to the stream's earlier work
   pdl_launch_dependents();
   const int t = blockIdx.x * kNormWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -70,9 +69,8 @@ __global__ void __launch_bounds__(kNormWarps * 32) add_rms_norm_kernel(
 }  // namespace
 
 cudaError_t launch_add_rms_norm(const uint16_t* a, const uint16_t* r, const uint16_t* w, float eps,
-                                int M, int H, uint16_t* res_out, uint16_t* xn, unsigned long long* spans,
-                                cudaStream_t st) {
-  void* args[] = {&a, &r, &w, &eps, &M, &H, &res_out, &xn, &spans};
+                                int M, int H, uint16_t* res_out, uint16_t* xn, cudaStream_t st) {
+  void* args[] = {&a, &r, &w, &eps, &M, &H, &res_out, &xn};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((M + kNormWarps - 1) / kNormWarps));
   cfg.blockDim = dim3(kNormWarps * 32);
@@ -84,5 +82,7 @@ cudaError_t launch_add_rms_norm(const uint16_t* a, const uint16_t* r, const uint
   cfg.numAttrs = 1;
   return cudaLaunchKernelExC(&cfg, (const void*)add_rms_norm_kernel, args);
 }
+
+FLINT_SPAN_SETTER(add_norm)
 
 }  // namespace flint

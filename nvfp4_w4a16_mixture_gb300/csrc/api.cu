@@ -13,7 +13,6 @@ static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 static std::atomic<int> g_fault_site{0};  // test hook, see flint_moe_debug_fault
 static std::atomic<int> g_prefer{0};      // flint_moe_prefer_path
-static std::atomic<unsigned long long*> g_spans{nullptr};  // flint_moe_record_spans
 int debug_fault_site() { return g_fault_site.load(std::memory_order_relaxed); }
 
 // A well-formed shape: H, I and SI multiples of 64 (the unit of the block's
@@ -169,7 +168,6 @@ int flint_moe_route(const void* x, const void* router_w, const flint_moe_shape* 
   a.tw_out = tw;
   a.M = shape->M; a.H = shape->H; a.E = shape->E; a.k = shape->top_k; a.I = shape->I; a.SI = shape->SI;
   a.fault = debug_fault_site();
-  a.spans = g_spans.load(std::memory_order_relaxed);
   a.ws = ws_pointers(workspace, L);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (launch_route(a, false, st, true) != cudaSuccess) return FLINT_ERR_CUDA;
@@ -236,7 +234,6 @@ static MoEArgs make_args(const void* x, const void* router_w, const uint8_t* w13
   a.tw_out = tw_out;
   a.M = shape->M; a.H = shape->H; a.E = shape->E; a.k = shape->top_k; a.I = shape->I; a.SI = shape->SI;
   a.fault = debug_fault_site();
-  a.spans = g_spans.load(std::memory_order_relaxed);
   a.ws = ws_pointers(workspace, ws_layout(*shape));
   return a;
 }
@@ -284,7 +281,7 @@ int flint_moe_forward_add_norm(const void* attn_out, const void* residual, const
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (launch_add_rms_norm(static_cast<const uint16_t*>(attn_out), static_cast<const uint16_t*>(residual),
                           static_cast<const uint16_t*>(ln_weight), eps, shape->M, shape->H,
-                          static_cast<uint16_t*>(residual_out), xn, a.spans, st) != cudaSuccess)
+                          static_cast<uint16_t*>(residual_out), xn, st) != cudaSuccess)
     return FLINT_ERR_CUDA;
   return enqueue_forward(a, shape, st);
 }
@@ -319,7 +316,11 @@ int flint_moe_prefer_path(int path) {
 }
 
 int flint_moe_record_spans(unsigned long long* spans) {
-  g_spans.store(spans, std::memory_order_relaxed);
+  cudaError_t (*const set[])(unsigned long long*) = {span_buffer_set_decode2, span_buffer_set_decode,
+                                                     span_buffer_set_fused, span_buffer_set_grouped,
+                                                     span_buffer_set_route, span_buffer_set_add_norm};
+  for (auto f : set)
+    if (f(spans) != cudaSuccess) return FLINT_ERR_CUDA;
   return FLINT_OK;
 }
 

@@ -297,27 +297,43 @@ FLINT_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.glob
 // ------------------------------------------------------------------ spans --
 // Kernel spans (flint_moe_record_spans): per kernel id and CTA (mod
 // kSpanCtas) the CTA's start, stored as its bitwise complement so that
-// atomicMax keeps the earliest, and the exit of its last warp.  The guard's
-// destructor runs on every return path; with a null buffer it does nothing.
+// atomicMax keeps the earliest, and the exit of its last warp.  The buffer
+// address is a device variable of each translation unit (set by its
+// span_buffer_set_*), read afresh at a CTA's start and at each warp's exit,
+// so a guard holds no register through the kernel; its destructor runs on
+// every return path, and with a null buffer it does nothing.
 constexpr int kSpanCtas = 1024;
 enum {
   kSpanRoute = 0, kSpanGateUp = 1, kSpanDown = 2, kSpanSingle = 3, kSpanGroupCount = 4,
   kSpanGroupScan = 5, kSpanGroupScatter = 6, kSpanPlan = 7, kSpanGather = 8, kSpanGemm1 = 9,
   kSpanGemm2 = 10, kSpanCombine = 11, kSpanAddNorm = 12
 };
+static __device__ unsigned long long* g_span_buf;
+FLINT_DEV unsigned long long* span_slot(int id) {
+  unsigned long long* b = *reinterpret_cast<unsigned long long* volatile*>(&g_span_buf);
+  if (!b) return nullptr;
+  return b + ((size_t)id * kSpanCtas + (blockIdx.x + gridDim.x * blockIdx.y) % kSpanCtas) * 2;
+}
+template <int ID>
 struct SpanGuard {
-  unsigned long long* slot;
-  __device__ __forceinline__ SpanGuard(unsigned long long* spans, int id) : slot(nullptr) {
-    if (spans) {
-      const unsigned cta = (blockIdx.x + gridDim.x * blockIdx.y) % kSpanCtas;
-      slot = spans + ((size_t)id * kSpanCtas + cta) * 2;
-      if (threadIdx.x == 0) atomicMax(slot, ~globaltimer_ns());
+  __device__ __forceinline__ SpanGuard() {
+    if (threadIdx.x == 0) {
+      unsigned long long* s = span_slot(ID);
+      if (s) atomicMax(s, ~globaltimer_ns());
     }
   }
   __device__ __forceinline__ ~SpanGuard() {
-    if (slot && (threadIdx.x & 31) == 0) atomicMax(slot + 1, globaltimer_ns());
+    if ((threadIdx.x & 31) == 0) {
+      unsigned long long* s = span_slot(ID);
+      if (s) atomicMax(s + 1, globaltimer_ns());
+    }
   }
 };
+// The host-side setter of this translation unit's buffer address.
+#define FLINT_SPAN_SETTER(unit)                                        \
+  cudaError_t span_buffer_set_##unit(unsigned long long* b) {          \
+    return cudaMemcpyToSymbol(g_span_buf, &b, sizeof(b));              \
+  }
 // Generic-proxy shared-memory accesses ordered with the async proxy's (bulk
 // copies and the tensor core read and write shared memory through it).
 FLINT_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }

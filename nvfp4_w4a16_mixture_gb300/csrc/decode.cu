@@ -116,7 +116,7 @@ FLINT_DEV float red_sum(const float (&red)[kDecWarps][kNT][32][4], int nt, int l
 // (tile rows 0..7 = gate rows r0.., rows 8..15 = up rows SI + r0..).  Items
 // after that: (routed expert u, 8 intermediate rows), u < U.
 __global__ void __launch_bounds__(kDecThreads) gate_up_decode_kernel(MoEArgs a, int ns_items) {
-  SpanGuard span_guard(a.spans, kSpanGateUp);
+  SpanGuard<kSpanGateUp> span_guard;
   __shared__ float red[kDecWarps][kNT][32][4];
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int warp = threadIdx.x >> 5;
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kDecThreads) gate_up_decode_kernel(MoEArgs a, 
 // the last item to finish an output row block (counter per block) forms
 // out = bf16(bf16(sum_j tw_j y_j) + ys) for every token of that block.
 __global__ void __launch_bounds__(kDecThreads) down_decode_kernel(MoEArgs a, int ns_items) {
-  SpanGuard span_guard(a.spans, kSpanDown);
+  SpanGuard<kSpanDown> span_guard;
   __shared__ float red[kDecWarps][kNT][32][4];
   __shared__ int s_last;
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -373,5 +373,7 @@ cudaError_t launch_decode_down(const MoEArgs& a, cudaStream_t st, bool pdl) {
   void* args[] = {&aa, &ns};
   return launch((const void*)down_decode_kernel, dim3(items), dim3(kDecThreads), args, st, pdl);
 }
+
+FLINT_SPAN_SETTER(decode)
 
 }  // namespace flint

@@ -391,7 +391,7 @@ FLINT_DEV void gu_issue_routed(const MoEArgs& a, uint8_t* stage, GuInfo& inf, ui
 // NTG: token n-tiles held in registers at a time (1 when M <= 8).
 template <int NTG>
 __global__ void __launch_bounds__(kGuThreads, 1) gate_up2_kernel(MoEArgs a) {
-  SpanGuard span_guard(a.spans, kSpanGateUp);
+  SpanGuard<kSpanGateUp> span_guard;
   extern __shared__ __align__(128) uint8_t smem[];
   const GuLayout L = gu_layout(a.M, a.H);
   const int S = L.stages;
@@ -800,7 +800,7 @@ FLINT_DEV int dn_block_bytes(int kind, int I, int SI) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
-  SpanGuard span_guard(a.spans, kSpanDown);
+  SpanGuard<kSpanDown> span_guard;
   extern __shared__ __align__(128) uint8_t smem[];
   // the next kernel may start now: a router launched after this one loads
   // only its weights before its own dependency wait
@@ -1153,5 +1153,7 @@ cudaError_t launch_decode2(const MoEArgs& a, cudaStream_t st) {
   return launch_ex((const void*)down2_kernel, dim3(a.H / 16), kThreads, dn_layout(a.M, a.k).total,
                    args, st, true);
 }
+
+FLINT_SPAN_SETTER(decode2)
 
 }  // namespace flint

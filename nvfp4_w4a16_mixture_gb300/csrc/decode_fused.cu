@@ -522,7 +522,7 @@ struct RecPlan {
 };
 
 __global__ void __launch_bounds__(kThreads, 1) moe_decode_fused_kernel(MoEArgs a) {
-  SpanGuard span_guard(a.spans, kSpanSingle);
+  SpanGuard<kSpanSingle> span_guard;
   extern __shared__ __align__(128) uint8_t smem[];
   const int M = a.M, H = a.H, E = a.E, k = a.k, I = a.I, SI = a.SI;
   const Layout L = fused_layout(M, H, SI);
@@ -1283,5 +1283,7 @@ cudaError_t launch_fused(const MoEArgs& a, cudaStream_t st, int sms) {
   cfg.numAttrs = 1;
   return cudaLaunchKernelExC(&cfg, (const void*)moe_decode_fused_kernel, args);
 }
+
+FLINT_SPAN_SETTER(fused)
 
 }  // namespace flint

@@ -233,7 +233,7 @@ template <int STAGE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     grouped_gemm_kernel(const MoEArgs a, const __grid_constant__ TMaps tm, int NT, int NTs,
                         int n_shared_tiles) {
-  SpanGuard span_guard(a.spans, STAGE == 1 ? kSpanGemm1 : kSpanGemm2);
+  SpanGuard<(STAGE == 1 ? kSpanGemm1 : kSpanGemm2)> span_guard;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   GCtl& C = *reinterpret_cast<GCtl*>(smem + (size_t)kOffScale + kScaleBytes);
@@ -641,7 +641,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
 // ------------------------------------------------------------- small kernels
 // Token tiles: per expert, ceil(cnt / 256) entries {e, row0, row_end}.
 __global__ void __launch_bounds__(256) plan_kernel(MoEArgs a) {
-  SpanGuard span_guard(a.spans, kSpanPlan);
+  SpanGuard<kSpanPlan> span_guard;
   pdl_wait();
   pdl_launch_dependents();
   __shared__ int s_n[kMaxE], s_start[kMaxE + 1];
@@ -669,7 +669,7 @@ __global__ void __launch_bounds__(256) plan_kernel(MoEArgs a) {
 
 // x_perm[pos] = x[sorted_pairs[pos] / k], one warp per row.
 __global__ void __launch_bounds__(256) gather_kernel(MoEArgs a) {
-  SpanGuard span_guard(a.spans, kSpanGather);
+  SpanGuard<kSpanGather> span_guard;
   pdl_wait();
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -683,7 +683,7 @@ __global__ void __launch_bounds__(256) gather_kernel(MoEArgs a) {
 
 // out[t, h..h+7] = bf16(bf16(sum_j tw_j y[row(t, j), h]) + ys[t, h]), j in rank order.
 __global__ void __launch_bounds__(256) combine_kernel(MoEArgs a) {
-  SpanGuard span_guard(a.spans, kSpanCombine);
+  SpanGuard<kSpanCombine> span_guard;
   pdl_wait();
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int hv = a.H / 8;
@@ -845,5 +845,7 @@ cudaError_t launch_grouped(const MoEArgs& a, cudaStream_t st) {
   return launch_pdl((const void*)combine_kernel, dim3((unsigned)((nthr + 255) / 256)), dim3(256), 0,
                     args0, st);
 }
+
+FLINT_SPAN_SETTER(grouped)
 
 }  // namespace flint

@@ -109,7 +109,6 @@ struct MoEArgs {
   float* tw_out;  // optional user copy
   int M, H, E, k, I, SI;
   int fault;  // test hook: a FLINT_FAULT_* site whose signal is left out (0: none)
-  unsigned long long* spans;  // flint_moe_record_spans buffer, or null
   Ws ws;
 };
 
@@ -149,8 +148,16 @@ cudaError_t launch_fused(const MoEArgs& a, cudaStream_t st, int sms);
 // norm.fused_add_rms_norm of rows a + r (add_norm.cu): residual' and xn, both
 // bf16 [M, H]; one warp per token, launched with programmatic dependent launch.
 cudaError_t launch_add_rms_norm(const uint16_t* a, const uint16_t* r, const uint16_t* w, float eps,
-                                int M, int H, uint16_t* res_out, uint16_t* xn, unsigned long long* spans,
-                                cudaStream_t st);
+                                int M, int H, uint16_t* res_out, uint16_t* xn, cudaStream_t st);
+
+// Kernel-span buffer setters, one per translation unit with kernels
+// (flint_moe_record_spans calls them all).
+cudaError_t span_buffer_set_decode2(unsigned long long* b);
+cudaError_t span_buffer_set_decode(unsigned long long* b);
+cudaError_t span_buffer_set_fused(unsigned long long* b);
+cudaError_t span_buffer_set_grouped(unsigned long long* b);
+cudaError_t span_buffer_set_route(unsigned long long* b);
+cudaError_t span_buffer_set_add_norm(unsigned long long* b);
 
 
 

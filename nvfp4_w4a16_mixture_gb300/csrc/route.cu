@@ -283,7 +283,7 @@ FLINT_DEV void topk_warp(Get get, int E, int k, int lane, int& out_e, float& out
 // expert grouping (M <= kDecodeMaxTokens).
 __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(MoEArgs a, int build_meta,
                                                                  int* rowof) {
-  SpanGuard span_guard(a.spans, kSpanRoute);
+  SpanGuard<kSpanRoute> span_guard;
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * kRouteWarps + warp;
@@ -357,7 +357,7 @@ constexpr int kGroupChunk = 1024;
 constexpr int kGroupThreads = 256;
 
 __global__ void __launch_bounds__(kGroupThreads) group_count_kernel(MoEArgs a, int* ccnt) {
-  SpanGuard span_guard(a.spans, kSpanGroupCount);
+  SpanGuard<kSpanGroupCount> span_guard;
   pdl_launch_dependents();
   pdl_wait();
   __shared__ int s_cnt[kMaxE];
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(kGroupThreads) group_count_kernel(MoEArgs a, i
 // One CTA: thread e walks the chunks of expert e.
 __global__ void __launch_bounds__(kMaxE) group_scan_kernel(MoEArgs a, const int* ccnt, int* coff,
                                                            int nchunks) {
-  SpanGuard span_guard(a.spans, kSpanGroupScan);
+  SpanGuard<kSpanGroupScan> span_guard;
   pdl_launch_dependents();
   pdl_wait();
   __shared__ int s_tot[kMaxE];
@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(kMaxE) group_scan_kernel(MoEArgs a, const int*
 // __match_any_sync inside a warp plus per-warp counts across warps.
 __global__ void __launch_bounds__(kGroupThreads) group_scatter_kernel(MoEArgs a, const int* coff,
                                                                       int* rowof) {
-  SpanGuard span_guard(a.spans, kSpanGroupScatter);
+  SpanGuard<kSpanGroupScatter> span_guard;
   pdl_launch_dependents();
   pdl_wait();
   constexpr int kW = kGroupThreads / 32;
@@ -498,7 +498,7 @@ struct RcSmem {
 
 __global__ void __cluster_dims__(kRcCtas, 1, 1) __launch_bounds__(kRcWarps * 32)
     route_cluster_kernel(MoEArgs a) {
-  SpanGuard span_guard(a.spans, kSpanRoute);
+  SpanGuard<kSpanRoute> span_guard;
   __shared__ RcSmem S;
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
@@ -660,7 +660,7 @@ constexpr int kRtTokens = 16;
 constexpr int kRtWarps = 16;
 
 __global__ void __launch_bounds__(kRtWarps * 32) route_tile_kernel(MoEArgs a) {
-  SpanGuard span_guard(a.spans, kSpanRoute);
+  SpanGuard<kSpanRoute> span_guard;
   extern __shared__ __align__(16) uint8_t rt_smem[];
   const int H = a.H, E = a.E, k = a.k;
   const bool f32 = H <= 2048;
@@ -804,5 +804,7 @@ cudaError_t launch_route(const MoEArgs& a, bool build_meta, cudaStream_t st, boo
   void* a3[] = {&aa, &coff, &rowof};
   return launch((const void*)group_scatter_kernel, dim3(nchunks), dim3(kGroupThreads), a3, st, true);
 }
+
+FLINT_SPAN_SETTER(route)
 
 }  // namespace flint

@@ -163,6 +163,31 @@ int flint_moe_forward_add_norm(const void* attn_out, const void* residual, const
                                void* residual_out, void* xn_out, int32_t* ids_out, float* tw_out,
                                void* workspace, size_t workspace_bytes, flint_stream_t stream);
 
+/* The decode MoE block on BF16 routed experts: "flint_moe_bf16_decode" on
+ * the page above.  The same routing as flint_moe_route, then per selected
+ * expert act = bf16(silu(g) * u) from the fp32 gate/up sums (no global
+ * scale), y_e = bf16(acc), routed = bf16(sum_j tw_j y_j) in fp32 in rank
+ * order, out = bf16(routed + shared_out).  Every gate/up and down sum is the
+ * exact sum of the products rounded once to fp32.
+ *
+ *   x            bf16 [M, H]
+ *   router_w     bf16 [E, H]
+ *   w13          bf16 [E, 2I, H]   gate rows [0, I) then up rows [I, 2I)
+ *                                   (row-major; the page's blocked storage
+ *                                   order is not used)
+ *   w2           bf16 [E, H, I]
+ *   shared_out   bf16 [M, H]       the shared expert's output, added to the
+ *                                   routed part (NULL: no shared expert)
+ *   out          bf16 [M, H]       (output)
+ *   ids_out, tw_out, workspace, stream: as for flint_moe_forward.
+ * The shape's SI must be 0 (FLINT_ERR_INVALID_ARG otherwise); M above 64
+ * returns FLINT_ERR_UNSUPPORTED.  Four launches (router, gate/up, down,
+ * combine) chained with programmatic dependent launch. */
+int flint_moe_forward_bf16(const void* x, const void* router_w, const void* w13, const void* w2,
+                           const void* shared_out, const flint_moe_shape* shape, void* out,
+                           int32_t* ids_out, float* tw_out, void* workspace, size_t workspace_bytes,
+                           flint_stream_t stream);
+
 /* Routing without caller memory: the same kernel, numerics and outputs as
  * flint_moe_route, but its intermediates live in a fixed scratch array that
  * the library itself holds in device memory (2 MiB per device, a file-scope

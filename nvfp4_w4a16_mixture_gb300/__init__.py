@@ -15,7 +15,7 @@ from ._lib import (EXPORTED, FLINT_ERR_CUDA, FLINT_ERR_INVALID_ARG, FLINT_ERR_SC
                    flint_moe_route_noalloc_capacity, flint_moe_status, flint_moe_strerror,
                    flint_moe_workspace_bytes, forward_layer, library_path, load,
                    flint_moe_forward_add_norm, forward_add_norm_layer, flint_moe_record_spans,
-                   spans_of, SPAN_NAMES)
+                   spans_of, SPAN_NAMES, flint_moe_forward_bf16)
 
 __all__ = [
     "EXPORTED", "FLINT_OK", "FLINT_ERR_INVALID_ARG", "FLINT_ERR_UNSUPPORTED",
@@ -23,7 +23,7 @@ __all__ = [
     "FLINT_FAULT_NONE", "FLINT_FAULT_DOWN_HANDOVER", "FLINT_PATH_NONE", "FLINT_PATH_SINGLE_LAUNCH",
     "FLINT_PATH_DECODE", "FLINT_PATH_DECODE_FALLBACK", "FLINT_PATH_GROUPED", "flint_moe_plan",
     "flint_moe_prefer_path", "flint_moe_forward_add_norm", "forward_add_norm_layer",
-    "flint_moe_record_spans", "spans_of", "SPAN_NAMES",
+    "flint_moe_record_spans", "spans_of", "SPAN_NAMES", "flint_moe_forward_bf16",
     "FlintMoEError", "alloc_workspace", "flint_moe_debug_fault", "flint_moe_forward",
     "flint_moe_route",
     "flint_moe_route_noalloc", "flint_moe_route_noalloc_bytes",

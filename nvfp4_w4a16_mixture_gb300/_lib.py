@@ -34,7 +34,7 @@ EXPORTED = ("flint_moe_workspace_bytes", "flint_moe_route", "flint_moe_forward",
             "flint_moe_route_noalloc", "flint_moe_route_noalloc_bytes",
             "flint_moe_route_noalloc_capacity", "flint_moe_status", "flint_moe_strerror",
             "flint_moe_debug_fault", "flint_moe_plan", "flint_moe_prefer_path",
-            "flint_moe_forward_add_norm", "flint_moe_record_spans")
+            "flint_moe_forward_add_norm", "flint_moe_record_spans", "flint_moe_forward_bf16")
 
 
 class FlintMoEError(RuntimeError):
@@ -89,6 +89,8 @@ def load() -> ctypes.CDLL:
             lib.flint_moe_plan.argtypes = [S]
             lib.flint_moe_prefer_path.restype = ctypes.c_int
             lib.flint_moe_prefer_path.argtypes = [ctypes.c_int]
+            lib.flint_moe_forward_bf16.restype = ctypes.c_int
+            lib.flint_moe_forward_bf16.argtypes = [P] * 5 + [S, P, P, P, P, ctypes.c_size_t, P]
             lib.flint_moe_record_spans.restype = ctypes.c_int
             lib.flint_moe_record_spans.argtypes = [P]
             _lib = lib
@@ -154,6 +156,21 @@ def flint_moe_forward(x, router_w, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, shared
         _ptr(tw_out), _ptr(workspace), workspace.numel(), _stream(stream))
     if rc != FLINT_OK:
         raise FlintMoEError(rc, "flint_moe_forward")
+
+
+def flint_moe_forward_bf16(x, router_w, w13, w2, top_k: int, out, workspace, shared_out=None,
+                           ids_out=None, tw_out=None, stream=None) -> None:
+    """The block on BF16 routed experts (flint_moe_bf16_decode): w13 bf16
+    [E, 2I, H], w2 bf16 [E, H, I], shared_out bf16 [M, H] or None."""
+    M, H = x.shape
+    E, I2, _ = w13.shape
+    s = _shape(M, H, E, top_k, I2 // 2, 0)
+    rc = load().flint_moe_forward_bf16(_ptr(x), _ptr(router_w), _ptr(w13), _ptr(w2), _ptr(shared_out),
+                                       ctypes.byref(s), _ptr(out), _ptr(ids_out), _ptr(tw_out),
+                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream))
+    if rc != FLINT_OK:
+        raise FlintMoEError(rc, "flint_moe_forward_bf16")
 
 
 def flint_moe_forward_add_norm(attn_out, residual, ln_weight, eps: float, router_w, w13, w13_sf,

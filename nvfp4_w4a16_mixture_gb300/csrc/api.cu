@@ -286,6 +286,30 @@ int flint_moe_forward_add_norm(const void* attn_out, const void* residual, const
   return enqueue_forward(a, shape, st);
 }
 
+int flint_moe_forward_bf16(const void* x, const void* router_w, const void* w13, const void* w2,
+                           const void* shared_out, const flint_moe_shape* shape, void* out, int32_t* ids_out,
+                           float* tw_out, void* workspace, size_t workspace_bytes, flint_stream_t stream) {
+  if (!shape_valid(shape) || shape->SI != 0) return FLINT_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return FLINT_ERR_UNSUPPORTED;
+  if (shape->M == 0) return FLINT_OK;
+  if (shape->M > kDecodeMaxTokens) return FLINT_ERR_UNSUPPORTED;
+  if (!x || !router_w || !w13 || !w2 || !out) return FLINT_ERR_INVALID_ARG;
+  const void* p16[] = {x, router_w, w13, w2, out};
+  for (const void* p : p16)
+    if (!aligned(p, 16)) return FLINT_ERR_INVALID_ARG;
+  if (shared_out && !aligned(shared_out, 16)) return FLINT_ERR_INVALID_ARG;
+  if ((ids_out && !aligned(ids_out, 4)) || (tw_out && !aligned(tw_out, 4))) return FLINT_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return FLINT_ERR_WORKSPACE;
+  if (workspace_bytes < ws_layout(*shape).total) return FLINT_ERR_WORKSPACE;
+  MoEArgs a = make_args(x, router_w, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                        shape, out, ids_out, tw_out, workspace);
+  if (launch_bf16_experts(a, static_cast<const uint16_t*>(w13), static_cast<const uint16_t*>(w2),
+                          static_cast<const uint16_t*>(shared_out),
+                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FLINT_ERR_CUDA;
+  return FLINT_OK;
+}
+
 int flint_moe_plan(const flint_moe_shape* shape) {
   if (!shape_valid(shape)) return FLINT_ERR_INVALID_ARG;
   if (!shape_supported(shape)) return FLINT_ERR_UNSUPPORTED;
@@ -318,7 +342,8 @@ int flint_moe_prefer_path(int path) {
 int flint_moe_record_spans(unsigned long long* spans) {
   cudaError_t (*const set[])(unsigned long long*) = {span_buffer_set_decode2, span_buffer_set_decode,
                                                      span_buffer_set_fused, span_buffer_set_grouped,
-                                                     span_buffer_set_route, span_buffer_set_add_norm};
+                                                     span_buffer_set_route, span_buffer_set_add_norm,
+                                                     span_buffer_set_bf16_experts};
   for (auto f : set)
     if (f(spans) != cudaSuccess) return FLINT_ERR_CUDA;
   return FLINT_OK;

@@ -158,6 +158,13 @@ cudaError_t span_buffer_set_fused(unsigned long long* b);
 cudaError_t span_buffer_set_grouped(unsigned long long* b);
 cudaError_t span_buffer_set_route(unsigned long long* b);
 cudaError_t span_buffer_set_add_norm(unsigned long long* b);
+cudaError_t span_buffer_set_bf16_experts(unsigned long long* b);
+
+// BF16 routed experts (bf16_experts.cu), M <= kDecodeMaxTokens: router with
+// the expert grouping, exact gate/up and down sums, combine with the given
+// shared output (null: none).
+cudaError_t launch_bf16_experts(const MoEArgs& a, const uint16_t* w13, const uint16_t* w2,
+                                const uint16_t* shared_out, cudaStream_t st);
 
 
 

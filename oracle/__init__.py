@@ -62,6 +62,8 @@ def _load():
             lib.oracle_topk.argtypes = [P, i32, i32, i32, P, P]
             lib.oracle_forward.restype = i32
             lib.oracle_forward.argtypes = [P] * 10 + [i32] * 6 + [P, i32] + [P] * 8 + [i32]
+            lib.oracle_forward_bf16.restype = i32
+            lib.oracle_forward_bf16.argtypes = [P] * 5 + [i32] * 5 + [P] * 5 + [i32]
             lib.oracle_add_rms_norm.restype = i32
             lib.oracle_add_rms_norm.argtypes = [P, P, P, i32, i32, ctypes.c_float, P, P]
             lib.oracle_max_threads.restype = i32
@@ -185,6 +187,32 @@ def forward(x, layer, top_k: int, tokens=None, intermediates: bool = False, nthr
         _ptr(g("y")), _ptr(g("sact")), _ptr(g("ys")), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_forward: invalid shape or token list")
+    return res
+
+
+def forward_bf16(x, router_w, w13, w2, top_k: int, shared_out=None, intermediates: bool = False,
+                 nthreads: int = 0):
+    """BF16 routed experts (reading R9): w13 bf16 [E, 2I, H], w2 bf16 [E, H, I],
+    shared_out bf16 [M, H] or None.  Returns out (bits), ids, tw and, with
+    ``intermediates``, act [M, k, I] and y [M, k, H] (bits)."""
+    xa, wra = _np(x, np.uint16), _np(router_w, np.uint16)
+    w13a, w2a = _np(w13, np.uint16), _np(w2, np.uint16)
+    M, H = xa.shape
+    E, I2, H2 = w13a.shape
+    I = I2 // 2
+    assert H2 == H and w2a.shape == (E, H, I)
+    sh = None if shared_out is None else _np(shared_out, np.uint16)
+    k = int(top_k)
+    res = {"out": np.empty((M, H), np.uint16), "ids": np.empty((M, k), np.int32),
+           "tw": np.empty((M, k), np.float32)}
+    if intermediates:
+        res.update(act=np.empty((M, k, I), np.uint16), y=np.empty((M, k, H), np.uint16))
+    g = res.get
+    rc = _load().oracle_forward_bf16(_ptr(xa), _ptr(wra), _ptr(w13a), _ptr(w2a), _ptr(sh), M, H, E, k, I,
+                                     _ptr(res["out"]), _ptr(res["ids"]), _ptr(res["tw"]), _ptr(g("act")),
+                                     _ptr(g("y")), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_forward_bf16: invalid shape")
     return res
 
 

@@ -41,6 +41,14 @@
  *      the page names the reciprocal square root (_rsqrt) without defining
  *      it: inv = 1 / sqrt(v) correctly rounded to fp32;
  *      xn = bf16((s * inv) * w), each product one fp32 rounding.
+ *  R9  BF16 routed experts (flint_moe_bf16_decode on the same page): the
+ *      same routing; g, u = fp32(exact dot) of x with BF16 w13 rows (R7),
+ *      act = bf16(silu(g) * u) (R4 form), y_e = bf16(fp32(exact dot)) of act
+ *      with BF16 w2 rows (no global scale), routed = bf16(sum_j tw_j y_j) in
+ *      fp32 rank order, out = bf16(routed + shared_output) with the shared
+ *      expert's output given (zero when absent).  The pages store the BF16
+ *      experts in a blocked order (BlockMajorK); here they are row-major
+ *      [E, 2I, H] and [E, H, I].
  *  R7  "products are accumulated in fp32" fixes the accumulator's type, not
  *      the order of the additions.  Every expert and shared-expert dot
  *      product therefore takes the order-independent value: the exact sum of
@@ -378,6 +386,74 @@ ORACLE_API int oracle_forward(const uint16_t* x, const uint16_t* wr, const uint8
                   tw ? tw + (int64_t)i * k : NULL, logits ? logits + (int64_t)i * E : NULL,
                   act ? act + (int64_t)i * k * I : NULL, y ? y + (int64_t)i * k * H : NULL,
                   sact ? sact + (int64_t)i * SI : NULL, ys ? ys + (int64_t)i * H : NULL);
+  }
+  return 0;
+}
+
+/* BF16 routed experts (reading R9), token rows x [M, H]: out and, optionally,
+ * ids / tw [M, k], act [M, k, I] and y [M, k, H] (bf16 bits). */
+ORACLE_API int oracle_forward_bf16(const uint16_t* x, const uint16_t* wr, const uint16_t* w13,
+                                   const uint16_t* w2, const uint16_t* shared_out, int M, int H,
+                                   int E, int k, int I, uint16_t* out, int32_t* ids_o, float* tw_o,
+                                   uint16_t* act_o, uint16_t* y_o, int nthreads) {
+  if (!shape_ok(M, H, E, k, I, 0))
+    return -1;
+#ifdef _OPENMP
+  if (nthreads > 0)
+    omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int t = 0; t < M; ++t) {
+    const uint16_t* xrow = x + (int64_t)t * H;
+    uint16_t logit_bits[256];
+    int32_t ids[64];
+    float tw[64];
+    float* xf = (float*)malloc(sizeof(float) * (size_t)H);
+    float* act = (float*)malloc(sizeof(float) * (size_t)I);
+    float* R = (float*)calloc((size_t)H, sizeof(float));
+    for (int h = 0; h < H; ++h)
+      xf[h] = bf16_to_f32(xrow[h]);
+    for (int e = 0; e < E; ++e)
+      logit_bits[e] = f32_to_bf16(router_logit(xrow, wr + (int64_t)e * H, H));
+    route_token(logit_bits, E, k, ids, tw);
+    for (int j = 0; j < k; ++j) {
+      const int64_t e = ids[j];
+      const uint16_t* g13 = w13 + e * (int64_t)(2 * I) * H;
+      for (int r = 0; r < I; ++r) {
+        double sg = 0.0, su = 0.0; /* reading R7: bf16 x bf16 products are exact */
+        for (int h = 0; h < H; ++h) {
+          sg += (double)(bf16_to_f32(g13[(int64_t)r * H + h]) * xf[h]);
+          su += (double)(bf16_to_f32(g13[(int64_t)(I + r) * H + h]) * xf[h]);
+        }
+        const float g = (float)sg, u = (float)su;
+        act[r] = round_bf16(silu_exact(g) * u);
+        if (act_o)
+          act_o[((int64_t)t * k + j) * I + r] = f32_to_bf16(act[r]);
+      }
+      const uint16_t* g2 = w2 + e * (int64_t)H * I;
+      for (int h = 0; h < H; ++h) {
+        double sum = 0.0;
+        for (int i = 0; i < I; ++i)
+          sum += (double)(bf16_to_f32(g2[(int64_t)h * I + i]) * act[i]);
+        const float y = round_bf16((float)sum); /* y_e = bf16(acc) */
+        if (y_o)
+          y_o[((int64_t)t * k + j) * H + h] = f32_to_bf16(y);
+        R[h] = R[h] + tw[j] * y;
+      }
+    }
+    for (int h = 0; h < H; ++h) {
+      const float sh = shared_out ? bf16_to_f32(shared_out[(int64_t)t * H + h]) : 0.0f;
+      out[(int64_t)t * H + h] = f32_to_bf16(round_bf16(R[h]) + sh);
+    }
+    for (int j = 0; j < k; ++j) {
+      if (ids_o)
+        ids_o[(int64_t)t * k + j] = ids[j];
+      if (tw_o)
+        tw_o[(int64_t)t * k + j] = tw[j];
+    }
+    free(xf);
+    free(act);
+    free(R);
   }
   return 0;
 }

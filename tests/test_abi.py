@@ -217,3 +217,23 @@ def test_forward_add_norm_validation_is_synchronous():
     empty = _lib.flint_moe_shape(0, 256, 8, 2, 128, 128)
     assert lib.flint_moe_forward_add_norm(*([None] * 3), 1e-6, *([None] * 9), ctypes.byref(empty),
                                           *([None] * 6), 0, None) == fm.FLINT_OK
+
+
+def test_forward_bf16_validation_is_synchronous():
+    """The BF16-experts entry point refuses a shared intermediate size (the
+    shared output comes in as a tensor), more than 64 tokens and odd
+    multiples of 64, before any CUDA call."""
+    lib = fm.load()
+    f = [0x10000 * (i + 1) for i in range(12)]
+
+    def call(shape, ws_bytes=1 << 30, x=f[0]):
+        s = _lib.flint_moe_shape(*shape)
+        return lib.flint_moe_forward_bf16(x, f[1], f[2], f[3], None, ctypes.byref(s), f[4], None, None,
+                                          f[5], ws_bytes, None)
+
+    assert call((2, 256, 8, 2, 128, 128)) == fm.FLINT_ERR_INVALID_ARG
+    assert call((65, 256, 8, 2, 128, 0)) == fm.FLINT_ERR_UNSUPPORTED
+    assert call((2, 192, 8, 2, 128, 0)) == fm.FLINT_ERR_UNSUPPORTED
+    assert call((2, 256, 8, 2, 128, 0), x=None) == fm.FLINT_ERR_INVALID_ARG
+    assert call((2, 256, 8, 2, 128, 0), ws_bytes=16) == fm.FLINT_ERR_WORKSPACE
+    assert call((0, 256, 8, 2, 128, 0), x=None) == fm.FLINT_OK

@@ -464,3 +464,34 @@ def test_kernel_spans_are_recorded(decode_layer):
     torch.cuda.synchronize()
     assert int(buf.abs().sum()) == 0
     assert fm.flint_moe_status(ws) == fm.FLINT_OK
+
+
+# ------------------------------------------------- BF16 routed experts
+@pytest.mark.parametrize("shape", [(1, 2048, 128, 8, 768), (8, 2048, 128, 8, 768), (64, 512, 64, 6, 256),
+                                   (5, 256, 8, 1, 128)])
+def test_forward_bf16_experts(shape):
+    """flint_moe_forward_bf16 (BF16 routed experts, shared output given):
+    ids bit-exact, the rule as stated; its sums are exact, so the outputs
+    match the oracle's bit for bit but for rare ties of the final roundings."""
+    M, H, E, k, I = shape
+    g = torch.Generator(device="cuda").manual_seed(700 + M)
+    x = synth.make_x(M, H, g, "cuda")
+    wr = (torch.randn(E, H, generator=g, device="cuda") * H ** -0.5).to(torch.bfloat16)
+    w13 = (torch.randn(E, 2 * I, H, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    w2 = (torch.randn(E, H, I, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    sh = (torch.randn(M, H, generator=g, device="cuda") * 0.05).to(torch.bfloat16)
+    ws = fm.alloc_workspace(M, H, E, k, I, 0)
+    out = torch.empty_like(x)
+    ids = torch.empty(M, k, dtype=torch.int32, device="cuda")
+    tw = torch.empty(M, k, dtype=torch.float32, device="cuda")
+    fm.flint_moe_forward_bf16(x, wr, w13, w2, k, out, ws, shared_out=sh, ids_out=ids, tw_out=tw)
+    assert fm.flint_moe_status(ws) == fm.FLINT_OK
+    ref = oracle.forward_bf16(x.cpu(), wr.cpu(), w13.cpu(), w2.cpu(), k, shared_out=sh.cpu())
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    st = check_bf16(bits(out), ref["out"], "out")
+    assert st["n_exact"] >= st["n"] - max(2, st["n"] // 10000), st
+    # no shared expert; the workspace serves the next call
+    fm.flint_moe_forward_bf16(x, wr, w13, w2, k, out, ws)
+    ref0 = oracle.forward_bf16(x.cpu(), wr.cpu(), w13.cpu(), w2.cpu(), k)
+    check_bf16(bits(out), ref0["out"], "out without shared")
+    assert fm.flint_moe_status(ws) == fm.FLINT_OK

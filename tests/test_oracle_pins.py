@@ -431,3 +431,65 @@ def test_add_rms_norm_eps_enters_before_the_root():
     a = torch.full((1, H), 2.0 ** -10).to(torch.bfloat16)
     _, xn = oracle.add_rms_norm(a, z, one, 3 * 2.0 ** -20)
     assert (bits_to_f64(xn) == 0.5).all()
+
+
+# ------------------------------------------------- BF16 routed experts (R9)
+def _bf16_layer_from_nvfp4(layer, gs_log2: int):
+    """BF16 expert weights equal to the NVFP4 ones times 2^gs_log2 (exact in
+    bf16: an e2m1 x e4m3 product has at most 6 significant bits)."""
+    E, I, H = layer.E, layer.I, layer.H
+    d13 = oracle.nvfp4_dequant(layer.w13.reshape(E * 2 * I, H // 2), layer.w13_sf.reshape(E * 2 * I, H // 16), H)
+    d2 = oracle.nvfp4_dequant(layer.w2.reshape(E * H, I // 2), layer.w2_sf.reshape(E * H, I // 16), I)
+    s = 2.0 ** gs_log2
+    w13 = torch.from_numpy((d13 * s).astype(np.float32)).reshape(E, 2 * I, H).to(torch.bfloat16)
+    w2 = torch.from_numpy((d2 * s).astype(np.float32)).reshape(E, H, I).to(torch.bfloat16)
+    assert torch.equal(w13.float(), torch.from_numpy((d13 * s).astype(np.float32)).reshape(E, 2 * I, H))
+    return w13, w2
+
+
+def test_bf16_experts_reduce_to_nvfp4_with_power_of_two_scales():
+    """With every global scale 2^-9, the NVFP4 block scales the accumulator
+    by an exact power of two, so BF16 experts holding the dequantised weights
+    times 2^-9 give the same g, u, act, y and outputs bit for bit (shared
+    output = the NVFP4 oracle's ys)."""
+    M, H, E, k, I, SI = 6, 256, 8, 3, 128, 128
+    x, layer = synth.make_problem(M, H, E, k, I, SI, seed=21)
+    layer.w13_gs.fill_(2.0 ** -9)
+    layer.w2_gs.fill_(2.0 ** -9)
+    r4 = oracle.forward(x, layer, k, intermediates=True)
+    w13, w2 = _bf16_layer_from_nvfp4(layer, -9)
+    ys = torch.from_numpy(r4["ys"].view(np.int16)).view(torch.bfloat16)
+    rb = oracle.forward_bf16(x, layer.router_w, w13, w2, k, shared_out=ys, intermediates=True)
+    assert np.array_equal(rb["ids"], r4["ids"]) and np.array_equal(rb["tw"], r4["tw"])
+    assert np.array_equal(rb["act"], r4["act"])
+    assert np.array_equal(rb["y"], r4["y"])
+    assert np.array_equal(rb["out"], r4["out"])
+
+
+def test_bf16_experts_match_float64():
+    """An independent float64 derivation (torch matmuls on the bf16 weights,
+    the stated BF16 roundings), within the rule; the shared output enters
+    as given."""
+    M, H, E, k, I = 5, 256, 8, 2, 128
+    g = torch.Generator().manual_seed(4)
+    x = torch.randn(M, H, generator=g).to(torch.bfloat16)
+    wr = (torch.randn(E, H, generator=g) * H ** -0.5).to(torch.bfloat16)
+    w13 = (torch.randn(E, 2 * I, H, generator=g) * 0.05).to(torch.bfloat16)
+    w2 = (torch.randn(E, H, I, generator=g) * 0.05).to(torch.bfloat16)
+    sh = (torch.randn(M, H, generator=g) * 0.1).to(torch.bfloat16)
+    r = oracle.forward_bf16(x, wr, w13, w2, k, shared_out=sh)
+    xf = x.double()
+    want = np.empty((M, H), np.uint16)
+    for t in range(M):
+        R = torch.zeros(H, dtype=torch.float64)
+        for j in range(k):
+            e = int(r["ids"][t, j])
+            gu = w13[e].double() @ xf[t]
+            gg, uu = gu[:I], gu[I:]
+            act = (gg / (1 + torch.exp(-gg)) * uu).float().to(torch.bfloat16).double()
+            y = (w2[e].double() @ act).float().to(torch.bfloat16).double()
+            R += float(r["tw"][t, j]) * y
+        Rb = R.float().to(torch.bfloat16).double()
+        want[t] = _bf16((Rb + sh[t].double()).float())
+    st = check_bf16(r["out"], want)
+    assert st["n_exact"] > 0.95 * st["n"]

@@ -163,6 +163,29 @@ int flint_moe_forward_add_norm(const void* attn_out, const void* residual, const
                                void* residual_out, void* xn_out, int32_t* ids_out, float* tw_out,
                                void* workspace, size_t workspace_bytes, flint_stream_t stream);
 
+/* The MoE block with an NVFP4 shared expert (the shared expert of
+ * "LLMoEWeights" on the page above: ModelOpt-packed gate/up and down with
+ * block scales and an fp32 global scale each).  The shared expert follows
+ * the routed experts' rule: g, u = fp32(sum) * sgu_gs,
+ * sact = bf16(silu(g) * u), ys = bf16(fp32(sum) * sdown_gs), and
+ * out = bf16(bf16(routed) + ys); its sums are exact (as in the single-launch
+ * path).  The routed part takes the path flint_moe_plan names for the shape
+ * with SI = 0.
+ *
+ *   sgu       uint8 [2*SI, H/2]   e2m1 codes, gate rows then up rows
+ *   sgu_sf    uint8 [2*SI, H/16]  e4m3 block scales;  sgu_gs fp32 [1]
+ *   sdown     uint8 [H, SI/2],  sdown_sf uint8 [H, SI/16],  sdown_gs fp32 [1]
+ *   the other arguments as for flint_moe_forward (shape->SI >= 128; the
+ *   workspace is the one flint_moe_workspace_bytes(shape) sizes). */
+int flint_moe_forward_nvfp4_shared(const void* x, const void* router_w, const uint8_t* w13,
+                                   const uint8_t* w13_sf, const float* w13_gs, const uint8_t* w2,
+                                   const uint8_t* w2_sf, const float* w2_gs, const uint8_t* sgu,
+                                   const uint8_t* sgu_sf, const float* sgu_gs,
+                                   const uint8_t* sdown, const uint8_t* sdown_sf,
+                                   const float* sdown_gs, const flint_moe_shape* shape, void* out,
+                                   int32_t* ids_out, float* tw_out, void* workspace,
+                                   size_t workspace_bytes, flint_stream_t stream);
+
 /* The decode MoE block on BF16 routed experts: "flint_moe_bf16_decode" on
  * the page above.  The same routing as flint_moe_route, then per selected
  * expert act = bf16(silu(g) * u) from the fp32 gate/up sums (no global
@@ -280,7 +303,8 @@ enum {
   FLINT_SPAN_ROUTE = 0, FLINT_SPAN_GATE_UP = 1, FLINT_SPAN_DOWN = 2, FLINT_SPAN_SINGLE_LAUNCH = 3,
   FLINT_SPAN_GROUP_COUNT = 4, FLINT_SPAN_GROUP_SCAN = 5, FLINT_SPAN_GROUP_SCATTER = 6,
   FLINT_SPAN_PLAN = 7, FLINT_SPAN_GATHER = 8, FLINT_SPAN_GEMM1 = 9, FLINT_SPAN_GEMM2 = 10,
-  FLINT_SPAN_COMBINE = 11, FLINT_SPAN_ADD_NORM = 12,
+  FLINT_SPAN_COMBINE = 11, FLINT_SPAN_ADD_NORM = 12, FLINT_SPAN_SHARED_GATE_UP = 13,
+  FLINT_SPAN_SHARED_DOWN = 14, FLINT_SPAN_SHARED_ADD = 15,
   FLINT_SPAN_KERNELS = 16, FLINT_SPAN_CTAS = 1024
 };
 int flint_moe_record_spans(unsigned long long* spans);

@@ -34,7 +34,8 @@ EXPORTED = ("flint_moe_workspace_bytes", "flint_moe_route", "flint_moe_forward",
             "flint_moe_route_noalloc", "flint_moe_route_noalloc_bytes",
             "flint_moe_route_noalloc_capacity", "flint_moe_status", "flint_moe_strerror",
             "flint_moe_debug_fault", "flint_moe_plan", "flint_moe_prefer_path",
-            "flint_moe_forward_add_norm", "flint_moe_record_spans", "flint_moe_forward_bf16")
+            "flint_moe_forward_add_norm", "flint_moe_record_spans", "flint_moe_forward_bf16",
+            "flint_moe_forward_nvfp4_shared")
 
 
 class FlintMoEError(RuntimeError):
@@ -89,6 +90,8 @@ def load() -> ctypes.CDLL:
             lib.flint_moe_plan.argtypes = [S]
             lib.flint_moe_prefer_path.restype = ctypes.c_int
             lib.flint_moe_prefer_path.argtypes = [ctypes.c_int]
+            lib.flint_moe_forward_nvfp4_shared.restype = ctypes.c_int
+            lib.flint_moe_forward_nvfp4_shared.argtypes = [P] * 14 + [S, P, P, P, P, ctypes.c_size_t, P]
             lib.flint_moe_forward_bf16.restype = ctypes.c_int
             lib.flint_moe_forward_bf16.argtypes = [P] * 5 + [S, P, P, P, P, ctypes.c_size_t, P]
             lib.flint_moe_record_spans.restype = ctypes.c_int
@@ -156,6 +159,25 @@ def flint_moe_forward(x, router_w, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, shared
         _ptr(tw_out), _ptr(workspace), workspace.numel(), _stream(stream))
     if rc != FLINT_OK:
         raise FlintMoEError(rc, "flint_moe_forward")
+
+
+def flint_moe_forward_nvfp4_shared(x, router_w, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, sgu, sgu_sf, sgu_gs,
+                                   sdown, sdown_sf, sdown_gs, top_k: int, out, workspace, ids_out=None,
+                                   tw_out=None, stream=None) -> None:
+    """The block with an NVFP4 shared expert (codes, e4m3 scale bytes and a
+    one-element fp32 global scale for its gate/up and its down)."""
+    M, H = x.shape
+    E = router_w.shape[0]
+    I = w2.shape[2] * 2
+    SI = sgu.shape[0] // 2
+    s = _shape(M, H, E, top_k, I, SI)
+    rc = load().flint_moe_forward_nvfp4_shared(
+        _ptr(x), _ptr(router_w), _ptr(w13), _ptr(w13_sf), _ptr(w13_gs), _ptr(w2), _ptr(w2_sf), _ptr(w2_gs),
+        _ptr(sgu), _ptr(sgu_sf), _ptr(sgu_gs), _ptr(sdown), _ptr(sdown_sf), _ptr(sdown_gs), ctypes.byref(s),
+        _ptr(out), _ptr(ids_out), _ptr(tw_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    if rc != FLINT_OK:
+        raise FlintMoEError(rc, "flint_moe_forward_nvfp4_shared")
 
 
 def flint_moe_forward_bf16(x, router_w, w13, w2, top_k: int, out, workspace, shared_out=None,
@@ -232,7 +254,8 @@ def flint_moe_prefer_path(path: int) -> None:
 
 
 SPAN_NAMES = ("route", "gate_up", "down", "single_launch", "group_count", "group_scan",
-              "group_scatter", "plan", "gather", "gemm1", "gemm2", "combine", "add_norm")
+              "group_scatter", "plan", "gather", "gemm1", "gemm2", "combine", "add_norm",
+              "shared_gate_up", "shared_down", "shared_add")
 SPAN_KERNELS = 16
 SPAN_CTAS = 1024
 

@@ -310,6 +310,42 @@ int flint_moe_forward_bf16(const void* x, const void* router_w, const void* w13,
   return FLINT_OK;
 }
 
+int flint_moe_forward_nvfp4_shared(const void* x, const void* router_w, const uint8_t* w13,
+                                   const uint8_t* w13_sf, const float* w13_gs, const uint8_t* w2,
+                                   const uint8_t* w2_sf, const float* w2_gs, const uint8_t* sgu,
+                                   const uint8_t* sgu_sf, const float* sgu_gs, const uint8_t* sdown,
+                                   const uint8_t* sdown_sf, const float* sdown_gs, const flint_moe_shape* shape,
+                                   void* out, int32_t* ids_out, float* tw_out, void* workspace,
+                                   size_t workspace_bytes, flint_stream_t stream) {
+  if (!shape_valid(shape) || shape->SI < 128) return FLINT_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return FLINT_ERR_UNSUPPORTED;
+  if (shape->M == 0) return FLINT_OK;
+  if (!sgu || !sgu_sf || !sgu_gs || !sdown || !sdown_sf || !sdown_gs) return FLINT_ERR_INVALID_ARG;
+  const void* p16[] = {sgu, sgu_sf, sdown, sdown_sf};
+  for (const void* p : p16)
+    if (!aligned(p, 16)) return FLINT_ERR_INVALID_ARG;
+  if (!aligned(sgu_gs, 4) || !aligned(sdown_gs, 4)) return FLINT_ERR_INVALID_ARG;
+  // the routed block: the checks and kernels of flint_moe_forward without a
+  // shared expert, on the workspace laid out for the whole shape
+  flint_moe_shape routed = *shape;
+  routed.SI = 0;
+  const int rc = check_forward(x, router_w, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, nullptr, nullptr, &routed,
+                               out, ids_out, tw_out, workspace, workspace_bytes);
+  if (rc != FLINT_OK) return rc;
+  if (workspace_bytes < ws_layout(*shape).total) return FLINT_ERR_WORKSPACE;
+  MoEArgs a = make_args(x, router_w, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, nullptr, nullptr, shape, out,
+                        ids_out, tw_out, workspace);
+  a.SI = 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int r = enqueue_forward(a, &routed, st);
+  if (r != FLINT_OK) return r;
+  if (launch_shared_nvfp4(static_cast<const uint16_t*>(x), sgu, sgu_sf, sgu_gs, sdown, sdown_sf, sdown_gs,
+                          shape->M, shape->H, shape->SI, a.ws.sact, a.ws.ys, static_cast<uint16_t*>(out),
+                          st) != cudaSuccess)
+    return FLINT_ERR_CUDA;
+  return FLINT_OK;
+}
+
 int flint_moe_plan(const flint_moe_shape* shape) {
   if (!shape_valid(shape)) return FLINT_ERR_INVALID_ARG;
   if (!shape_supported(shape)) return FLINT_ERR_UNSUPPORTED;
@@ -343,7 +379,8 @@ int flint_moe_record_spans(unsigned long long* spans) {
   cudaError_t (*const set[])(unsigned long long*) = {span_buffer_set_decode2, span_buffer_set_decode,
                                                      span_buffer_set_fused, span_buffer_set_grouped,
                                                      span_buffer_set_route, span_buffer_set_add_norm,
-                                                     span_buffer_set_bf16_experts};
+                                                     span_buffer_set_bf16_experts,
+                                                     span_buffer_set_shared_nvfp4};
   for (auto f : set)
     if (f(spans) != cudaSuccess) return FLINT_ERR_CUDA;
   return FLINT_OK;

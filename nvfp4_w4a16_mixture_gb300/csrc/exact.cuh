@@ -180,20 +180,22 @@ FLINT_DEV uint32_t split_const(int ef) {
   return cb | (cb << 16);
 }
 
-// One 128-K slice of a 16-row BF16 tile (rows g, g + 8 in natural order at
-// ra / rb, this lane's 32 K at offset 32 t of the slice) against xb: the
-// weights are split per row over the slice, w_hi * x_hi accumulates exactly
-// in one chained mma (products of two <= 6-bit integers, 128 of them), the
-// rest goes to C.  The grids come first (one pass over the words); the
-// words are then split one at a time, so few registers stay live.
-FLINT_DEV void slice_bf16_exact(float (&S)[4], float (&C)[4], const uint16_t* ra, const uint16_t* rb,
-                                const uint4 (&xb)[4]) {
+// One 128-K slice of a 16-row tile against xb, exactly: rows g and g + 8
+// are read through la(q) / lb(q) (word q = K 32 t + 8 q .. + 7 of the slice
+// as 8 bf16 in natural order), the lane's activations are xb.  Weights and
+// activations are split per row / column over the slice (split_hi_lo grids),
+// w_hi * x_hi accumulates exactly in one chained mma (products of two <= 6-bit
+// integers, 128 of them), the rest goes to C.  The grids come first (one pass
+// over the words); the words are then split one at a time, so few registers
+// stay live.
+template <class RowA, class RowB>
+FLINT_DEV void slice_exact(float (&S)[4], float (&C)[4], RowA la, RowB lb, const uint4 (&xb)[4]) {
   int ex = 0, ea = 0, eb = 0;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     ex = max(ex, max_exp_word(xb[q]));
-    ea = max(ea, max_exp_word(*reinterpret_cast<const uint4*>(ra + 8 * q)));
-    eb = max(eb, max_exp_word(*reinterpret_cast<const uint4*>(rb + 8 * q)));
+    ea = max(ea, max_exp_word(la(q)));
+    eb = max(eb, max_exp_word(lb(q)));
   }
 #pragma unroll
   for (int o = 1; o <= 2; o <<= 1) {
@@ -205,8 +207,7 @@ FLINT_DEV void slice_bf16_exact(float (&S)[4], float (&C)[4], const uint16_t* ra
   float hh[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ap[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint4 wa = *reinterpret_cast<const uint4*>(ra + 8 * q);
-    const uint4 wb = *reinterpret_cast<const uint4*>(rb + 8 * q);
+    const uint4 wa = la(q), wb = lb(q);
     uint4 xh, xl, wah, wal, wbh, wbl;
     split_word(xb[q], cx, xh, xl);
     split_word(wa, ca, wah, wal);
@@ -229,6 +230,40 @@ FLINT_DEV void slice_bf16_exact(float (&S)[4], float (&C)[4], const uint16_t* ra
     two_sum(S[i], C[i], hh[i]);
     C[i] = __fadd_rn(C[i], ap[i]);
   }
+}
+
+// The slice of a 16-row BF16 tile (rows g, g + 8 in natural order at ra /
+// rb, this lane's 32 K at offset 32 t of the slice).
+FLINT_DEV void slice_bf16_exact(float (&S)[4], float (&C)[4], const uint16_t* ra, const uint16_t* rb,
+                                const uint4 (&xb)[4]) {
+  slice_exact(S, C, [&](int q) { return *reinterpret_cast<const uint4*>(ra + 8 * q); },
+              [&](int q) { return *reinterpret_cast<const uint4*>(rb + 8 * q); }, xb);
+}
+
+// 8 NVFP4 weights (one word of codes, K 2b in the low nibble of byte b) as
+// 8 bf16 e2m1 * scale * 2^-7 in natural order, exactly; sc: bf16x2 of the
+// block's scale * 2^119 (twice).
+FLINT_DEV uint4 nvfp4_word_bf16(uint32_t w, uint32_t sc) {
+  uint32_t o[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t byte = (w >> (8 * b)) & 0xFFu;
+    o[b] = bf16x2_mul(e2m1x2_to_bf16x2_scaled((byte & 0xFu) | ((byte >> 4) << 16)), sc);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// The slice of a 16-row NVFP4 tile: ca / cb this lane's 16 code bytes of
+// rows g, g + 8 (K 32 t .. 32 t + 31 of the slice), sa / sb their two block
+// scale bytes (blocks 2 t, 2 t + 1).  The sums are of the weights times
+// 2^-7: the caller scales them back.
+FLINT_DEV void slice_nvfp4_exact(float (&S)[4], float (&C)[4], const uint8_t* ca, const uint8_t* cb,
+                                 uint32_t sa, uint32_t sb, const uint4 (&xb)[4]) {
+  const uint32_t a2 = e4m3x2_to_bf16x2_x2p119(sa), b2 = e4m3x2_to_bf16x2_x2p119(sb);
+  const uint4 wa = *reinterpret_cast<const uint4*>(ca), wb = *reinterpret_cast<const uint4*>(cb);
+  const uint32_t wa4[4] = {wa.x, wa.y, wa.z, wa.w}, wb4[4] = {wb.x, wb.y, wb.z, wb.w};
+  slice_exact(S, C, [&](int q) { return nvfp4_word_bf16(wa4[q], bf16x2_bcast(a2, q >> 1)); },
+              [&](int q) { return nvfp4_word_bf16(wb4[q], bf16x2_bcast(b2, q >> 1)); }, xb);
 }
 
 }  // namespace

@@ -159,6 +159,13 @@ cudaError_t span_buffer_set_grouped(unsigned long long* b);
 cudaError_t span_buffer_set_route(unsigned long long* b);
 cudaError_t span_buffer_set_add_norm(unsigned long long* b);
 cudaError_t span_buffer_set_bf16_experts(unsigned long long* b);
+cudaError_t span_buffer_set_shared_nvfp4(unsigned long long* b);
+
+// NVFP4 shared expert (shared_nvfp4.cu): sact and ys (workspace), then
+// out = bf16(out + ys) over the block's routed output.
+cudaError_t launch_shared_nvfp4(const uint16_t* x, const uint8_t* gu, const uint8_t* gu_sf, const float* gu_gs,
+                                const uint8_t* dn, const uint8_t* dn_sf, const float* dn_gs, int M, int H,
+                                int SI, uint16_t* sact, uint16_t* ys, uint16_t* out, cudaStream_t st);
 
 // BF16 routed experts (bf16_experts.cu), M <= kDecodeMaxTokens: router with
 // the expert grouping, exact gate/up and down sums, combine with the given

@@ -62,6 +62,9 @@ def _load():
             lib.oracle_topk.argtypes = [P, i32, i32, i32, P, P]
             lib.oracle_forward.restype = i32
             lib.oracle_forward.argtypes = [P] * 10 + [i32] * 6 + [P, i32] + [P] * 8 + [i32]
+            lib.oracle_shared_nvfp4.restype = i32
+            lib.oracle_shared_nvfp4.argtypes = [P, P, P, ctypes.c_float, P, P, ctypes.c_float, i32, i32, i32,
+                                                P, P]
             lib.oracle_forward_bf16.restype = i32
             lib.oracle_forward_bf16.argtypes = [P] * 5 + [i32] * 5 + [P] * 5 + [i32]
             lib.oracle_add_rms_norm.restype = i32
@@ -188,6 +191,25 @@ def forward(x, layer, top_k: int, tokens=None, intermediates: bool = False, nthr
     if rc != 0:
         raise ValueError("oracle_forward: invalid shape or token list")
     return res
+
+
+def shared_nvfp4(x, sgu, sgu_sf, sgu_gs: float, sdn, sdn_sf, sdn_gs: float):
+    """NVFP4 shared expert (reading R10): returns (ys bits [M, H], sact bits
+    [M, SI])."""
+    xa = _np(x, np.uint16)
+    M, H = xa.shape
+    ga, gfa = _np(sgu, np.uint8), _np(sgu_sf, np.uint8)
+    da, dfa = _np(sdn, np.uint8), _np(sdn_sf, np.uint8)
+    SI = ga.shape[0] // 2
+    assert ga.shape == (2 * SI, H // 2) and gfa.shape == (2 * SI, H // 16)
+    assert da.shape == (H, SI // 2) and dfa.shape == (H, SI // 16)
+    ys = np.empty((M, H), np.uint16)
+    sact = np.empty((M, SI), np.uint16)
+    rc = _load().oracle_shared_nvfp4(_ptr(xa), _ptr(ga), _ptr(gfa), float(sgu_gs), _ptr(da), _ptr(dfa),
+                                     float(sdn_gs), M, H, SI, _ptr(ys), _ptr(sact))
+    if rc != 0:
+        raise ValueError("oracle_shared_nvfp4: invalid shape")
+    return ys, sact
 
 
 def forward_bf16(x, router_w, w13, w2, top_k: int, shared_out=None, intermediates: bool = False,

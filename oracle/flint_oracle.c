@@ -49,6 +49,12 @@
  *      expert's output given (zero when absent).  The pages store the BF16
  *      experts in a blocked order (BlockMajorK); here they are row-major
  *      [E, 2I, H] and [E, H, I].
+ *  R10 an NVFP4 shared expert (LLMoEWeights on the same page: ModelOpt-packed
+ *      gate/up and down with block scales and an fp32 global scale each)
+ *      follows the routed experts' rule, as the page passes it to the same
+ *      kernels: g, u = fp32(exact dot) * gs_gu, sact = bf16(silu(g) * u)
+ *      (R4 form), ys = bf16(fp32(exact dot(sact, Wd)) * gs_d); the block's
+ *      output is then bf16(bf16(routed) + ys) as with the BF16 shared expert.
  *  R7  "products are accumulated in fp32" fixes the accumulator's type, not
  *      the order of the additions.  Every expert and shared-expert dot
  *      product therefore takes the order-independent value: the exact sum of
@@ -386,6 +392,47 @@ ORACLE_API int oracle_forward(const uint16_t* x, const uint16_t* wr, const uint8
                   tw ? tw + (int64_t)i * k : NULL, logits ? logits + (int64_t)i * E : NULL,
                   act ? act + (int64_t)i * k * I : NULL, y ? y + (int64_t)i * k * H : NULL,
                   sact ? sact + (int64_t)i * SI : NULL, ys ? ys + (int64_t)i * H : NULL);
+  }
+  return 0;
+}
+
+/* NVFP4 shared expert (reading R10) of token rows x [M, H]: ys [M, H] and,
+ * optionally, sact [M, SI] (bf16 bits).  sgu codes [2SI, H/2] (gate rows
+ * then up rows), sf [2SI, H/16]; sdn codes [H, SI/2], sf [H, SI/16]. */
+ORACLE_API int oracle_shared_nvfp4(const uint16_t* x, const uint8_t* sgu, const uint8_t* sgu_sf,
+                                   float sgu_gs, const uint8_t* sdn, const uint8_t* sdn_sf,
+                                   float sdn_gs, int M, int H, int SI, uint16_t* ys_o,
+                                   uint16_t* sact_o) {
+  if (M < 0 || H <= 0 || H % 16 != 0 || SI <= 0 || SI % 16 != 0)
+    return -1;
+  init_tables();
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int t = 0; t < M; ++t) {
+    float* xf = (float*)malloc(sizeof(float) * (size_t)H);
+    float* sact = (float*)malloc(sizeof(float) * (size_t)SI);
+    for (int h = 0; h < H; ++h)
+      xf[h] = bf16_to_f32(x[(int64_t)t * H + h]);
+    for (int r = 0; r < SI; ++r) {
+      double sg = 0.0, su = 0.0; /* reading R7 */
+      for (int h = 0; h < H; ++h) {
+        sg += (double)(nvfp4_deq(sgu, sgu_sf, r, H, h) * xf[h]);
+        su += (double)(nvfp4_deq(sgu, sgu_sf, SI + r, H, h) * xf[h]);
+      }
+      const float g = (float)sg * sgu_gs, u = (float)su * sgu_gs;
+      sact[r] = round_bf16(silu_exact(g) * u);
+      if (sact_o)
+        sact_o[(int64_t)t * SI + r] = f32_to_bf16(sact[r]);
+    }
+    for (int h = 0; h < H; ++h) {
+      double sum = 0.0;
+      for (int i = 0; i < SI; ++i)
+        sum += (double)(nvfp4_deq(sdn, sdn_sf, h, SI, i) * sact[i]);
+      ys_o[(int64_t)t * H + h] = f32_to_bf16((float)sum * sdn_gs);
+    }
+    free(xf);
+    free(sact);
   }
   return 0;
 }

@@ -495,3 +495,35 @@ def test_forward_bf16_experts(shape):
     ref0 = oracle.forward_bf16(x.cpu(), wr.cpu(), w13.cpu(), w2.cpu(), k)
     check_bf16(bits(out), ref0["out"], "out without shared")
     assert fm.flint_moe_status(ws) == fm.FLINT_OK
+
+
+# -------------------------------------------------- NVFP4 shared expert
+@pytest.mark.parametrize("shape", [(1, 2048, 128, 8, 768, 768), (16, 2048, 128, 8, 768, 768),
+                                   (100, 384, 24, 4, 256, 256)])
+def test_forward_nvfp4_shared(shape):
+    """flint_moe_forward_nvfp4_shared: ids bit-exact; out against the oracle's
+    routed block (SI = 0) plus its NVFP4 shared expert, bf16(bf16(R) + ys),
+    under the allowance of the path the routed part takes (M = 100 runs the
+    grouped path)."""
+    M, H, E, k, I, SI = shape
+    x, layer = synth.make_problem(M, H, E, k, I, 0, seed=M + 17, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(800 + M)
+    gu_c, gu_sf, gu_gs = synth.quantize_nvfp4(torch.randn(2 * SI, H, generator=g, device="cuda") * 0.02)
+    dn_c, dn_sf, dn_gs = synth.quantize_nvfp4(torch.randn(H, SI, generator=g, device="cuda") * 0.02)
+    gu_gs, dn_gs = gu_gs.reshape(1).contiguous(), dn_gs.reshape(1).contiguous()
+    ws = fm.alloc_workspace(M, H, E, k, I, SI)
+    out = torch.empty_like(x)
+    ids = torch.empty(M, k, dtype=torch.int32, device="cuda")
+    fm.flint_moe_forward_nvfp4_shared(x, layer.router_w, layer.w13, layer.w13_sf, layer.w13_gs, layer.w2,
+                                      layer.w2_sf, layer.w2_gs, gu_c, gu_sf, gu_gs, dn_c, dn_sf, dn_gs, k,
+                                      out, ws, ids_out=ids)
+    assert fm.flint_moe_status(ws) == fm.FLINT_OK
+    xc, lc = x.cpu(), layer.to("cpu")
+    r = oracle.forward(xc, lc, k)
+    ys, _ = oracle.shared_nvfp4(xc, gu_c.cpu(), gu_sf.cpu(), float(gu_gs), dn_c.cpu(), dn_sf.cpu(), float(dn_gs))
+    want = ((torch.from_numpy(r["out"].view(np.int16)).view(torch.bfloat16).float()
+             + torch.from_numpy(ys.view(np.int16)).view(torch.bfloat16).float()).to(torch.bfloat16))
+    assert np.array_equal(ids.cpu().numpy(), r["ids"])
+    got = bits(out)
+    check_bf16(got, want.view(torch.int16).numpy().view(np.uint16), "out",
+               allow_outside=allowance((M, H, E, k, I, 0), got.size))

@@ -493,3 +493,20 @@ def test_bf16_experts_match_float64():
         want[t] = _bf16((Rb + sh[t].double()).float())
     st = check_bf16(r["out"], want)
     assert st["n_exact"] > 0.95 * st["n"]
+
+
+# ------------------------------------------------ NVFP4 shared expert (R10)
+def test_nvfp4_shared_expert_is_a_routed_expert_of_weight_one():
+    """The NVFP4 shared expert follows the routed rule: a layer whose only
+    routed expert (E = 1, top_k = 1, so tw = 1 and bf16(R) = y) holds the
+    same NVFP4 weights and global scales gives ys = y and sact = act, bit
+    for bit."""
+    M, H, I = 5, 256, 128
+    x, layer = synth.make_problem(M, H, 1, 1, I, 0, seed=8)
+    r = oracle.forward(x, layer, 1, intermediates=True)
+    assert (r["tw"] == 1.0).all()
+    ys, sact = oracle.shared_nvfp4(x, layer.w13[0], layer.w13_sf[0], float(layer.w13_gs[0]),
+                                   layer.w2[0], layer.w2_sf[0], float(layer.w2_gs[0]))
+    assert np.array_equal(ys, r["y"][:, 0, :])
+    assert np.array_equal(sact, r["act"][:, 0, :])
+    assert np.array_equal(ys, r["out"])  # bf16(bf16(y) + 0) = y

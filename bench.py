@@ -264,12 +264,15 @@ SWEEP = ("decode2", "decode4", "decode8", "decode16", "decode32", "decode64", "p
 
 class Workload:
     """Resident weights and inputs of one configuration (several layers
-    rotated) and the graphs of its steps."""
+    rotated) and the graphs of its steps.  kind: "forward" (the block),
+    "add_norm" (the block with its add-RMSNorm prologue), "bf16" (BF16 routed
+    experts, shared output given), "nvfp4_shared" (NVFP4 shared expert)."""
 
-    def __init__(self, cfg, dev, rank, n_layers, layers=None):
+    def __init__(self, cfg, dev, rank, n_layers, layers=None, kind="forward"):
         import nvfp4_w4a16_mixture_gb300 as fm
         self.fm = fm
         self.cfg = cfg
+        self.kind = kind
         self.M, self.H, self.E, self.k, self.I, self.SI = synth.CONFIGS[cfg]
         self.n_layers = n_layers
         if layers is None:
@@ -281,12 +284,58 @@ class Workload:
         self.outs = [torch.empty_like(x) for x in self.xs]
         self.ids = [torch.empty(self.M, self.k, dtype=torch.int32, device=dev) for _ in self.xs]
         self.stream = torch.cuda.Stream(device=dev)
-        self.path = fm.flint_moe_plan(self.M, self.H, self.E, self.k, self.I, self.SI)
+        self.path = fm.flint_moe_plan(self.M, self.H, self.E, self.k, self.I,
+                                      0 if kind in ("bf16", "nvfp4_shared") else self.SI)
+        M, H, E, I, SI = self.M, self.H, self.E, self.I, self.SI
+        g = torch.Generator(device=dev).manual_seed(4242 + rank)
+        if kind == "add_norm":
+            self.res = [synth.make_x(M, H, g, dev) for _ in range(n_layers)]
+            self.res_out = [torch.empty_like(r) for r in self.res]
+            self.lnw = (1 + 0.1 * torch.randn(H, generator=g, device=dev)).to(torch.bfloat16)
+        elif kind == "bf16":
+            # BF16 routed experts of the same shapes (one set per rotated layer)
+            self.w13 = [(torch.randn(E, 2 * I, H, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+                        for _ in range(n_layers)]
+            self.w2 = [(torch.randn(E, H, I, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+                       for _ in range(n_layers)]
+            self.shared = [(torch.randn(M, H, generator=g, device=dev) * 0.05).to(torch.bfloat16)
+                           for _ in range(n_layers)]
+            self.ws = fm.alloc_workspace(M, H, E, self.k, I, 0, dev)
+        elif kind == "nvfp4_shared":
+            self.sh = []
+            for _ in range(n_layers):
+                gc, gf, gg = synth.quantize_nvfp4(torch.randn(2 * SI, H, generator=g, device=dev) * 0.02)
+                dc, df, dg = synth.quantize_nvfp4(torch.randn(H, SI, generator=g, device=dev) * 0.02)
+                self.sh.append((gc, gf, gg.reshape(1).contiguous(), dc, df, dg.reshape(1).contiguous()))
+
+    def bytes_per_step(self, unique_experts: float) -> float:
+        """Algorithmic weight bytes of one step."""
+        M, H, E, I, SI = self.M, self.H, self.E, self.I, self.SI
+        if self.kind == "bf16":
+            return unique_experts * 3 * I * H * 2 + E * H * 2 + M * H * 2
+        wb = synth.weight_bytes(H, E, I, SI, int(round(unique_experts)))
+        if self.kind == "nvfp4_shared":
+            return wb["total"] - wb["shared"] + 3 * SI * H // 2 + 3 * SI * H // 16
+        return wb["total"]
 
     def step(self, i, s):
         li = i % self.n_layers
-        self.fm.forward_layer(self.xs[li], self.layers[li], self.k, workspace=self.ws, out=self.outs[li],
-                              ids_out=self.ids[li], stream=s)
+        fm, L = self.fm, self.layers[li] if self.layers else None
+        if self.kind == "forward":
+            fm.forward_layer(self.xs[li], L, self.k, workspace=self.ws, out=self.outs[li], ids_out=self.ids[li],
+                             stream=s)
+        elif self.kind == "add_norm":
+            fm.forward_add_norm_layer(self.xs[li], self.res[li], self.lnw, 1e-6, L, self.k, workspace=self.ws,
+                                      out=self.outs[li], residual_out=self.res_out[li], ids_out=self.ids[li],
+                                      stream=s)
+        elif self.kind == "bf16":
+            fm.flint_moe_forward_bf16(self.xs[li], L.router_w, self.w13[li], self.w2[li], self.k, self.outs[li],
+                                      self.ws, shared_out=self.shared[li], ids_out=self.ids[li], stream=s)
+        else:
+            gc, gf, gg, dc, df, dg = self.sh[li]
+            fm.flint_moe_forward_nvfp4_shared(self.xs[li], L.router_w, L.w13, L.w13_sf, L.w13_gs, L.w2, L.w2_sf,
+                                              L.w2_gs, gc, gf, gg, dc, df, dg, self.k, self.outs[li], self.ws,
+                                              ids_out=self.ids[li], stream=s)
 
 
 def time_workload(w: Workload, steps: int, warmup: int, world: int, local: int):
@@ -360,15 +409,22 @@ def record_of(w: Workload, ms_total: float, steps: int, world: int, clk, peaks) 
     step_s = ms_step / 1e3
     uniq = [int(torch.unique(t).numel()) for t in w.ids]
     wb = [synth.weight_bytes(H, E, I, SI, u) for u in uniq]
-    mean_bytes = sum(x["total"] for x in wb) / len(wb)
+    mean_bytes = sum(w.bytes_per_step(u) for u in uniq) / len(uniq)
     mean_expert_bytes = sum(x["experts"] for x in wb) / len(wb)
+    if w.kind == "bf16":
+        mean_expert_bytes = sum(u * 3 * I * H * 2 for u in uniq) / len(uniq)
     flops = synth.flops_of(M, H, E, k, I, SI)
     rec = {"workload": workload_name(w.cfg), "tokens_per_step": M, "steps": steps,
            "ms_per_step": round(ms_step, 6),
            "tokens_per_s": round(job_tokens_per_s(M, steps, world, ms_total), 2),
-           "path": {1: "single launch", 2: "decode (3 kernels)", 3: "decode fallback (3 kernels)",
-                    4: "grouped (9 kernels)"}.get(w.path, str(w.path)),
-           "gpu_launches_per_step": launches_per_step(M, w.path),
+           "path": ({"forward": "", "add_norm": "add-RMSNorm kernel + ", "bf16": "",
+                     "nvfp4_shared": ""}[w.kind] +
+                    ({1: "single launch", 2: "decode (3 kernels)", 3: "decode fallback (3 kernels)",
+                      4: "grouped (9 kernels)"}.get(w.path, str(w.path)) if w.kind != "bf16" else
+                     "BF16 experts (router, gate/up, down, combine)") +
+                    (" + NVFP4 shared expert (gate/up, down, add)" if w.kind == "nvfp4_shared" else "")),
+           "gpu_launches_per_step": (4 if w.kind == "bf16" else launches_per_step(M, w.path) +
+                                     {"forward": 0, "add_norm": 1, "nvfp4_shared": 3}[w.kind]),
            "weight_gbs": round(mean_bytes / step_s / 1e9, 1),
            "expert_weight_gbs": round(mean_expert_bytes / step_s / 1e9, 1),
            "tflops": round(flops["total"] / step_s / 1e12, 3),
@@ -542,6 +598,24 @@ def run_ours(args, rank, world, local):
             r["kernel_spans"] = kernel_spans(wc, steps=10 if Mc > DECODE_MAX_TOKENS else 40)
             r["roofline"]["dominant_kernel"] = dominant_roofline(wc, r["kernel_spans"], peaks)
             r["gpu_launches"] = steps_c * r["gpu_launches_per_step"]
+            recs[c] = r
+            del wc
+            torch.cuda.empty_cache()
+        # the widened rows at the headline's shape: add-RMSNorm prologue, BF16
+        # routed experts, NVFP4 shared expert
+        wide = (("decode1_add_norm", "add_norm", n_layers,
+                 "NVFP4 experts, BF16 shared, residual add + RMSNorm before the router"),
+                ("decode1_bf16_experts", "bf16", 8, "BF16 routed experts, shared output given"),
+                ("decode1_nvfp4_shared", "nvfp4_shared", n_layers, "NVFP4 experts, NVFP4 shared"))
+        for c, kind, nl, what in (wide if synth.CONFIGS[cfg][1:] == synth.CONFIGS["decode1"][1:] else ()):
+            nl = min(nl, len(w.layers))
+            wc = Workload("decode1", dev, rank, nl, layers=w.layers[:nl], kind=kind)
+            ms_c, clk_c = time_workload(wc, 2000, 50, world, local)
+            r = record_of(wc, ms_c, 2000, world, clk_c, peaks)
+            r["workload"] = f"{c}: M=1 H={wc.H} E={wc.E} top_k={wc.k} I={wc.I} SI={wc.SI} ({what})"
+            r["traffic"] = None
+            r["roofline"]["traffic"] = None
+            r["gpu_launches"] = 2000 * r["gpu_launches_per_step"]
             recs[c] = r
             del wc
             torch.cuda.empty_cache()

@@ -55,10 +55,11 @@ constexpr int kKP = kCons / 2;  // K parts of a routed stage (x 2 A tiles)
 
 // ---- down ring: a stage holds up to 8 weight blocks of 16 output rows.
 constexpr int kDnStages = 3;
-// down stages whose weights are requested before the dependency wait; the
-// activation copies of stage 0 then go out right after it, ahead of the
-// later stages' weights
-constexpr int kDnPrefetch = 1;
+// down stages whose weights are requested before the dependency wait (the
+// kernel starts while gate/up is still running, so they have landed by the
+// time the activation copies go out)
+constexpr int kDnPrefetch = 3;
+static_assert(kDnPrefetch <= kDnStages, "prefetched stages fit the ring");
 constexpr int kDnStageBytes = 57344;
 constexpr int kDnMaxBlocks = 8;
 constexpr int kDnMaxItems = 64;
@@ -376,11 +377,15 @@ FLINT_DEV void gu_issue_routed(const MoEArgs& a, uint8_t* stage, GuInfo& inf, ui
     mbar_arrive_expect_tx(full, 32u * (kst / 2) + 32u * sfp);
   }
   __syncwarp();
-  if (whole) {  // four copies: gate codes, up codes, gate scales, up scales
-    if (lane == 0) bulk_g2s(stage, a.w13 + g0 * (H / 2), 16u * (H / 2), full);
-    if (lane == 1) bulk_g2s(stage + 16 * pitch, a.w13 + u0 * (H / 2), 16u * (H / 2), full);
-    if (lane == 2) bulk_g2s(stage + sf_off, a.w13_sf + g0 * (H / 16), 16u * sfp, full);
-    if (lane == 3) bulk_g2s(stage + sf_off + 16 * sfp, a.w13_sf + u0 * (H / 16), 16u * sfp, full);
+  if (whole) {  // four copies in one instruction: lanes 0, 1 the gate and up
+                // codes, lanes 2, 3 their scale rows
+    if (lane < 4) {
+      const size_t row = (lane & 1) ? u0 : g0;
+      const bool sc = lane >= 2;
+      uint8_t* dst = stage + (sc ? sf_off + (lane & 1) * 16 * sfp : (lane & 1) * 16 * pitch);
+      const uint8_t* src = sc ? a.w13_sf + row * (H / 16) : a.w13 + row * (H / 2);
+      bulk_g2s(dst, src, sc ? 16u * sfp : 16u * (H / 2), full);
+    }
   } else {  // a K chunk of each row, rows padded against bank conflicts
     const size_t row = lane < 16 ? g0 + lane : u0 + (lane - 16);
     bulk_g2s(stage + lane * pitch, a.w13 + row * (H / 2) + k0 / 2, kst / 2, full);
@@ -855,24 +860,36 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
     int n = 0, unit = 0, pend = 0;  // stages [pend, n) still need their activations
     bool waited = false;
     // Activation rows of a stage: copied once the gate/up grid has finished,
-    // then the producer's arrival completes the stage.
+    // one copy per block, all issued by one instruction of the warp (lane =
+    // block); then the producer's arrival completes the stage.
     auto finish = [&](int m) {
       const int sl = m % kDnStages;
       const DnInfo& inf = SM.info[sl];
       uint8_t* st = stages + (size_t)sl * kDnStageBytes;
       if (lane == 0) mbar_expect_tx(&SM.ctl.full[sl], (uint32_t)inf.abytes);
       __syncwarp();
-      for (int bi = lane; bi < inf.nblocks; bi += 32) {
-        const DnBlock& b = inf.blk[bi];
-        if (b.act_smem < 0) continue;
-        if (b.kind == 0)
-          bulk_g2s(st + b.act_smem, a.ws.sact, (uint32_t)M * SI * 2, &SM.ctl.full[sl]);
-        else
-          bulk_g2s(st + b.act_smem, a.ws.act + (size_t)b.off * I, (uint32_t)b.cnt * I * 2,
-                   &SM.ctl.full[sl]);
+      if (lane < inf.nblocks && inf.blk[lane].act_smem >= 0) {
+        const DnBlock& b = inf.blk[lane];
+        const uint16_t* srcp = b.kind == 0 ? a.ws.sact : a.ws.act + (size_t)b.off * I;
+        bulk_g2s(st + b.act_smem, srcp, (uint32_t)b.cnt * (b.kind == 0 ? SI : I) * 2u, &SM.ctl.full[sl]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&SM.ctl.full[sl]);
+    };
+    // Stage n takes units unit, unit + 1, ...: the longest run (at most
+    // kDnMaxBlocks) whose weight rows and activation rows fit the stage and
+    // whose items fit its table; a first unit whose activations alone do not
+    // fit is taken with them read from global memory.  Lane l looks at unit
+    // unit + l, so the plan is a few prefix sums over the lanes, and every
+    // block's copies go out in one instruction of the warp: a warp issuing
+    // bulk copies one lane at a time pays a round trip per copy.
+    auto prefix = [&](int v) {  // inclusive prefix sum over lanes 0 .. kDnMaxBlocks - 1
+#pragma unroll
+      for (int o = 1; o < kDnMaxBlocks; o <<= 1) {
+        const int w = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += w;
+      }
+      return v;
     };
     while (unit < nunits) {
       int ok = 1;
@@ -883,61 +900,65 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
       DnInfo& inf = SM.info[sl];
       // a stage holds at most kDnMaxBlocks units: move the window if needed
       if (unit - nsh + kDnMaxBlocks > win + 32) load_window(max(unit - nsh, 0));
-      int used = 0, nb = 0, ni = 0;
-      uint32_t wbytes = 0, abytes = 0;
-      while (unit < nunits && nb < kDnMaxBlocks) {  // same plan in every lane
-        const bool shared = nsh && unit == 0;
-        const int wb = dn_block_bytes(shared ? 0 : 1, I, SI);
-        const int src = (unit - nsh - win) & 31;  // lane holding this unit's header
-        const int e = __shfl_sync(0xffffffffu, hdr_e, src);
-        const int cnt = shared ? M : __shfl_sync(0xffffffffu, hdr_c, src);
-        const int off = __shfl_sync(0xffffffffu, hdr_o, src);
-        const int ab = cnt * (shared ? SI : I) * 2;
-        int act_at = -1;
-        if (used + wb + ab <= kDnStageBytes) act_at = used + wb;
-        else if (nb > 0 || used + wb > kDnStageBytes) break;
-        const int nit = (cnt + 7) / 8;
-        if (ni + nit > kDnMaxItems) break;
-        DnBlock& b = inf.blk[nb];
-        if (lane == 0) {
-          b.kind = shared ? 0 : 1; b.e = shared ? -1 : e; b.u = unit - nsh;
-          b.cnt = cnt; b.off = off; b.smem = used;
-          b.pitch = shared ? 2 * SI : I / 2;
-          b.act_smem = act_at;
-          for (int i = 0; i < nit; ++i) {
-            inf.item_blk[ni + i] = (unsigned char)nb;
-            inf.item_nt[ni + i] = (unsigned char)i;
-          }
-        }
-        wbytes += shared ? 16u * 2u * SI : 16u * (I / 2) + 16u * (I / 16);
-        if (act_at >= 0) abytes += ab;
-        used += wb + (act_at >= 0 ? ab : 0);
-        ++nb;
-        ni += nit;
-        ++unit;
+      const int cu = unit + lane;
+      const bool cand = lane < kDnMaxBlocks && cu < nunits;
+      const bool shared = nsh && cu == 0;
+      const int hl = (cu - nsh - win) & 31;  // lane holding this unit's header
+      const int he = __shfl_sync(0xffffffffu, hdr_e, hl);
+      const int hc = __shfl_sync(0xffffffffu, hdr_c, hl);
+      const int ho = __shfl_sync(0xffffffffu, hdr_o, hl);
+      const int cnt = shared ? M : hc;
+      const int wb = cand ? dn_block_bytes(shared ? 0 : 1, I, SI) : 0;
+      const int ab = cand ? cnt * (shared ? SI : I) * 2 : 0;
+      const int nit = cand ? (cnt + 7) / 8 : 0;
+      const int pit = prefix(nit);
+      int sz = wb + ab;
+      int pre = prefix(sz);
+      bool fit = cand && pre <= kDnStageBytes && pit <= kDnMaxItems;
+      const bool lone = __shfl_sync(0xffffffffu, fit ? 1 : 0, 0) == 0;
+      if (lone) {  // the first unit with its activations read from global memory
+        if (lane == 0) sz = wb;
+        pre = prefix(sz);
+        fit = cand && pre <= kDnStageBytes && pit <= kDnMaxItems;
       }
+      const int nb = __popc(__ballot_sync(0xffffffffu, fit));  // fit holds for lanes 0 .. nb - 1
       if (nb == 0) {  // cannot happen for supported shapes; never spin on it
         if (lane == 0) { *abort = 1; record_timeout(status, 12, n); }
         break;
       }
+      const bool mine = lane < nb;
+      const bool staged = mine && !(lone && lane == 0);
+      const int at = pre - sz;  // byte offset of this block's weight rows in the stage
+      if (mine) {
+        DnBlock& b = inf.blk[lane];
+        b.kind = shared ? 0 : 1; b.e = shared ? -1 : he; b.u = cu - nsh;
+        b.cnt = cnt; b.off = ho; b.smem = at;
+        b.pitch = shared ? 2 * SI : I / 2;
+        b.act_smem = staged ? at + wb : -1;
+        for (int i = 0; i < nit; ++i) {
+          inf.item_blk[pit - nit + i] = (unsigned char)lane;
+          inf.item_nt[pit - nit + i] = (unsigned char)i;
+        }
+      }
+      const uint32_t wbytes = __reduce_add_sync(0xffffffffu, mine ? (uint32_t)wb : 0u);
+      const uint32_t abytes = __reduce_add_sync(0xffffffffu, staged ? (uint32_t)ab : 0u);
+      const int ni = __shfl_sync(0xffffffffu, pit, nb - 1);
       if (lane == 0) {
         inf.nblocks = nb; inf.nitems = ni; inf.abytes = (int)abytes;
         mbar_expect_tx(&SM.ctl.full[sl], wbytes);
       }
       __syncwarp();
-      for (int bi = 0; bi < nb; ++bi) {  // weights: known before the dependency wait
-        const DnBlock& b = inf.blk[bi];
-        uint8_t* dst = st + b.smem;
-        if ((bi & 15) != (lane >> 1)) continue;  // two lanes per block
-        if (b.kind == 0) {
-          if (!(lane & 1))
-            bulk_g2s(dst, a.shared_down + (size_t)h0 * SI, 16u * 2u * SI, &SM.ctl.full[sl]);
-        } else {
-          const size_t row0 = (size_t)b.e * H + h0;
-          if (!(lane & 1)) bulk_g2s(dst, a.w2 + row0 * (I / 2), 16u * (I / 2), &SM.ctl.full[sl]);
-          else bulk_g2s(dst + 16 * b.pitch, a.w2_sf + row0 * (I / 16), 16u * (I / 16), &SM.ctl.full[sl]);
-        }
+      // weights (known before the dependency wait): the block's rows, then
+      // a routed block's scale rows
+      const size_t row0 = (size_t)he * H + h0;
+      if (mine) {
+        const uint8_t* srcp = shared ? reinterpret_cast<const uint8_t*>(a.shared_down + (size_t)h0 * SI)
+                                     : a.w2 + row0 * (I / 2);
+        bulk_g2s(st + at, srcp, shared ? 16u * 2u * SI : 16u * (I / 2), &SM.ctl.full[sl]);
       }
+      if (mine && !shared)
+        bulk_g2s(st + at + 16 * (I / 2), a.w2_sf + row0 * (I / 16), 16u * (I / 16), &SM.ctl.full[sl]);
+      unit += nb;
       ++n;
       if (waited) {
         finish(n - 1);

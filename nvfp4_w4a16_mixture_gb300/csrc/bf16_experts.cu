@@ -10,10 +10,12 @@
 //
 // After the router (which also groups the pairs by expert), a gate/up grid
 // of (8 intermediate rows, routed expert) CTAs and a down grid of (16 output
-// rows, routed expert) CTAs; warp w of a CTA takes the expert's tokens
-// 8w .. 8w + 7 and sums all of K exactly (exact.cuh: weights and activations
-// split per 128-K slice so that the high products chain exactly in the
-// tensor cores, the rest in a compensation term, slices added with TwoSum),
+// rows, routed expert) CTAs; the 8 warps of a CTA split over the expert's
+// 8-token tiles and, when there are fewer tiles than warps, over K (kw warps
+// per tile, their pairs added in warp order), and sum exactly (exact.cuh:
+// weights and activations split per 128-K slice so that the high products
+// chain exactly in the tensor cores, the rest in a compensation term, slices
+// added with TwoSum),
 // so both act and y are the roundings of the exact sums.  A combine
 // kernel forms the outputs.  All launches are chained with programmatic
 // dependent launch.  The weights are read straight from global memory (each
@@ -44,21 +46,32 @@ __global__ void __launch_bounds__(kBfWarps * 32) bf16_gate_up_kernel(MoEArgs a, 
   const int* rec = a.ws.urec + (size_t)u * kUrecInts;
   const int e = ldg_cg_i32(rec), cnt = ldg_cg_i32(rec + 1), off = ldg_cg_i32(rec + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  if (8 * warp >= cnt) return;
+  __shared__ float4 red[kBfWarps * 64];
+  const int ntiles = (cnt + 7) / 8;
+  const int kw = max(1, kBfWarps / ntiles), tile = warp / kw, part = warp % kw;
+  const bool active = tile < ntiles;
   const int H = a.H, I = a.I, k = a.k, r0 = 8 * blockIdx.x;
-  const int nn = 8 * warp + g;  // this lane's token column
-  const uint16_t* xrow = nn < cnt ? a.x + (size_t)(ldg_cg_i32(rec + 4 + nn) / k) * H : nullptr;
+  const int nn = 8 * tile + g;  // this lane's token column
+  const uint16_t* xrow = active && nn < cnt ? a.x + (size_t)(ldg_cg_i32(rec + 4 + nn) / k) * H : nullptr;
   const uint16_t* ra = w13 + ((size_t)e * 2 * I + r0 + g) * H;      // gate row r0 + g
   const uint16_t* rb = w13 + ((size_t)e * 2 * I + I + r0 + g) * H;  // up row r0 + g
   float S[4] = {0.0f, 0.0f, 0.0f, 0.0f}, C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  for (int s = 0; s < H / kSliceK; ++s) {
+  for (int s = part; active && s < H / kSliceK; s += kw) {
     uint4 xb[4];
     load_xcol(xb, xrow ? xrow + s * kSliceK + 32 * t : nullptr);
     slice_bf16_exact(S, C, ra + s * kSliceK + 32 * t, rb + s * kSliceK + 32 * t, xb);
   }
+  if (kw > 1) {
+    store_pair(red, warp, lane, S, C);
+    __syncthreads();
+    if (!active || part != 0) return;
+    add_pairs(S, C, red, warp, kw, lane);
+  } else if (!active) {
+    return;
+  }
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) {
-    const int tok = 8 * warp + 2 * t + cc;
+    const int tok = 8 * tile + 2 * t + cc;
     if (tok < cnt)
       a.ws.act[(size_t)(off + tok) * I + r0 + g] =
           (uint16_t)act_bits(__fadd_rn(S[cc], C[cc]), __fadd_rn(S[2 + cc], C[2 + cc]));
@@ -77,21 +90,32 @@ __global__ void __launch_bounds__(kBfWarps * 32) bf16_down_kernel(MoEArgs a, con
   const int* rec = a.ws.urec + (size_t)u * kUrecInts;
   const int e = ldg_cg_i32(rec), cnt = ldg_cg_i32(rec + 1), off = ldg_cg_i32(rec + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  if (8 * warp >= cnt) return;
+  __shared__ float4 red[kBfWarps * 64];
+  const int ntiles = (cnt + 7) / 8;
+  const int kw = max(1, kBfWarps / ntiles), tile = warp / kw, part = warp % kw;
+  const bool active = tile < ntiles;
   const int H = a.H, I = a.I, h0 = 16 * blockIdx.x;
-  const int nn = 8 * warp + g;
-  const uint16_t* arow = nn < cnt ? a.ws.act + (size_t)(off + nn) * I : nullptr;
+  const int nn = 8 * tile + g;
+  const uint16_t* arow = active && nn < cnt ? a.ws.act + (size_t)(off + nn) * I : nullptr;
   const uint16_t* ra = w2 + ((size_t)e * H + h0 + g) * I;
   const uint16_t* rb = w2 + ((size_t)e * H + h0 + 8 + g) * I;
   float S[4] = {0.0f, 0.0f, 0.0f, 0.0f}, C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  for (int s = 0; s < I / kSliceK; ++s) {
+  for (int s = part; active && s < I / kSliceK; s += kw) {
     uint4 xb[4];
     load_xcol(xb, arow ? arow + s * kSliceK + 32 * t : nullptr);
     slice_bf16_exact(S, C, ra + s * kSliceK + 32 * t, rb + s * kSliceK + 32 * t, xb);
   }
+  if (kw > 1) {
+    store_pair(red, warp, lane, S, C);
+    __syncthreads();
+    if (!active || part != 0) return;
+    add_pairs(S, C, red, warp, kw, lane);
+  } else if (!active) {
+    return;
+  }
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) {
-    const int tok = 8 * warp + 2 * t + cc;
+    const int tok = 8 * tile + 2 * t + cc;
     if (tok < cnt) {
       uint16_t* yrow = a.ws.y + (size_t)(off + tok) * H + h0;
       yrow[g] = (uint16_t)f32_to_bf16_bits(__fadd_rn(S[cc], C[cc]));

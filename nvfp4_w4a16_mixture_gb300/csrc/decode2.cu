@@ -771,11 +771,22 @@ __global__ void __launch_bounds__(kGuThreads, 1) gate_up2_kernel(MoEArgs a) {
 // whole K of its item, so no cross-warp reduction is needed.  Results go to
 // smem: y (bf16, per pair t * k + j) and ys (bf16, per token); after the last
 // stage the CTA forms out = bf16(bf16(sum_j tw_j y_j) + ys) for its rows.
-// A stage with at most 8 items gives each item P = 2 warps, one per half of
-// its K slices; parts 1 .. P - 1 hand their fp32 partials to
-// part 0 through shared memory (a float4 per lane) and a per-part flag
-// holding the stage number + 1; part 0 adds them in part order.
-constexpr int kDnPartSlots = kCons / 2;  // items * (P - 1) when P = 2
+// A stage with few items gives each item P > 1 warps, one per P-th of its K
+// slices (dn_parts); parts 1 .. P - 1 hand their fp32 partials to part 0
+// through shared memory (a float4 per lane) and a per-part flag holding the
+// stage number + 1; part 0 adds them in part order.
+constexpr int kDnPartSlots = kCons / 2;  // items * (P - 1) at most
+constexpr int kDnMaxParts = 8;
+
+// K parts per item of a stage with ni items: as many warps per item as the
+// consumers and the hand-over slots allow, and no more than the items' K
+// slices (kmin: the smaller K of the stage's kinds).
+FLINT_DEV int dn_parts(int ni, int kmin) {
+  const int pmax = min(kDnMaxParts, max(1, kmin / kSliceK));
+  int P = 1;
+  while (P < pmax && ni * (P + 1) <= kCons && ni * P <= kDnPartSlots) ++P;
+  return P;
+}
 
 struct DnSmem {
   Ctl ctl;
@@ -892,12 +903,8 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
       return v;
     };
     while (unit < nunits) {
-      int ok = 1;
-      if (lane == 0) ok = acquire_slot(SM.ctl, n, kDnStages, abort, status, 11);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      const int sl = n % kDnStages;
-      uint8_t* st = stages + (size_t)sl * kDnStageBytes;
-      DnInfo& inf = SM.info[sl];
+      // the plan lives in registers until the slot is free, so planning the
+      // next stage overlaps the consumers' work on the earlier ones
       // a stage holds at most kDnMaxBlocks units: move the window if needed
       if (unit - nsh + kDnMaxBlocks > win + 32) load_window(max(unit - nsh, 0));
       const int cu = unit + lane;
@@ -929,6 +936,15 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
       const bool mine = lane < nb;
       const bool staged = mine && !(lone && lane == 0);
       const int at = pre - sz;  // byte offset of this block's weight rows in the stage
+      const uint32_t wbytes = __reduce_add_sync(0xffffffffu, mine ? (uint32_t)wb : 0u);
+      const uint32_t abytes = __reduce_add_sync(0xffffffffu, staged ? (uint32_t)ab : 0u);
+      const int ni = __shfl_sync(0xffffffffu, pit, nb - 1);
+      int ok = 1;
+      if (lane == 0) ok = acquire_slot(SM.ctl, n, kDnStages, abort, status, 11);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const int sl = n % kDnStages;
+      uint8_t* st = stages + (size_t)sl * kDnStageBytes;
+      DnInfo& inf = SM.info[sl];
       if (mine) {
         DnBlock& b = inf.blk[lane];
         b.kind = shared ? 0 : 1; b.e = shared ? -1 : he; b.u = cu - nsh;
@@ -940,9 +956,6 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
           inf.item_nt[pit - nit + i] = (unsigned char)i;
         }
       }
-      const uint32_t wbytes = __reduce_add_sync(0xffffffffu, mine ? (uint32_t)wb : 0u);
-      const uint32_t abytes = __reduce_add_sync(0xffffffffu, staged ? (uint32_t)ab : 0u);
-      const int ni = __shfl_sync(0xffffffffu, pit, nb - 1);
       if (lane == 0) {
         inf.nblocks = nb; inf.nitems = ni; inf.abytes = (int)abytes;
         mbar_expect_tx(&SM.ctl.full[sl], wbytes);
@@ -1001,7 +1014,7 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
     const DnInfo& inf = SM.info[sl];
     if (inf.nblocks == 0) break;
     const uint8_t* st = stages + (size_t)sl * kDnStageBytes;
-    const int P = inf.nitems <= kCons / 2 ? 2 : 1;  // K parts per item
+    const int P = dn_parts(inf.nitems, SI > 0 ? min(I, SI) : I);  // K parts per item
     const int kp = warp % P;                                     // this warp's part
     for (int it = warp / P; it < inf.nitems; it += kCons / P) {
       const DnBlock& b = inf.blk[inf.item_blk[it]];

@@ -266,5 +266,29 @@ FLINT_DEV void slice_nvfp4_exact(float (&S)[4], float (&C)[4], const uint8_t* ca
               [&](int q) { return nvfp4_word_bf16(wb4[q], bf16x2_bcast(b2, q >> 1)); }, xb);
 }
 
+// K split over warps: a tile of 8 token columns is summed by kw warps, warp
+// w0 + p taking the slices s = p (mod kw).  Each warp leaves its (sum,
+// compensation) pair in red (float4 sum, then float4 compensation, per lane:
+// 64 float4 per warp); after a CTA barrier the first warp of the tile adds
+// the others' pairs to its own in warp order with TwoSum, so the result
+// does not depend on which warp finished first.
+FLINT_DEV void store_pair(float4* red, int warp, int lane, const float (&S)[4], const float (&C)[4]) {
+  red[(2 * warp) * 32 + lane] = make_float4(S[0], S[1], S[2], S[3]);
+  red[(2 * warp + 1) * 32 + lane] = make_float4(C[0], C[1], C[2], C[3]);
+}
+FLINT_DEV void add_pairs(float (&S)[4], float (&C)[4], const float4* red, int w0, int kw, int lane) {
+  for (int p = 1; p < kw; ++p) {
+    const float4 s = red[(2 * (w0 + p)) * 32 + lane], c = red[(2 * (w0 + p) + 1) * 32 + lane];
+    two_sum(S[0], C[0], s.x);
+    two_sum(S[1], C[1], s.y);
+    two_sum(S[2], C[2], s.z);
+    two_sum(S[3], C[3], s.w);
+    C[0] = __fadd_rn(C[0], c.x);
+    C[1] = __fadd_rn(C[1], c.y);
+    C[2] = __fadd_rn(C[2], c.z);
+    C[3] = __fadd_rn(C[3], c.w);
+  }
+}
+
 }  // namespace
 }  // namespace flint

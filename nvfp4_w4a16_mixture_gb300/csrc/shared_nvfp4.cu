@@ -9,11 +9,13 @@
 // The routed part runs as the block without a shared expert, whose output is
 // bf16(routed) exactly (bf16(bf16(R) + 0)); these kernels then form ys and
 // replace each output o by bf16(o + ys), which is the block's rounding.
-// Gate/up: CTA (8 intermediate rows, 64 tokens), warp w the tokens
-// 64 chunk + 8 w .. + 7, every sum exact (exact.cuh slice_nvfp4_exact), act
-// with the correctly rounded exp where it decides the rounding; down: CTA
-// (16 output rows, 64 tokens) likewise.  Weights are read straight from
-// global memory.  Chained with programmatic dependent launch.
+// Gate/up: CTA (8 intermediate rows, 64 tokens), its 8 warps split over the
+// chunk's 8-token tiles and, when there are fewer tiles than warps, over K
+// (kw warps per tile, their exact pairs added in warp order); every sum exact
+// (exact.cuh slice_nvfp4_exact), act with the correctly rounded exp where it
+// decides the rounding; down: CTA (16 output rows, 64 tokens) likewise.
+// Weights are read straight from global memory.  Chained with programmatic
+// dependent launch.
 #include "common.cuh"
 #include "exact.cuh"
 #include "frag.cuh"
@@ -35,23 +37,34 @@ __global__ void __launch_bounds__(kShWarps * 32) shared_nvfp4_gate_up_kernel(
   SpanGuard<kSpanSharedGateUp> span_guard;
   pdl_wait();
   pdl_launch_dependents();
+  __shared__ float4 red[kShWarps * 64];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int t0 = 64 * blockIdx.y + 8 * warp;
-  if (t0 >= M) return;
+  const int ntiles = (min(64, M - 64 * (int)blockIdx.y) + 7) / 8;
+  const int kw = max(1, kShWarps / ntiles), tile = warp / kw, part = warp % kw;
+  const bool active = tile < ntiles;
+  const int t0 = 64 * blockIdx.y + 8 * tile;
   const int r0 = 8 * blockIdx.x;
   const int tok = t0 + g;
-  const uint16_t* xrow = tok < M ? x + (size_t)tok * H : nullptr;
+  const uint16_t* xrow = active && tok < M ? x + (size_t)tok * H : nullptr;
   const uint8_t* ca = gu + (size_t)(r0 + g) * (H / 2);
   const uint8_t* cb = gu + (size_t)(SI + r0 + g) * (H / 2);
   const uint8_t* sa = gu_sf + (size_t)(r0 + g) * (H / 16);
   const uint8_t* sb = gu_sf + (size_t)(SI + r0 + g) * (H / 16);
   float S[4] = {0.0f, 0.0f, 0.0f, 0.0f}, C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  for (int s = 0; s < H / kSliceK; ++s) {
+  for (int s = part; active && s < H / kSliceK; s += kw) {
     uint4 xb[4];
     load_col(xb, xrow ? xrow + s * kSliceK + 32 * t : nullptr);
     slice_nvfp4_exact(S, C, ca + s * (kSliceK / 2) + 16 * t, cb + s * (kSliceK / 2) + 16 * t,
                       *reinterpret_cast<const uint16_t*>(sa + s * (kSliceK / 16) + 2 * t),
                       *reinterpret_cast<const uint16_t*>(sb + s * (kSliceK / 16) + 2 * t), xb);
+  }
+  if (kw > 1) {
+    store_pair(red, warp, lane, S, C);
+    __syncthreads();
+    if (!active || part != 0) return;
+    add_pairs(S, C, red, warp, kw, lane);
+  } else if (!active) {
+    return;
   }
   const float gs = *gu_gs;
 #pragma unroll
@@ -73,23 +86,34 @@ __global__ void __launch_bounds__(kShWarps * 32) shared_nvfp4_down_kernel(
   SpanGuard<kSpanSharedDown> span_guard;
   pdl_wait();
   pdl_launch_dependents();
+  __shared__ float4 red[kShWarps * 64];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int t0 = 64 * blockIdx.y + 8 * warp;
-  if (t0 >= M) return;
+  const int ntiles = (min(64, M - 64 * (int)blockIdx.y) + 7) / 8;
+  const int kw = max(1, kShWarps / ntiles), tile = warp / kw, part = warp % kw;
+  const bool active = tile < ntiles;
+  const int t0 = 64 * blockIdx.y + 8 * tile;
   const int h0 = 16 * blockIdx.x;
   const int tok = t0 + g;
-  const uint16_t* arow = tok < M ? sact + (size_t)tok * SI : nullptr;
+  const uint16_t* arow = active && tok < M ? sact + (size_t)tok * SI : nullptr;
   const uint8_t* ca = dn + (size_t)(h0 + g) * (SI / 2);
   const uint8_t* cb = dn + (size_t)(h0 + 8 + g) * (SI / 2);
   const uint8_t* sa = dn_sf + (size_t)(h0 + g) * (SI / 16);
   const uint8_t* sb = dn_sf + (size_t)(h0 + 8 + g) * (SI / 16);
   float S[4] = {0.0f, 0.0f, 0.0f, 0.0f}, C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  for (int s = 0; s < SI / kSliceK; ++s) {
+  for (int s = part; active && s < SI / kSliceK; s += kw) {
     uint4 xb[4];
     load_col(xb, arow ? arow + s * kSliceK + 32 * t : nullptr);
     slice_nvfp4_exact(S, C, ca + s * (kSliceK / 2) + 16 * t, cb + s * (kSliceK / 2) + 16 * t,
                       *reinterpret_cast<const uint16_t*>(sa + s * (kSliceK / 16) + 2 * t),
                       *reinterpret_cast<const uint16_t*>(sb + s * (kSliceK / 16) + 2 * t), xb);
+  }
+  if (kw > 1) {
+    store_pair(red, warp, lane, S, C);
+    __syncthreads();
+    if (!active || part != 0) return;
+    add_pairs(S, C, red, warp, kw, lane);
+  } else if (!active) {
+    return;
   }
   const float gs = *dn_gs;
 #pragma unroll

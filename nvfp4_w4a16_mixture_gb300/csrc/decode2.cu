@@ -302,6 +302,7 @@ FLINT_DEV void mma_b16(float (&acc)[4], const uint32_t (&af)[4][2][4], const uin
 struct EpiRec {
   int kind;  // 0 shared, 1 routed, -1 no more tiles
   int r0, e, off, cnt, f16p;
+  float gs;  // routed, few tokens: the expert's global scale (loaded while the tile is summed)
   int exp[32];  // f16 path: scale exponent of pair nn's token (nn < cnt <= 16)
 };
 
@@ -451,7 +452,9 @@ __global__ void __launch_bounds__(kGuThreads, 1) gate_up2_kernel(MoEArgs a) {
       if (kind == 1) {
         // bf16 path: 2^7 undoes the operand scaling; f16 path: 2^-exp of the
         // token undoes the activations' scaling
-        const float gs = er.f16p ? a.w13_gs[er.e] : a.w13_gs[er.e] * 128.0f;
+        // (many tokens: the consumers have no register to spare for it)
+        const float egs = NTG == 1 ? er.gs : a.w13_gs[er.e];
+        const float gs = er.f16p ? egs : egs * 128.0f;
         for (int it = 0; it < 2 * ntiles; ++it) {
           const int at = it & 1, nt = it >> 1;
           float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -695,9 +698,11 @@ __global__ void __launch_bounds__(kGuThreads, 1) gate_up2_kernel(MoEArgs a) {
       continue;
     }
     const bool f16p = kind == 1 && inf.x16;
-    // the scale exponent of this lane's pair (f16 path), for the epilogue record
+    // the scale exponent of this lane's pair (f16 path) and the expert's
+    // global scale, for the epilogue record: loaded now, used after the sums
     const int cexp =
         f16p && last && warp == 0 && lane < cnt ? ldg_cg_i32(a.ws.x16_exp + inf.tok[lane]) : 0;
+    const float egs = NTG == 1 && last && warp == 0 && lane == 0 ? ldg_cg_f32(a.w13_gs + inf.e) : 0.0f;
     for (int n0 = 0; n0 < ntiles; n0 += NTG) {
       float acc[NTG][4];
       const uint16_t* brow[NTG];
@@ -750,6 +755,7 @@ __global__ void __launch_bounds__(kGuThreads, 1) gate_up2_kernel(MoEArgs a) {
       if (lane == 0) {
         er.kind = kind; er.r0 = inf.r0; er.e = inf.e; er.off = inf.off; er.cnt = cnt;
         er.f16p = f16p ? 1 : 0;
+        er.gs = egs;
       }
       er.exp[lane] = cexp;
     }
@@ -771,22 +777,11 @@ __global__ void __launch_bounds__(kGuThreads, 1) gate_up2_kernel(MoEArgs a) {
 // whole K of its item, so no cross-warp reduction is needed.  Results go to
 // smem: y (bf16, per pair t * k + j) and ys (bf16, per token); after the last
 // stage the CTA forms out = bf16(bf16(sum_j tw_j y_j) + ys) for its rows.
-// A stage with few items gives each item P > 1 warps, one per P-th of its K
-// slices (dn_parts); parts 1 .. P - 1 hand their fp32 partials to part 0
-// through shared memory (a float4 per lane) and a per-part flag holding the
-// stage number + 1; part 0 adds them in part order.
-constexpr int kDnPartSlots = kCons / 2;  // items * (P - 1) at most
-constexpr int kDnMaxParts = 8;
-
-// K parts per item of a stage with ni items: as many warps per item as the
-// consumers and the hand-over slots allow, and no more than the items' K
-// slices (kmin: the smaller K of the stage's kinds).
-FLINT_DEV int dn_parts(int ni, int kmin) {
-  const int pmax = min(kDnMaxParts, max(1, kmin / kSliceK));
-  int P = 1;
-  while (P < pmax && ni * (P + 1) <= kCons && ni * P <= kDnPartSlots) ++P;
-  return P;
-}
+// A stage with at most 8 items gives each item P = 2 warps, one per half of
+// its K slices; parts 1 .. P - 1 hand their fp32 partials to
+// part 0 through shared memory (a float4 per lane) and a per-part flag
+// holding the stage number + 1; part 0 adds them in part order.
+constexpr int kDnPartSlots = kCons / 2;  // items * (P - 1) when P = 2
 
 struct DnSmem {
   Ctl ctl;
@@ -903,8 +898,12 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
       return v;
     };
     while (unit < nunits) {
-      // the plan lives in registers until the slot is free, so planning the
-      // next stage overlaps the consumers' work on the earlier ones
+      int ok = 1;
+      if (lane == 0) ok = acquire_slot(SM.ctl, n, kDnStages, abort, status, 11);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const int sl = n % kDnStages;
+      uint8_t* st = stages + (size_t)sl * kDnStageBytes;
+      DnInfo& inf = SM.info[sl];
       // a stage holds at most kDnMaxBlocks units: move the window if needed
       if (unit - nsh + kDnMaxBlocks > win + 32) load_window(max(unit - nsh, 0));
       const int cu = unit + lane;
@@ -936,15 +935,6 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
       const bool mine = lane < nb;
       const bool staged = mine && !(lone && lane == 0);
       const int at = pre - sz;  // byte offset of this block's weight rows in the stage
-      const uint32_t wbytes = __reduce_add_sync(0xffffffffu, mine ? (uint32_t)wb : 0u);
-      const uint32_t abytes = __reduce_add_sync(0xffffffffu, staged ? (uint32_t)ab : 0u);
-      const int ni = __shfl_sync(0xffffffffu, pit, nb - 1);
-      int ok = 1;
-      if (lane == 0) ok = acquire_slot(SM.ctl, n, kDnStages, abort, status, 11);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      const int sl = n % kDnStages;
-      uint8_t* st = stages + (size_t)sl * kDnStageBytes;
-      DnInfo& inf = SM.info[sl];
       if (mine) {
         DnBlock& b = inf.blk[lane];
         b.kind = shared ? 0 : 1; b.e = shared ? -1 : he; b.u = cu - nsh;
@@ -956,6 +946,9 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
           inf.item_nt[pit - nit + i] = (unsigned char)i;
         }
       }
+      const uint32_t wbytes = __reduce_add_sync(0xffffffffu, mine ? (uint32_t)wb : 0u);
+      const uint32_t abytes = __reduce_add_sync(0xffffffffu, staged ? (uint32_t)ab : 0u);
+      const int ni = __shfl_sync(0xffffffffu, pit, nb - 1);
       if (lane == 0) {
         inf.nblocks = nb; inf.nitems = ni; inf.abytes = (int)abytes;
         mbar_expect_tx(&SM.ctl.full[sl], wbytes);
@@ -1014,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
     const DnInfo& inf = SM.info[sl];
     if (inf.nblocks == 0) break;
     const uint8_t* st = stages + (size_t)sl * kDnStageBytes;
-    const int P = dn_parts(inf.nitems, SI > 0 ? min(I, SI) : I);  // K parts per item
+    const int P = inf.nitems <= kCons / 2 ? 2 : 1;  // K parts per item
     const int kp = warp % P;                                     // this warp's part
     for (int it = warp / P; it < inf.nitems; it += kCons / P) {
       const DnBlock& b = inf.blk[inf.item_blk[it]];
@@ -1041,7 +1034,8 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
         if (b.act_smem >= 0) bsm = st + b.act_smem + (size_t)nn * K * 2;
         else brow = routed ? a.ws.act + (size_t)(b.off + nn) * I : a.ws.sact + (size_t)nn * SI;
       }
-      const float gs2 = routed ? ldg_cg_f32(a.w2_gs + b.e) * 128.0f : 0.0f;
+      // the global scale, used only after the sums (2^7 undoes the operand scaling)
+      const float gs2 = routed ? ldg_cg_f32(a.w2_gs + b.e) : 0.0f;
       const uint8_t* sg = st + b.smem + 16 * b.pitch + g * (I / 16);
       const uint8_t* sg8 = sg + 8 * (I / 16);
       const int nsl = K / kSliceK;
@@ -1096,7 +1090,8 @@ __global__ void __launch_bounds__(kThreads, 1) down2_kernel(MoEArgs a) {
         for (int i = 0; i < 4; ++i) {
           const int tok = nt * 8 + 2 * t + (i & 1);
           if (tok < ncnt)
-            ysm[(size_t)pr[i & 1] * 16 + g + (i >> 1) * 8] = (uint16_t)f32_to_bf16_bits(acc[i] * gs2);
+            ysm[(size_t)pr[i & 1] * 16 + g + (i >> 1) * 8] =
+                (uint16_t)f32_to_bf16_bits(__fmul_rn(acc[i], gs2) * 128.0f);
         }
       } else {
 #pragma unroll

@@ -479,8 +479,9 @@ static cudaError_t launch(const void* fn, dim3 grid, dim3 block, void** args, cu
 // warp w of CTA r computes the logits of experts r * kRcWarps + w (+ multiples
 // of kRcCtas * kRcWarps) for every token, with router_dot (the canonical
 // order, so ids match route_kernel bit for bit), and stores them into the
-// leader CTA's shared memory.  After the cluster barrier the leader runs the
-// top-k (warp per token) and the expert grouping from shared memory: per
+// leader CTA's shared memory.  After the cluster barrier the other CTAs make
+// the f16 copy of x for the gate/up kernel while the leader runs the top-k
+// (warp per token) and the expert grouping from shared memory: per
 // expert a bit mask of its tokens, counts and offsets by a scan, a pair's
 // sorted position = its expert's offset + the number of earlier tokens in the
 // mask.  No global atomics and no re-reads of global results on the way.
@@ -525,12 +526,15 @@ __global__ void __cluster_dims__(kRcCtas, 1, 1) __launch_bounds__(kRcWarps * 32)
       if (lane == 0) lead->logit[t][e] = (uint16_t)f32_to_bf16_bits(acc);
     }
   }
-  // f16 copy of x for the gate/up kernel: per token the power of two that
-  // puts the largest magnitude in [2^14, 2^15); this CTA converts columns
-  // rank * H / kRcCtas .. of every token and reports whether every value
-  // survived the round trip (then the copy is exact)
-  static_assert(kRcMaxTokens <= kX16MaxTokens, "the f16 copy covers the cluster router's tokens");
-  {
+  cl.sync();  // every logit is in the leader's shared memory
+  if (rank != 0) {
+    // f16 copy of x for the gate/up kernel, made by the other CTAs while the
+    // leader runs the top-k: per token the power of two that puts the largest
+    // magnitude in [2^14, 2^15); CTA r converts the column pairs
+    // [(r - 1) P / (kRcCtas - 1), r P / (kRcCtas - 1)) of every token (P =
+    // H / 2) and reports whether every value survived the round trip (then
+    // the copy is exact)
+    static_assert(kRcMaxTokens <= kX16MaxTokens, "the f16 copy covers the cluster router's tokens");
     __shared__ int s_exp[kRcMaxTokens];
     __shared__ int s_bad;
     if (tid == 0) s_bad = 0;
@@ -551,10 +555,11 @@ __global__ void __cluster_dims__(kRcCtas, 1, 1) __launch_bounds__(kRcWarps * 32)
       }
     }
     __syncthreads();
-    const int hn = H / kRcCtas, h0 = rank * hn;
+    const int P = H / 2, p0 = (rank - 1) * P / (kRcCtas - 1), p1 = rank * P / (kRcCtas - 1);
+    const int np = p1 - p0;
     bool bad = false;
-    for (int i = tid; i < M * (hn / 2); i += kRcWarps * 32) {
-      const int t = i / (hn / 2), h = h0 + 2 * (i % (hn / 2));
+    for (int i = tid; i < M * np; i += kRcWarps * 32) {
+      const int t = i / np, h = 2 * (p0 + i % np);
       const int e = s_exp[t];
       if (e == 1000) { bad = true; continue; }
       const uint32_t xv = *reinterpret_cast<const uint32_t*>(a.x + (size_t)t * H + h);
@@ -568,11 +573,9 @@ __global__ void __cluster_dims__(kRcCtas, 1, 1) __launch_bounds__(kRcWarps * 32)
     if (bad) s_bad = 1;
     __syncthreads();
     if (tid == 0 && s_bad) atomicAdd(&a.ws.glob_cnt[1], 1);
-    if (rank == 0 && tid < M) a.ws.x16_exp[tid] = s_exp[tid];
+    if (rank == 1 && tid < M) a.ws.x16_exp[tid] = s_exp[tid];
+    return;
   }
-
-  cl.sync();  // every logit is in the leader's shared memory
-  if (rank != 0) return;
 
   for (int e = tid; e < E; e += kRcWarps * 32) S.mask[e] = 0ull;
   for (int t = warp; t < M; t += kRcWarps) {

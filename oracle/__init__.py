@@ -71,6 +71,9 @@ def _load():
             lib.oracle_add_rms_norm.argtypes = [P, P, P, i32, i32, ctypes.c_float, P, P]
             lib.oracle_max_threads.restype = i32
             lib.oracle_max_threads.argtypes = []
+            lib.oracle_qkv_fused.argtypes = ([P, P, P, ctypes.c_float, P, P, ctypes.c_float, P, P, P,
+                                              ctypes.c_float, P, P, P, i32, i32, i32, i32, i32, i32,
+                                              ctypes.c_int64, ctypes.c_int64, ctypes.c_int64] + [P] * 6)
             _lib = lib
     return _lib
 
@@ -254,3 +257,46 @@ def add_rms_norm(a, r, w, eps: float):
 
 def max_threads() -> int:
     return int(_load().oracle_max_threads())
+
+
+def qkv_fused(x, residual, norm_w, eps: float, weight, weight_scale, global_scale, q_norm_w, k_norm_w,
+              qk_eps: float, cos_sin, positions, k_cache, v_cache, slot_mapping, nq: int, nkv: int):
+    """Fused decode qkv (reading R11).  weight: NVFP4 codes uint8 [N, H/2]
+    (with weight_scale uint8 [N, H/16] and the fp32 global_scale) or BF16
+    [N, H] (weight_scale None).  k_cache / v_cache: bf16 [blocks,
+    block_size, nkv, 128] arrays, updated in place (numpy) at the mapped
+    slots.  Returns (q bits [M, nq*128], residual' bits [M, H] or None,
+    xn bits [M, H], qkv bits [M, N])."""
+    xa = _np(x, np.uint16)
+    M, H = xa.shape
+    ra = None if residual is None else _np(residual, np.uint16)
+    nwa = _np(norm_w, np.uint16)
+    N = (nq + 2 * nkv) * 128
+    nvfp4 = weight_scale is not None
+    if nvfp4:
+        wc, wsf, wb = _np(weight, np.uint8), _np(weight_scale, np.uint8), None
+        assert wc.shape == (N, H // 2) and wsf.shape == (N, H // 16)
+        gs = float(global_scale)
+    else:
+        wc, wsf, wb = None, None, _np(weight, np.uint16)
+        assert wb.shape == (N, H)
+        gs = 1.0
+    qa, ka = _np(q_norm_w, np.uint16), _np(k_norm_w, np.uint16)
+    cs = None if cos_sin is None else np.ascontiguousarray(np.asarray(cos_sin, np.float32))
+    pos = np.ascontiguousarray(np.asarray(positions, np.int64))
+    slots = np.ascontiguousarray(np.asarray(slot_mapping, np.int64))
+    assert isinstance(k_cache, np.ndarray) and isinstance(v_cache, np.ndarray)
+    assert k_cache.dtype == np.uint16 and k_cache.flags.c_contiguous and v_cache.shape == k_cache.shape
+    blocks, bs, kv_heads, D = k_cache.shape
+    assert kv_heads == nkv and D == 128
+    q = np.empty((M, nq * 128), np.uint16)
+    res = np.empty((M, H), np.uint16) if ra is not None else None
+    xn = np.empty((M, H), np.uint16)
+    qkv = np.empty((M, N), np.uint16)
+    rc = _load().oracle_qkv_fused(_ptr(xa), _ptr(ra), _ptr(nwa), float(eps), _ptr(wc), _ptr(wsf), gs, _ptr(wb),
+                                  _ptr(qa), _ptr(ka), float(qk_eps), _ptr(cs), _ptr(pos), _ptr(slots),
+                                  int(slots.shape[0]), M, H, nq, nkv, bs, bs * kv_heads * D, kv_heads * D, D,
+                                  _ptr(k_cache), _ptr(v_cache), _ptr(q), _ptr(res), _ptr(xn), _ptr(qkv))
+    if rc != 0:
+        raise ValueError("oracle_qkv_fused: invalid arguments")
+    return q, res, xn, qkv

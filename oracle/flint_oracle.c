@@ -55,6 +55,26 @@
  *      kernels: g, u = fp32(exact dot) * gs_gu, sact = bf16(silu(g) * u)
  *      (R4 form), ys = bf16(fp32(exact dot(sact, Wd)) * gs_d); the block's
  *      output is then bf16(bf16(routed) + ys) as with the BF16 shared expert.
+ *  R11 fused decode qkv (flint_qkv_fused on the page
+ *      "vllm.models.flint.ops.qkv_fused": add-RMSNorm, the qkv GEMV, per-head
+ *      q/k RMSNorm, NeoX RoPE and the paged KV-cache write).  xn follows R8
+ *      (with no residual: s = x and no residual output); qkv = bf16(fp32(exact
+ *      dot(xn, W row)) * gs) for NVFP4 weights (the routed rule, R7), bf16(fp32
+ *      exact dot) for BF16 weights; rows [0, nq*128) are the q heads, then
+ *      nkv k heads, then nkv v heads.  The NVFP4 scales are taken row-major
+ *      [N, H/16] (the MoE experts' order; the page's 128x4-swizzled order is
+ *      a permutation of the same bytes).  q/k head norm (qk_norm_rope_cache is
+ *      not on the pages; its order of the squares is left open): ss = exact
+ *      sum of the squares of the head's 128 bf16 values rounded once to fp32,
+ *      v = ss / 128 + qk_eps in fp32, inv = 1 / sqrt(v) correctly rounded,
+ *      n = (q * inv) * w in fp32, kept in fp32 for RoPE ("FP32 math"); NeoX
+ *      RoPE with c, s = the fp32 table's cos | sin at the token's position:
+ *      o[d] = n[d] c[d] - n[d+64] s[d], o[d+64] = n[d+64] c[d] + n[d] s[d]
+ *      for d < 64, each product and the sum one fp32 rounding; o = n without
+ *      a table; then bf16.  q heads go to q; k heads (o) and v heads (the qkv
+ *      values) go to the paged caches at slot = slot_mapping[t] (block
+ *      slot / block_size, offset slot % block_size), for t < the mapping's
+ *      length and slot >= 0 only.
  *  R7  "products are accumulated in fp32" fixes the accumulator's type, not
  *      the order of the additions.  Every expert and shared-expert dot
  *      product therefore takes the order-independent value: the exact sum of
@@ -531,6 +551,112 @@ ORACLE_API int oracle_add_rms_norm(const uint16_t* a, const uint16_t* r, const u
     }
   }
   free(s);
+  return 0;
+}
+
+/* Fused decode qkv (reading R11) for M tokens: q [M, nq*128] and the cache
+ * writes; optionally residual' [M, H] (only with a residual), xn [M, H] and
+ * qkv [M, N] (bf16 bits).  Weights: NVFP4 codes [N, H/2] with scales
+ * [N, H/16] and global scale gs, or (w_codes NULL) BF16 [N, H].  Caches: bf16
+ * element offsets block * s0 + offset * s1 + head * s2 + d. */
+ORACLE_API int oracle_qkv_fused(const uint16_t* x, const uint16_t* residual, const uint16_t* norm_w,
+                                float eps, const uint8_t* w_codes, const uint8_t* w_sf, float gs,
+                                const uint16_t* w_bf16, const uint16_t* q_norm_w,
+                                const uint16_t* k_norm_w, float qk_eps, const float* cos_sin,
+                                const int64_t* positions, const int64_t* slot_mapping, int n_slots,
+                                int M, int H, int nq, int nkv, int block_size, int64_t s0, int64_t s1,
+                                int64_t s2, uint16_t* k_cache, uint16_t* v_cache, uint16_t* q_out,
+                                uint16_t* res_out, uint16_t* xn_out, uint16_t* qkv_out) {
+  enum { D = 128 };
+  if (M < 0 || H <= 0 || H % 16 != 0 || nq < 1 || nkv < 0 || block_size < 1)
+    return -1;
+  if (!w_codes && !w_bf16)
+    return -1;
+  init_tables();
+  const int N = (nq + 2 * nkv) * D;
+  float* s = (float*)malloc(sizeof(float) * (size_t)H);
+  float* xn = (float*)malloc(sizeof(float) * (size_t)H);
+  uint16_t* qkv = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)N);
+  if (!s || !xn || !qkv) {
+    free(s);
+    free(xn);
+    free(qkv);
+    return -1;
+  }
+  for (int t = 0; t < M; ++t) {
+    /* the input RMSNorm (reading R8) */
+    double sq = 0.0;
+    for (int h = 0; h < H; ++h) {
+      s[h] = bf16_to_f32(x[(int64_t)t * H + h]);
+      if (residual) {
+        s[h] = s[h] + bf16_to_f32(residual[(int64_t)t * H + h]);
+        if (res_out)
+          res_out[(int64_t)t * H + h] = f32_to_bf16(s[h]);
+      }
+      sq += (double)s[h] * (double)s[h];
+    }
+    const float v = (float)sq / (float)H + eps;
+    const float inv = (float)(1.0 / sqrt((double)v));
+    for (int h = 0; h < H; ++h) {
+      xn[h] = round_bf16((s[h] * inv) * bf16_to_f32(norm_w[h]));
+      if (xn_out)
+        xn_out[(int64_t)t * H + h] = f32_to_bf16(xn[h]);
+    }
+    /* the qkv GEMV (reading R7 sums) */
+    for (int n = 0; n < N; ++n) {
+      double acc = 0.0;
+      if (w_codes) {
+        for (int h = 0; h < H; ++h)
+          acc += (double)(nvfp4_deq(w_codes, w_sf, n, H, h) * xn[h]);
+        qkv[n] = f32_to_bf16((float)acc * gs);
+      } else {
+        for (int h = 0; h < H; ++h)
+          acc += (double)(bf16_to_f32(w_bf16[(int64_t)n * H + h]) * xn[h]);
+        qkv[n] = f32_to_bf16((float)acc);
+      }
+      if (qkv_out)
+        qkv_out[(int64_t)t * N + n] = qkv[n];
+    }
+    const int64_t slot = t < n_slots ? slot_mapping[t] : -1;
+    const int64_t cache_row = slot >= 0 ? (slot / block_size) * s0 + (slot % block_size) * s1 : 0;
+    /* q and k heads: norm, RoPE */
+    for (int hh = 0; hh < nq + nkv; ++hh) {
+      const uint16_t* hv = qkv + hh * D;
+      const uint16_t* nw = hh < nq ? q_norm_w : k_norm_w;
+      double hs = 0.0;
+      for (int d = 0; d < D; ++d)
+        hs += (double)bf16_to_f32(hv[d]) * (double)bf16_to_f32(hv[d]);
+      const float hvar = (float)hs / (float)D + qk_eps;
+      const float hinv = (float)(1.0 / sqrt((double)hvar));
+      float nrm[D], o[D];
+      for (int d = 0; d < D; ++d)
+        nrm[d] = (bf16_to_f32(hv[d]) * hinv) * bf16_to_f32(nw[d]);
+      if (cos_sin) {
+        const float* cs = cos_sin + positions[t] * D;
+        for (int d = 0; d < D / 2; ++d) {
+          const float c = cs[d], sn = cs[D / 2 + d];
+          o[d] = nrm[d] * c - nrm[d + D / 2] * sn;
+          o[d + D / 2] = nrm[d + D / 2] * c + nrm[d] * sn;
+        }
+      } else {
+        for (int d = 0; d < D; ++d)
+          o[d] = nrm[d];
+      }
+      for (int d = 0; d < D; ++d) {
+        if (hh < nq)
+          q_out[(int64_t)t * nq * D + hh * D + d] = f32_to_bf16(o[d]);
+        else if (slot >= 0)
+          k_cache[cache_row + (int64_t)(hh - nq) * s2 + d] = f32_to_bf16(o[d]);
+      }
+    }
+    /* v heads: the qkv values */
+    for (int vh = 0; vh < nkv && slot >= 0; ++vh)
+      for (int d = 0; d < D; ++d)
+        v_cache[cache_row + (int64_t)vh * s2 + d] = qkv[(nq + nkv + vh) * D + d];
+  }
+  free(s);
+  free(xn);
+  free(qkv);
   return 0;
 }
 

@@ -510,3 +510,170 @@ def test_nvfp4_shared_expert_is_a_routed_expert_of_weight_one():
     assert np.array_equal(ys, r["y"][:, 0, :])
     assert np.array_equal(sact, r["act"][:, 0, :])
     assert np.array_equal(ys, r["out"])  # bf16(bf16(y) + 0) = y
+
+
+# ------------------------------------------------- fused decode qkv (R11)
+def _qkv_problem(M=3, H=256, nq=2, nkv=1, nvfp4=True, seed=5, residual=True, rope=True):
+    g = torch.Generator().manual_seed(seed)
+    N = (nq + 2 * nkv) * 128
+    x = synth.make_x(M, H, g)
+    res = synth.make_x(M, H, g) if residual else None
+    nw = (1 + 0.1 * torch.randn(H, generator=g)).to(torch.bfloat16)
+    w = torch.randn(N, H, generator=g) * 0.05
+    if nvfp4:
+        codes, sf, gs = synth.quantize_nvfp4(w)
+        weight, scale, gsv = codes, sf, float(gs)
+    else:
+        weight, scale, gsv = w.to(torch.bfloat16), None, None
+    qn = (1 + 0.1 * torch.randn(128, generator=g)).to(torch.bfloat16)
+    kn = (1 + 0.1 * torch.randn(128, generator=g)).to(torch.bfloat16)
+    max_pos = 16
+    if rope:
+        ang = torch.arange(max_pos, dtype=torch.float64)[:, None] * (10000.0 ** (-torch.arange(64) / 64.0))[None, :]
+        cs = torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).float().numpy()
+    else:
+        cs = None
+    pos = np.array([3, 0, 11, 7, 1, 2, 5, 9][:M], np.int64)
+    return dict(x=x, residual=res, norm_w=nw, eps=1e-6, weight=weight, weight_scale=scale, global_scale=gsv,
+                q_norm_w=qn, k_norm_w=kn, qk_eps=1e-6, cos_sin=cs, positions=pos, nq=nq, nkv=nkv)
+
+
+def _caches(nkv=1, blocks=4, bs=4):
+    k = np.full((blocks, bs, nkv, 128), 0x7FC1, np.uint16)  # NaN marker: untouched
+    return k, k.copy()
+
+
+def _run_qkv(p, slots, blocks=4, bs=4, **over):
+    q = dict(p, **over)
+    kc, vc = _caches(q["nkv"], blocks, bs)
+    assert kc.shape[2] == q["nkv"]
+    out = oracle.qkv_fused(q["x"], q["residual"], q["norm_w"], q["eps"], q["weight"], q["weight_scale"],
+                           q["global_scale"], q["q_norm_w"], q["k_norm_w"], q["qk_eps"], q["cos_sin"],
+                           q["positions"], kc, vc, np.asarray(slots, np.int64), q["nq"], q["nkv"])
+    return out, kc, vc
+
+
+def test_qkv_input_norm_is_the_add_rms_norm():
+    """xn and residual' equal the add-RMSNorm oracle's (itself pinned); with
+    no residual xn is the RMSNorm of x, i.e. add_rms_norm(x, 0)."""
+    p = _qkv_problem()
+    (q, res, xn, qkv), _, _ = _run_qkv(p, [0, 1, 2])
+    r_ref, xn_ref = oracle.add_rms_norm(p["x"], p["residual"], p["norm_w"], p["eps"])
+    assert np.array_equal(res, r_ref) and np.array_equal(xn, xn_ref)
+    p0 = _qkv_problem(residual=False)
+    (q0, res0, xn0, _), _, _ = _run_qkv(p0, [0, 1, 2])
+    assert res0 is None
+    _, xn0_ref = oracle.add_rms_norm(p0["x"], torch.zeros_like(p0["x"]), p0["norm_w"], p0["eps"])
+    assert np.array_equal(xn0, xn0_ref)
+
+
+@pytest.mark.parametrize("nvfp4", [True, False])
+def test_qkv_gemv_is_the_exact_dot(nvfp4):
+    """qkv = bf16(fp32(exact dot) * gs): with the weights decoded by torch
+    (float8 scales, the e2m1 embedding) and a float64 matmul, whose sums of
+    these few-bit products are exact, the values agree bit for bit."""
+    p = _qkv_problem(nvfp4=nvfp4)
+    (q, res, xn, qkv), _, _ = _run_qkv(p, [0, 1, 2])
+    xn64 = bf16_bits_to_f64(xn)
+    if nvfp4:
+        N, H = p["weight"].shape[0], p["x"].shape[1]
+        w64 = dequant(p["weight"].numpy(), p["weight_scale"].numpy())
+        acc = (xn64 @ w64.T).astype(np.float32) * np.float32(p["global_scale"])
+    else:
+        w64 = bf16_bits_to_f64(tensor_bits(p["weight"]))
+        acc = (xn64 @ w64.T).astype(np.float32)
+    assert np.array_equal(qkv, tensor_bits(torch.from_numpy(acc).to(torch.bfloat16)))
+
+
+def test_qkv_rope_identity_and_quarter_turn():
+    """NeoX RoPE on closed forms: a table with cos = 1, sin = 0 gives the
+    output without RoPE; cos = 0, sin = 1 (a quarter turn) gives
+    o[d] = -n[d + 64], o[d + 64] = n[d] exactly (pairs d, d + 64, signs)."""
+    p = _qkv_problem(rope=False)
+    (q_plain, _, _, _), k_plain, _ = _run_qkv(p, [0, 1, 2])
+    ident = np.concatenate([np.ones((16, 64)), np.zeros((16, 64))], axis=1).astype(np.float32)
+    (q_id, _, _, _), k_id, _ = _run_qkv(p, [0, 1, 2], cos_sin=ident)
+    assert np.array_equal(q_id, q_plain) and np.array_equal(k_id, k_plain)
+    quarter = np.concatenate([np.zeros((16, 64)), np.ones((16, 64))], axis=1).astype(np.float32)
+    (q_qt, _, _, _), k_qt, _ = _run_qkv(p, [0, 1, 2], cos_sin=quarter)
+    M, nq = q_plain.shape[0], p["nq"]
+    a = q_plain.reshape(M, nq, 128)
+    b = q_qt.reshape(M, nq, 128)
+    assert np.array_equal(b[..., 64:], a[..., :64])
+    assert np.array_equal(b[..., :64], a[..., 64:] ^ np.uint16(0x8000))  # -n: the sign bit
+
+
+def test_qkv_head_norm_closed_forms():
+    """A head whose 128 values are equal normalises to sign * w exactly (eps
+    0); doubling the q rows of the weight changes no q output (the norm is
+    scale-free in binary floating point)."""
+    p = _qkv_problem(nvfp4=False, rope=False, M=2)
+    w = p["weight"].clone()
+    w[:128] = w[0]  # q head 0: every row alike, so every value alike
+    (q, _, _, qkv), _, _ = _run_qkv(p, [0, 1], weight=w, qk_eps=0.0)
+    qn = bf16_bits_to_f64(tensor_bits(p["q_norm_w"]))
+    for t in range(2):
+        c = bf16_bits_to_f64(qkv[t, 0])
+        assert np.all(bf16_bits_to_f64(qkv[t, :128]) == c) and c != 0
+        assert np.array_equal(bf16_bits_to_f64(q[t, :128]), np.sign(c) * qn)
+    w2 = p["weight"].clone()
+    w2[:256] = (w2[:256].float() * 2).to(torch.bfloat16)  # both q heads, exactly doubled
+    (q2, _, _, _), _, _ = _run_qkv(p, [0, 1], weight=w2, qk_eps=0.0)
+    (q1, _, _, _), _, _ = _run_qkv(p, [0, 1], qk_eps=0.0)
+    assert np.array_equal(q2, q1)
+
+
+def test_qkv_cache_slots():
+    """Brute force over the paged layout: token t's k and v land at block
+    slot // block_size, offset slot % block_size; a negative slot and the
+    tokens past the mapping's length write nothing; v is the qkv values."""
+    p = _qkv_problem(M=3, nkv=2, rope=False)
+    (q, _, _, qkv), kc, vc = _run_qkv(p, [6, -1], blocks=4, bs=4)
+    (q_all, _, _, _), kc_all, _ = _run_qkv(p, [6, 1, 13], blocks=4, bs=4)
+    written = ~np.all(kc == 0x7FC1, axis=-1)
+    # slot 6 -> block 1, offset 2, both kv heads
+    assert written.sum() == 2 and written[1, 2, 0] and written[1, 2, 1]
+    assert np.array_equal(vc[1, 2, 0], qkv[0, 512:640]) and np.array_equal(vc[1, 2, 1], qkv[0, 640:768])
+    assert not np.array_equal(kc[1, 2, 0], kc[1, 2, 1])
+    assert np.array_equal(kc_all[1, 2], kc[1, 2])
+    assert np.all(kc_all[0, 1] != 0x7FC1) and np.all(kc_all[3, 1] != 0x7FC1)
+    # without RoPE the cached k is the normalised k head, as q is for q heads
+    assert np.array_equal(q, q_all)
+
+
+def test_qkv_matches_float64():
+    """An independent float64 derivation of the whole chain (torch decode of
+    the weights, float64 sums and sqrt, the stated roundings), within the
+    rule; q and the cached k and v."""
+    p = _qkv_problem(M=3, nq=2, nkv=1)
+    (q, res, xn, qkv), kc, vc = _run_qkv(p, [2, 5, 9], blocks=4, bs=4)
+    x = bf16_bits_to_f64(tensor_bits(p["x"]))
+    r = bf16_bits_to_f64(tensor_bits(p["residual"]))
+    s = (x + r).astype(np.float32).astype(np.float64)
+    nw = bf16_bits_to_f64(tensor_bits(p["norm_w"]))
+    inv = 1.0 / np.sqrt((s * s).sum(1, keepdims=True) / s.shape[1] + p["eps"])
+    xn64 = bf16_bits_to_f64(tensor_bits(torch.from_numpy(s * inv * nw).to(torch.bfloat16)))
+    H = s.shape[1]
+    w64 = dequant(p["weight"].numpy(), p["weight_scale"].numpy()) * p["global_scale"]
+    qkv64 = bf16_bits_to_f64(tensor_bits(torch.from_numpy(xn64 @ w64.T).to(torch.bfloat16)))
+    cs = p["cos_sin"].astype(np.float64)
+    want_q = np.empty_like(q)
+    want_k = []
+    for t in range(3):
+        c, sn = cs[p["positions"][t], :64], cs[p["positions"][t], 64:]
+        for hh in range(3):
+            v = qkv64[t, hh * 128:(hh + 1) * 128]
+            wv = bf16_bits_to_f64(tensor_bits(p["q_norm_w"] if hh < 2 else p["k_norm_w"]))
+            n = v / np.sqrt((v * v).mean() + p["qk_eps"]) * wv
+            o = np.concatenate([n[:64] * c - n[64:] * sn, n[64:] * c + n[:64] * sn])
+            ob = tensor_bits(torch.from_numpy(o).to(torch.bfloat16))
+            if hh < 2:
+                want_q[t, hh * 128:(hh + 1) * 128] = ob
+            else:
+                want_k.append(ob)
+    st = check_bf16(q, want_q)
+    assert st["n_exact"] > 0.9 * st["n"]
+    got_k = np.stack([kc[0, 2, 0], kc[1, 1, 0], kc[2, 1, 0]])
+    check_bf16(got_k, np.stack(want_k))
+    got_v = np.stack([vc[0, 2, 0], vc[1, 1, 0], vc[2, 1, 0]])
+    check_bf16(got_v, tensor_bits(torch.from_numpy(qkv64[:, 384:512]).to(torch.bfloat16)))

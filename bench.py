@@ -389,6 +389,47 @@ def time_workload(w: Workload, steps: int, warmup: int, world: int, local: int):
     return ms_total, clk
 
 
+class QkvWorkload:
+    """The fused decode qkv (flint_qkv_fused) of one token: H = 2048, 32 q
+    heads, 4 kv heads of 128 (N = 5120 rows), NVFP4 weights, a residual,
+    RoPE from a 4096-position table and a paged cache of 256 blocks of 16
+    slots; `n_layers` weight sets rotated (5.9 MB each, more than L2 in all)."""
+
+    def __init__(self, dev, rank, n_layers=32, M=1, H=2048, nq=32, nkv=4):
+        import nvfp4_w4a16_mixture_gb300 as fm
+        self.fm, self.M, self.H, self.nq, self.nkv, self.n_layers = fm, M, H, nq, nkv, n_layers
+        N = (nq + 2 * nkv) * 128
+        g = torch.Generator(device=dev).manual_seed(777 + rank)
+        self.x = [synth.make_x(M, H, g, dev) for _ in range(n_layers)]
+        self.res = [synth.make_x(M, H, g, dev) for _ in range(n_layers)]
+        self.nw = (1 + 0.1 * torch.randn(H, generator=g, device=dev)).to(torch.bfloat16)
+        self.w = []
+        for _ in range(n_layers):
+            c, sf, gs = synth.quantize_nvfp4(torch.randn(N, H, generator=g, device=dev) * 0.03)
+            self.w.append((c, sf, gs.reshape(1).contiguous()))
+        self.qn = (1 + 0.1 * torch.randn(128, generator=g, device=dev)).to(torch.bfloat16)
+        self.kn = (1 + 0.1 * torch.randn(128, generator=g, device=dev)).to(torch.bfloat16)
+        ang = torch.arange(4096, dtype=torch.float64, device=dev)[:, None] * \
+            (1e6 ** (-torch.arange(64, device=dev) / 64.0))[None, :]
+        self.cs = torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).float().contiguous()
+        self.pos = torch.randint(0, 4096, (M,), generator=g, device=dev, dtype=torch.int64)
+        self.kc = torch.zeros(256, 16, nkv, 128, dtype=torch.bfloat16, device=dev)
+        self.vc = torch.zeros_like(self.kc)
+        self.slots = torch.randint(0, 256 * 16, (M,), generator=g, device=dev, dtype=torch.int64)
+        self.q = torch.empty(M, nq * 128, dtype=torch.bfloat16, device=dev)
+        self.r_out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+        self.ws = torch.zeros(fm.flint_qkv_workspace_bytes(M, H, nq, nkv), dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.Stream(device=dev)
+        self.bytes = N * H // 2 + N * H // 16 + 4
+
+    def step(self, i, s):
+        li = i % self.n_layers
+        c, sf, gs = self.w[li]
+        self.fm.flint_qkv_fused(self.x[li], self.res[li], self.nw, 1e-6, c, sf, gs, self.qn, self.kn, 1e-6,
+                                self.cs, self.pos, self.kc, self.vc, self.slots, self.nq, self.nkv,
+                                q_out=self.q, residual_out=self.r_out, workspace=self.ws, stream=s)
+
+
 def expert_load(w: Workload) -> dict:
     """Pairs per expert over the resident batches (one step per layer)."""
     cnt = torch.zeros(w.E, dtype=torch.int64)
@@ -619,6 +660,24 @@ def run_ours(args, rank, world, local):
             recs[c] = r
             del wc
             torch.cuda.empty_cache()
+        # the fused decode qkv of one token (the attention-side widened row)
+        wq = QkvWorkload(dev, rank)
+        ms_q, clk_q = time_workload(wq, 2000, 50, world, local)
+        step_s = ms_q / 2000 / 1e3
+        ach = wq.bytes / step_s / 1e9
+        recs["qkv_decode1"] = {
+            "workload": "qkv_decode1: M=1 H=2048 32 q heads, 4 kv heads of 128 (N=5120), NVFP4 weights, "
+                        "residual add-RMSNorm, q/k RMSNorm, NeoX RoPE, paged KV write",
+            "tokens_per_step": 1, "steps": 2000, "ms_per_step": round(ms_q / 2000, 6),
+            "tokens_per_s": round(job_tokens_per_s(1, 2000, world, ms_q), 2),
+            "path": "input RMSNorm, qkv GEMV, heads (3 kernels)", "gpu_launches_per_step": 3,
+            "gpu_launches": 3 * 2000, "weight_gbs": round(ach, 1), "clocks": clk_q, "traffic": None,
+            "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                         "algorithmic_bytes_per_step": wq.bytes,
+                         "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"}}
+        del wq
+        torch.cuda.empty_cache()
         res["records"] = recs
     return res
 

@@ -186,6 +186,63 @@ int flint_moe_forward_nvfp4_shared(const void* x, const void* router_w, const ui
                                    int32_t* ids_out, float* tw_out, void* workspace,
                                    size_t workspace_bytes, flint_stream_t stream);
 
+/* Fused decode qkv: "flint_qkv_fused" on the page
+ * "vllm.models.flint.ops.qkv_fused".  Per token t < M:
+ *   s = x + residual (fp32; s = x without a residual), residual_out =
+ *   bf16(s), xn = bf16((s * inv) * norm_weight) with inv = 1 / sqrt(mean(s^2)
+ *   + eps) (the add-RMSNorm of flint_moe_forward_add_norm);
+ *   qkv = bf16(fp32(xn . W row) * global_scale) for NVFP4 weights (every sum
+ *   the exact sum of the products rounded once to fp32), bf16(fp32 sum) for
+ *   BF16 weights; rows [0, 128 nq) are the q heads, then nkv k heads, then
+ *   nkv v heads;
+ *   per q and k head (128 values v): n = (v * inv) * w (w = q_norm_weight or
+ *   k_norm_weight, inv = 1 / sqrt(sum(v^2) / 128 + qk_eps), the sum of the
+ *   squares exact and rounded once), then NeoX RoPE with the fp32 table row
+ *   c | s = cos_sin_cache[positions[t]]: o[d] = n[d] c[d] - n[d+64] s[d],
+ *   o[d+64] = n[d+64] c[d] + n[d] s[d] (d < 64), fp32 math, o = n without a
+ *   table; q_out[t, 128 h + d] = bf16(o) for q head h;
+ *   with slot = slot_mapping[t] (t < num_slots) and slot >= 0: the k head h's
+ *   bf16(o) and the v head h's values go to k_cache / v_cache at element
+ *   offset (slot / block_size) * stride_block + (slot % block_size) *
+ *   stride_slot + h * stride_head + d.
+ *
+ *   x, residual  bf16 [M, H] (residual NULL: plain RMSNorm, residual_out
+ *                unused)
+ *   norm_weight  bf16 [H]
+ *   weight       NVFP4 codes uint8 [N, H/2] (even K in the low nibble) with
+ *                weight_scale uint8 [N, H/16] e4m3 row-major and one fp32
+ *                global_scale; or BF16 [N, H] with weight_scale and
+ *                global_scale NULL.  N = (num_q_heads + 2 num_kv_heads) * 128.
+ *                (The page's 128x4-swizzled scale order is a permutation of
+ *                the same bytes; this entry point takes them row-major.)
+ *   q_norm_weight, k_norm_weight  bf16 [128]
+ *   cos_sin_cache  fp32 [max_pos, 128] (cos | sin) or NULL (no RoPE);
+ *                positions int64 [M]
+ *   k_cache, v_cache  bf16 paged caches (same strides, in elements), with
+ *                num_blocks blocks of block_size slots; slot_mapping int64
+ *                [num_slots]
+ *   q_out        bf16 [M, num_q_heads * 128] (output)
+ *   residual_out bf16 [M, H] (output, with a residual)
+ *   workspace    flint_qkv_workspace_bytes(M, H, nq, nkv) bytes, 256-byte
+ *                aligned; its first word is a status word that
+ *                flint_moe_status reads.
+ * H must be a multiple of 64 (FLINT_ERR_INVALID_ARG otherwise); an odd
+ * multiple returns FLINT_ERR_UNSUPPORTED.  M = 0 is a no-op.  A position
+ * outside [0, max_pos) leaves that token's heads without RoPE, and a slot at
+ * or past num_blocks * block_size is not written; either records
+ * FLINT_ERR_INVALID_ARG in the status word.  Three launches (input norm,
+ * GEMV, heads) chained with programmatic dependent launch on `stream`. */
+size_t flint_qkv_workspace_bytes(int M, int H, int num_q_heads, int num_kv_heads);
+int flint_qkv_fused(const void* x, const void* residual, const void* norm_weight, float eps,
+                    const void* weight, const uint8_t* weight_scale, const float* global_scale,
+                    const void* q_norm_weight, const void* k_norm_weight, float qk_eps,
+                    const float* cos_sin_cache, long long max_pos, const long long* positions,
+                    void* k_cache, void* v_cache, long long stride_block, long long stride_slot,
+                    long long stride_head, int block_size, long long num_blocks,
+                    const long long* slot_mapping, int num_slots, int M, int H, int num_q_heads,
+                    int num_kv_heads, void* q_out, void* residual_out, void* workspace,
+                    size_t workspace_bytes, flint_stream_t stream);
+
 /* The decode MoE block on BF16 routed experts: "flint_moe_bf16_decode" on
  * the page above.  The same routing as flint_moe_route, then per selected
  * expert act = bf16(silu(g) * u) from the fp32 gate/up sums (no global
@@ -304,8 +361,9 @@ enum {
   FLINT_SPAN_GROUP_COUNT = 4, FLINT_SPAN_GROUP_SCAN = 5, FLINT_SPAN_GROUP_SCATTER = 6,
   FLINT_SPAN_PLAN = 7, FLINT_SPAN_GATHER = 8, FLINT_SPAN_GEMM1 = 9, FLINT_SPAN_GEMM2 = 10,
   FLINT_SPAN_COMBINE = 11, FLINT_SPAN_ADD_NORM = 12, FLINT_SPAN_SHARED_GATE_UP = 13,
-  FLINT_SPAN_SHARED_DOWN = 14, FLINT_SPAN_SHARED_ADD = 15,
-  FLINT_SPAN_KERNELS = 16, FLINT_SPAN_CTAS = 1024
+  FLINT_SPAN_SHARED_DOWN = 14, FLINT_SPAN_SHARED_ADD = 15, FLINT_SPAN_QKV_GEMV = 16,
+  FLINT_SPAN_QKV_HEADS = 17,
+  FLINT_SPAN_KERNELS = 18, FLINT_SPAN_CTAS = 1024
 };
 int flint_moe_record_spans(unsigned long long* spans);
 

@@ -15,7 +15,8 @@ from ._lib import (EXPORTED, FLINT_ERR_CUDA, FLINT_ERR_INVALID_ARG, FLINT_ERR_SC
                    flint_moe_route_noalloc_capacity, flint_moe_status, flint_moe_strerror,
                    flint_moe_workspace_bytes, forward_layer, library_path, load,
                    flint_moe_forward_add_norm, forward_add_norm_layer, flint_moe_record_spans,
-                   spans_of, SPAN_NAMES, flint_moe_forward_bf16, flint_moe_forward_nvfp4_shared)
+                   spans_of, SPAN_NAMES, flint_moe_forward_bf16, flint_moe_forward_nvfp4_shared,
+                   flint_qkv_workspace_bytes, flint_qkv_fused)
 
 __all__ = [
     "EXPORTED", "FLINT_OK", "FLINT_ERR_INVALID_ARG", "FLINT_ERR_UNSUPPORTED",
@@ -24,7 +25,7 @@ __all__ = [
     "FLINT_PATH_DECODE", "FLINT_PATH_DECODE_FALLBACK", "FLINT_PATH_GROUPED", "flint_moe_plan",
     "flint_moe_prefer_path", "flint_moe_forward_add_norm", "forward_add_norm_layer",
     "flint_moe_record_spans", "spans_of", "SPAN_NAMES", "flint_moe_forward_bf16",
-    "flint_moe_forward_nvfp4_shared",
+    "flint_moe_forward_nvfp4_shared", "flint_qkv_workspace_bytes", "flint_qkv_fused",
     "FlintMoEError", "alloc_workspace", "flint_moe_debug_fault", "flint_moe_forward",
     "flint_moe_route",
     "flint_moe_route_noalloc", "flint_moe_route_noalloc_bytes",

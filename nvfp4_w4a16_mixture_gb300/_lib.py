@@ -35,7 +35,7 @@ EXPORTED = ("flint_moe_workspace_bytes", "flint_moe_route", "flint_moe_forward",
             "flint_moe_route_noalloc_capacity", "flint_moe_status", "flint_moe_strerror",
             "flint_moe_debug_fault", "flint_moe_plan", "flint_moe_prefer_path",
             "flint_moe_forward_add_norm", "flint_moe_record_spans", "flint_moe_forward_bf16",
-            "flint_moe_forward_nvfp4_shared")
+            "flint_moe_forward_nvfp4_shared", "flint_qkv_workspace_bytes", "flint_qkv_fused")
 
 
 class FlintMoEError(RuntimeError):
@@ -96,6 +96,12 @@ def load() -> ctypes.CDLL:
             lib.flint_moe_forward_bf16.argtypes = [P] * 5 + [S, P, P, P, P, ctypes.c_size_t, P]
             lib.flint_moe_record_spans.restype = ctypes.c_int
             lib.flint_moe_record_spans.argtypes = [P]
+            I, LL, F = ctypes.c_int, ctypes.c_longlong, ctypes.c_float
+            lib.flint_qkv_workspace_bytes.restype = ctypes.c_size_t
+            lib.flint_qkv_workspace_bytes.argtypes = [I, I, I, I]
+            lib.flint_qkv_fused.restype = ctypes.c_int
+            lib.flint_qkv_fused.argtypes = ([P, P, P, F, P, P, P, P, P, F, P, LL, P, P, P, LL, LL, LL, I, LL, P,
+                                             I, I, I, I, I, P, P, P, ctypes.c_size_t, P])
             _lib = lib
     return _lib
 
@@ -255,8 +261,8 @@ def flint_moe_prefer_path(path: int) -> None:
 
 SPAN_NAMES = ("route", "gate_up", "down", "single_launch", "group_count", "group_scan",
               "group_scatter", "plan", "gather", "gemm1", "gemm2", "combine", "add_norm",
-              "shared_gate_up", "shared_down", "shared_add")
-SPAN_KERNELS = 16
+              "shared_gate_up", "shared_down", "shared_add", "qkv_gemv", "qkv_heads")
+SPAN_KERNELS = 18
 SPAN_CTAS = 1024
 
 
@@ -341,3 +347,42 @@ def forward_layer(x, layer, top_k: int, workspace=None, out=None, ids_out=None, 
                       layer.shared_down if layer.SI else None, top_k, out, workspace,
                       ids_out=ids_out, tw_out=tw_out, stream=stream)
     return out
+
+
+def flint_qkv_workspace_bytes(M: int, H: int, num_q_heads: int, num_kv_heads: int) -> int:
+    """Workspace bytes of flint_qkv_fused (0 for an invalid or unsupported shape)."""
+    return int(load().flint_qkv_workspace_bytes(int(M), int(H), int(num_q_heads), int(num_kv_heads)))
+
+
+def flint_qkv_fused(x, residual, norm_weight, eps: float, weight, weight_scale, global_scale, q_norm_weight,
+                    k_norm_weight, qk_eps: float, cos_sin_cache, positions, k_cache, v_cache, slot_mapping,
+                    num_q_heads: int, num_kv_heads: int, q_out=None, residual_out=None, workspace=None,
+                    stream=None):
+    """Fused decode qkv (flint_qkv_fused on the qkv_fused page): input
+    (add-)RMSNorm, the qkv GEMV (NVFP4 codes uint8 [N, H/2] with e4m3 scale
+    bytes [N, H/16] and a one-element fp32 global scale, or BF16 [N, H]),
+    per-head q/k RMSNorm, NeoX RoPE and the paged KV-cache write.  k_cache /
+    v_cache: bf16 [blocks, block_size, kv_heads, 128] views (any strides but a
+    unit last one).  Returns (q, residual_out or None)."""
+    M, H = x.shape
+    if q_out is None:
+        q_out = torch.empty(M, num_q_heads * 128, dtype=torch.bfloat16, device=x.device)
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty_like(x)
+    if workspace is None:
+        workspace = torch.zeros(max(1, flint_qkv_workspace_bytes(M, H, num_q_heads, num_kv_heads)),
+                                dtype=torch.uint8, device=x.device)
+    assert k_cache.stride() == v_cache.stride() and k_cache.stride(-1) == 1
+    blocks, bs = k_cache.shape[0], k_cache.shape[1]
+    max_pos = cos_sin_cache.shape[0] if cos_sin_cache is not None else 0
+    rc = load().flint_qkv_fused(
+        _ptr(x), _ptr(residual), _ptr(norm_weight), float(eps), _ptr(weight), _ptr(weight_scale),
+        _ptr(global_scale), _ptr(q_norm_weight), _ptr(k_norm_weight), float(qk_eps), _ptr(cos_sin_cache),
+        int(max_pos), _ptr(positions), _ptr(k_cache), _ptr(v_cache), int(k_cache.stride(0)),
+        int(k_cache.stride(1)), int(k_cache.stride(2)), int(bs), int(blocks), _ptr(slot_mapping),
+        int(slot_mapping.shape[0]) if slot_mapping is not None else 0, M, H, int(num_q_heads),
+        int(num_kv_heads), _ptr(q_out), _ptr(residual_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != FLINT_OK:
+        raise FlintMoEError(rc, "flint_qkv_fused")
+    return q_out, residual_out

@@ -6,6 +6,9 @@
 // unrounded fp32 sum s = a + r, inv = rsqrt(mean(s^2) + eps),
 // xn = bf16(s * inv * w)), then runs the MoE block on x.
 //
+// Without a residual (r == nullptr) it is the plain RMSNorm of a, and
+// res_out (then optional) is not written.
+//
 // One CTA of 8 warps per token, each thread a few 8-element vectors of the
 // row, kept in registers between the two passes (rows up to 4096 wide; the
 // rest of a wider row is read again).  The sum of squares is taken in double
@@ -24,8 +27,20 @@ namespace {
 constexpr int kNormThreads = 256;
 constexpr int kNormCache = 2;  // row vectors kept in registers per thread
 
-FLINT_DEV void add_vec(const uint4& av, const uint4& rv, float (&s)[8]) {
-  const uint32_t aw[4] = {av.x, av.y, av.z, av.w}, rw[4] = {rv.x, rv.y, rv.z, rv.w};
+// s = a + r in fp32 (r == nullptr: s = a, no addition)
+FLINT_DEV void add_vec(const uint16_t* ap, const uint16_t* rp, float (&s)[8]) {
+  const uint4 av = ldg_nc_v4(ap);
+  const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+  if (!rp) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      s[2 * q] = __uint_as_float(aw[q] << 16);
+      s[2 * q + 1] = __uint_as_float(aw[q] & 0xFFFF0000u);
+    }
+    return;
+  }
+  const uint4 rv = ldg_nc_v4(rp);
+  const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     s[2 * q] = __fadd_rn(__uint_as_float(aw[q] << 16), __uint_as_float(rw[q] << 16));
@@ -43,13 +58,13 @@ __global__ void __launch_bounds__(kNormThreads) add_rms_norm_kernel(
   __shared__ float s_inv;
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint16_t* at = a + (size_t)t * H;
-  const uint16_t* rt = r + (size_t)t * H;
+  const uint16_t* rt = r ? r + (size_t)t * H : nullptr;  // no residual: plain RMSNorm
   const int nv = H / 8;  // 8-element vectors of the row
   float cache[kNormCache][8];
   double sq0 = 0.0, sq1 = 0.0;
   for (int v = tid, i = 0; v < nv; v += kNormThreads, ++i) {
     float sv[8];
-    add_vec(ldg_nc_v4(at + 8 * v), ldg_nc_v4(rt + 8 * v), sv);
+    add_vec(at + 8 * v, rt ? rt + 8 * v : nullptr, sv);
     uint32_t o[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -57,7 +72,8 @@ __global__ void __launch_bounds__(kNormThreads) add_rms_norm_kernel(
       sq0 = fma((double)sv[2 * q], (double)sv[2 * q], sq0);
       sq1 = fma((double)sv[2 * q + 1], (double)sv[2 * q + 1], sq1);
     }
-    *reinterpret_cast<uint4*>(res_out + (size_t)t * H + 8 * v) = make_uint4(o[0], o[1], o[2], o[3]);
+    if (res_out)
+      *reinterpret_cast<uint4*>(res_out + (size_t)t * H + 8 * v) = make_uint4(o[0], o[1], o[2], o[3]);
 #pragma unroll
     for (int c = 0; c < kNormCache; ++c)
       if (c == i)
@@ -86,7 +102,7 @@ __global__ void __launch_bounds__(kNormThreads) add_rms_norm_kernel(
 #pragma unroll
           for (int j = 0; j < 8; ++j) sv[j] = cache[c][j];
     } else {
-      add_vec(ldg_nc_v4(at + 8 * v), ldg_nc_v4(rt + 8 * v), sv);
+      add_vec(at + 8 * v, rt ? rt + 8 * v : nullptr, sv);
     }
     const uint4 wv = ldg_nc_v4(w + 8 * v);
     const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};

@@ -380,10 +380,85 @@ int flint_moe_record_spans(unsigned long long* spans) {
                                                      span_buffer_set_fused, span_buffer_set_grouped,
                                                      span_buffer_set_route, span_buffer_set_add_norm,
                                                      span_buffer_set_bf16_experts,
-                                                     span_buffer_set_shared_nvfp4};
+                                                     span_buffer_set_shared_nvfp4, span_buffer_set_qkv};
   for (auto f : set)
     if (f(spans) != cudaSuccess) return FLINT_ERR_CUDA;
   return FLINT_OK;
+}
+
+// ---------------------------------------------------------- fused qkv --
+// Workspace: status word (offset 0, read by flint_moe_status), xn [M, H],
+// qkv [M, (nq + 2 nkv) * 128], each region 256-byte aligned.
+static size_t qkv_ws(int M, int H, int nq, int nkv, size_t* xn_off, size_t* qkv_off) {
+  auto al = [](size_t v) { return (v + 255) / 256 * 256; };
+  const size_t xo = 256, qo = xo + al((size_t)M * H * 2);
+  if (xn_off) *xn_off = xo;
+  if (qkv_off) *qkv_off = qo;
+  return qo + al((size_t)M * (nq + 2 * nkv) * 128 * 2);
+}
+
+size_t flint_qkv_workspace_bytes(int M, int H, int num_q_heads, int num_kv_heads) {
+  if (M < 0 || H <= 0 || H % 128 != 0 || num_q_heads < 1 || num_kv_heads < 0) return 0;
+  return qkv_ws(M, H, num_q_heads, num_kv_heads, nullptr, nullptr);
+}
+
+int flint_qkv_fused(const void* x, const void* residual, const void* norm_weight, float eps,
+                    const void* weight, const uint8_t* weight_scale, const float* global_scale,
+                    const void* q_norm_weight, const void* k_norm_weight, float qk_eps,
+                    const float* cos_sin_cache, long long max_pos, const long long* positions,
+                    void* k_cache, void* v_cache, long long stride_block, long long stride_slot,
+                    long long stride_head, int block_size, long long num_blocks,
+                    const long long* slot_mapping, int num_slots, int M, int H, int num_q_heads,
+                    int num_kv_heads, void* q_out, void* residual_out, void* workspace, size_t ws_bytes,
+                    flint_stream_t stream) {
+  if (M < 0 || H <= 0 || H % 64 != 0 || num_q_heads < 1 || num_kv_heads < 0 || num_slots < 0)
+    return FLINT_ERR_INVALID_ARG;
+  if (H % 128 != 0) return FLINT_ERR_UNSUPPORTED;
+  if (M == 0) return FLINT_OK;
+  if (!x || !norm_weight || !weight || !q_norm_weight || !q_out) return FLINT_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(norm_weight, 16) || !aligned(weight, 16) || !aligned(q_out, 16) ||
+      !aligned(q_norm_weight, 2))
+    return FLINT_ERR_INVALID_ARG;
+  if (residual && (!aligned(residual, 16) || !residual_out || !aligned(residual_out, 16)))
+    return FLINT_ERR_INVALID_ARG;
+  if (weight_scale && (!global_scale || !aligned(global_scale, 4))) return FLINT_ERR_INVALID_ARG;
+  if (cos_sin_cache && (!positions || max_pos < 1 || !aligned(cos_sin_cache, 4) || !aligned(positions, 8)))
+    return FLINT_ERR_INVALID_ARG;
+  if (num_kv_heads > 0 && (!k_norm_weight || !aligned(k_norm_weight, 2))) return FLINT_ERR_INVALID_ARG;
+  const bool writes = num_kv_heads > 0 && num_slots > 0;
+  if (writes && (!k_cache || !v_cache || !slot_mapping || !aligned(k_cache, 2) || !aligned(v_cache, 2) ||
+                 !aligned(slot_mapping, 8) || block_size < 1 || num_blocks < 0 || stride_block < 0 ||
+                 stride_slot < 0 || stride_head < 0))
+    return FLINT_ERR_INVALID_ARG;
+  size_t xo = 0, qo = 0;
+  const size_t need = qkv_ws(M, H, num_q_heads, num_kv_heads, &xo, &qo);
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < need) return FLINT_ERR_WORKSPACE;
+  uint8_t* wb = static_cast<uint8_t*>(workspace);
+  QkvArgs a = {};
+  a.M = M; a.H = H; a.nq = num_q_heads; a.nkv = num_kv_heads;
+  a.q_norm_w = static_cast<const uint16_t*>(q_norm_weight);
+  a.k_norm_w = static_cast<const uint16_t*>(k_norm_weight);
+  a.qk_eps = qk_eps;
+  a.cos_sin = cos_sin_cache;
+  a.max_pos = max_pos;
+  a.positions = positions;
+  a.slot_mapping = writes ? slot_mapping : nullptr;
+  a.n_slots = writes ? num_slots : 0;
+  a.k_cache = static_cast<uint16_t*>(k_cache);
+  a.v_cache = static_cast<uint16_t*>(v_cache);
+  a.s_block = stride_block; a.s_slot = stride_slot; a.s_head = stride_head;
+  a.block_size = block_size > 0 ? block_size : 1;
+  a.num_blocks = num_blocks;
+  a.q_out = static_cast<uint16_t*>(q_out);
+  a.xn = reinterpret_cast<uint16_t*>(wb + xo);
+  a.qkv = reinterpret_cast<uint16_t*>(wb + qo);
+  a.status = reinterpret_cast<int*>(wb);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t err =
+      launch_qkv_fused(a, static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(residual),
+                       static_cast<const uint16_t*>(norm_weight), eps, weight, weight_scale, global_scale,
+                       residual ? static_cast<uint16_t*>(residual_out) : nullptr, st);
+  return err == cudaSuccess ? FLINT_OK : FLINT_ERR_CUDA;
 }
 
 int flint_moe_debug_fault(int site) {

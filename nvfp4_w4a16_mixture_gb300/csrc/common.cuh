@@ -307,7 +307,7 @@ enum {
   kSpanRoute = 0, kSpanGateUp = 1, kSpanDown = 2, kSpanSingle = 3, kSpanGroupCount = 4,
   kSpanGroupScan = 5, kSpanGroupScatter = 6, kSpanPlan = 7, kSpanGather = 8, kSpanGemm1 = 9,
   kSpanGemm2 = 10, kSpanCombine = 11, kSpanAddNorm = 12, kSpanSharedGateUp = 13, kSpanSharedDown = 14,
-  kSpanSharedAdd = 15
+  kSpanSharedAdd = 15, kSpanQkvGemv = 16, kSpanQkvHeads = 17
 };
 static __device__ unsigned long long* g_span_buf;
 FLINT_DEV unsigned long long* span_slot(int id) {

@@ -160,12 +160,40 @@ cudaError_t span_buffer_set_route(unsigned long long* b);
 cudaError_t span_buffer_set_add_norm(unsigned long long* b);
 cudaError_t span_buffer_set_bf16_experts(unsigned long long* b);
 cudaError_t span_buffer_set_shared_nvfp4(unsigned long long* b);
+cudaError_t span_buffer_set_qkv(unsigned long long* b);
 
 // NVFP4 shared expert (shared_nvfp4.cu): sact and ys (workspace), then
 // out = bf16(out + ys) over the block's routed output.
 cudaError_t launch_shared_nvfp4(const uint16_t* x, const uint8_t* gu, const uint8_t* gu_sf, const float* gu_gs,
                                 const uint8_t* dn, const uint8_t* dn_sf, const float* dn_gs, int M, int H,
                                 int SI, uint16_t* sact, uint16_t* ys, uint16_t* out, cudaStream_t st);
+
+// Fused decode qkv (qkv.cu): the arguments of its GEMV and head kernels.
+struct QkvArgs {
+  int M, H, nq, nkv;
+  const uint16_t* q_norm_w;
+  const uint16_t* k_norm_w;
+  float qk_eps;
+  const float* cos_sin;  // [max_pos, 128] fp32 (cos | sin), or null: no RoPE
+  long long max_pos;
+  const long long* positions;     // [M]
+  const long long* slot_mapping;  // [n_slots]
+  int n_slots;
+  uint16_t* k_cache;  // element offsets block * s_block + offset * s_slot + head * s_head + d
+  uint16_t* v_cache;
+  long long s_block, s_slot, s_head;
+  int block_size;
+  long long num_blocks;
+  uint16_t* q_out;  // [M, nq * 128]
+  uint16_t* xn;     // workspace [M, H]
+  uint16_t* qkv;    // workspace [M, (nq + 2 nkv) * 128]
+  int* status;      // workspace status word
+};
+// Input RMSNorm (add_norm.cu, residual may be null), the qkv GEMV (NVFP4 when
+// w_sf is not null) and the head kernel.
+cudaError_t launch_qkv_fused(const QkvArgs& a, const uint16_t* x, const uint16_t* residual,
+                             const uint16_t* norm_w, float eps, const void* w, const uint8_t* w_sf,
+                             const float* gs, uint16_t* res_out, cudaStream_t st);
 
 // BF16 routed experts (bf16_experts.cu), M <= kDecodeMaxTokens: router with
 // the expert grouping, exact gate/up and down sums, combine with the given

@@ -20,7 +20,7 @@ def declared_functions() -> set[str]:
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
         text = open(h).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        for m in re.finditer(r"\b(flint_moe_\w+)\s*\(", text):
+        for m in re.finditer(r"\b(flint_\w+)\s*\(", text):
             names.add(m.group(1))
     return names
 
@@ -237,3 +237,35 @@ def test_forward_bf16_validation_is_synchronous():
     assert call((2, 256, 8, 2, 128, 0), x=None) == fm.FLINT_ERR_INVALID_ARG
     assert call((2, 256, 8, 2, 128, 0), ws_bytes=16) == fm.FLINT_ERR_WORKSPACE
     assert call((0, 256, 8, 2, 128, 0), x=None) == fm.FLINT_OK
+
+
+def test_qkv_fused_validation_is_synchronous():
+    """The fused qkv entry point sizes its workspace, refuses bad shapes,
+    odd multiples of 64, missing pointers and a short workspace, and treats
+    M = 0 as a no-op, before any CUDA call."""
+    lib = fm.load()
+    M, H, nq, nkv = 2, 256, 2, 1
+    need = fm.flint_qkv_workspace_bytes(M, H, nq, nkv)
+    N = (nq + 2 * nkv) * 128
+    assert need >= 256 + M * H * 2 + M * N * 2
+    assert fm.flint_qkv_workspace_bytes(M, 192, nq, nkv) == 0
+    assert fm.flint_qkv_workspace_bytes(M, H, 0, nkv) == 0
+    f = [0x10000 * (i + 1) for i in range(16)]
+
+    def call(M=M, H=H, nq=nq, nkv=nkv, x=f[0], weight=f[2], ws=f[10], ws_bytes=need, slots=f[8], n_slots=M,
+             k_cache=f[6], q_out=f[9], block_size=16):
+        return lib.flint_qkv_fused(x, None, f[1], 1e-6, weight, None, None, f[3], f[4], 1e-6, None, 0, None,
+                                   k_cache, f[7], 1024, 256, 128, block_size, 4, slots, n_slots, M, H, nq, nkv,
+                                   q_out, None, ws, ws_bytes, None)
+
+    assert call(H=250) == fm.FLINT_ERR_INVALID_ARG
+    assert call(H=192) == fm.FLINT_ERR_UNSUPPORTED
+    assert call(nq=0) == fm.FLINT_ERR_INVALID_ARG
+    assert call(x=None) == fm.FLINT_ERR_INVALID_ARG
+    assert call(weight=f[2] + 8) == fm.FLINT_ERR_INVALID_ARG  # not 16-byte aligned
+    assert call(q_out=None) == fm.FLINT_ERR_INVALID_ARG
+    assert call(k_cache=None) == fm.FLINT_ERR_INVALID_ARG
+    assert call(block_size=0) == fm.FLINT_ERR_INVALID_ARG
+    assert call(ws_bytes=need - 1) == fm.FLINT_ERR_WORKSPACE
+    assert call(ws=None) == fm.FLINT_ERR_WORKSPACE
+    assert call(M=0, x=None, ws=None) == fm.FLINT_OK

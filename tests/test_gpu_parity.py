@@ -447,7 +447,7 @@ def test_kernel_spans_are_recorded(decode_layer):
     buffer stays untouched."""
     x1, layer, k = decode_layer
     ws = fm.alloc_workspace(1, layer.H, layer.E, k, layer.I, layer.SI)
-    buf = torch.zeros(16 * 1024 * 2, dtype=torch.int64, device="cuda")
+    buf = torch.zeros(fm._lib.SPAN_KERNELS * fm._lib.SPAN_CTAS * 2, dtype=torch.int64, device="cuda")
     fm.flint_moe_record_spans(buf)
     try:
         fm.forward_layer(x1, layer, k, workspace=ws)
@@ -527,3 +527,97 @@ def test_forward_nvfp4_shared(shape):
     got = bits(out)
     check_bf16(got, want.view(torch.int16).numpy().view(np.uint16), "out",
                allow_outside=allowance((M, H, E, k, I, 0), got.size))
+
+
+# ------------------------------------------------------------ fused qkv (R11)
+MARK = 0x7FC1  # a NaN pattern no kernel writes: cache entries that must stay untouched
+
+
+def _qkv_inputs(M, H, nq, nkv, nvfp4, residual, rope, seed, max_pos=64):
+    g = torch.Generator().manual_seed(seed)
+    N = (nq + 2 * nkv) * 128
+    x = synth.make_x(M, H, g)
+    res = synth.make_x(M, H, g) if residual else None
+    nw = (1 + 0.1 * torch.randn(H, generator=g)).to(torch.bfloat16)
+    w = torch.randn(N, H, generator=g) * 0.03
+    if nvfp4:
+        codes, sf, gs = synth.quantize_nvfp4(w)
+        weight, scale, gsv = codes, sf, gs.reshape(1).float()
+    else:
+        weight, scale, gsv = w.to(torch.bfloat16), None, None
+    qn = (1 + 0.1 * torch.randn(128, generator=g)).to(torch.bfloat16)
+    kn = (1 + 0.1 * torch.randn(128, generator=g)).to(torch.bfloat16)
+    if rope:
+        ang = torch.arange(max_pos, dtype=torch.float64)[:, None] * (1e6 ** (-torch.arange(64) / 64.0))[None, :]
+        cs = torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).float()
+    else:
+        cs = None
+    pos = torch.randint(0, max_pos, (M,), generator=g, dtype=torch.int64)
+    return x, res, nw, weight, scale, gsv, qn, kn, cs, pos
+
+
+@pytest.mark.parametrize("M,H,nq,nkv,nvfp4,residual,rope", [
+    (1, 2048, 32, 4, True, True, True),
+    (8, 2048, 32, 4, True, True, True),
+    (8, 2048, 32, 4, False, True, True),
+    (3, 256, 2, 2, True, False, True),
+    (5, 384, 3, 1, False, True, False),
+])
+def test_qkv_fused(M, H, nq, nkv, nvfp4, residual, rope):
+    """flint_qkv_fused against the oracle (reading R11): q, residual' and
+    the cache entries under the rule as stated, most of them bit for bit;
+    cache entries of negative slots and of tokens past the mapping untouched."""
+    x, res, nw, weight, scale, gsv, qn, kn, cs, pos = _qkv_inputs(M, H, nq, nkv, nvfp4, residual, rope, seed=M + H)
+    blocks, bs = 8, 4
+    slots = torch.tensor([5, -1, 30, 0, 17, 9, 22, 3][:max(1, M - 1)], dtype=torch.int64)  # one token unmapped
+    kc = torch.full((blocks, bs, nkv, 128), MARK, dtype=torch.int16).view(torch.bfloat16)
+    vc = kc.clone()
+    dev = "cuda"
+    kcg, vcg = kc.to(dev), vc.to(dev)
+    q, r_out = fm.flint_qkv_fused(x.to(dev), None if res is None else res.to(dev), nw.to(dev), 1e-6,
+                                  weight.to(dev), None if scale is None else scale.to(dev),
+                                  None if gsv is None else gsv.to(dev), qn.to(dev), kn.to(dev), 1e-6,
+                                  None if cs is None else cs.to(dev), pos.to(dev), kcg, vcg, slots.to(dev), nq, nkv)
+    torch.cuda.synchronize()
+    kco, vco = bits(kc).copy(), bits(vc).copy()
+    q_ref, r_ref, _, _ = oracle.qkv_fused(x, res, nw, 1e-6, weight, scale, None if gsv is None else float(gsv),
+                                          qn, kn, 1e-6, None if cs is None else cs.numpy(), pos.numpy(), kco, vco,
+                                          slots.numpy(), nq, nkv)
+    st = check_bf16(bits(q), q_ref, "q")
+    assert st["n_exact"] >= st["n"] - max(2, st["n"] // 1000), st
+    if res is not None:
+        assert np.array_equal(bits(r_out), r_ref)
+    kg, vg = bits(kcg), bits(vcg)
+    untouched = kco == MARK
+    assert np.array_equal(kg == MARK, untouched) and np.array_equal(vg == MARK, vco == MARK)
+    if (~untouched).any():
+        check_bf16(kg[~untouched], kco[~untouched], "k cache")
+        check_bf16(vg[vco != MARK], vco[vco != MARK], "v cache")
+
+
+def test_qkv_fused_bad_position_and_slot_are_reported():
+    """A position past the table and a slot past the cache are skipped and
+    reported in the status word; the other tokens are computed as usual."""
+    M, H, nq, nkv = 3, 256, 2, 1
+    x, res, nw, weight, scale, gsv, qn, kn, cs, pos = _qkv_inputs(M, H, nq, nkv, True, True, True, seed=3)
+    dev = "cuda"
+    pos = pos.clone()
+    pos[1] = 64  # the table has 64 rows
+    slots = torch.tensor([2, 5, 1000], dtype=torch.int64)  # 1000 is past 8 blocks of 4
+    kc = torch.full((8, 4, nkv, 128), MARK, dtype=torch.int16).view(torch.bfloat16).to(dev)
+    vc = kc.clone()
+    ws = torch.zeros(fm.flint_qkv_workspace_bytes(M, H, nq, nkv), dtype=torch.uint8, device=dev)
+    q, _ = fm.flint_qkv_fused(x.to(dev), res.to(dev), nw.to(dev), 1e-6, weight.to(dev), scale.to(dev), gsv.to(dev),
+                              qn.to(dev), kn.to(dev), 1e-6, cs.to(dev), pos.to(dev), kc, vc, slots.to(dev), nq, nkv,
+                              workspace=ws)
+    assert fm.flint_moe_status(ws) == fm.FLINT_ERR_INVALID_ARG
+    assert fm.flint_moe_status(ws) == fm.FLINT_OK  # read and cleared
+    kco = np.full((8, 4, nkv, 128), MARK, np.uint16)
+    vco = kco.copy()
+    q_ref, _, _, _ = oracle.qkv_fused(x, res, nw, 1e-6, weight, scale, float(gsv), qn, kn, 1e-6, cs.numpy(),
+                                      np.array([int(pos[0]), 0, int(pos[2])]), kco, vco, np.array([2, 5, -1]),
+                                      nq, nkv)
+    got = bits(q)
+    check_bf16(got[[0, 2]], q_ref[[0, 2]], "q of the valid tokens")
+    assert np.array_equal(bits(kc)[0, 2], kco[0, 2]) and np.array_equal(bits(kc)[1, 1], kco[1, 1])
+    assert int((bits(kc) != MARK).sum()) == 2 * 128  # tokens 0 and 1 only

@@ -12,6 +12,7 @@ Rules and citations are in the C file's header.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -41,41 +42,77 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _bind(lib):
+    """Declare the C signatures on a loaded oracle library."""
+    P = ctypes.c_void_p
+    i32 = ctypes.c_int
+    lib.oracle_e2m1_value.restype = ctypes.c_float
+    lib.oracle_e2m1_value.argtypes = [i32]
+    lib.oracle_e4m3_value.restype = ctypes.c_float
+    lib.oracle_e4m3_value.argtypes = [i32]
+    lib.oracle_bf16_round.restype = None
+    lib.oracle_bf16_round.argtypes = [P, P, ctypes.c_int64]
+    lib.oracle_nvfp4_dequant.restype = None
+    lib.oracle_nvfp4_dequant.argtypes = [P, P, ctypes.c_int64, i32, P]
+    lib.oracle_route.restype = i32
+    lib.oracle_route.argtypes = [P, P, i32, i32, i32, i32, P, P, P]
+    lib.oracle_topk.restype = i32
+    lib.oracle_topk.argtypes = [P, i32, i32, i32, P, P]
+    lib.oracle_forward.restype = i32
+    lib.oracle_forward.argtypes = [P] * 10 + [i32] * 6 + [P, i32] + [P] * 8 + [i32]
+    lib.oracle_shared_nvfp4.restype = i32
+    lib.oracle_shared_nvfp4.argtypes = [P, P, P, ctypes.c_float, P, P, ctypes.c_float, i32, i32, i32, P, P]
+    lib.oracle_forward_bf16.restype = i32
+    lib.oracle_forward_bf16.argtypes = [P] * 5 + [i32] * 5 + [P] * 5 + [i32]
+    lib.oracle_add_rms_norm.restype = i32
+    lib.oracle_add_rms_norm.argtypes = [P, P, P, i32, i32, ctypes.c_float, P, P]
+    lib.oracle_max_threads.restype = i32
+    lib.oracle_max_threads.argtypes = []
+    lib.oracle_qkv_fused.restype = i32
+    lib.oracle_qkv_fused.argtypes = ([P, P, P, ctypes.c_float, P, P, ctypes.c_float, P, P, P, ctypes.c_float,
+                                      P, P, P, i32, i32, i32, i32, i32, i32, ctypes.c_int64, ctypes.c_int64,
+                                      ctypes.c_int64] + [P] * 6)
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            P = ctypes.c_void_p
-            i32 = ctypes.c_int
-            lib.oracle_e2m1_value.restype = ctypes.c_float
-            lib.oracle_e2m1_value.argtypes = [i32]
-            lib.oracle_e4m3_value.restype = ctypes.c_float
-            lib.oracle_e4m3_value.argtypes = [i32]
-            lib.oracle_bf16_round.restype = None
-            lib.oracle_bf16_round.argtypes = [P, P, ctypes.c_int64]
-            lib.oracle_nvfp4_dequant.restype = None
-            lib.oracle_nvfp4_dequant.argtypes = [P, P, ctypes.c_int64, i32, P]
-            lib.oracle_route.restype = i32
-            lib.oracle_route.argtypes = [P, P, i32, i32, i32, i32, P, P, P]
-            lib.oracle_topk.restype = i32
-            lib.oracle_topk.argtypes = [P, i32, i32, i32, P, P]
-            lib.oracle_forward.restype = i32
-            lib.oracle_forward.argtypes = [P] * 10 + [i32] * 6 + [P, i32] + [P] * 8 + [i32]
-            lib.oracle_shared_nvfp4.restype = i32
-            lib.oracle_shared_nvfp4.argtypes = [P, P, P, ctypes.c_float, P, P, ctypes.c_float, i32, i32, i32,
-                                                P, P]
-            lib.oracle_forward_bf16.restype = i32
-            lib.oracle_forward_bf16.argtypes = [P] * 5 + [i32] * 5 + [P] * 5 + [i32]
-            lib.oracle_add_rms_norm.restype = i32
-            lib.oracle_add_rms_norm.argtypes = [P, P, P, i32, i32, ctypes.c_float, P, P]
-            lib.oracle_max_threads.restype = i32
-            lib.oracle_max_threads.argtypes = []
-            lib.oracle_qkv_fused.argtypes = ([P, P, P, ctypes.c_float, P, P, ctypes.c_float, P, P, P,
-                                              ctypes.c_float, P, P, P, i32, i32, i32, i32, i32, i32,
-                                              ctypes.c_int64, ctypes.c_int64, ctypes.c_int64] + [P] * 6)
-            _lib = lib
+            _lib = _bind(ctypes.CDLL(build()))
     return _lib
+
+
+def build_variant(source: str, out_path: str) -> str:
+    """Test hook: compile another version of the oracle's C source (a
+    planted mistake) with the oracle's own flags; returns the .so path."""
+    src = out_path + ".c"
+    with open(src, "w") as f:
+        f.write(source)
+    subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared",
+                    "-std=c11", "-o", out_path, src, "-lm"], check=True)
+    return out_path
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Test hook: route every oracle call to the library at `path` (built by
+    build_variant) for the duration of the block."""
+    global _lib
+    _load()
+    with _lock:
+        saved, _lib = _lib, _bind(ctypes.CDLL(path))
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = saved
+
+
+def source() -> str:
+    """The oracle's C source text (for test variants)."""
+    with open(_SRC) as f:
+        return f.read()
 
 
 def _np(t, dtype):

@@ -677,3 +677,22 @@ def test_qkv_matches_float64():
     check_bf16(got_k, np.stack(want_k))
     got_v = np.stack([vc[0, 2, 0], vc[1, 1, 0], vc[2, 1, 0]])
     check_bf16(got_v, tensor_bits(torch.from_numpy(qkv64[:, 384:512]).to(torch.bfloat16)))
+
+
+# ------------------------------------------------------- exact sums (R7)
+def test_expert_sums_are_exact_not_sequential():
+    """Reading R7 on a constructed row: x = (2^24, 1, -2^24, 0, ...) against
+    unit weights.  The exact sum is 1; an fp32 loop in index order would
+    lose the 1 (2^24 + 1 rounds to 2^24) and give 0.  So g = u = 1 and act =
+    bf16(silu(1) * 1), with silu(1) from float64."""
+    M, H, E, k, I, SI = 1, 256, 1, 1, 64, 0
+    x, layer = synth.make_problem(M, H, E, k, I, SI, seed=3)
+    xv = torch.zeros(M, H)
+    xv[0, 0], xv[0, 1], xv[0, 2] = 2.0 ** 24, 1.0, -(2.0 ** 24)
+    x = xv.to(torch.bfloat16)
+    layer.w13.fill_(0x22)  # two e2m1 codes 2 = 1.0 per byte
+    layer.w13_sf.fill_(0x38)  # e4m3 1.0
+    layer.w13_gs.fill_(1.0)
+    r = oracle.forward(x, layer, k, intermediates=True)
+    want = torch.tensor(1.0 / (1.0 + np.exp(-1.0)), dtype=torch.float64).float().to(torch.bfloat16)
+    assert np.array_equal(r["act"][0, 0], np.full(I, tensor_bits(want), np.uint16))

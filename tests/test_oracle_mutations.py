@@ -24,6 +24,10 @@ CASES = [
      "unsigned code = (k & 1) ? (byte >> 4) : (byte & 15u);",
      "unsigned code = (k & 1) ? (byte & 15u) : (byte >> 4);",
      pins.test_unit_scales_reduce_to_matmul),
+    ("router butterfly run from offset 1 up (reading R1)",
+     "for (int o = 16; o >= 1; o >>= 1) {",
+     "for (int o = 1; o <= 16; o <<= 1) {",
+     pins.test_router_order_is_the_lane_butterfly),
     ("e4m3 exponent bias 8 instead of 7",
      "mag = ldexpf(1.0f + (float)m / 8.0f, (int)e - 7);",
      "mag = ldexpf(1.0f + (float)m / 8.0f, (int)e - 8);",

@@ -696,3 +696,19 @@ def test_expert_sums_are_exact_not_sequential():
     r = oracle.forward(x, layer, k, intermediates=True)
     want = torch.tensor(1.0 / (1.0 + np.exp(-1.0)), dtype=torch.float64).float().to(torch.bfloat16)
     assert np.array_equal(r["act"][0, 0], np.full(I, tensor_bits(want), np.uint16))
+
+
+def test_router_order_is_the_lane_butterfly():
+    """Reading R1 on a constructed row (H = 256: lane l holds the products of
+    elements 8 l .. 8 l + 7): lane 0's partial is 2^24, lane 1's 1, lane
+    16's -2^24.  The butterfly (offsets 16, 8, 4, 2, 1 as seen from lane 0)
+    cancels 2^24 first and keeps the 1: the logit is 1.  A loop in index
+    order, or the butterfly run from offset 1 up, loses the 1 and gives 0."""
+    H = 256
+    x = torch.zeros(1, H)
+    w = torch.zeros(1, H)
+    x[0, 0], w[0, 0] = 2.0 ** 12, 2.0 ** 12    # lane 0
+    x[0, 8], w[0, 8] = 1.0, 1.0                # lane 1
+    x[0, 128], w[0, 128] = 2.0 ** 12, -(2.0 ** 12)  # lane 16
+    logits, _, _ = oracle.route(x.to(torch.bfloat16), w.to(torch.bfloat16), 1)
+    assert bf16_bits_to_f64(logits[0, 0]) == 1.0

@@ -10,12 +10,16 @@
  * accumulator), act = bf16(silu(g) * u), an NVFP4 down projection
  * y_e = bf16(acc * gs_e), the routed sum bf16(sum_j tw_j * y_j) accumulated
  * in fp32 in rank order, plus an ungated BF16 shared expert:
- * out = bf16(routed + shared).
+ * out = bf16(routed + shared).  Variants take an NVFP4 shared expert, BF16
+ * routed experts or an add-RMSNorm prologue; flint_qkv_fused is the decode
+ * step before attention (page "vllm.models.flint.ops.qkv_fused").
  *
  * Conventions for every entry point:
  *  - All tensor pointers are DEVICE pointers, row-major, contiguous and
- *    16-byte aligned.  The caller owns every buffer; the library keeps no
- *    per-call global state and allocates nothing.
+ *    16-byte aligned (fp32 scalars and int32/int64 index arrays: aligned to
+ *    their size; the paged KV caches of flint_qkv_fused take strides).  The
+ *    caller owns every buffer; the library keeps no per-call global state
+ *    and allocates nothing.
  *  - Work is enqueued on `stream` and returns before it completes.  Argument
  *    errors are reported synchronously (negative return, nothing enqueued);
  *    launch failures return FLINT_ERR_CUDA.
